@@ -1,0 +1,322 @@
+/*
+ * m2_oracle.c -- plain, slow CPU oracle for the Nemotron-H Mamba-2 layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or calls
+ * this file; only the tests, the smoke check and the benchmark's CPU-baseline
+ * leg do.  It shares no code, header, table or constant generator with the CUDA
+ * library: every function below is written from the definitions on the pages.
+ *
+ * Arithmetic is IEEE double.  Values are rounded to bfloat16 only at the six
+ * rounding points the layer's "a16" activations imply (R1..R6 below); the SSM
+ * state and everything between rounding points stay in double.
+ *
+ * Sources (page title, then the section on that page):
+ *   [SRC]  spark_model/layers/nemotron_mamba2.rs -- module header "Forward pass"
+ *          steps 1..8; `conv1d_update_biased` (conv with learned bias);
+ *          `ssm_decode` (arguments of the SSM decode step, dt_min=1e-9,
+ *          dt_max=1e9 "no effective clamp"); struct fields (h_state is fp32
+ *          [num_heads, head_dim, state_size]).
+ *   [QWEN] Struct Qwen3SsmLayer -- `set_fp8_decode_weights`: the w8a16 GEMV
+ *          out[n] = sum_k A[k] * E4M3(B[n,k]) * block_scale[n/BS, k/BS], BS=128,
+ *          scales [N/BS, K/BS] BF16.
+ *   [NEMO] Struct NemotronMamba2Layer -- `set_fp8_weights`: the scale index
+ *          block_scale[n/128 * k_blocks + k/128].
+ *   [TRAIT] Trait TransformerLayer -- `decode` (hidden modified in place),
+ *          `prefill` ("Default: falls back to sequential single-token decode
+ *          calls"), `decode_multi_seq` (N sequences, one token each, own state).
+ *
+ * Readings where the pages are silent (each one is listed in the design notes):
+ *   - E4M3 is the OCP "E4M3FN" encoding: bias 7, no infinities, S.1111.111 is NaN.
+ *   - Rounding points: R1 hidden input is bf16; R2 RMSNorm output -> bf16;
+ *     R3 in_proj output -> bf16; R4 conv output -> bf16; R5 gated-norm output ->
+ *     bf16; R6 (hidden_in + out_proj) -> bf16 once.  bf16 rounding is
+ *     round-to-nearest-even.
+ *   - in_proj output order [z | xBC | dt]; xBC = [x | B (group-major) | C].
+ *   - conv state: (d_conv-1) bf16 slots per channel used as a ring; `pos` counts
+ *     tokens seen; token t is stored in slot t mod (d_conv-1).  The window from
+ *     oldest to newest is slots pos, pos+1, .. (mod d_conv-1), then the current
+ *     token; tap j multiplies window element j (tap d_conv-1 = current token).
+ *   - head h uses group g = h / (H/G).
+ *   - softplus(v) = log1p(exp(v)), and v itself for v > 20.
+ *   - RMSNorm multiplies by the weight (not 1+weight); gated RMSNorm normalises
+ *     y over groups of `group` elements (the whole d_inner by default), then
+ *     multiplies by the weight and by silu(z).
+ *   - residual: out = hidden_in + out_proj(...), a self-contained pre-norm block.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- formats */
+
+/* E4M3FN closed form: for exponent field e>0, (-1)^s * 2^(e-7) * (1 + m/8);
+ * for e=0, (-1)^s * 2^-6 * (m/8); 0x7F and 0xFF are NaN. */
+double or_e4m3_to_f64(uint8_t b) {
+  int s = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* bfloat16 is the top half of an IEEE binary32: sign, 8 exponent bits, 7
+ * fraction bits. */
+double or_bf16_to_f64(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Round a double to the nearest bfloat16, ties to even, directly (one rounding,
+ * not double->float->bf16).  Normal bf16 values carry 8 significant bits; below
+ * 2^-126 the spacing is fixed at 2^-133 (subnormals).  Overflow goes to inf. */
+uint16_t or_f64_to_bf16(double v) {
+  if (isnan(v)) return signbit(v) ? 0xFFC0 : 0x7FC0;
+  int neg = signbit(v) ? 1 : 0;
+  double a = fabs(v);
+  double r;
+  if (a == 0.0) {
+    r = 0.0;
+  } else if (isinf(a)) {
+    r = INFINITY;
+  } else {
+    int e;
+    frexp(a, &e); /* a = f * 2^e, 0.5 <= f < 1 */
+    int q_exp = (e - 1 >= -126) ? (e - 1 - 7) : -133; /* value of one ulp */
+    double q = ldexp(a, -q_exp);                      /* exact scaling     */
+    double qr = nearbyint(q);                         /* default mode: RNE */
+    r = ldexp(qr, q_exp);
+    /* largest finite bf16 = (2 - 2^-7) * 2^127; anything rounding above it
+     * (i.e. a >= max + half ulp, ties going to the even "2^128") is inf */
+    if (r > ldexp(2.0 - ldexp(1.0, -7), 127)) r = INFINITY;
+  }
+  float f = (float)r; /* exact: r is a bf16 value */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  uint16_t h = (uint16_t)(u >> 16);
+  if (neg) h |= 0x8000;
+  return h;
+}
+
+static double g_e4m3_table[256];
+static int g_init = 0;
+
+void or_init(void) {
+  for (int b = 0; b < 256; ++b) g_e4m3_table[b] = or_e4m3_to_f64((uint8_t)b);
+  g_init = 1;
+}
+
+static double e4m3(uint8_t b) {
+  if (!g_init) or_init();
+  return g_e4m3_table[b];
+}
+
+static double bf(uint16_t h) { return or_bf16_to_f64(h); }
+
+/* ----------------------------------------------------------- elementwise */
+
+double or_softplus(double v) { return v > 20.0 ? v : log1p(exp(v)); }
+
+double or_silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* ---------------------------------------------------------------- step 1 */
+
+/* RMSNorm with weight*x scaling ([SRC] step 1): out = x / sqrt(mean(x^2)+eps) * w,
+ * rounded to bf16 (R2). */
+void or_rmsnorm(const uint16_t* x, const uint16_t* w, int K, double eps, uint16_t* out) {
+  double ss = 0.0;
+  for (int k = 0; k < K; ++k) ss += bf(x[k]) * bf(x[k]);
+  double r = 1.0 / sqrt(ss / (double)K + eps);
+  for (int k = 0; k < K; ++k) out[k] = or_f64_to_bf16(bf(x[k]) * r * bf(w[k]));
+}
+
+/* ---------------------------------------------------------------- step 2 / 7 */
+
+/* The w8a16 GEMV ([QWEN] set_fp8_decode_weights; [NEMO] set_fp8_weights):
+ *   out[m][n] = sum_k A[m][k] * E4M3(W[n][k]) * S[(n/128)*kb + k/128],
+ * with kb = ceil(K/128), summed with k ascending, unrounded (double). */
+void or_w8a16_gemv(const uint16_t* A, int M, const uint8_t* W, const uint16_t* S, int N, int K,
+                   double* out) {
+  int kb = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    const uint8_t* wrow = W + (size_t)n * K;
+    const uint16_t* srow = S + (size_t)(n / 128) * kb;
+    for (int m = 0; m < M; ++m) {
+      const uint16_t* a = A + (size_t)m * K;
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += bf(a[k]) * e4m3(wrow[k]) * bf(srow[k / 128]);
+      out[(size_t)m * N + n] = acc;
+    }
+  }
+}
+
+/* Dense BF16-weight GEMV of the unquantised projections ([SRC] struct field
+ * comment on native BF16 projections): out[m][n] = sum_k A[m][k] * W[n][k]. */
+void or_bf16_gemv(const uint16_t* A, int M, const uint16_t* W, int N, int K, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    const uint16_t* wrow = W + (size_t)n * K;
+    for (int m = 0; m < M; ++m) {
+      const uint16_t* a = A + (size_t)m * K;
+      double acc = 0.0;
+      for (int k = 0; k < K; ++k) acc += bf(a[k]) * bf(wrow[k]);
+      out[(size_t)m * N + n] = acc;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------- step 3 */
+
+/* One-token causal depthwise conv update with learned bias and fused SiLU
+ * ([SRC] step 3 and `conv1d_update_biased`).  ring is [(d_conv-1)][C] bf16;
+ * *pos is the number of tokens seen so far (not advanced here).  The current
+ * token x (bf16, R3) is used as tap d_conv-1 and then stored into slot
+ * pos mod (d_conv-1).  Output rounded to bf16 (R4). */
+void or_conv1d_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
+                      const uint16_t* b, int C, int dconv, int silu, uint16_t* out) {
+  int L = dconv - 1;
+  int p = *pos;
+  for (int c = 0; c < C; ++c) {
+    double acc = b ? bf(b[c]) : 0.0;
+    for (int j = 0; j < L; ++j) {
+      int slot = (p + j) % L; /* oldest first */
+      acc += bf(w[(size_t)c * dconv + j]) * bf(ring[(size_t)slot * C + c]);
+    }
+    acc += bf(w[(size_t)c * dconv + L]) * bf(x[c]);
+    out[c] = or_f64_to_bf16(silu ? or_silu(acc) : acc);
+  }
+  int wslot = p % L;
+  for (int c = 0; c < C; ++c) ring[(size_t)wslot * C + c] = x[c];
+}
+
+/* ---------------------------------------------------------------- step 5 */
+
+/* Mamba-2 SSM decode step ([SRC] step 5 and `ssm_decode`), one sequence:
+ *   dt = clamp(softplus(dt_raw[h] + dt_bias[h]), 1e-9, 1e9)
+ *   A  = -exp(A_log[h]);  dA = exp(dt * A)
+ *   h[h][p][n] = dA * h[h][p][n] + dt * x[h*P+p] * B[g*N+n]
+ *   y[h*P+p]   = sum_n C[g*N+n] * h[h][p][n] + D[h] * x[h*P+p]
+ * with g = h / (H/G).  h and y in double; *clamp_hits counts clamp events. */
+void or_ssm_step(double* hs, const uint16_t* x, const uint16_t* Bm, const uint16_t* Cm,
+                 const uint16_t* dt_raw, const float* A_log, const float* D, const float* dt_bias,
+                 int H, int P, int N, int G, double* y, long* clamp_hits) {
+  int hpg = H / G;
+  for (int h = 0; h < H; ++h) {
+    int g = h / hpg;
+    double dt = or_softplus(bf(dt_raw[h]) + (double)dt_bias[h]);
+    if (dt < 1e-9) { dt = 1e-9; if (clamp_hits) ++*clamp_hits; }
+    if (dt > 1e9) { dt = 1e9; if (clamp_hits) ++*clamp_hits; }
+    double A = -exp((double)A_log[h]);
+    double dA = exp(dt * A);
+    for (int p = 0; p < P; ++p) {
+      double xv = bf(x[h * P + p]);
+      double* hrow = hs + ((size_t)h * P + p) * N;
+      double acc = 0.0;
+      for (int n = 0; n < N; ++n) {
+        hrow[n] = dA * hrow[n] + dt * xv * bf(Bm[g * N + n]);
+        acc += bf(Cm[g * N + n]) * hrow[n];
+      }
+      y[h * P + p] = acc + (double)D[h] * xv;
+    }
+  }
+}
+
+/* ---------------------------------------------------------------- step 6 */
+
+/* Gated RMSNorm ([SRC] step 6, "rms_norm(y, ssm_norm) * silu(z)"): for each
+ * group of `group` consecutive elements, out = y / sqrt(mean(y^2)+eps) * w *
+ * silu(z), rounded to bf16 (R5). */
+void or_gated_rmsnorm(const double* y, const uint16_t* z, const uint16_t* w, int d, int group,
+                      double eps, uint16_t* out) {
+  for (int g0 = 0; g0 < d; g0 += group) {
+    double ss = 0.0;
+    for (int i = g0; i < g0 + group; ++i) ss += y[i] * y[i];
+    double r = 1.0 / sqrt(ss / (double)group + eps);
+    for (int i = g0; i < g0 + group; ++i)
+      out[i] = or_f64_to_bf16(y[i] * r * bf(w[i]) * or_silu(bf(z[i])));
+  }
+}
+
+/* ---------------------------------------------------------------- layer */
+
+typedef struct {
+  int hidden, H, P, N, G, dconv, gnorm_group;
+  double eps_in, eps_gated;
+  const uint16_t* norm_w;   /* [hidden] */
+  int in_fmt;               /* 1 = E4M3 + 128x128 bf16 block scales, 2 = bf16 */
+  const void* in_w;         /* [n_in][hidden] */
+  const uint16_t* in_s;     /* [ceil(n_in/128)][ceil(hidden/128)] */
+  const uint16_t* conv_w;   /* [d_xbc][dconv] */
+  const uint16_t* conv_b;   /* [d_xbc] */
+  const float* A_log;       /* [H] */
+  const float* D;           /* [H] */
+  const float* dt_bias;     /* [H] */
+  const uint16_t* gnorm_w;  /* [d_inner] */
+  int out_fmt;
+  const void* out_w;        /* [hidden][d_inner] */
+  const uint16_t* out_s;    /* [ceil(hidden/128)][ceil(d_inner/128)] */
+} or_layer;
+
+static void proj(int fmt, const void* w, const uint16_t* s, const uint16_t* a, int N, int K,
+                 double* out) {
+  if (fmt == 1) or_w8a16_gemv(a, 1, (const uint8_t*)w, s, N, K, out);
+  else or_bf16_gemv(a, 1, (const uint16_t*)w, N, K, out);
+}
+
+/* One token of one sequence through the whole layer, steps 1..8 in the order
+ * of the [SRC] module header.  hidden [hidden] bf16 is modified in place
+ * ([TRAIT] decode).  hs [H][P][N] double, ring [(dconv-1)][d_xbc] bf16 and
+ * *pos are the sequence's state and are advanced by one token. */
+long or_layer_token(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* ring, int32_t* pos) {
+  int d_inner = L->H * L->P;
+  int d_xbc = d_inner + 2 * L->G * L->N;
+  int n_in = d_inner + d_xbc + L->H;
+  long hits = 0;
+  uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * L->hidden);
+  double* zx = (double*)malloc(sizeof(double) * n_in);
+  uint16_t* zxb = (uint16_t*)malloc(sizeof(uint16_t) * n_in);
+  uint16_t* u = (uint16_t*)malloc(sizeof(uint16_t) * d_xbc);
+  double* y = (double*)malloc(sizeof(double) * d_inner);
+  uint16_t* gout = (uint16_t*)malloc(sizeof(uint16_t) * d_inner);
+  double* o = (double*)malloc(sizeof(double) * L->hidden);
+
+  /* 1. RMSNorm (R2) */
+  or_rmsnorm(hidden, L->norm_w, L->hidden, L->eps_in, xn);
+  /* 2. in_proj -> [z, xBC, dt] (R3) */
+  proj(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, zx);
+  for (int i = 0; i < n_in; ++i) zxb[i] = or_f64_to_bf16(zx[i]);
+  const uint16_t* z = zxb;
+  const uint16_t* xbc = zxb + d_inner;
+  const uint16_t* dt = zxb + d_inner + d_xbc;
+  /* 3. conv1d update on xBC with bias and SiLU (R4) */
+  or_conv1d_update(ring, pos, xbc, L->conv_w, L->conv_b, d_xbc, L->dconv, 1, u);
+  *pos += 1;
+  /* 4. split into x, B, C */
+  const uint16_t* xs = u;
+  const uint16_t* Bm = u + d_inner;
+  const uint16_t* Cm = u + d_inner + L->G * L->N;
+  /* 5. SSM state update and output */
+  or_ssm_step(hs, xs, Bm, Cm, dt, L->A_log, L->D, L->dt_bias, L->H, L->P, L->N, L->G, y, &hits);
+  /* 6. gated RMSNorm (R5) */
+  or_gated_rmsnorm(y, z, L->gnorm_w, d_inner, L->gnorm_group, L->eps_gated, gout);
+  /* 7. out_proj, 8. residual add, rounded once (R6) */
+  proj(L->out_fmt, L->out_w, L->out_s, gout, L->hidden, d_inner, o);
+  for (int i = 0; i < L->hidden; ++i) hidden[i] = or_f64_to_bf16(bf(hidden[i]) + o[i]);
+
+  free(xn); free(zx); free(zxb); free(u); free(y); free(gout); free(o);
+  return hits;
+}
+
+/* Prefill of T tokens of one sequence, by its definition: T sequential
+ * single-token decode steps ([TRAIT] prefill default).  hidden is [T][hidden]. */
+long or_layer_prefill(const or_layer* L, uint16_t* hidden, int T, double* hs, uint16_t* ring,
+                      int32_t* pos) {
+  long hits = 0;
+  for (int t = 0; t < T; ++t)
+    hits += or_layer_token(L, hidden + (size_t)t * L->hidden, hs, ring, pos);
+  return hits;
+}
