@@ -1,0 +1,194 @@
+/*
+ * mamba2.h -- C ABI of the GB300 (sm_103a) Mamba-2 layer forward library
+ * (libmamba2_gb300.so).
+ *
+ * The layer is the Nemotron-H Mamba-2 mixer block as the source listing
+ * "spark_model/layers/nemotron_mamba2.rs" describes it in its module header
+ * ("Forward pass", steps 1-8):
+ *   1 RMSNorm (weight * x)        2 in_proj GEMV -> [z, xBC, dt]
+ *   3 conv1d update on xBC, with bias, fused SiLU
+ *   4 split xBC -> x, B, C        5 Mamba-2 SSM state update and output
+ *   6 gated RMSNorm: rms_norm(y, ssm_norm) * silu(z)
+ *   7 out_proj GEMV               8 residual add
+ * FP8 projections use the w8a16 block-scaled GEMV of the page "Struct
+ * Qwen3SsmLayer" (`set_fp8_decode_weights`):
+ *   out[n] = sum_k A[k] * E4M3(W[n,k]) * block_scale[n/128, k/128],
+ * with the scale grid [ceil(N/128)][ceil(K/128)] in bf16 and the index
+ * block_scale[n/128 * k_blocks + k/128] of "Struct NemotronMamba2Layer"
+ * (`set_fp8_weights`).
+ *
+ * Conventions for every entry point below:
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
+ *    allocates and frees no device memory; scratch comes from the caller's
+ *    workspace (`ws`, `ws_bytes`).
+ *  - bf16 values are passed as uint16_t bit patterns; E4M3 as uint8_t.
+ *    Matrices are row-major with the last index contiguous.
+ *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream)
+ *    of the current device; the call returns once it is enqueued.
+ *  - Return value: M2_OK (0) or a negative M2_ERR_* code.  All arguments are
+ *    checked on the host before anything is launched: on an argument error
+ *    nothing is launched and no buffer is touched.  M2_ERR_LAUNCH reports a
+ *    launch failure seen by cudaGetLastError after enqueueing.
+ *  - Kernels never spin without a bound.  If a bounded wait inside a kernel
+ *    gives up, the kernel records M2_ERR_TIMEOUT in a device status word that
+ *    m2_device_status() returns.
+ *  - Calls that share state or workspace must be ordered (same stream, or
+ *    synchronised); concurrent calls on distinct buffers are independent.
+ */
+#ifndef MAMBA2_GB300_H
+#define MAMBA2_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------ status codes */
+enum {
+  M2_OK = 0,
+  M2_ERR_ARG = -1,         /* null pointer, non-positive or inconsistent size */
+  M2_ERR_FORMAT = -2,      /* weight format tag / scale grid inconsistent     */
+  M2_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required      */
+  M2_ERR_LAUNCH = -4,      /* a CUDA launch or attribute call failed          */
+  M2_ERR_UNSUPPORTED = -5, /* shape outside the supported range               */
+  M2_ERR_ALIGN = -6,       /* pointer not 16-byte aligned where required      */
+  M2_ERR_DEVICE = -7,      /* no device, or a device older than sm_103        */
+  M2_ERR_TIMEOUT = -8      /* a bounded in-kernel wait gave up                */
+};
+
+/* Weight formats.  FP8_BLOCK128: E4M3 bytes [n][k] plus bf16 scales
+ * [ceil(n/128)][ceil(k/128)] ("Fp8BlockScaled").  BF16: bf16 [n][k], no scale
+ * (the unquantised projections of a mixed-precision checkpoint, source listing
+ * struct comment on native BF16 projections). */
+enum { M2_W_FP8_BLOCK128 = 1, M2_W_BF16 = 2 };
+
+/* Layer dimensions.  d_inner = nheads*head_dim; d_xbc = d_inner +
+ * 2*n_groups*d_state; in_proj rows n_in = 2*d_inner + 2*n_groups*d_state +
+ * nheads.  gnorm_group is the span of the gated RMSNorm (d_inner: the whole
+ * row; a divisor of d_inner: group-wise).  Supported: hidden and d_inner
+ * multiples of 16 and <= 16384; d_state in {16,32,64,128}; head_dim <= 256;
+ * nheads % n_groups == 0; 2 <= d_conv <= 8. */
+typedef struct m2_dims {
+  int32_t hidden, nheads, head_dim, d_state, n_groups, d_conv;
+  float eps_in;     /* input RMSNorm epsilon (1e-5) */
+  float eps_gated;  /* gated RMSNorm epsilon (1e-5) */
+  int32_t gnorm_group;
+} m2_dims;
+
+typedef struct m2_weight {
+  const void* w;          /* [n][k]: uint8 E4M3 or uint16 bf16; 16-byte aligned */
+  const uint16_t* scale;  /* FP8: bf16 [ceil(n/128)][ceil(k/128)]; BF16: NULL   */
+  int32_t n, k;
+  int32_t fmt;            /* M2_W_FP8_BLOCK128 or M2_W_BF16                    */
+} m2_weight;
+
+/* One layer's parameters (all device pointers; the caller keeps them alive). */
+typedef struct m2_layer {
+  const uint16_t* norm_w;  /* [hidden] bf16, input RMSNorm weight            */
+  m2_weight in_proj;       /* n = n_in, k = hidden                           */
+  const uint16_t* conv_w;  /* [d_xbc][d_conv] bf16 (tap d_conv-1 = current)  */
+  const uint16_t* conv_b;  /* [d_xbc] bf16                                   */
+  const float* A_log;      /* [nheads]; A = -exp(A_log)                      */
+  const float* D;          /* [nheads]                                       */
+  const float* dt_bias;    /* [nheads]                                       */
+  const uint16_t* gnorm_w; /* [d_inner] bf16, gated RMSNorm weight           */
+  m2_weight out_proj;      /* n = hidden, k = d_inner                        */
+} m2_layer;
+
+/* Human-readable text for a status code (static storage). */
+const char* m2_strerror(int status);
+
+/* Host-only check of dimensions and parameters (formats, scale grids, shapes,
+ * alignment).  Launches nothing.  The layer entry points run it themselves. */
+int m2_validate(const m2_dims* dims, const m2_layer* layer);
+
+/* Bytes of workspace that mamba2_layer_decode with batch <= max_batch and
+ * mamba2_layer_prefill with T <= max_tokens need (the larger of the two).
+ * Returns 0 for invalid dims. */
+size_t m2_workspace_bytes(const m2_dims* dims, int32_t max_batch, int32_t max_tokens);
+
+/* One decode step of B independent sequences, one token each (page "Trait
+ * TransformerLayer", `decode` / `decode_multi_seq`: weights are read once for
+ * all B rows).
+ *   hidden     [B][hidden] bf16, read and overwritten with the layer output
+ *              hidden + out_proj(...)  (in place, as `decode` specifies).
+ *   ssm_state  [B][nheads][head_dim][d_state] fp32, updated in place.
+ *   conv_state [B][d_conv-1][d_xbc] bf16 ring: token t of a sequence lives in
+ *              slot t mod (d_conv-1); zero-initialise for a new sequence.
+ *   conv_pos   [B] int32, tokens seen so far per sequence; advanced by 1.
+ *   ws         workspace of at least m2_workspace_bytes(dims, B, 0) bytes,
+ *              256-byte aligned; its contents are scratch. */
+int mamba2_layer_decode(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t B,
+                        float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
+                        size_t ws_bytes, cudaStream_t stream);
+
+/* Prefill of T tokens of ONE sequence (page "Trait TransformerLayer",
+ * `prefill`: projections as GEMMs over the T tokens; the result equals T
+ * sequential decode steps).  hidden [T][hidden] bf16 in/out; ssm_state
+ * [nheads][head_dim][d_state] fp32, conv_state [d_conv-1][d_xbc] bf16 and
+ * conv_pos [1] int32 are the sequence's state before the block and are left
+ * as the state after it (conv_pos += T).  ws: m2_workspace_bytes(dims, 0, T). */
+int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t T,
+                         float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
+                         size_t ws_bytes, cudaStream_t stream);
+
+/* The w8a16 block-scaled GEMV/GEMM (page "Struct Qwen3SsmLayer",
+ * `set_fp8_decode_weights`):
+ *   out[m][n] = bf16( sum_k A[m][k] * E4M3(W[n][k]) * S[n/128][k/128] )
+ * A [M][K] bf16, W [N][K] E4M3 (16-byte aligned, K % 16 == 0), S bf16
+ * [ceil(N/128)][ceil(K/128)], out [M][N] bf16.  fp32 accumulation. */
+int w8a16_gemv(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* out, int32_t M,
+               int32_t N, int32_t K, cudaStream_t stream);
+
+/* One-token causal depthwise conv update with bias and optional SiLU (source
+ * listing, `conv1d_update_biased`) for B sequences of C channels:
+ *   out[b][c] = act( bias[c] + sum_{j<d_conv-1} w[c][j] * ring[b][(pos_b+j) mod (d_conv-1)][c]
+ *                    + w[c][d_conv-1] * x[b][c] )
+ * then x[b][c] is stored into slot pos_b mod (d_conv-1) and conv_pos[b] += 1.
+ * x rows are ld_x elements apart (so x can be a view into a wider row); out
+ * is [B][C].  bias may be NULL (no bias).  act = SiLU if silu != 0. */
+int conv1d_update(uint16_t* conv_state, int32_t* conv_pos, const uint16_t* x, int32_t ld_x,
+                  const uint16_t* w, const uint16_t* bias, uint16_t* out, int32_t B, int32_t C,
+                  int32_t d_conv, int32_t silu, cudaStream_t stream);
+
+/* One Mamba-2 SSM decode step for B sequences (source listing, `ssm_decode`;
+ * dt clamp [1e-9, 1e9] as passed there):
+ *   dt = clamp(softplus(dt_raw[b][h] + dt_bias[h]), 1e-9, 1e9);  dA = exp(-dt*exp(A_log[h]))
+ *   h[b][h][p][n] = dA*h + dt * x[b][h*P+p] * Bm[b][g*N+n],   g = h / (H/G)
+ *   y[b][h*P+p]   = sum_n Cm[b][g*N+n] * h[b][h][p][n] + D[h] * x[b][h*P+p]
+ * x, Bm, Cm, dt_raw are bf16 with rows ld_in elements apart (views into one
+ * [B][ld_in] buffer are fine); h fp32 [B][H][P][N] in place; y fp32 [B][H*P]. */
+int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint16_t* Cm,
+                    const uint16_t* dt_raw, int32_t ld_in, const float* A_log, const float* D,
+                    const float* dt_bias, float* y, int32_t B, int32_t H, int32_t P, int32_t N,
+                    int32_t G, cudaStream_t stream);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/* Device status word: M2_OK, or the first M2_ERR_TIMEOUT a kernel recorded on
+ * the current device.  Synchronises the device.  clear != 0 resets it. */
+int m2_device_status(int clear);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t m2_launch_count(void);
+
+/* Per-kernel timing: m2_trace_begin(capacity) makes every later launch record
+ * a CUDA event pair around itself on its stream (up to `capacity` launches);
+ * m2_trace_end synchronises, writes per kernel id the summed milliseconds and
+ * the launch count into ms[n_ids] / launches[n_ids], and stops tracing.
+ * Events are host-side objects (cudaEventCreate); no device memory is used.
+ * Tracing serialises kernels that could otherwise overlap. */
+int m2_trace_begin(int32_t capacity);
+int m2_trace_end(double* ms, int32_t* launches, int32_t n_ids);
+/* Name of kernel id `id` (0 <= id < m2_kernel_count()), or NULL. */
+const char* m2_kernel_name(int32_t id);
+int32_t m2_kernel_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MAMBA2_GB300_H */

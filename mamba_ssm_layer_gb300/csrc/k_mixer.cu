@@ -1,0 +1,320 @@
+// k_mixer.cu -- the non-GEMM steps of the Mamba-2 mixer: conv1d update
+// (decode and prefill), the SSM decode step, the sequential prefill scan, and
+// the gated RMSNorm.  All are memory- or latency-bound elementwise/reduction
+// kernels; the layouts keep every global access coalesced.
+//
+// Formulas (source listing "spark_model/layers/nemotron_mamba2.rs", module
+// header steps 3-6, and its `conv1d_update_biased` / `ssm_decode` launchers):
+//   conv:  u = silu(b + sum_j w[j] * window[j]), window = the d_conv-1
+//          previous xBC tokens (oldest first) then the current one
+//   SSM:   dt = clamp(softplus(dt_raw + dt_bias), 1e-9, 1e9), dA = exp(-dt*exp(A_log))
+//          h = dA*h + dt*x*B;  y = C.h + D*x           (head h uses group h/(H/G))
+//   gate:  g = rms_norm(y) * w * silu(z)
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "m2_common.cuh"
+#include "m2_kernels.h"
+
+namespace m2 {
+
+// ------------------------------------------------------------------ conv
+
+__global__ void __launch_bounds__(256) conv_update_kernel(uint16_t* __restrict__ ring,
+                                                          const int32_t* __restrict__ pos,
+                                                          const uint16_t* __restrict__ x, int ldx,
+                                                          const uint16_t* __restrict__ w,
+                                                          const uint16_t* __restrict__ bias,
+                                                          uint16_t* __restrict__ out, int ldo, int C, int dconv,
+                                                          int silu) {
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  const int b = blockIdx.y;
+  if (c >= C) return;
+  const int L = dconv - 1;
+  const int p = pos[b];
+  uint16_t* rg = ring + (size_t)b * L * C;
+  const uint16_t xv = x[(size_t)b * ldx + c];
+  float s = bias ? bf16_to_f32(bias[c]) : 0.0f;
+  for (int j = 0; j < L; ++j) s += bf16_to_f32(w[(size_t)c * dconv + j]) * bf16_to_f32(rg[(size_t)((p + j) % L) * C + c]);
+  s += bf16_to_f32(w[(size_t)c * dconv + L]) * bf16_to_f32(xv);
+  out[(size_t)b * ldo + c] = f32_to_bf16(silu ? silu_f(s) : s);
+  rg[(size_t)(p % L) * C + c] = xv;
+}
+
+__global__ void conv_pos_kernel(int32_t* pos, int B, int add) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) pos[b] += add;
+}
+
+cudaError_t launch_conv_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, int32_t ldx,
+                               const uint16_t* w, const uint16_t* b, uint16_t* out, int32_t ldo, int32_t B,
+                               int32_t C, int32_t dconv, int32_t silu, cudaStream_t s) {
+  trace_pre(K_CONV_UPDATE, s);
+  conv_update_kernel<<<dim3((C + 255) / 256, B), 256, 0, s>>>(ring, pos, x, ldx, w, b, out, ldo, C, dconv, silu);
+  trace_post(K_CONV_UPDATE, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_pos(int32_t* pos, int32_t B, int32_t add, cudaStream_t s) {
+  trace_pre(K_CONV_POS, s);
+  conv_pos_kernel<<<(B + 127) / 128, 128, 0, s>>>(pos, B, add);
+  trace_post(K_CONV_POS, s);
+  return cudaGetLastError();
+}
+
+// Prefill conv over T tokens of one sequence.  A CTA owns 32 channels for all
+// T tokens (8 token lanes of 32 channels), so it can read the ring for the
+// first taps and afterwards overwrite it with the block's last tokens without
+// racing any other CTA.
+__global__ void __launch_bounds__(256) conv_prefill_kernel(uint16_t* __restrict__ ring,
+                                                           const int32_t* __restrict__ pos,
+                                                           const uint16_t* __restrict__ xbc, int ldx,
+                                                           const uint16_t* __restrict__ w,
+                                                           const uint16_t* __restrict__ bias,
+                                                           uint16_t* __restrict__ u, int ldu, int T, int C,
+                                                           int dconv) {
+  const int c = blockIdx.x * 32 + (threadIdx.x & 31);
+  const int tl = threadIdx.x >> 5;
+  const int L = dconv - 1;
+  const int p0 = pos[0];
+  if (c < C) {
+    float wl[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) wl[j] = j < dconv ? bf16_to_f32(w[(size_t)c * dconv + j]) : 0.0f;
+    const float bv = bias ? bf16_to_f32(bias[c]) : 0.0f;
+    for (int t = tl; t < T; t += 8) {
+      float s = bv;
+#pragma unroll
+      for (int j = 0; j < 7; ++j) {
+        if (j < L) {
+          const int src = t - L + j;  // token offset within the block (negative: history)
+          float v;
+          if (src >= 0) v = bf16_to_f32(xbc[(size_t)src * ldx + c]);
+          else v = bf16_to_f32(ring[(size_t)((((p0 + src) % L) + L) % L) * C + c]);
+          s = fmaf(wl[j], v, s);
+        }
+      }
+      s = fmaf(wl[L], bf16_to_f32(xbc[(size_t)t * ldx + c]), s);
+      u[(size_t)t * ldu + c] = f32_to_bf16(silu_f(s));
+    }
+  }
+  __syncthreads();
+  if (c < C && tl < L) {
+    const int t = T - L + tl;
+    if (t >= 0) ring[(size_t)((p0 + t) % L) * C + c] = xbc[(size_t)t * ldx + c];
+  }
+}
+
+cudaError_t launch_conv_prefill(uint16_t* ring, const int32_t* pos, const uint16_t* xbc, int32_t ldx,
+                                const uint16_t* w, const uint16_t* b, uint16_t* u, int32_t ldu, int32_t T,
+                                int32_t C, int32_t dconv, cudaStream_t s) {
+  trace_pre(K_CONV_PREFILL, s);
+  conv_prefill_kernel<<<(C + 31) / 32, 256, 0, s>>>(ring, pos, xbc, ldx, w, b, u, ldu, T, C, dconv);
+  trace_post(K_CONV_PREFILL, s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ SSM step
+
+// Thread layout shared by the SSM kernels: a row p of the state (N fp32) is
+// covered by LPR = N/4 lanes holding 4 consecutive n each (one float4), so a
+// warp covers 32/LPR rows and the 8 warps 8*32/LPR rows per pass.
+__device__ __forceinline__ float4 ld4bf(const uint16_t* p) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  return make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+}
+
+__device__ __forceinline__ void head_scalars(const uint16_t* dt_row, const float* dt_bias, const float* A_log, int h,
+                                             float& dt, float& dA) {
+  float d = softplus_f(bf16_to_f32(dt_row[h]) + dt_bias[h]);
+  d = fminf(fmaxf(d, 1e-9f), 1e9f);
+  dt = d;
+  dA = expf(d * -expf(A_log[h]));
+}
+
+template <int LPR>
+__global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int psplit, int rows_per_cta) {
+  constexpr int RPW = 32 / LPR;
+  const int b = blockIdx.y;
+  const int h = blockIdx.x / psplit;
+  const int pc = blockIdx.x % psplit;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n4 = (lane % LPR) * 4;
+  const int g = h / (a.H / a.G);
+  const uint16_t* xr = a.x + (size_t)b * a.ld_in;
+  float dt, dA;
+  head_scalars(a.dt + (size_t)b * a.ld_in, a.dt_bias, a.A_log, h, dt, dA);
+  const float Dh = a.D[h];
+  const float4 Bv = ld4bf(a.Bm + (size_t)b * a.ld_in + (size_t)g * a.N + n4);
+  const float4 Cv = ld4bf(a.Cm + (size_t)b * a.ld_in + (size_t)g * a.N + n4);
+  const int p_begin = pc * rows_per_cta;
+  const int p_end = min(a.P, p_begin + rows_per_cta);
+  float* hb = a.h + ((size_t)b * a.H + h) * a.P * a.N;
+  for (int p = p_begin + warp * RPW + lane / LPR; p < p_end; p += 8 * RPW) {
+    const float xv = bf16_to_f32(xr[(size_t)h * a.P + p]);
+    float4* hp = reinterpret_cast<float4*>(hb + (size_t)p * a.N + n4);
+    float4 hv = *hp;
+    const float dtx = dt * xv;
+    hv.x = fmaf(dA, hv.x, dtx * Bv.x);
+    hv.y = fmaf(dA, hv.y, dtx * Bv.y);
+    hv.z = fmaf(dA, hv.z, dtx * Bv.z);
+    hv.w = fmaf(dA, hv.w, dtx * Bv.w);
+    *hp = hv;
+    float yp = Cv.x * hv.x + Cv.y * hv.y + Cv.z * hv.z + Cv.w * hv.w;
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
+    if ((lane % LPR) == 0) a.y[(size_t)b * a.ldy + (size_t)h * a.P + p] = yp + Dh * xv;
+  }
+  if (a.pos_inc && blockIdx.x == 0 && threadIdx.x == 0) a.pos_inc[b] += 1;
+}
+
+cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s) {
+  const int lpr = a.N / 4;
+  const int rows_pass = 8 * (32 / lpr);
+  // split heads along p until there are >= 2 CTAs per SM (p rows are independent)
+  int psplit = 1;
+  const long long target = 2LL * num_sms();
+  while ((long long)a.B * a.H * psplit < target && a.P / (psplit * 2) >= rows_pass) psplit *= 2;
+  const int rows_per_cta = (a.P + psplit - 1) / psplit;
+  dim3 grid(a.H * psplit, a.B);
+  trace_pre(K_SSM_STEP, s);
+  switch (lpr) {
+    case 4: ssm_step_kernel<4><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
+    case 8: ssm_step_kernel<8><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
+    case 16: ssm_step_kernel<16><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
+    default: ssm_step_kernel<32><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
+  }
+  trace_post(K_SSM_STEP, s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ sequential scan
+
+// T steps of the recurrence for one sequence; the CTA's slice of the state
+// (one row per thread group) lives in registers for the whole block of tokens.
+// Inputs of step t+1 are fetched while step t is computed.
+template <int LPR>
+__global__ void __launch_bounds__(256) ssm_scan_seq_kernel(const ScanArgs a, int psplit) {
+  constexpr int RPW = 32 / LPR;
+  constexpr int ROWS = 8 * RPW;  // rows per CTA
+  const int h = blockIdx.x / psplit;
+  const int pc = blockIdx.x % psplit;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n4 = (lane % LPR) * 4;
+  const int g = h / (a.H / a.G);
+  const int p = pc * ROWS + warp * RPW + lane / LPR;
+  const bool active = p < a.P;
+  const int pp = active ? p : 0;
+  const float Dh = a.D[h];
+  const float Ah = -expf(a.A_log[h]);
+  const float dtb = a.dt_bias[h];
+  float4* hp = reinterpret_cast<float4*>(a.h + ((size_t)h * a.P + pp) * a.N + n4);
+  float4 hv = active ? *hp : make_float4(0.f, 0.f, 0.f, 0.f);
+
+  const size_t xoff = (size_t)h * a.P + pp;
+  const size_t boff = (size_t)g * a.N + n4;
+  // prefetch step 0
+  float x_n = bf16_to_f32(a.x[xoff]);
+  float dr_n = bf16_to_f32(a.dt[h]);
+  float4 B_n = ld4bf(a.Bm + boff), C_n = ld4bf(a.Cm + boff);
+  for (int t = 0; t < a.T; ++t) {
+    const float xv = x_n, dr = dr_n;
+    const float4 Bv = B_n, Cv = C_n;
+    if (t + 1 < a.T) {
+      x_n = bf16_to_f32(a.x[(size_t)(t + 1) * a.ld_in + xoff]);
+      dr_n = bf16_to_f32(a.dt[(size_t)(t + 1) * a.ld_dt + h]);
+      B_n = ld4bf(a.Bm + (size_t)(t + 1) * a.ld_in + boff);
+      C_n = ld4bf(a.Cm + (size_t)(t + 1) * a.ld_in + boff);
+    }
+    float dt = softplus_f(dr + dtb);
+    dt = fminf(fmaxf(dt, 1e-9f), 1e9f);
+    const float dA = expf(dt * Ah);
+    const float dtx = dt * xv;
+    hv.x = fmaf(dA, hv.x, dtx * Bv.x);
+    hv.y = fmaf(dA, hv.y, dtx * Bv.y);
+    hv.z = fmaf(dA, hv.z, dtx * Bv.z);
+    hv.w = fmaf(dA, hv.w, dtx * Bv.w);
+    float yp = Cv.x * hv.x + Cv.y * hv.y + Cv.z * hv.z + Cv.w * hv.w;
+#pragma unroll
+    for (int o = LPR / 2; o > 0; o >>= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
+    if (active && (lane % LPR) == 0) a.y[(size_t)t * a.ldy + xoff] = yp + Dh * xv;
+  }
+  if (active) *hp = hv;
+  if (a.pos_inc && blockIdx.x == 0 && threadIdx.x == 0) a.pos_inc[0] += a.T;
+}
+
+cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s) {
+  const int lpr = a.N / 4;
+  const int rows = 8 * (32 / lpr);
+  const int psplit = (a.P + rows - 1) / rows;
+  trace_pre(K_SSM_SCAN_SEQ, s);
+  switch (lpr) {
+    case 4: ssm_scan_seq_kernel<4><<<a.H * psplit, 256, 0, s>>>(a, psplit); break;
+    case 8: ssm_scan_seq_kernel<8><<<a.H * psplit, 256, 0, s>>>(a, psplit); break;
+    case 16: ssm_scan_seq_kernel<16><<<a.H * psplit, 256, 0, s>>>(a, psplit); break;
+    default: ssm_scan_seq_kernel<32><<<a.H * psplit, 256, 0, s>>>(a, psplit); break;
+  }
+  trace_post(K_SSM_SCAN_SEQ, s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ gated norm
+
+// g = bf16( y / sqrt(mean_group(y^2) + eps) * w * silu(z) ), one CTA per
+// (row, group).
+__global__ void __launch_bounds__(256) gated_norm_kernel(const float* __restrict__ y, int ldy,
+                                                         const uint16_t* __restrict__ z, int ldz,
+                                                         const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                                         int ldo, int group, float eps) {
+  const int m = blockIdx.x;
+  const int g0 = blockIdx.y * group;
+  const float* yr = y + (size_t)m * ldy + g0;
+  __shared__ float red[8];
+  float ss = 0.0f;
+  for (int i = threadIdx.x * 4; i < group; i += 1024) {
+    const float4 v = *reinterpret_cast<const float4*>(yr + i);
+    ss = fmaf(v.x, v.x, ss);
+    ss = fmaf(v.y, v.y, ss);
+    ss = fmaf(v.z, v.z, ss);
+    ss = fmaf(v.w, v.w, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tot += red[i];
+  const float r = 1.0f / sqrtf(tot / (float)group + eps);
+  const uint16_t* zr = z + (size_t)m * ldz + g0;
+  const uint16_t* wr = w + g0;
+  uint16_t* o = out + (size_t)m * ldo + g0;
+  for (int i = threadIdx.x * 4; i < group; i += 1024) {
+    const float4 v = *reinterpret_cast<const float4*>(yr + i);
+    const float4 zz = ld4bf(zr + i);
+    const float4 ww = ld4bf(wr + i);
+    const uint32_t lo = pack_bf16x2(v.x * r * ww.x * silu_f(zz.x), v.y * r * ww.y * silu_f(zz.y));
+    const uint32_t hi = pack_bf16x2(v.z * r * ww.z * silu_f(zz.z), v.w * r * ww.w * silu_f(zz.w));
+    *reinterpret_cast<uint2*>(o + i) = make_uint2(lo, hi);
+  }
+}
+
+cudaError_t launch_gated_norm(const float* y, int32_t ldy, const uint16_t* z, int32_t ldz, const uint16_t* w,
+                              uint16_t* out, int32_t ldo, int32_t M, int32_t d, int32_t group, float eps,
+                              cudaStream_t s) {
+  trace_pre(K_GATED_NORM, s);
+  gated_norm_kernel<<<dim3(M, d / group), 256, 0, s>>>(y, ldy, z, ldz, w, out, ldo, group, eps);
+  trace_post(K_GATED_NORM, s);
+  return cudaGetLastError();
+}
+
+int status_mixer(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
+  if (clear) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
+  }
+  return v;
+}
+
+}  // namespace m2

@@ -1,0 +1,453 @@
+// m2_abi.cu -- the exported C ABI (include/mamba2.h): host-side validation,
+// workspace carving, the launch sequence of the decode and prefill paths,
+// launch counting, per-kernel event tracing and the device status word.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/mamba2.h"
+#include "m2_kernels.h"
+
+namespace m2 {
+
+// ------------------------------------------------------------------ device info
+
+static int g_sms[64];
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (g_sms[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    g_sms[dev] = v;
+  }
+  return g_sms[dev];
+}
+
+cudaError_t set_smem_once(const void* func, int bytes, int* done_mask) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done_mask[dev] >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done_mask[dev] = bytes;
+  return e;
+}
+
+// ------------------------------------------------------------------ tracing
+
+static std::atomic<int64_t> g_launches{0};
+static std::mutex g_trace_mu;
+struct TraceSlot {
+  cudaEvent_t a, b;
+  int32_t id;
+};
+static std::vector<TraceSlot> g_trace;
+static int32_t g_trace_used = 0;
+static bool g_trace_on = false;
+
+void trace_pre(int32_t id, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_trace_on) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_trace_used < (int32_t)g_trace.size()) {
+    g_trace[g_trace_used].id = id;
+    cudaEventRecord(g_trace[g_trace_used].a, s);
+  }
+}
+
+void trace_post(int32_t id, cudaStream_t s) {
+  (void)id;
+  if (!g_trace_on) return;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (g_trace_used < (int32_t)g_trace.size()) {
+    cudaEventRecord(g_trace[g_trace_used].b, s);
+    ++g_trace_used;
+  }
+}
+
+static const char* kNames[K_COUNT] = {
+    "rmsnorm",       "gemv_fp8",        "gemv_fp8_inproj_conv", "gemv_fp8_outproj_resid",
+    "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
+    "conv_pos",      "ssm_step",        "gated_norm",      "conv_prefill",
+    "ssm_scan_seq",  "gemm_tc",         "ssd_chunk_state", "ssd_state_pass",
+    "ssd_chunk_out"};
+
+// ------------------------------------------------------------------ helpers
+
+static inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static inline bool al8(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
+static inline size_t rup(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Derived {
+  int d_inner, d_xbc, n_in, ldz;
+};
+
+static Derived derive(const m2_dims& d) {
+  Derived r;
+  r.d_inner = d.nheads * d.head_dim;
+  r.d_xbc = r.d_inner + 2 * d.n_groups * d.d_state;
+  r.n_in = r.d_inner + r.d_xbc + d.nheads;
+  r.ldz = (int)rup((size_t)r.n_in, 8);
+  return r;
+}
+
+static int check_dims(const m2_dims* d) {
+  if (!d) return M2_ERR_ARG;
+  if (d->hidden <= 0 || d->nheads <= 0 || d->head_dim <= 0 || d->d_state <= 0 || d->n_groups <= 0 || d->d_conv <= 0)
+    return M2_ERR_ARG;
+  if (d->nheads % d->n_groups) return M2_ERR_ARG;
+  if (!(d->eps_in >= 0.0f) || !(d->eps_gated >= 0.0f)) return M2_ERR_ARG;
+  const int d_inner = d->nheads * d->head_dim;
+  if (d->hidden % 16 || d->hidden > 16384 || d_inner % 16 || d_inner > 16384) return M2_ERR_UNSUPPORTED;
+  if (!(d->d_state == 16 || d->d_state == 32 || d->d_state == 64 || d->d_state == 128)) return M2_ERR_UNSUPPORTED;
+  if (d->head_dim > 256 || d->d_conv < 2 || d->d_conv > 8) return M2_ERR_UNSUPPORTED;
+  if (d->gnorm_group <= 0 || d_inner % d->gnorm_group || d->gnorm_group % 16) return M2_ERR_UNSUPPORTED;
+  return M2_OK;
+}
+
+static int check_weight(const m2_weight& w, int n, int k) {
+  if (!w.w) return M2_ERR_ARG;
+  if (w.n != n || w.k != k) return M2_ERR_ARG;
+  if (!al16(w.w)) return M2_ERR_ALIGN;
+  if (w.fmt == M2_W_FP8_BLOCK128) {
+    if (!w.scale) return M2_ERR_FORMAT;
+    if (k % 16 || k > 16384) return M2_ERR_UNSUPPORTED;
+  } else if (w.fmt == M2_W_BF16) {
+    if (w.scale) return M2_ERR_FORMAT;
+    if (k % 8 || k > 16384) return M2_ERR_UNSUPPORTED;
+  } else {
+    return M2_ERR_FORMAT;
+  }
+  return M2_OK;
+}
+
+static size_t decode_ws(const m2_dims& d, int B) {
+  const Derived r = derive(d);
+  size_t o = 0;
+  o = rup(o + (size_t)B * d.hidden * 2, 256);
+  o = rup(o + (size_t)B * r.ldz * 2, 256);
+  o = rup(o + (size_t)B * r.d_inner * 4, 256);
+  o = rup(o + (size_t)B * r.d_inner * 2, 256);
+  return o;
+}
+
+static size_t prefill_ws(const m2_dims& d, int T) {
+  const Derived r = derive(d);
+  size_t o = 0;
+  o = rup(o + (size_t)T * d.hidden * 2, 256);   // xn
+  o = rup(o + (size_t)T * r.ldz * 2, 256);      // zx (raw in_proj output)
+  o = rup(o + (size_t)T * r.d_xbc * 2, 256);    // u (conv output)
+  o = rup(o + (size_t)T * r.d_inner * 4, 256);  // y
+  o = rup(o + (size_t)T * r.d_inner * 2, 256);  // g
+  return o;
+}
+
+static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
+                        GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr) {
+  GemvArgs a;
+  memset(&a, 0, sizeof(a));
+  if (extra) a = *extra;
+  a.A = A;
+  a.lda = lda;
+  a.W = w.w;
+  a.S = w.scale;
+  a.M = M;
+  a.N = w.n;
+  a.K = w.k;
+  a.out = out;
+  a.ldo = ldo;
+  a.epi = epi;
+  a.resid = resid;
+  a.ldr = ldr;
+  const int rowbytes = w.k * (w.fmt == M2_W_FP8_BLOCK128 ? 1 : 2);
+  const int grp = rowbytes <= 4096 ? 4 : (rowbytes <= 8192 ? 2 : 1);
+  a.evict_first = M <= grp ? 1 : 0;
+  return launch_gemv(a, w.fmt == M2_W_FP8_BLOCK128, s);
+}
+
+static int launch_status(cudaError_t e) {
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return M2_ERR_LAUNCH;
+  }
+  return M2_OK;
+}
+
+}  // namespace m2
+
+using namespace m2;
+
+extern "C" {
+
+const char* m2_strerror(int status) {
+  switch (status) {
+    case M2_OK: return "ok";
+    case M2_ERR_ARG: return "invalid argument (null pointer or bad size)";
+    case M2_ERR_FORMAT: return "weight format tag or scale grid inconsistent";
+    case M2_ERR_WORKSPACE: return "workspace missing or too small";
+    case M2_ERR_LAUNCH: return "CUDA launch failed";
+    case M2_ERR_UNSUPPORTED: return "shape outside the supported range";
+    case M2_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case M2_ERR_DEVICE: return "no usable CUDA device";
+    case M2_ERR_TIMEOUT: return "a bounded in-kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int m2_validate(const m2_dims* dims, const m2_layer* L) {
+  int st = check_dims(dims);
+  if (st) return st;
+  if (!L) return M2_ERR_ARG;
+  const Derived r = derive(*dims);
+  if (!L->norm_w || !L->conv_w || !L->A_log || !L->D || !L->dt_bias || !L->gnorm_w) return M2_ERR_ARG;
+  if (!al16(L->norm_w) || !al16(L->gnorm_w)) return M2_ERR_ALIGN;
+  if ((st = check_weight(L->in_proj, r.n_in, dims->hidden))) return st;
+  if ((st = check_weight(L->out_proj, dims->hidden, r.d_inner))) return st;
+  return M2_OK;
+}
+
+size_t m2_workspace_bytes(const m2_dims* dims, int32_t max_batch, int32_t max_tokens) {
+  if (check_dims(dims) || max_batch < 0 || max_tokens < 0) return 0;
+  const size_t a = decode_ws(*dims, max_batch), b = prefill_ws(*dims, max_tokens);
+  return a > b ? a : b;
+}
+
+int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t B, float* ssm_state,
+                        uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int st = m2_validate(dims, L);
+  if (st) return st;
+  if (B <= 0 || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
+  if (!al16(hidden) || !al16(ssm_state) || !al8(conv_state)) return M2_ERR_ALIGN;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < decode_ws(*dims, B)) return M2_ERR_WORKSPACE;
+  const m2_dims& d = *dims;
+  const Derived r = derive(d);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  size_t o = 0;
+  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + o);
+  o = rup(o + (size_t)B * d.hidden * 2, 256);
+  uint16_t* zxu = reinterpret_cast<uint16_t*>(w8 + o);
+  o = rup(o + (size_t)B * r.ldz * 2, 256);
+  float* y = reinterpret_cast<float*>(w8 + o);
+  o = rup(o + (size_t)B * r.d_inner * 4, 256);
+  uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
+
+  cudaError_t e;
+  // 1. RMSNorm
+  if ((e = launch_rmsnorm(hidden, d.hidden, L->norm_w, xn, d.hidden, B, d.hidden, d.eps_in, stream))) return launch_status(e);
+  // 2+3. in_proj with the conv1d update (bias, SiLU) fused into its epilogue
+  GemvArgs ex;
+  memset(&ex, 0, sizeof(ex));
+  ex.ring = conv_state;
+  ex.pos = conv_pos;
+  ex.conv_w = L->conv_w;
+  ex.conv_b = L->conv_b;
+  ex.xbc0 = r.d_inner;
+  ex.d_xbc = r.d_xbc;
+  ex.dconv = d.d_conv;
+  if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex)))
+    return launch_status(e);
+  // 4+5. split and SSM step (advances conv_pos)
+  SsmArgs sa;
+  sa.h = ssm_state;
+  sa.x = zxu + r.d_inner;
+  sa.Bm = zxu + 2 * r.d_inner;
+  sa.Cm = zxu + 2 * r.d_inner + d.n_groups * d.d_state;
+  sa.dt = zxu + r.d_inner + r.d_xbc;
+  sa.ld_in = r.ldz;
+  sa.A_log = L->A_log;
+  sa.D = L->D;
+  sa.dt_bias = L->dt_bias;
+  sa.y = y;
+  sa.ldy = r.d_inner;
+  sa.B = B;
+  sa.H = d.nheads;
+  sa.P = d.head_dim;
+  sa.N = d.d_state;
+  sa.G = d.n_groups;
+  sa.pos_inc = conv_pos;
+  if ((e = launch_ssm_step(sa, stream))) return launch_status(e);
+  // 6. gated RMSNorm
+  if ((e = launch_gated_norm(y, r.d_inner, zxu, r.ldz, L->gnorm_w, g, r.d_inner, B, r.d_inner, d.gnorm_group,
+                             d.eps_gated, stream)))
+    return launch_status(e);
+  // 7+8. out_proj with the residual add fused into its epilogue (in place)
+  if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream)))
+    return launch_status(e);
+  return M2_OK;
+}
+
+int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t T, float* ssm_state,
+                         uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  int st = m2_validate(dims, L);
+  if (st) return st;
+  if (T <= 0 || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
+  if (!al16(hidden) || !al16(ssm_state) || !al8(conv_state)) return M2_ERR_ALIGN;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < prefill_ws(*dims, T)) return M2_ERR_WORKSPACE;
+  const m2_dims& d = *dims;
+  const Derived r = derive(d);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  size_t o = 0;
+  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + o);
+  o = rup(o + (size_t)T * d.hidden * 2, 256);
+  uint16_t* zx = reinterpret_cast<uint16_t*>(w8 + o);
+  o = rup(o + (size_t)T * r.ldz * 2, 256);
+  uint16_t* u = reinterpret_cast<uint16_t*>(w8 + o);
+  o = rup(o + (size_t)T * r.d_xbc * 2, 256);
+  float* y = reinterpret_cast<float*>(w8 + o);
+  o = rup(o + (size_t)T * r.d_inner * 4, 256);
+  uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
+
+  cudaError_t e;
+  if ((e = launch_rmsnorm(hidden, d.hidden, L->norm_w, xn, d.hidden, T, d.hidden, d.eps_in, stream))) return launch_status(e);
+  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream))) return launch_status(e);
+  if ((e = launch_conv_prefill(conv_state, conv_pos, zx + r.d_inner, r.ldz, L->conv_w, L->conv_b, u, r.d_xbc, T,
+                               r.d_xbc, d.d_conv, stream)))
+    return launch_status(e);
+  ScanArgs sa;
+  sa.h = ssm_state;
+  sa.x = u;
+  sa.Bm = u + r.d_inner;
+  sa.Cm = u + r.d_inner + d.n_groups * d.d_state;
+  sa.dt = zx + r.d_inner + r.d_xbc;
+  sa.ld_in = r.d_xbc;
+  sa.ld_dt = r.ldz;
+  sa.A_log = L->A_log;
+  sa.D = L->D;
+  sa.dt_bias = L->dt_bias;
+  sa.y = y;
+  sa.ldy = r.d_inner;
+  sa.T = T;
+  sa.H = d.nheads;
+  sa.P = d.head_dim;
+  sa.N = d.d_state;
+  sa.G = d.n_groups;
+  sa.pos_inc = conv_pos;
+  if ((e = launch_ssm_scan_seq(sa, stream))) return launch_status(e);
+  if ((e = launch_gated_norm(y, r.d_inner, zx, r.ldz, L->gnorm_w, g, r.d_inner, T, r.d_inner, d.gnorm_group,
+                             d.eps_gated, stream)))
+    return launch_status(e);
+  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream)))
+    return launch_status(e);
+  return M2_OK;
+}
+
+int w8a16_gemv(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* out, int32_t M, int32_t N,
+               int32_t K, cudaStream_t stream) {
+  if (!A || !W || !S || !out || M <= 0 || N <= 0 || K <= 0) return M2_ERR_ARG;
+  if (K % 16 || K > 16384) return M2_ERR_UNSUPPORTED;
+  if (!al16(A) || !al16(W)) return M2_ERR_ALIGN;
+  m2_weight w;
+  w.w = W;
+  w.scale = S;
+  w.n = N;
+  w.k = K;
+  w.fmt = M2_W_FP8_BLOCK128;
+  return launch_status(proj(w, A, K, M, out, N, EPI_STORE, nullptr, 0, stream));
+}
+
+int conv1d_update(uint16_t* conv_state, int32_t* conv_pos, const uint16_t* x, int32_t ld_x, const uint16_t* w,
+                  const uint16_t* bias, uint16_t* out, int32_t B, int32_t C, int32_t d_conv, int32_t silu,
+                  cudaStream_t stream) {
+  if (!conv_state || !conv_pos || !x || !w || !out || B <= 0 || C <= 0 || ld_x < C) return M2_ERR_ARG;
+  if (d_conv < 2 || d_conv > 8) return M2_ERR_UNSUPPORTED;
+  cudaError_t e = launch_conv_update(conv_state, conv_pos, x, ld_x, w, bias, out, C, B, C, d_conv, silu, stream);
+  if (e) return launch_status(e);
+  return launch_status(launch_conv_pos(conv_pos, B, 1, stream));
+}
+
+int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint16_t* Cm, const uint16_t* dt_raw,
+                    int32_t ld_in, const float* A_log, const float* D, const float* dt_bias, float* y, int32_t B,
+                    int32_t H, int32_t P, int32_t N, int32_t G, cudaStream_t stream) {
+  if (!h || !x || !Bm || !Cm || !dt_raw || !A_log || !D || !dt_bias || !y) return M2_ERR_ARG;
+  if (B <= 0 || H <= 0 || P <= 0 || N <= 0 || G <= 0 || H % G) return M2_ERR_ARG;
+  if (!(N == 16 || N == 32 || N == 64 || N == 128) || P > 256) return M2_ERR_UNSUPPORTED;
+  if (ld_in % 4 || ld_in < H * P) return M2_ERR_ARG;
+  if (!al16(h) || !al8(Bm) || !al8(Cm)) return M2_ERR_ALIGN;
+  SsmArgs sa;
+  sa.h = h;
+  sa.x = x;
+  sa.Bm = Bm;
+  sa.Cm = Cm;
+  sa.dt = dt_raw;
+  sa.ld_in = ld_in;
+  sa.A_log = A_log;
+  sa.D = D;
+  sa.dt_bias = dt_bias;
+  sa.y = y;
+  sa.ldy = H * P;
+  sa.B = B;
+  sa.H = H;
+  sa.P = P;
+  sa.N = N;
+  sa.G = G;
+  sa.pos_inc = nullptr;
+  return launch_status(launch_ssm_step(sa, stream));
+}
+
+int m2_device_status(int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return M2_ERR_LAUNCH;
+  const int parts[] = {status_gemv(clear), status_mixer(clear)};
+  for (int v : parts)
+    if (v != 0) return v;
+  return M2_OK;
+}
+
+int64_t m2_launch_count(void) { return g_launches.load(); }
+
+int m2_trace_begin(int32_t capacity) {
+  if (capacity <= 0) return M2_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  for (auto& t : g_trace) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  g_trace.assign(capacity, TraceSlot{});
+  for (auto& t : g_trace) {
+    if (cudaEventCreate(&t.a) != cudaSuccess || cudaEventCreate(&t.b) != cudaSuccess) return M2_ERR_LAUNCH;
+  }
+  g_trace_used = 0;
+  g_trace_on = true;
+  return M2_OK;
+}
+
+int m2_trace_end(double* ms, int32_t* launches, int32_t n_ids) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = false;
+  if (ms && launches) {
+    for (int i = 0; i < n_ids; ++i) {
+      ms[i] = 0.0;
+      launches[i] = 0;
+    }
+  }
+  for (int i = 0; i < g_trace_used; ++i) {
+    const TraceSlot& t = g_trace[i];
+    if (cudaEventSynchronize(t.b) != cudaSuccess) return M2_ERR_LAUNCH;
+    float v = 0.f;
+    cudaEventElapsedTime(&v, t.a, t.b);
+    if (ms && launches && t.id >= 0 && t.id < n_ids) {
+      ms[t.id] += v;
+      launches[t.id] += 1;
+    }
+  }
+  for (auto& t : g_trace) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  g_trace.clear();
+  const int used = g_trace_used;
+  g_trace_used = 0;
+  return used;
+}
+
+const char* m2_kernel_name(int32_t id) { return (id >= 0 && id < K_COUNT) ? kNames[id] : nullptr; }
+
+int32_t m2_kernel_count(void) { return K_COUNT; }
+
+}  // extern "C"

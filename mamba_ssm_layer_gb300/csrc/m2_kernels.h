@@ -1,0 +1,137 @@
+// m2_kernels.h -- internal (not exported) launcher interface between the ABI
+// layer (m2_abi.cu) and the kernel translation units.  Launchers enqueue on
+// `stream`, do no argument validation (the ABI layer did it) and return a
+// cudaError_t from the launch.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace m2 {
+
+// Kernel ids for launch counting and tracing (names in m2_abi.cu).
+enum KernelId : int32_t {
+  K_RMSNORM = 0,
+  K_GEMV_FP8,        // + GemvEpi: store, conv (in_proj), resid (out_proj)
+  K_GEMV_FP8_CONV,
+  K_GEMV_FP8_RESID,
+  K_GEMV_BF16,
+  K_GEMV_BF16_CONV,
+  K_GEMV_BF16_RESID,
+  K_CONV_UPDATE,
+  K_CONV_POS,
+  K_SSM_STEP,
+  K_GATED_NORM,
+  K_CONV_PREFILL,
+  K_SSM_SCAN_SEQ,
+  K_GEMM_TC,
+  K_SSD_CHUNK_STATE,
+  K_SSD_STATE_PASS,
+  K_SSD_CHUNK_OUT,
+  K_COUNT
+};
+
+// Called by every launcher around its launch (counting / tracing).
+void trace_pre(int32_t id, cudaStream_t s);
+void trace_post(int32_t id, cudaStream_t s);
+
+// Host readers of each translation unit's device status word (0 or
+// M2_ERR_TIMEOUT); clear != 0 resets it.
+int status_gemv(int clear);
+int status_mixer(int clear);
+
+// Number of SMs of the current device (cached).
+int num_sms();
+
+// Opt a kernel into large dynamic shared memory once per device.
+cudaError_t set_smem_once(const void* func, int bytes, int* done_mask);
+
+// ------------------------------------------------------------------ GEMV
+
+enum GemvEpi : int32_t {
+  EPI_STORE = 0,       // out[m*ldo+n] = bf16(acc)
+  EPI_RESID = 1,       // out[m*ldo+n] = bf16(resid[m*ldr+n] + acc)   (resid may alias out)
+  EPI_INPROJ_CONV = 2  // rows [xbc0, xbc0+d_xbc): conv update + SiLU; other rows: store
+};
+
+struct GemvArgs {
+  const uint16_t* A;   // [M][lda] bf16
+  int32_t lda;
+  const void* W;       // [N][K] E4M3 or bf16
+  const uint16_t* S;   // E4M3 scales [ceil(N/128)][ceil(K/128)] (unused for bf16)
+  int32_t M, N, K;
+  uint16_t* out;       // [M][ldo]
+  int32_t ldo;
+  int32_t epi;
+  const uint16_t* resid;  // EPI_RESID
+  int32_t ldr;
+  // EPI_INPROJ_CONV: ring [M][dconv-1][d_xbc], pos [M], conv_w [d_xbc][dconv], conv_b [d_xbc]
+  uint16_t* ring;
+  const int32_t* pos;
+  const uint16_t* conv_w;
+  const uint16_t* conv_b;
+  int32_t xbc0, d_xbc, dconv;
+  int32_t evict_first;  // stream weights with the L2 evict-first policy
+};
+
+// CUDA-core GEMV (fp32 accumulation) with bulk-copy weight streaming; any M
+// (processed in groups of up to 4 rows, re-streaming the weights per group).
+cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s);
+
+// ------------------------------------------------------------------ mixer ops
+
+cudaError_t launch_rmsnorm(const uint16_t* x, int32_t ldx, const uint16_t* w, uint16_t* out, int32_t ldo,
+                           int32_t M, int32_t K, float eps, cudaStream_t s);
+
+// One-token conv update for B sequences (no pos advance; see launch_conv_pos).
+cudaError_t launch_conv_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, int32_t ldx,
+                               const uint16_t* w, const uint16_t* b, uint16_t* out, int32_t ldo, int32_t B,
+                               int32_t C, int32_t dconv, int32_t silu, cudaStream_t s);
+cudaError_t launch_conv_pos(int32_t* pos, int32_t B, int32_t add, cudaStream_t s);
+
+struct SsmArgs {
+  float* h;            // [B][H][P][N]
+  const uint16_t* x;   // rows ld_in apart
+  const uint16_t* Bm;
+  const uint16_t* Cm;
+  const uint16_t* dt;
+  int32_t ld_in;
+  const float* A_log;
+  const float* D;
+  const float* dt_bias;
+  float* y;            // [B][ldy]
+  int32_t ldy;
+  int32_t B, H, P, N, G;
+  int32_t* pos_inc;    // if non-null: pos_inc[b] += 1 (decode fusion)
+};
+cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s);
+
+cudaError_t launch_gated_norm(const float* y, int32_t ldy, const uint16_t* z, int32_t ldz, const uint16_t* w,
+                              uint16_t* out, int32_t ldo, int32_t M, int32_t d, int32_t group, float eps,
+                              cudaStream_t s);
+
+// Prefill conv over T tokens of one sequence: xbc rows ldx apart -> u [T][ldu];
+// reads the ring for the first d_conv-1 taps and leaves it holding the last
+// tokens.  Does not advance pos.
+cudaError_t launch_conv_prefill(uint16_t* ring, const int32_t* pos, const uint16_t* xbc, int32_t ldx,
+                                const uint16_t* w, const uint16_t* b, uint16_t* u, int32_t ldu, int32_t T,
+                                int32_t C, int32_t dconv, cudaStream_t s);
+
+// Sequential per-token scan of one sequence (T steps, state in registers).
+struct ScanArgs {
+  float* h;            // [H][P][N]
+  const uint16_t* x;   // [T] rows ld_in apart
+  const uint16_t* Bm;
+  const uint16_t* Cm;
+  const uint16_t* dt;  // [T] rows ld_dt apart
+  int32_t ld_in, ld_dt;
+  const float* A_log;
+  const float* D;
+  const float* dt_bias;
+  float* y;            // [T][ldy]
+  int32_t ldy;
+  int32_t T, H, P, N, G;
+  int32_t* pos_inc;    // pos_inc[0] += T if non-null
+};
+cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s);
+
+}  // namespace m2

@@ -1,0 +1,77 @@
+"""Device-side holders for one Mamba-2 layer and its per-sequence state.
+
+PyTorch provides the device memory and the stream; every computation is one of
+the C entry points in ``abi``.  Host arrays (numpy, bf16 as uint16 bits) are
+uploaded once.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import abi
+
+
+def to_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    """Upload a numpy array (uint16 bf16 bits stay int16-typed bit patterns)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16))
+    elif a.dtype == np.uint8:
+        t = torch.from_numpy(a)
+    else:
+        t = torch.from_numpy(a)
+    return t.to(device)
+
+
+def bits_u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().view(np.uint16)
+
+
+class DeviceLayer:
+    """One layer's parameters on the device plus the ctypes structs that point at them."""
+
+    def __init__(self, layer: dict, device="cuda"):
+        d = layer["dims"]
+        self.dims_dict = d
+        self.dims = abi.dims_struct(d)
+        d_inner = d["nheads"] * d["head_dim"]
+        self.d_inner = d_inner
+        self.d_xbc = d_inner + 2 * d["n_groups"] * d["d_state"]
+        self.n_in = d_inner + self.d_xbc + d["nheads"]
+        self.t = {k: to_dev(layer[k], device) for k in ("norm_w", "in_w", "conv_w", "conv_b", "A_log", "D", "dt_bias",
+                                                         "gnorm_w", "out_w")}
+        for k in ("in_s", "out_s"):
+            self.t[k] = None if layer.get(k) is None else to_dev(layer[k], device)
+        fi = abi.M2_W_FP8_BLOCK128 if layer["in_fmt"] == "fp8" else abi.M2_W_BF16
+        fo = abi.M2_W_FP8_BLOCK128 if layer["out_fmt"] == "fp8" else abi.M2_W_BF16
+        t = self.t
+        self.struct = abi.M2Layer(
+            t["norm_w"].data_ptr(),
+            abi.weight_struct(t["in_w"], t["in_s"], self.n_in, d["hidden"], fi),
+            t["conv_w"].data_ptr(), t["conv_b"].data_ptr(), t["A_log"].data_ptr(), t["D"].data_ptr(),
+            t["dt_bias"].data_ptr(), t["gnorm_w"].data_ptr(),
+            abi.weight_struct(t["out_w"], t["out_s"], d["hidden"], d_inner, fo))
+
+    def new_state(self, B: int, device="cuda"):
+        d = self.dims_dict
+        h = torch.zeros((B, d["nheads"], d["head_dim"], d["d_state"]), dtype=torch.float32, device=device)
+        ring = torch.zeros((B, d["d_conv"] - 1, self.d_xbc), dtype=torch.int16, device=device)
+        pos = torch.zeros(B, dtype=torch.int32, device=device)
+        return h, ring, pos
+
+    def workspace(self, max_batch: int, max_tokens: int, device="cuda") -> torch.Tensor:
+        n = abi.m2_workspace_bytes(self.dims, max_batch, max_tokens)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+    def decode(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None) -> None:
+        h, ring, pos = state
+        B = hidden.shape[0]
+        abi.mamba2_layer_decode(self.dims, self.struct, hidden, B, h, ring, pos, ws, ws.numel(),
+                                stream if stream is not None else torch.cuda.current_stream())
+
+    def prefill(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None) -> None:
+        h, ring, pos = state
+        T = hidden.shape[0]
+        abi.mamba2_layer_prefill(self.dims, self.struct, hidden, T, h, ring, pos, ws, ws.numel(),
+                                 stream if stream is not None else torch.cuda.current_stream())
