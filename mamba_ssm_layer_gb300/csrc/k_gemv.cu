@@ -4,20 +4,32 @@
 // (page "Struct Qwen3SsmLayer", `set_fp8_decode_weights`; scale index of
 // "Struct NemotronMamba2Layer", `set_fp8_weights`) or W~ = bf16 W (native BF16
 // projections).  The decode GEMV is HBM-bound: every weight byte is read once
-// per call, so the design goal is to keep ~200 KB of weight reads in flight per
-// SM and to spend few instructions per byte.
+// per call, so the design keeps ~180 KB of weight reads in flight per SM and
+// keeps every latency (activation prologue, reductions, epilogue inputs) off
+// the streaming loop.
 //
-// Layout of one CTA (one per SM, persistent over a contiguous row range):
-//   warp 8      producer: one lane streams R whole weight rows per stage
+// One CTA per SM, persistent over a contiguous range of rows:
+//   warp 16     producer: one lane streams R whole weight rows per stage
 //               (R*K contiguous bytes) into a shared-memory ring with 1-D bulk
 //               copies (cp.async.bulk, mbarrier completion, L2 evict-first);
-//   warps 0..7  consumers: thread t owns the 16-byte chunks t, t+256, ... of
-//               every row, so its activations (<= 64 fp32) stay in registers
-//               for the whole call; per row it forms 16-element partial dot
-//               products, multiplies each by the chunk's block scale and
-//               accumulates.  Per stage the R*MB partial sums are reduced
-//               with a transposing warp butterfly and one shared-memory pass.
-// E4M3 is decoded in registers with the exact hardware E4M3->f16 conversion.
+//   warps 0..15 consumers, two groups of 8 warps that take alternate stages
+//               (two warps per scheduler per group hide the load/convert/FMA
+//               latencies): thread t of a group owns the 16-byte chunks t,
+//               t+256, ... of every row, so its activations stay in registers
+//               for the whole call.  The activation prologue optionally fuses
+//               the norm that produces A (input RMSNorm, or the gated RMSNorm
+//               of y and z), reduced across the consumers.  Per row a thread
+//               forms 16-element partial dot products, multiplies each by the
+//               chunk's block scale and accumulates; per stage the R*MB sums
+//               are reduced with a transposing warp butterfly and handed to
+//               the helper through a shared-memory slot;
+//   warp 17     helper: stages the block scales and the epilogue inputs (conv
+//               taps and ring, residual) into shared memory, then adds the 8
+//               warps' partials of every stage into the row totals.
+// After the loop all threads run the epilogue (store / residual add / the
+// conv1d update with bias and SiLU) from shared memory.
+// E4M3 is decoded in registers with the exact hardware E4M3->f16 conversion
+// and multiplied by f16 activations with fp32 accumulation (fma.rn.f32.f16).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -26,17 +38,55 @@
 
 namespace m2 {
 
-constexpr int kGemvConsumerWarps = 8;
-constexpr int kGemvConsumers = kGemvConsumerWarps * 32;  // 256
-constexpr int kGemvThreads = kGemvConsumers + 32;        // + producer warp
-constexpr int kGemvStageBudget = 196608;                 // bytes of weight ring
+constexpr int kGemvConsumerWarps = 8;                    // warps per consumer group
+constexpr int kGemvGroups = 2;                           // groups take alternate stages
+constexpr int kGemvConsumers = kGemvConsumerWarps * 32;  // 256 threads per group
+constexpr int kGemvAllConsumers = kGemvGroups * kGemvConsumers;
+constexpr int kGemvProducerWarp = kGemvGroups * kGemvConsumerWarps;  // warp 16
+constexpr int kGemvHelperWarp = kGemvProducerWarp + 1;               // warp 17
+constexpr int kGemvThreads = kGemvAllConsumers + 64;                 // 576
+constexpr int kGemvStageBudget = 184320;                 // bytes of weight ring
 constexpr int kGemvMaxStages = 8;
+constexpr int kGemvSlots = 4;                            // reduction slots
+constexpr int kMaxGroups = 64;                           // gated-norm groups per row
 
 struct GemvSmemTail {
   uint64_t full[kGemvMaxStages];
   uint64_t empty[kGemvMaxStages];
-  float red[2][kGemvConsumerWarps][32];
+  uint64_t red_full[kGemvSlots];
+  uint64_t red_empty[kGemvSlots];
+  float red[kGemvSlots][kGemvConsumerWarps][32];
+  float nsum[4][kMaxGroups];  // norm reductions (per batch row, per group)
+  float nss[2][4][kGemvConsumerWarps];  // input-RMSNorm (hi, lo) per row per warp
+  double nrd[4];              // 1/sqrt(mean(x^2)+eps) per row, in double
+  unsigned amax[4];           // max |activation| per batch row (float bits)
+  float unscale[4];           // 2^-j undoing the f16 prescale of row m
 };
+
+// Mixed-precision multiply-add with fp32 accumulation (a*b+c, one rounding):
+// two f16 (or bf16) pairs against two fp32 chains.
+__device__ __forceinline__ void fma2_f16(uint32_t w2, uint32_t a2, float& c0, float& c1) {
+  asm("{\n\t.reg .f16 wl, wh, al, ah;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {al, ah}, %3;\n\t"
+      "fma.rn.f32.f16 %0, wl, al, %0;\n\tfma.rn.f32.f16 %1, wh, ah, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(w2), "r"(a2));
+}
+__device__ __forceinline__ void fma2_bf16(uint32_t w2, uint32_t a2, float& c0, float& c1) {
+  asm("{\n\t.reg .b16 wl, wh, al, ah;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {al, ah}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, wl, al, %0;\n\tfma.rn.f32.bf16 %1, wh, ah, %1;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(w2), "r"(a2));
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  return h2;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
 template <bool FP8>
 struct WTraits;
@@ -63,7 +113,8 @@ struct Log2<1> {
 // One level of the transposing warp reduction: lanes with bit `O` set keep the
 // upper half of the CNT live values, the others the lower half, each adding
 // the partner lane's copy of the half it keeps.  Once one value is left the
-// remaining levels are plain xor-reductions.
+// remaining levels are plain xor-reductions.  Afterwards lane l holds the warp
+// total of value index l >> (5 - log2(CNT)).
 template <int CNT, int O>
 struct Butterfly {
   static __device__ __forceinline__ void run(float* v, int lane) {
@@ -82,40 +133,30 @@ struct Butterfly {
     }
   }
 };
-template <int V, int O>
-__device__ __forceinline__ void butterfly(float* v, int lane) {
-  Butterfly<V, O>::run(v, lane);
-}
 
-// Epilogue for one output element (row n, batch row m).
-__device__ __forceinline__ void gemv_epilogue(const GemvArgs& a, int n, int m, float acc) {
-  if (a.epi == EPI_RESID) {
-    float r = bf16_to_f32(a.resid[(size_t)m * a.ldr + n]);
-    a.out[(size_t)m * a.ldo + n] = f32_to_bf16(r + acc);
-    return;
-  }
-  uint16_t vb = f32_to_bf16(acc);  // rounding point of the in_proj output
-  if (a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc) {
-    // conv1d update with bias + SiLU for channel c; this thread owns channel c
-    // of sequence m for the whole call, so reading the ring and then writing
-    // its oldest slot is race-free.
-    const int c = n - a.xbc0;
-    const int L = a.dconv - 1;
-    const int p = a.pos[m];
-    uint16_t* rg = a.ring + (size_t)m * L * a.d_xbc;
-    const uint16_t* wc = a.conv_w + (size_t)c * a.dconv;
-    float s = a.conv_b ? bf16_to_f32(a.conv_b[c]) : 0.0f;
-    for (int j = 0; j < L; ++j) s += bf16_to_f32(wc[j]) * bf16_to_f32(rg[(size_t)((p + j) % L) * a.d_xbc + c]);
-    s += bf16_to_f32(wc[L]) * bf16_to_f32(vb);
-    a.out[(size_t)m * a.ldo + n] = f32_to_bf16(silu_f(s));
-    rg[(size_t)(p % L) * a.d_xbc + c] = vb;
-    return;
-  }
-  a.out[(size_t)m * a.ldo + n] = vb;
+// Shared-memory layout beyond the weight ring (offsets in bytes, host and
+// device agree through this function).
+struct GemvLayout {
+  int tail, sc, tot, epi, total;
+};
+__host__ __device__ inline GemvLayout gemv_layout(int stages, int stage_bytes, int rows_max, int mb, int kb,
+                                                  int epi, int dconv) {
+  GemvLayout L;
+  L.tail = stages * stage_bytes;
+  L.sc = L.tail + (int)((sizeof(GemvSmemTail) + 15) / 16 * 16);
+  const int nbs = rows_max / 128 + 2;  // n-blocks a row range can touch
+  L.tot = L.sc + (nbs * kb * 4 + 15) / 16 * 16;
+  L.epi = L.tot + (rows_max * mb * 4 + 15) / 16 * 16;
+  int epi_bytes = 0;
+  if (epi == EPI_INPROJ_CONV) epi_bytes = rows_max * (dconv + 1) * 2 + mb * rows_max * (dconv - 1) * 2 + 16 * 4;
+  if (epi == EPI_RESID) epi_bytes = mb * rows_max * 2;
+  L.total = L.epi + (epi_bytes + 15) / 16 * 16;
+  return L;
 }
 
 template <bool FP8, int MB, int CPT, int R>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a, int m0, int stages) {
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    gemv_kernel(const GemvArgs a, int m0, int stages, int rows_max) {
   using T = WTraits<FP8>;
   constexpr int V = R * MB;
   constexpr int LOGV = Log2<V>::value;
@@ -124,7 +165,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   extern __shared__ __align__(128) uint8_t smem[];
   const int rowbytes = a.K * T::kEsize;
   const int stage_bytes = R * rowbytes;
-  GemvSmemTail* tail = reinterpret_cast<GemvSmemTail*>(smem + (size_t)stages * stage_bytes);
+  const int kb = (a.K + 127) / 128;
+  const GemvLayout lay = gemv_layout(stages, stage_bytes, rows_max, MB, kb, a.epi, a.dconv);
+  GemvSmemTail* tail = reinterpret_cast<GemvSmemTail*>(smem + lay.tail);
+  float* sc = reinterpret_cast<float*>(smem + lay.sc);
+  float* tot = reinterpret_cast<float*>(smem + lay.tot);
+  uint8_t* epi_s = smem + lay.epi;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -134,135 +180,359 @@ __global__ void __launch_bounds__(kGemvThreads, 1) gemv_kernel(const GemvArgs a,
   const int nrows = row_end - row_begin;
   const int niter = (nrows + R - 1) / R;
   const int nchunks = rowbytes / 16;
-  const int kb = (a.K + 127) / 128;
   const int mvalid = min(MB, a.M - m0);
+  const int nb0 = row_begin >> 7;
+  const int L = a.dconv - 1;
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(&tail->full[s], 1);
       mbar_init(&tail->empty[s], kGemvConsumerWarps);
     }
+    for (int s = 0; s < kGemvSlots; ++s) {
+      mbar_init(&tail->red_full[s], kGemvConsumerWarps);
+      mbar_init(&tail->red_empty[s], 1);
+    }
+    for (int m = 0; m < 4; ++m) tail->amax[m] = 0u;
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kGemvConsumerWarps) {
+  const uint64_t pol = a.evict_first ? policy_evict_first() : policy_evict_normal();
+  const uint8_t* wbase = static_cast<const uint8_t*>(a.W) + (size_t)row_begin * rowbytes;
+  // the producer puts the first stages in flight before anything else: weights
+  // do not depend on the previous kernel
+  if (warp == kGemvProducerWarp && lane == 0) {
+    for (int it = 0; it < niter && it < stages; ++it) {
+      const int rows = min(R, nrows - it * R);
+      const uint32_t bytes = (uint32_t)(rows * rowbytes);
+      mbar_arrive_expect_tx(&tail->full[it], bytes);
+      bulk_g2s(smem + (size_t)it * stage_bytes, wbase + (size_t)it * R * rowbytes, bytes, &tail->full[it], pol);
+    }
+  }
+  if (warp == kGemvHelperWarp && FP8) {
+    // block scales of the n-blocks this row range touches, as fp32
+    const int nbs = ((row_end - 1) >> 7) - nb0 + 1;
+    for (int i = lane; i < nbs * kb; i += 32)
+      sc[i] = bf16_to_f32(__ldg(a.S + (size_t)(nb0 + i / kb) * kb + (i % kb)));
+  }
+  pdl_trigger();
+
+  // ------------------------------------------------ activation prologue
+  // Activations are cached in registers as packed pairs: f16 for E4M3
+  // weights (E4M3 -> f16 is exact, and the products then run as
+  // fma.rn.f32.f16 at full FFMA rate), bf16 for bf16 weights.  For f16 each
+  // batch row is first multiplied by an exact power of two 2^j that puts its
+  // largest magnitude in [2^14, 2^15): every bf16 value within 2^31 of the row
+  // maximum is then exactly representable, and the 2^-j is applied to the
+  // row totals.
+  uint32_t acth[MB][CPT][T::kEpc / 2];
+  const int grp = warp / kGemvConsumerWarps;  // consumer group (consumers only)
+  const int gtid = tid % kGemvConsumers;      // thread index within the group
+  const int gwarp = warp % kGemvConsumerWarps;
+  if (warp < kGemvGroups * kGemvConsumerWarps) {
+    float act[MB][CPT][T::kEpc];
+    pdl_wait();  // A / y / z come from the previous kernel
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+      for (int j = 0; j < CPT; ++j) {
+        const int c = gtid + j * kGemvConsumers;
+        const bool live = m < mvalid && c < nchunks;
+        const int k0 = c * T::kEpc;
+        if (live && a.act == ACT_GATED) {
+          const float4* src = reinterpret_cast<const float4*>(a.y + (size_t)(m0 + m) * a.ldy + k0);
+#pragma unroll
+          for (int q = 0; q < T::kEpc / 4; ++q) {
+            const float4 v = __ldg(src + q);
+            act[m][j][4 * q] = v.x;
+            act[m][j][4 * q + 1] = v.y;
+            act[m][j][4 * q + 2] = v.z;
+            act[m][j][4 * q + 3] = v.w;
+          }
+        } else if (live) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.A + (size_t)(m0 + m) * a.lda + k0);
+#pragma unroll
+          for (int q = 0; q < T::kEpc / 8; ++q) {
+            const uint4 v = __ldg(src + q);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              act[m][j][q * 8 + 2 * e] = bf16lo(w4[e]);
+              act[m][j][q * 8 + 2 * e + 1] = bf16hi(w4[e]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < T::kEpc; ++e) act[m][j][e] = 0.0f;
+        }
+      }
+    if (a.act == ACT_RMSNORM) {
+      // input RMSNorm: sum of squares carried as an error-free fp32 pair and
+      // r evaluated once in double, so that the bf16 rounding of x * r * w
+      // does not depend on the summation order
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+#pragma unroll
+          for (int e = 0; e < T::kEpc; ++e) two_sum_acc(hi, lo, act[m][j][e] * act[m][j][e]);
+        two_sum_warp(hi, lo);
+        if (grp == 0 && lane == 0) {
+          tail->nss[0][m][gwarp] = hi;
+          tail->nss[1][m][gwarp] = lo;
+        }
+      }
+      named_bar(1, kGemvAllConsumers);
+      if (tid < MB) {
+        double tot = 0.0;
+        for (int w = 0; w < kGemvConsumerWarps; ++w) tot += (double)tail->nss[0][tid][w] + (double)tail->nss[1][tid][w];
+        tail->nrd[tid] = 1.0 / sqrt(tot / (double)a.K + (double)a.eps);
+      }
+      named_bar(1, kGemvAllConsumers);
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const double rd = tail->nrd[m];
+        const float rf = (float)rd;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const int c = gtid + j * kGemvConsumers;
+          if (m < mvalid && c < nchunks) {
+            const int k0 = c * T::kEpc;
+#pragma unroll
+            for (int e = 0; e < T::kEpc; ++e)
+              act[m][j][e] = bf16_to_f32(norm_round_bf16(act[m][j][e], bf16_to_f32(a.norm_w[k0 + e]), rf, rd));
+          }
+        }
+      }
+    } else if (a.act == ACT_GATED) {
+      // sums of squares per (row, group): chunks never straddle a group
+      const int group = a.group;
+      const int ngroups = a.K / group;
+      for (int i = tid; i < 4 * kMaxGroups; i += kGemvAllConsumers) (&tail->nsum[0][0])[i] = 0.0f;
+      named_bar(1, kGemvAllConsumers);
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const int c = gtid + j * kGemvConsumers;
+          float ss = 0.0f;
+#pragma unroll
+          for (int e = 0; e < T::kEpc; ++e) ss = fmaf(act[m][j][e], act[m][j][e], ss);
+          if (grp == 0) {  // both groups hold the same values; group 0 reduces
+            if (ngroups == 1) {
+              ss = warp_sum(ss);
+              if (lane == 0) atomicAdd(&tail->nsum[m][0], ss);
+            } else if (m < mvalid && c < nchunks) {
+              atomicAdd(&tail->nsum[m][(c * T::kEpc) / group], ss);
+            }
+          }
+        }
+      named_bar(1, kGemvAllConsumers);
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const int c = gtid + j * kGemvConsumers;
+          if (m < mvalid && c < nchunks) {
+            const int k0 = c * T::kEpc;
+            const float r = 1.0f / sqrtf(tail->nsum[m][k0 / group] / (float)group + a.eps);
+#pragma unroll
+            for (int e = 0; e < T::kEpc; ++e) {
+              float v = act[m][j][e] * r * bf16_to_f32(a.norm_w[k0 + e]);
+              v *= silu_f(bf16_to_f32(a.z[(size_t)(m0 + m) * a.ldz + k0 + e]));
+              act[m][j][e] = bf16_to_f32(f32_to_bf16(v));  // the gated norm's rounding point
+            }
+          }
+        }
+    }
+    if constexpr (FP8) {
+      // per-row power-of-two prescale into the f16 range
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        float mx = 0.0f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+#pragma unroll
+          for (int e = 0; e < T::kEpc; ++e) mx = fmaxf(mx, fabsf(act[m][j][e]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0 && grp == 0) atomicMax(&tail->amax[m], __float_as_uint(mx));
+      }
+      named_bar(1, kGemvAllConsumers);
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        const unsigned bits = tail->amax[m];
+        // amax in [2^e, 2^(e+1)) -> j = 14 - e; zero rows keep j = 0
+        const int e = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
+        const int jx = max(-120, min(120, 14 - e));
+        const float up = ldexpf(1.0f, jx);
+        if (tid == 0) tail->unscale[m] = ldexpf(1.0f, -jx);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+#pragma unroll
+          for (int e2 = 0; e2 < T::kEpc / 2; ++e2)
+            acth[m][j][e2] = pack_f16x2(act[m][j][2 * e2] * up, act[m][j][2 * e2 + 1] * up);
+      }
+    } else {
+      if (tid < 4) tail->unscale[tid] = 1.0f;
+#pragma unroll
+      for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+#pragma unroll
+          for (int e2 = 0; e2 < T::kEpc / 2; ++e2) acth[m][j][e2] = pack_bf16x2(act[m][j][2 * e2], act[m][j][2 * e2 + 1]);
+    }
+  }
+  if (warp == kGemvHelperWarp) {
+    pdl_wait();  // ring / pos / residual may be written by the previous kernel
+    // epilogue inputs of this CTA's rows
+    if (a.epi == EPI_INPROJ_CONV) {
+      uint16_t* cw = reinterpret_cast<uint16_t*>(epi_s);              // [rows_max][dconv+1]
+      uint16_t* rg = cw + (size_t)rows_max * (a.dconv + 1);            // [MB][L][rows_max]
+      int32_t* ps = reinterpret_cast<int32_t*>(
+          (reinterpret_cast<uintptr_t>(rg + (size_t)MB * L * rows_max) + 3) & ~uintptr_t(3));
+      if (lane < MB) ps[lane] = lane < mvalid ? a.pos[m0 + lane] : 0;
+      __syncwarp();
+      for (int r = lane; r < nrows; r += 32) {
+        const int n = row_begin + r;
+        if (n < a.xbc0 || n >= a.xbc0 + a.d_xbc) continue;
+        const int c = n - a.xbc0;
+        for (int j = 0; j < a.dconv; ++j) cw[r * (a.dconv + 1) + j] = a.conv_w[(size_t)c * a.dconv + j];
+        cw[r * (a.dconv + 1) + a.dconv] = a.conv_b ? a.conv_b[c] : (uint16_t)0;
+        for (int m = 0; m < mvalid; ++m) {
+          const int p = ps[m];
+          const uint16_t* ring = a.ring + (size_t)(m0 + m) * L * a.d_xbc;
+          for (int j = 0; j < L; ++j) rg[((size_t)m * L + j) * rows_max + r] = ring[(size_t)((p + j) % L) * a.d_xbc + c];
+        }
+      }
+    } else if (a.epi == EPI_RESID) {
+      uint16_t* rs = reinterpret_cast<uint16_t*>(epi_s);  // [MB][rows_max]
+      for (int i = lane; i < nrows * mvalid; i += 32) {
+        const int m = i / nrows, r = i % nrows;
+        rs[m * rows_max + r] = a.resid[(size_t)(m0 + m) * a.ldr + row_begin + r];
+      }
+    }
+  }
+  __syncthreads();  // scales staged; epilogue inputs staged
+
+  bool dead = false;
+  if (warp == kGemvProducerWarp) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      const uint64_t pol = a.evict_first ? policy_evict_first() : policy_evict_normal();
-      const uint8_t* wbase = static_cast<const uint8_t*>(a.W) + (size_t)row_begin * rowbytes;
-      for (int it = 0; it < niter; ++it) {
+      for (int it = stages; it < niter; ++it) {
         const int s = it % stages;
-        if (it >= stages && !mbar_wait(&tail->empty[s], ((it / stages) - 1) & 1)) return;  // status recorded
+        if (!mbar_wait(&tail->empty[s], ((it / stages) - 1) & 1)) break;  // status recorded
         const int rows = min(R, nrows - it * R);
         const uint32_t bytes = (uint32_t)(rows * rowbytes);
         mbar_arrive_expect_tx(&tail->full[s], bytes);
         bulk_g2s(smem + (size_t)s * stage_bytes, wbase + (size_t)it * R * rowbytes, bytes, &tail->full[s], pol);
       }
     }
-    return;
-  }
-
-  // ------------------------------------------------------------ consumers
-  // activations of my chunks, fp32 in registers
-  float act[MB][CPT][T::kEpc];
+  } else if (warp == kGemvHelperWarp) {
+    // ---------------------------------------------------------- helper
+    for (int it = 0; it < niter; ++it) {
+      const int slot = it % kGemvSlots;
+      if (!dead && !mbar_wait(&tail->red_full[slot], (it / kGemvSlots) & 1)) dead = true;
+      if (!dead && lane < V) {
+        float t = 0.0f;
 #pragma unroll
-  for (int m = 0; m < MB; ++m)
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      const int c = tid + j * kGemvConsumers;
-      if (m < mvalid && c < nchunks) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.A + (size_t)(m0 + m) * a.lda + (size_t)c * T::kEpc);
-#pragma unroll
-        for (int q = 0; q < T::kEpc / 8; ++q) {
-          const uint4 v = __ldg(src + q);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            act[m][j][q * 8 + 2 * e] = bf16lo(w4[e]);
-            act[m][j][q * 8 + 2 * e + 1] = bf16hi(w4[e]);
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < T::kEpc; ++e) act[m][j][e] = 0.0f;
+        for (int w = 0; w < kGemvConsumerWarps; ++w) t += tail->red[slot][w][lane];
+        tot[(it * R + lane / MB) * MB + (lane % MB)] = t;  // rows beyond nrows land in the padding
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->red_empty[slot]);
     }
+  } else {
+    // ---------------------------------------------------------- consumers
+    for (int it = grp; it < niter; it += kGemvGroups) {
+      const int s = it % stages;
+      const int row0 = row_begin + it * R;
+      const int rows = min(R, nrows - it * R);
+      if (!dead && !mbar_wait(&tail->full[s], (it / stages) & 1)) dead = true;
+      const uint8_t* st = smem + (size_t)s * stage_bytes;
 
-  // After a timed-out wait a warp stops touching memory but keeps taking part
-  // in the named barrier, so that no other warp waits on it forever.
-  bool dead = false;
-  for (int it = 0; it < niter; ++it) {
-    const int s = it % stages;
-    const int row0 = row_begin + it * R;
-    const int rows = dead ? 0 : min(R, nrows - it * R);
-    if (!dead && !mbar_wait(&tail->full[s], (it / stages) & 1)) dead = true;
-    const uint8_t* st = smem + (size_t)s * stage_bytes;
-
-    float v[V];
+      float v[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) v[i] = 0.0f;
-
+      for (int i = 0; i < V; ++i) v[i] = 0.0f;
+      if (!dead) {
+        // rows past `rows` in a partial last stage compute on stale shared
+        // memory; their sums are discarded (the butterfly keeps rows apart)
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      if (r < rows && !dead) {
-        const int n = row0 + r;
+        for (int r = 0; r < R; ++r) {
+          const int n = min(row0 + r, row_end - 1);
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const int c = tid + j * kGemvConsumers;
-          if (c < nchunks) {
-            const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)r * rowbytes + (size_t)c * 16);
-            const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
-            float p[MB];
+          for (int j = 0; j < CPT; ++j) {
+            const int c = gtid + j * kGemvConsumers;
+            if (c < nchunks) {
+              const uint4 wv = *reinterpret_cast<const uint4*>(st + (size_t)r * rowbytes + (size_t)c * 16);
+              const uint32_t w4[4] = {wv.x, wv.y, wv.z, wv.w};
+              float p0[MB], p1[MB];
 #pragma unroll
-            for (int m = 0; m < MB; ++m) p[m] = 0.0f;
-            if constexpr (FP8) {
+              for (int m = 0; m < MB; ++m) p0[m] = p1[m] = 0.0f;
+              if constexpr (FP8) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float w0, w1;
-                e4m3x2_to_f32((uint16_t)(w4[e >> 1] >> ((e & 1) * 16)), w0, w1);
+                for (int e = 0; e < 8; ++e) {
+                  const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(w4[e >> 1] >> ((e & 1) * 16)));
 #pragma unroll
-                for (int m = 0; m < MB; ++m) {
-                  p[m] = fmaf(w0, act[m][j][2 * e], p[m]);
-                  p[m] = fmaf(w1, act[m][j][2 * e + 1], p[m]);
+                  for (int m = 0; m < MB; ++m) fma2_f16(h2, acth[m][j][e], p0[m], p1[m]);
                 }
+                const float scv = sc[((n >> 7) - nb0) * kb + ((c * 16) >> 7)];
+#pragma unroll
+                for (int m = 0; m < MB; ++m) v[r * MB + m] = fmaf(p0[m] + p1[m], scv, v[r * MB + m]);
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+#pragma unroll
+                  for (int m = 0; m < MB; ++m) fma2_bf16(w4[e], acth[m][j][e], p0[m], p1[m]);
+#pragma unroll
+                for (int m = 0; m < MB; ++m) v[r * MB + m] += p0[m] + p1[m];
               }
-              const float sc = bf16_to_f32(__ldg(a.S + (size_t)(n >> 7) * kb + ((c * 16) >> 7)));
-#pragma unroll
-              for (int m = 0; m < MB; ++m) v[r * MB + m] = fmaf(p[m], sc, v[r * MB + m]);
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float w0 = bf16lo(w4[e]), w1 = bf16hi(w4[e]);
-#pragma unroll
-                for (int m = 0; m < MB; ++m) {
-                  p[m] = fmaf(w0, act[m][j][2 * e], p[m]);
-                  p[m] = fmaf(w1, act[m][j][2 * e + 1], p[m]);
-                }
-              }
-#pragma unroll
-              for (int m = 0; m < MB; ++m) v[r * MB + m] += p[m];
             }
           }
         }
       }
+      // stage consumed: hand it back to the producer before reducing
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->empty[s]);
+      Butterfly<V, 16>::run(v, lane);
+      const int slot = it % kGemvSlots;
+      if (it >= kGemvSlots && !dead && !mbar_wait(&tail->red_empty[slot], ((it / kGemvSlots) - 1) & 1)) dead = true;
+      if ((lane & ((1 << (5 - LOGV)) - 1)) == 0) tail->red[slot][gwarp][lane >> (5 - LOGV)] = v[0];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->red_full[slot]);
     }
-    // stage consumed: hand it back to the producer before reducing
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&tail->empty[s]);
+  }
+  __syncthreads();  // all row totals are in shared memory
+  if (dead) return;
 
-    // transposing butterfly: after it, lane l holds the warp total of value
-    // index l >> (5 - LOGV)
-    butterfly<V, 16>(v, lane);
-    const int buf = it & 1;
-    if ((lane & ((1 << (5 - LOGV)) - 1)) == 0) tail->red[buf][warp][lane >> (5 - LOGV)] = v[0];
-    named_bar(1, kGemvConsumers);
-    if (tid < V) {
-      float tot = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kGemvConsumerWarps; ++w) tot += tail->red[buf][w][tid];
-      const int r = tid / MB, m = tid % MB;
-      if (!dead && r < rows && m < mvalid) gemv_epilogue(a, row0 + r, m0 + m, tot);
+  // ------------------------------------------------ epilogue (all threads)
+  const uint16_t* cw = reinterpret_cast<const uint16_t*>(epi_s);
+  const uint16_t* rg = cw + (size_t)rows_max * (a.dconv + 1);
+  const int32_t* ps = reinterpret_cast<const int32_t*>(
+      (reinterpret_cast<uintptr_t>(rg + (size_t)MB * L * rows_max) + 3) & ~uintptr_t(3));
+  for (int i = tid; i < nrows * mvalid; i += kGemvThreads) {
+    const int r = i / mvalid, m = i % mvalid;
+    const int n = row_begin + r;
+    const float acc = tot[r * MB + m] * tail->unscale[m];
+    uint16_t* o = a.out + (size_t)(m0 + m) * a.ldo + n;
+    if (a.epi == EPI_RESID) {
+      const float res = bf16_to_f32(reinterpret_cast<const uint16_t*>(epi_s)[m * rows_max + r]);
+      *o = f32_to_bf16(res + acc);
+    } else if (a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc) {
+      // conv1d update with bias + SiLU; this thread alone owns (sequence m,
+      // channel c) in this call, and the ring taps were staged before any write
+      const uint16_t vb = f32_to_bf16(acc);  // rounding point of the in_proj output
+      const int c = n - a.xbc0;
+      const uint16_t* w = cw + r * (a.dconv + 1);
+      float s = bf16_to_f32(w[a.dconv]);
+      for (int j = 0; j < L; ++j) s += bf16_to_f32(w[j]) * bf16_to_f32(rg[((size_t)m * L + j) * rows_max + r]);
+      s += bf16_to_f32(w[L]) * bf16_to_f32(vb);
+      *o = f32_to_bf16(silu_f(s));
+      a.ring[(size_t)(m0 + m) * L * a.d_xbc + (size_t)(ps[m] % L) * a.d_xbc + c] = vb;
+    } else {
+      *o = f32_to_bf16(acc);
     }
   }
 }
@@ -273,22 +543,26 @@ static cudaError_t launch_one(const GemvArgs& a, int m0, cudaStream_t s) {
   using T = WTraits<FP8>;
   const int rowbytes = a.K * T::kEsize;
   const int stage_bytes = R * rowbytes;
-  int stages = kGemvStageBudget / stage_bytes;
-  if (stages > kGemvMaxStages) stages = kGemvMaxStages;
-  if (stages < 1) stages = 1;
-  const int smem = stages * stage_bytes + (int)sizeof(GemvSmemTail);
-  auto kern = gemv_kernel<FP8, MB, CPT, R>;
-  cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
-  if (e != cudaSuccess) return e;
   int grid = num_sms();
   const int maxg = (a.N + R - 1) / R;
   if (grid > maxg) grid = maxg;
+  const int rows_max = (a.N + grid - 1) / grid + R;  // stage padding of the last range
+  const int kb = (a.K + 127) / 128;
+  int stages = kGemvStageBudget / stage_bytes;
+  if (stages > kGemvMaxStages) stages = kGemvMaxStages;
+  if (stages < 1) stages = 1;
+  GemvLayout lay = gemv_layout(stages, stage_bytes, rows_max, MB, kb, a.epi, a.dconv);
+  while (lay.total > 227 * 1024 && stages > 1) lay = gemv_layout(--stages, stage_bytes, rows_max, MB, kb, a.epi, a.dconv);
+  if (lay.total > 227 * 1024) return cudaErrorInvalidConfiguration;
+  auto kern = gemv_kernel<FP8, MB, CPT, R>;
+  cudaError_t e = set_smem_once((const void*)kern, lay.total, done_mask);
+  if (e != cudaSuccess) return e;
   // EPI_STORE / EPI_RESID / EPI_INPROJ_CONV -> trace ids store / resid / conv
   const int id = (FP8 ? K_GEMV_FP8 : K_GEMV_BF16) + (a.epi == EPI_INPROJ_CONV ? 1 : (a.epi == EPI_RESID ? 2 : 0));
   trace_pre(id, s);
-  kern<<<grid, kGemvThreads, smem, s>>>(a, m0, stages);
+  e = launch_k(kern, dim3(grid), dim3(kGemvThreads), lay.total, s, a.pdl != 0, a, m0, stages, rows_max);
   trace_post(id, s);
-  return cudaGetLastError();
+  return e;
 }
 
 // Launches one pass over the weights for batch rows [m0, m0 + rows) and
@@ -296,6 +570,7 @@ static cudaError_t launch_one(const GemvArgs& a, int m0, cudaStream_t s) {
 // cache: MB * CPT <= 4 (CPT = 16-byte chunks per consumer thread per row).
 template <bool FP8>
 static int launch_group(const GemvArgs& a, int m0, cudaStream_t s, cudaError_t* err) {
+  // stages of ~32 KB: R = 32 KB / row bytes rows per stage
   const int rowbytes = a.K * WTraits<FP8>::kEsize;
   const int cpt = (rowbytes + 4095) / 4096;
   const int rem = a.M - m0;
@@ -306,12 +581,12 @@ static int launch_group(const GemvArgs& a, int m0, cudaStream_t s, cudaError_t* 
     return 1;
   }
   if (cpt == 2) {
-    if (rem >= 2) { *err = launch_one<FP8, 2, 2, 8>(a, m0, s); return 2; }
-    *err = launch_one<FP8, 1, 2, 8>(a, m0, s);
+    if (rem >= 2) { *err = launch_one<FP8, 2, 2, 4>(a, m0, s); return 2; }
+    *err = launch_one<FP8, 1, 2, 4>(a, m0, s);
     return 1;
   }
-  if (cpt <= 4) { *err = launch_one<FP8, 1, 4, 4>(a, m0, s); return 1; }
-  if constexpr (!FP8) { *err = launch_one<FP8, 1, 8, 2>(a, m0, s); return 1; }
+  if (cpt <= 4) { *err = launch_one<FP8, 1, 4, 2>(a, m0, s); return 1; }
+  if constexpr (!FP8) { *err = launch_one<FP8, 1, 8, 1>(a, m0, s); return 1; }
   *err = cudaErrorInvalidValue;
   return 1;
 }
@@ -319,10 +594,19 @@ static int launch_group(const GemvArgs& a, int m0, cudaStream_t s, cudaError_t* 
 cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s) {
   for (int m0 = 0; m0 < a.M;) {
     cudaError_t e = cudaSuccess;
-    m0 += fp8 ? launch_group<true>(a, m0, s, &e) : launch_group<false>(a, m0, s, &e);
+    GemvArgs b = a;
+    if (m0 > 0) b.pdl = 0;  // later passes follow a GEMV of this call
+    m0 += fp8 ? launch_group<true>(b, m0, s, &e) : launch_group<false>(b, m0, s, &e);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Largest batch row count one GEMV pass covers for a K-wide row (the fused
+// norm prologue needs the whole batch in one pass).
+int gemv_rows_per_pass(int K, bool fp8) {
+  const int cpt = (K * (fp8 ? 1 : 2) + 4095) / 4096;
+  return cpt == 1 ? 4 : (cpt == 2 ? 2 : 1);
 }
 
 // ------------------------------------------------------------------ RMSNorm
@@ -332,26 +616,36 @@ cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s) {
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int ldx,
                                                       const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
                                                       int ldo, int K, float eps) {
+  // sum of squares as an error-free fp32 pair, r once in double (see
+  // norm_round_bf16)
   const uint16_t* xr = x + (size_t)blockIdx.x * ldx;
-  __shared__ float red[8];
-  float ss = 0.0f;
+  __shared__ float red[2][8];
+  __shared__ double rds;
+  float hi = 0.0f, lo = 0.0f;
   for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float a0 = bf16lo(w4[e]), a1 = bf16hi(w4[e]);
-      ss = fmaf(a0, a0, ss);
-      ss = fmaf(a1, a1, ss);
+      two_sum_acc(hi, lo, a0 * a0);
+      two_sum_acc(hi, lo, a1 * a1);
     }
   }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  two_sum_warp(hi, lo);
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = hi;
+    red[1][threadIdx.x >> 5] = lo;
+  }
   __syncthreads();
-  float tot = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) tot += red[i];
-  const float r = 1.0f / sqrtf(tot / (float)K + eps);
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    for (int i = 0; i < 8; ++i) tot += (double)red[0][i] + (double)red[1][i];
+    rds = 1.0 / sqrt(tot / (double)K + (double)eps);
+  }
+  __syncthreads();
+  const double rd = rds;
+  const float rf = (float)rd;
   uint16_t* o = out + (size_t)blockIdx.x * ldo;
   for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
@@ -360,7 +654,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict
     uint32_t o4[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      o4[e] = pack_bf16x2(bf16lo(x4[e]) * r * bf16lo(g4[e]), bf16hi(x4[e]) * r * bf16hi(g4[e]));
+      o4[e] = (uint32_t)norm_round_bf16(bf16lo(x4[e]), bf16lo(g4[e]), rf, rd) |
+              ((uint32_t)norm_round_bf16(bf16hi(x4[e]), bf16hi(g4[e]), rf, rd) << 16);
     *reinterpret_cast<uint4*>(o + k) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
   }
 }

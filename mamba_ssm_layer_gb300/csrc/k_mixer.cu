@@ -132,9 +132,14 @@ __device__ __forceinline__ void head_scalars(const uint16_t* dt_row, const float
   dA = expf(d * -expf(A_log[h]));
 }
 
-template <int LPR>
-__global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int psplit, int rows_per_cta) {
+template <int LPR, int ROWS>
+__global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int psplit) {
+  // A CTA covers 8 * RPW * ROWS consecutive rows p of one head; each thread
+  // ROWS rows, whose state loads are all issued before any is used.
   constexpr int RPW = 32 / LPR;
+  constexpr int CTA_ROWS = 8 * RPW * ROWS;
+  pdl_trigger();
+  pdl_wait();  // everything below may depend on the previous kernel
   const int b = blockIdx.y;
   const int h = blockIdx.x / psplit;
   const int pc = blockIdx.x % psplit;
@@ -147,45 +152,71 @@ __global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int pspl
   const float Dh = a.D[h];
   const float4 Bv = ld4bf(a.Bm + (size_t)b * a.ld_in + (size_t)g * a.N + n4);
   const float4 Cv = ld4bf(a.Cm + (size_t)b * a.ld_in + (size_t)g * a.N + n4);
-  const int p_begin = pc * rows_per_cta;
-  const int p_end = min(a.P, p_begin + rows_per_cta);
   float* hb = a.h + ((size_t)b * a.H + h) * a.P * a.N;
-  for (int p = p_begin + warp * RPW + lane / LPR; p < p_end; p += 8 * RPW) {
-    const float xv = bf16_to_f32(xr[(size_t)h * a.P + p]);
-    float4* hp = reinterpret_cast<float4*>(hb + (size_t)p * a.N + n4);
-    float4 hv = *hp;
-    const float dtx = dt * xv;
-    hv.x = fmaf(dA, hv.x, dtx * Bv.x);
-    hv.y = fmaf(dA, hv.y, dtx * Bv.y);
-    hv.z = fmaf(dA, hv.z, dtx * Bv.z);
-    hv.w = fmaf(dA, hv.w, dtx * Bv.w);
-    *hp = hv;
-    float yp = Cv.x * hv.x + Cv.y * hv.y + Cv.z * hv.z + Cv.w * hv.w;
+  const int p0 = pc * CTA_ROWS + warp * RPW + lane / LPR;
+  float4 hv[ROWS];
+  float xv[ROWS];
+#pragma unroll
+  for (int i = 0; i < ROWS; ++i) {
+    const int p = p0 + i * 8 * RPW;
+    if (p < a.P) {
+      hv[i] = *reinterpret_cast<const float4*>(hb + (size_t)p * a.N + n4);
+      xv[i] = bf16_to_f32(xr[(size_t)h * a.P + p]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < ROWS; ++i) {
+    const int p = p0 + i * 8 * RPW;
+    const bool live = p < a.P;  // uniform across the lanes of one row
+    if (live) {
+      const float dtx = dt * xv[i];
+      hv[i].x = fmaf(dA, hv[i].x, dtx * Bv.x);
+      hv[i].y = fmaf(dA, hv[i].y, dtx * Bv.y);
+      hv[i].z = fmaf(dA, hv[i].z, dtx * Bv.z);
+      hv[i].w = fmaf(dA, hv[i].w, dtx * Bv.w);
+      *reinterpret_cast<float4*>(hb + (size_t)p * a.N + n4) = hv[i];
+    }
+    float yp = live ? Cv.x * hv[i].x + Cv.y * hv[i].y + Cv.z * hv[i].z + Cv.w * hv[i].w : 0.0f;
 #pragma unroll
     for (int o = LPR / 2; o > 0; o >>= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
-    if ((lane % LPR) == 0) a.y[(size_t)b * a.ldy + (size_t)h * a.P + p] = yp + Dh * xv;
+    if (live && (lane % LPR) == 0) a.y[(size_t)b * a.ldy + (size_t)h * a.P + p] = yp + Dh * xv[i];
   }
   if (a.pos_inc && blockIdx.x == 0 && threadIdx.x == 0) a.pos_inc[b] += 1;
 }
 
-cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s) {
-  const int lpr = a.N / 4;
-  const int rows_pass = 8 * (32 / lpr);
-  // split heads along p until there are >= 2 CTAs per SM (p rows are independent)
-  int psplit = 1;
-  const long long target = 2LL * num_sms();
-  while ((long long)a.B * a.H * psplit < target && a.P / (psplit * 2) >= rows_pass) psplit *= 2;
-  const int rows_per_cta = (a.P + psplit - 1) / psplit;
+template <int LPR>
+static cudaError_t launch_ssm_lpr(const SsmArgs& a, cudaStream_t s, bool pdl) {
+  // rows per thread: 1 when the batch is small (most CTAs, most loads in
+  // flight), up to 8 when B*H alone fills the GPU
+  constexpr int RPW = 32 / LPR;
+  const long long heads = (long long)a.B * a.H;
+  const int max_rows = (a.P + 8 * RPW - 1) / (8 * RPW);  // rows per thread with one CTA per head
+  int rows = 1;
+  while (rows < 8 && rows < max_rows && heads * ((a.P + 8 * RPW * rows * 2 - 1) / (8 * RPW * rows * 2)) >= 8LL * num_sms())
+    rows *= 2;
+  const int cta_rows = 8 * RPW * rows;
+  const int psplit = (a.P + cta_rows - 1) / cta_rows;
   dim3 grid(a.H * psplit, a.B);
+  switch (rows) {
+    case 1: return launch_k(ssm_step_kernel<LPR, 1>, grid, dim3(256), 0, s, pdl, a, psplit);
+    case 2: return launch_k(ssm_step_kernel<LPR, 2>, grid, dim3(256), 0, s, pdl, a, psplit);
+    case 4: return launch_k(ssm_step_kernel<LPR, 4>, grid, dim3(256), 0, s, pdl, a, psplit);
+    default: return launch_k(ssm_step_kernel<LPR, 8>, grid, dim3(256), 0, s, pdl, a, psplit);
+  }
+}
+
+cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s) {
+  const bool pdl = a.pdl != 0;
+  cudaError_t e;
   trace_pre(K_SSM_STEP, s);
-  switch (lpr) {
-    case 4: ssm_step_kernel<4><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
-    case 8: ssm_step_kernel<8><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
-    case 16: ssm_step_kernel<16><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
-    default: ssm_step_kernel<32><<<grid, 256, 0, s>>>(a, psplit, rows_per_cta); break;
+  switch (a.N / 4) {
+    case 4: e = launch_ssm_lpr<4>(a, s, pdl); break;
+    case 8: e = launch_ssm_lpr<8>(a, s, pdl); break;
+    case 16: e = launch_ssm_lpr<16>(a, s, pdl); break;
+    default: e = launch_ssm_lpr<32>(a, s, pdl); break;
   }
   trace_post(K_SSM_STEP, s);
-  return cudaGetLastError();
+  return e;
 }
 
 // ------------------------------------------------------------------ sequential scan

@@ -239,9 +239,15 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
 
   cudaError_t e;
-  // 1. RMSNorm
-  if ((e = launch_rmsnorm(hidden, d.hidden, L->norm_w, xn, d.hidden, B, d.hidden, d.eps_in, stream))) return launch_status(e);
-  // 2+3. in_proj with the conv1d update (bias, SiLU) fused into its epilogue
+  const bool in_fp8 = L->in_proj.fmt == M2_W_FP8_BLOCK128;
+  const bool out_fp8 = L->out_proj.fmt == M2_W_FP8_BLOCK128;
+  // The norms fuse into the GEMV prologues when one weight pass covers the
+  // whole batch; the three kernels of the decode chain are launched as
+  // programmatic dependents so each streams its weights while its
+  // predecessor drains.
+  const bool fuse_in = B <= gemv_rows_per_pass(d.hidden, in_fp8);
+  const bool fuse_out = B <= gemv_rows_per_pass(r.d_inner, out_fp8) && r.d_inner / d.gnorm_group <= 64;
+  // 1+2+3. RMSNorm, in_proj, conv1d update (bias, SiLU) in its epilogue
   GemvArgs ex;
   memset(&ex, 0, sizeof(ex));
   ex.ring = conv_state;
@@ -251,10 +257,22 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   ex.xbc0 = r.d_inner;
   ex.d_xbc = r.d_xbc;
   ex.dconv = d.d_conv;
-  if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex)))
-    return launch_status(e);
+  if (fuse_in) {
+    ex.act = ACT_RMSNORM;
+    ex.norm_w = L->norm_w;
+    ex.eps = d.eps_in;
+    ex.pdl = 1;
+    if ((e = proj(L->in_proj, hidden, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex)))
+      return launch_status(e);
+  } else {
+    if ((e = launch_rmsnorm(hidden, d.hidden, L->norm_w, xn, d.hidden, B, d.hidden, d.eps_in, stream)))
+      return launch_status(e);
+    if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex)))
+      return launch_status(e);
+  }
   // 4+5. split and SSM step (advances conv_pos)
   SsmArgs sa;
+  memset(&sa, 0, sizeof(sa));
   sa.h = ssm_state;
   sa.x = zxu + r.d_inner;
   sa.Bm = zxu + 2 * r.d_inner;
@@ -272,14 +290,30 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   sa.N = d.d_state;
   sa.G = d.n_groups;
   sa.pos_inc = conv_pos;
+  sa.pdl = 1;
   if ((e = launch_ssm_step(sa, stream))) return launch_status(e);
-  // 6. gated RMSNorm
-  if ((e = launch_gated_norm(y, r.d_inner, zxu, r.ldz, L->gnorm_w, g, r.d_inner, B, r.d_inner, d.gnorm_group,
-                             d.eps_gated, stream)))
-    return launch_status(e);
-  // 7+8. out_proj with the residual add fused into its epilogue (in place)
-  if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream)))
-    return launch_status(e);
+  // 6+7+8. gated RMSNorm, out_proj, residual add (in place on hidden)
+  GemvArgs eo;
+  memset(&eo, 0, sizeof(eo));
+  if (fuse_out) {
+    eo.act = ACT_GATED;
+    eo.norm_w = L->gnorm_w;
+    eo.eps = d.eps_gated;
+    eo.y = y;
+    eo.ldy = r.d_inner;
+    eo.z = zxu;
+    eo.ldz = r.ldz;
+    eo.group = d.gnorm_group;
+    eo.pdl = 1;
+    if ((e = proj(L->out_proj, nullptr, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, &eo)))
+      return launch_status(e);
+  } else {
+    if ((e = launch_gated_norm(y, r.d_inner, zxu, r.ldz, L->gnorm_w, g, r.d_inner, B, r.d_inner, d.gnorm_group,
+                               d.eps_gated, stream)))
+      return launch_status(e);
+    if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream)))
+      return launch_status(e);
+  }
   return M2_OK;
 }
 
@@ -311,6 +345,7 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
                                r.d_xbc, d.d_conv, stream)))
     return launch_status(e);
   ScanArgs sa;
+  memset(&sa, 0, sizeof(sa));
   sa.h = ssm_state;
   sa.x = u;
   sa.Bm = u + r.d_inner;
@@ -371,6 +406,7 @@ int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint1
   if (ld_in % 4 || ld_in < H * P) return M2_ERR_ARG;
   if (!al16(h) || !al8(Bm) || !al8(Cm)) return M2_ERR_ALIGN;
   SsmArgs sa;
+  memset(&sa, 0, sizeof(sa));
   sa.h = h;
   sa.x = x;
   sa.Bm = Bm;

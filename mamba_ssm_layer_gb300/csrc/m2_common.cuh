@@ -40,6 +40,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// Error-free accumulation in two fp32 words (Knuth's two-sum): hi + lo holds
+// the running sum to ~2^-48 relative, independent of the summation order to
+// that accuracy.  Used for the RMSNorm sums of squares (x^2 of a bf16 x is
+// exact in fp32), so that r = 1/sqrt(mean + eps) matches a double evaluation.
+__device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float p) {
+  const float s = hi + p;
+  const float z = s - hi;
+  lo += (hi - (s - z)) + (p - z);
+  hi = s;
+}
+__device__ __forceinline__ void two_sum_warp(float& hi, float& lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float olo = __shfl_xor_sync(0xffffffffu, lo, o);
+    two_sum_acc(hi, lo, ohi);
+    lo += olo;
+  }
+}
+
+// Correct rounding of a double to bf16: round to odd at fp32 precision, then
+// to nearest even at bf16 precision (24 >= 8 + 2 bits, so the result equals a
+// single round-to-nearest-even of v).
+static __device__ __noinline__ uint16_t f64_to_bf16_rn(double v) {
+  float f = __double2float_rz(v);
+  if ((double)f != v) f = __uint_as_float(__float_as_uint(f) | 1u);
+  return f32_to_bf16(f);
+}
+
+// bf16(x * r * w) rounded as the exact product would round: the fp32 product
+// (<= 1.5 fp32 ulps from exact) decides unless it lies within 32 fp32 ulps of
+// a bf16 rounding tie; then the product in double (r given in double) decides.
+// This makes the RMSNorm's rounding point independent of summation order.
+static __device__ __noinline__ uint16_t norm_round_bf16_slow(float x, float w, double rd) {
+  return f64_to_bf16_rn((double)x * rd * (double)w);
+}
+__device__ __forceinline__ uint16_t norm_round_bf16(float x, float w, float rf, double rd) {
+  const float v = x * rf * w;
+  const int low = (int)(__float_as_uint(v) & 0xFFFFu);
+  if (abs(low - 0x8000) <= 32) return norm_round_bf16_slow(x, w, rd);  // rare; kept out of line
+  return f32_to_bf16(v);
+}
+
 // ------------------------------------------------------------------ E4M3
 
 // Two E4M3 bytes -> two fp32, exactly: the hardware E4M3 -> f16 conversion is
@@ -134,6 +177,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
+
+// Programmatic dependent launch: wait until the previous grid in the stream
+// has completed and its writes are visible / let the next grid start early.
+// Both are no-ops for a kernel launched without the PDL attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Named barrier among `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar(int id, int nthreads) {

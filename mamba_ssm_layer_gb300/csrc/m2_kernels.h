@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace m2 {
 
 // Kernel ids for launch counting and tracing (names in m2_abi.cu).
@@ -71,11 +73,46 @@ struct GemvArgs {
   const uint16_t* conv_b;
   int32_t xbc0, d_xbc, dconv;
   int32_t evict_first;  // stream weights with the L2 evict-first policy
+  // Activation prologue (fuses the norm that produces A into the GEMV):
+  int32_t act;          // GemvAct
+  const uint16_t* norm_w;  // ACT_RMSNORM: RMSNorm weight [K]; ACT_GATED: gated-norm weight [K]
+  float eps;
+  const float* y;       // ACT_GATED: y [M][ldy] fp32
+  int32_t ldy;
+  const uint16_t* z;    // ACT_GATED: z [M][ldz] bf16
+  int32_t ldz;
+  int32_t group;        // ACT_GATED: norm span (divides K, K/group <= 64)
+  int32_t pdl;          // launch as a programmatic dependent of the previous kernel
+};
+
+enum GemvAct : int32_t {
+  ACT_PLAIN = 0,    // A is the bf16 activation
+  ACT_RMSNORM = 1,  // activation = bf16(A * rsqrt(mean(A^2)+eps) * norm_w)       (A = hidden)
+  ACT_GATED = 2     // activation = bf16(y * rsqrt(mean_group(y^2)+eps) * norm_w * silu(z))
 };
 
 // CUDA-core GEMV (fp32 accumulation) with bulk-copy weight streaming; any M
 // (processed in groups of up to 4 rows, re-streaming the weights per group).
 cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s);
+
+// Launch helper: plain launch, or with programmatic stream serialisation (the
+// kernel may start while the previous kernel in the stream is still running;
+// it must execute griddepcontrol.wait before touching that kernel's outputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
+}
 
 // ------------------------------------------------------------------ mixer ops
 
@@ -102,8 +139,12 @@ struct SsmArgs {
   int32_t ldy;
   int32_t B, H, P, N, G;
   int32_t* pos_inc;    // if non-null: pos_inc[b] += 1 (decode fusion)
+  int32_t pdl;         // launch as a programmatic dependent of the previous kernel
 };
 cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s);
+
+// Largest batch row count one CUDA-core GEMV pass covers for a K-wide row.
+int gemv_rows_per_pass(int K, bool fp8);
 
 cudaError_t launch_gated_norm(const float* y, int32_t ldy, const uint16_t* z, int32_t ldz, const uint16_t* w,
                               uint16_t* out, int32_t ldo, int32_t M, int32_t d, int32_t group, float eps,

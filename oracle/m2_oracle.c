@@ -169,6 +169,23 @@ void or_bf16_gemv(const uint16_t* A, int M, const uint16_t* W, int N, int K, dou
   }
 }
 
+/* Sum of |terms| of the same products (the scale of the summation error of
+ * any floating-point evaluation of the dot product); used only by tests that
+ * judge rounding decisions. */
+static void proj_abs(int fmt, const void* w, const uint16_t* s, const uint16_t* a, int N, int K, double* out) {
+  int kb = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int k = 0; k < K; ++k) {
+      double wv = fmt == 1 ? e4m3(((const uint8_t*)w)[(size_t)n * K + k]) * bf(s[(size_t)(n / 128) * kb + k / 128])
+                           : bf(((const uint16_t*)w)[(size_t)n * K + k]);
+      acc += fabs(bf(a[k]) * wv);
+    }
+    out[n] = acc;
+  }
+}
+
 /* ---------------------------------------------------------------- step 3 */
 
 /* One-token causal depthwise conv update with learned bias and fused SiLU
@@ -176,21 +193,33 @@ void or_bf16_gemv(const uint16_t* A, int M, const uint16_t* W, int N, int K, dou
  * *pos is the number of tokens seen so far (not advanced here).  The current
  * token x (bf16, R3) is used as tap d_conv-1 and then stored into slot
  * pos mod (d_conv-1).  Output rounded to bf16 (R4). */
-void or_conv1d_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
-                      const uint16_t* b, int C, int dconv, int silu, uint16_t* out) {
+static void conv1d_update_exact(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
+                                const uint16_t* b, int C, int dconv, int silu, uint16_t* out, double* exact,
+                                double* exact_abs) {
   int L = dconv - 1;
   int p = *pos;
   for (int c = 0; c < C; ++c) {
     double acc = b ? bf(b[c]) : 0.0;
+    double aacc = fabs(acc);
     for (int j = 0; j < L; ++j) {
       int slot = (p + j) % L; /* oldest first */
       acc += bf(w[(size_t)c * dconv + j]) * bf(ring[(size_t)slot * C + c]);
+      aacc += fabs(bf(w[(size_t)c * dconv + j]) * bf(ring[(size_t)slot * C + c]));
     }
     acc += bf(w[(size_t)c * dconv + L]) * bf(x[c]);
-    out[c] = or_f64_to_bf16(silu ? or_silu(acc) : acc);
+    aacc += fabs(bf(w[(size_t)c * dconv + L]) * bf(x[c]));
+    double v = silu ? or_silu(acc) : acc;
+    if (exact) exact[c] = v;
+    if (exact_abs) exact_abs[c] = aacc;
+    out[c] = or_f64_to_bf16(v);
   }
   int wslot = p % L;
   for (int c = 0; c < C; ++c) ring[(size_t)wslot * C + c] = x[c];
+}
+
+void or_conv1d_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
+                      const uint16_t* b, int C, int dconv, int silu, uint16_t* out) {
+  conv1d_update_exact(ring, pos, x, w, b, C, dconv, silu, out, NULL, NULL);
 }
 
 /* ---------------------------------------------------------------- step 5 */
@@ -270,8 +299,12 @@ static void proj(int fmt, const void* w, const uint16_t* s, const uint16_t* a, i
 /* One token of one sequence through the whole layer, steps 1..8 in the order
  * of the [SRC] module header.  hidden [hidden] bf16 is modified in place
  * ([TRAIT] decode).  hs [H][P][N] double, ring [(dconv-1)][d_xbc] bf16 and
- * *pos are the sequence's state and are advanced by one token. */
-long or_layer_token(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* ring, int32_t* pos) {
+ * *pos are the sequence's state and are advanced by one token.  If tr_zx /
+ * tr_u are non-NULL they receive the unrounded in_proj outputs [n_in] and conv
+ * outputs [d_xbc] (the values rounded at R3 and R4), for tests that inspect
+ * rounding decisions. */
+long or_layer_token_traced(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* ring, int32_t* pos,
+                           double* tr_zx, double* tr_u, double* tr_zx_abs, double* tr_u_abs) {
   int d_inner = L->H * L->P;
   int d_xbc = d_inner + 2 * L->G * L->N;
   int n_in = d_inner + d_xbc + L->H;
@@ -289,11 +322,13 @@ long or_layer_token(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* r
   /* 2. in_proj -> [z, xBC, dt] (R3) */
   proj(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, zx);
   for (int i = 0; i < n_in; ++i) zxb[i] = or_f64_to_bf16(zx[i]);
+  if (tr_zx) memcpy(tr_zx, zx, sizeof(double) * n_in);
+  if (tr_zx_abs) proj_abs(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, tr_zx_abs);
   const uint16_t* z = zxb;
   const uint16_t* xbc = zxb + d_inner;
   const uint16_t* dt = zxb + d_inner + d_xbc;
   /* 3. conv1d update on xBC with bias and SiLU (R4) */
-  or_conv1d_update(ring, pos, xbc, L->conv_w, L->conv_b, d_xbc, L->dconv, 1, u);
+  conv1d_update_exact(ring, pos, xbc, L->conv_w, L->conv_b, d_xbc, L->dconv, 1, u, tr_u, tr_u_abs);
   *pos += 1;
   /* 4. split into x, B, C */
   const uint16_t* xs = u;
@@ -311,6 +346,10 @@ long or_layer_token(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* r
   return hits;
 }
 
+long or_layer_token(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* ring, int32_t* pos) {
+  return or_layer_token_traced(L, hidden, hs, ring, pos, NULL, NULL, NULL, NULL);
+}
+
 /* Prefill of T tokens of one sequence, by its definition: T sequential
  * single-token decode steps ([TRAIT] prefill default).  hidden is [T][hidden]. */
 long or_layer_prefill(const or_layer* L, uint16_t* hidden, int T, double* hs, uint16_t* ring,
@@ -319,4 +358,24 @@ long or_layer_prefill(const or_layer* L, uint16_t* hidden, int T, double* hs, ui
   for (int t = 0; t < T; ++t)
     hits += or_layer_token(L, hidden + (size_t)t * L->hidden, hs, ring, pos);
   return hits;
+}
+
+/* The same, recording per token the unrounded in_proj and conv outputs
+ * (tr_zx [T][n_in], tr_u [T][d_xbc]) and their sums of |terms|. */
+long or_layer_prefill_traced(const or_layer* L, uint16_t* hidden, int T, double* hs, uint16_t* ring,
+                             int32_t* pos, double* tr_zx, double* tr_u, double* tr_zx_abs, double* tr_u_abs) {
+  int d_inner = L->H * L->P;
+  int d_xbc = d_inner + 2 * L->G * L->N;
+  int n_in = d_inner + d_xbc + L->H;
+  long hits = 0;
+  for (int t = 0; t < T; ++t)
+    hits += or_layer_token_traced(L, hidden + (size_t)t * L->hidden, hs, ring, pos, tr_zx + (size_t)t * n_in,
+                                  tr_u + (size_t)t * d_xbc, tr_zx_abs + (size_t)t * n_in,
+                                  tr_u_abs + (size_t)t * d_xbc);
+  return hits;
+}
+
+/* Vector form of or_f64_to_bf16. */
+void or_f64_to_bf16_array(const double* v, uint16_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = or_f64_to_bf16(v[i]);
 }

@@ -61,6 +61,9 @@ def lib():
             l.or_gated_rmsnorm.argtypes = [P, P, P, C.c_int, C.c_int, d, P]
             l.or_layer_token.argtypes = [P, P, P, P, P]; l.or_layer_token.restype = C.c_long
             l.or_layer_prefill.argtypes = [P, P, C.c_int, P, P, P]; l.or_layer_prefill.restype = C.c_long
+            l.or_layer_prefill_traced.argtypes = [P, P, C.c_int, P, P, P, P, P, P, P]
+            l.or_layer_prefill_traced.restype = C.c_long
+            l.or_f64_to_bf16_array.argtypes = [P, P, C.c_long]
             l.or_init()
             _lib = l
     return _lib
@@ -104,9 +107,10 @@ def bf16_array_to_f64(h: np.ndarray) -> np.ndarray:
 
 
 def f64_array_to_bf16(v: np.ndarray) -> np.ndarray:
-    f = lib().or_f64_to_bf16
-    v = np.asarray(v, dtype=np.float64)
-    return np.array([f(float(x)) for x in v.ravel()], dtype=np.uint16).reshape(v.shape)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().or_f64_to_bf16_array(_p(v), _p(out), v.size)
+    return out
 
 
 # ------------------------------------------------------------------ steps
@@ -227,3 +231,21 @@ class OracleLayer:
         assert h.dtype == np.float64 and ring.dtype == np.uint16 and pos.dtype == np.int32
         T = hidden.shape[0]
         return lib().or_layer_prefill(C.byref(self._s), _p(hidden), T, _p(h), _p(ring), _p(pos))
+
+    def run_traced(self, hidden, h, ring, pos):
+        """As run(), also returning the unrounded in_proj outputs [T][n_in] and conv
+        outputs [T][d_xbc] (the values rounded to bf16 at R3 and R4), and the
+        sums of |terms| of each (the scale of any evaluation's rounding error)."""
+        assert hidden.dtype == np.uint16 and hidden.flags["C_CONTIGUOUS"]
+        d = self.dims
+        d_inner = d["nheads"] * d["head_dim"]
+        d_xbc = d_inner + 2 * d["n_groups"] * d["d_state"]
+        n_in = d_inner + d_xbc + d["nheads"]
+        T = hidden.shape[0]
+        zx = np.empty((T, n_in), np.float64)
+        u = np.empty((T, d_xbc), np.float64)
+        zxa = np.empty((T, n_in), np.float64)
+        ua = np.empty((T, d_xbc), np.float64)
+        hits = lib().or_layer_prefill_traced(C.byref(self._s), _p(hidden), T, _p(h), _p(ring), _p(pos), _p(zx),
+                                             _p(u), _p(zxa), _p(ua))
+        return hits, (zx, zxa), (u, ua)

@@ -9,7 +9,7 @@ import torch
 from mamba_ssm_layer_gb300 import abi, synth
 from mamba_ssm_layer_gb300.layer import DeviceLayer, bits_u16, to_dev
 from oracle import oracle as orc
-from tests.helpers import TOL_BF16, TOL_STATE, bf16_to_f64, floored_rel_err, state_rel_err
+from tests.helpers import TOL_BF16, TOL_STATE, FlipTracker, bf16_to_f64, floored_rel_err, state_rel_err
 
 pytestmark = pytest.mark.gpu
 
@@ -152,37 +152,76 @@ def test_ssm_step_matches_oracle(B, H, P, N, G):
 
 # ------------------------------------------------------------------ layer
 
-def _oracle_layer_cache(lay):
-    return orc.OracleLayer(lay)
+def _rup(v, a):
+    return (v + a - 1) // a * a
+
+
+def _codes_decode(ws, B, lay, st, pos_before):
+    """GPU rounding decisions of the last decode step: R3 codes [B][n_in]
+    (z, raw xBC from the ring slot just written, dt) and R4 codes [B][d_xbc]."""
+    d = lay["dims"]
+    dd = synth.derived(d)
+    ldz = _rup(dd["n_in"], 8)
+    off = _rup(B * d["hidden"] * 2, 256)
+    zxu = ws[off: off + B * ldz * 2].view(torch.int16).view(B, ldz).cpu().numpy().view(np.uint16)
+    ring = bits_u16(st[1])
+    L = d["d_conv"] - 1
+    r3 = np.empty((B, dd["n_in"]), np.uint16)
+    di, dx = dd["d_inner"], dd["d_xbc"]
+    r3[:, :di] = zxu[:, :di]
+    for b in range(B):
+        r3[b, di:di + dx] = ring[b, pos_before[b] % L]
+    r3[:, di + dx:] = zxu[:, di + dx:dd["n_in"]]
+    return r3, zxu[:, di:di + dx].copy()
+
+
+def _codes_prefill(ws, T, lay):
+    d = lay["dims"]
+    dd = synth.derived(d)
+    ldz = _rup(dd["n_in"], 8)
+    off = _rup(T * d["hidden"] * 2, 256)
+    zx = ws[off: off + T * ldz * 2].view(torch.int16).view(T, ldz).cpu().numpy().view(np.uint16)
+    off_u = off + _rup(T * ldz * 2, 256)
+    u = ws[off_u: off_u + T * dd["d_xbc"] * 2].view(torch.int16).view(T, dd["d_xbc"]).cpu().numpy().view(np.uint16)
+    return zx[:, :dd["n_in"]].copy(), u.copy()
 
 
 def _run_decode(lay, B, steps, seqs_checked, hidden_key, warm=0):
-    """Decode `warm + steps` steps of B sequences on the GPU; check sequences
-    `seqs_checked` against the oracle after every checked step."""
+    """Decode `warm + steps` steps of B sequences on the GPU; follow sequences
+    `seqs_checked` with the oracle, checking every output row and every
+    rounding decision, and the final state."""
     dl = DeviceLayer(lay)
-    ol = _oracle_layer_cache(lay)
+    ol = orc.OracleLayer(lay)
     st = dl.new_state(B)
     ws = dl.workspace(B, 0)
     ost = {b: ol.new_state() for b in seqs_checked}
+    trk = {b: FlipTracker(lay["dims"], lay["A_log"], lay["dt_bias"], lay["conv_w"]) for b in seqs_checked}
     hd = lay["dims"]["hidden"]
     worst_out = 0.0
     for t in range(warm + steps):
         hid = synth.make_hidden(B, hd, *hidden_key, t)
         x = to_dev(hid)
+        pos_before = st[2].cpu().numpy().copy()
         dl.decode(x, st, ws)
         _sync()
         got = bits_u16(x)
+        r3, r4 = _codes_decode(ws, B, lay, st, pos_before)
         for b in seqs_checked:
             ref = np.ascontiguousarray(hid[b:b + 1])
-            ol.run(ref, *ost[b])
+            _, e3, e4 = ol.run_traced(ref, *ost[b])
+            trk[b].token(r3[b], (e3[0][0], e3[1][0]), r4[b], (e4[0][0], e4[1][0]))
             if t >= warm:
                 worst_out = max(worst_out, floored_rel_err(bf16_to_f64(got[b]), bf16_to_f64(ref[0])))
     h = st[0].cpu().numpy()
+    reports = []
     for b in seqs_checked:
-        assert state_rel_err(h[b], ost[b][0]) <= TOL_STATE
-        assert np.array_equal(bits_u16(st[1])[b], ost[b][1]), "conv ring"
+        reports.append(trk[b].check_state(h[b], ost[b][0]))
+        # ring values are rounded in_proj outputs (checked with their rounding
+        # decisions above); positions are integer work
+        assert floored_rel_err(bf16_to_f64(bits_u16(st[1])[b]), bf16_to_f64(ost[b][1]), axis=-1) <= TOL_BF16
         assert int(st[2][b]) == int(ost[b][2][0]) == warm + steps
     assert worst_out <= TOL_BF16
+    print("decode parity", B, steps, worst_out, reports)
     return worst_out
 
 
@@ -195,6 +234,7 @@ def test_decode_tiny_batch_and_batch_invariance():
     lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
     _run_decode(lay, 5, 6, [0, 3, 4], (synth.WL_TINY_DECODE, 1))
     # a sequence's result does not depend on the batch it is decoded in
+    # (batches that fit one GEMV pass use identical per-row arithmetic)
     dl = DeviceLayer(lay)
     hid = synth.make_hidden(3, 256, 9, 9, 9)
     outs = []
@@ -221,30 +261,40 @@ def test_decode_8b_layer_b64_sampled():
 
 
 def _prefill_case(lay, T, warm_decode, key):
-    """Decode `warm_decode` tokens, then prefill T tokens; compare with the oracle."""
+    """Decode `warm_decode` tokens, then prefill T tokens; compare with the oracle
+    (the prefill of T tokens is T sequential decode steps by definition)."""
     dl = DeviceLayer(lay)
     ol = orc.OracleLayer(lay)
     hd = lay["dims"]["hidden"]
     st = dl.new_state(1)
     ws = dl.workspace(1, T)
     ost = ol.new_state()
+    trk = FlipTracker(lay["dims"], lay["A_log"], lay["dt_bias"], lay["conv_w"])
     for t in range(warm_decode):
         hid = synth.make_hidden(1, hd, *key, 1000 + t)
         x = to_dev(hid)
+        pos_before = st[2].cpu().numpy().copy()
         dl.decode(x, st, ws)
-        ol.run(hid, *ost)
+        _sync()
+        r3, r4 = _codes_decode(ws, 1, lay, st, pos_before)
+        _, e3, e4 = ol.run_traced(hid, *ost)
+        trk.token(r3[0], (e3[0][0], e3[1][0]), r4[0], (e4[0][0], e4[1][0]))
     hid = synth.make_hidden(T, hd, *key, 0)
     x = to_dev(hid)
     dl.prefill(x, (st[0][0], st[1][0], st[2][:1]), ws)
     _sync()
+    r3, r4 = _codes_prefill(ws, T, lay)
     ref = hid.copy()
-    ol.run(ref, *ost)
+    _, e3, e4 = ol.run_traced(ref, *ost)
+    for t in range(T):
+        trk.token(r3[t], (e3[0][t], e3[1][t]), r4[t], (e4[0][t], e4[1][t]))
     got = bits_u16(x)
     err = floored_rel_err(bf16_to_f64(got), bf16_to_f64(ref), axis=-1)
     assert err <= TOL_BF16, err
-    assert state_rel_err(st[0][0].cpu().numpy(), ost[0]) <= TOL_STATE
-    assert np.array_equal(bits_u16(st[1])[0], ost[1])
+    rep = trk.check_state(st[0][0].cpu().numpy(), ost[0])
+    assert floored_rel_err(bf16_to_f64(bits_u16(st[1])[0]), bf16_to_f64(ost[1]), axis=-1) <= TOL_BF16
     assert int(st[2][0]) == warm_decode + T
+    print("prefill parity", T, err, rep)
     return err
 
 
