@@ -57,7 +57,9 @@ enum {
   M2_ERR_UNSUPPORTED = -5, /* shape outside the supported range               */
   M2_ERR_ALIGN = -6,       /* pointer not 16-byte aligned where required      */
   M2_ERR_DEVICE = -7,      /* no device, or a device older than sm_103        */
-  M2_ERR_TIMEOUT = -8      /* a bounded in-kernel wait gave up                */
+  M2_ERR_TIMEOUT = -8,     /* a bounded in-kernel wait gave up                */
+  M2_ERR_SCRATCH = -9      /* request larger than the built-in scratch of
+                              mamba2_layer_decode_noalloc                     */
 };
 
 /* Weight formats.  FP8_BLOCK128: E4M3 bytes [n][k] plus bf16 scales
@@ -166,6 +168,32 @@ int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint1
                     const uint16_t* dt_raw, int32_t ld_in, const float* A_log, const float* D,
                     const float* dt_bias, float* y, int32_t B, int32_t H, int32_t P, int32_t N,
                     int32_t G, cudaStream_t stream);
+
+/* Decode without any caller-provided or library-allocated workspace.  The
+ * pages have no counterpart: this entry point exists for callers that cannot
+ * allocate device memory on demand -- for example a plug-in running inside a
+ * host application that reserved all device memory for its own pool up
+ * front, or a latency-critical serving loop that must not call into the
+ * allocator (cudaMalloc may synchronise the device and can fail once memory
+ * is committed).  It behaves exactly like mamba2_layer_decode (same
+ * arguments apart from the workspace, same kernels, same results), but its
+ * scratch lives in one fixed array inside the library, M2_NOALLOC_SCRATCH_BYTES
+ * (8 MiB) per device, which every GPU that loads the library holds until the
+ * process exits.  It allocates nothing itself.
+ *  - Requests whose decode workspace (m2_workspace_bytes(dims, B, 0)) exceeds
+ *    M2_NOALLOC_SCRATCH_BYTES return M2_ERR_SCRATCH and launch nothing (for
+ *    the hidden-4096 / 8192-inner layer that is B > 88).
+ *  - The first call on a device looks up the array's device address for that
+ *    device (cudaGetSymbolAddress, with that device current); make that first
+ *    call before any stream capture on the device.
+ *  - All calls share the one array and it keeps the previous call's
+ *    contents; nothing in it needs to start at zero (the per-sequence state
+ *    lives in the caller's buffers).  Calls whose work overlaps on the GPU --
+ *    concurrent streams, or several host threads -- race on the array: order
+ *    them on one stream or synchronise between them. */
+#define M2_NOALLOC_SCRATCH_BYTES (8u << 20)
+int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t B,
+                                float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, cudaStream_t stream);
 
 /* ------------------------------------------------------------ diagnostics */
 

@@ -24,12 +24,15 @@ M2_ERR_UNSUPPORTED = -5
 M2_ERR_ALIGN = -6
 M2_ERR_DEVICE = -7
 M2_ERR_TIMEOUT = -8
+M2_ERR_SCRATCH = -9
+M2_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 M2_W_FP8_BLOCK128 = 1
 M2_W_BF16 = 2
 
 # Every entry point include/mamba2.h declares (checked by the host tests).
 EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_decode", "mamba2_layer_prefill",
+           "mamba2_layer_decode_noalloc",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
            "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count")
 
@@ -79,6 +82,8 @@ def lib():
             l.m2_workspace_bytes.argtypes = [C.POINTER(M2Dims), I32, I32]; l.m2_workspace_bytes.restype = SZ
             l.mamba2_layer_decode.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P, SZ, P]
             l.mamba2_layer_decode.restype = C.c_int
+            l.mamba2_layer_decode_noalloc.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P]
+            l.mamba2_layer_decode_noalloc.restype = C.c_int
             l.mamba2_layer_prefill.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P, SZ, P]
             l.mamba2_layer_prefill.restype = C.c_int
             l.w8a16_gemv.argtypes = [P, P, P, P, I32, I32, I32, P]; l.w8a16_gemv.restype = C.c_int
@@ -150,6 +155,15 @@ def mamba2_layer_decode(dims, layer, hidden, B, ssm_state, conv_state, conv_pos,
     st = lib().mamba2_layer_decode(C.byref(dims), C.byref(layer), _ptr(hidden), B, _ptr(ssm_state),
                                    _ptr(conv_state), _ptr(conv_pos), _ptr(ws), ws_bytes, _stream(stream))
     return _check("mamba2_layer_decode", st) if check else st
+
+
+def mamba2_layer_decode_noalloc(dims, layer, hidden, B, ssm_state, conv_state, conv_pos, stream=None,
+                                check=True) -> int:
+    """Decode step with the library's built-in scratch instead of a workspace
+    (for callers that cannot allocate device memory; see include/mamba2.h)."""
+    st = lib().mamba2_layer_decode_noalloc(C.byref(dims), C.byref(layer), _ptr(hidden), B, _ptr(ssm_state),
+                                           _ptr(conv_state), _ptr(conv_pos), _stream(stream))
+    return _check("mamba2_layer_decode_noalloc", st) if check else st
 
 
 def mamba2_layer_prefill(dims, layer, hidden, T, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream=None,

@@ -197,6 +197,7 @@ const char* m2_strerror(int status) {
     case M2_ERR_ALIGN: return "pointer not 16-byte aligned";
     case M2_ERR_DEVICE: return "no usable CUDA device";
     case M2_ERR_TIMEOUT: return "a bounded in-kernel wait timed out";
+    case M2_ERR_SCRATCH: return "decode workspace larger than the built-in scratch of mamba2_layer_decode_noalloc";
     default: return "unknown status";
   }
 }
@@ -425,6 +426,40 @@ int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint1
   sa.G = G;
   sa.pos_inc = nullptr;
   return launch_status(launch_ssm_step(sa, stream));
+}
+
+// Scratch of mamba2_layer_decode_noalloc: a fixed device array, so that
+// callers who cannot allocate still get a workspace.  Host code must not use
+// the symbol as an address; the device address is looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[M2_NOALLOC_SCRATCH_BYTES];
+static void* g_noalloc_ptr[64];
+static std::mutex g_noalloc_mu;
+
+int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t B,
+                                float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, cudaStream_t stream) {
+  int st = m2_validate(dims, layer);
+  if (st) return st;
+  if (B <= 0) return M2_ERR_ARG;
+  const size_t need = decode_ws(*dims, B);
+  if (need > (size_t)M2_NOALLOC_SCRATCH_BYTES) return M2_ERR_SCRATCH;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return M2_ERR_DEVICE;
+  void* ptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      // the current device is `dev`: this resolves the array's address there
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+        cudaGetLastError();
+        return M2_ERR_DEVICE;
+      }
+      g_noalloc_ptr[dev] = p;
+    }
+    ptr = g_noalloc_ptr[dev];
+  }
+  return mamba2_layer_decode(dims, layer, hidden, B, ssm_state, conv_state, conv_pos, ptr,
+                             (size_t)M2_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int m2_device_status(int clear) {
