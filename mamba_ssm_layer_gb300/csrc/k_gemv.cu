@@ -16,9 +16,7 @@
 //               (two warps per scheduler per group hide the load/convert/FMA
 //               latencies): thread t of a group owns the 16-byte chunks t,
 //               t+256, ... of every row, so its activations stay in registers
-//               for the whole call.  The activation prologue optionally fuses
-//               the norm that produces A (input RMSNorm, or the gated RMSNorm
-//               of y and z), reduced across the consumers.  Per row a thread
+//               for the whole call.  Per row a thread
 //               forms 16-element partial dot products, multiplies each by the
 //               chunk's block scale and accumulates; per stage the R*MB sums
 //               are reduced with a transposing warp butterfly and handed to
@@ -48,7 +46,6 @@ constexpr int kGemvThreads = kGemvAllConsumers + 64;                 // 576
 constexpr int kGemvStageBudget = 184320;                 // bytes of weight ring
 constexpr int kGemvMaxStages = 8;
 constexpr int kGemvSlots = 4;                            // reduction slots
-constexpr int kMaxGroups = 64;                           // gated-norm groups per row
 
 struct GemvSmemTail {
   uint64_t full[kGemvMaxStages];
@@ -56,9 +53,6 @@ struct GemvSmemTail {
   uint64_t red_full[kGemvSlots];
   uint64_t red_empty[kGemvSlots];
   float red[kGemvSlots][kGemvConsumerWarps][32];
-  float nsum[4][kMaxGroups];  // norm reductions (per batch row, per group)
-  float nss[2][4][kGemvConsumerWarps];  // input-RMSNorm (hi, lo) per row per warp
-  double nrd[4];              // 1/sqrt(mean(x^2)+eps) per row, in double
   unsigned amax[4];           // max |activation| per batch row (float bits)
   float unscale[4];           // 2^-j undoing the f16 prescale of row m
 };
@@ -216,146 +210,54 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     for (int i = lane; i < nbs * kb; i += 32)
       sc[i] = bf16_to_f32(__ldg(a.S + (size_t)(nb0 + i / kb) * kb + (i % kb)));
   }
-  pdl_trigger();
 
   // ------------------------------------------------ activation prologue
   // Activations are cached in registers as packed pairs: f16 for E4M3
   // weights (E4M3 -> f16 is exact, and the products then run as
-  // fma.rn.f32.f16 at full FFMA rate), bf16 for bf16 weights.  For f16 each
-  // batch row is first multiplied by an exact power of two 2^j that puts its
-  // largest magnitude in [2^14, 2^15): every bf16 value within 2^31 of the row
-  // maximum is then exactly representable, and the 2^-j is applied to the
-  // row totals.
+  // fma.rn.f32.f16 at full FFMA rate), bf16 for bf16 weights.  f16 rows carry
+  // an exact power-of-two prescale 2^j that puts the row maximum in
+  // [2^14, 2^15): every bf16 value within 2^31 of the row maximum is then
+  // exactly representable; 2^-j is applied to the row totals.  Prepared
+  // activations (ACT_PREPARED) arrive in that form; plain bf16 rows are
+  // converted here.
   uint32_t acth[MB][CPT][T::kEpc / 2];
   const int grp = warp / kGemvConsumerWarps;  // consumer group (consumers only)
   const int gtid = tid % kGemvConsumers;      // thread index within the group
   const int gwarp = warp % kGemvConsumerWarps;
   if (warp < kGemvGroups * kGemvConsumerWarps) {
-    float act[MB][CPT][T::kEpc];
-    pdl_wait();  // A / y / z come from the previous kernel
+    pdl_wait();  // A comes from the previous kernel
 #pragma unroll
     for (int m = 0; m < MB; ++m)
 #pragma unroll
       for (int j = 0; j < CPT; ++j) {
         const int c = gtid + j * kGemvConsumers;
-        const bool live = m < mvalid && c < nchunks;
-        const int k0 = c * T::kEpc;
-        if (live && a.act == ACT_GATED) {
-          const float4* src = reinterpret_cast<const float4*>(a.y + (size_t)(m0 + m) * a.ldy + k0);
-#pragma unroll
-          for (int q = 0; q < T::kEpc / 4; ++q) {
-            const float4 v = __ldg(src + q);
-            act[m][j][4 * q] = v.x;
-            act[m][j][4 * q + 1] = v.y;
-            act[m][j][4 * q + 2] = v.z;
-            act[m][j][4 * q + 3] = v.w;
-          }
-        } else if (live) {
-          const uint4* src = reinterpret_cast<const uint4*>(a.A + (size_t)(m0 + m) * a.lda + k0);
+        if (m < mvalid && c < nchunks) {
+          const uint4* src = reinterpret_cast<const uint4*>(a.A + (size_t)(m0 + m) * a.lda + (size_t)c * T::kEpc);
 #pragma unroll
           for (int q = 0; q < T::kEpc / 8; ++q) {
-            const uint4 v = __ldg(src + q);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              act[m][j][q * 8 + 2 * e] = bf16lo(w4[e]);
-              act[m][j][q * 8 + 2 * e + 1] = bf16hi(w4[e]);
-            }
+            const uint4 v = src[q];  // coherent load: written by the PDL predecessor
+            acth[m][j][4 * q] = v.x;
+            acth[m][j][4 * q + 1] = v.y;
+            acth[m][j][4 * q + 2] = v.z;
+            acth[m][j][4 * q + 3] = v.w;
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < T::kEpc; ++e) act[m][j][e] = 0.0f;
+          for (int e = 0; e < T::kEpc / 2; ++e) acth[m][j][e] = 0u;
         }
       }
-    if (a.act == ACT_RMSNORM) {
-      // input RMSNorm: sum of squares carried as an error-free fp32 pair and
-      // r evaluated once in double, so that the bf16 rounding of x * r * w
-      // does not depend on the summation order
-#pragma unroll
-      for (int m = 0; m < MB; ++m) {
-        float hi = 0.0f, lo = 0.0f;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j)
-#pragma unroll
-          for (int e = 0; e < T::kEpc; ++e) two_sum_acc(hi, lo, act[m][j][e] * act[m][j][e]);
-        two_sum_warp(hi, lo);
-        if (grp == 0 && lane == 0) {
-          tail->nss[0][m][gwarp] = hi;
-          tail->nss[1][m][gwarp] = lo;
-        }
-      }
-      named_bar(1, kGemvAllConsumers);
-      if (tid < MB) {
-        double tot = 0.0;
-        for (int w = 0; w < kGemvConsumerWarps; ++w) tot += (double)tail->nss[0][tid][w] + (double)tail->nss[1][tid][w];
-        tail->nrd[tid] = 1.0 / sqrt(tot / (double)a.K + (double)a.eps);
-      }
-      named_bar(1, kGemvAllConsumers);
-#pragma unroll
-      for (int m = 0; m < MB; ++m) {
-        const double rd = tail->nrd[m];
-        const float rf = (float)rd;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const int c = gtid + j * kGemvConsumers;
-          if (m < mvalid && c < nchunks) {
-            const int k0 = c * T::kEpc;
-#pragma unroll
-            for (int e = 0; e < T::kEpc; ++e)
-              act[m][j][e] = bf16_to_f32(norm_round_bf16(act[m][j][e], bf16_to_f32(a.norm_w[k0 + e]), rf, rd));
-          }
-        }
-      }
-    } else if (a.act == ACT_GATED) {
-      // sums of squares per (row, group): chunks never straddle a group
-      const int group = a.group;
-      const int ngroups = a.K / group;
-      for (int i = tid; i < 4 * kMaxGroups; i += kGemvAllConsumers) (&tail->nsum[0][0])[i] = 0.0f;
-      named_bar(1, kGemvAllConsumers);
-#pragma unroll
-      for (int m = 0; m < MB; ++m)
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const int c = gtid + j * kGemvConsumers;
-          float ss = 0.0f;
-#pragma unroll
-          for (int e = 0; e < T::kEpc; ++e) ss = fmaf(act[m][j][e], act[m][j][e], ss);
-          if (grp == 0) {  // both groups hold the same values; group 0 reduces
-            if (ngroups == 1) {
-              ss = warp_sum(ss);
-              if (lane == 0) atomicAdd(&tail->nsum[m][0], ss);
-            } else if (m < mvalid && c < nchunks) {
-              atomicAdd(&tail->nsum[m][(c * T::kEpc) / group], ss);
-            }
-          }
-        }
-      named_bar(1, kGemvAllConsumers);
-#pragma unroll
-      for (int m = 0; m < MB; ++m)
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-          const int c = gtid + j * kGemvConsumers;
-          if (m < mvalid && c < nchunks) {
-            const int k0 = c * T::kEpc;
-            const float r = 1.0f / sqrtf(tail->nsum[m][k0 / group] / (float)group + a.eps);
-#pragma unroll
-            for (int e = 0; e < T::kEpc; ++e) {
-              float v = act[m][j][e] * r * bf16_to_f32(a.norm_w[k0 + e]);
-              v *= silu_f(bf16_to_f32(a.z[(size_t)(m0 + m) * a.ldz + k0 + e]));
-              act[m][j][e] = bf16_to_f32(f32_to_bf16(v));  // the gated norm's rounding point
-            }
-          }
-        }
-    }
-    if constexpr (FP8) {
-      // per-row power-of-two prescale into the f16 range
+    if (a.act == ACT_PREPARED) {
+      if (tid < 4) tail->unscale[tid] = tid < mvalid ? a.unscale[m0 + tid] : 1.0f;
+    } else if constexpr (FP8) {
+      // plain bf16 rows: find each row's prescale, convert to f16
 #pragma unroll
       for (int m = 0; m < MB; ++m) {
         float mx = 0.0f;
 #pragma unroll
         for (int j = 0; j < CPT; ++j)
 #pragma unroll
-          for (int e = 0; e < T::kEpc; ++e) mx = fmaxf(mx, fabsf(act[m][j][e]));
+          for (int e = 0; e < T::kEpc / 2; ++e)
+            mx = fmaxf(mx, fmaxf(fabsf(bf16lo(acth[m][j][e])), fabsf(bf16hi(acth[m][j][e]))));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (lane == 0 && grp == 0) atomicMax(&tail->amax[m], __float_as_uint(mx));
@@ -373,16 +275,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         for (int j = 0; j < CPT; ++j)
 #pragma unroll
           for (int e2 = 0; e2 < T::kEpc / 2; ++e2)
-            acth[m][j][e2] = pack_f16x2(act[m][j][2 * e2] * up, act[m][j][2 * e2 + 1] * up);
+            acth[m][j][e2] = pack_f16x2(bf16lo(acth[m][j][e2]) * up, bf16hi(acth[m][j][e2]) * up);
       }
     } else {
-      if (tid < 4) tail->unscale[tid] = 1.0f;
-#pragma unroll
-      for (int m = 0; m < MB; ++m)
-#pragma unroll
-        for (int j = 0; j < CPT; ++j)
-#pragma unroll
-          for (int e2 = 0; e2 < T::kEpc / 2; ++e2) acth[m][j][e2] = pack_bf16x2(act[m][j][2 * e2], act[m][j][2 * e2 + 1]);
+      if (tid < 4) tail->unscale[tid] = 1.0f;  // bf16 weights use the bf16 rows as they are
     }
   }
   if (warp == kGemvHelperWarp) {
@@ -416,6 +312,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
   }
   __syncthreads();  // scales staged; epilogue inputs staged
+  pdl_trigger();    // every consumer has passed its wait
 
   bool dead = false;
   if (warp == kGemvProducerWarp) {
@@ -592,6 +489,9 @@ static int launch_group(const GemvArgs& a, int m0, cudaStream_t s, cudaError_t* 
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s) {
+  // batches of up to 8 rows with K % 64 == 0, K <= 8192: one weight pass on
+  // the warp-MMA GEMV (k_gemv_mma.cu)
+  if (gemv_mma_supported(a.M, a.K)) return launch_gemv_mma(a, fp8, s);
   for (int m0 = 0; m0 < a.M;) {
     cudaError_t e = cudaSuccess;
     GemvArgs b = a;
@@ -605,67 +505,9 @@ cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s) {
 // Largest batch row count one GEMV pass covers for a K-wide row (the fused
 // norm prologue needs the whole batch in one pass).
 int gemv_rows_per_pass(int K, bool fp8) {
+  if (gemv_mma_supported(8, K)) return 8;
   const int cpt = (K * (fp8 ? 1 : 2) + 4095) / 4096;
   return cpt == 1 ? 4 : (cpt == 2 ? 2 : 1);
-}
-
-// ------------------------------------------------------------------ RMSNorm
-
-// Input RMSNorm, weight * x scaling (source listing "nemotron_mamba2.rs",
-// module header step 1): out = bf16( x / sqrt(mean(x^2) + eps) * w ).
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t* __restrict__ x, int ldx,
-                                                      const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
-                                                      int ldo, int K, float eps) {
-  // sum of squares as an error-free fp32 pair, r once in double (see
-  // norm_round_bf16)
-  const uint16_t* xr = x + (size_t)blockIdx.x * ldx;
-  __shared__ float red[2][8];
-  __shared__ double rds;
-  float hi = 0.0f, lo = 0.0f;
-  for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a0 = bf16lo(w4[e]), a1 = bf16hi(w4[e]);
-      two_sum_acc(hi, lo, a0 * a0);
-      two_sum_acc(hi, lo, a1 * a1);
-    }
-  }
-  two_sum_warp(hi, lo);
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = hi;
-    red[1][threadIdx.x >> 5] = lo;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double tot = 0.0;
-    for (int i = 0; i < 8; ++i) tot += (double)red[0][i] + (double)red[1][i];
-    rds = 1.0 / sqrt(tot / (double)K + (double)eps);
-  }
-  __syncthreads();
-  const double rd = rds;
-  const float rf = (float)rd;
-  uint16_t* o = out + (size_t)blockIdx.x * ldo;
-  for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
-    const uint4 g = *reinterpret_cast<const uint4*>(w + k);
-    const uint32_t x4[4] = {v.x, v.y, v.z, v.w}, g4[4] = {g.x, g.y, g.z, g.w};
-    uint32_t o4[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      o4[e] = (uint32_t)norm_round_bf16(bf16lo(x4[e]), bf16lo(g4[e]), rf, rd) |
-              ((uint32_t)norm_round_bf16(bf16hi(x4[e]), bf16hi(g4[e]), rf, rd) << 16);
-    *reinterpret_cast<uint4*>(o + k) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-  }
-}
-
-cudaError_t launch_rmsnorm(const uint16_t* x, int32_t ldx, const uint16_t* w, uint16_t* out, int32_t ldo,
-                           int32_t M, int32_t K, float eps, cudaStream_t s) {
-  trace_pre(K_RMSNORM, s);
-  rmsnorm_kernel<<<M, 256, 0, s>>>(x, ldx, w, out, ldo, K, eps);
-  trace_post(K_RMSNORM, s);
-  return cudaGetLastError();
 }
 
 int status_gemv(int clear) {

@@ -138,31 +138,36 @@ __global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int pspl
   // ROWS rows, whose state loads are all issued before any is used.
   constexpr int RPW = 32 / LPR;
   constexpr int CTA_ROWS = 8 * RPW * ROWS;
-  pdl_trigger();
-  pdl_wait();  // everything below may depend on the previous kernel
   const int b = blockIdx.y;
   const int h = blockIdx.x / psplit;
   const int pc = blockIdx.x % psplit;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n4 = (lane % LPR) * 4;
   const int g = h / (a.H / a.G);
+  float* hb = a.h + ((size_t)b * a.H + h) * a.P * a.N;
+  const int p0 = pc * CTA_ROWS + warp * RPW + lane / LPR;
+  float4 hv[ROWS];
+  // The state is written only by the SSM kernels of earlier steps, which have
+  // completed by now (every kernel of the chain lets its successor launch only
+  // after its own wait), so it can be fetched before waiting on the in_proj.
+#pragma unroll
+  for (int i = 0; i < ROWS; ++i) {
+    const int p = p0 + i * 8 * RPW;
+    if (p < a.P) hv[i] = *reinterpret_cast<const float4*>(hb + (size_t)p * a.N + n4);
+  }
+  pdl_wait();  // x, B, C, dt come from the previous kernel
+  pdl_trigger();
   const uint16_t* xr = a.x + (size_t)b * a.ld_in;
   float dt, dA;
   head_scalars(a.dt + (size_t)b * a.ld_in, a.dt_bias, a.A_log, h, dt, dA);
   const float Dh = a.D[h];
   const float4 Bv = ld4bf(a.Bm + (size_t)b * a.ld_in + (size_t)g * a.N + n4);
   const float4 Cv = ld4bf(a.Cm + (size_t)b * a.ld_in + (size_t)g * a.N + n4);
-  float* hb = a.h + ((size_t)b * a.H + h) * a.P * a.N;
-  const int p0 = pc * CTA_ROWS + warp * RPW + lane / LPR;
-  float4 hv[ROWS];
   float xv[ROWS];
 #pragma unroll
   for (int i = 0; i < ROWS; ++i) {
     const int p = p0 + i * 8 * RPW;
-    if (p < a.P) {
-      hv[i] = *reinterpret_cast<const float4*>(hb + (size_t)p * a.N + n4);
-      xv[i] = bf16_to_f32(xr[(size_t)h * a.P + p]);
-    }
+    xv[i] = p < a.P ? bf16_to_f32(xr[(size_t)h * a.P + p]) : 0.0f;
   }
 #pragma unroll
   for (int i = 0; i < ROWS; ++i) {
@@ -289,53 +294,176 @@ cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ gated norm
+// ------------------------------------------------------------------ activation prep
 
-// g = bf16( y / sqrt(mean_group(y^2) + eps) * w * silu(z) ), one CTA per
-// (row, group).
-__global__ void __launch_bounds__(256) gated_norm_kernel(const float* __restrict__ y, int ldy,
-                                                         const uint16_t* __restrict__ z, int ldz,
-                                                         const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
-                                                         int ldo, int group, float eps) {
+// The norm that produces a GEMV's activation, one CTA (512 threads) per row:
+//   PREP_RMSNORM  x * r * w,            r = 1/sqrt(mean(x^2) + eps)   (source
+//                 listing "nemotron_mamba2.rs", module header step 1: weight*x)
+//   PREP_GATED    y * r * w * silu(z),  r over groups of `group`      (step 6:
+//                 rms_norm(y, ssm_norm) * silu(z))
+// rounded to bf16 (the layer's rounding point), then stored as bf16 or, for an
+// E4M3-weight GEMV, as f16 after the exact row prescale 2^j (max |v| * 2^j in
+// [2^14, 2^15); unscale = 2^-j).  The RMSNorm sum of squares is an error-free
+// fp32 pair and r is evaluated once in double, so its rounding decisions do
+// not depend on the summation order (norm_round_bf16).
+constexpr int kPrepThreads = 512;
+constexpr int kPrepMaxPer = 32;  // elements per thread (K <= 16384)
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int m = blockIdx.x;
-  const int g0 = blockIdx.y * group;
-  const float* yr = y + (size_t)m * ldy + g0;
-  __shared__ float red[8];
-  float ss = 0.0f;
-  for (int i = threadIdx.x * 4; i < group; i += 1024) {
-    const float4 v = *reinterpret_cast<const float4*>(yr + i);
-    ss = fmaf(v.x, v.x, ss);
-    ss = fmaf(v.y, v.y, ss);
-    ss = fmaf(v.z, v.z, ss);
-    ss = fmaf(v.w, v.w, ss);
-  }
-  ss = warp_sum(ss);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-  __syncthreads();
-  float tot = 0.0f;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float s_hi[16], s_lo[16], s_max[16];
+  __shared__ float gsum[1024];
+  __shared__ double s_rd;
+  const int K = a.K;
+  float v[kPrepMaxPer];
+  // element e of this thread: k = (tid + 512 * (e / 8)) * 8 + e % 8
 #pragma unroll
-  for (int i = 0; i < 8; ++i) tot += red[i];
-  const float r = 1.0f / sqrtf(tot / (float)group + eps);
-  const uint16_t* zr = z + (size_t)m * ldz + g0;
-  const uint16_t* wr = w + g0;
-  uint16_t* o = out + (size_t)m * ldo + g0;
-  for (int i = threadIdx.x * 4; i < group; i += 1024) {
-    const float4 v = *reinterpret_cast<const float4*>(yr + i);
-    const float4 zz = ld4bf(zr + i);
-    const float4 ww = ld4bf(wr + i);
-    const uint32_t lo = pack_bf16x2(v.x * r * ww.x * silu_f(zz.x), v.y * r * ww.y * silu_f(zz.y));
-    const uint32_t hi = pack_bf16x2(v.z * r * ww.z * silu_f(zz.z), v.w * r * ww.w * silu_f(zz.w));
-    *reinterpret_cast<uint2*>(o + i) = make_uint2(lo, hi);
+  for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+    const int k0 = (tid + kPrepThreads * c) * 8;
+    if (k0 < K) {
+      if (a.mode == PREP_RMSNORM) {
+        const uint4 u = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.ldx + k0);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[c * 8 + 2 * e] = bf16lo(w4[e]);
+          v[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
+        }
+      } else {
+        const float4 f0 = *reinterpret_cast<const float4*>(a.y + (size_t)m * a.ldy + k0);
+        const float4 f1 = *reinterpret_cast<const float4*>(a.y + (size_t)m * a.ldy + k0 + 4);
+        v[c * 8 + 0] = f0.x; v[c * 8 + 1] = f0.y; v[c * 8 + 2] = f0.z; v[c * 8 + 3] = f0.w;
+        v[c * 8 + 4] = f1.x; v[c * 8 + 5] = f1.y; v[c * 8 + 6] = f1.z; v[c * 8 + 7] = f1.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
+    }
+  }
+  if (a.mode == PREP_RMSNORM) {
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kPrepMaxPer; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
+    two_sum_warp(hi, lo);
+    if (lane == 0) {
+      s_hi[warp] = hi;
+      s_lo[warp] = lo;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      // combine the warps' pairs, then r = 1/sqrt(mean + eps) from the fp32
+      // estimate and one Newton step in double (relative error ~2^-44)
+      float h = 0.0f, l = 0.0f;
+      for (int w = 0; w < 16; ++w) {
+        two_sum_acc(h, l, s_hi[w]);
+        l += s_lo[w];
+      }
+      const double v = ((double)h + (double)l) / (double)K + (double)a.eps;
+      const double r0 = (double)rsqrtf((float)v);
+      s_rd = r0 * (1.5 - 0.5 * v * r0 * r0);
+    }
+    __syncthreads();
+    const double rd = s_rd;
+    const float rf = (float)rd;
+#pragma unroll
+    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+      const int k0 = (tid + kPrepThreads * c) * 8;
+      if (k0 < K) {
+        const uint4 u = *reinterpret_cast<const uint4*>(a.w + k0);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, rd));
+          v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, rd));
+        }
+      }
+    }
+  } else {
+    const int ngroups = K / a.group;
+    for (int i = tid; i < ngroups; i += kPrepThreads) gsum[i] = 0.0f;
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+      const int k0 = (tid + kPrepThreads * c) * 8;
+      float ss = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
+      if (a.group % 256 == 0) {
+        // a warp's 256 consecutive elements lie in one group: reduce, then one atomic
+        ss = warp_sum(ss);
+        const int kw = (warp * 32 + kPrepThreads * c) * 8;
+        if (lane == 0 && kw < K) atomicAdd(&gsum[kw / a.group], ss);
+      } else if (k0 < K) {
+        atomicAdd(&gsum[k0 / a.group], ss);  // a run of 8 never straddles a group (group % 16 == 0)
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+      const int k0 = (tid + kPrepThreads * c) * 8;
+      if (k0 < K) {
+        const float r = 1.0f / sqrtf(gsum[k0 / a.group] / (float)a.group + a.eps);
+        const uint4 u = *reinterpret_cast<const uint4*>(a.w + k0);
+        const uint4 zz = *reinterpret_cast<const uint4*>(a.z + (size_t)m * a.ldz + k0);
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w}, z4[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float g0 = v[c * 8 + 2 * e] * r * bf16lo(w4[e]) * silu_f(bf16lo(z4[e]));
+          const float g1 = v[c * 8 + 2 * e + 1] * r * bf16hi(w4[e]) * silu_f(bf16hi(z4[e]));
+          v[c * 8 + 2 * e] = bf16_to_f32(f32_to_bf16(g0));
+          v[c * 8 + 2 * e + 1] = bf16_to_f32(f32_to_bf16(g1));
+        }
+      }
+    }
+  }
+  float up = 1.0f;
+  if (a.f16) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kPrepMaxPer; ++e) mx = fmaxf(mx, fabsf(v[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) s_max[warp] = mx;
+    __syncthreads();
+    mx = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) mx = fmaxf(mx, s_max[w]);
+    const unsigned bits = __float_as_uint(mx);
+    const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
+    const int jx = max(-120, min(120, 14 - ex));
+    up = ldexpf(1.0f, jx);
+    if (tid == 0) a.unscale[m] = ldexpf(1.0f, -jx);
+  } else if (a.unscale && tid == 0) {
+    a.unscale[m] = 1.0f;
+  }
+#pragma unroll
+  for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+    const int k0 = (tid + kPrepThreads * c) * 8;
+    if (k0 < K) {
+      uint32_t o4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (a.f16) {
+          uint32_t h;
+          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(v[c * 8 + 2 * e + 1] * up), "f"(v[c * 8 + 2 * e] * up));
+          o4[e] = h;
+        } else {
+          o4[e] = pack_bf16x2(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+        }
+      }
+      *reinterpret_cast<uint4*>(a.out + (size_t)m * a.ldo + k0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
   }
 }
 
-cudaError_t launch_gated_norm(const float* y, int32_t ldy, const uint16_t* z, int32_t ldz, const uint16_t* w,
-                              uint16_t* out, int32_t ldo, int32_t M, int32_t d, int32_t group, float eps,
-                              cudaStream_t s) {
-  trace_pre(K_GATED_NORM, s);
-  gated_norm_kernel<<<dim3(M, d / group), 256, 0, s>>>(y, ldy, z, ldz, w, out, ldo, group, eps);
-  trace_post(K_GATED_NORM, s);
-  return cudaGetLastError();
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+  trace_pre(K_PREP, s);
+  cudaError_t e = launch_k(prep_kernel, dim3(a.M), dim3(kPrepThreads), 0, s, a.pdl != 0, a);
+  trace_post(K_PREP, s);
+  return e;
 }
 
 int status_mixer(int clear) {

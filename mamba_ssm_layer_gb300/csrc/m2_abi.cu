@@ -73,11 +73,10 @@ void trace_post(int32_t id, cudaStream_t s) {
 }
 
 static const char* kNames[K_COUNT] = {
-    "rmsnorm",       "gemv_fp8",        "gemv_fp8_inproj_conv", "gemv_fp8_outproj_resid",
+    "norm_prep",     "gemv_fp8",        "gemv_fp8_inproj_conv", "gemv_fp8_outproj_resid",
     "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
-    "conv_pos",      "ssm_step",        "gated_norm",      "conv_prefill",
-    "ssm_scan_seq",  "gemm_tc",         "ssd_chunk_state", "ssd_state_pass",
-    "ssd_chunk_out"};
+    "conv_pos",      "ssm_step",        "conv_prefill",    "ssm_scan_seq",
+    "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out"};
 
 // ------------------------------------------------------------------ helpers
 
@@ -128,6 +127,11 @@ static int check_weight(const m2_weight& w, int n, int k) {
   return M2_OK;
 }
 
+// Workspace layouts (each region 256-byte aligned).
+//   decode:  act_in [B][hidden] (2 B), zxu [B][ldz] bf16 (z | conv output u | dt),
+//            y [B][d_inner] fp32, act_out [B][d_inner] (2 B), unscale [2][B] fp32
+//   prefill: act_in [T][hidden], zx [T][ldz] (raw in_proj output), u [T][d_xbc],
+//            y [T][d_inner] fp32, act_out [T][d_inner], unscale [2][T] fp32
 static size_t decode_ws(const m2_dims& d, int B) {
   const Derived r = derive(d);
   size_t o = 0;
@@ -135,6 +139,7 @@ static size_t decode_ws(const m2_dims& d, int B) {
   o = rup(o + (size_t)B * r.ldz * 2, 256);
   o = rup(o + (size_t)B * r.d_inner * 4, 256);
   o = rup(o + (size_t)B * r.d_inner * 2, 256);
+  o = rup(o + (size_t)2 * B * 4, 256);
   return o;
 }
 
@@ -146,11 +151,13 @@ static size_t prefill_ws(const m2_dims& d, int T) {
   o = rup(o + (size_t)T * r.d_xbc * 2, 256);    // u (conv output)
   o = rup(o + (size_t)T * r.d_inner * 4, 256);  // y
   o = rup(o + (size_t)T * r.d_inner * 2, 256);  // g
+  o = rup(o + (size_t)2 * T * 4, 256);          // unscale
   return o;
 }
 
 static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
-                        GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr) {
+                        GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr,
+                        const float* unscale = nullptr, int pdl = 0) {
   GemvArgs a;
   memset(&a, 0, sizeof(a));
   if (extra) a = *extra;
@@ -166,6 +173,9 @@ static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, u
   a.epi = epi;
   a.resid = resid;
   a.ldr = ldr;
+  a.act = unscale ? ACT_PREPARED : ACT_PLAIN;
+  a.unscale = unscale;
+  a.pdl = pdl;
   const int rowbytes = w.k * (w.fmt == M2_W_FP8_BLOCK128 ? 1 : 2);
   const int grp = rowbytes <= 4096 ? 4 : (rowbytes <= 8192 ? 2 : 1);
   a.evict_first = M <= grp ? 1 : 0;
@@ -239,16 +249,32 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   o = rup(o + (size_t)B * r.d_inner * 4, 256);
   uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
 
+  o = rup(o + (size_t)B * r.d_inner * 2, 256);
+  float* us_in = reinterpret_cast<float*>(w8 + o);
+  float* us_out = us_in + B;
+
   cudaError_t e;
   const bool in_fp8 = L->in_proj.fmt == M2_W_FP8_BLOCK128;
   const bool out_fp8 = L->out_proj.fmt == M2_W_FP8_BLOCK128;
-  // The norms fuse into the GEMV prologues when one weight pass covers the
-  // whole batch; the three kernels of the decode chain are launched as
-  // programmatic dependents so each streams its weights while its
-  // predecessor drains.
-  const bool fuse_in = B <= gemv_rows_per_pass(d.hidden, in_fp8);
-  const bool fuse_out = B <= gemv_rows_per_pass(r.d_inner, out_fp8) && r.d_inner / d.gnorm_group <= 64;
-  // 1+2+3. RMSNorm, in_proj, conv1d update (bias, SiLU) in its epilogue
+  // Five kernels, each launched as a programmatic dependent of the previous
+  // one, so that a GEMV streams its weights while its predecessor drains.
+  // 1. input RMSNorm -> GEMV activation
+  PrepArgs pa;
+  memset(&pa, 0, sizeof(pa));
+  pa.mode = PREP_RMSNORM;
+  pa.x = hidden;
+  pa.ldx = d.hidden;
+  pa.w = L->norm_w;
+  pa.eps = d.eps_in;
+  pa.M = B;
+  pa.K = d.hidden;
+  pa.out = xn;
+  pa.ldo = d.hidden;
+  pa.f16 = in_fp8 ? 1 : 0;
+  pa.unscale = us_in;
+  pa.pdl = 1;
+  if ((e = launch_prep(pa, stream))) return launch_status(e);
+  // 2+3. in_proj, conv1d update (bias, SiLU) in its epilogue
   GemvArgs ex;
   memset(&ex, 0, sizeof(ex));
   ex.ring = conv_state;
@@ -258,19 +284,8 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   ex.xbc0 = r.d_inner;
   ex.d_xbc = r.d_xbc;
   ex.dconv = d.d_conv;
-  if (fuse_in) {
-    ex.act = ACT_RMSNORM;
-    ex.norm_w = L->norm_w;
-    ex.eps = d.eps_in;
-    ex.pdl = 1;
-    if ((e = proj(L->in_proj, hidden, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex)))
-      return launch_status(e);
-  } else {
-    if ((e = launch_rmsnorm(hidden, d.hidden, L->norm_w, xn, d.hidden, B, d.hidden, d.eps_in, stream)))
-      return launch_status(e);
-    if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex)))
-      return launch_status(e);
-  }
+  if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex, us_in, 1)))
+    return launch_status(e);
   // 4+5. split and SSM step (advances conv_pos)
   SsmArgs sa;
   memset(&sa, 0, sizeof(sa));
@@ -293,28 +308,28 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   sa.pos_inc = conv_pos;
   sa.pdl = 1;
   if ((e = launch_ssm_step(sa, stream))) return launch_status(e);
-  // 6+7+8. gated RMSNorm, out_proj, residual add (in place on hidden)
-  GemvArgs eo;
-  memset(&eo, 0, sizeof(eo));
-  if (fuse_out) {
-    eo.act = ACT_GATED;
-    eo.norm_w = L->gnorm_w;
-    eo.eps = d.eps_gated;
-    eo.y = y;
-    eo.ldy = r.d_inner;
-    eo.z = zxu;
-    eo.ldz = r.ldz;
-    eo.group = d.gnorm_group;
-    eo.pdl = 1;
-    if ((e = proj(L->out_proj, nullptr, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, &eo)))
-      return launch_status(e);
-  } else {
-    if ((e = launch_gated_norm(y, r.d_inner, zxu, r.ldz, L->gnorm_w, g, r.d_inner, B, r.d_inner, d.gnorm_group,
-                               d.eps_gated, stream)))
-      return launch_status(e);
-    if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream)))
-      return launch_status(e);
-  }
+  // 6. gated RMSNorm -> GEMV activation
+  memset(&pa, 0, sizeof(pa));
+  pa.mode = PREP_GATED;
+  pa.y = y;
+  pa.ldy = r.d_inner;
+  pa.z = zxu;
+  pa.ldz = r.ldz;
+  pa.w = L->gnorm_w;
+  pa.eps = d.eps_gated;
+  pa.group = d.gnorm_group;
+  pa.M = B;
+  pa.K = r.d_inner;
+  pa.out = g;
+  pa.ldo = r.d_inner;
+  pa.f16 = out_fp8 ? 1 : 0;
+  pa.unscale = us_out;
+  pa.pdl = 1;
+  if ((e = launch_prep(pa, stream))) return launch_status(e);
+  // 7+8. out_proj with the residual add in its epilogue (in place on hidden)
+  if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out,
+                1)))
+    return launch_status(e);
   return M2_OK;
 }
 
@@ -339,9 +354,29 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   o = rup(o + (size_t)T * r.d_inner * 4, 256);
   uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
 
+  o = rup(o + (size_t)T * r.d_inner * 2, 256);
+  float* us_in = reinterpret_cast<float*>(w8 + o);
+  float* us_out = us_in + T;
+
   cudaError_t e;
-  if ((e = launch_rmsnorm(hidden, d.hidden, L->norm_w, xn, d.hidden, T, d.hidden, d.eps_in, stream))) return launch_status(e);
-  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream))) return launch_status(e);
+  const bool in_fp8 = L->in_proj.fmt == M2_W_FP8_BLOCK128;
+  const bool out_fp8 = L->out_proj.fmt == M2_W_FP8_BLOCK128;
+  PrepArgs pa;
+  memset(&pa, 0, sizeof(pa));
+  pa.mode = PREP_RMSNORM;
+  pa.x = hidden;
+  pa.ldx = d.hidden;
+  pa.w = L->norm_w;
+  pa.eps = d.eps_in;
+  pa.M = T;
+  pa.K = d.hidden;
+  pa.out = xn;
+  pa.ldo = d.hidden;
+  pa.f16 = in_fp8 ? 1 : 0;
+  pa.unscale = us_in;
+  if ((e = launch_prep(pa, stream))) return launch_status(e);
+  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream, nullptr, us_in)))
+    return launch_status(e);
   if ((e = launch_conv_prefill(conv_state, conv_pos, zx + r.d_inner, r.ldz, L->conv_w, L->conv_b, u, r.d_xbc, T,
                                r.d_xbc, d.d_conv, stream)))
     return launch_status(e);
@@ -366,10 +401,23 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   sa.G = d.n_groups;
   sa.pos_inc = conv_pos;
   if ((e = launch_ssm_scan_seq(sa, stream))) return launch_status(e);
-  if ((e = launch_gated_norm(y, r.d_inner, zx, r.ldz, L->gnorm_w, g, r.d_inner, T, r.d_inner, d.gnorm_group,
-                             d.eps_gated, stream)))
-    return launch_status(e);
-  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream)))
+  memset(&pa, 0, sizeof(pa));
+  pa.mode = PREP_GATED;
+  pa.y = y;
+  pa.ldy = r.d_inner;
+  pa.z = zx;
+  pa.ldz = r.ldz;
+  pa.w = L->gnorm_w;
+  pa.eps = d.eps_gated;
+  pa.group = d.gnorm_group;
+  pa.M = T;
+  pa.K = r.d_inner;
+  pa.out = g;
+  pa.ldo = r.d_inner;
+  pa.f16 = out_fp8 ? 1 : 0;
+  pa.unscale = us_out;
+  if ((e = launch_prep(pa, stream))) return launch_status(e);
+  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out)))
     return launch_status(e);
   return M2_OK;
 }
@@ -464,7 +512,7 @@ int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint
 
 int m2_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return M2_ERR_LAUNCH;
-  const int parts[] = {status_gemv(clear), status_mixer(clear)};
+  const int parts[] = {status_gemv(clear), status_gemv_mma(clear), status_mixer(clear)};
   for (int v : parts)
     if (v != 0) return v;
   return M2_OK;

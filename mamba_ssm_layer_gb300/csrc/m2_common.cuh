@@ -180,7 +180,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // Programmatic dependent launch: wait until the previous grid in the stream
 // has completed and its writes are visible / let the next grid start early.
-// Both are no-ops for a kernel launched without the PDL attribute.
+// Both are no-ops for a kernel launched without the PDL attribute.  A kernel
+// launched this way may already run while its predecessor writes, so data the
+// predecessor produces must be read with ordinary (coherent) loads after
+// pdl_wait(), never through the non-coherent read-only path (__ldg /
+// ld.global.nc), which requires the data to stay unchanged for the whole
+// lifetime of the reading kernel.  Every kernel here triggers its successor
+// only after its own wait has returned, so at most two consecutive kernels of
+// a chain run at once and a kernel's pre-wait reads can only race with its
+// immediate predecessor.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -12,7 +12,7 @@ namespace m2 {
 
 // Kernel ids for launch counting and tracing (names in m2_abi.cu).
 enum KernelId : int32_t {
-  K_RMSNORM = 0,
+  K_PREP = 0,
   K_GEMV_FP8,        // + GemvEpi: store, conv (in_proj), resid (out_proj)
   K_GEMV_FP8_CONV,
   K_GEMV_FP8_RESID,
@@ -22,7 +22,6 @@ enum KernelId : int32_t {
   K_CONV_UPDATE,
   K_CONV_POS,
   K_SSM_STEP,
-  K_GATED_NORM,
   K_CONV_PREFILL,
   K_SSM_SCAN_SEQ,
   K_GEMM_TC,
@@ -39,6 +38,7 @@ void trace_post(int32_t id, cudaStream_t s);
 // Host readers of each translation unit's device status word (0 or
 // M2_ERR_TIMEOUT); clear != 0 resets it.
 int status_gemv(int clear);
+int status_gemv_mma(int clear);
 int status_mixer(int clear);
 
 // Number of SMs of the current device (cached).
@@ -73,23 +73,45 @@ struct GemvArgs {
   const uint16_t* conv_b;
   int32_t xbc0, d_xbc, dconv;
   int32_t evict_first;  // stream weights with the L2 evict-first policy
-  // Activation prologue (fuses the norm that produces A into the GEMV):
+  // Activation input of the GEMV:
   int32_t act;          // GemvAct
-  const uint16_t* norm_w;  // ACT_RMSNORM: RMSNorm weight [K]; ACT_GATED: gated-norm weight [K]
-  float eps;
-  const float* y;       // ACT_GATED: y [M][ldy] fp32
-  int32_t ldy;
-  const uint16_t* z;    // ACT_GATED: z [M][ldz] bf16
-  int32_t ldz;
-  int32_t group;        // ACT_GATED: norm span (divides K, K/group <= 64)
+  const float* unscale; // ACT_PREPARED: per batch row factor applied to the row totals
   int32_t pdl;          // launch as a programmatic dependent of the previous kernel
 };
 
 enum GemvAct : int32_t {
-  ACT_PLAIN = 0,    // A is the bf16 activation
-  ACT_RMSNORM = 1,  // activation = bf16(A * rsqrt(mean(A^2)+eps) * norm_w)       (A = hidden)
-  ACT_GATED = 2     // activation = bf16(y * rsqrt(mean_group(y^2)+eps) * norm_w * silu(z))
+  ACT_PLAIN = 0,    // A is bf16; for E4M3 weights the kernel finds each row's f16 prescale
+  ACT_PREPARED = 1  // A is already f16 (E4M3 weights: prescaled by 2^j, unscale = 2^-j) or bf16
 };
+
+// Activation preparation (one CTA per batch row): the norm that produces a
+// GEMV's activation, rounded to bf16 at the layer's rounding point, then
+// either stored as bf16 or, for an E4M3-weight GEMV, as f16 after an exact
+// per-row power-of-two prescale 2^j that puts the row maximum in [2^14, 2^15)
+// (unscale[m] = 2^-j).
+enum PrepMode : int32_t {
+  PREP_RMSNORM = 0,  // x * r * w, r = 1/sqrt(mean(x^2) + eps) (input RMSNorm)
+  PREP_GATED = 1     // y * r * w * silu(z), r over groups of `group` (gated RMSNorm)
+};
+struct PrepArgs {
+  int32_t mode;
+  const uint16_t* x;  // PREP_RMSNORM: [M][ldx] bf16
+  int32_t ldx;
+  const float* y;     // PREP_GATED: [M][ldy] fp32
+  int32_t ldy;
+  const uint16_t* z;  // PREP_GATED: [M][ldz] bf16
+  int32_t ldz;
+  const uint16_t* w;  // norm weight [K] bf16
+  float eps;
+  int32_t group;
+  int32_t M, K;
+  uint16_t* out;      // [M][ldo]
+  int32_t ldo;
+  int32_t f16;        // 1: prescaled f16 + unscale; 0: bf16
+  float* unscale;     // [M] (f16 mode)
+  int32_t pdl;
+};
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
 // CUDA-core GEMV (fp32 accumulation) with bulk-copy weight streaming; any M
 // (processed in groups of up to 4 rows, re-streaming the weights per group).
@@ -116,9 +138,6 @@ cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 
 // ------------------------------------------------------------------ mixer ops
 
-cudaError_t launch_rmsnorm(const uint16_t* x, int32_t ldx, const uint16_t* w, uint16_t* out, int32_t ldo,
-                           int32_t M, int32_t K, float eps, cudaStream_t s);
-
 // One-token conv update for B sequences (no pos advance; see launch_conv_pos).
 cudaError_t launch_conv_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, int32_t ldx,
                                const uint16_t* w, const uint16_t* b, uint16_t* out, int32_t ldo, int32_t B,
@@ -143,12 +162,13 @@ struct SsmArgs {
 };
 cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s);
 
-// Largest batch row count one CUDA-core GEMV pass covers for a K-wide row.
+// Largest batch row count one GEMV pass covers for a K-wide row.
 int gemv_rows_per_pass(int K, bool fp8);
 
-cudaError_t launch_gated_norm(const float* y, int32_t ldy, const uint16_t* z, int32_t ldz, const uint16_t* w,
-                              uint16_t* out, int32_t ldo, int32_t M, int32_t d, int32_t group, float eps,
-                              cudaStream_t s);
+// Warp-MMA decode GEMV (k_gemv_mma.cu): M <= 8, K % 64 == 0, K <= 8192.
+bool gemv_mma_supported(int M, int K);
+cudaError_t launch_gemv_mma(const GemvArgs& a, bool fp8, cudaStream_t s);
+
 
 // Prefill conv over T tokens of one sequence: xbc rows ldx apart -> u [T][ldu];
 // reads the ring for the first d_conv-1 taps and leaves it holding the last
