@@ -18,10 +18,11 @@
 // inside a group is permuted identically for A and B, which a dot product
 // allows.  Loads for the next unit of work are issued before the current one
 // is computed (two register buffers), so each warp keeps 8 x 16 B per lane in
-// flight.  Activations (f16 with the exact per-row prescale for E4M3, or bf16)
-// sit in shared memory; E4M3 partials are scaled per 128-element block; each
-// warp adds its 16 x MB tile to the row totals with shared-memory atomics, and
-// all threads run the epilogue at the end.
+// flight, and L2 prefetches run four units further ahead.  Activations (f16
+// with the exact per-row prescale for E4M3, or bf16) sit in shared memory;
+// E4M3 partials are scaled per 128-element block; each warp leaves its 16 x MB
+// tile per row group in shared memory, and at the end all threads add the 16
+// warps' tiles in a fixed order (deterministic) and run the epilogue.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,7 +42,7 @@ struct MmaTail {
 };
 
 struct MmaLayout {
-  int act_ld, tail, act, sc, tot, epi, total;
+  int act_ld, tail, act, tot, epi, total;
 };
 // act_ld: elements per activation row in shared memory (K + 8 pads the rows
 // onto different banks).
@@ -50,10 +51,9 @@ __host__ __device__ inline MmaLayout mma_layout(int K, int rows_max, int mb, int
   L.act_ld = K + 8;
   L.tail = 0;
   L.act = (int)((sizeof(MmaTail) + 127) / 128 * 128);
-  L.sc = L.act + ((mb + 1) * L.act_ld * 2 + 15) / 16 * 16;  // + one zero row for lanes past the batch
-  const int nbs = rows_max / 128 + 2;
-  L.tot = L.sc + (nbs * kb * 4 + 15) / 16 * 16;
-  L.epi = L.tot + (rows_max * mb * 4 + 15) / 16 * 16;
+  L.tot = L.act + ((mb + 1) * L.act_ld * 2 + 15) / 16 * 16;  // + one zero row for lanes past the batch
+  (void)kb;
+  L.epi = L.tot + (rows_max * kMmaWarps * mb * 4 + 15) / 16 * 16;  // per-warp partials
   int epi_bytes = 0;
   if (epi == EPI_INPROJ_CONV) epi_bytes = rows_max * (dconv + 1) * 2 + mb * rows_max * (dconv - 1) * 2;
   if (epi == EPI_RESID) epi_bytes = mb * rows_max * 2;
@@ -114,7 +114,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const MmaLayout lay = mma_layout(a.K, rows_max, MB, kb, a.epi, a.dconv);
   MmaTail* tail = reinterpret_cast<MmaTail*>(smem + lay.tail);
   uint16_t* act_s = reinterpret_cast<uint16_t*>(smem + lay.act);  // [MB + 1][act_ld]
-  float* sc = reinterpret_cast<float*>(smem + lay.sc);
   float* tot = reinterpret_cast<float*>(smem + lay.tot);
   uint8_t* epi_s = smem + lay.epi;
 
@@ -129,7 +128,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int nrows = row_end - row_begin;
   const int nrg = rg_end - rg_begin;
   const int mvalid = min(MB, a.M);
-  const int nb0 = row_begin >> 7;
   const int L = a.dconv - 1;
   // this warp's 64-element groups [q0, q1) of every row, processed in units
   const int ngrp = a.K / 64;
@@ -156,17 +154,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
   };
+  // L2 prefetch of a whole unit (16 rows x the unit's k-range), one bulk
+  // prefetch per row from lanes 0..15: keeps HBM busy beyond the two register
+  // buffers, including while the prologue below waits and stages.
+  auto prefetch_unit = [&](int u) {
+    if (u >= nunit || lane >= kMmaRows) return;
+    const int rg = rg_begin + u / nunit_rg;
+    const int qb = q0 + (u % nunit_rg) * kMmaUnit;
+    const int ng = min(kMmaUnit, q1 - qb);
+    const int r = min(rg * kMmaRows + lane, a.N - 1);
+    const uint8_t* p = W + ((size_t)r * a.K + (size_t)qb * 64) * ES;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)(ng * 64 * ES)) : "memory");
+  };
+  constexpr int kPrefetchUnits = 4;
   WBuf<FP8> buf0, buf1;  // two named buffers: register arrays must be indexed statically
   if (nunit > 0) load_unit(0, buf0);  // weights never depend on the previous kernel
+  for (int u = 1; u <= kPrefetchUnits; ++u) prefetch_unit(u);
 
   // ------------------------------------------------ prologue
   pdl_wait();
   pdl_trigger();
-  for (int i = tid; i < rows_max * MB; i += kMmaThreads) tot[i] = 0.0f;
+  for (int i = tid; i < rows_max * kMmaWarps * MB; i += kMmaThreads) tot[i] = 0.0f;
   if (tid < 8) tail->amax[tid] = 0u;
-  if (FP8)
-    for (int i = tid; i < (((row_end - 1) >> 7) - nb0 + 1) * kb; i += kMmaThreads)
-      sc[i] = bf16_to_f32(__ldg(a.S + (size_t)(nb0 + i / kb) * kb + (i % kb)));
   __syncthreads();
   // activations -> shared memory (coherent loads: written by the previous kernel)
   const int kv = a.K / 8;  // 16-byte vectors per row
@@ -257,8 +266,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           // one 128-element scale block per group; rows g and g+8 may sit in different n-blocks
           const int kbk = q >> 1;
           const int r0 = min(rg * kMmaRows + g, row_end - 1), r8 = min(rg * kMmaRows + g + 8, row_end - 1);
-          const float s0 = sc[((r0 >> 7) - nb0) * kb + kbk];
-          const float s8 = sc[((r8 >> 7) - nb0) * kb + kbk];
+          const float s0 = bf16_to_f32(__ldg(a.S + (size_t)(r0 >> 7) * kb + kbk));  // read-only: L1 hits
+          const float s8 = bf16_to_f32(__ldg(a.S + (size_t)(r8 >> 7) * kb + kbk));
           acc[0] = fmaf(d[0], s0, acc[0]);
           acc[1] = fmaf(d[1], s0, acc[1]);
           acc[2] = fmaf(d[2], s8, acc[2]);
@@ -277,16 +286,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if ((u % nunit_rg) == nunit_rg - 1) {
-      // row group done: add this warp's 16 x MB tile to the row totals
+      // row group done: this warp's 16 x MB tile goes to its own slots; the
+      // epilogue adds the 16 warps in a fixed order (deterministic results)
       const int lr = (rg - rg_begin) * kMmaRows;
       const int c0 = 2 * t, c1 = 2 * t + 1;
+      float* t0 = tot + ((size_t)(lr + g) * kMmaWarps + warp) * MB;
+      float* t8 = tot + ((size_t)(lr + g + 8) * kMmaWarps + warp) * MB;
       if (c0 < MB) {
-        atomicAdd(&tot[(lr + g) * MB + c0], acc[0]);
-        atomicAdd(&tot[(lr + g + 8) * MB + c0], acc[2]);
+        t0[c0] = acc[0];
+        t8[c0] = acc[2];
       }
       if (c1 < MB) {
-        atomicAdd(&tot[(lr + g) * MB + c1], acc[1]);
-        atomicAdd(&tot[(lr + g + 8) * MB + c1], acc[3]);
+        t0[c1] = acc[1];
+        t8[c1] = acc[3];
       }
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
@@ -294,9 +306,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // loads of the next unit are in flight while the current one is computed
   for (int u = 0; u < nunit; u += 2) {
     if (u + 1 < nunit) load_unit(u + 1, buf1);
+    prefetch_unit(u + 1 + kPrefetchUnits);
     process(u, buf0);
     if (u + 1 < nunit) {
       if (u + 2 < nunit) load_unit(u + 2, buf0);
+      prefetch_unit(u + 2 + kPrefetchUnits);
       process(u + 1, buf1);
     }
   }
@@ -308,7 +322,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   for (int i = tid; i < nrows * mvalid; i += kMmaThreads) {
     const int r = i / mvalid, m = i % mvalid;
     const int n = row_begin + r;
-    const float accv = tot[r * MB + m] * tail->unscale[m];
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) sum += tot[((size_t)r * kMmaWarps + w) * MB + m];
+    const float accv = sum * tail->unscale[m];
     uint16_t* o = a.out + (size_t)m * a.ldo + n;
     if (a.epi == EPI_RESID) {
       const float res = bf16_to_f32(reinterpret_cast<const uint16_t*>(epi_s)[m * rows_max + r]);

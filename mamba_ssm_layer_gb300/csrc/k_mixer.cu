@@ -319,11 +319,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   __shared__ double s_rd;
   const int K = a.K;
   float v[kPrepMaxPer];
+  uint4 wv[kPrepMaxPer / 8], zv[kPrepMaxPer / 8];  // issued with the inputs: independent loads
   // element e of this thread: k = (tid + 512 * (e / 8)) * 8 + e % 8
 #pragma unroll
   for (int c = 0; c < kPrepMaxPer / 8; ++c) {
     const int k0 = (tid + kPrepThreads * c) * 8;
     if (k0 < K) {
+      wv[c] = *reinterpret_cast<const uint4*>(a.w + k0);
+      if (a.mode == PREP_GATED) zv[c] = *reinterpret_cast<const uint4*>(a.z + (size_t)m * a.ldz + k0);
       if (a.mode == PREP_RMSNORM) {
         const uint4 u = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.ldx + k0);
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
@@ -339,6 +342,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
         v[c * 8 + 4] = f1.x; v[c * 8 + 5] = f1.y; v[c * 8 + 6] = f1.z; v[c * 8 + 7] = f1.w;
       }
     } else {
+      wv[c] = zv[c] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
     }
@@ -361,7 +365,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
         two_sum_acc(h, l, s_hi[w]);
         l += s_lo[w];
       }
-      const double v = ((double)h + (double)l) / (double)K + (double)a.eps;
+      const double v = ((double)h + (double)l) * a.inv_k + (double)a.eps;
       const double r0 = (double)rsqrtf((float)v);
       s_rd = r0 * (1.5 - 0.5 * v * r0 * r0);
     }
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
     for (int c = 0; c < kPrepMaxPer / 8; ++c) {
       const int k0 = (tid + kPrepThreads * c) * 8;
       if (k0 < K) {
-        const uint4 u = *reinterpret_cast<const uint4*>(a.w + k0);
+        const uint4 u = wv[c];
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -406,8 +410,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       const int k0 = (tid + kPrepThreads * c) * 8;
       if (k0 < K) {
         const float r = 1.0f / sqrtf(gsum[k0 / a.group] / (float)a.group + a.eps);
-        const uint4 u = *reinterpret_cast<const uint4*>(a.w + k0);
-        const uint4 zz = *reinterpret_cast<const uint4*>(a.z + (size_t)m * a.ldz + k0);
+        const uint4 u = wv[c];
+        const uint4 zz = zv[c];
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w}, z4[4] = {zz.x, zz.y, zz.z, zz.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -459,7 +463,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   }
 }
 
-cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s) {
+cudaError_t launch_prep(const PrepArgs& a0, cudaStream_t s) {
+  PrepArgs a = a0;
+  a.inv_k = 1.0 / (double)a.K;
   trace_pre(K_PREP, s);
   cudaError_t e = launch_k(prep_kernel, dim3(a.M), dim3(kPrepThreads), 0, s, a.pdl != 0, a);
   trace_post(K_PREP, s);

@@ -110,6 +110,7 @@ struct PrepArgs {
   int32_t f16;        // 1: prescaled f16 + unscale; 0: bf16
   float* unscale;     // [M] (f16 mode)
   int32_t pdl;
+  double inv_k;       // 1/K (PREP_RMSNORM), so the kernel needs no double division
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 
