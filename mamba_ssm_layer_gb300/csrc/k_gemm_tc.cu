@@ -1,0 +1,432 @@
+// k_gemm_tc.cu -- tensor-core (tcgen05) w8a16 / bf16 GEMM for prefill and
+// batched decode: out[m][n] = sum_k A[m][k] * W~[n][k] for M > 8 token rows.
+//
+// W~ = E4M3(W) * S[n/128][k/128] (page "Struct Qwen3SsmLayer",
+// `set_fp8_decode_weights`; scale index of "Struct NemotronMamba2Layer",
+// `set_fp8_weights`), or bf16 W.  tcgen05 has no bf16 x E4M3 MMA and E4M3
+// activations would change the numbers, so the weight tile is converted
+// E4M3 -> bf16 exactly (every E4M3 value is a bf16 value) in shared memory and
+// multiplied by the bf16 activations with kind::f16 (fp32 accumulation in
+// TMEM).  The 128x128 block scale is not a power of two and varies with the k
+// block, so it cannot ride on the MMA: each 128-wide k block is accumulated
+// alone into a TMEM buffer and the epilogue promotes it, acc += s * partial.
+//
+// The MMA computes D^T: UMMA M = 128 weight rows (one scale row block), UMMA N
+// = NT token rows, so one tile is [128 weight rows] x [NT tokens].
+// Persistent CTAs walk tiles n-major (all token tiles of a weight tile are
+// adjacent, so the E4M3 tile is re-read from L2, not HBM).  Warp roles:
+//   warp 0      TMA producer: E4M3 weight tile [128][128] (plain 2-D map) into
+//               a 4-stage ring; bf16 activation tile [NT][128] (two 64-wide
+//               boxes, 128-byte swizzle = the UMMA K-major canonical layout)
+//               into a 2-stage ring;
+//   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each) per k block
+//               into TMEM buffer (k block & 1) and commits to an mbarrier;
+//   warps 2-5   converters: E4M3 tile -> bf16 tile in the 128-byte-swizzled
+//               K-major layout the MMA descriptor expects;
+//   warps 6-9   epilogue: per k block, TMEM -> registers, acc += s * partial;
+//               per tile, the store / residual / conv-update epilogue.
+// Every wait is bounded (see mbar_wait); TMEM is freed on every exit path.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "m2_common.cuh"
+#include "m2_kernels.h"
+
+namespace m2 {
+
+constexpr int kTcThreads = 320;
+constexpr int kTcW8Stages = 4;
+constexpr int kTcBM = 128;  // weight rows per tile (UMMA M)
+constexpr int kTcBK = 128;  // k per block (= scale block)
+
+struct TcBars {
+  uint64_t w8_full[kTcW8Stages], w8_empty[kTcW8Stages];
+  uint64_t wbf_full[2], a_full[2], mma_done[2], tmem_empty[2];
+  uint32_t tmem_base;
+};
+
+template <int NT>
+struct TcLayout {
+  // offsets from a 1024-byte aligned base
+  static constexpr int kW8 = 0;                                   // 4 x 16 KB raw E4M3
+  static constexpr int kWbf = kW8 + kTcW8Stages * kTcBM * kTcBK;  // 2 x 32 KB bf16, swizzled
+  static constexpr int kA = kWbf + 2 * kTcBM * kTcBK * 2;         // 2 x NT*256 B bf16, swizzled
+  static constexpr int kBars = kA + 2 * NT * kTcBK * 2;
+  static constexpr int kTotal = kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
+};
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// K-major operand descriptor, 128-byte swizzle: rows of 128 bytes, 8-row atoms
+// 1024 bytes apart (stride byte offset), leading byte offset unused.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive fp32 columns of TMEM into registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Two E4M3 -> two bf16, exactly (E4M3 -> f16 -> f32 -> bf16 are all exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+  float lo, hi;
+  asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+  return pack_bf16x2(lo, hi);
+}
+
+// ------------------------------------------------------------------ kernel
+
+struct TcArgs {
+  GemvArgs g;      // operand pointers, sizes, epilogue
+  int32_t m_tiles, n_tiles, kblocks;
+  int32_t fp8;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, const TcArgs ta) {
+  using Lay = TcLayout<NT>;
+  const GemvArgs& a = ta.g;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  TcBars* bars = reinterpret_cast<TcBars*>(smem + Lay::kBars);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntiles = ta.m_tiles * ta.n_tiles;
+  const int KB = ta.kblocks;
+  const int L = a.dconv - 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTcW8Stages; ++s) {
+      mbar_init(&bars->w8_full[s], 1);
+      mbar_init(&bars->w8_empty[s], 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->wbf_full[b], 4);
+      mbar_init(&bars->a_full[b], 1);
+      mbar_init(&bars->mma_done[b], 1);
+      mbar_init(&bars->tmem_empty[b], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    // 2 x NT fp32 columns of TMEM (a power of two >= 32)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&bars->tmem_base)),
+                 "r"(2 * NT));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  bool dead = false;
+
+  if (warp == 0) {
+    // -------------------------------------------------------- TMA producer
+    pdl_wait();
+    if (lane == 0) {
+      const uint64_t polw = policy_evict_normal();  // weight tiles are re-read by the token tiles
+      const uint64_t pola = policy_evict_last();    // activations are re-read by every weight tile
+      int gk = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
+        const int nt = tile / ta.m_tiles, mt = tile % ta.m_tiles;
+        for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
+          const int s8 = gk % kTcW8Stages, b = gk & 1;
+          if (ta.fp8) {
+            if (gk >= kTcW8Stages && !mbar_wait(&bars->w8_empty[s8], ((gk / kTcW8Stages) - 1) & 1)) dead = true;
+            if (dead) break;
+            mbar_arrive_expect_tx(&bars->w8_full[s8], kTcBM * kTcBK);
+            tma_load_2d(smem + Lay::kW8 + s8 * kTcBM * kTcBK, &tmW, kb * kTcBK, nt * kTcBM, &bars->w8_full[s8], polw);
+          }
+          if (gk >= 2 && !mbar_wait(&bars->mma_done[b], ((gk / 2) - 1) & 1)) dead = true;
+          if (dead) break;
+          uint8_t* abuf = smem + Lay::kA + b * NT * kTcBK * 2;
+          if (ta.fp8) {
+            mbar_arrive_expect_tx(&bars->a_full[b], NT * kTcBK * 2);
+          } else {
+            // bf16 weights go straight into the swizzled weight buffer (no conversion)
+            mbar_arrive_expect_tx(&bars->a_full[b], NT * kTcBK * 2 + kTcBM * kTcBK * 2);
+            uint8_t* wbuf = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
+            tma_load_2d(wbuf, &tmW, kb * kTcBK, nt * kTcBM, &bars->a_full[b], polw);
+            tma_load_2d(wbuf + kTcBM * 128, &tmW, kb * kTcBK + 64, nt * kTcBM, &bars->a_full[b], polw);
+          }
+          tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[b], pola);
+          tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[b], pola);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc_idesc(kTcBM, NT);
+      int gk = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
+        for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
+          const int b = gk & 1;
+          if (ta.fp8 && !mbar_wait(&bars->wbf_full[b], (gk / 2) & 1)) dead = true;
+          if (!dead && !mbar_wait(&bars->a_full[b], (gk / 2) & 1)) dead = true;
+          if (!dead && gk >= 2 && !mbar_wait(&bars->tmem_empty[b], ((gk / 2) - 1) & 1)) dead = true;
+          if (dead) break;
+          tc_fence_after();
+          const uint32_t wb = smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2);
+          const uint32_t ab = smem_addr(smem + Lay::kA + b * NT * kTcBK * 2);
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const int atom = kk >> 2, within = (kk & 3) * 32;  // 64-k atoms of 128 bytes per row
+            const uint64_t ad = sw128_desc(wb + atom * kTcBM * 128 + within);
+            const uint64_t bd = sw128_desc(ab + atom * NT * 128 + within);
+            tc_mma(tmem + b * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
+          }
+          tc_commit(&bars->mma_done[b]);
+        }
+      }
+    }
+  } else if (warp < 6) {
+    // -------------------------------------------------------- converters
+    if (ta.fp8) {
+      const int ct = tid - 64;  // 0..127
+      int gk = 0;
+      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
+        for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
+          const int s8 = gk % kTcW8Stages, b = gk & 1;
+          if (!mbar_wait(&bars->w8_full[s8], (gk / kTcW8Stages) & 1)) dead = true;
+          if (!dead && gk >= 2 && !mbar_wait(&bars->mma_done[b], ((gk / 2) - 1) & 1)) dead = true;
+          if (dead) break;
+          const uint8_t* raw = smem + Lay::kW8 + s8 * kTcBM * kTcBK;
+          uint8_t* dst = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
+#pragma unroll 2
+          for (int i = 0; i < 8; ++i) {
+            const int id = ct + 128 * i;
+            const int row = id >> 3, j = id & 7;  // 16-byte chunk j of the row: k = 16j .. 16j+15
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kTcBK + 16 * j);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint4 o0, o1;
+            o0.x = e4m3x2_to_bf16x2(w4[0]);
+            o0.y = e4m3x2_to_bf16x2(w4[0] >> 16);
+            o0.z = e4m3x2_to_bf16x2(w4[1]);
+            o0.w = e4m3x2_to_bf16x2(w4[1] >> 16);
+            o1.x = e4m3x2_to_bf16x2(w4[2]);
+            o1.y = e4m3x2_to_bf16x2(w4[2] >> 16);
+            o1.z = e4m3x2_to_bf16x2(w4[3]);
+            o1.w = e4m3x2_to_bf16x2(w4[3] >> 16);
+            // bf16 chunks c, c+1 (8 elements each) of atom j/4, 128-byte swizzle
+            const int atom = j >> 2, c = (j & 3) * 2, r8 = row & 7;
+            uint8_t* base = dst + atom * kTcBM * 128 + row * 128;
+            *reinterpret_cast<uint4*>(base + ((c ^ r8) << 4)) = o0;
+            *reinterpret_cast<uint4*>(base + (((c + 1) ^ r8) << 4)) = o1;
+          }
+          fence_proxy_async();  // generic-proxy stores -> visible to the MMA (async proxy)
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->wbf_full[b]);
+            mbar_arrive(&bars->w8_empty[s8]);
+          }
+        }
+      }
+    }
+  } else {
+    // -------------------------------------------------------- epilogue
+    const int q = warp & 3;       // TMEM lane quarter of this warp
+    const int row = 32 * q + lane;  // weight row within the tile
+    pdl_wait();
+    float acc[NT];
+    int gk = 0;
+    for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
+      const int nt = tile / ta.m_tiles, mt = tile % ta.m_tiles;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
+        const int b = gk & 1;
+        const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * KB + kb)) : 1.0f;
+        if (!mbar_wait(&bars->mma_done[b], (gk / 2) & 1)) dead = true;
+        if (dead) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < NT / 32; ++c) {
+          float v[32];
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + b * NT + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, v[i], acc[c * 32 + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->tmem_empty[b]);
+      }
+      if (dead) break;
+      // tile epilogue: row n of the weights, token columns m
+      const int n = nt * kTcBM + row;
+      if (n < a.N) {
+        const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
+        float cw[9];
+        uint16_t cb = 0;
+        if (conv) {
+          const int c = n - a.xbc0;
+          for (int j = 0; j < a.dconv; ++j) cw[j] = bf16_to_f32(a.conv_w[(size_t)c * a.dconv + j]);
+          cb = a.conv_b ? a.conv_b[c] : (uint16_t)0;
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const int m = mt * NT + j;
+          if (m < a.M) {
+            uint16_t* o = a.out + (size_t)m * a.ldo + n;
+            if (a.epi == EPI_RESID) {
+              *o = f32_to_bf16(bf16_to_f32(a.resid[(size_t)m * a.ldr + n]) + acc[j]);
+            } else if (conv) {
+              // decode batch row m: conv1d update with bias + SiLU for channel c
+              const uint16_t vb = f32_to_bf16(acc[j]);
+              const int c = n - a.xbc0;
+              uint16_t* rg = a.ring + (size_t)m * L * a.d_xbc;
+              const int p = a.pos[m];
+              float sv = bf16_to_f32(cb);
+              for (int t2 = 0; t2 < L; ++t2) sv += cw[t2] * bf16_to_f32(rg[(size_t)((p + t2) % L) * a.d_xbc + c]);
+              sv += cw[L] * bf16_to_f32(vb);
+              *o = f32_to_bf16(silu_f(sv));
+              rg[(size_t)(p % L) * a.d_xbc + c] = vb;
+            } else {
+              *o = f32_to_bf16(acc[j]);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  pdl_trigger();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * NT));
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gemm_tc_supported(int M, int N, int K, bool fp8) {
+  (void)N;
+  (void)fp8;
+  return M > 8 && K % 16 == 0;
+}
+
+template <int NT>
+static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
+  static int done_mask[64] = {0};
+  CUtensorMap tmW, tmA;
+  if (fp8) {
+    if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.W, g.K, g.N, (uint64_t)g.K, kTcBK, kTcBM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+  } else {
+    if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.W, g.K, g.N, (uint64_t)g.K * 2, 64, kTcBM,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64, NT,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  TcArgs ta;
+  ta.g = g;
+  ta.m_tiles = (g.M + NT - 1) / NT;
+  ta.n_tiles = (g.N + kTcBM - 1) / kTcBM;
+  ta.kblocks = (g.K + kTcBK - 1) / kTcBK;
+  ta.fp8 = fp8 ? 1 : 0;
+  const int smem = TcLayout<NT>::kTotal;
+  auto kern = gemm_tc_kernel<NT>;
+  cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
+  if (e != cudaSuccess) return e;
+  int grid = num_sms();
+  const int ntiles = ta.m_tiles * ta.n_tiles;
+  if (grid > ntiles) grid = ntiles;
+  trace_pre(K_GEMM_TC, s);
+  e = launch_k(kern, dim3(grid), dim3(kTcThreads), smem, s, g.pdl != 0, tmW, tmA, ta);
+  trace_post(K_GEMM_TC, s);
+  return e;
+}
+
+cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
+  if (g.M <= 64) return launch_tc<64>(g, fp8, s);
+  return launch_tc<128>(g, fp8, s);
+}
+
+int status_gemm_tc(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
+  if (clear) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
+  }
+  return v;
+}
+
+}  // namespace m2

@@ -489,6 +489,8 @@ static int launch_group(const GemvArgs& a, int m0, cudaStream_t s, cudaError_t* 
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s) {
+  // more than 8 rows: the tcgen05 tensor-core GEMM (k_gemm_tc.cu)
+  if (gemm_tc_supported(a.M, a.N, a.K, fp8)) return launch_gemm_tc(a, fp8, s);
   // batches of up to 8 rows with K % 64 == 0, K <= 8192: one weight pass on
   // the warp-MMA GEMV (k_gemv_mma.cu)
   if (gemv_mma_supported(a.M, a.K)) return launch_gemv_mma(a, fp8, s);

@@ -155,6 +155,12 @@ static size_t prefill_ws(const m2_dims& d, int T) {
   return o;
 }
 
+// Whether a projection over M rows consumes f16 prescaled activations (the
+// E4M3 GEMV paths, M <= 8) or bf16 ones (bf16 weights, or the tensor-core GEMM).
+static bool proj_f16(const m2_weight& w, int M) {
+  return w.fmt == M2_W_FP8_BLOCK128 && !gemm_tc_supported(M, w.n, w.k, true);
+}
+
 static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
                         GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr,
                         const float* unscale = nullptr, int pdl = 0) {
@@ -173,7 +179,8 @@ static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, u
   a.epi = epi;
   a.resid = resid;
   a.ldr = ldr;
-  a.act = unscale ? ACT_PREPARED : ACT_PLAIN;
+  // prepared f16 rows carry a prescale; prepared bf16 rows are plain bf16
+  a.act = (unscale && proj_f16(w, M)) ? ACT_PREPARED : ACT_PLAIN;
   a.unscale = unscale;
   a.pdl = pdl;
   const int rowbytes = w.k * (w.fmt == M2_W_FP8_BLOCK128 ? 1 : 2);
@@ -254,8 +261,6 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   float* us_out = us_in + B;
 
   cudaError_t e;
-  const bool in_fp8 = L->in_proj.fmt == M2_W_FP8_BLOCK128;
-  const bool out_fp8 = L->out_proj.fmt == M2_W_FP8_BLOCK128;
   // Five kernels, each launched as a programmatic dependent of the previous
   // one, so that a GEMV streams its weights while its predecessor drains.
   // 1. input RMSNorm -> GEMV activation
@@ -270,7 +275,7 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   pa.K = d.hidden;
   pa.out = xn;
   pa.ldo = d.hidden;
-  pa.f16 = in_fp8 ? 1 : 0;
+  pa.f16 = proj_f16(L->in_proj, B) ? 1 : 0;
   pa.unscale = us_in;
   pa.pdl = 1;
   if ((e = launch_prep(pa, stream))) return launch_status(e);
@@ -322,7 +327,7 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   pa.K = r.d_inner;
   pa.out = g;
   pa.ldo = r.d_inner;
-  pa.f16 = out_fp8 ? 1 : 0;
+  pa.f16 = proj_f16(L->out_proj, B) ? 1 : 0;
   pa.unscale = us_out;
   pa.pdl = 1;
   if ((e = launch_prep(pa, stream))) return launch_status(e);
@@ -359,8 +364,6 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   float* us_out = us_in + T;
 
   cudaError_t e;
-  const bool in_fp8 = L->in_proj.fmt == M2_W_FP8_BLOCK128;
-  const bool out_fp8 = L->out_proj.fmt == M2_W_FP8_BLOCK128;
   PrepArgs pa;
   memset(&pa, 0, sizeof(pa));
   pa.mode = PREP_RMSNORM;
@@ -372,7 +375,7 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   pa.K = d.hidden;
   pa.out = xn;
   pa.ldo = d.hidden;
-  pa.f16 = in_fp8 ? 1 : 0;
+  pa.f16 = proj_f16(L->in_proj, T) ? 1 : 0;
   pa.unscale = us_in;
   if ((e = launch_prep(pa, stream))) return launch_status(e);
   if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream, nullptr, us_in)))
@@ -414,7 +417,7 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   pa.K = r.d_inner;
   pa.out = g;
   pa.ldo = r.d_inner;
-  pa.f16 = out_fp8 ? 1 : 0;
+  pa.f16 = proj_f16(L->out_proj, T) ? 1 : 0;
   pa.unscale = us_out;
   if ((e = launch_prep(pa, stream))) return launch_status(e);
   if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out)))
@@ -512,7 +515,7 @@ int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint
 
 int m2_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return M2_ERR_LAUNCH;
-  const int parts[] = {status_gemv(clear), status_gemv_mma(clear), status_mixer(clear)};
+  const int parts[] = {status_gemv(clear), status_gemv_mma(clear), status_gemm_tc(clear), status_mixer(clear)};
   for (int v : parts)
     if (v != 0) return v;
   return M2_OK;

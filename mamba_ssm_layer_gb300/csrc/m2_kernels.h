@@ -39,6 +39,7 @@ void trace_post(int32_t id, cudaStream_t s);
 // M2_ERR_TIMEOUT); clear != 0 resets it.
 int status_gemv(int clear);
 int status_gemv_mma(int clear);
+int status_gemm_tc(int clear);
 int status_mixer(int clear);
 
 // Number of SMs of the current device (cached).
@@ -165,6 +166,10 @@ cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s);
 
 // Largest batch row count one GEMV pass covers for a K-wide row.
 int gemv_rows_per_pass(int K, bool fp8);
+
+// tcgen05 GEMM (k_gemm_tc.cu) for M > 8 rows: bf16 activations (ACT_PLAIN).
+bool gemm_tc_supported(int M, int N, int K, bool fp8);
+cudaError_t launch_gemm_tc(const GemvArgs& a, bool fp8, cudaStream_t s);
 
 // Warp-MMA decode GEMV (k_gemv_mma.cu): M <= 8, K % 64 == 0, K <= 8192.
 bool gemv_mma_supported(int M, int K);

@@ -105,7 +105,7 @@ class FlipTracker:
         o3 = orc.f64_array_to_bf16(e3)
         idx3, ok3 = legit_flips(g3, e3, o3, a3)
         self.n_r3 += idx3.size
-        self.bad += [("R3", int(i)) for i in idx3[~ok3]]
+        self.bad += [("R3", int(i), int(g3[i]), int(o3[i]), float(e3[i]), float(a3[i])) for i in idx3[~ok3]]
         # the conv consumes the xBC codes of this and the previous L tokens;
         # a difference there propagates as sum_j |w_j| * |dx_j| (SiLU' <= 1.1)
         dxc = np.abs(bf16_to_f64(g3[di:di + dx]) - bf16_to_f64(o3[di:di + dx]))
@@ -121,7 +121,7 @@ class FlipTracker:
             gv = bf16_to_f64(g4[i:i + 1])[0]
             half_ulp = 0.5 * float(np.spacing(np.float32(abs(gv)))) * 65536.0
             if abs(gv - e4[i]) > half_ulp + FLIP_REL * max(a4[i], abs(e4[i])) + prop[i]:
-                self.bad.append(("R4", int(i)))
+                self.bad.append(("R4", int(i), int(g4[i]), int(o4[i]), float(e4[i]), float(prop[i])))
         # heads whose state inputs differ this token
         u_diff = set(int(i) for i in idx4)
         r3_diff = set(int(i) for i in idx3)

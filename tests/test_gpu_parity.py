@@ -38,7 +38,7 @@ def _rand_fp8(N, K, seed):
     return synth.quantize_fp8_block128((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
 
 
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 16, 70])
 def test_gemv_one_hot_is_bit_exact(M):
     # one-hot activations with power-of-two scales: out = E4M3(W[n,k]) * S exactly
     N, K = 300, 448
@@ -62,7 +62,9 @@ def test_gemv_one_hot_is_bit_exact(M):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 552, 256), (3, 300, 448), (1, 18560, 4096), (2, 4096, 8192),
-                                   (5, 1000, 4096), (4, 129, 16384)])
+                                   (5, 1000, 4096), (4, 129, 16384),
+                                   # tensor-core GEMM (M > 8): ragged M / N / K tiles
+                                   (9, 300, 448), (64, 552, 256), (130, 1000, 4096), (200, 256, 8192)])
 def test_gemv_matches_oracle(M, N, K):
     W, S = _rand_fp8(N, K, N + K)
     A = synth.to_bf16_bits(np.random.default_rng(M).standard_normal((M, K)))
@@ -328,3 +330,26 @@ def test_prefill_split_equals_whole():
 def test_prefill_8b_layer_1024_tokens():
     lay = synth.make_layer(synth.NEMOTRON_H_8B, synth.WL_8B_PREFILL_1K)
     _prefill_case(lay, 1024, 0, (synth.WL_8B_PREFILL_1K, 0))
+
+
+# ------------------------------------------------------------------ bf16 weights
+
+def _bf16_layer():
+    return synth.make_layer(synth.TINY, synth.WL_TINY_DECODE, layer=2, in_fmt="bf16", out_fmt="bf16")
+
+
+@pytest.mark.parametrize("B", [1, 5, 16])
+def test_decode_tiny_bf16_weights(B):
+    # the unquantised projections of a mixed-precision checkpoint: warp-MMA GEMV
+    # for B <= 8, tensor-core GEMM above
+    _run_decode(_bf16_layer(), B, 6, sorted({0, B - 1}), (synth.WL_TINY_DECODE, 31))
+
+
+@pytest.mark.parametrize("T", [7, 129])
+def test_prefill_tiny_bf16_weights(T):
+    _prefill_case(_bf16_layer(), T, 2, (synth.WL_TINY_DECODE, 32))
+
+
+def test_decode_tiny_b16_tensor_core_path():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    _run_decode(lay, 16, 5, [0, 9, 15], (synth.WL_TINY_DECODE, 33))
