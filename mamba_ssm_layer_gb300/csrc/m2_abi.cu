@@ -152,6 +152,8 @@ static size_t prefill_ws(const m2_dims& d, int T) {
   o = rup(o + (size_t)T * r.d_inner * 4, 256);  // y
   o = rup(o + (size_t)T * r.d_inner * 2, 256);  // g
   o = rup(o + (size_t)2 * T * 4, 256);          // unscale
+  if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups))
+    o += ssd_workspace_bytes(T, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
   return o;
 }
 
@@ -383,27 +385,55 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   if ((e = launch_conv_prefill(conv_state, conv_pos, zx + r.d_inner, r.ldz, L->conv_w, L->conv_b, u, r.d_xbc, T,
                                r.d_xbc, d.d_conv, stream)))
     return launch_status(e);
-  ScanArgs sa;
-  memset(&sa, 0, sizeof(sa));
-  sa.h = ssm_state;
-  sa.x = u;
-  sa.Bm = u + r.d_inner;
-  sa.Cm = u + r.d_inner + d.n_groups * d.d_state;
-  sa.dt = zx + r.d_inner + r.d_xbc;
-  sa.ld_in = r.d_xbc;
-  sa.ld_dt = r.ldz;
-  sa.A_log = L->A_log;
-  sa.D = L->D;
-  sa.dt_bias = L->dt_bias;
-  sa.y = y;
-  sa.ldy = r.d_inner;
-  sa.T = T;
-  sa.H = d.nheads;
-  sa.P = d.head_dim;
-  sa.N = d.d_state;
-  sa.G = d.n_groups;
-  sa.pos_inc = conv_pos;
-  if ((e = launch_ssm_scan_seq(sa, stream))) return launch_status(e);
+  if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups)) {
+    SsdArgs sa;
+    memset(&sa, 0, sizeof(sa));
+    sa.h = ssm_state;
+    sa.x = u;
+    sa.Bm = u + r.d_inner;
+    sa.Cm = u + r.d_inner + d.n_groups * d.d_state;
+    sa.dt = zx + r.d_inner + r.d_xbc;
+    sa.ld_in = r.d_xbc;
+    sa.ld_dt = r.ldz;
+    sa.A_log = L->A_log;
+    sa.D = L->D;
+    sa.dt_bias = L->dt_bias;
+    sa.y = y;
+    sa.ldy = r.d_inner;
+    sa.T = T;
+    sa.H = d.nheads;
+    sa.P = d.head_dim;
+    sa.N = d.d_state;
+    sa.G = d.n_groups;
+    sa.pos_inc = conv_pos;
+    o = rup(o + (size_t)2 * T * 4, 256);
+    sa.dH = reinterpret_cast<float*>(w8 + o);
+    const size_t nc = (size_t)(T + 127) / 128;
+    sa.decay = reinterpret_cast<float*>(w8 + rup(o + nc * d.nheads * d.head_dim * d.d_state * 4, 256));
+    if ((e = launch_ssd(sa, stream))) return launch_status(e);
+  } else {
+    ScanArgs sa;
+    memset(&sa, 0, sizeof(sa));
+    sa.h = ssm_state;
+    sa.x = u;
+    sa.Bm = u + r.d_inner;
+    sa.Cm = u + r.d_inner + d.n_groups * d.d_state;
+    sa.dt = zx + r.d_inner + r.d_xbc;
+    sa.ld_in = r.d_xbc;
+    sa.ld_dt = r.ldz;
+    sa.A_log = L->A_log;
+    sa.D = L->D;
+    sa.dt_bias = L->dt_bias;
+    sa.y = y;
+    sa.ldy = r.d_inner;
+    sa.T = T;
+    sa.H = d.nheads;
+    sa.P = d.head_dim;
+    sa.N = d.d_state;
+    sa.G = d.n_groups;
+    sa.pos_inc = conv_pos;
+    if ((e = launch_ssm_scan_seq(sa, stream))) return launch_status(e);
+  }
   memset(&pa, 0, sizeof(pa));
   pa.mode = PREP_GATED;
   pa.y = y;

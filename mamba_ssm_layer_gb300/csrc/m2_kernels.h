@@ -201,4 +201,28 @@ struct ScanArgs {
 };
 cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s);
 
+// Chunked (state-space dual) scan of one sequence, chunk length 128
+// (k_ssd.cu): chunk states, a sequential pass over chunk states, chunk outputs.
+struct SsdArgs {
+  float* h;            // [H][P][N], updated in place
+  const uint16_t* x;   // [T] rows ld_in apart
+  const uint16_t* Bm;
+  const uint16_t* Cm;
+  const uint16_t* dt;  // [T] rows ld_dt apart
+  int32_t ld_in, ld_dt;
+  const float* A_log;
+  const float* D;
+  const float* dt_bias;
+  float* y;            // [T][ldy]
+  int32_t ldy;
+  int32_t T, H, P, N, G;
+  int32_t* pos_inc;    // pos_inc[0] += T if non-null
+  float* dH;           // scratch [H][ceil(T/128)][P][N]
+  float* decay;        // scratch [H][ceil(T/128)]
+  int32_t nchunks;     // set by launch_ssd
+};
+bool ssd_supported(int H, int P, int N, int G);
+size_t ssd_workspace_bytes(int T, int H, int P, int N);  // dH then decay, each 256-aligned
+cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t s);
+
 }  // namespace m2
