@@ -71,6 +71,51 @@ def inproj_bytes(d, B):
             + B * d_xbc * 2 * d["d_conv"] + d_xbc * (d["d_conv"] + 1) * 2)
 
 
+def sources_sha256(paths) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    ncu capture recorded in profiles/traffic.txt, or None when there is none or
+    the kernel's sources changed since it was taken (the line stores their
+    sha256)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) != 5 or line.startswith("#") or f[0] != kernel or f[1] != workload:
+            continue
+        try:
+            if sources_sha256(f[3].split(",")) == f[4]:
+                return float(f[2])
+        except OSError:
+            return None
+    return None
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """Max of a per-rank scalar over all ranks (all-reduce MAX); x itself at world 1."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -211,13 +256,6 @@ def main():
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     d = synth.NEMOTRON_H_8B
     B = 1
     lay = synth.make_layer(d, synth.WL_8B_DECODE_B1)
@@ -256,9 +294,9 @@ def main():
     barrier()
     torch.cuda.synchronize()
     launches = abi.m2_launch_count() - launches0
-    ms = max_over_ranks(e0.elapsed_time(e1))
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_step = ms / K
-    value = world * K * B / (ms / 1e3)
+    value = job_rate(K * B, world, ms)
 
     # per-kernel device time of the same steps, from the library's event trace
     # (events between launches serialise them; these are per-launch durations)
@@ -274,7 +312,7 @@ def main():
     if tr_in:
         achieved = in_bytes / (tr_in / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": None, "kernel": "gemv_fp8 (in_proj, conv1d fused)", "bytes_per_launch": in_bytes,
+                "traffic": captured_traffic("gemv_fp8_inproj_conv", "decode_b1"), "kernel": "gemv_fp8 (in_proj, conv1d fused)", "bytes_per_launch": in_bytes,
                 "launch_us": tr_in * 1e3, "peak_source": f"{peak_src} hbm_gbs"}
 
     out = {
@@ -297,6 +335,7 @@ def main():
     if not args.no_extras:
         out["decode_b64"] = _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, 8 if args.quick else 32)
         out["prefill_1k"] = _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, 2 if args.quick else 5)
+        out["stack8"] = _bench_stack8(torch, synth, to_dev)
         out["e2e"] = _bench_e2e(torch, synth, reps, ws, d, B, min(K, 100))
         if rank == 0:
             v, n, dt, cores = oracle_decode_rate(4.0 if args.quick else 15.0)
@@ -373,6 +412,46 @@ def _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, reps):
     tr = abi.trace_end()
     return {"value": T / (ms / 1e3), "unit": "tokens/s", "ms_per_prefill": ms, "tokens": T,
             "kernels_ms": {k: v[0] for k, v in tr.items()}}
+
+
+def _bench_stack8(torch, synth, to_dev):
+    """Eight-layer stack (layers 2 and 5 BF16): 16 prompts of 64..512 tokens
+    prefilled one sequence at a time through all layers, then 256 decode steps of
+    all 16 sequences.  Inputs (prompts and the per-step decode rows) are
+    resident on the device before the timed region; the stack's 1.1 GB of
+    weights and 0.5 GB of states exceed L2.  Timed once after an untimed run."""
+    from mamba_ssm_layer_gb300.stack import DeviceStack
+    spec, d = synth.STACK8, synth.NEMOTRON_H_8B
+    hid = d["hidden"]
+    lens = synth.stack_prompt_lengths(spec)
+    S, steps = spec["n_seqs"], spec["decode_steps"]
+    stk = DeviceStack(synth.stack_layers(d, spec))
+    ws = stk.workspace(S, int(lens.max()))
+    prompts = [to_dev(synth.stack_prompt(s, int(lens[s]), hid)) for s in range(S)]
+    rows = to_dev(np.stack([synth.stack_decode_rows(k, S, hid) for k in range(steps)]))
+    res = {}
+    for rep in range(2):
+        st = stk.new_state(S)
+        xs = [p.clone() for p in prompts]
+        rw = rows.clone()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        for s in range(S):
+            stk.prefill(xs[s], st, s, ws)
+        ev[1].record()
+        for k in range(steps):
+            stk.decode(rw[k], st, ws)
+        ev[2].record()
+        torch.cuda.synchronize()
+        pre, dec = ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+        ntok = int(lens.sum()) + S * steps
+        res = {"value": ntok / ((pre + dec) / 1e3), "unit": "tokens/s", "ms_total": pre + dec,
+               "prefill_tokens_per_s": int(lens.sum()) / (pre / 1e3), "prefill_ms": pre,
+               "decode_tokens_per_s": S * steps / (dec / 1e3), "decode_ms": dec,
+               "decode_ms_per_step": dec / steps, "prompt_tokens": int(lens.sum()), "seqs": S,
+               "decode_steps": steps, "layers": spec["n_layers"], "bf16_layers": list(spec["bf16_layers"])}
+    return res
 
 
 def _bench_e2e(torch, synth, reps, ws, d, B, K):

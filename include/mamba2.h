@@ -130,7 +130,10 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* layer, uint16_t* hi
 
 /* Prefill of T tokens of ONE sequence (page "Trait TransformerLayer",
  * `prefill`: projections as GEMMs over the T tokens; the result equals T
- * sequential decode steps).  hidden [T][hidden] bf16 in/out; ssm_state
+ * sequential decode steps).  The recurrence runs as the chunked
+ * state-space-dual scan with 128-token chunks (source listing kernel table,
+ * "SSD chunked prefill scan"): only chunk states are carried serially.
+ * hidden [T][hidden] bf16 in/out; ssm_state
  * [nheads][head_dim][d_state] fp32, conv_state [d_conv-1][d_xbc] bf16 and
  * conv_pos [1] int32 are the sequence's state before the block and are left
  * as the state after it (conv_pos += T).  ws: m2_workspace_bytes(dims, 0, T). */

@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   const int m = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float s_hi[16], s_lo[16], s_max[16];
-  __shared__ float gsum[1024];
+  __shared__ float part[kPrepThreads * kPrepMaxPer / 8];  // gated mode: per-run sums of squares
   __shared__ double s_rd;
   const int K = a.K;
   float v[kPrepMaxPer];
@@ -386,30 +386,58 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       }
     }
   } else {
-    const int ngroups = K / a.group;
-    for (int i = tid; i < ngroups; i += kPrepThreads) gsum[i] = 0.0f;
-    __syncthreads();
+    // sum of squares per group in a fixed order (results do not depend on
+    // scheduling, so equal rows give equal outputs): each run of 8 elements
+    // in sequence, then either warp butterflies and the warps' chunks of 256
+    // in index order (group % 256 == 0), or a pairwise tree over the runs of
+    // each group
+    const int nrun = K / 8;  // runs of 8 in the row; a run never straddles a group (group % 16 == 0)
+    float ssr[kPrepMaxPer / 8];
 #pragma unroll
     for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-      const int k0 = (tid + kPrepThreads * c) * 8;
       float ss = 0.0f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
-      if (a.group % 256 == 0) {
-        // a warp's 256 consecutive elements lie in one group: reduce, then one atomic
-        ss = warp_sum(ss);
-        const int kw = (warp * 32 + kPrepThreads * c) * 8;
-        if (lane == 0 && kw < K) atomicAdd(&gsum[kw / a.group], ss);
-      } else if (k0 < K) {
-        atomicAdd(&gsum[k0 / a.group], ss);  // a run of 8 never straddles a group (group % 16 == 0)
+      ssr[c] = ss;  // zero past K
+    }
+    int gstride;  // part[] index of group j's sum = j * gstride
+    if (a.group % 256 == 0) {
+#pragma unroll
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        const float ws = warp_sum(ssr[c]);
+        if (lane == 0) part[c * 16 + warp] = ws;  // chunk of 256 elements starting at (warp + 16c) * 256
       }
+      __syncthreads();
+      const int cpg = a.group / 256, ngroups = K / a.group;
+      float gs = 0.0f;
+      if (tid < ngroups)
+        for (int j = 0; j < cpg; ++j) gs += part[tid * cpg + j];
+      __syncthreads();
+      if (tid < ngroups) part[tid] = gs;
+      gstride = 1;
+    } else {
+      const int R = a.group / 8;
+#pragma unroll
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        const int run = tid + kPrepThreads * c;
+        if (run < nrun) part[run] = ssr[c];
+      }
+      __syncthreads();
+      for (int st = 1; st < R; st <<= 1) {
+        for (int run = tid; run < nrun; run += kPrepThreads) {
+          const int li = run % R;
+          if ((li & (2 * st - 1)) == 0 && li + st < R) part[run] += part[run + st];
+        }
+        __syncthreads();
+      }
+      gstride = R;
     }
     __syncthreads();
 #pragma unroll
     for (int c = 0; c < kPrepMaxPer / 8; ++c) {
       const int k0 = (tid + kPrepThreads * c) * 8;
       if (k0 < K) {
-        const float r = 1.0f / sqrtf(gsum[k0 / a.group] / (float)a.group + a.eps);
+        const float r = 1.0f / sqrtf(part[(k0 / a.group) * gstride] / (float)a.group + a.eps);
         const uint4 u = wv[c];
         const uint4 zz = zv[c];
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w}, z4[4] = {zz.x, zz.y, zz.z, zz.w};

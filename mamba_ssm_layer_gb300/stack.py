@@ -1,0 +1,37 @@
+"""A stack of Mamba-2 layers run back to back (the hidden rows of one layer's
+output are the next layer's input), with per-layer, per-sequence state.
+
+Prefill runs one sequence at a time through every layer; decode advances all
+sequences one token through every layer.  Every computation is a C entry point
+(``mamba2_layer_prefill`` / ``mamba2_layer_decode``) on one stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import abi
+from .layer import DeviceLayer
+
+
+class DeviceStack:
+    def __init__(self, layers: list[dict], device="cuda"):
+        self.layers = [DeviceLayer(l, device) for l in layers]
+        self.device = device
+
+    def new_state(self, B: int):
+        """Per layer: (h [B,H,P,N] fp32, ring [B,d_conv-1,d_xbc] bf16 bits, pos [B] int32), zeroed."""
+        return [dl.new_state(B, self.device) for dl in self.layers]
+
+    def workspace(self, max_batch: int, max_tokens: int) -> torch.Tensor:
+        n = max(abi.m2_workspace_bytes(dl.dims, max_batch, max_tokens) for dl in self.layers)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+
+    def prefill(self, hidden: torch.Tensor, states, seq: int, ws: torch.Tensor, stream=None) -> None:
+        """hidden [T, hidden] bf16 bits of sequence `seq`, transformed in place by every layer."""
+        for dl, (h, ring, pos) in zip(self.layers, states):
+            dl.prefill(hidden, (h[seq], ring[seq], pos[seq:seq + 1]), ws, stream)
+
+    def decode(self, hidden: torch.Tensor, states, ws: torch.Tensor, stream=None) -> None:
+        """hidden [B, hidden]: one token of each of the B sequences, in place through every layer."""
+        for dl, st in zip(self.layers, states):
+            dl.decode(hidden, st, ws, stream)

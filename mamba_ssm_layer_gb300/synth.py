@@ -109,3 +109,31 @@ def make_hidden(rows: int, hidden: int, *key) -> np.ndarray:
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# Eight-layer stack of the 8B-like layer: layers 2 and 5 (0-based) carry BF16
+# projections, the others E4M3; 16 sequences with prompt lengths drawn from the
+# integers 64..512 inclusive, then 256 batched decode steps with fresh hidden
+# rows each step (outputs are not fed back).
+STACK8 = dict(n_layers=8, bf16_layers=(2, 5), n_seqs=16, prompt_min=64, prompt_max=512, decode_steps=256)
+_S_PROMPT_LEN, _S_PROMPT, _S_DECODE = 100, 101, 102
+
+
+def stack_layers(dims: dict = NEMOTRON_H_8B, spec: dict = STACK8) -> list[dict]:
+    out = []
+    for l in range(spec["n_layers"]):
+        fmt = "bf16" if l in spec["bf16_layers"] else "fp8"
+        out.append(make_layer(dims, WL_8B_STACK8, l, fmt, fmt))
+    return out
+
+
+def stack_prompt_lengths(spec: dict = STACK8) -> np.ndarray:
+    return _rng(WL_8B_STACK8, _S_PROMPT_LEN).integers(spec["prompt_min"], spec["prompt_max"] + 1, spec["n_seqs"])
+
+
+def stack_prompt(seq: int, T: int, hidden: int) -> np.ndarray:
+    return make_hidden(T, hidden, WL_8B_STACK8, _S_PROMPT, seq)
+
+
+def stack_decode_rows(step: int, n_seqs: int, hidden: int) -> np.ndarray:
+    return make_hidden(n_seqs, hidden, WL_8B_STACK8, _S_DECODE, step)

@@ -353,3 +353,23 @@ def test_prefill_tiny_bf16_weights(T):
 def test_decode_tiny_b16_tensor_core_path():
     lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
     _run_decode(lay, 16, 5, [0, 9, 15], (synth.WL_TINY_DECODE, 33))
+
+
+@pytest.mark.parametrize("dims,wl", [(synth.TINY, synth.WL_TINY_DECODE), (synth.NEMOTRON_H_8B, synth.WL_8B_DECODE_B64)])
+def test_decode_equal_rows_give_bit_equal_results(dims, wl):
+    # every reduction runs in a fixed order, so sequences with equal inputs and
+    # states give bit-equal outputs and states, on the GEMV (B = 4) and the
+    # tensor-core (B = 16) projections alike
+    lay = synth.make_layer(dims, wl)
+    dl = DeviceLayer(lay)
+    hd = dims["hidden"]
+    for B in (4, 16):
+        st = dl.new_state(B)
+        ws = dl.workspace(B, 0)
+        for k in range(6):
+            x = to_dev(np.repeat(synth.make_hidden(1, hd, 77, 0, k), B, axis=0))
+            dl.decode(x, st, ws)
+            got = bits_u16(x)
+            assert np.array_equal(got, np.repeat(got[:1], B, axis=0)), (B, k)
+        h = st[0].cpu().numpy()
+        assert np.array_equal(h, np.repeat(h[:1], B, axis=0)), B
