@@ -13,18 +13,26 @@
 //
 // The MMA computes D^T: UMMA M = 128 weight rows (one scale row block), UMMA N
 // = NT token rows, so one tile is [128 weight rows] x [NT tokens].
-// Persistent CTAs walk tiles n-major (all token tiles of a weight tile are
-// adjacent, so the E4M3 tile is re-read from L2, not HBM).  Warp roles:
-//   warp 0      TMA producer: E4M3 weight tile [128][128] (plain 2-D map) into
-//               a 4-stage ring; bf16 activation tile [NT][128] (two 64-wide
-//               boxes, 128-byte swizzle = the UMMA K-major canonical layout)
-//               into a 2-stage ring;
+// Persistent CTAs walk work items (a tile, or a k range of a tile when the
+// tiles alone would leave most SMs idle) weight-tile major, so the token tiles
+// of one weight tile are adjacent and its bytes are re-read from L2.  Roles
+// (each ring has its own full/empty mbarriers, so no role waits on another
+// role's unrelated progress):
+//   warp 0      weight producer (lane 0): TMA of the E4M3 tile [128][128]
+//               (plain 2-D map) into a 4-stage ring; bf16 weights go straight
+//               into a 4-stage ring of 128-byte-swizzled tiles.  It does not
+//               wait for the previous kernel: weights are never its output.
+//   warp 10     activation producer (lane 0): after the dependency wait, TMA of
+//               the bf16 activation tile [NT][128] (two 64-wide boxes, 128-byte
+//               swizzle = the UMMA K-major canonical layout), 3-4 stages;
+//   warps 2-5   converters: E4M3 tile -> bf16 tile in the swizzled layout the
+//               MMA descriptor expects (double-buffered);
 //   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each) per k block
-//               into TMEM buffer (k block & 1) and commits to an mbarrier;
-//   warps 2-5   converters: E4M3 tile -> bf16 tile in the 128-byte-swizzled
-//               K-major layout the MMA descriptor expects;
+//               into one of 4 TMEM partial buffers and commits to the barriers
+//               that free the buffers it read and wake the epilogue;
 //   warps 6-9   epilogue: per k block, TMEM -> registers, acc += s * partial;
-//               per tile, the store / residual / conv-update epilogue.
+//               per item, the store / residual / conv-update epilogue, or fp32
+//               partials that a second kernel sums in split order.
 // Every wait is bounded (see mbar_wait); TMEM is freed on every exit path.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -36,26 +44,34 @@
 
 namespace m2 {
 
-constexpr int kTcThreads = 320;
-constexpr int kTcW8Stages = 4;
-constexpr int kTcBM = 128;  // weight rows per tile (UMMA M)
-constexpr int kTcBK = 128;  // k per block (= scale block)
+constexpr int kTcThreads = 352;  // 11 warps
+constexpr int kTcWStages = 4;    // weight tiles in flight
+constexpr int kTcTmemBufs = 4;   // k-block partials in TMEM
+constexpr int kTcBM = 128;       // weight rows per tile (UMMA M)
+constexpr int kTcBK = 128;       // k per block (= scale block)
+
+template <int NT>
+struct TcLayout {
+  static constexpr int kAStages = NT <= 64 ? 4 : 3;
+  // offsets from a 1024-byte aligned base
+  static constexpr int kW = 0;         // fp8: 4 x 16 KB E4M3; bf16: 4 x 32 KB swizzled (through kWbf)
+  static constexpr int kWbf = 65536;   // fp8: 2 x 32 KB converted bf16, swizzled
+  static constexpr int kA = 131072;    // kAStages x NT*256 B bf16, swizzled
+  static constexpr int kBars = kA + kAStages * NT * kTcBK * 2;
+};
 
 struct TcBars {
-  uint64_t w8_full[kTcW8Stages], w8_empty[kTcW8Stages];
-  uint64_t wbf_full[2], a_full[2], mma_done[2], tmem_empty[2];
+  uint64_t w_full[kTcWStages], w_empty[kTcWStages];
+  uint64_t wbf_full[2], wbf_empty[2];
+  uint64_t a_full[4], a_empty[4];
+  uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
   uint32_t tmem_base;
 };
 
 template <int NT>
-struct TcLayout {
-  // offsets from a 1024-byte aligned base
-  static constexpr int kW8 = 0;                                   // 4 x 16 KB raw E4M3
-  static constexpr int kWbf = kW8 + kTcW8Stages * kTcBM * kTcBK;  // 2 x 32 KB bf16, swizzled
-  static constexpr int kA = kWbf + 2 * kTcBM * kTcBK * 2;         // 2 x NT*256 B bf16, swizzled
-  static constexpr int kBars = kA + 2 * NT * kTcBK * 2;
-  static constexpr int kTotal = kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
-};
+constexpr int tc_smem_bytes() {
+  return TcLayout<NT>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
+}
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -86,6 +102,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
 }
+// Arrives on the mbarrier once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
@@ -121,45 +138,103 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
   return pack_bf16x2(lo, hi);
 }
 
+// Conv taps of one channel: history taps 0..L-1 (oldest first) and the tap
+// of the current token, in registers (indexed with compile-time indices only).
+struct ConvTaps {
+  float hist[7];
+  float cur, bias;
+};
+
+__device__ __forceinline__ void load_taps(const GemvArgs& a, int c, int L, ConvTaps& t) {
+#pragma unroll
+  for (int j = 0; j < 7; ++j) t.hist[j] = j < L ? bf16_to_f32(a.conv_w[(size_t)c * a.dconv + j]) : 0.0f;
+  t.cur = bf16_to_f32(a.conv_w[(size_t)c * a.dconv + L]);
+  t.bias = a.conv_b ? bf16_to_f32(a.conv_b[c]) : 0.0f;
+}
+
+// The store / residual / conv-update epilogue of one output (token m, row n).
+// Conv rows: this thread alone owns (sequence m, channel c), so the ring taps
+// it reads are the previous tokens' and the slot it writes is its own.
+__device__ __forceinline__ void tc_epi_elem(const GemvArgs& a, int m, int n, float acc, bool conv,
+                                            const ConvTaps& t, int L) {
+  uint16_t* o = a.out + (size_t)m * a.ldo + n;
+  if (a.epi == EPI_RESID) {
+    *o = f32_to_bf16(bf16_to_f32(a.resid[(size_t)m * a.ldr + n]) + acc);
+  } else if (conv) {
+    const uint16_t vb = f32_to_bf16(acc);  // rounding point of the in_proj output
+    const int c = n - a.xbc0;
+    uint16_t* rg = a.ring + (size_t)m * L * a.d_xbc;
+    const int p = a.pos[m];
+    float sv = t.bias;
+#pragma unroll
+    for (int j = 0; j < 7; ++j)
+      if (j < L) sv += t.hist[j] * bf16_to_f32(rg[(size_t)((p + j) % L) * a.d_xbc + c]);
+    sv += t.cur * bf16_to_f32(vb);
+    *o = f32_to_bf16(silu_f(sv));
+    rg[(size_t)(p % L) * a.d_xbc + c] = vb;
+  } else {
+    *o = f32_to_bf16(acc);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 struct TcArgs {
   GemvArgs g;      // operand pointers, sizes, epilogue
   int32_t m_tiles, n_tiles, kblocks;
   int32_t fp8;
+  int32_t ksplit;  // > 1: k blocks split over work items, fp32 partials to `part`
+  float* part;     // [ksplit][M][N]
 };
+
+// Work item i: tile i / ksplit (weight tile major, so the token tiles of one
+// weight tile are adjacent and its E4M3 bytes are re-read from L2), k range
+// ks = i % ksplit.
+__device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int& nt, int& mt, int& kb0, int& kb1) {
+  const int tile = item / ta.ksplit, ks = item % ta.ksplit;
+  nt = tile / ta.m_tiles;
+  mt = tile % ta.m_tiles;
+  kb0 = (int)((long long)ta.kblocks * ks / ta.ksplit);
+  kb1 = (int)((long long)ta.kblocks * (ks + 1) / ta.ksplit);
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, const TcArgs ta) {
   using Lay = TcLayout<NT>;
+  constexpr int SA = Lay::kAStages;
   const GemvArgs& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + Lay::kBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ntiles = ta.m_tiles * ta.n_tiles;
-  const int KB = ta.kblocks;
+  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
   const int L = a.dconv - 1;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcW8Stages; ++s) {
-      mbar_init(&bars->w8_full[s], 1);
-      mbar_init(&bars->w8_empty[s], 4);
+    for (int s = 0; s < kTcWStages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], ta.fp8 ? 4 : 1);  // the converter warps, or the MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->wbf_full[b], 4);
-      mbar_init(&bars->a_full[b], 1);
+      mbar_init(&bars->wbf_empty[b], 1);
+    }
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(&bars->a_full[s], 1);
+      mbar_init(&bars->a_empty[s], 1);
+    }
+    for (int b = 0; b < kTcTmemBufs; ++b) {
       mbar_init(&bars->mma_done[b], 1);
       mbar_init(&bars->tmem_empty[b], 4);
     }
     fence_mbar_init();
   }
   if (warp == 1) {
-    // 2 x NT fp32 columns of TMEM (a power of two >= 32)
+    // kTcTmemBufs x NT fp32 columns of TMEM (a power of two >= 32)
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&bars->tmem_base)),
-                 "r"(2 * NT));
+                 "r"(kTcTmemBufs * NT));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -169,36 +244,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   bool dead = false;
 
   if (warp == 0) {
-    // -------------------------------------------------------- TMA producer
-    pdl_wait();
+    // -------------------------------------------------------- weight producer
+    // Weights never come from the previous kernel: no dependency wait, so the
+    // first tiles stream in while that kernel finishes.
     if (lane == 0) {
       const uint64_t polw = policy_evict_normal();  // weight tiles are re-read by the token tiles
-      const uint64_t pola = policy_evict_last();    // activations are re-read by every weight tile
       int gk = 0;
-      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
-        const int nt = tile / ta.m_tiles, mt = tile % ta.m_tiles;
-        for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
-          const int s8 = gk % kTcW8Stages, b = gk & 1;
-          if (ta.fp8) {
-            if (gk >= kTcW8Stages && !mbar_wait(&bars->w8_empty[s8], ((gk / kTcW8Stages) - 1) & 1)) dead = true;
-            if (dead) break;
-            mbar_arrive_expect_tx(&bars->w8_full[s8], kTcBM * kTcBK);
-            tma_load_2d(smem + Lay::kW8 + s8 * kTcBM * kTcBK, &tmW, kb * kTcBK, nt * kTcBM, &bars->w8_full[s8], polw);
-          }
-          if (gk >= 2 && !mbar_wait(&bars->mma_done[b], ((gk / 2) - 1) & 1)) dead = true;
+      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
+          const int s = gk % kTcWStages;
+          if (gk >= kTcWStages && !mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)) dead = true;
           if (dead) break;
-          uint8_t* abuf = smem + Lay::kA + b * NT * kTcBK * 2;
           if (ta.fp8) {
-            mbar_arrive_expect_tx(&bars->a_full[b], NT * kTcBK * 2);
+            mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK);
+            tma_load_2d(smem + Lay::kW + s * kTcBM * kTcBK, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
           } else {
-            // bf16 weights go straight into the swizzled weight buffer (no conversion)
-            mbar_arrive_expect_tx(&bars->a_full[b], NT * kTcBK * 2 + kTcBM * kTcBK * 2);
-            uint8_t* wbuf = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
-            tma_load_2d(wbuf, &tmW, kb * kTcBK, nt * kTcBM, &bars->a_full[b], polw);
-            tma_load_2d(wbuf + kTcBM * 128, &tmW, kb * kTcBK + 64, nt * kTcBM, &bars->a_full[b], polw);
+            uint8_t* wbuf = smem + Lay::kW + s * kTcBM * kTcBK * 2;
+            mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK * 2);
+            tma_load_2d(wbuf, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
+            tma_load_2d(wbuf + kTcBM * 128, &tmW, kb * kTcBK + 64, nt * kTcBM, &bars->w_full[s], polw);
           }
-          tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[b], pola);
-          tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[b], pola);
+        }
+      }
+    }
+  } else if (warp == 10) {
+    // -------------------------------------------------------- activation producer
+    pdl_wait();  // A is written by the previous kernel
+    if (lane == 0) {
+      const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
+      int gk = 0;
+      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
+          const int s = gk % SA;
+          if (gk >= SA && !mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)) dead = true;
+          if (dead) break;
+          uint8_t* abuf = smem + Lay::kA + s * NT * kTcBK * 2;
+          mbar_arrive_expect_tx(&bars->a_full[s], NT * kTcBK * 2);
+          tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
+          tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
         }
       }
     }
@@ -207,24 +294,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = tc_idesc(kTcBM, NT);
       int gk = 0;
-      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
-        for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
-          const int b = gk & 1;
-          if (ta.fp8 && !mbar_wait(&bars->wbf_full[b], (gk / 2) & 1)) dead = true;
-          if (!dead && !mbar_wait(&bars->a_full[b], (gk / 2) & 1)) dead = true;
-          if (!dead && gk >= 2 && !mbar_wait(&bars->tmem_empty[b], ((gk / 2) - 1) & 1)) dead = true;
+      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
+          const int s = gk % kTcWStages, b = gk & 1, sa = gk % SA, tb = gk % kTcTmemBufs;
+          if (ta.fp8) {
+            if (!mbar_wait(&bars->wbf_full[b], (gk / 2) & 1)) dead = true;
+          } else {
+            if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
+          }
+          if (!dead && !mbar_wait(&bars->a_full[sa], (gk / SA) & 1)) dead = true;
+          if (!dead && gk >= kTcTmemBufs && !mbar_wait(&bars->tmem_empty[tb], ((gk / kTcTmemBufs) - 1) & 1))
+            dead = true;
           if (dead) break;
           tc_fence_after();
-          const uint32_t wb = smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2);
-          const uint32_t ab = smem_addr(smem + Lay::kA + b * NT * kTcBK * 2);
+          const uint32_t wb = ta.fp8 ? smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2)
+                                     : smem_addr(smem + Lay::kW + s * kTcBM * kTcBK * 2);
+          const uint32_t ab = smem_addr(smem + Lay::kA + sa * NT * kTcBK * 2);
 #pragma unroll
           for (int kk = 0; kk < kTcBK / 16; ++kk) {
             const int atom = kk >> 2, within = (kk & 3) * 32;  // 64-k atoms of 128 bytes per row
             const uint64_t ad = sw128_desc(wb + atom * kTcBM * 128 + within);
             const uint64_t bd = sw128_desc(ab + atom * NT * 128 + within);
-            tc_mma(tmem + b * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
+            tc_mma(tmem + tb * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
           }
-          tc_commit(&bars->mma_done[b]);
+          tc_commit(&bars->mma_done[tb]);
+          tc_commit(&bars->a_empty[sa]);
+          tc_commit(ta.fp8 ? &bars->wbf_empty[b] : &bars->w_empty[s]);
         }
       }
     }
@@ -233,13 +330,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (ta.fp8) {
       const int ct = tid - 64;  // 0..127
       int gk = 0;
-      for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
-        for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
-          const int s8 = gk % kTcW8Stages, b = gk & 1;
-          if (!mbar_wait(&bars->w8_full[s8], (gk / kTcW8Stages) & 1)) dead = true;
-          if (!dead && gk >= 2 && !mbar_wait(&bars->mma_done[b], ((gk / 2) - 1) & 1)) dead = true;
+      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
+          const int s = gk % kTcWStages, b = gk & 1;
+          if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
+          if (!dead && gk >= 2 && !mbar_wait(&bars->wbf_empty[b], ((gk / 2) - 1) & 1)) dead = true;
           if (dead) break;
-          const uint8_t* raw = smem + Lay::kW8 + s8 * kTcBM * kTcBK;
+          const uint8_t* raw = smem + Lay::kW + s * kTcBM * kTcBK;
           uint8_t* dst = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
 #pragma unroll 2
           for (int i = 0; i < 8; ++i) {
@@ -266,72 +365,59 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(&bars->wbf_full[b]);
-            mbar_arrive(&bars->w8_empty[s8]);
+            mbar_arrive(&bars->w_empty[s]);
           }
         }
       }
     }
   } else {
     // -------------------------------------------------------- epilogue
-    const int q = warp & 3;       // TMEM lane quarter of this warp
+    const int q = warp & 3;         // TMEM lane quarter of this warp
     const int row = 32 * q + lane;  // weight row within the tile
     pdl_wait();
     float acc[NT];
     int gk = 0;
-    for (int tile = blockIdx.x; tile < ntiles && !dead; tile += gridDim.x) {
-      const int nt = tile / ta.m_tiles, mt = tile % ta.m_tiles;
+    for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+      int nt, mt, kb0, kb1;
+      tc_item(ta, item, nt, mt, kb0, kb1);
+      const int ks = item % ta.ksplit;
 #pragma unroll
       for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
-      for (int kb = 0; kb < KB && !dead; ++kb, ++gk) {
-        const int b = gk & 1;
-        const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * KB + kb)) : 1.0f;
-        if (!mbar_wait(&bars->mma_done[b], (gk / 2) & 1)) dead = true;
+      for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
+        const int tb = gk % kTcTmemBufs;
+        const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb)) : 1.0f;
+        if (!mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1)) dead = true;
         if (dead) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < NT / 32; ++c) {
           float v[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + b * NT + c * 32, v);
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + c * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, v[i], acc[c * 32 + i]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->tmem_empty[b]);
+        if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
       }
       if (dead) break;
-      // tile epilogue: row n of the weights, token columns m
       const int n = nt * kTcBM + row;
       if (n < a.N) {
-        const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
-        float cw[9];
-        uint16_t cb = 0;
-        if (conv) {
-          const int c = n - a.xbc0;
-          for (int j = 0; j < a.dconv; ++j) cw[j] = bf16_to_f32(a.conv_w[(size_t)c * a.dconv + j]);
-          cb = a.conv_b ? a.conv_b[c] : (uint16_t)0;
-        }
+        if (ta.ksplit > 1) {
+          float* pp = ta.part + ((size_t)ks * a.M) * a.N + n;
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          const int m = mt * NT + j;
-          if (m < a.M) {
-            uint16_t* o = a.out + (size_t)m * a.ldo + n;
-            if (a.epi == EPI_RESID) {
-              *o = f32_to_bf16(bf16_to_f32(a.resid[(size_t)m * a.ldr + n]) + acc[j]);
-            } else if (conv) {
-              // decode batch row m: conv1d update with bias + SiLU for channel c
-              const uint16_t vb = f32_to_bf16(acc[j]);
-              const int c = n - a.xbc0;
-              uint16_t* rg = a.ring + (size_t)m * L * a.d_xbc;
-              const int p = a.pos[m];
-              float sv = bf16_to_f32(cb);
-              for (int t2 = 0; t2 < L; ++t2) sv += cw[t2] * bf16_to_f32(rg[(size_t)((p + t2) % L) * a.d_xbc + c]);
-              sv += cw[L] * bf16_to_f32(vb);
-              *o = f32_to_bf16(silu_f(sv));
-              rg[(size_t)(p % L) * a.d_xbc + c] = vb;
-            } else {
-              *o = f32_to_bf16(acc[j]);
-            }
+          for (int j = 0; j < NT; ++j) {
+            const int m = mt * NT + j;
+            if (m < a.M) pp[(size_t)m * a.N] = acc[j];
+          }
+        } else {
+          const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
+          ConvTaps taps;
+          if (conv) load_taps(a, n - a.xbc0, L, taps);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int m = mt * NT + j;
+            if (m < a.M) tc_epi_elem(a, m, n, acc[j], conv, taps, L);
           }
         }
       }
@@ -342,7 +428,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * NT));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemBufs * NT));
+  }
+}
+
+// Split-k reduction: sums the k-split partials of each output in split order
+// (deterministic) and runs the epilogue.
+__global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const GemvArgs a, const float* part, int ksplit) {
+  pdl_wait();
+  pdl_trigger();
+  const int L = a.dconv - 1;
+  const size_t total = (size_t)a.M * a.N;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    const int m = (int)(i / a.N), n = (int)(i % a.N);
+    float acc = 0.0f;
+    for (int ks = 0; ks < ksplit; ++ks) acc += part[((size_t)ks * a.M + m) * a.N + n];
+    const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
+    ConvTaps taps;
+    if (conv) load_taps(a, n - a.xbc0, L, taps);
+    tc_epi_elem(a, m, n, acc, conv, taps, L);
   }
 }
 
@@ -379,6 +483,24 @@ bool gemm_tc_supported(int M, int N, int K, bool fp8) {
   return M > 8 && K % 16 == 0;
 }
 
+static int tc_nt(int M) { return M <= 64 ? 64 : 128; }
+
+// k split for grids that would leave most SMs idle (few weight tiles at small
+// M): enough items to cover the SMs, at least 4 k blocks per item.
+int gemm_tc_ksplit(int M, int N, int K) {
+  const int nt = tc_nt(M);
+  const int tiles = ((M + nt - 1) / nt) * ((N + kTcBM - 1) / kTcBM);
+  const int kb = (K + kTcBK - 1) / kTcBK;
+  int ks = num_sms() / tiles;
+  if (ks > kb / 4) ks = kb / 4;
+  return ks > 1 ? ks : 1;
+}
+
+size_t gemm_tc_partial_bytes(int M, int N, int K) {
+  const int ks = gemm_tc_ksplit(M, N, K);
+  return ks > 1 ? (size_t)ks * M * N * 4 : 0;
+}
+
 template <int NT>
 static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   static int done_mask[64] = {0};
@@ -401,21 +523,32 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   ta.n_tiles = (g.N + kTcBM - 1) / kTcBM;
   ta.kblocks = (g.K + kTcBK - 1) / kTcBK;
   ta.fp8 = fp8 ? 1 : 0;
-  const int smem = TcLayout<NT>::kTotal;
+  ta.ksplit = gemm_tc_ksplit(g.M, g.N, g.K);
+  ta.part = g.part;
+  if (ta.ksplit > 1 && (!g.part || g.part_bytes < gemm_tc_partial_bytes(g.M, g.N, g.K))) ta.ksplit = 1;
+  const int smem = tc_smem_bytes<NT>();
   auto kern = gemm_tc_kernel<NT>;
   cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
   if (e != cudaSuccess) return e;
   int grid = num_sms();
-  const int ntiles = ta.m_tiles * ta.n_tiles;
-  if (grid > ntiles) grid = ntiles;
+  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
+  if (grid > nitems) grid = nitems;
   trace_pre(K_GEMM_TC, s);
   e = launch_k(kern, dim3(grid), dim3(kTcThreads), smem, s, g.pdl != 0, tmW, tmA, ta);
   trace_post(K_GEMM_TC, s);
+  if (e != cudaSuccess || ta.ksplit == 1) return e;
+  const size_t total = (size_t)g.M * g.N;
+  int rgrid = (int)((total + 255) / 256);
+  if (rgrid > 8 * num_sms()) rgrid = 8 * num_sms();
+  trace_pre(K_GEMM_TC_REDUCE, s);
+  e = launch_k(gemm_tc_reduce_kernel, dim3(rgrid), dim3(256), 0, s, g.pdl != 0, g, (const float*)ta.part,
+               ta.ksplit);
+  trace_post(K_GEMM_TC_REDUCE, s);
   return e;
 }
 
 cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
-  if (g.M <= 64) return launch_tc<64>(g, fp8, s);
+  if (tc_nt(g.M) == 64) return launch_tc<64>(g, fp8, s);
   return launch_tc<128>(g, fp8, s);
 }
 

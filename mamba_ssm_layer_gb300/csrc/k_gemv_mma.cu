@@ -34,6 +34,8 @@ namespace m2 {
 constexpr int kMmaWarps = 16;
 constexpr int kMmaThreads = kMmaWarps * 32;  // 512
 constexpr int kMmaRows = 16;                 // rows per group (MMA M)
+// Weight matrices up to this size are prefetched into L2 whole at launch.
+constexpr size_t kSlabPrefetchMax = 96ull << 20;
 
 struct MmaTail {
   unsigned amax[8];
@@ -169,9 +171,63 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   constexpr int kPrefetchUnits = 4;
   WBuf<FP8> buf0, buf1;  // two named buffers: register arrays must be indexed statically
   if (nunit > 0) load_unit(0, buf0);  // weights never depend on the previous kernel
-  for (int u = 1; u <= kPrefetchUnits; ++u) prefetch_unit(u);
+  // L2 prefetch: a weight matrix that fits comfortably in L2 is requested
+  // whole at launch (this CTA's contiguous rows, 32 KB per request), so HBM
+  // streams at full rate while this kernel waits for its activations and the
+  // register loads then hit L2; larger matrices are prefetched a few units
+  // ahead of each warp instead.
+  const bool whole = (size_t)a.N * a.K * ES <= kSlabPrefetchMax;
+  if (whole) {
+    const size_t slab0 = (size_t)row_begin * a.K * ES, slab = (size_t)nrows * a.K * ES;
+    for (size_t off = (size_t)tid * 32768; off < slab; off += (size_t)kMmaThreads * 32768) {
+      const uint32_t n = (uint32_t)(slab - off < 32768 ? slab - off : 32768);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + slab0 + off), "r"(n) : "memory");
+    }
+  } else {
+    for (int u = 1; u <= kPrefetchUnits; ++u) prefetch_unit(u);
+  }
 
   // ------------------------------------------------ prologue
+  // Epilogue inputs of this CTA's rows.  Under programmatic dependent launch
+  // they come from launches before the immediately preceding kernel, which have
+  // completed by now, so they are staged before the wait (L2 loads: not L1).
+  if (tid < 8) tail->pos[tid] = (a.epi == EPI_INPROJ_CONV && tid < mvalid) ? __ldcg(a.pos + tid) : 0;
+  if (a.epi == EPI_INPROJ_CONV) {
+    uint16_t* cw = reinterpret_cast<uint16_t*>(epi_s);  // [rows_max][dconv+1]
+    uint16_t* rgs = cw + (size_t)rows_max * (a.dconv + 1);  // [MB][L][rows_max]
+    for (int r = tid; r < nrows; r += kMmaThreads) {
+      const int n = row_begin + r;
+      if (n < a.xbc0 || n >= a.xbc0 + a.d_xbc) continue;
+      const int c = n - a.xbc0;
+      uint16_t wv[9];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) wv[j] = j < a.dconv ? __ldg(a.conv_w + (size_t)c * a.dconv + j) : (uint16_t)0;
+      wv[8] = a.conv_b ? __ldg(a.conv_b + c) : (uint16_t)0;
+#pragma unroll
+      for (int m = 0; m < MB; ++m) {
+        if (m < mvalid) {
+          const int p = __ldcg(a.pos + m);
+          const uint16_t* ring = a.ring + (size_t)m * L * a.d_xbc;
+          uint16_t rv[7];
+#pragma unroll
+          for (int j = 0; j < 7; ++j) rv[j] = j < L ? __ldcg(ring + (size_t)((p + j) % L) * a.d_xbc + c) : (uint16_t)0;
+#pragma unroll
+          for (int j = 0; j < 7; ++j)
+            if (j < L) rgs[((size_t)m * L + j) * rows_max + r] = rv[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < a.dconv) cw[r * (a.dconv + 1) + j] = wv[j];
+      cw[r * (a.dconv + 1) + a.dconv] = wv[8];
+    }
+  } else if (a.epi == EPI_RESID) {
+    uint16_t* rs = reinterpret_cast<uint16_t*>(epi_s);  // [MB][rows_max]
+    for (int i = tid; i < nrows * mvalid; i += kMmaThreads) {
+      const int m = i / nrows, r = i % nrows;
+      rs[m * rows_max + r] = __ldcg(a.resid + (size_t)m * a.ldr + row_begin + r);
+    }
+  }
   pdl_wait();
   pdl_trigger();
   for (int i = tid; i < rows_max * kMmaWarps * MB; i += kMmaThreads) tot[i] = 0.0f;
@@ -192,7 +248,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     *reinterpret_cast<uint4*>(act_s + (size_t)m * lay.act_ld + k8) = v;
   }
-  if (tid < 8) tail->pos[tid] = (a.epi == EPI_INPROJ_CONV && tid < mvalid) ? a.pos[tid] : 0;
   __syncthreads();
   if (FP8 && a.act == ACT_PLAIN) {
     // plain bf16 rows: per-row prescale into the f16 range, converted in place
@@ -216,29 +271,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   } else if (tid < 8) {
     tail->unscale[tid] = (a.act == ACT_PREPARED && tid < mvalid) ? a.unscale[tid] : 1.0f;
-  }
-  // epilogue inputs of this CTA's rows
-  if (a.epi == EPI_INPROJ_CONV) {
-    uint16_t* cw = reinterpret_cast<uint16_t*>(epi_s);  // [rows_max][dconv+1]
-    uint16_t* rgs = cw + (size_t)rows_max * (a.dconv + 1);  // [MB][L][rows_max]
-    for (int r = tid; r < nrows; r += kMmaThreads) {
-      const int n = row_begin + r;
-      if (n < a.xbc0 || n >= a.xbc0 + a.d_xbc) continue;
-      const int c = n - a.xbc0;
-      for (int j = 0; j < a.dconv; ++j) cw[r * (a.dconv + 1) + j] = a.conv_w[(size_t)c * a.dconv + j];
-      cw[r * (a.dconv + 1) + a.dconv] = a.conv_b ? a.conv_b[c] : (uint16_t)0;
-      for (int m = 0; m < mvalid; ++m) {
-        const int p = a.pos[m];
-        const uint16_t* ring = a.ring + (size_t)m * L * a.d_xbc;
-        for (int j = 0; j < L; ++j) rgs[((size_t)m * L + j) * rows_max + r] = ring[(size_t)((p + j) % L) * a.d_xbc + c];
-      }
-    }
-  } else if (a.epi == EPI_RESID) {
-    uint16_t* rs = reinterpret_cast<uint16_t*>(epi_s);  // [MB][rows_max]
-    for (int i = tid; i < nrows * mvalid; i += kMmaThreads) {
-      const int m = i / nrows, r = i % nrows;
-      rs[m * rows_max + r] = a.resid[(size_t)m * a.ldr + row_begin + r];
-    }
   }
   __syncthreads();
 
@@ -306,11 +338,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // loads of the next unit are in flight while the current one is computed
   for (int u = 0; u < nunit; u += 2) {
     if (u + 1 < nunit) load_unit(u + 1, buf1);
-    prefetch_unit(u + 1 + kPrefetchUnits);
+    if (!whole) prefetch_unit(u + 1 + kPrefetchUnits);
     process(u, buf0);
     if (u + 1 < nunit) {
       if (u + 2 < nunit) load_unit(u + 2, buf0);
-      prefetch_unit(u + 2 + kPrefetchUnits);
+      if (!whole) prefetch_unit(u + 2 + kPrefetchUnits);
       process(u + 1, buf1);
     }
   }

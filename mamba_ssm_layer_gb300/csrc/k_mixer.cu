@@ -146,6 +146,17 @@ __global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int pspl
   const int g = h / (a.H / a.G);
   float* hb = a.h + ((size_t)b * a.H + h) * a.P * a.N;
   const int p0 = pc * CTA_ROWS + warp * RPW + lane / LPR;
+  if (a.l2_prefetch_bytes && threadIdx.x == 0) {
+    // this CTA's share of the L2 prefetch range, in 16-byte units
+    const size_t units = a.l2_prefetch_bytes / 16, nct = (size_t)gridDim.x * gridDim.y;
+    const size_t cta = (size_t)blockIdx.y * gridDim.x + blockIdx.x;
+    const size_t u0 = units * cta / nct, u1 = units * (cta + 1) / nct;
+    const char* base = static_cast<const char*>(a.l2_prefetch);
+    for (size_t u = u0; u < u1; u += 4096) {  // at most 64 KB per request
+      const size_t n = (u1 - u < 4096 ? u1 - u : 4096) * 16;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + u * 16), "r"((uint32_t)n) : "memory");
+    }
+  }
   float4 hv[ROWS];
   // The state is written only by the SSM kernels of earlier steps, which have
   // completed by now (every kernel of the chain lets its successor launch only

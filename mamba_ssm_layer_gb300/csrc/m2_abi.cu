@@ -76,7 +76,7 @@ static const char* kNames[K_COUNT] = {
     "norm_prep",     "gemv_fp8",        "gemv_fp8_inproj_conv", "gemv_fp8_outproj_resid",
     "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
     "conv_pos",      "ssm_step",        "conv_prefill",    "ssm_scan_seq",
-    "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out"};
+    "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out",   "gemm_tc_reduce"};
 
 // ------------------------------------------------------------------ helpers
 
@@ -132,6 +132,14 @@ static int check_weight(const m2_weight& w, int n, int k) {
 //            y [B][d_inner] fp32, act_out [B][d_inner] (2 B), unscale [2][B] fp32
 //   prefill: act_in [T][hidden], zx [T][ldz] (raw in_proj output), u [T][d_xbc],
 //            y [T][d_inner] fp32, act_out [T][d_inner], unscale [2][T] fp32
+// Scratch for the k-split partials of the tensor-core projections over M rows.
+static size_t proj_part_bytes(const m2_dims& d, int M) {
+  if (M <= 0 || !gemm_tc_supported(M, 0, 16, true)) return 0;
+  const Derived r = derive(d);
+  const size_t a = gemm_tc_partial_bytes(M, r.n_in, d.hidden), b = gemm_tc_partial_bytes(M, d.hidden, r.d_inner);
+  return rup(a > b ? a : b, 256);
+}
+
 static size_t decode_ws(const m2_dims& d, int B) {
   const Derived r = derive(d);
   size_t o = 0;
@@ -140,6 +148,7 @@ static size_t decode_ws(const m2_dims& d, int B) {
   o = rup(o + (size_t)B * r.d_inner * 4, 256);
   o = rup(o + (size_t)B * r.d_inner * 2, 256);
   o = rup(o + (size_t)2 * B * 4, 256);
+  o += proj_part_bytes(d, B);  // tensor-core k-split partials
   return o;
 }
 
@@ -154,6 +163,7 @@ static size_t prefill_ws(const m2_dims& d, int T) {
   o = rup(o + (size_t)2 * T * 4, 256);          // unscale
   if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups))
     o += ssd_workspace_bytes(T, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
+  o += proj_part_bytes(d, T);  // tensor-core k-split partials
   return o;
 }
 
@@ -165,7 +175,8 @@ static bool proj_f16(const m2_weight& w, int M) {
 
 static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
                         GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr,
-                        const float* unscale = nullptr, int pdl = 0) {
+                        const float* unscale = nullptr, int pdl = 0, float* part = nullptr,
+                        size_t part_bytes = 0) {
   GemvArgs a;
   memset(&a, 0, sizeof(a));
   if (extra) a = *extra;
@@ -185,6 +196,8 @@ static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, u
   a.act = (unscale && proj_f16(w, M)) ? ACT_PREPARED : ACT_PLAIN;
   a.unscale = unscale;
   a.pdl = pdl;
+  a.part = part;
+  a.part_bytes = part_bytes;
   const int rowbytes = w.k * (w.fmt == M2_W_FP8_BLOCK128 ? 1 : 2);
   const int grp = rowbytes <= 4096 ? 4 : (rowbytes <= 8192 ? 2 : 1);
   a.evict_first = M <= grp ? 1 : 0;
@@ -261,6 +274,9 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   o = rup(o + (size_t)B * r.d_inner * 2, 256);
   float* us_in = reinterpret_cast<float*>(w8 + o);
   float* us_out = us_in + B;
+  o = rup(o + (size_t)2 * B * 4, 256);
+  float* part = reinterpret_cast<float*>(w8 + o);
+  const size_t part_bytes = proj_part_bytes(d, B);
 
   cudaError_t e;
   // Five kernels, each launched as a programmatic dependent of the previous
@@ -291,7 +307,8 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   ex.xbc0 = r.d_inner;
   ex.d_xbc = r.d_xbc;
   ex.dconv = d.d_conv;
-  if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex, us_in, 1)))
+  if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex, us_in, 1, part,
+                part_bytes)))
     return launch_status(e);
   // 4+5. split and SSM step (advances conv_pos)
   SsmArgs sa;
@@ -314,6 +331,16 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   sa.G = d.n_groups;
   sa.pos_inc = conv_pos;
   sa.pdl = 1;
+  {
+    // the SSM kernel starts while the in_proj drains and moves little data
+    // itself: it pulls the out_proj weights into L2 for the GEMV two launches on
+    const m2_weight& wo = L->out_proj;
+    const size_t wo_bytes = (size_t)wo.n * wo.k * (wo.fmt == M2_W_BF16 ? 2 : 1);
+    if (wo_bytes <= (64ull << 20)) {
+      sa.l2_prefetch = wo.w;
+      sa.l2_prefetch_bytes = wo_bytes;
+    }
+  }
   if ((e = launch_ssm_step(sa, stream))) return launch_status(e);
   // 6. gated RMSNorm -> GEMV activation
   memset(&pa, 0, sizeof(pa));
@@ -335,7 +362,7 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   if ((e = launch_prep(pa, stream))) return launch_status(e);
   // 7+8. out_proj with the residual add in its epilogue (in place on hidden)
   if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out,
-                1)))
+                1, part, part_bytes)))
     return launch_status(e);
   return M2_OK;
 }
@@ -364,6 +391,14 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   o = rup(o + (size_t)T * r.d_inner * 2, 256);
   float* us_in = reinterpret_cast<float*>(w8 + o);
   float* us_out = us_in + T;
+  o = rup(o + (size_t)2 * T * 4, 256);
+  const bool ssd = ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups);
+  float* ssd_dh = reinterpret_cast<float*>(w8 + o);
+  const size_t nchunk = (size_t)(T + 127) / 128;
+  float* ssd_decay = reinterpret_cast<float*>(w8 + rup(o + nchunk * d.nheads * d.head_dim * d.d_state * 4, 256));
+  if (ssd) o += ssd_workspace_bytes(T, d.nheads, d.head_dim, d.d_state);
+  float* part = reinterpret_cast<float*>(w8 + o);
+  const size_t part_bytes = proj_part_bytes(d, T);
 
   cudaError_t e;
   PrepArgs pa;
@@ -380,12 +415,13 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   pa.f16 = proj_f16(L->in_proj, T) ? 1 : 0;
   pa.unscale = us_in;
   if ((e = launch_prep(pa, stream))) return launch_status(e);
-  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream, nullptr, us_in)))
+  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream, nullptr, us_in, 0, part,
+                part_bytes)))
     return launch_status(e);
   if ((e = launch_conv_prefill(conv_state, conv_pos, zx + r.d_inner, r.ldz, L->conv_w, L->conv_b, u, r.d_xbc, T,
                                r.d_xbc, d.d_conv, stream)))
     return launch_status(e);
-  if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups)) {
+  if (ssd) {
     SsdArgs sa;
     memset(&sa, 0, sizeof(sa));
     sa.h = ssm_state;
@@ -406,10 +442,8 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
     sa.N = d.d_state;
     sa.G = d.n_groups;
     sa.pos_inc = conv_pos;
-    o = rup(o + (size_t)2 * T * 4, 256);
-    sa.dH = reinterpret_cast<float*>(w8 + o);
-    const size_t nc = (size_t)(T + 127) / 128;
-    sa.decay = reinterpret_cast<float*>(w8 + rup(o + nc * d.nheads * d.head_dim * d.d_state * 4, 256));
+    sa.dH = ssd_dh;
+    sa.decay = ssd_decay;
     if ((e = launch_ssd(sa, stream))) return launch_status(e);
   } else {
     ScanArgs sa;
@@ -450,7 +484,8 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   pa.f16 = proj_f16(L->out_proj, T) ? 1 : 0;
   pa.unscale = us_out;
   if ((e = launch_prep(pa, stream))) return launch_status(e);
-  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out)))
+  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out,
+                0, part, part_bytes)))
     return launch_status(e);
   return M2_OK;
 }

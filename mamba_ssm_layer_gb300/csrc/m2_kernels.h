@@ -28,6 +28,7 @@ enum KernelId : int32_t {
   K_SSD_CHUNK_STATE,
   K_SSD_STATE_PASS,
   K_SSD_CHUNK_OUT,
+  K_GEMM_TC_REDUCE,
   K_COUNT
 };
 
@@ -77,7 +78,14 @@ struct GemvArgs {
   // Activation input of the GEMV:
   int32_t act;          // GemvAct
   const float* unscale; // ACT_PREPARED: per batch row factor applied to the row totals
-  int32_t pdl;          // launch as a programmatic dependent of the previous kernel
+  // Launch as a programmatic dependent of the previous kernel.  Then only A and
+  // unscale may be produced by that immediately preceding kernel; the
+  // epilogue inputs (ring, pos, resid) must come from earlier launches, and
+  // are read before the dependency wait.
+  int32_t pdl;
+  // tensor-core GEMM only: scratch for k-split partials (may be null: no split)
+  float* part;
+  size_t part_bytes;
 };
 
 enum GemvAct : int32_t {
@@ -161,6 +169,10 @@ struct SsmArgs {
   int32_t B, H, P, N, G;
   int32_t* pos_inc;    // if non-null: pos_inc[b] += 1 (decode fusion)
   int32_t pdl;         // launch as a programmatic dependent of the previous kernel
+  // Optional L2 prefetch issued at kernel start (the weights of the launch
+  // after next): a byte range, 16-byte aligned, size a multiple of 16.
+  const void* l2_prefetch;
+  size_t l2_prefetch_bytes;
 };
 cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s);
 
@@ -169,6 +181,10 @@ int gemv_rows_per_pass(int K, bool fp8);
 
 // tcgen05 GEMM (k_gemm_tc.cu) for M > 8 rows: bf16 activations (ACT_PLAIN).
 bool gemm_tc_supported(int M, int N, int K, bool fp8);
+// k-split factor the GEMM uses for this shape, and the partial scratch it needs
+// (0 when it does not split).
+int gemm_tc_ksplit(int M, int N, int K);
+size_t gemm_tc_partial_bytes(int M, int N, int K);
 cudaError_t launch_gemm_tc(const GemvArgs& a, bool fp8, cudaStream_t s);
 
 // Warp-MMA decode GEMV (k_gemv_mma.cu): M <= 8, K % 64 == 0, K <= 8192.

@@ -373,3 +373,10 @@ def test_decode_equal_rows_give_bit_equal_results(dims, wl):
             assert np.array_equal(got, np.repeat(got[:1], B, axis=0)), (B, k)
         h = st[0].cpu().numpy()
         assert np.array_equal(h, np.repeat(h[:1], B, axis=0)), B
+
+
+def test_prefill_8b_layer_40_tokens_k_split():
+    # 40 tokens: the tensor-core GEMM takes 64-token tiles and splits the
+    # out_proj's k range over work items (fp32 partials summed in split order)
+    lay = synth.make_layer(synth.NEMOTRON_H_8B, synth.WL_8B_PREFILL_1K)
+    _prefill_case(lay, 40, 0, (synth.WL_8B_PREFILL_1K, 40))
