@@ -294,9 +294,46 @@ def main():
     barrier()
     torch.cuda.synchronize()
     launches = abi.m2_launch_count() - launches0
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    ms_step = ms / K
-    value = job_rate(K * B, world, ms)
+    ms_eager = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    eager = {"value": job_rate(K * B, world, ms_eager), "ms_per_step": ms_eager / K, "steps": K}
+
+    # The same steps replayed from a CUDA graph: one pass over the replicas is
+    # captured once (the library's launches, with their programmatic-dependent
+    # edges) and replayed, as a serving loop would run a fixed decode step;
+    # this removes the host's per-launch cost from the timed region.
+    graph_info, ms, K_run, clk_g = None, ms_eager, K, None
+    try:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(R):
+                step(W + i)
+        torch.cuda.current_stream().wait_stream(cap)
+        reps_g = max(1, round(K / R))
+        g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(torch.cuda.current_device()) as clk_g:
+            e0.record()
+            for _ in range(reps_g):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ms_g = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        graph_info = {"value": job_rate(reps_g * R * B, world, ms_g), "ms_per_step": ms_g / (reps_g * R),
+                      "steps": reps_g * R, "steps_per_graph": R}
+        if graph_info["value"] > eager["value"]:
+            ms, K_run = ms_g, reps_g * R
+    except Exception as ex:  # capture unsupported here: the eager number stands
+        graph_info = {"error": f"{type(ex).__name__}: {ex}"[:200]}
+    ms_step = ms / K_run
+    value = job_rate(K_run * B, world, ms)
+    use_graph = K_run != K or ms != ms_eager
+    launches_per_step = launches / K
 
     # per-kernel device time of the same steps, from the library's event trace
     # (events between launches serialise them; these are per-launch durations)
@@ -317,19 +354,22 @@ def main():
 
     out = {
         "metric": "decode tokens/s (Mamba-2 layer, batch 1)", "value": value, "unit": "tokens/s",
-        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
+        "n_gpus": world, "steps": K_run, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "nemotron_h_8b_like_decode_b1", "batch": B, "hidden": 4096, "nheads": 128,
                    "head_dim": 64, "d_state": 128, "n_groups": 8, "d_conv": 4,
                    "weights": "e4m3 128x128 block-scaled, bf16 scales", "activations": "bf16",
                    "l2": f"rotating {R} layer replicas ({R * per_rep / 1e9:.2f} GB) > L2 {l2 / 2**20:.0f} MiB",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "launch": "cuda_graph replay of the library's launches" if use_graph else "eager calls"},
         "step_hbm": {"bytes_per_token": per_rep, "gbs": per_rep / (ms_step / 1e3) / 1e9,
                      "frac": per_rep / (ms_step / 1e3) / 1e9 / hbm_peak},
         "roofline": roof,
-        "gpu_launches": launches,
+        "gpu_launches": int(round(launches_per_step * K_run)),
+        "eager": eager,
+        "graph": graph_info,
         "kernels_ms_per_step": {k: v[0] / K for k, v in tr.items()},
-        "clocks": clk.summary(),
+        "clocks": (clk_g.summary() if use_graph and clk_g is not None else clk.summary()),
     }
 
     if not args.no_extras:

@@ -1,27 +1,27 @@
 // k_gemv_mma.cu -- decode GEMV (batch <= 8) on warp-level MMA, weights
-// streamed straight from HBM into registers.
+// streamed from HBM into shared memory by bulk copies.
 //
 // Same contract as the CUDA-core GEMV in k_gemv.cu (GemvArgs: w8a16 E4M3
 // block-scaled or bf16 weights, plain or prepared activations, store /
 // residual / conv-update epilogue), for K % 64 == 0, K <= 8192 and up to 8
-// batch rows.  The GEMV is HBM-bound; the MMA only replaces the per-weight
-// multiply-adds: one m16n8k16 instruction consumes 256 weights (16 rows x 16
-// k), so a weight costs well under one instruction (its half of an exact
-// E4M3->f16x2 conversion plus a share of the load and the MMA) instead of ~4
-// on the FMA pipes, and the 8 MMA columns carry up to 8 batch rows for free.
+// batch rows.  The GEMV is HBM-bound.  Register-destination loads keep too few
+// bytes in flight per SM to reach the HBM rate, so one producer warp streams
+// the weights with 1-D bulk copies (async proxy, mbarrier completion) through
+// a ring of shared-memory stages, each 16 rows x KC bytes (one copy per row,
+// rows padded by 64 bytes so that the fragment loads below are free of bank
+// conflicts); the producer starts before the dependency wait, since weights
+// are never the previous kernel's output.
 //
-// One CTA (16 warps) per SM over a contiguous range of 16-row groups.  Warp w
-// owns a k-slice of every row (a run of 64-element groups).  Lane (g, t) =
-// (lane/4, lane%4) loads, per group, the 16 weight bytes [16t, 16t+16) of rows
-// g and g+8 with one 128-bit load each (4 lanes cover a row's 64 contiguous
-// bytes), converts them to the A fragments and issues 4 MMAs; the k order
-// inside a group is permuted identically for A and B, which a dot product
-// allows.  Loads for the next unit of work are issued before the current one
-// is computed (two register buffers), so each warp keeps 8 x 16 B per lane in
-// flight, and L2 prefetches run four units further ahead.  Activations (f16
-// with the exact per-row prescale for E4M3, or bf16) sit in shared memory;
-// E4M3 partials are scaled per 128-element block; each warp leaves its 16 x MB
-// tile per row group in shared memory, and at the end all threads add the 16
+// 16 consumer warps split each stage's 64-element groups.  Lane (g, t) =
+// (lane/4, lane%4) reads, per group, the 16 weight bytes [16t, 16t+16) (E4M3;
+// 32 bytes for bf16) of rows g and g+8, converts E4M3 exactly to f16 and
+// issues 4 m16n8k16 MMAs against the activations (up to 8 batch rows in the
+// 8 MMA columns); the k order inside a group is permuted identically for both
+// operands, which a dot product allows.  One m16n8k16 consumes 256 weights,
+// so a weight costs a fraction of an instruction.  Activations (f16 with the
+// exact per-row prescale for E4M3, or bf16) sit in shared memory; E4M3
+// partials are scaled per 128-element block; each warp leaves its 16 x MB tile
+// per row group in shared memory, and at the end all threads add the 16
 // warps' tiles in a fixed order (deterministic) and run the epilogue.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -31,35 +31,45 @@
 
 namespace m2 {
 
-constexpr int kMmaWarps = 16;
-constexpr int kMmaThreads = kMmaWarps * 32;  // 512
+constexpr int kMmaWarps = 16;                // consumer warps
+constexpr int kMmaThreads = (kMmaWarps + 1) * 32;  // + one producer warp
 constexpr int kMmaRows = 16;                 // rows per group (MMA M)
-// Weight matrices up to this size are prefetched into L2 whole at launch.
-constexpr size_t kSlabPrefetchMax = 96ull << 20;
+constexpr int kRowPad = 64;                  // bytes of padding per staged row
+constexpr int kMaxStages = 8;
 
 struct MmaTail {
   unsigned amax[8];
   float unscale[8];
   int32_t pos[8];
+  uint64_t full[kMaxStages], empty[kMaxStages];
 };
 
+// Shared-memory layout.  kc: bytes of a row per stage (a multiple of 64
+// elements); stages: ring depth.
 struct MmaLayout {
-  int act_ld, tail, act, tot, epi, total;
+  int act_ld, tail, act, tot, epi, stage, stage_bytes, kc, stages, total;
 };
-// act_ld: elements per activation row in shared memory (K + 8 pads the rows
-// onto different banks).
-__host__ __device__ inline MmaLayout mma_layout(int K, int rows_max, int mb, int kb, int epi, int dconv) {
+__host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int mb, int epi, int dconv) {
   MmaLayout L;
-  L.act_ld = K + 8;
+  L.act_ld = K + 8;  // elements per activation row (the pad spreads rows over banks)
   L.tail = 0;
   L.act = (int)((sizeof(MmaTail) + 127) / 128 * 128);
-  L.tot = L.act + ((mb + 1) * L.act_ld * 2 + 15) / 16 * 16;  // + one zero row for lanes past the batch
-  (void)kb;
-  L.epi = L.tot + (rows_max * kMmaWarps * mb * 4 + 15) / 16 * 16;  // per-warp partials
+  L.tot = L.act + ((mb + 1) * L.act_ld * 2 + 127) / 128 * 128;  // + one zero row for lanes past the batch
+  L.epi = L.tot + (rows_max * kMmaWarps * mb * 4 + 127) / 128 * 128;  // per-warp partials
   int epi_bytes = 0;
   if (epi == EPI_INPROJ_CONV) epi_bytes = rows_max * (dconv + 1) * 2 + mb * rows_max * (dconv - 1) * 2;
   if (epi == EPI_RESID) epi_bytes = mb * rows_max * 2;
-  L.total = L.epi + (epi_bytes + 15) / 16 * 16;
+  L.stage = L.epi + (epi_bytes + 127) / 128 * 128;
+  const int budget = 227 * 1024 - L.stage;
+  const int row_bytes = K * es;
+  // the largest chunk (<= 4 KB of a row) that leaves at least 3 stages, then as many stages as fit
+  int kc = row_bytes < 4096 ? row_bytes : 4096;
+  while (kc > 64 * es && budget / (kMmaRows * (kc + kRowPad)) < 3) kc = (kc / 2 + 64 * es - 1) / (64 * es) * (64 * es);
+  L.kc = kc;
+  L.stage_bytes = kMmaRows * (kc + kRowPad);
+  L.stages = budget / L.stage_bytes;
+  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  L.total = L.stage + L.stages * L.stage_bytes;
   return L;
 }
 
@@ -92,32 +102,158 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
   }
 }
 
-// 64-element groups per unit of work: 4 for E4M3 (16 bytes per lane per row
-// and group), 2 for bf16 (32 bytes), so that a unit's weights take 32
-// registers per lane in both cases.
-template <bool FP8>
-struct Unit {
-  static constexpr int kGroups = FP8 ? 4 : 2;
-};
-// Weight registers of one unit: kGroups groups x rows {g, g+8}.
-template <bool FP8>
-struct WBuf {
-  uint4 r0[4];
-  uint4 r8[4];
-};
+// Fused activation norm for the decode GEMV (consumer threads only, nC of
+// them; `red` is 64 floats of shared scratch).  Row m of the activation is
+// computed into act (bf16, or f16 after the exact power-of-two prescale for
+// E4M3 weights, unscale[m] = 2^-j).  Same arithmetic as the separate norm
+// kernel (k_mixer.cu): the RMSNorm sum of squares as error-free fp32 pairs
+// and r in double, so its rounding decisions do not depend on the order; the
+// gated sum in a fixed order (every CTA computes the same row identically).
+template <bool F16>
+__device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* red, double* red_d, float* unscale,
+                               int tid, int nC) {
+  const int K = a.K, warp = tid >> 5, lane = tid & 31;
+  constexpr int kPer = 2;  // 16-byte chunks of 8 elements per thread (K <= 8192 with 512 threads)
+  float v[kPer * 8];
+  uint4 wv[kPer], zv[kPer];
+#pragma unroll
+  for (int c = 0; c < kPer; ++c) {
+    const int k0 = (tid + nC * c) * 8;
+    wv[c] = zv[c] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
+    if (k0 < K) {
+      wv[c] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + k0));
+      if (a.norm == NORM_RMS) {
+        const uint4 u = *reinterpret_cast<const uint4*>(a.A + (size_t)m * a.lda + k0);  // coherent: previous kernel
+        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[c * 8 + 2 * e] = bf16lo(w4[e]);
+          v[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
+        }
+      } else {
+        zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
+        const float4 f0 = *reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0);
+        const float4 f1 = *reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0 + 4);
+        v[c * 8 + 0] = f0.x; v[c * 8 + 1] = f0.y; v[c * 8 + 2] = f0.z; v[c * 8 + 3] = f0.w;
+        v[c * 8 + 4] = f1.x; v[c * 8 + 5] = f1.y; v[c * 8 + 6] = f1.z; v[c * 8 + 7] = f1.w;
+      }
+    }
+  }
+  uint16_t o[kPer * 8];
+  if (a.norm == NORM_RMS) {
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kPer * 8; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
+    two_sum_warp(hi, lo);
+    if (lane == 0) {
+      red[warp] = hi;
+      red[32 + warp] = lo;
+    }
+    named_bar(1, nC);
+    if (tid == 0) {
+      float h = 0.0f, l = 0.0f;
+      for (int w = 0; w < nC / 32; ++w) {
+        two_sum_acc(h, l, red[w]);
+        l += red[32 + w];
+      }
+      const double vv = ((double)h + (double)l) * a.norm_inv_k + (double)a.norm_eps;
+      const double r0 = (double)rsqrtf((float)vv);
+      *red_d = r0 * (1.5 - 0.5 * vv * r0 * r0);
+    }
+    named_bar(1, nC);
+    const double rd = *red_d;
+    const float rf = (float)rd;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) {
+      const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[c * 8 + 2 * e] = norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, rd);
+        o[c * 8 + 2 * e + 1] = norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, rd);
+      }
+    }
+  } else {
+    // sum of squares in the order of the separate gated-norm kernel: runs of 8
+    // in sequence, warp butterflies, then the 256-element chunks in index order
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) {
+      float ss = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
+      ss = warp_sum(ss);
+      if (lane == 0) red[c * (nC / 32) + warp] = ss;  // chunk (warp + 16c) of 256 elements
+    }
+    named_bar(1, nC);
+    if (tid == 0) {
+      float gs = 0.0f;
+      for (int j = 0; j < K / 256; ++j) gs += red[j];
+      red[63] = 1.0f / sqrtf(gs / (float)K + a.norm_eps);
+    }
+    named_bar(1, nC);
+    const float r = red[63];
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) {
+      const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w}, z4[4] = {zv[c].x, zv[c].y, zv[c].z, zv[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[c * 8 + 2 * e] = f32_to_bf16(v[c * 8 + 2 * e] * r * bf16lo(w4[e]) * silu_f(bf16lo(z4[e])));
+        o[c * 8 + 2 * e + 1] = f32_to_bf16(v[c * 8 + 2 * e + 1] * r * bf16hi(w4[e]) * silu_f(bf16hi(z4[e])));
+      }
+    }
+  }
+  float up = 1.0f;
+  if (F16) {
+    float mx = 0.0f;
+#pragma unroll
+    for (int e = 0; e < kPer * 8; ++e) mx = fmaxf(mx, fabsf(bf16_to_f32(o[e])));
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+    named_bar(1, nC);  // every reader of red[] above is done
+    if (lane == 0) red[warp] = mx;
+    named_bar(1, nC);
+    mx = 0.0f;
+    for (int w = 0; w < nC / 32; ++w) mx = fmaxf(mx, red[w]);
+    const unsigned bits = __float_as_uint(mx);
+    const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
+    const int jx = max(-120, min(120, 14 - ex));
+    up = ldexpf(1.0f, jx);
+    if (tid == 0) unscale[m] = ldexpf(1.0f, -jx);
+  } else if (tid == 0) {
+    unscale[m] = 1.0f;
+  }
+#pragma unroll
+  for (int c = 0; c < kPer; ++c) {
+    const int k0 = (tid + nC * c) * 8;
+    if (k0 < K) {
+      uint32_t o4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (F16) {
+          o4[e] = pack_h2(bf16_to_f32(o[c * 8 + 2 * e]) * up, bf16_to_f32(o[c * 8 + 2 * e + 1]) * up);
+        } else {
+          o4[e] = (uint32_t)o[c * 8 + 2 * e] | ((uint32_t)o[c * 8 + 2 * e + 1] << 16);
+        }
+      }
+      *reinterpret_cast<uint4*>(act + k0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+  }
+  named_bar(1, nC);  // red[] is reused by the next row
+}
 
 template <bool FP8, int MB>
 __global__ void __launch_bounds__(kMmaThreads, 1)
     gemv_mma_kernel(const GemvArgs a, int rows_max) {
   constexpr int ES = FP8 ? 1 : 2;  // bytes per weight
-  constexpr int kMmaUnit = Unit<FP8>::kGroups;
   extern __shared__ __align__(128) uint8_t smem[];
   const int kb = (a.K + 127) / 128;
-  const MmaLayout lay = mma_layout(a.K, rows_max, MB, kb, a.epi, a.dconv);
+  const MmaLayout lay = mma_layout(a.K, ES, rows_max, MB, a.epi, a.dconv);
   MmaTail* tail = reinterpret_cast<MmaTail*>(smem + lay.tail);
   uint16_t* act_s = reinterpret_cast<uint16_t*>(smem + lay.act);  // [MB + 1][act_ld]
   float* tot = reinterpret_cast<float*>(smem + lay.tot);
   uint8_t* epi_s = smem + lay.epi;
+  uint8_t* stg = smem + lay.stage;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -131,71 +267,70 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int nrg = rg_end - rg_begin;
   const int mvalid = min(MB, a.M);
   const int L = a.dconv - 1;
-  // this warp's 64-element groups [q0, q1) of every row, processed in units
-  const int ngrp = a.K / 64;
-  const int q0 = (ngrp * warp) / kMmaWarps, q1 = (ngrp * (warp + 1)) / kMmaWarps;
-  const int nunit_rg = (q1 - q0 + kMmaUnit - 1) / kMmaUnit;  // units per row group
-  const int nunit = nunit_rg * nrg;
+  const int row_bytes = a.K * ES;
+  const int nch = (row_bytes + lay.kc - 1) / lay.kc;  // chunks (stages) per row group
+  const int nst = nrg * nch;                          // stages this CTA streams
+  const int pitch = lay.kc + kRowPad;
+  const int S = lay.stages;
 
-  const uint8_t* W = static_cast<const uint8_t*>(a.W);
-  // loads of unit u into buffer b (rows past N load row N-1; groups past q1 load nothing)
-  auto load_unit = [&](int u, WBuf<FP8>& b) {
-    const int rg = rg_begin + u / nunit_rg;
-    const int qb = q0 + (u % nunit_rg) * kMmaUnit;
-    const int r0 = min(rg * kMmaRows + g, a.N - 1), r8 = min(rg * kMmaRows + g + 8, a.N - 1);
-    const uint8_t* p0 = W + ((size_t)r0 * a.K + (size_t)qb * 64 + 16 * t) * ES;
-    const uint8_t* p8 = W + ((size_t)r8 * a.K + (size_t)qb * 64 + 16 * t) * ES;
-#pragma unroll
-    for (int i = 0; i < kMmaUnit; ++i) {
-      if (qb + i < q1) {
-#pragma unroll
-        for (int h = 0; h < ES; ++h) {
-          b.r0[i * ES + h] = __ldcs(reinterpret_cast<const uint4*>(p0 + (size_t)i * 64 * ES) + h);
-          b.r8[i * ES + h] = __ldcs(reinterpret_cast<const uint4*>(p8 + (size_t)i * 64 * ES) + h);
-        }
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->empty[i], kMmaWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  bool dead = false;
+  if (warp == kMmaWarps) {
+    // ------------------------------------------------ producer warp
+    // Weights are never written by the previous kernel: stream without waiting.
+    const uint64_t pol = a.evict_first ? policy_evict_first() : policy_evict_normal();
+    const uint8_t* W = static_cast<const uint8_t*>(a.W);
+    int j = 0;
+    bool waited = false;
+    for (; j < nst && !dead; ++j) {
+      const int s = j % S;
+      if (j == S) {
+        // the ring is full: now take part in the dependency protocol
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+      }
+      if (j >= S && !mbar_wait(&tail->empty[s], ((j / S) - 1) & 1)) dead = true;
+      if (dead) break;
+      const int rg = rg_begin + j / nch, ch = j % nch;
+      const int cb = min(lay.kc, row_bytes - ch * lay.kc);  // bytes of each row in this chunk
+      if (lane == 0) mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(kMmaRows * cb));
+      __syncwarp();
+      if (lane < kMmaRows) {
+        const int r = min(rg * kMmaRows + lane, a.N - 1);  // rows past N repeat row N-1 (results unused)
+        bulk_g2s(stg + (size_t)s * lay.stage_bytes + (size_t)lane * pitch, W + (size_t)r * row_bytes + (size_t)ch * lay.kc,
+                 (uint32_t)cb, &tail->full[s], pol);
       }
     }
-  };
-  // L2 prefetch of a whole unit (16 rows x the unit's k-range), one bulk
-  // prefetch per row from lanes 0..15: keeps HBM busy beyond the two register
-  // buffers, including while the prologue below waits and stages.
-  auto prefetch_unit = [&](int u) {
-    if (u >= nunit || lane >= kMmaRows) return;
-    const int rg = rg_begin + u / nunit_rg;
-    const int qb = q0 + (u % nunit_rg) * kMmaUnit;
-    const int ng = min(kMmaUnit, q1 - qb);
-    const int r = min(rg * kMmaRows + lane, a.N - 1);
-    const uint8_t* p = W + ((size_t)r * a.K + (size_t)qb * 64) * ES;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"((uint32_t)(ng * 64 * ES)) : "memory");
-  };
-  constexpr int kPrefetchUnits = 4;
-  WBuf<FP8> buf0, buf1;  // two named buffers: register arrays must be indexed statically
-  if (nunit > 0) load_unit(0, buf0);  // weights never depend on the previous kernel
-  // L2 prefetch: a weight matrix that fits comfortably in L2 is requested
-  // whole at launch (this CTA's contiguous rows, 32 KB per request), so HBM
-  // streams at full rate while this kernel waits for its activations and the
-  // register loads then hit L2; larger matrices are prefetched a few units
-  // ahead of each warp instead.
-  const bool whole = (size_t)a.N * a.K * ES <= kSlabPrefetchMax;
-  if (whole) {
-    const size_t slab0 = (size_t)row_begin * a.K * ES, slab = (size_t)nrows * a.K * ES;
-    for (size_t off = (size_t)tid * 32768; off < slab; off += (size_t)kMmaThreads * 32768) {
-      const uint32_t n = (uint32_t)(slab - off < 32768 ? slab - off : 32768);
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + slab0 + off), "r"(n) : "memory");
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
     }
-  } else {
-    for (int u = 1; u <= kPrefetchUnits; ++u) prefetch_unit(u);
+    // drain: every copy this warp issued has landed before the CTA may exit
+    for (int k = max(0, j - S); k < j; ++k)
+      if (!mbar_wait(&tail->full[k % S], (k / S) & 1)) break;
+    __syncthreads();  // pairs with the consumers' barrier before the epilogue
+    return;
   }
 
-  // ------------------------------------------------ prologue
+  // ------------------------------------------------ consumers: prologue
   // Epilogue inputs of this CTA's rows.  Under programmatic dependent launch
   // they come from launches before the immediately preceding kernel, which have
   // completed by now, so they are staged before the wait (L2 loads: not L1).
+  constexpr int kC = kMmaWarps * 32;  // consumer threads
   if (tid < 8) tail->pos[tid] = (a.epi == EPI_INPROJ_CONV && tid < mvalid) ? __ldcg(a.pos + tid) : 0;
   if (a.epi == EPI_INPROJ_CONV) {
-    uint16_t* cw = reinterpret_cast<uint16_t*>(epi_s);  // [rows_max][dconv+1]
+    uint16_t* cw = reinterpret_cast<uint16_t*>(epi_s);      // [rows_max][dconv+1]
     uint16_t* rgs = cw + (size_t)rows_max * (a.dconv + 1);  // [MB][L][rows_max]
-    for (int r = tid; r < nrows; r += kMmaThreads) {
+    for (int r = tid; r < nrows; r += kC) {
       const int n = row_begin + r;
       if (n < a.xbc0 || n >= a.xbc0 + a.d_xbc) continue;
       const int c = n - a.xbc0;
@@ -223,101 +358,127 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   } else if (a.epi == EPI_RESID) {
     uint16_t* rs = reinterpret_cast<uint16_t*>(epi_s);  // [MB][rows_max]
-    for (int i = tid; i < nrows * mvalid; i += kMmaThreads) {
+    for (int i = tid; i < nrows * mvalid; i += kC) {
       const int m = i / nrows, r = i % nrows;
       rs[m * rows_max + r] = __ldcg(a.resid + (size_t)m * a.ldr + row_begin + r);
     }
   }
   pdl_wait();
   pdl_trigger();
-  for (int i = tid; i < rows_max * kMmaWarps * MB; i += kMmaThreads) tot[i] = 0.0f;
+  for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
   if (tid < 8) tail->amax[tid] = 0u;
-  __syncthreads();
-  // activations -> shared memory (coherent loads: written by the previous kernel)
-  const int kv = a.K / 8;  // 16-byte vectors per row
-  for (int i = tid; i < (MB + 1) * kv; i += kMmaThreads) {
-    const int m = i / kv, k8 = (i % kv) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (m < mvalid) v = *reinterpret_cast<const uint4*>(a.A + (size_t)m * a.lda + k8);
-    if (FP8 && a.act == ACT_PLAIN && m < mvalid) {
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-      float mx = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w4[e])), fabsf(bf16hi(w4[e]))));
-      atomicMax(&tail->amax[m], __float_as_uint(mx));
-    }
-    *reinterpret_cast<uint4*>(act_s + (size_t)m * lay.act_ld + k8) = v;
-  }
-  __syncthreads();
-  if (FP8 && a.act == ACT_PLAIN) {
-    // plain bf16 rows: per-row prescale into the f16 range, converted in place
-    for (int i = tid; i < mvalid * kv; i += kMmaThreads) {
+  named_bar(1, kC);
+  if (a.norm != NORM_NONE) {
+    // the activation rows are this kernel's own norm of its inputs
+    float* red = tot;  // scratch: tot is zeroed again below
+    double* red_d = reinterpret_cast<double*>(tot + 64);
+    for (int m = 0; m < mvalid; ++m)
+      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, red_d, tail->unscale, tid, kC);
+    const int kv = a.K / 8;
+    for (int i = tid; i < kv; i += kC)  // zero row for lanes past the batch
+      *reinterpret_cast<uint4*>(act_s + (size_t)MB * lay.act_ld + i * 8) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
+    named_bar(1, kC);
+  } else {
+    // activations -> shared memory (coherent loads: written by the previous kernel)
+    const int kv = a.K / 8;  // 16-byte vectors per row
+    for (int i = tid; i < (MB + 1) * kv; i += kC) {
       const int m = i / kv, k8 = (i % kv) * 8;
-      const unsigned bits = tail->amax[m];
-      const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
-      const float up = ldexpf(1.0f, max(-120, min(120, 14 - ex)));
-      uint4* p = reinterpret_cast<uint4*>(act_s + (size_t)m * lay.act_ld + k8);
-      uint4 v = *p;
-      v.x = pack_h2(bf16lo(v.x) * up, bf16hi(v.x) * up);
-      v.y = pack_h2(bf16lo(v.y) * up, bf16hi(v.y) * up);
-      v.z = pack_h2(bf16lo(v.z) * up, bf16hi(v.z) * up);
-      v.w = pack_h2(bf16lo(v.w) * up, bf16hi(v.w) * up);
-      *p = v;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (m < mvalid) v = *reinterpret_cast<const uint4*>(a.A + (size_t)m * a.lda + k8);
+      if (FP8 && a.act == ACT_PLAIN && m < mvalid) {
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float mx = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fmaxf(fabsf(bf16lo(w4[e])), fabsf(bf16hi(w4[e]))));
+        atomicMax(&tail->amax[m], __float_as_uint(mx));
+      }
+      *reinterpret_cast<uint4*>(act_s + (size_t)m * lay.act_ld + k8) = v;
     }
-    if (tid < 8) {
-      const unsigned bits = tail->amax[tid];
-      const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
-      tail->unscale[tid] = ldexpf(1.0f, -max(-120, min(120, 14 - ex)));
+    named_bar(1, kC);
+    if (FP8 && a.act == ACT_PLAIN) {
+      // plain bf16 rows: per-row prescale into the f16 range, converted in place
+      for (int i = tid; i < mvalid * kv; i += kC) {
+        const int m = i / kv, k8 = (i % kv) * 8;
+        const unsigned bits = tail->amax[m];
+        const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
+        const float up = ldexpf(1.0f, max(-120, min(120, 14 - ex)));
+        uint4* p = reinterpret_cast<uint4*>(act_s + (size_t)m * lay.act_ld + k8);
+        uint4 v = *p;
+        v.x = pack_h2(bf16lo(v.x) * up, bf16hi(v.x) * up);
+        v.y = pack_h2(bf16lo(v.y) * up, bf16hi(v.y) * up);
+        v.z = pack_h2(bf16lo(v.z) * up, bf16hi(v.z) * up);
+        v.w = pack_h2(bf16lo(v.w) * up, bf16hi(v.w) * up);
+        *p = v;
+      }
+      if (tid < 8) {
+        const unsigned bits = tail->amax[tid];
+        const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
+        tail->unscale[tid] = ldexpf(1.0f, -max(-120, min(120, 14 - ex)));
+      }
+    } else if (tid < 8) {
+      tail->unscale[tid] = (a.act == ACT_PREPARED && tid < mvalid) ? a.unscale[tid] : 1.0f;
     }
-  } else if (tid < 8) {
-    tail->unscale[tid] = (a.act == ACT_PREPARED && tid < mvalid) ? a.unscale[tid] : 1.0f;
+    named_bar(1, kC);
   }
-  __syncthreads();
 
-  // ------------------------------------------------ main loop
+  // ------------------------------------------------ consumers: main loop
   const uint16_t* act_g = act_s + (size_t)(g < mvalid ? g : MB) * lay.act_ld;  // zero row past the batch
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  auto process = [&](int u, const WBuf<FP8>& cur) {
-    const int rg = rg_begin + u / nunit_rg;
-    const int qb = q0 + (u % nunit_rg) * kMmaUnit;
+  for (int j = 0; j < nst && !dead; ++j) {
+    const int s = j % S;
+    const int rg = rg_begin + j / nch, ch = j % nch;
+    const int cb = min(lay.kc, row_bytes - ch * lay.kc);
+    const int ng = cb / (64 * ES);                      // 64-element groups in this chunk
+    const int q0 = (ng * warp) / kMmaWarps, q1 = (ng * (warp + 1)) / kMmaWarps;
+    const int kel0 = ch * (lay.kc / ES);                // first k of the chunk
+    if (!mbar_wait(&tail->full[s], (j / S) & 1)) {
+      dead = true;
+      break;
+    }
+    const uint8_t* st0 = stg + (size_t)s * lay.stage_bytes + (size_t)g * pitch;
+    const uint8_t* st8 = st0 + (size_t)8 * pitch;
+    const int r0 = min(rg * kMmaRows + g, row_end - 1), r8 = min(rg * kMmaRows + g + 8, row_end - 1);
+    for (int q = q0; q < q1; ++q) {
+      const int k0 = kel0 + q * 64;  // first k of the group
+      const uint4 bl = *reinterpret_cast<const uint4*>(act_g + k0 + 16 * t);
+      const uint4 bh = *reinterpret_cast<const uint4*>(act_g + k0 + 16 * t + 8);
+      const uint32_t bw[8] = {bl.x, bl.y, bl.z, bl.w, bh.x, bh.y, bh.z, bh.w};
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (FP8) {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(st0 + q * 64 + 16 * t);
+        const uint4 v8 = *reinterpret_cast<const uint4*>(st8 + q * 64 + 16 * t);
+        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+        const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w};
 #pragma unroll
-    for (int i = 0; i < kMmaUnit; ++i) {
-      const int q = qb + i;
-      if (q < q1) {
-        const uint4 bl = *reinterpret_cast<const uint4*>(act_g + q * 64 + 16 * t);
-        const uint4 bh = *reinterpret_cast<const uint4*>(act_g + q * 64 + 16 * t + 8);
-        const uint32_t bw[8] = {bl.x, bl.y, bl.z, bl.w, bh.x, bh.y, bh.z, bh.w};
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        if constexpr (FP8) {
-          const uint32_t w0[4] = {cur.r0[i].x, cur.r0[i].y, cur.r0[i].z, cur.r0[i].w};
-          const uint32_t w8[4] = {cur.r8[i].x, cur.r8[i].y, cur.r8[i].z, cur.r8[i].w};
+        for (int sp = 0; sp < 4; ++sp)
+          mma16816<FP8>(d, cvt_e4m3x2(w0[sp]), cvt_e4m3x2(w8[sp]), cvt_e4m3x2(w0[sp] >> 16),
+                        cvt_e4m3x2(w8[sp] >> 16), bw[2 * sp], bw[2 * sp + 1]);
+        // one 128-element scale block per group; rows g and g+8 may sit in different n-blocks
+        const int kbk = k0 >> 7;
+        const float s0 = bf16_to_f32(__ldg(a.S + (size_t)(r0 >> 7) * kb + kbk));  // read-only: L1 hits
+        const float s8 = bf16_to_f32(__ldg(a.S + (size_t)(r8 >> 7) * kb + kbk));
+        acc[0] = fmaf(d[0], s0, acc[0]);
+        acc[1] = fmaf(d[1], s0, acc[1]);
+        acc[2] = fmaf(d[2], s8, acc[2]);
+        acc[3] = fmaf(d[3], s8, acc[3]);
+      } else {
+        const uint4 v0a = *reinterpret_cast<const uint4*>(st0 + q * 128 + 32 * t);
+        const uint4 v0b = *reinterpret_cast<const uint4*>(st0 + q * 128 + 32 * t + 16);
+        const uint4 v8a = *reinterpret_cast<const uint4*>(st8 + q * 128 + 32 * t);
+        const uint4 v8b = *reinterpret_cast<const uint4*>(st8 + q * 128 + 32 * t + 16);
+        const uint32_t w0[8] = {v0a.x, v0a.y, v0a.z, v0a.w, v0b.x, v0b.y, v0b.z, v0b.w};
+        const uint32_t w8[8] = {v8a.x, v8a.y, v8a.z, v8a.w, v8b.x, v8b.y, v8b.z, v8b.w};
 #pragma unroll
-          for (int sp = 0; sp < 4; ++sp)
-            mma16816<FP8>(d, cvt_e4m3x2(w0[sp]), cvt_e4m3x2(w8[sp]), cvt_e4m3x2(w0[sp] >> 16),
-                          cvt_e4m3x2(w8[sp] >> 16), bw[2 * sp], bw[2 * sp + 1]);
-          // one 128-element scale block per group; rows g and g+8 may sit in different n-blocks
-          const int kbk = q >> 1;
-          const int r0 = min(rg * kMmaRows + g, row_end - 1), r8 = min(rg * kMmaRows + g + 8, row_end - 1);
-          const float s0 = bf16_to_f32(__ldg(a.S + (size_t)(r0 >> 7) * kb + kbk));  // read-only: L1 hits
-          const float s8 = bf16_to_f32(__ldg(a.S + (size_t)(r8 >> 7) * kb + kbk));
-          acc[0] = fmaf(d[0], s0, acc[0]);
-          acc[1] = fmaf(d[1], s0, acc[1]);
-          acc[2] = fmaf(d[2], s8, acc[2]);
-          acc[3] = fmaf(d[3], s8, acc[3]);
-        } else {
-          const uint32_t w0[8] = {cur.r0[2 * i].x, cur.r0[2 * i].y, cur.r0[2 * i].z, cur.r0[2 * i].w,
-                                  cur.r0[2 * i + 1].x, cur.r0[2 * i + 1].y, cur.r0[2 * i + 1].z, cur.r0[2 * i + 1].w};
-          const uint32_t w8[8] = {cur.r8[2 * i].x, cur.r8[2 * i].y, cur.r8[2 * i].z, cur.r8[2 * i].w,
-                                  cur.r8[2 * i + 1].x, cur.r8[2 * i + 1].y, cur.r8[2 * i + 1].z, cur.r8[2 * i + 1].w};
+        for (int sp = 0; sp < 4; ++sp)
+          mma16816<FP8>(d, w0[2 * sp], w8[2 * sp], w0[2 * sp + 1], w8[2 * sp + 1], bw[2 * sp], bw[2 * sp + 1]);
 #pragma unroll
-          for (int sp = 0; sp < 4; ++sp)
-            mma16816<FP8>(d, w0[2 * sp], w8[2 * sp], w0[2 * sp + 1], w8[2 * sp + 1], bw[2 * sp], bw[2 * sp + 1]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[j] += d[j];
-        }
+        for (int i = 0; i < 4; ++i) acc[i] += d[i];
       }
     }
-    if ((u % nunit_rg) == nunit_rg - 1) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->empty[s]);
+    if (ch == nch - 1) {
       // row group done: this warp's 16 x MB tile goes to its own slots; the
       // epilogue adds the 16 warps in a fixed order (deterministic results)
       const int lr = (rg - rg_begin) * kMmaRows;
@@ -334,24 +495,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
-  };
-  // loads of the next unit are in flight while the current one is computed
-  for (int u = 0; u < nunit; u += 2) {
-    if (u + 1 < nunit) load_unit(u + 1, buf1);
-    if (!whole) prefetch_unit(u + 1 + kPrefetchUnits);
-    process(u, buf0);
-    if (u + 1 < nunit) {
-      if (u + 2 < nunit) load_unit(u + 2, buf0);
-      if (!whole) prefetch_unit(u + 2 + kPrefetchUnits);
-      process(u + 1, buf1);
-    }
   }
-  __syncthreads();
+  __syncthreads();  // all consumers and the producer (after its drain)
 
-  // ------------------------------------------------ epilogue (all threads)
+  // ------------------------------------------------ epilogue (consumer threads)
   const uint16_t* cw = reinterpret_cast<const uint16_t*>(epi_s);
   const uint16_t* rgp = cw + (size_t)rows_max * (a.dconv + 1);
-  for (int i = tid; i < nrows * mvalid; i += kMmaThreads) {
+  for (int i = tid; i < nrows * mvalid; i += kC) {
     const int r = i / mvalid, m = i % mvalid;
     const int n = row_begin + r;
     float sum = 0.0f;
@@ -386,9 +536,8 @@ static cudaError_t launch_mma_one(const GemvArgs& a, cudaStream_t s) {
   int grid = num_sms();
   if (grid > nrg) grid = nrg;
   const int rows_max = ((nrg + grid - 1) / grid) * kMmaRows;
-  const int kb = (a.K + 127) / 128;
-  const MmaLayout lay = mma_layout(a.K, rows_max, MB, kb, a.epi, a.dconv);
-  if (lay.total > 227 * 1024) return cudaErrorInvalidConfiguration;
+  const MmaLayout lay = mma_layout(a.K, FP8 ? 1 : 2, rows_max, MB, a.epi, a.dconv);
+  if (lay.stages < 2 || lay.total > 227 * 1024) return cudaErrorInvalidConfiguration;
   auto kern = gemv_mma_kernel<FP8, MB>;
   cudaError_t e = set_smem_once((const void*)kern, lay.total, done_mask);
   if (e != cudaSuccess) return e;

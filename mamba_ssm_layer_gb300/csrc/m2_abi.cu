@@ -279,24 +279,31 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   const size_t part_bytes = proj_part_bytes(d, B);
 
   cudaError_t e;
-  // Five kernels, each launched as a programmatic dependent of the previous
-  // one, so that a GEMV streams its weights while its predecessor drains.
+  // Each kernel is launched as a programmatic dependent of the previous one,
+  // so that a GEMV streams its weights while its predecessor drains.  With the
+  // decode GEMV (B <= 8) the two norms run inside the GEMVs' prologues: three
+  // kernels per step.  Otherwise (tensor-core projections) a norm kernel
+  // precedes each projection: five.
+  const bool fuse = !gemm_tc_supported(B, r.n_in, d.hidden, true) && gemv_mma_supported(B, d.hidden) &&
+                    gemv_mma_supported(B, r.d_inner) && d.gnorm_group == r.d_inner;
   // 1. input RMSNorm -> GEMV activation
   PrepArgs pa;
   memset(&pa, 0, sizeof(pa));
-  pa.mode = PREP_RMSNORM;
-  pa.x = hidden;
-  pa.ldx = d.hidden;
-  pa.w = L->norm_w;
-  pa.eps = d.eps_in;
-  pa.M = B;
-  pa.K = d.hidden;
-  pa.out = xn;
-  pa.ldo = d.hidden;
-  pa.f16 = proj_f16(L->in_proj, B) ? 1 : 0;
-  pa.unscale = us_in;
-  pa.pdl = 1;
-  if ((e = launch_prep(pa, stream))) return launch_status(e);
+  if (!fuse) {
+    pa.mode = PREP_RMSNORM;
+    pa.x = hidden;
+    pa.ldx = d.hidden;
+    pa.w = L->norm_w;
+    pa.eps = d.eps_in;
+    pa.M = B;
+    pa.K = d.hidden;
+    pa.out = xn;
+    pa.ldo = d.hidden;
+    pa.f16 = proj_f16(L->in_proj, B) ? 1 : 0;
+    pa.unscale = us_in;
+    pa.pdl = 1;
+    if ((e = launch_prep(pa, stream))) return launch_status(e);
+  }
   // 2+3. in_proj, conv1d update (bias, SiLU) in its epilogue
   GemvArgs ex;
   memset(&ex, 0, sizeof(ex));
@@ -307,8 +314,14 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   ex.xbc0 = r.d_inner;
   ex.d_xbc = r.d_xbc;
   ex.dconv = d.d_conv;
-  if ((e = proj(L->in_proj, xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex, us_in, 1, part,
-                part_bytes)))
+  if (fuse) {
+    ex.norm = NORM_RMS;
+    ex.norm_w = L->norm_w;
+    ex.norm_eps = d.eps_in;
+    ex.norm_inv_k = 1.0 / (double)d.hidden;
+  }
+  if ((e = proj(L->in_proj, fuse ? hidden : xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex,
+                fuse ? nullptr : us_in, 1, part, part_bytes)))
     return launch_status(e);
   // 4+5. split and SSM step (advances conv_pos)
   SsmArgs sa;
@@ -343,26 +356,40 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   }
   if ((e = launch_ssm_step(sa, stream))) return launch_status(e);
   // 6. gated RMSNorm -> GEMV activation
-  memset(&pa, 0, sizeof(pa));
-  pa.mode = PREP_GATED;
-  pa.y = y;
-  pa.ldy = r.d_inner;
-  pa.z = zxu;
-  pa.ldz = r.ldz;
-  pa.w = L->gnorm_w;
-  pa.eps = d.eps_gated;
-  pa.group = d.gnorm_group;
-  pa.M = B;
-  pa.K = r.d_inner;
-  pa.out = g;
-  pa.ldo = r.d_inner;
-  pa.f16 = proj_f16(L->out_proj, B) ? 1 : 0;
-  pa.unscale = us_out;
-  pa.pdl = 1;
-  if ((e = launch_prep(pa, stream))) return launch_status(e);
+  if (!fuse) {
+    memset(&pa, 0, sizeof(pa));
+    pa.mode = PREP_GATED;
+    pa.y = y;
+    pa.ldy = r.d_inner;
+    pa.z = zxu;
+    pa.ldz = r.ldz;
+    pa.w = L->gnorm_w;
+    pa.eps = d.eps_gated;
+    pa.group = d.gnorm_group;
+    pa.M = B;
+    pa.K = r.d_inner;
+    pa.out = g;
+    pa.ldo = r.d_inner;
+    pa.f16 = proj_f16(L->out_proj, B) ? 1 : 0;
+    pa.unscale = us_out;
+    pa.pdl = 1;
+    if ((e = launch_prep(pa, stream))) return launch_status(e);
+  }
   // 7+8. out_proj with the residual add in its epilogue (in place on hidden)
-  if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out,
-                1, part, part_bytes)))
+  GemvArgs eo;
+  memset(&eo, 0, sizeof(eo));
+  if (fuse) {
+    eo.norm = NORM_GATED;
+    eo.norm_w = L->gnorm_w;
+    eo.norm_eps = d.eps_gated;
+    eo.norm_inv_k = 1.0 / (double)r.d_inner;
+    eo.gy = y;
+    eo.ldgy = r.d_inner;
+    eo.gz = zxu;
+    eo.ldgz = r.ldz;
+  }
+  if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, &eo,
+                fuse ? nullptr : us_out, 1, part, part_bytes)))
     return launch_status(e);
   return M2_OK;
 }

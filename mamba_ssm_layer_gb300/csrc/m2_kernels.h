@@ -86,6 +86,22 @@ struct GemvArgs {
   // tensor-core GEMM only: scratch for k-split partials (may be null: no split)
   float* part;
   size_t part_bytes;
+  // Decode GEMV only: the activation rows are computed in the GEMV's prologue
+  // from the norm's inputs instead of being read prepared (NORM_NONE).
+  int32_t norm;             // GemvNorm
+  const uint16_t* norm_w;   // [K] bf16 norm weight
+  float norm_eps;
+  double norm_inv_k;        // 1/K
+  const float* gy;          // NORM_GATED: y [M][ldgy] fp32, z [M][ldgz] bf16 (whole-row span)
+  int32_t ldgy;
+  const uint16_t* gz;
+  int32_t ldgz;
+};
+
+enum GemvNorm : int32_t {
+  NORM_NONE = 0,
+  NORM_RMS = 1,    // A rows are the hidden rows x: activation = bf16(x * r * w)
+  NORM_GATED = 2   // activation = bf16(y * r * w * silu(z)), r over the whole row
 };
 
 enum GemvAct : int32_t {
