@@ -258,6 +258,276 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_out_kernel(const SsdArg
 static int smem_state_bytes(int P, int N) { return (kQ * P + kQ * N) * 4; }
 static int smem_out_bytes(int P, int N) { return (N * kQ + (N > kQ ? N : kQ) * kQ + kQ * P + N * P) * 4; }
 
+// ------------------------------------------------------------------ tensor-core chunk kernels
+//
+// The same three products on warp MMA (m16n8k16, bf16 operands, fp32
+// accumulation).  x, B and C are bf16 values (the conv output's rounding
+// point), so C B^T, C h^T and x-side operands enter the MMA exactly.  The fp32
+// operands (the decay-weighted L, the carried state h_in and w_s x_s) are split
+// into two bf16 parts, v = hi + lo with hi = bf16(v), lo = bf16(v - hi), so each
+// product keeps about 16 significant bits and the sums stay fp32.  Shared
+// arrays are row-major with rows padded by 16 bytes (conflict-free ldmatrix).
+
+__device__ __forceinline__ void ldsm_x4(const void* p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(const void* p, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+__device__ __forceinline__ void ldsm_x2_t(const void* p, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// v = hi + lo, both bf16 (packed pairs)
+__device__ __forceinline__ void split2(float v0, float v1, uint32_t& hi, uint32_t& lo) {
+  const uint16_t h0 = f32_to_bf16(v0), h1 = f32_to_bf16(v1);
+  hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+  lo = (uint32_t)f32_to_bf16(v0 - bf16_to_f32(h0)) | ((uint32_t)f32_to_bf16(v1 - bf16_to_f32(h1)) << 16);
+}
+
+// Row-major bf16 tile [rows][cols] from global rows (ld elements apart) into
+// shared memory with pitch cols + 8; rows >= valid are zero.
+template <int COLS>
+__device__ __forceinline__ void stage_rows(uint16_t* dst, const uint16_t* src, size_t ld, int rows, int valid) {
+  constexpr int V = COLS / 8;  // 16-byte vectors per row
+  for (int i = threadIdx.x; i < rows * V; i += blockDim.x) {
+    const int r = i / V, v = i % V;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (r < valid) x = *reinterpret_cast<const uint4*>(src + (size_t)r * ld + v * 8);
+    *reinterpret_cast<uint4*>(dst + r * (COLS + 8) + v * 8) = x;
+  }
+}
+
+// dH[h][c] = sum_s w_s x_s B_s^T (P x N), w_s = exp(s_last - s_s) dt_s; decay = exp(s_last).
+template <int P, int N>
+__global__ void __launch_bounds__(kSsdThreads) ssd_state_mma_kernel(const SsdArgs a) {
+  constexpr int BP = N + 8, XP = P + 8;
+  const int h = blockIdx.x, c = blockIdx.y;
+  const int t0 = c * kQ, qc = min(kQ, a.T - t0);
+  const int g = h / (a.H / a.G);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float dt_s[kQ], cs_s[kQ];
+  extern __shared__ __align__(16) uint16_t sm16[];
+  uint16_t* Bs = sm16;                 // [Q][BP]
+  uint16_t* Wh = Bs + kQ * BP;         // [Q][XP]  hi part of w_s x_s
+  uint16_t* Wl = Wh + kQ * XP;         // [Q][XP]  lo part
+  chunk_decay(a, h, t0, qc, dt_s, cs_s);
+  stage_rows<N>(Bs, a.Bm + (size_t)t0 * a.ld_in + (size_t)g * N, a.ld_in, kQ, qc);
+  const float last = cs_s[max(qc - 1, 0)];
+  for (int i = threadIdx.x; i < kQ * (P / 2); i += blockDim.x) {
+    const int s_ = i / (P / 2), p2 = (i % (P / 2)) * 2;
+    float v0 = 0.0f, v1 = 0.0f;
+    if (s_ < qc) {
+      const uint32_t xx = *reinterpret_cast<const uint32_t*>(a.x + (size_t)(t0 + s_) * a.ld_in + (size_t)h * P + p2);
+      const float w = expf(last - cs_s[s_]) * dt_s[s_];
+      v0 = w * bf16lo(xx);
+      v1 = w * bf16hi(xx);
+    }
+    uint32_t hi, lo;
+    split2(v0, v1, hi, lo);
+    *reinterpret_cast<uint32_t*>(Wh + s_ * XP + p2) = hi;
+    *reinterpret_cast<uint32_t*>(Wl + s_ * XP + p2) = lo;
+  }
+  __syncthreads();
+  float* out = a.dH + ((size_t)h * a.nchunks + c) * P * N;
+  const int gq = lane >> 2, tq = lane & 3;
+  constexpr int units = (P / 16) * (N / 8);
+  for (int u = warp; u < units; u += kSsdThreads / 32) {
+    const int mp = u / (N / 8), j = u % (N / 8);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < kQ / 16; ++kk) {
+      uint32_t ah[4], al[4], b0, b1;
+      const int ar = 16 * kk + (lane & 7) + ((lane >> 4) & 1) * 8, ac = 16 * mp + ((lane >> 3) & 1) * 8;
+      ldsm_x4_t(Wh + ar * XP + ac, ah);
+      ldsm_x4_t(Wl + ar * XP + ac, al);
+      ldsm_x2_t(Bs + (16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8) * BP + 8 * j, b0, b1);
+      mma_bf16(acc, ah, b0, b1);
+      mma_bf16(acc, al, b0, b1);
+    }
+    const int p0 = 16 * mp + gq, n0 = 8 * j + 2 * tq;
+    *reinterpret_cast<float2*>(out + (size_t)p0 * N + n0) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2*>(out + (size_t)(p0 + 8) * N + n0) = make_float2(acc[2], acc[3]);
+  }
+  if (threadIdx.x == 0) a.decay[(size_t)h * a.nchunks + c] = expf(last);
+}
+
+// y for the chunk: warp w owns the 16 tokens [16w, 16w+16).
+//   G = C B^T (only s <= t), L = G * exp(s_t - s_s) * dt_s (mask s <= t),
+//   y = L x + exp(s_t) * (C h_in^T) + D x.
+template <int P, int N>
+__global__ void __launch_bounds__(kSsdThreads) ssd_out_mma_kernel(const SsdArgs a) {
+  constexpr int CP = N + 8, XP = P + 8;
+  static_assert(kSsdThreads / 32 * 16 == kQ, "one 16-token strip per warp");
+  const int h = blockIdx.x, c = blockIdx.y;
+  const int t0 = c * kQ, qc = min(kQ, a.T - t0);
+  const int g = h / (a.H / a.G);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  __shared__ float dt_s[kQ], cs_s[kQ];
+  extern __shared__ __align__(16) uint16_t sm16[];
+  uint16_t* Cs = sm16;             // [Q][CP]
+  uint16_t* Bs = Cs + kQ * CP;     // [Q][CP]
+  uint16_t* Xs = Bs + kQ * CP;     // [Q][XP]
+  uint16_t* Hh = Xs + kQ * XP;     // [P][CP]  hi part of h_in
+  uint16_t* Hl = Hh + P * CP;      // [P][CP]  lo part
+  chunk_decay(a, h, t0, qc, dt_s, cs_s);
+  stage_rows<N>(Cs, a.Cm + (size_t)t0 * a.ld_in + (size_t)g * N, a.ld_in, kQ, qc);
+  stage_rows<N>(Bs, a.Bm + (size_t)t0 * a.ld_in + (size_t)g * N, a.ld_in, kQ, qc);
+  stage_rows<P>(Xs, a.x + (size_t)t0 * a.ld_in + (size_t)h * P, a.ld_in, kQ, qc);
+  const float* hin = a.dH + ((size_t)h * a.nchunks + c) * P * N;
+  for (int i = threadIdx.x; i < P * N / 2; i += blockDim.x) {
+    const int pp = i / (N / 2), n2 = (i % (N / 2)) * 2;
+    const float2 v = *reinterpret_cast<const float2*>(hin + (size_t)pp * N + n2);
+    uint32_t hi, lo;
+    split2(v.x, v.y, hi, lo);
+    *reinterpret_cast<uint32_t*>(Hh + pp * CP + n2) = hi;
+    *reinterpret_cast<uint32_t*>(Hl + pp * CP + n2) = lo;
+  }
+  __syncthreads();
+  const int w = warp;
+  const int tr0 = 16 * w + gq, tr1 = tr0 + 8;  // this thread's two token rows
+  // ---- G = C B^T for s tiles 0 .. 2w+1
+  float G[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) G[j][0] = G[j][1] = G[j][2] = G[j][3] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < N / 16; ++kk) {
+    uint32_t af[4];
+    ldsm_x4(Cs + (16 * w + (lane & 15)) * CP + 16 * kk + (lane >> 4) * 8, af);
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+      if (jp <= w) {
+        uint32_t bf[4];
+        ldsm_x4(Bs + (16 * jp + (lane & 7) + ((lane >> 4) << 3)) * CP + 16 * kk + ((lane >> 3) & 1) * 8, bf);
+        mma_bf16(G[2 * jp], af, bf[0], bf[1]);
+        mma_bf16(G[2 * jp + 1], af, bf[2], bf[3]);
+      }
+    }
+  }
+  // ---- L (in place)
+  const float cs0 = cs_s[tr0], cs1 = cs_s[tr1];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j <= 2 * w + 1) {
+      const int s0 = 8 * j + 2 * tq, s1 = s0 + 1;
+      const float e00 = expf(fminf(cs0 - cs_s[s0], 0.0f)) * dt_s[s0], e01 = expf(fminf(cs0 - cs_s[s1], 0.0f)) * dt_s[s1];
+      const float e10 = expf(fminf(cs1 - cs_s[s0], 0.0f)) * dt_s[s0], e11 = expf(fminf(cs1 - cs_s[s1], 0.0f)) * dt_s[s1];
+      G[j][0] = s0 <= tr0 ? G[j][0] * e00 : 0.0f;
+      G[j][1] = s1 <= tr0 ? G[j][1] * e01 : 0.0f;
+      G[j][2] = s0 <= tr1 ? G[j][2] * e10 : 0.0f;
+      G[j][3] = s1 <= tr1 ? G[j][3] * e11 : 0.0f;
+    }
+  }
+  // ---- y_intra = L x
+  float Y[P / 8][4];
+#pragma unroll
+  for (int q = 0; q < P / 8; ++q) Y[q][0] = Y[q][1] = Y[q][2] = Y[q][3] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    if (kk <= w) {
+      uint32_t ah[4], al[4];
+      split2(G[2 * kk][0], G[2 * kk][1], ah[0], al[0]);
+      split2(G[2 * kk][2], G[2 * kk][3], ah[1], al[1]);
+      split2(G[2 * kk + 1][0], G[2 * kk + 1][1], ah[2], al[2]);
+      split2(G[2 * kk + 1][2], G[2 * kk + 1][3], ah[3], al[3]);
+#pragma unroll
+      for (int qp = 0; qp < P / 16; ++qp) {
+        uint32_t bf[4];
+        ldsm_x4_t(Xs + (16 * kk + (lane & 7) + ((lane >> 3) & 1) * 8) * XP + 16 * qp + (lane >> 4) * 8, bf);
+        mma_bf16(Y[2 * qp], ah, bf[0], bf[1]);
+        mma_bf16(Y[2 * qp], al, bf[0], bf[1]);
+        mma_bf16(Y[2 * qp + 1], ah, bf[2], bf[3]);
+        mma_bf16(Y[2 * qp + 1], al, bf[2], bf[3]);
+      }
+    }
+  }
+  // ---- y_inter = C h_in^T
+  float Yi[P / 8][4];
+#pragma unroll
+  for (int q = 0; q < P / 8; ++q) Yi[q][0] = Yi[q][1] = Yi[q][2] = Yi[q][3] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < N / 16; ++kk) {
+    uint32_t af[4];
+    ldsm_x4(Cs + (16 * w + (lane & 15)) * CP + 16 * kk + (lane >> 4) * 8, af);
+#pragma unroll
+    for (int qp = 0; qp < P / 16; ++qp) {
+      uint32_t bh[4], bl[4];
+      const int hr = 16 * qp + (lane & 7) + ((lane >> 4) << 3), hc = 16 * kk + ((lane >> 3) & 1) * 8;
+      ldsm_x4(Hh + hr * CP + hc, bh);
+      ldsm_x4(Hl + hr * CP + hc, bl);
+      mma_bf16(Yi[2 * qp], af, bh[0], bh[1]);
+      mma_bf16(Yi[2 * qp], af, bl[0], bl[1]);
+      mma_bf16(Yi[2 * qp + 1], af, bh[2], bh[3]);
+      mma_bf16(Yi[2 * qp + 1], af, bl[2], bl[3]);
+    }
+  }
+  // ---- y = y_intra + exp(s_t) y_inter + D x
+  const float Dh = a.D[h];
+  const float ex0 = expf(cs0), ex1 = expf(cs1);
+#pragma unroll
+  for (int q = 0; q < P / 8; ++q) {
+    const int p0 = 8 * q + 2 * tq;
+    if (tr0 < qc) {
+      const uint32_t xx = *reinterpret_cast<const uint32_t*>(Xs + tr0 * XP + p0);
+      float* yo = a.y + (size_t)(t0 + tr0) * a.ldy + (size_t)h * P + p0;
+      *reinterpret_cast<float2*>(yo) =
+          make_float2(Y[q][0] + ex0 * Yi[q][0] + Dh * bf16lo(xx), Y[q][1] + ex0 * Yi[q][1] + Dh * bf16hi(xx));
+    }
+    if (tr1 < qc) {
+      const uint32_t xx = *reinterpret_cast<const uint32_t*>(Xs + tr1 * XP + p0);
+      float* yo = a.y + (size_t)(t0 + tr1) * a.ldy + (size_t)h * P + p0;
+      *reinterpret_cast<float2*>(yo) =
+          make_float2(Y[q][2] + ex1 * Yi[q][2] + Dh * bf16lo(xx), Y[q][3] + ex1 * Yi[q][3] + Dh * bf16hi(xx));
+    }
+  }
+}
+
+template <int P, int N>
+constexpr int ssd_state_mma_smem() { return (kQ * (N + 8) + 2 * kQ * (P + 8)) * 2; }
+template <int P, int N>
+constexpr int ssd_out_mma_smem() { return (2 * kQ * (N + 8) + kQ * (P + 8) + 2 * P * (N + 8)) * 2; }
+
+// Shapes with tensor-core chunk kernels.
+static bool ssd_mma_shape(int P, int N) {
+  return (P == 64 && N == 128) || (P == 32 && N == 16) || (P == 64 && N == 64) || (P == 32 && N == 128);
+}
+
+template <int P, int N>
+static cudaError_t launch_ssd_mma_t(const SsdArgs& a, const dim3& grid, int which, cudaStream_t s) {
+  static int done_s[64], done_o[64];
+  if (which == 0) {
+    constexpr int smem = ssd_state_mma_smem<P, N>();
+    cudaError_t e = set_smem_once((const void*)ssd_state_mma_kernel<P, N>, smem, done_s);
+    if (e != cudaSuccess) return e;
+    ssd_state_mma_kernel<P, N><<<grid, kSsdThreads, smem, s>>>(a);
+  } else {
+    constexpr int smem = ssd_out_mma_smem<P, N>();
+    cudaError_t e = set_smem_once((const void*)ssd_out_mma_kernel<P, N>, smem, done_o);
+    if (e != cudaSuccess) return e;
+    ssd_out_mma_kernel<P, N><<<grid, kSsdThreads, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_ssd_mma(const SsdArgs& a, const dim3& grid, int which, cudaStream_t s) {
+  if (a.P == 64 && a.N == 128) return launch_ssd_mma_t<64, 128>(a, grid, which, s);
+  if (a.P == 32 && a.N == 16) return launch_ssd_mma_t<32, 16>(a, grid, which, s);
+  if (a.P == 64 && a.N == 64) return launch_ssd_mma_t<64, 64>(a, grid, which, s);
+  return launch_ssd_mma_t<32, 128>(a, grid, which, s);
+}
+
 bool ssd_supported(int H, int P, int N, int G) {
   if (G <= 0 || H % G || P % 8 || N % 4) return false;
   return smem_out_bytes(P, N) <= 227 * 1024 && smem_state_bytes(P, N) <= 227 * 1024;
@@ -280,19 +550,30 @@ cudaError_t launch_ssd(const SsdArgs& a0, cudaStream_t s) {
   e = set_smem_once((const void*)ssd_chunk_out_kernel, smem_out, done_out);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.H, a.nchunks);
+  const bool mma = ssd_mma_shape(a.P, a.N);
   trace_pre(K_SSD_CHUNK_STATE, s);
-  ssd_chunk_state_kernel<<<grid, kSsdThreads, smem_state, s>>>(a);
+  if (mma) {
+    e = launch_ssd_mma(a, grid, 0, s);
+  } else {
+    ssd_chunk_state_kernel<<<grid, kSsdThreads, smem_state, s>>>(a);
+    e = cudaGetLastError();
+  }
   trace_post(K_SSD_CHUNK_STATE, s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (e != cudaSuccess) return e;
   const size_t n4 = (size_t)a.H * a.P * a.N / 4;
   trace_pre(K_SSD_STATE_PASS, s);
   ssd_state_pass_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(a);
   trace_post(K_SSD_STATE_PASS, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   trace_pre(K_SSD_CHUNK_OUT, s);
-  ssd_chunk_out_kernel<<<grid, kSsdThreads, smem_out, s>>>(a);
+  if (mma) {
+    e = launch_ssd_mma(a, grid, 1, s);
+  } else {
+    ssd_chunk_out_kernel<<<grid, kSsdThreads, smem_out, s>>>(a);
+    e = cudaGetLastError();
+  }
   trace_post(K_SSD_CHUNK_OUT, s);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace m2
