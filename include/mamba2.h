@@ -141,6 +141,34 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* layer, uint16_t* h
                          float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
                          size_t ws_bytes, cudaStream_t stream);
 
+/* Prefill of a varlen batch of sequences in one call per kernel ("Trait
+ * TransformerLayer": `decode_batched` runs K tokens of one sequence with
+ * GEMM-batched projections, `decode_verify_multi` n sequences x k tokens in one
+ * weight sweep, rows sequence-major; the same batching serves prompts of
+ * different lengths).  Token rows cu_seqlens[i] .. cu_seqlens[i+1]-1 of hidden
+ * belong to sequence i; each sequence's result equals its own prefill (and so
+ * its T_i sequential decode steps).  K-token decode of n sequences is the case
+ * cu_seqlens = {0, K, 2K, ...}.
+ *   hidden      [T][hidden] bf16 in/out, T = cu_seqlens[nseq] >= 1.
+ *   nseq        number of sequences (>= 1); sequences of length 0 are allowed
+ *               and left untouched.
+ *   cu_seqlens  HOST array of nseq + 1 int32 offsets: cu_seqlens[0] = 0,
+ *               non-decreasing.  Read during the call only.
+ *   ssm_state   [nseq][nheads][head_dim][d_state] fp32, conv_state
+ *               [nseq][d_conv-1][d_xbc] bf16, conv_pos [nseq] int32: each
+ *               sequence's state before its block, left as the state after it
+ *               (conv_pos[i] += T_i).
+ *   ws          m2_workspace_bytes_varlen(dims, nseq, T) bytes suffice.
+ * The call enqueues one small host-to-device copy of the sequence tables into
+ * the workspace ahead of the kernels. */
+int mamba2_layer_prefill_varlen(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t nseq,
+                                const int32_t* cu_seqlens, float* ssm_state, uint16_t* conv_state,
+                                int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for mamba2_layer_prefill_varlen with at most max_seqs
+ * sequences and max_total_tokens token rows.  Returns 0 for invalid dims. */
+size_t m2_workspace_bytes_varlen(const m2_dims* dims, int32_t max_seqs, int32_t max_total_tokens);
+
 /* The w8a16 block-scaled GEMV/GEMM (page "Struct Qwen3SsmLayer",
  * `set_fp8_decode_weights`):
  *   out[m][n] = bf16( sum_k A[m][k] * E4M3(W[n][k]) * S[n/128][k/128] )

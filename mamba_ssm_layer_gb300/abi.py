@@ -32,7 +32,7 @@ M2_W_BF16 = 2
 
 # Every entry point include/mamba2.h declares (checked by the host tests).
 EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_decode", "mamba2_layer_prefill",
-           "mamba2_layer_decode_noalloc",
+           "mamba2_layer_decode_noalloc", "mamba2_layer_prefill_varlen", "m2_workspace_bytes_varlen",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
            "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count")
 
@@ -86,6 +86,11 @@ def lib():
             l.mamba2_layer_decode_noalloc.restype = C.c_int
             l.mamba2_layer_prefill.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P, SZ, P]
             l.mamba2_layer_prefill.restype = C.c_int
+            l.mamba2_layer_prefill_varlen.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32,
+                                                      C.POINTER(C.c_int32), P, P, P, P, SZ, P]
+            l.mamba2_layer_prefill_varlen.restype = C.c_int
+            l.m2_workspace_bytes_varlen.argtypes = [C.POINTER(M2Dims), I32, I32]
+            l.m2_workspace_bytes_varlen.restype = SZ
             l.w8a16_gemv.argtypes = [P, P, P, P, I32, I32, I32, P]; l.w8a16_gemv.restype = C.c_int
             l.conv1d_update.argtypes = [P, P, P, I32, P, P, P, I32, I32, I32, I32, P]; l.conv1d_update.restype = C.c_int
             l.mamba2_ssm_step.argtypes = [P, P, P, P, P, I32, P, P, P, P, I32, I32, I32, I32, I32, P]
@@ -171,6 +176,20 @@ def mamba2_layer_prefill(dims, layer, hidden, T, ssm_state, conv_state, conv_pos
     st = lib().mamba2_layer_prefill(C.byref(dims), C.byref(layer), _ptr(hidden), T, _ptr(ssm_state),
                                     _ptr(conv_state), _ptr(conv_pos), _ptr(ws), ws_bytes, _stream(stream))
     return _check("mamba2_layer_prefill", st) if check else st
+
+
+def mamba2_layer_prefill_varlen(dims, layer, hidden, cu_seqlens, ssm_state, conv_state, conv_pos, ws, ws_bytes,
+                                stream=None, check=True) -> int:
+    """cu_seqlens: host sequence of nseq + 1 token offsets."""
+    cu = (C.c_int32 * len(cu_seqlens))(*[int(v) for v in cu_seqlens])
+    st = lib().mamba2_layer_prefill_varlen(C.byref(dims), C.byref(layer), _ptr(hidden), len(cu_seqlens) - 1, cu,
+                                           _ptr(ssm_state), _ptr(conv_state), _ptr(conv_pos), _ptr(ws), ws_bytes,
+                                           _stream(stream))
+    return _check("mamba2_layer_prefill_varlen", st) if check else st
+
+
+def m2_workspace_bytes_varlen(dims: M2Dims, max_seqs: int, max_total_tokens: int) -> int:
+    return lib().m2_workspace_bytes_varlen(C.byref(dims), max_seqs, max_total_tokens)
 
 
 def w8a16_gemv(A, W, S, out, M, N, K, stream=None, check=True) -> int:

@@ -62,56 +62,98 @@ cudaError_t launch_conv_pos(int32_t* pos, int32_t B, int32_t add, cudaStream_t s
   return cudaGetLastError();
 }
 
-// Prefill conv over T tokens of one sequence.  A CTA owns 32 channels for all
-// T tokens (8 token lanes of 32 channels), so it can read the ring for the
-// first taps and afterwards overwrite it with the block's last tokens without
-// racing any other CTA.
-__global__ void __launch_bounds__(256) conv_prefill_kernel(uint16_t* __restrict__ ring,
+// Sequence of token row t in a varlen batch: the i with cu[i] <= t < cu[i+1]
+// (sequences of length 0 are skipped by taking the last such i).
+__device__ __forceinline__ int seq_of(const int32_t* cu, int n, int t) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Prefill conv over a varlen batch of sequences (token rows cu[i] .. cu[i+1]-1
+// belong to sequence i, whose ring and position are ring[i], pos[i]).  A thread
+// owns two adjacent channels and 8 consecutive token rows; the taps before a
+// sequence's first token come from its ring.  The ring is not written here
+// (other CTAs may still read it): conv_ring_store runs afterwards.
+__global__ void __launch_bounds__(256) conv_prefill_kernel(const uint16_t* __restrict__ ring,
                                                            const int32_t* __restrict__ pos,
                                                            const uint16_t* __restrict__ xbc, int ldx,
                                                            const uint16_t* __restrict__ w,
                                                            const uint16_t* __restrict__ bias,
                                                            uint16_t* __restrict__ u, int ldu, int T, int C,
-                                                           int dconv) {
-  const int c = blockIdx.x * 32 + (threadIdx.x & 31);
-  const int tl = threadIdx.x >> 5;
+                                                           int dconv, const int32_t* __restrict__ cu, int nseq) {
+  const int c = (blockIdx.x * 32 + (threadIdx.x & 31)) * 2;
+  const int tb = (blockIdx.y * 8 + (threadIdx.x >> 5)) * 8;
   const int L = dconv - 1;
-  const int p0 = pos[0];
-  if (c < C) {
-    float wl[8];
+  if (c >= C || tb >= T) return;
+  float w0[8], w1[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) wl[j] = j < dconv ? bf16_to_f32(w[(size_t)c * dconv + j]) : 0.0f;
-    const float bv = bias ? bf16_to_f32(bias[c]) : 0.0f;
-    for (int t = tl; t < T; t += 8) {
-      float s = bv;
+  for (int j = 0; j < 8; ++j) {
+    w0[j] = j < dconv ? bf16_to_f32(w[(size_t)c * dconv + j]) : 0.0f;
+    w1[j] = j < dconv ? bf16_to_f32(w[(size_t)(c + 1) * dconv + j]) : 0.0f;
+  }
+  const float b0 = bias ? bf16_to_f32(bias[c]) : 0.0f, b1 = bias ? bf16_to_f32(bias[c + 1]) : 0.0f;
 #pragma unroll
-      for (int j = 0; j < 7; ++j) {
-        if (j < L) {
-          const int src = t - L + j;  // token offset within the block (negative: history)
-          float v;
-          if (src >= 0) v = bf16_to_f32(xbc[(size_t)src * ldx + c]);
-          else v = bf16_to_f32(ring[(size_t)((((p0 + src) % L) + L) % L) * C + c]);
-          s = fmaf(wl[j], v, s);
+  for (int k = 0; k < 8; ++k) {
+    const int t = tb + k;
+    if (t < T) {
+      const int i = seq_of(cu, nseq, t);
+      const int start = cu[i];
+      float s0 = b0, s1 = b1;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j <= L) {
+          const int src = t - L + j;  // j == L: the current token
+          uint32_t v;
+          if (src >= start) {
+            v = *reinterpret_cast<const uint32_t*>(xbc + (size_t)src * ldx + c);
+          } else {  // history: the (start - src)-th token before the block, from the ring
+            const int slot = (((pos[i] + (src - start)) % L) + L) % L;
+            v = *reinterpret_cast<const uint32_t*>(ring + ((size_t)i * L + slot) * C + c);
+          }
+          s0 = fmaf(w0[j], bf16lo(v), s0);
+          s1 = fmaf(w1[j], bf16hi(v), s1);
         }
       }
-      s = fmaf(wl[L], bf16_to_f32(xbc[(size_t)t * ldx + c]), s);
-      u[(size_t)t * ldu + c] = f32_to_bf16(silu_f(s));
+      *reinterpret_cast<uint32_t*>(u + (size_t)t * ldu + c) = pack_bf16x2(silu_f(s0), silu_f(s1));
     }
   }
-  __syncthreads();
-  if (c < C && tl < L) {
-    const int t = T - L + tl;
-    if (t >= 0) ring[(size_t)((p0 + t) % L) * C + c] = xbc[(size_t)t * ldx + c];
+}
+
+// After the conv: each sequence's ring takes its last min(L, T_i) tokens, token
+// k of the block (0-based) into slot (pos[i] + k) mod L.  pos is not advanced.
+__global__ void __launch_bounds__(256) conv_ring_store_kernel(uint16_t* __restrict__ ring,
+                                                              const int32_t* __restrict__ pos,
+                                                              const uint16_t* __restrict__ xbc, int ldx, int C,
+                                                              int dconv, const int32_t* __restrict__ cu) {
+  const int i = blockIdx.y;
+  const int L = dconv - 1;
+  const int start = cu[i], len = cu[i + 1] - cu[i];
+  const int first = len > L ? len - L : 0;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < (len - first) * C; idx += gridDim.x * blockDim.x) {
+    const int k = first + idx / C, c = idx % C;
+    ring[((size_t)i * L + (pos[i] + k) % L) * C + c] = xbc[(size_t)(start + k) * ldx + c];
   }
 }
 
 cudaError_t launch_conv_prefill(uint16_t* ring, const int32_t* pos, const uint16_t* xbc, int32_t ldx,
                                 const uint16_t* w, const uint16_t* b, uint16_t* u, int32_t ldu, int32_t T,
-                                int32_t C, int32_t dconv, cudaStream_t s) {
+                                int32_t C, int32_t dconv, const int32_t* cu, int32_t nseq, cudaStream_t s) {
   trace_pre(K_CONV_PREFILL, s);
-  conv_prefill_kernel<<<(C + 31) / 32, 256, 0, s>>>(ring, pos, xbc, ldx, w, b, u, ldu, T, C, dconv);
+  const dim3 grid((C / 2 + 31) / 32, (T + 63) / 64);
+  conv_prefill_kernel<<<grid, 256, 0, s>>>(ring, pos, xbc, ldx, w, b, u, ldu, T, C, dconv, cu, nseq);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    conv_ring_store_kernel<<<dim3((C * (dconv - 1) + 255) / 256, nseq), 256, 0, s>>>(ring, pos, xbc, ldx, C, dconv,
+                                                                                  cu);
+    e = cudaGetLastError();
+  }
   trace_post(K_CONV_PREFILL, s);
-  return cudaGetLastError();
+  return e;
 }
 
 // ------------------------------------------------------------------ SSM step

@@ -29,6 +29,20 @@ namespace m2 {
 constexpr int kQ = 128;  // chunk length
 constexpr int kSsdThreads = 256;
 
+// Global chunk id -> sequence, first token row, valid tokens (<= 128), and the
+// sequence's token offset.
+__device__ __forceinline__ void chunk_info(const SsdArgs& a, int cid, int& seq, int& t0, int& qc) {
+  int lo = 0, hi = a.nseq - 1;
+  while (lo < hi) {  // last i with cprefix[i] <= cid
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.cprefix[mid] <= cid) lo = mid;
+    else hi = mid - 1;
+  }
+  seq = lo;
+  t0 = a.cu[lo] + (cid - a.cprefix[lo]) * kQ;
+  qc = min(kQ, a.cu[lo + 1] - t0);
+}
+
 // dt, inclusive cumulative log-decay and the last value for one chunk of one
 // head, into shared memory (Qc <= 128 valid tokens; the rest are zero).
 __device__ __forceinline__ void chunk_decay(const SsdArgs& a, int h, int t0, int qc, float* dt_s, float* cs_s) {
@@ -61,7 +75,8 @@ __device__ __forceinline__ void chunk_decay(const SsdArgs& a, int h, int t0, int
 // Thread tile: 8 p x 4 n (P = 64, N = 128 -> 256 threads; other shapes loop).
 __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdArgs a) {
   const int h = blockIdx.x, c = blockIdx.y;
-  const int t0 = c * kQ, qc = min(kQ, a.T - t0);
+  int seq, t0, qc;
+  chunk_info(a, c, seq, t0, qc);
   const int g = h / (a.H / a.G);
   __shared__ float dt_s[kQ], cs_s[kQ], w_s[kQ];
   extern __shared__ float dyn[];
@@ -110,17 +125,20 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_state_kernel(const SsdA
 
 // ------------------------------------------------------------------ state pass
 
-// Sequential over chunks for each state element (float4 of n): replaces dH[c]
-// with the state entering chunk c, and writes the final state into h.
+// Sequential over each sequence's chunks for each state element (float4 of n):
+// replaces dH[c] with the state entering chunk c and writes the final state
+// back.  Grid: (elements, sequences).
 __global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs a) {
+  const int seq = blockIdx.y;
   const size_t per_head = (size_t)a.P * a.N / 4;
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int c0 = a.cprefix[seq], c1 = a.cprefix[seq + 1];
   if (i < (size_t)a.H * per_head) {
     const int h = (int)(i / per_head);
     const size_t e = i % per_head;
-    float4* st = reinterpret_cast<float4*>(a.h) + i;
+    float4* st = reinterpret_cast<float4*>(a.h + (size_t)seq * a.H * a.P * a.N) + i;
     float4 cur = *st;
-    for (int c = 0; c < a.nchunks; ++c) {
+    for (int c = c0; c < c1; ++c) {
       float4* d = reinterpret_cast<float4*>(a.dH + ((size_t)h * a.nchunks + c) * a.P * a.N) + e;
       const float4 dh = *d;
       const float dec = a.decay[(size_t)h * a.nchunks + c];
@@ -132,7 +150,7 @@ __global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs a) {
     }
     *st = cur;
   }
-  if (a.pos_inc && blockIdx.x == 0 && threadIdx.x == 0) a.pos_inc[0] += a.T;
+  if (a.pos_inc && blockIdx.x == 0 && threadIdx.x == 0) a.pos_inc[seq] += a.cu[seq + 1] - a.cu[seq];
 }
 
 // ------------------------------------------------------------------ chunk outputs
@@ -144,7 +162,8 @@ __global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs a) {
 __global__ void __launch_bounds__(kSsdThreads) ssd_chunk_out_kernel(const SsdArgs a) {
   static_assert(kSsdThreads == (kQ / 8) * (kQ / 8), "one L tile per thread");
   const int h = blockIdx.x, c = blockIdx.y;
-  const int t0 = c * kQ, qc = min(kQ, a.T - t0);
+  int seq, t0, qc;
+  chunk_info(a, c, seq, t0, qc);
   const int g = h / (a.H / a.G);
   const int tid = threadIdx.x;
   __shared__ float dt_s[kQ], cs_s[kQ];
@@ -314,7 +333,8 @@ template <int P, int N>
 __global__ void __launch_bounds__(kSsdThreads) ssd_state_mma_kernel(const SsdArgs a) {
   constexpr int BP = N + 8, XP = P + 8;
   const int h = blockIdx.x, c = blockIdx.y;
-  const int t0 = c * kQ, qc = min(kQ, a.T - t0);
+  int seq, t0, qc;
+  chunk_info(a, c, seq, t0, qc);
   const int g = h / (a.H / a.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float dt_s[kQ], cs_s[kQ];
@@ -371,7 +391,8 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_mma_kernel(const SsdArgs 
   constexpr int CP = N + 8, XP = P + 8;
   static_assert(kSsdThreads / 32 * 16 == kQ, "one 16-token strip per warp");
   const int h = blockIdx.x, c = blockIdx.y;
-  const int t0 = c * kQ, qc = min(kQ, a.T - t0);
+  int seq, t0, qc;
+  chunk_info(a, c, seq, t0, qc);
   const int g = h / (a.H / a.G);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -533,8 +554,19 @@ bool ssd_supported(int H, int P, int N, int G) {
   return smem_out_bytes(P, N) <= 227 * 1024 && smem_state_bytes(P, N) <= 227 * 1024;
 }
 
-size_t ssd_workspace_bytes(int T, int H, int P, int N) {
-  const size_t nc = (size_t)(T + kQ - 1) / kQ;
+int32_t ssd_chunk_table(const int32_t* cu, int32_t nseq, int32_t* tab) {
+  int32_t nc = 0;
+  for (int i = 0; i <= nseq; ++i) tab[i] = cu[i];
+  for (int i = 0; i < nseq; ++i) {
+    tab[nseq + 1 + i] = nc;
+    nc += (cu[i + 1] - cu[i] + kQ - 1) / kQ;
+  }
+  tab[2 * nseq + 1] = nc;
+  return nc;
+}
+
+size_t ssd_workspace_bytes(int nchunks, int H, int P, int N) {
+  const size_t nc = (size_t)nchunks;
   return ((nc * H * P * N * 4 + 255) / 256) * 256 + ((nc * H * 4 + 255) / 256) * 256;
 }
 
@@ -542,7 +574,6 @@ static int done_state[64], done_out[64];
 
 cudaError_t launch_ssd(const SsdArgs& a0, cudaStream_t s) {
   SsdArgs a = a0;
-  a.nchunks = (a.T + kQ - 1) / kQ;
   const int smem_state = smem_state_bytes(a.P, a.N);
   const int smem_out = smem_out_bytes(a.P, a.N);
   cudaError_t e = set_smem_once((const void*)ssd_chunk_state_kernel, smem_state, done_state);
@@ -562,7 +593,7 @@ cudaError_t launch_ssd(const SsdArgs& a0, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const size_t n4 = (size_t)a.H * a.P * a.N / 4;
   trace_pre(K_SSD_STATE_PASS, s);
-  ssd_state_pass_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, s>>>(a);
+  ssd_state_pass_kernel<<<dim3((unsigned)((n4 + 255) / 256), a.nseq), 256, 0, s>>>(a);
   trace_post(K_SSD_STATE_PASS, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   trace_pre(K_SSD_CHUNK_OUT, s);

@@ -140,7 +140,9 @@ static size_t proj_part_bytes(const m2_dims& d, int M) {
   return rup(a > b ? a : b, 256);
 }
 
-static size_t decode_ws(const m2_dims& d, int B) {
+// Decode workspace without (min) and with the tensor-core k-split partials;
+// a workspace between the two runs the projections without the split.
+static size_t decode_ws_min(const m2_dims& d, int B) {
   const Derived r = derive(d);
   size_t o = 0;
   o = rup(o + (size_t)B * d.hidden * 2, 256);
@@ -148,11 +150,13 @@ static size_t decode_ws(const m2_dims& d, int B) {
   o = rup(o + (size_t)B * r.d_inner * 4, 256);
   o = rup(o + (size_t)B * r.d_inner * 2, 256);
   o = rup(o + (size_t)2 * B * 4, 256);
-  o += proj_part_bytes(d, B);  // tensor-core k-split partials
   return o;
 }
+static size_t decode_ws(const m2_dims& d, int B) { return decode_ws_min(d, B) + proj_part_bytes(d, B); }
 
-static size_t prefill_ws(const m2_dims& d, int T) {
+// Prefill workspace for T token rows in nseq sequences with nchunks SSD chunks
+// in total (ceil(T_i / 128) summed; at most T / 128 + nseq).
+static size_t prefill_ws(const m2_dims& d, int T, int nseq, int nchunks) {
   const Derived r = derive(d);
   size_t o = 0;
   o = rup(o + (size_t)T * d.hidden * 2, 256);   // xn
@@ -161,10 +165,14 @@ static size_t prefill_ws(const m2_dims& d, int T) {
   o = rup(o + (size_t)T * r.d_inner * 4, 256);  // y
   o = rup(o + (size_t)T * r.d_inner * 2, 256);  // g
   o = rup(o + (size_t)2 * T * 4, 256);          // unscale
+  o = rup(o + (size_t)2 * (nseq + 1) * 4, 256); // token and chunk offsets of the sequences
   if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups))
-    o += ssd_workspace_bytes(T, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
+    o += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
   o += proj_part_bytes(d, T);  // tensor-core k-split partials
   return o;
+}
+static size_t prefill_ws_bound(const m2_dims& d, int T, int nseq) {
+  return prefill_ws(d, T, nseq, (T + 127) / 128 + nseq);
 }
 
 // Whether a projection over M rows consumes f16 prescaled activations (the
@@ -248,7 +256,8 @@ int m2_validate(const m2_dims* dims, const m2_layer* L) {
 
 size_t m2_workspace_bytes(const m2_dims* dims, int32_t max_batch, int32_t max_tokens) {
   if (check_dims(dims) || max_batch < 0 || max_tokens < 0) return 0;
-  const size_t a = decode_ws(*dims, max_batch), b = prefill_ws(*dims, max_tokens);
+  const size_t a = max_batch > 0 ? decode_ws(*dims, max_batch) : 0;
+  const size_t b = max_tokens > 0 ? prefill_ws_bound(*dims, max_tokens, 1) : 0;
   return a > b ? a : b;
 }
 
@@ -258,7 +267,7 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   if (st) return st;
   if (B <= 0 || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
   if (!al16(hidden) || !al16(ssm_state) || !al8(conv_state)) return M2_ERR_ALIGN;
-  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < decode_ws(*dims, B)) return M2_ERR_WORKSPACE;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < decode_ws_min(*dims, B)) return M2_ERR_WORKSPACE;
   const m2_dims& d = *dims;
   const Derived r = derive(d);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -276,7 +285,7 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   float* us_out = us_in + B;
   o = rup(o + (size_t)2 * B * 4, 256);
   float* part = reinterpret_cast<float*>(w8 + o);
-  const size_t part_bytes = proj_part_bytes(d, B);
+  const size_t part_bytes = ws_bytes >= decode_ws(d, B) ? proj_part_bytes(d, B) : 0;  // 0: no k split
 
   cudaError_t e;
   // Each kernel is launched as a programmatic dependent of the previous one,
@@ -394,14 +403,28 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   return M2_OK;
 }
 
-int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t T, float* ssm_state,
-                         uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace m2 {
+
+// Prefill of a varlen batch (cu: host token offsets, nseq + 1 entries).
+static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t nseq, const int32_t* cu,
+                        float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes,
+                        cudaStream_t stream) {
   int st = m2_validate(dims, L);
   if (st) return st;
-  if (T <= 0 || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
+  if (nseq <= 0 || !cu || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
+  if (cu[0] != 0) return M2_ERR_ARG;
+  for (int i = 0; i < nseq; ++i)
+    if (cu[i + 1] < cu[i]) return M2_ERR_ARG;
+  const int T = cu[nseq];
+  if (T <= 0) return M2_ERR_ARG;
   if (!al16(hidden) || !al16(ssm_state) || !al8(conv_state)) return M2_ERR_ALIGN;
-  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < prefill_ws(*dims, T)) return M2_ERR_WORKSPACE;
   const m2_dims& d = *dims;
+  std::vector<int32_t> tab(2 * (size_t)(nseq + 1));
+  const int nchunks = ssd_chunk_table(cu, nseq, tab.data());
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < prefill_ws(d, T, nseq, nchunks))
+    return M2_ERR_WORKSPACE;
   const Derived r = derive(d);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   size_t o = 0;
@@ -419,15 +442,21 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
   float* us_in = reinterpret_cast<float*>(w8 + o);
   float* us_out = us_in + T;
   o = rup(o + (size_t)2 * T * 4, 256);
+  int32_t* dtab = reinterpret_cast<int32_t*>(w8 + o);  // cu, then chunk offsets
+  o = rup(o + (size_t)2 * (nseq + 1) * 4, 256);
   const bool ssd = ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups);
   float* ssd_dh = reinterpret_cast<float*>(w8 + o);
-  const size_t nchunk = (size_t)(T + 127) / 128;
-  float* ssd_decay = reinterpret_cast<float*>(w8 + rup(o + nchunk * d.nheads * d.head_dim * d.d_state * 4, 256));
-  if (ssd) o += ssd_workspace_bytes(T, d.nheads, d.head_dim, d.d_state);
+  float* ssd_decay =
+      reinterpret_cast<float*>(w8 + rup(o + (size_t)nchunks * d.nheads * d.head_dim * d.d_state * 4, 256));
+  if (ssd) o += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);
   float* part = reinterpret_cast<float*>(w8 + o);
   const size_t part_bytes = proj_part_bytes(d, T);
 
   cudaError_t e;
+  // the sequence tables, stream-ordered before the kernels that read them
+  // (pageable source: the call returns once the bytes are staged)
+  if ((e = cudaMemcpyAsync(dtab, tab.data(), tab.size() * 4, cudaMemcpyHostToDevice, stream)))
+    return launch_status(e);
   PrepArgs pa;
   memset(&pa, 0, sizeof(pa));
   pa.mode = PREP_RMSNORM;
@@ -446,7 +475,7 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
                 part_bytes)))
     return launch_status(e);
   if ((e = launch_conv_prefill(conv_state, conv_pos, zx + r.d_inner, r.ldz, L->conv_w, L->conv_b, u, r.d_xbc, T,
-                               r.d_xbc, d.d_conv, stream)))
+                               r.d_xbc, d.d_conv, dtab, nseq, stream)))
     return launch_status(e);
   if (ssd) {
     SsdArgs sa;
@@ -471,29 +500,39 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
     sa.pos_inc = conv_pos;
     sa.dH = ssd_dh;
     sa.decay = ssd_decay;
+    sa.nchunks = nchunks;
+    sa.nseq = nseq;
+    sa.cu = dtab;
+    sa.cprefix = dtab + nseq + 1;
     if ((e = launch_ssd(sa, stream))) return launch_status(e);
   } else {
-    ScanArgs sa;
-    memset(&sa, 0, sizeof(sa));
-    sa.h = ssm_state;
-    sa.x = u;
-    sa.Bm = u + r.d_inner;
-    sa.Cm = u + r.d_inner + d.n_groups * d.d_state;
-    sa.dt = zx + r.d_inner + r.d_xbc;
-    sa.ld_in = r.d_xbc;
-    sa.ld_dt = r.ldz;
-    sa.A_log = L->A_log;
-    sa.D = L->D;
-    sa.dt_bias = L->dt_bias;
-    sa.y = y;
-    sa.ldy = r.d_inner;
-    sa.T = T;
-    sa.H = d.nheads;
-    sa.P = d.head_dim;
-    sa.N = d.d_state;
-    sa.G = d.n_groups;
-    sa.pos_inc = conv_pos;
-    if ((e = launch_ssm_scan_seq(sa, stream))) return launch_status(e);
+    // shapes without the chunked scan: the sequential scan, one sequence at a time
+    const size_t hstride = (size_t)d.nheads * d.head_dim * d.d_state;
+    for (int i = 0; i < nseq; ++i) {
+      const int Ti = cu[i + 1] - cu[i];
+      if (Ti == 0) continue;
+      ScanArgs sa;
+      memset(&sa, 0, sizeof(sa));
+      sa.h = ssm_state + (size_t)i * hstride;
+      sa.x = u + (size_t)cu[i] * r.d_xbc;
+      sa.Bm = sa.x + r.d_inner;
+      sa.Cm = sa.x + r.d_inner + d.n_groups * d.d_state;
+      sa.dt = zx + (size_t)cu[i] * r.ldz + r.d_inner + r.d_xbc;
+      sa.ld_in = r.d_xbc;
+      sa.ld_dt = r.ldz;
+      sa.A_log = L->A_log;
+      sa.D = L->D;
+      sa.dt_bias = L->dt_bias;
+      sa.y = y + (size_t)cu[i] * r.d_inner;
+      sa.ldy = r.d_inner;
+      sa.T = Ti;
+      sa.H = d.nheads;
+      sa.P = d.head_dim;
+      sa.N = d.d_state;
+      sa.G = d.n_groups;
+      sa.pos_inc = conv_pos + i;
+      if ((e = launch_ssm_scan_seq(sa, stream))) return launch_status(e);
+    }
   }
   memset(&pa, 0, sizeof(pa));
   pa.mode = PREP_GATED;
@@ -515,6 +554,28 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
                 0, part, part_bytes)))
     return launch_status(e);
   return M2_OK;
+}
+
+}  // namespace m2
+
+extern "C" {
+
+int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t T, float* ssm_state,
+                         uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (T <= 0) return M2_ERR_ARG;
+  const int32_t cu[2] = {0, T};
+  return prefill_impl(dims, L, hidden, 1, cu, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream);
+}
+
+int mamba2_layer_prefill_varlen(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t nseq,
+                                const int32_t* cu_seqlens, float* ssm_state, uint16_t* conv_state, int32_t* conv_pos,
+                                void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return prefill_impl(dims, L, hidden, nseq, cu_seqlens, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream);
+}
+
+size_t m2_workspace_bytes_varlen(const m2_dims* dims, int32_t max_seqs, int32_t max_total_tokens) {
+  if (check_dims(dims) || max_seqs <= 0 || max_total_tokens < 0) return 0;
+  return prefill_ws_bound(*dims, max_total_tokens, max_seqs);
 }
 
 int w8a16_gemv(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* out, int32_t M, int32_t N,
@@ -583,7 +644,7 @@ int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint
   int st = m2_validate(dims, layer);
   if (st) return st;
   if (B <= 0) return M2_ERR_ARG;
-  const size_t need = decode_ws(*dims, B);
+  const size_t need = decode_ws_min(*dims, B);
   if (need > (size_t)M2_NOALLOC_SCRATCH_BYTES) return M2_ERR_SCRATCH;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return M2_ERR_DEVICE;

@@ -208,12 +208,13 @@ bool gemv_mma_supported(int M, int K);
 cudaError_t launch_gemv_mma(const GemvArgs& a, bool fp8, cudaStream_t s);
 
 
-// Prefill conv over T tokens of one sequence: xbc rows ldx apart -> u [T][ldu];
-// reads the ring for the first d_conv-1 taps and leaves it holding the last
-// tokens.  Does not advance pos.
+// Prefill conv over a varlen batch: T token rows (xbc rows ldx apart -> u
+// [T][ldu]), rows cu[i] .. cu[i+1]-1 of sequence i (cu: device, nseq+1
+// entries); reads each sequence's ring [nseq][d_conv-1][C] for the first taps
+// and leaves it holding the sequence's last tokens.  Does not advance pos.
 cudaError_t launch_conv_prefill(uint16_t* ring, const int32_t* pos, const uint16_t* xbc, int32_t ldx,
                                 const uint16_t* w, const uint16_t* b, uint16_t* u, int32_t ldu, int32_t T,
-                                int32_t C, int32_t dconv, cudaStream_t s);
+                                int32_t C, int32_t dconv, const int32_t* cu, int32_t nseq, cudaStream_t s);
 
 // Sequential per-token scan of one sequence (T steps, state in registers).
 struct ScanArgs {
@@ -233,14 +234,16 @@ struct ScanArgs {
 };
 cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s);
 
-// Chunked (state-space dual) scan of one sequence, chunk length 128
-// (k_ssd.cu): chunk states, a sequential pass over chunk states, chunk outputs.
+// Chunked (state-space dual) scan of a varlen batch of sequences, chunk
+// length 128 (k_ssd.cu): chunk states, a sequential pass over each sequence's
+// chunk states, chunk outputs.  Sequence i owns token rows cu[i] .. cu[i+1]-1
+// and chunks cprefix[i] .. cprefix[i+1]-1 (ceil(T_i / 128) of them).
 struct SsdArgs {
-  float* h;            // [H][P][N], updated in place
-  const uint16_t* x;   // [T] rows ld_in apart
+  float* h;            // [nseq][H][P][N], updated in place
+  const uint16_t* x;   // token rows ld_in apart
   const uint16_t* Bm;
   const uint16_t* Cm;
-  const uint16_t* dt;  // [T] rows ld_dt apart
+  const uint16_t* dt;  // token rows ld_dt apart
   int32_t ld_in, ld_dt;
   const float* A_log;
   const float* D;
@@ -248,13 +251,18 @@ struct SsdArgs {
   float* y;            // [T][ldy]
   int32_t ldy;
   int32_t T, H, P, N, G;
-  int32_t* pos_inc;    // pos_inc[0] += T if non-null
-  float* dH;           // scratch [H][ceil(T/128)][P][N]
-  float* decay;        // scratch [H][ceil(T/128)]
-  int32_t nchunks;     // set by launch_ssd
+  int32_t* pos_inc;    // pos_inc[i] += T_i if non-null
+  float* dH;           // scratch [H][nchunks][P][N]
+  float* decay;        // scratch [H][nchunks]
+  int32_t nchunks;     // total chunks of all sequences
+  int32_t nseq;
+  const int32_t* cu;       // device [nseq + 1] token offsets
+  const int32_t* cprefix;  // device [nseq + 1] chunk offsets
 };
+// Chunks of a varlen batch and the host tables (cu then cprefix, 2 * (nseq + 1) ints).
+int32_t ssd_chunk_table(const int32_t* cu_host, int32_t nseq, int32_t* table_out);
 bool ssd_supported(int H, int P, int N, int G);
-size_t ssd_workspace_bytes(int T, int H, int P, int N);  // dH then decay, each 256-aligned
+size_t ssd_workspace_bytes(int nchunks, int H, int P, int N);  // dH then decay, each 256-aligned
 cudaError_t launch_ssd(const SsdArgs& a, cudaStream_t s);
 
 }  // namespace m2

@@ -22,14 +22,23 @@ class DeviceStack:
         """Per layer: (h [B,H,P,N] fp32, ring [B,d_conv-1,d_xbc] bf16 bits, pos [B] int32), zeroed."""
         return [dl.new_state(B, self.device) for dl in self.layers]
 
-    def workspace(self, max_batch: int, max_tokens: int) -> torch.Tensor:
-        n = max(abi.m2_workspace_bytes(dl.dims, max_batch, max_tokens) for dl in self.layers)
+    def workspace(self, max_batch: int, max_tokens: int, max_seqs: int = 1) -> torch.Tensor:
+        """Workspace for decode of max_batch sequences, single-sequence prefill of
+        max_tokens, and varlen prefill of max_seqs sequences with max_tokens rows."""
+        n = max(max(abi.m2_workspace_bytes(dl.dims, max_batch, max_tokens),
+                    abi.m2_workspace_bytes_varlen(dl.dims, max_seqs, max_tokens)) for dl in self.layers)
         return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
 
     def prefill(self, hidden: torch.Tensor, states, seq: int, ws: torch.Tensor, stream=None) -> None:
         """hidden [T, hidden] bf16 bits of sequence `seq`, transformed in place by every layer."""
         for dl, (h, ring, pos) in zip(self.layers, states):
             dl.prefill(hidden, (h[seq], ring[seq], pos[seq:seq + 1]), ws, stream)
+
+    def prefill_varlen(self, hidden: torch.Tensor, cu_seqlens, states, ws: torch.Tensor, stream=None) -> None:
+        """hidden [T, hidden]: all sequences' prompt rows (sequence i at rows
+        cu_seqlens[i] .. cu_seqlens[i+1]-1), through every layer in one call per layer."""
+        for dl, st in zip(self.layers, states):
+            dl.prefill_varlen(hidden, cu_seqlens, st, ws, stream)
 
     def decode(self, hidden: torch.Tensor, states, ws: torch.Tensor, stream=None) -> None:
         """hidden [B, hidden]: one token of each of the B sequences, in place through every layer."""

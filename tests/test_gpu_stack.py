@@ -5,7 +5,8 @@ of 64..512 tokens prefilled through every layer, then 256 batched decode steps
 
 The oracle follows one sampled sequence (the one with the shortest prompt)
 from the same seeded inputs on its own: all 8 layers, every prompt row and all
-256 decode outputs.  Sequences are independent, so the sampled sequence's
+256 decode outputs.  The GPU prefills the 16 prompts in one varlen call per
+layer.  Sequences are independent, so the sampled sequence's
 outputs and states are the oracle's quantities.
 
 Two comparisons:
@@ -93,13 +94,12 @@ def test_stack8_prefill_and_256_decode_steps_sampled_sequence():
     # ---- GPU: the whole workload
     stk = DeviceStack(layers)
     st = stk.new_state(S)
-    ws = stk.workspace(S, int(lens.max()))
-    prompt_out = None
-    for s in range(S):
-        x = to_dev(synth.stack_prompt(s, int(lens[s]), hid))
-        stk.prefill(x, st, s, ws)
-        if s == samp:
-            prompt_out = x
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    ws = stk.workspace(S, int(cu[-1]), S)
+    # all 16 prompts in one varlen prefill call per layer
+    xall = to_dev(np.concatenate([synth.stack_prompt(s, int(lens[s]), hid) for s in range(S)]))
+    stk.prefill_varlen(xall, cu, st, ws)
+    prompt_out = xall[int(cu[samp]):int(cu[samp + 1])]
     outs = torch.empty((steps, hid), dtype=torch.int16, device="cuda")
     for k in range(steps):
         x = to_dev(synth.stack_decode_rows(k, S, hid))

@@ -1,0 +1,135 @@
+"""GPU parity of the varlen prefill (several sequences of different lengths in
+one call per kernel; K-token decode of n sequences is the equal-length case)
+against the oracle, sequence by sequence: each sequence's prefill is by
+definition its T_i sequential decode steps, so the oracle runs them on that
+sequence's own state.  Rounding decisions and states are checked as in the
+single-sequence tests (tests/helpers.py)."""
+import numpy as np
+import pytest
+import torch
+
+from mamba_ssm_layer_gb300 import abi, synth
+from mamba_ssm_layer_gb300.layer import DeviceLayer, bits_u16, to_dev
+from oracle import oracle as orc
+from tests.helpers import TOL_BF16, TOL_STATE, FlipTracker, bf16_to_f64, floored_rel_err, state_rel_err
+from tests.test_gpu_parity import _codes_decode, _codes_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from __graft_entry__ import build
+    build()
+    abi.m2_device_status(clear=True)
+    yield
+    assert abi.m2_device_status() == abi.M2_OK
+
+
+def _varlen_case(lay, lens, warm, key):
+    """`warm` batched decode steps of all sequences, then one varlen prefill of
+    lens[i] tokens per sequence; every sequence checked against the oracle."""
+    d = lay["dims"]
+    hd = d["hidden"]
+    n = len(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(cu[-1])
+    dl = DeviceLayer(lay)
+    ol = orc.OracleLayer(lay)
+    st = dl.new_state(n)
+    ost = [ol.new_state() for _ in range(n)]
+    trk = [FlipTracker(d, lay["A_log"], lay["dt_bias"], lay["conv_w"]) for _ in range(n)]
+    wsd = dl.workspace(n, 0)
+    for t in range(warm):
+        hid = synth.make_hidden(n, hd, *key, 1000 + t)
+        x = to_dev(hid)
+        pos_before = st[2].cpu().numpy().copy()
+        dl.decode(x, st, wsd)
+        torch.cuda.synchronize()
+        r3, r4 = _codes_decode(wsd, n, lay, st, pos_before)
+        for i in range(n):
+            _, e3, e4 = ol.run_traced(np.ascontiguousarray(hid[i:i + 1]), *ost[i])
+            trk[i].token(r3[i], (e3[0][0], e3[1][0]), r4[i], (e4[0][0], e4[1][0]))
+    hid = synth.make_hidden(T, hd, *key, 0)
+    x = to_dev(hid)
+    ws = dl.workspace_varlen(n, T)
+    dl.prefill_varlen(x, cu, st, ws)
+    torch.cuda.synchronize()
+    assert abi.m2_device_status() == abi.M2_OK
+    r3, r4 = _codes_prefill(ws, T, lay)
+    got = bits_u16(x)
+    worst = 0.0
+    reps = []
+    h = st[0].cpu().numpy()
+    ring = bits_u16(st[1])
+    for i in range(n):
+        a, b = int(cu[i]), int(cu[i + 1])
+        ref = hid[a:b].copy()
+        if b > a:
+            _, e3, e4 = ol.run_traced(ref, *ost[i])
+            for t in range(b - a):
+                trk[i].token(r3[a + t], (e3[0][t], e3[1][t]), r4[a + t], (e4[0][t], e4[1][t]))
+            worst = max(worst, floored_rel_err(bf16_to_f64(got[a:b]), bf16_to_f64(ref), axis=-1))
+        reps.append(trk[i].check_state(h[i], ost[i][0]))
+        assert floored_rel_err(bf16_to_f64(ring[i]), bf16_to_f64(ost[i][1]), axis=-1) <= TOL_BF16, i
+        assert int(st[2][i]) == warm + (b - a), i  # positions: integer work
+    assert worst <= TOL_BF16, worst
+    print("varlen parity", lens, worst, reps)
+    return dl, st, hid, cu
+
+
+def test_varlen_tiny_mixed_lengths_with_empty_sequence():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    _varlen_case(lay, [5, 0, 130, 1, 127, 128, 3], 2, (synth.WL_TINY_DECODE, 70))
+
+
+def test_varlen_tiny_bf16_weights():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE, layer=2, in_fmt="bf16", out_fmt="bf16")
+    _varlen_case(lay, [9, 200, 4], 1, (synth.WL_TINY_DECODE, 71))
+
+
+def test_k_token_decode_8b_layer():
+    # speculative-verify shape: 4 sequences x 4 tokens after 3 ordinary decode steps
+    lay = synth.make_layer(synth.NEMOTRON_H_8B, synth.WL_8B_DECODE_B64)
+    _varlen_case(lay, [4, 4, 4, 4], 3, (synth.WL_8B_DECODE_B64, 72))
+
+
+def test_varlen_8b_layer_chunk_boundaries():
+    lay = synth.make_layer(synth.NEMOTRON_H_8B, synth.WL_8B_PREFILL_1K)
+    _varlen_case(lay, [200, 1, 129], 0, (synth.WL_8B_PREFILL_1K, 73))
+
+
+def test_varlen_equals_separate_prefills():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    lens = [70, 3, 129]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    hid = synth.make_hidden(int(cu[-1]), 256, 8, 8, 8)
+    dl = DeviceLayer(lay)
+    st1 = dl.new_state(len(lens))
+    x = to_dev(hid)
+    dl.prefill_varlen(x, cu, st1, dl.workspace_varlen(len(lens), int(cu[-1])))
+    st2 = dl.new_state(len(lens))
+    ws = dl.workspace(1, int(max(lens)))
+    outs = []
+    for i in range(len(lens)):
+        xi = to_dev(hid[cu[i]:cu[i + 1]])
+        dl.prefill(xi, (st2[0][i], st2[1][i], st2[2][i:i + 1]), ws)
+        outs.append(xi)
+    torch.cuda.synchronize()
+    sep = np.concatenate([bits_u16(o) for o in outs])
+    assert floored_rel_err(bf16_to_f64(bits_u16(x)), bf16_to_f64(sep), axis=-1) <= TOL_BF16
+    assert state_rel_err(st1[0].cpu().numpy(), st2[0].cpu().numpy()) <= TOL_STATE
+    assert np.array_equal(st1[2].cpu().numpy(), st2[2].cpu().numpy())
+
+
+def test_varlen_rejects_bad_offsets():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    dl = DeviceLayer(lay)
+    st = dl.new_state(2)
+    x = to_dev(synth.make_hidden(4, 256, 1, 1, 1))
+    ws = dl.workspace_varlen(2, 4)
+    n0 = abi.m2_launch_count()
+    for cu in ([1, 2, 4], [0, 3, 2], [0, 0, 0]):
+        st_code = abi.mamba2_layer_prefill_varlen(dl.dims, dl.struct, x, cu, *st, ws, ws.numel(), check=False)
+        assert st_code == abi.M2_ERR_ARG, cu
+    assert abi.m2_launch_count() == n0
