@@ -22,7 +22,7 @@
 //               (plain 2-D map) into a 4-stage ring; bf16 weights go straight
 //               into a 4-stage ring of 128-byte-swizzled tiles.  It does not
 //               wait for the previous kernel: weights are never its output.
-//   warp 10     activation producer (lane 0): after the dependency wait, TMA of
+//   warp 14     activation producer (lane 0): after the dependency wait, TMA of
 //               the bf16 activation tile [NT][128] (two 64-wide boxes, 128-byte
 //               swizzle = the UMMA K-major canonical layout), 3-4 stages;
 //   warps 2-5   converters: E4M3 tile -> bf16 tile in the swizzled layout the
@@ -30,7 +30,8 @@
 //   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each) per k block
 //               into one of 4 TMEM partial buffers and commits to the barriers
 //               that free the buffers it read and wake the epilogue;
-//   warps 6-9   epilogue: per k block, TMEM -> registers, acc += s * partial;
+//   warps 6-13  epilogue, two warps per TMEM lane quarter (each half of the
+//               token columns): per k block, TMEM -> registers, acc += s * partial;
 //               per item, the store / residual / conv-update epilogue, or fp32
 //               partials that a second kernel sums in split order.
 // Every wait is bounded (see mbar_wait); TMEM is freed on every exit path.
@@ -44,7 +45,8 @@
 
 namespace m2 {
 
-constexpr int kTcThreads = 352;  // 11 warps
+constexpr int kTcEpiWarps = 8;   // two per TMEM lane quarter, each half of the token columns
+constexpr int kTcThreads = 480;  // 15 warps
 constexpr int kTcWStages = 4;    // weight tiles in flight
 constexpr int kTcTmemBufs = 4;   // k-block partials in TMEM
 constexpr int kTcBM = 128;       // weight rows per tile (UMMA M)
@@ -84,6 +86,25 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// The same 2-D load delivered to the same shared-memory offset (and mbarrier)
+// of every CTA in the cluster named by mask.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // K-major operand descriptor, 128-byte swizzle: rows of 128 bytes, 8-row atoms
 // 1024 bytes apart (stride byte offset), leading byte offset unused.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -105,6 +126,13 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 // Arrives on the mbarrier once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+// The same, arriving on the mbarrier at this offset in every CTA of the mask.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_addr(bar)),
+               "h"(mask)
                : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -185,15 +213,23 @@ struct TcArgs {
   int32_t fp8;
   int32_t ksplit;  // > 1: k blocks split over work items, fp32 partials to `part`
   float* part;     // [ksplit][M][N]
+  int32_t cs;      // cluster size: the cs CTAs of a cluster take cs adjacent weight tiles of the same
+                   // token tile and k range, each loading 1/cs of the activation tile for all of them
 };
 
-// Work item i: tile i / ksplit (weight tile major, so the token tiles of one
-// weight tile are adjacent and its E4M3 bytes are re-read from L2), k range
-// ks = i % ksplit.
-__device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int& nt, int& mt, int& kb0, int& kb1) {
+// Work item i of a cluster (the same for its cs CTAs): token tile, k range and
+// a group of cs adjacent weight tiles, weight-tile-group major so that the
+// token tiles of one weight tile are adjacent and its bytes are re-read from
+// L2; this CTA takes the tile of its rank (past the last tile: a dummy that
+// repeats the last tile's loads and stores nothing).
+__device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int rank, int& nt, int& mt, int& kb0, int& kb1,
+                                        bool& real) {
   const int tile = item / ta.ksplit, ks = item % ta.ksplit;
-  nt = tile / ta.m_tiles;
+  const int ntg = tile / ta.m_tiles;
   mt = tile % ta.m_tiles;
+  nt = ntg * ta.cs + rank;
+  real = nt < ta.n_tiles;
+  if (!real) nt = ta.n_tiles - 1;
   kb0 = (int)((long long)ta.kblocks * ks / ta.ksplit);
   kb1 = (int)((long long)ta.kblocks * (ks + 1) / ta.ksplit);
 }
@@ -208,7 +244,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + Lay::kBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
+  const int ngroups = (ta.n_tiles + ta.cs - 1) / ta.cs;
+  const int nitems = ta.m_tiles * ngroups * ta.ksplit;  // per cluster
+  const int rank = ta.cs > 1 ? (int)cluster_rank() : 0;
+  const int cid = blockIdx.x / ta.cs, ncl = gridDim.x / ta.cs;
+  const uint16_t cmask = (uint16_t)((1u << ta.cs) - 1u);
   const int L = a.dconv - 1;
 
   if (tid == 0) {
@@ -222,11 +262,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(&bars->a_full[s], 1);
-      mbar_init(&bars->a_empty[s], 1);
+      mbar_init(&bars->a_empty[s], ta.cs);  // the MMA commits of every CTA of the cluster
     }
     for (int b = 0; b < kTcTmemBufs; ++b) {
       mbar_init(&bars->mma_done[b], 1);
-      mbar_init(&bars->tmem_empty[b], 4);
+      mbar_init(&bars->tmem_empty[b], kTcEpiWarps);
     }
     fence_mbar_init();
   }
@@ -240,6 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (ta.cs > 1) cluster_sync_all();  // every CTA's barriers exist before any multicast lands
   const uint32_t tmem = bars->tmem_base;
   bool dead = false;
 
@@ -250,9 +291,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint64_t polw = policy_evict_normal();  // weight tiles are re-read by the token tiles
       int gk = 0;
-      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+      for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        tc_item(ta, item, nt, mt, kb0, kb1);
+        bool real;
+        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages;
           if (gk >= kTcWStages && !mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)) dead = true;
@@ -269,34 +311,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == 14) {
     // -------------------------------------------------------- activation producer
     pdl_wait();  // A is written by the previous kernel
     if (lane == 0) {
       const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
       int gk = 0;
-      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+      for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        tc_item(ta, item, nt, mt, kb0, kb1);
+        bool real;
+        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % SA;
           if (gk >= SA && !mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)) dead = true;
           if (dead) break;
           uint8_t* abuf = smem + Lay::kA + s * NT * kTcBK * 2;
-          mbar_arrive_expect_tx(&bars->a_full[s], NT * kTcBK * 2);
-          tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
-          tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
+          mbar_arrive_expect_tx(&bars->a_full[s], NT * kTcBK * 2);  // from all cs slices
+          if (ta.cs == 1) {
+            tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
+            tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
+          } else {
+            // rows [rank*NT/cs, (rank+1)*NT/cs) of the tile, to every CTA of the cluster
+            const int rs = NT / ta.cs, r0 = rank * rs;
+            tma_load_2d_mc(abuf + r0 * 128, &tmA, kb * kTcBK, mt * NT + r0, &bars->a_full[s], cmask, pola);
+            tma_load_2d_mc(abuf + NT * 128 + r0 * 128, &tmA, kb * kTcBK + 64, mt * NT + r0, &bars->a_full[s], cmask,
+                           pola);
+          }
         }
       }
+      // drain: every CTA of the cluster has finished reading the last stages
+      // (their commits arrive here) before this CTA may exit
+      if (ta.cs > 1)
+        for (int k = max(0, gk - SA); k < gk && !dead; ++k)
+          if (!mbar_wait(&bars->a_empty[k % SA], (k / SA) & 1)) dead = true;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc_idesc(kTcBM, NT);
       int gk = 0;
-      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+      for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        tc_item(ta, item, nt, mt, kb0, kb1);
+        bool real;
+        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1, sa = gk % SA, tb = gk % kTcTmemBufs;
           if (ta.fp8) {
@@ -320,7 +377,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_mma(tmem + tb * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
           }
           tc_commit(&bars->mma_done[tb]);
-          tc_commit(&bars->a_empty[sa]);
+          if (ta.cs > 1) tc_commit_mc(&bars->a_empty[sa], cmask);
+          else tc_commit(&bars->a_empty[sa]);
           tc_commit(ta.fp8 ? &bars->wbf_empty[b] : &bars->w_empty[s]);
         }
       }
@@ -330,9 +388,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (ta.fp8) {
       const int ct = tid - 64;  // 0..127
       int gk = 0;
-      for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+      for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        tc_item(ta, item, nt, mt, kb0, kb1);
+        bool real;
+        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1;
           if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
@@ -372,17 +431,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // -------------------------------------------------------- epilogue
-    const int q = warp & 3;         // TMEM lane quarter of this warp
+    // warps 6..13: TMEM lane quarter warp % 4 (a warp reaches only its own
+    // quarter), token columns [hf * NT/2, (hf + 1) * NT/2)
+    constexpr int HC = NT / 2;
+    const int q = warp & 3;
+    const int hf = (warp - 6) >> 2;
     const int row = 32 * q + lane;  // weight row within the tile
     pdl_wait();
-    float acc[NT];
+    float acc[HC];
     int gk = 0;
-    for (int item = blockIdx.x; item < nitems && !dead; item += gridDim.x) {
+    for (int item = cid; item < nitems && !dead; item += ncl) {
       int nt, mt, kb0, kb1;
-      tc_item(ta, item, nt, mt, kb0, kb1);
+      bool real;
+      tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
       const int ks = item % ta.ksplit;
 #pragma unroll
-      for (int j = 0; j < NT; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < HC; ++j) acc[j] = 0.0f;
       for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
         const int tb = gk % kTcTmemBufs;
         const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb)) : 1.0f;
@@ -390,9 +454,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (dead) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < NT / 32; ++c) {
+        for (int c = 0; c < HC / 32; ++c) {
           float v[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + c * 32, v);
+          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 32, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, v[i], acc[c * 32 + i]);
         }
@@ -402,12 +466,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (dead) break;
       const int n = nt * kTcBM + row;
-      if (n < a.N) {
+      if (real && n < a.N) {
         if (ta.ksplit > 1) {
           float* pp = ta.part + ((size_t)ks * a.M) * a.N + n;
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const int m = mt * NT + j;
+          for (int j = 0; j < HC; ++j) {
+            const int m = mt * NT + hf * HC + j;
             if (m < a.M) pp[(size_t)m * a.N] = acc[j];
           }
         } else {
@@ -415,8 +479,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ConvTaps taps;
           if (conv) load_taps(a, n - a.xbc0, L, taps);
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const int m = mt * NT + j;
+          for (int j = 0; j < HC; ++j) {
+            const int m = mt * NT + hf * HC + j;
             if (m < a.M) tc_epi_elem(a, m, n, acc[j], conv, taps, L);
           }
         }
@@ -514,9 +578,6 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64, NT,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
   TcArgs ta;
   ta.g = g;
   ta.m_tiles = (g.M + NT - 1) / NT;
@@ -526,15 +587,21 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   ta.ksplit = gemm_tc_ksplit(g.M, g.N, g.K);
   ta.part = g.part;
   if (ta.ksplit > 1 && (!g.part || g.part_bytes < gemm_tc_partial_bytes(g.M, g.N, g.K))) ta.ksplit = 1;
+  // one CTA per cluster: sharing the activation tile across a cluster of CTAs
+  // by multicast (ta.cs > 1, supported by the kernel) measured slower here
+  ta.cs = 1;
+  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64, NT / ta.cs,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   const int smem = tc_smem_bytes<NT>();
   auto kern = gemm_tc_kernel<NT>;
   cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
   if (e != cudaSuccess) return e;
-  int grid = num_sms();
-  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
-  if (grid > nitems) grid = nitems;
+  const int nitems = ta.m_tiles * ((ta.n_tiles + ta.cs - 1) / ta.cs) * ta.ksplit;  // per cluster
+  int clusters = num_sms() / ta.cs;
+  if (clusters > nitems) clusters = nitems;
   trace_pre(K_GEMM_TC, s);
-  e = launch_k(kern, dim3(grid), dim3(kTcThreads), smem, s, g.pdl != 0, tmW, tmA, ta);
+  e = launch_kc(kern, dim3(clusters * ta.cs), dim3(kTcThreads), smem, s, g.pdl != 0, ta.cs, tmW, tmA, ta);
   trace_post(K_GEMM_TC, s);
   if (e != cudaSuccess || ta.ksplit == 1) return e;
   const size_t total = (size_t)g.M * g.N;
