@@ -146,13 +146,15 @@ cudaError_t launch_conv_prefill(uint16_t* ring, const int32_t* pos, const uint16
   trace_pre(K_CONV_PREFILL, s);
   const dim3 grid((C / 2 + 31) / 32, (T + 63) / 64);
   conv_prefill_kernel<<<grid, 256, 0, s>>>(ring, pos, xbc, ldx, w, b, u, ldu, T, C, dconv, cu, nseq);
+  trace_post(K_CONV_PREFILL, s);
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) {
+    trace_pre(K_CONV_RING, s);
     conv_ring_store_kernel<<<dim3((C * (dconv - 1) + 255) / 256, nseq), 256, 0, s>>>(ring, pos, xbc, ldx, C, dconv,
                                                                                   cu);
+    trace_post(K_CONV_RING, s);
     e = cudaGetLastError();
   }
-  trace_post(K_CONV_PREFILL, s);
   return e;
 }
 

@@ -76,7 +76,8 @@ static const char* kNames[K_COUNT] = {
     "norm_prep",     "gemv_fp8",        "gemv_fp8_inproj_conv", "gemv_fp8_outproj_resid",
     "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
     "conv_pos",      "ssm_step",        "conv_prefill",    "ssm_scan_seq",
-    "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out",   "gemm_tc_reduce"};
+    "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out",   "gemm_tc_reduce",
+    "conv_ring_store"};
 
 // ------------------------------------------------------------------ helpers
 

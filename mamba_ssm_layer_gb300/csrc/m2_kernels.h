@@ -29,6 +29,7 @@ enum KernelId : int32_t {
   K_SSD_STATE_PASS,
   K_SSD_CHUNK_OUT,
   K_GEMM_TC_REDUCE,
+  K_CONV_RING,
   K_COUNT
 };
 
