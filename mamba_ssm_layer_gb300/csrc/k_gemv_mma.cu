@@ -7,10 +7,11 @@
 // batch rows.  The GEMV is HBM-bound.  Register-destination loads keep too few
 // bytes in flight per SM to reach the HBM rate, so one producer warp streams
 // the weights with 1-D bulk copies (async proxy, mbarrier completion) through
-// a ring of shared-memory stages, each 16 rows x KC bytes (one copy per row,
-// rows padded by 64 bytes so that the fragment loads below are free of bank
-// conflicts); the producer starts before the dependency wait, since weights
-// are never the previous kernel's output.
+// a ring of shared-memory stages, each 16 rows x KC bytes: one copy of the 16
+// whole rows when a row is at most 4 KB, else one copy per row with rows
+// padded by 64 bytes (conflict-free fragment loads); the producer starts
+// before the dependency wait, since weights are never the previous kernel's
+// output.
 //
 // 16 consumer warps split each stage's 64-element groups.  Lane (g, t) =
 // (lane/4, lane%4) reads, per group, the 16 weight bytes [16t, 16t+16) (E4M3;
@@ -42,12 +43,14 @@ struct MmaTail {
   float unscale[8];
   int32_t pos[8];
   uint64_t full[kMaxStages], empty[kMaxStages];
+  uint64_t epi_bar;  // epilogue inputs staged by bulk copies
 };
 
 // Shared-memory layout.  kc: bytes of a row per stage (a multiple of 64
 // elements); stages: ring depth.
 struct MmaLayout {
-  int act_ld, tail, act, tot, epi, stage, stage_bytes, kc, stages, total;
+  int act_ld, tail, act, tot, epi, stage, stage_bytes, kc, pitch, stages, total;
+  bool whole;  // a stage is one contiguous block of 16 whole rows (one copy, no row padding)
 };
 __host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int mb, int epi, int dconv) {
   MmaLayout L;
@@ -57,16 +60,23 @@ __host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int
   L.tot = L.act + ((mb + 1) * L.act_ld * 2 + 127) / 128 * 128;  // + one zero row for lanes past the batch
   L.epi = L.tot + (rows_max * kMmaWarps * mb * 4 + 127) / 128 * 128;  // per-warp partials
   int epi_bytes = 0;
-  if (epi == EPI_INPROJ_CONV) epi_bytes = rows_max * (dconv + 1) * 2 + mb * rows_max * (dconv - 1) * 2;
+  // conv: taps [rows_max][dconv], bias [rows_max], ring slots [mb][dconv-1][rows_max] (storage order)
+  if (epi == EPI_INPROJ_CONV) epi_bytes = rows_max * dconv * 2 + rows_max * 2 + mb * rows_max * (dconv - 1) * 2;
   if (epi == EPI_RESID) epi_bytes = mb * rows_max * 2;
   L.stage = L.epi + (epi_bytes + 127) / 128 * 128;
   const int budget = 227 * 1024 - L.stage;
   const int row_bytes = K * es;
-  // the largest chunk (<= 4 KB of a row) that leaves at least 3 stages, then as many stages as fit
+  // Rows of at most 4 KB whose 16-row groups fit 3 stages travel as one copy
+  // per row group (fewer, larger copies stream faster; the unpadded rows cost
+  // a 2-way bank conflict in the fragment loads).  Otherwise: the largest chunk
+  // (<= 4 KB of a row, rows padded) that leaves at least 3 stages.
+  L.whole = row_bytes <= 4096 && budget / (kMmaRows * row_bytes) >= 3;
   int kc = row_bytes < 4096 ? row_bytes : 4096;
-  while (kc > 64 * es && budget / (kMmaRows * (kc + kRowPad)) < 3) kc = (kc / 2 + 64 * es - 1) / (64 * es) * (64 * es);
+  if (!L.whole)
+    while (kc > 64 * es && budget / (kMmaRows * (kc + kRowPad)) < 3) kc = (kc / 2 + 64 * es - 1) / (64 * es) * (64 * es);
   L.kc = kc;
-  L.stage_bytes = kMmaRows * (kc + kRowPad);
+  L.pitch = L.whole ? row_bytes : kc + kRowPad;
+  L.stage_bytes = kMmaRows * L.pitch;
   L.stages = budget / L.stage_bytes;
   if (L.stages > kMaxStages) L.stages = kMaxStages;
   L.total = L.stage + L.stages * L.stage_bytes;
@@ -270,14 +280,33 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int row_bytes = a.K * ES;
   const int nch = (row_bytes + lay.kc - 1) / lay.kc;  // chunks (stages) per row group
   const int nst = nrg * nch;                          // stages this CTA streams
-  const int pitch = lay.kc + kRowPad;
+  const int pitch = lay.pitch;
   const int S = lay.stages;
+  // epilogue input regions of shared memory
+  uint16_t* cwS = reinterpret_cast<uint16_t*>(epi_s);  // conv taps [rows_max][dconv]
+  uint16_t* bS = cwS + (size_t)rows_max * a.dconv;      // conv bias [rows_max]
+  uint16_t* rgS = bS + rows_max;                         // ring slots [MB][L][rows_max], storage order
+  uint16_t* rsS = reinterpret_cast<uint16_t*>(epi_s);  // residual rows [MB][rows_max]
+  // this CTA's conv rows: local rows [rx0, rx0 + nx) = channels [cx0, cx0 + nx)
+  const int xa = max(row_begin, a.xbc0), xb = min(row_end, a.xbc0 + a.d_xbc);
+  const int nx = (a.epi == EPI_INPROJ_CONV && xb > xa) ? xb - xa : 0;
+  const int rx0 = nx ? xa - row_begin : 0, cx0 = nx ? xa - a.xbc0 : 0;
+  auto al16p = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  bool epi_bulk;
+  if (a.epi == EPI_INPROJ_CONV)
+    epi_bulk = nx > 0 && nx % 8 == 0 && cx0 % 8 == 0 && rx0 % 8 == 0 && a.d_xbc % 8 == 0 && a.conv_b &&
+               al16p(a.conv_w) && al16p(a.conv_b) && al16p(a.ring);
+  else if (a.epi == EPI_RESID)
+    epi_bulk = nrows % 8 == 0 && row_begin % 8 == 0 && a.ldr % 8 == 0 && al16p(a.resid);
+  else
+    epi_bulk = false;
 
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(&tail->full[i], 1);
       mbar_init(&tail->empty[i], kMmaWarps);
     }
+    mbar_init(&tail->epi_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -288,6 +317,28 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // Weights are never written by the previous kernel: stream without waiting.
     const uint64_t pol = a.evict_first ? policy_evict_first() : policy_evict_normal();
     const uint8_t* W = static_cast<const uint8_t*>(a.W);
+    if (epi_bulk && lane == 0) {
+      // epilogue inputs of this CTA's rows, a few contiguous ranges (weights,
+      // or state written by launches before the immediately preceding kernel)
+      const uint64_t pn = policy_evict_normal();
+      uint32_t bytes = 0;
+      if (a.epi == EPI_INPROJ_CONV) bytes = (uint32_t)(nx * (a.dconv + 1) * 2 + mvalid * L * nx * 2);
+      else bytes = (uint32_t)(mvalid * nrows * 2);
+      mbar_arrive_expect_tx(&tail->epi_bar, bytes);
+      if (a.epi == EPI_INPROJ_CONV) {
+        bulk_g2s(cwS + (size_t)rx0 * a.dconv, a.conv_w + (size_t)cx0 * a.dconv, (uint32_t)(nx * a.dconv * 2),
+                 &tail->epi_bar, pn);
+        bulk_g2s(bS + rx0, a.conv_b + cx0, (uint32_t)(nx * 2), &tail->epi_bar, pn);
+        for (int m = 0; m < mvalid; ++m)
+          for (int jj = 0; jj < L; ++jj)
+            bulk_g2s(rgS + ((size_t)m * L + jj) * rows_max + rx0, a.ring + ((size_t)m * L + jj) * a.d_xbc + cx0,
+                     (uint32_t)(nx * 2), &tail->epi_bar, pn);
+      } else {
+        for (int m = 0; m < mvalid; ++m)
+          bulk_g2s(rsS + (size_t)m * rows_max, a.resid + (size_t)m * a.ldr + row_begin, (uint32_t)(nrows * 2),
+                   &tail->epi_bar, pn);
+      }
+    }
     int j = 0;
     bool waited = false;
     for (; j < nst && !dead; ++j) {
@@ -302,12 +353,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       if (dead) break;
       const int rg = rg_begin + j / nch, ch = j % nch;
       const int cb = min(lay.kc, row_bytes - ch * lay.kc);  // bytes of each row in this chunk
-      if (lane == 0) mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(kMmaRows * cb));
-      __syncwarp();
-      if (lane < kMmaRows) {
-        const int r = min(rg * kMmaRows + lane, a.N - 1);  // rows past N repeat row N-1 (results unused)
-        bulk_g2s(stg + (size_t)s * lay.stage_bytes + (size_t)lane * pitch, W + (size_t)r * row_bytes + (size_t)ch * lay.kc,
-                 (uint32_t)cb, &tail->full[s], pol);
+      if (lay.whole) {
+        // rows rg*16 .. min(N, rg*16+16) are contiguous: one copy (rows past N stay stale, results unused)
+        if (lane == 0) {
+          const int nr = min(kMmaRows, a.N - rg * kMmaRows);
+          mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(nr * row_bytes));
+          bulk_g2s(stg + (size_t)s * lay.stage_bytes, W + (size_t)rg * kMmaRows * row_bytes, (uint32_t)(nr * row_bytes),
+                   &tail->full[s], pol);
+        }
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(kMmaRows * cb));
+        __syncwarp();
+        if (lane < kMmaRows) {
+          const int r = min(rg * kMmaRows + lane, a.N - 1);  // rows past N repeat row N-1 (results unused)
+          bulk_g2s(stg + (size_t)s * lay.stage_bytes + (size_t)lane * pitch,
+                   W + (size_t)r * row_bytes + (size_t)ch * lay.kc, (uint32_t)cb, &tail->full[s], pol);
+        }
       }
     }
     if (!waited) {
@@ -326,41 +387,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   // they come from launches before the immediately preceding kernel, which have
   // completed by now, so they are staged before the wait (L2 loads: not L1).
   constexpr int kC = kMmaWarps * 32;  // consumer threads
-  if (tid < 8) tail->pos[tid] = (a.epi == EPI_INPROJ_CONV && tid < mvalid) ? __ldcg(a.pos + tid) : 0;
-  if (a.epi == EPI_INPROJ_CONV) {
-    uint16_t* cw = reinterpret_cast<uint16_t*>(epi_s);      // [rows_max][dconv+1]
-    uint16_t* rgs = cw + (size_t)rows_max * (a.dconv + 1);  // [MB][L][rows_max]
-    for (int r = tid; r < nrows; r += kC) {
-      const int n = row_begin + r;
-      if (n < a.xbc0 || n >= a.xbc0 + a.d_xbc) continue;
-      const int c = n - a.xbc0;
-      uint16_t wv[9];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) wv[j] = j < a.dconv ? __ldg(a.conv_w + (size_t)c * a.dconv + j) : (uint16_t)0;
-      wv[8] = a.conv_b ? __ldg(a.conv_b + c) : (uint16_t)0;
-#pragma unroll
-      for (int m = 0; m < MB; ++m) {
-        if (m < mvalid) {
-          const int p = __ldcg(a.pos + m);
-          const uint16_t* ring = a.ring + (size_t)m * L * a.d_xbc;
-          uint16_t rv[7];
-#pragma unroll
-          for (int j = 0; j < 7; ++j) rv[j] = j < L ? __ldcg(ring + (size_t)((p + j) % L) * a.d_xbc + c) : (uint16_t)0;
-#pragma unroll
-          for (int j = 0; j < 7; ++j)
-            if (j < L) rgs[((size_t)m * L + j) * rows_max + r] = rv[j];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < a.dconv) cw[r * (a.dconv + 1) + j] = wv[j];
-      cw[r * (a.dconv + 1) + a.dconv] = wv[8];
+  // Epilogue inputs of this CTA's rows.  Under programmatic dependent launch
+  // they come from launches before the immediately preceding kernel, which have
+  // completed by now, so they may be read before the wait: by the producer's
+  // bulk copies when aligned (waited for only before the epilogue), else here
+  // (L2 loads: not L1).  The positions stay in registers until the epilogue.
+  const int pos_r = (a.epi == EPI_INPROJ_CONV && tid < mvalid) ? __ldcg(a.pos + tid) : 0;
+  if (!epi_bulk && a.epi == EPI_INPROJ_CONV) {
+    for (int r = rx0 + tid; r < rx0 + nx; r += kC) {
+      const int c = cx0 + (r - rx0);
+      for (int jj = 0; jj < a.dconv; ++jj) cwS[r * a.dconv + jj] = __ldg(a.conv_w + (size_t)c * a.dconv + jj);
+      bS[r] = a.conv_b ? __ldg(a.conv_b + c) : (uint16_t)0;
+      for (int m = 0; m < mvalid; ++m)
+        for (int jj = 0; jj < L; ++jj)
+          rgS[((size_t)m * L + jj) * rows_max + r] = __ldcg(a.ring + ((size_t)m * L + jj) * a.d_xbc + c);
     }
-  } else if (a.epi == EPI_RESID) {
-    uint16_t* rs = reinterpret_cast<uint16_t*>(epi_s);  // [MB][rows_max]
+  } else if (!epi_bulk && a.epi == EPI_RESID) {
     for (int i = tid; i < nrows * mvalid; i += kC) {
       const int m = i / nrows, r = i % nrows;
-      rs[m * rows_max + r] = __ldcg(a.resid + (size_t)m * a.ldr + row_begin + r);
+      rsS[m * rows_max + r] = __ldcg(a.resid + (size_t)m * a.ldr + row_begin + r);
     }
   }
   pdl_wait();
@@ -496,11 +541,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     }
   }
+  if (tid < 8) tail->pos[tid] = pos_r;
+  if (epi_bulk && !mbar_wait(&tail->epi_bar, 0)) dead = true;
   __syncthreads();  // all consumers and the producer (after its drain)
 
   // ------------------------------------------------ epilogue (consumer threads)
-  const uint16_t* cw = reinterpret_cast<const uint16_t*>(epi_s);
-  const uint16_t* rgp = cw + (size_t)rows_max * (a.dconv + 1);
   for (int i = tid; i < nrows * mvalid; i += kC) {
     const int r = i / mvalid, m = i % mvalid;
     const int n = row_begin + r;
@@ -510,16 +555,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const float accv = sum * tail->unscale[m];
     uint16_t* o = a.out + (size_t)m * a.ldo + n;
     if (a.epi == EPI_RESID) {
-      const float res = bf16_to_f32(reinterpret_cast<const uint16_t*>(epi_s)[m * rows_max + r]);
+      const float res = bf16_to_f32(rsS[m * rows_max + r]);
       *o = f32_to_bf16(res + accv);
     } else if (a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc) {
       // conv1d update with bias + SiLU; this thread alone owns (sequence m,
       // channel c) in this call, and the ring taps were staged before any write
       const uint16_t vb = f32_to_bf16(accv);  // rounding point of the in_proj output
       const int c = n - a.xbc0;
-      const uint16_t* w = cw + r * (a.dconv + 1);
-      float s = bf16_to_f32(w[a.dconv]);
-      for (int j = 0; j < L; ++j) s += bf16_to_f32(w[j]) * bf16_to_f32(rgp[((size_t)m * L + j) * rows_max + r]);
+      const uint16_t* w = cwS + r * a.dconv;
+      const int p = tail->pos[m];
+      float s = bf16_to_f32(bS[r]);
+      for (int j = 0; j < L; ++j) s += bf16_to_f32(w[j]) * bf16_to_f32(rgS[((size_t)m * L + (p + j) % L) * rows_max + r]);
       s += bf16_to_f32(w[L]) * bf16_to_f32(vb);
       *o = f32_to_bf16(silu_f(s));
       a.ring[(size_t)m * L * a.d_xbc + (size_t)(tail->pos[m] % L) * a.d_xbc + c] = vb;
