@@ -528,8 +528,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // epilogue adds the 16 warps in a fixed order (deterministic results)
       const int lr = (rg - rg_begin) * kMmaRows;
       const int c0 = 2 * t, c1 = 2 * t + 1;
-      float* t0 = tot + ((size_t)(lr + g) * kMmaWarps + warp) * MB;
-      float* t8 = tot + ((size_t)(lr + g + 8) * kMmaWarps + warp) * MB;
+      // tot [warp][rows_max][MB]: the epilogue's threads (consecutive rows) read
+      // consecutive words
+      float* t0 = tot + ((size_t)warp * rows_max + lr + g) * MB;
+      float* t8 = tot + ((size_t)warp * rows_max + lr + g + 8) * MB;
       if (c0 < MB) {
         t0[c0] = acc[0];
         t8[c0] = acc[2];
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int n = row_begin + r;
     float sum = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w) sum += tot[((size_t)r * kMmaWarps + w) * MB + m];
+    for (int w = 0; w < kMmaWarps; ++w) sum += tot[((size_t)w * rows_max + r) * MB + m];
     const float accv = sum * tail->unscale[m];
     uint16_t* o = a.out + (size_t)m * a.ldo + n;
     if (a.epi == EPI_RESID) {

@@ -97,6 +97,27 @@ __global__ void __launch_bounds__(256) conv_prefill_kernel(const uint16_t* __res
     w1[j] = j < dconv ? bf16_to_f32(w[(size_t)(c + 1) * dconv + j]) : 0.0f;
   }
   const float b0 = bias ? bf16_to_f32(bias[c]) : 0.0f, b1 = bias ? bf16_to_f32(bias[c + 1]) : 0.0f;
+  if (tb + 7 < T && dconv == 4) {
+    const int i = seq_of(cu, nseq, tb);
+    if (cu[i] <= tb - 3 && tb + 7 < cu[i + 1]) {
+      // common case: the 8 tokens and their 3 predecessors are rows of one
+      // sequence: the 11-row window is loaded once
+      uint32_t win[11];
+#pragma unroll
+      for (int r = 0; r < 11; ++r) win[r] = *reinterpret_cast<const uint32_t*>(xbc + (size_t)(tb - 3 + r) * ldx + c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float s0 = b0, s1 = b1;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          s0 = fmaf(w0[j], bf16lo(win[k + j]), s0);
+          s1 = fmaf(w1[j], bf16hi(win[k + j]), s1);
+        }
+        *reinterpret_cast<uint32_t*>(u + (size_t)(tb + k) * ldu + c) = pack_bf16x2(silu_f(s0), silu_f(s1));
+      }
+      return;
+    }
+  }
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int t = tb + k;
@@ -361,15 +382,18 @@ cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s) {
 // [2^14, 2^15); unscale = 2^-j).  The RMSNorm sum of squares is an error-free
 // fp32 pair and r is evaluated once in double, so its rounding decisions do
 // not depend on the summation order (norm_round_bf16).
-constexpr int kPrepThreads = 512;
-constexpr int kPrepMaxPer = 32;  // elements per thread (K <= 16384)
+constexpr int kPrepMaxPer = 32;  // elements per thread: K <= 32 * threads
 
+// One CTA of kPrepThreads threads per row (128 for K <= 4096, 256 for K <= 8192,
+// 512 above): small CTAs keep several rows resident per SM.
+template <int kPrepThreads>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+  constexpr int kW = kPrepThreads / 32;  // warps
   pdl_wait();
   pdl_trigger();
   const int m = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ float s_hi[16], s_lo[16], s_max[16];
+  __shared__ float s_hi[kW], s_lo[kW], s_max[kW];
   __shared__ float part[kPrepThreads * kPrepMaxPer / 8];  // gated mode: per-run sums of squares
   __shared__ double s_rd;
   const int K = a.K;
@@ -416,7 +440,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       // combine the warps' pairs, then r = 1/sqrt(mean + eps) from the fp32
       // estimate and one Newton step in double (relative error ~2^-44)
       float h = 0.0f, l = 0.0f;
-      for (int w = 0; w < 16; ++w) {
+      for (int w = 0; w < kW; ++w) {
         two_sum_acc(h, l, s_hi[w]);
         l += s_lo[w];
       }
@@ -460,7 +484,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 #pragma unroll
       for (int c = 0; c < kPrepMaxPer / 8; ++c) {
         const float ws = warp_sum(ssr[c]);
-        if (lane == 0) part[c * 16 + warp] = ws;  // chunk of 256 elements starting at (warp + 16c) * 256
+        if (lane == 0) part[c * kW + warp] = ws;  // chunk of 256 elements starting at (warp + kW c) * 256
       }
       __syncthreads();
       const int cpg = a.group / 256, ngroups = K / a.group;
@@ -517,7 +541,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
     __syncthreads();
     mx = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 16; ++w) mx = fmaxf(mx, s_max[w]);
+    for (int w = 0; w < kW; ++w) mx = fmaxf(mx, s_max[w]);
     const unsigned bits = __float_as_uint(mx);
     const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
     const int jx = max(-120, min(120, 14 - ex));
@@ -550,7 +574,10 @@ cudaError_t launch_prep(const PrepArgs& a0, cudaStream_t s) {
   PrepArgs a = a0;
   a.inv_k = 1.0 / (double)a.K;
   trace_pre(K_PREP, s);
-  cudaError_t e = launch_k(prep_kernel, dim3(a.M), dim3(kPrepThreads), 0, s, a.pdl != 0, a);
+  cudaError_t e;
+  if (a.K <= 128 * kPrepMaxPer) e = launch_k(prep_kernel<128>, dim3(a.M), dim3(128), 0, s, a.pdl != 0, a);
+  else if (a.K <= 256 * kPrepMaxPer) e = launch_k(prep_kernel<256>, dim3(a.M), dim3(256), 0, s, a.pdl != 0, a);
+  else e = launch_k(prep_kernel<512>, dim3(a.M), dim3(512), 0, s, a.pdl != 0, a);
   trace_post(K_PREP, s);
   return e;
 }

@@ -138,15 +138,28 @@ __global__ void __launch_bounds__(256) ssd_state_pass_kernel(const SsdArgs a) {
     const size_t e = i % per_head;
     float4* st = reinterpret_cast<float4*>(a.h + (size_t)seq * a.H * a.P * a.N) + i;
     float4 cur = *st;
-    for (int c = c0; c < c1; ++c) {
-      float4* d = reinterpret_cast<float4*>(a.dH + ((size_t)h * a.nchunks + c) * a.P * a.N) + e;
-      const float4 dh = *d;
-      const float dec = a.decay[(size_t)h * a.nchunks + c];
-      *d = cur;  // state entering chunk c
-      cur.x = fmaf(dec, cur.x, dh.x);
-      cur.y = fmaf(dec, cur.y, dh.y);
-      cur.z = fmaf(dec, cur.z, dh.z);
-      cur.w = fmaf(dec, cur.w, dh.w);
+    // the chunk states of up to 8 chunks are loaded together (independent of
+    // the carried state), then folded in order
+    for (int cb = c0; cb < c1; cb += 8) {
+      float4 dh[8];
+      float dec[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (cb + k < c1) {
+          dh[k] = *(reinterpret_cast<const float4*>(a.dH + ((size_t)h * a.nchunks + cb + k) * a.P * a.N) + e);
+          dec[k] = a.decay[(size_t)h * a.nchunks + cb + k];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (cb + k < c1) {
+          *(reinterpret_cast<float4*>(a.dH + ((size_t)h * a.nchunks + cb + k) * a.P * a.N) + e) = cur;  // state entering the chunk
+          cur.x = fmaf(dec[k], cur.x, dh[k].x);
+          cur.y = fmaf(dec[k], cur.y, dh[k].y);
+          cur.z = fmaf(dec[k], cur.z, dh[k].z);
+          cur.w = fmaf(dec[k], cur.w, dh[k].w);
+        }
+      }
     }
     *st = cur;
   }
