@@ -117,11 +117,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // computed into act (bf16, or f16 after the exact power-of-two prescale for
 // E4M3 weights, unscale[m] = 2^-j).  Same arithmetic as the separate norm
 // kernel (k_mixer.cu): the RMSNorm sum of squares as error-free fp32 pairs
-// and r in double, so its rounding decisions do not depend on the order; the
+// and near-tie decisions in double, so its rounding decisions do not depend on
+// the order; the
 // gated sum in a fixed order (every CTA computes the same row identically).
+// red[] (64 floats): warp partials; red[62..63] the combined pair.
 template <bool F16>
-__device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* red, double* red_d, float* unscale,
-                               int tid, int nC) {
+__device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* red, float* unscale, int tid,
+                               int nC) {
   const int K = a.K, warp = tid >> 5, lane = tid & 31;
   constexpr int kPer = 2;  // 16-byte chunks of 8 elements per thread (K <= 8192 with 512 threads)
   float v[kPer * 8];
@@ -168,20 +170,23 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
         two_sum_acc(h, l, red[w]);
         l += red[32 + w];
       }
-      const double vv = ((double)h + (double)l) * a.norm_inv_k + (double)a.norm_eps;
-      const double r0 = (double)rsqrtf((float)vv);
-      *red_d = r0 * (1.5 - 0.5 * vv * r0 * r0);
+      red[62] = h;
+      red[63] = l;
     }
     named_bar(1, nC);
-    const double rd = *red_d;
-    const float rf = (float)rd;
+    NormR nr;
+    nr.h = red[62];
+    nr.l = red[63];
+    nr.inv_k = a.norm_inv_k;
+    nr.eps = a.norm_eps;
+    const float rf = norm_rf(nr);
 #pragma unroll
     for (int c = 0; c < kPer; ++c) {
       const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        o[c * 8 + 2 * e] = norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, rd);
-        o[c * 8 + 2 * e + 1] = norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, rd);
+        o[c * 8 + 2 * e] = norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, nr);
+        o[c * 8 + 2 * e + 1] = norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, nr);
       }
     }
   } else {
@@ -416,9 +421,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   if (a.norm != NORM_NONE) {
     // the activation rows are this kernel's own norm of its inputs
     float* red = tot;  // scratch: tot is zeroed again below
-    double* red_d = reinterpret_cast<double*>(tot + 64);
     for (int m = 0; m < mvalid; ++m)
-      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, red_d, tail->unscale, tid, kC);
+      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, tail->unscale, tid, kC);
     const int kv = a.K / 8;
     for (int i = tid; i < kv; i += kC)  // zero row for lanes past the batch
       *reinterpret_cast<uint4*>(act_s + (size_t)MB * lay.act_ld + i * 8) = make_uint4(0u, 0u, 0u, 0u);

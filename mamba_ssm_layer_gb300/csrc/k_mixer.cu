@@ -395,7 +395,6 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ float s_hi[kW], s_lo[kW], s_max[kW];
   __shared__ float part[kPrepThreads * kPrepMaxPer / 8];  // gated mode: per-run sums of squares
-  __shared__ double s_rd;
   const int K = a.K;
   float v[kPrepMaxPer];
   uint4 wv[kPrepMaxPer / 8], zv[kPrepMaxPer / 8];  // issued with the inputs: independent loads
@@ -437,20 +436,22 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
     }
     __syncthreads();
     if (tid == 0) {
-      // combine the warps' pairs, then r = 1/sqrt(mean + eps) from the fp32
-      // estimate and one Newton step in double (relative error ~2^-44)
+      // combine the warps' pairs in a fixed order
       float h = 0.0f, l = 0.0f;
       for (int w = 0; w < kW; ++w) {
         two_sum_acc(h, l, s_hi[w]);
         l += s_lo[w];
       }
-      const double v = ((double)h + (double)l) * a.inv_k + (double)a.eps;
-      const double r0 = (double)rsqrtf((float)v);
-      s_rd = r0 * (1.5 - 0.5 * v * r0 * r0);
+      s_hi[0] = h;
+      s_lo[0] = l;
     }
     __syncthreads();
-    const double rd = s_rd;
-    const float rf = (float)rd;
+    NormR nr;
+    nr.h = s_hi[0];
+    nr.l = s_lo[0];
+    nr.inv_k = a.inv_k;
+    nr.eps = a.eps;
+    const float rf = norm_rf(nr);
 #pragma unroll
     for (int c = 0; c < kPrepMaxPer / 8; ++c) {
       const int k0 = (tid + kPrepThreads * c) * 8;
@@ -459,8 +460,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, rd));
-          v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, rd));
+          v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, nr));
+          v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, nr));
         }
       }
     }

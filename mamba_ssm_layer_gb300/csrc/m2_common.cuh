@@ -69,17 +69,36 @@ static __device__ __noinline__ uint16_t f64_to_bf16_rn(double v) {
   return f32_to_bf16(f);
 }
 
-// bf16(x * r * w) rounded as the exact product would round: the fp32 product
-// (<= 1.5 fp32 ulps from exact) decides unless it lies within 32 fp32 ulps of
-// a bf16 rounding tie; then the product in double (r given in double) decides.
-// This makes the RMSNorm's rounding point independent of summation order.
-static __device__ __noinline__ uint16_t norm_round_bf16_slow(float x, float w, double rd) {
-  return f64_to_bf16_rn((double)x * rd * (double)w);
+// r = 1/sqrt(mean + eps) of an RMSNorm row, from its sum of squares held as
+// an fp32 pair (h + l): rf is the fp32 estimate (all threads of a row compute
+// the same one); the double value, ~2^-44 accurate, is evaluated only where a
+// rounding decision needs it.
+struct NormR {
+  float h, l;     // sum of squares, error-free pair
+  double inv_k;   // 1 / K
+  float eps;
+};
+__device__ __forceinline__ float norm_rf(const NormR& n) {
+  return rsqrtf((n.h + n.l) * (float)n.inv_k + n.eps);
 }
-__device__ __forceinline__ uint16_t norm_round_bf16(float x, float w, float rf, double rd) {
+__device__ __forceinline__ double norm_rd(const NormR& n) {
+  const double v = ((double)n.h + (double)n.l) * n.inv_k + (double)n.eps;
+  const double r0 = (double)rsqrtf((float)v);
+  return r0 * (1.5 - 0.5 * v * r0 * r0);  // one Newton step
+}
+
+// bf16(x * r * w) rounded as the exact product would round: the fp32 product
+// (rf within ~3 fp32 ulps of r, so the product within ~4 ulps of exact) decides
+// unless it lies within 32 fp32 ulps of a bf16 rounding tie; then the product
+// in double (r in double) decides.  This makes the RMSNorm's rounding point
+// independent of summation order.
+static __device__ __noinline__ uint16_t norm_round_bf16_slow(float x, float w, NormR n) {
+  return f64_to_bf16_rn((double)x * norm_rd(n) * (double)w);
+}
+__device__ __forceinline__ uint16_t norm_round_bf16(float x, float w, float rf, const NormR& n) {
   const float v = x * rf * w;
   const int low = (int)(__float_as_uint(v) & 0xFFFFu);
-  if (abs(low - 0x8000) <= 32) return norm_round_bf16_slow(x, w, rd);  // rare; kept out of line
+  if (abs(low - 0x8000) <= 32) return norm_round_bf16_slow(x, w, n);  // rare; kept out of line
   return f32_to_bf16(v);
 }
 
