@@ -270,6 +270,79 @@ void or_gated_rmsnorm(const double* y, const uint16_t* z, const uint16_t* w, int
   }
 }
 
+/* ---------------------------------------------------------------- W8A8 arm */
+
+/* The W8A8 projections (FP8 activations as well as weights).  The pages give
+ * FP8 GEMMs and a bf16 -> FP8 activation conversion for prefill but not its
+ * scaling; the reading used here: per row and 128-element k block,
+ * amax = max |a|; the block's codes are E4M3(a * (448 / amax)) and its scale
+ * amax / 448, both computed in fp32 (an all-zero block has scale 0, codes 0).
+ * E4M3 rounding is round-to-nearest-even with saturation to +-448. */
+
+/* fp32 -> E4M3FN code, round to nearest even, saturating to +-448. */
+uint8_t or_f32_to_e4m3_sat(float v) {
+  uint8_t sign = signbit(v) ? 0x80 : 0;
+  double a = fabs((double)v);
+  if (a != a) return 0x7F; /* NaN (not produced by the quantizer) */
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormals: multiples of 2^-9; 8 * 2^-9 = 2^-6 is the first normal (code 0x08) */
+    double r = nearbyint(a * 512.0);
+    return sign | (uint8_t)r;
+  }
+  int e;
+  double f = frexp(a, &e);  /* a = f * 2^e, f in [0.5, 1) */
+  double r = nearbyint(f * 16.0); /* 8 + mantissa, in [8, 16] */
+  int E = e + 6;                  /* biased exponent of 2^(e-1) */
+  if (r == 16.0) {
+    r = 8.0;
+    E += 1;
+  }
+  if (E > 15 || (E == 15 && r - 8.0 > 6.0)) return sign | 0x7E;
+  return sign | (uint8_t)((E << 3) | ((int)r - 8));
+}
+
+/* One row a[K] (bf16) -> codes q[K] and block scales s[ceil(K/128)] (fp32). */
+void or_act_quant(const uint16_t* a, int K, uint8_t* q, float* s) {
+  int kb = (K + 127) / 128;
+  for (int b = 0; b < kb; ++b) {
+    int k0 = b * 128, k1 = k0 + 128 < K ? k0 + 128 : K;
+    float amax = 0.0f;
+    for (int k = k0; k < k1; ++k) {
+      float v = (float)fabs(bf(a[k]));
+      if (v > amax) amax = v;
+    }
+    if (amax == 0.0f) {
+      s[b] = 0.0f;
+      for (int k = k0; k < k1; ++k) q[k] = 0;
+      continue;
+    }
+    volatile float inv = 448.0f / amax; /* fp32 division, rounded */
+    for (int k = k0; k < k1; ++k) {
+      volatile float p = (float)bf(a[k]) * inv; /* fp32 product, rounded */
+      q[k] = or_f32_to_e4m3_sat(p);
+    }
+    s[b] = amax / 448.0f;
+  }
+}
+
+/* out[n] = sum over k blocks b of sa[b] * S[n/128][b] * sum_{k in b} E4M3(q[k]) * E4M3(W[n][k]). */
+void or_w8a8_gemv(const uint8_t* q, const float* sa, const uint8_t* W, const uint16_t* S, int N, int K,
+                  double* out) {
+  int kb = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int b = 0; b < kb; ++b) {
+      int k0 = b * 128, k1 = k0 + 128 < K ? k0 + 128 : K;
+      double part = 0.0;
+      for (int k = k0; k < k1; ++k) part += e4m3(q[k]) * e4m3(W[(size_t)n * K + k]);
+      acc += (double)sa[b] * bf(S[(size_t)(n / 128) * kb + b]) * part;
+    }
+    out[n] = acc;
+  }
+}
+
 /* ---------------------------------------------------------------- layer */
 
 typedef struct {
@@ -288,12 +361,23 @@ typedef struct {
   int out_fmt;
   const void* out_w;        /* [hidden][d_inner] */
   const uint16_t* out_s;    /* [ceil(hidden/128)][ceil(d_inner/128)] */
+  int act_fp8;              /* 1: E4M3 projections use the W8A8 arm (FP8 activations) */
 } or_layer;
 
-static void proj(int fmt, const void* w, const uint16_t* s, const uint16_t* a, int N, int K,
+static void proj(int fmt, int act_fp8, const void* w, const uint16_t* s, const uint16_t* a, int N, int K,
                  double* out) {
-  if (fmt == 1) or_w8a16_gemv(a, 1, (const uint8_t*)w, s, N, K, out);
-  else or_bf16_gemv(a, 1, (const uint16_t*)w, N, K, out);
+  if (fmt == 1 && act_fp8) {
+    uint8_t* q = (uint8_t*)malloc((size_t)K);
+    float* sa = (float*)malloc(sizeof(float) * (size_t)((K + 127) / 128));
+    or_act_quant(a, K, q, sa);
+    or_w8a8_gemv(q, sa, (const uint8_t*)w, s, N, K, out);
+    free(q);
+    free(sa);
+  } else if (fmt == 1) {
+    or_w8a16_gemv(a, 1, (const uint8_t*)w, s, N, K, out);
+  } else {
+    or_bf16_gemv(a, 1, (const uint16_t*)w, N, K, out);
+  }
 }
 
 /* One token of one sequence through the whole layer, steps 1..8 in the order
@@ -320,7 +404,7 @@ long or_layer_token_traced(const or_layer* L, uint16_t* hidden, double* hs, uint
   /* 1. RMSNorm (R2) */
   or_rmsnorm(hidden, L->norm_w, L->hidden, L->eps_in, xn);
   /* 2. in_proj -> [z, xBC, dt] (R3) */
-  proj(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, zx);
+  proj(L->in_fmt, L->act_fp8, L->in_w, L->in_s, xn, n_in, L->hidden, zx);
   for (int i = 0; i < n_in; ++i) zxb[i] = or_f64_to_bf16(zx[i]);
   if (tr_zx) memcpy(tr_zx, zx, sizeof(double) * n_in);
   if (tr_zx_abs) proj_abs(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, tr_zx_abs);
@@ -339,7 +423,7 @@ long or_layer_token_traced(const or_layer* L, uint16_t* hidden, double* hs, uint
   /* 6. gated RMSNorm (R5) */
   or_gated_rmsnorm(y, z, L->gnorm_w, d_inner, L->gnorm_group, L->eps_gated, gout);
   /* 7. out_proj, 8. residual add, rounded once (R6) */
-  proj(L->out_fmt, L->out_w, L->out_s, gout, L->hidden, d_inner, o);
+  proj(L->out_fmt, L->act_fp8, L->out_w, L->out_s, gout, L->hidden, d_inner, o);
   for (int i = 0; i < L->hidden; ++i) hidden[i] = or_f64_to_bf16(bf(hidden[i]) + o[i]);
 
   free(xn); free(zx); free(zxb); free(u); free(y); free(gout); free(o);

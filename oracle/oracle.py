@@ -64,6 +64,9 @@ def lib():
             l.or_layer_prefill_traced.argtypes = [P, P, C.c_int, P, P, P, P, P, P, P]
             l.or_layer_prefill_traced.restype = C.c_long
             l.or_f64_to_bf16_array.argtypes = [P, P, C.c_long]
+            l.or_f32_to_e4m3_sat.argtypes = [C.c_float]; l.or_f32_to_e4m3_sat.restype = u8
+            l.or_act_quant.argtypes = [P, C.c_int, P, P]
+            l.or_w8a8_gemv.argtypes = [P, P, P, P, C.c_int, C.c_int, P]
             l.or_init()
             _lib = l
     return _lib
@@ -179,6 +182,30 @@ def gated_rmsnorm(y: np.ndarray, z: np.ndarray, w: np.ndarray, group: int, eps: 
     return out
 
 
+def f32_to_e4m3_sat(v: float) -> int:
+    """fp32 -> E4M3FN code, round to nearest even, saturating to +-448."""
+    return int(lib().or_f32_to_e4m3_sat(float(np.float32(v))))
+
+
+def act_quant(a_bits: np.ndarray):
+    """One bf16 row [K] -> (E4M3 codes [K], fp32 block scales [ceil(K/128)]) of the W8A8 arm."""
+    a = _c(a_bits, np.uint16)
+    K = a.shape[0]
+    q = np.empty(K, np.uint8)
+    s = np.empty((K + 127) // 128, np.float32)
+    lib().or_act_quant(_p(a), K, _p(q), _p(s))
+    return q, s
+
+
+def w8a8_gemv(q: np.ndarray, sa: np.ndarray, W: np.ndarray, S: np.ndarray) -> np.ndarray:
+    """W8A8 product of one quantized row with E4M3 W [N][K] and bf16 block scales S (double)."""
+    q = _c(q, np.uint8); sa = _c(sa, np.float32); W = _c(W, np.uint8); S = _c(S, np.uint16)
+    N, K = W.shape
+    out = np.empty(N, np.float64)
+    lib().or_w8a8_gemv(_p(q), _p(sa), _p(W), _p(S), N, K, _p(out))
+    return out
+
+
 # ------------------------------------------------------------------ layer
 
 class _OrLayer(C.Structure):
@@ -188,7 +215,7 @@ class _OrLayer(C.Structure):
                 ("in_w", C.c_void_p), ("in_s", C.c_void_p), ("conv_w", C.c_void_p),
                 ("conv_b", C.c_void_p), ("A_log", C.c_void_p), ("D", C.c_void_p),
                 ("dt_bias", C.c_void_p), ("gnorm_w", C.c_void_p), ("out_fmt", C.c_int),
-                ("out_w", C.c_void_p), ("out_s", C.c_void_p)]
+                ("out_w", C.c_void_p), ("out_s", C.c_void_p), ("act_fp8", C.c_int)]
 
 
 class OracleLayer:
@@ -197,7 +224,8 @@ class OracleLayer:
     ``layer`` is the dict returned by ``mamba_ssm_layer_gb300.synth.make_layer``.
     """
 
-    def __init__(self, layer: dict):
+    def __init__(self, layer: dict, act_fp8: bool = False):
+        """act_fp8: the E4M3 projections take FP8 activations (the W8A8 arm)."""
         d = layer["dims"]
         self.dims = d
         keep = {}
@@ -213,6 +241,7 @@ class OracleLayer:
         s.eps_in, s.eps_gated = d["eps"], d["eps"]
         s.in_fmt = 1 if layer["in_fmt"] == "fp8" else 2
         s.out_fmt = 1 if layer["out_fmt"] == "fp8" else 2
+        s.act_fp8 = 1 if act_fp8 else 0
         for k, v in keep.items():
             setattr(s, k, None if v is None else v.ctypes.data)
         self._s = s

@@ -453,3 +453,82 @@ def test_layer_composition_against_library_pipeline():
     ref = t(bf(hid))[0] + Wout @ g
     np.testing.assert_allclose(bf(out)[0], ref.numpy(), rtol=2e-2, atol=2e-2)
     np.testing.assert_allclose(h, hs.numpy(), rtol=1e-2, atol=1e-6)
+
+
+# ------------------------------------------------------------------ W8A8 arm
+
+def _torch_e4m3_codes(v32: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(v32, np.float32)).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy()
+
+
+def test_e4m3_quantizer_matches_library_cast_in_range():
+    rng = np.random.default_rng(40)
+    v = np.concatenate([
+        rng.uniform(-448, 448, 20000), rng.uniform(-1, 1, 20000) * 2.0 ** -6,   # normals, subnormals
+        np.ldexp(rng.integers(-16, 16, 2000).astype(np.float64), -10),        # exact ties in the subnormal range
+        (np.arange(8, 16) + 0.5)[None, :].repeat(16, 0).ravel() * np.ldexp(1.0, np.repeat(np.arange(-6, 10), 8) - 3),
+        [0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10]]).astype(np.float32)
+    v = v[np.abs(v) <= 448.0]
+    ours = np.array([orc.f32_to_e4m3_sat(x) for x in v], np.uint8)
+    assert np.array_equal(ours, _torch_e4m3_codes(v))
+
+
+def test_e4m3_quantizer_saturates():
+    for x in (448.5, 464.0, 1e6, np.float32(3.4e38)):
+        assert orc.f32_to_e4m3_sat(x) == 0x7E
+        assert orc.f32_to_e4m3_sat(-x) == 0xFE
+
+
+def test_activation_quantization_blocks():
+    rng = np.random.default_rng(41)
+    a32 = (rng.standard_normal(300) * np.exp(rng.uniform(-3, 3, 300))).astype(np.float32)
+    a32[128:256] = 0.0                                  # an all-zero block
+    a = synth.to_bf16_bits(a32)
+    q, s = orc.act_quant(a)
+    av = bf(a).astype(np.float32)
+    for b, (k0, k1) in enumerate([(0, 128), (128, 256), (256, 300)]):
+        amax = np.float32(np.abs(av[k0:k1]).max())
+        if amax == 0:
+            assert s[b] == 0 and np.all(q[k0:k1] == 0)
+            continue
+        inv = np.float32(448.0) / amax
+        assert s[b] == amax / np.float32(448.0)
+        assert np.array_equal(q[k0:k1], _torch_e4m3_codes(av[k0:k1] * inv))
+        # the block maximum maps to +-448 exactly
+        assert np.abs(np.array([orc.e4m3_to_f64(c) for c in q[k0:k1]])).max() == 448.0
+
+
+def test_w8a8_gemv_matches_library_matmul():
+    rng = np.random.default_rng(42)
+    N, K = 260, 300
+    W, S = synth.quantize_fp8_block128((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+    q = rng.integers(0, 256, K, dtype=np.uint8)
+    q[(q & 0x7F) == 0x7F] = 0x30
+    sa = rng.uniform(0.1, 2.0, 3).astype(np.float32)
+    ours = orc.w8a8_gemv(q, sa, W, S)
+    qa = torch_e4m3_to_f64(q) * np.repeat(sa.astype(np.float64), 128)[:K]
+    Wd = torch_e4m3_to_f64(W) * np.repeat(np.repeat(bf(S), 128, 0), 128, 1)[:N, :K]
+    np.testing.assert_allclose(ours, Wd @ qa, rtol=1e-12, atol=1e-12)
+
+
+def test_w8a8_layer_zero_out_proj_scales_is_identity_and_close_to_w8a16():
+    lay = _tiny_layer()
+    hid = synth.make_hidden(5, 256, 0, 0, 4)
+    outs = []
+    for fp8a in (False, True):
+        L = orc.OracleLayer(lay, act_fp8=fp8a)
+        h, ring, pos = L.new_state()
+        out = hid.copy()
+        L.run(out, h, ring, pos)
+        outs.append(bf(out))
+    # FP8 activations change the result by about the E4M3 step (2^-4 relative per term)
+    d = np.abs(outs[1] - outs[0]).max() / np.abs(outs[0]).max()
+    assert 0.0 < d < 0.1
+    lay2 = dict(lay)
+    lay2["out_s"] = np.zeros_like(lay["out_s"])
+    L = orc.OracleLayer(lay2, act_fp8=True)
+    h, ring, pos = L.new_state()
+    out = hid.copy()
+    L.run(out, h, ring, pos)
+    assert np.array_equal(out, hid)
