@@ -375,6 +375,8 @@ def main():
     if not args.no_extras:
         out["decode_b64"] = _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, 8 if args.quick else 32)
         out["prefill_1k"] = _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, 2 if args.quick else 5)
+        out["prefill_1k_w8a8"] = _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, 2 if args.quick else 5,
+                                                w8a8=True)
         out["stack8"] = _bench_stack8(torch, synth, to_dev)
         out["e2e"] = _bench_e2e(torch, synth, reps, ws, d, B, min(K, 100))
         if rank == 0:
@@ -428,29 +430,38 @@ def _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, steps):
             "hbm_gbs": per / (ms / 1e3) / 1e9, "hbm_frac": per / (ms / 1e3) / 1e9 / hbm}
 
 
-def _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, reps):
+def _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, reps, w8a8=False):
+    """1024-token prefill of one sequence (w8a8: the FP8-activation arm)."""
     d = synth.NEMOTRON_H_8B
     T = 1024
     lay = synth.make_layer(d, synth.WL_8B_PREFILL_1K)
     dl = DeviceLayer(lay)
-    ws = dl.workspace(1, T)
+    ws = dl.workspace_varlen(1, T)
     hid = synth.make_hidden(T, d["hidden"], synth.WL_8B_PREFILL_1K, 0, 0)
     xs = [to_dev(hid) for _ in range(reps + 1)]
     st = dl.new_state(1)
-    s1 = (st[0][0], st[1][0], st[2][:1])
-    dl.prefill(xs[0], s1, ws)
+    s1 = (st[0][:1], st[1][:1], st[2][:1])
+
+    def run(x):
+        dl.prefill_varlen(x, [0, T], s1, ws, w8a8=w8a8)
+
+    run(xs[0])
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(reps):
-        dl.prefill(xs[i + 1], s1, ws)
+        run(xs[i + 1])
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     abi.trace_begin(64)
-    dl.prefill(xs[0], s1, ws)
+    run(xs[0])
     tr = abi.trace_end()
+    gemm_ms = tr.get("gemm_tc", (0.0, 0))[0]
+    flops = 2.0 * T * (synth.derived(d)["n_in"] * d["hidden"] + d["hidden"] * synth.derived(d)["d_inner"])
     return {"value": T / (ms / 1e3), "unit": "tokens/s", "ms_per_prefill": ms, "tokens": T,
+            "arm": "w8a8 (E4M3 activations, kind::f8f6f4)" if w8a8 else "w8a16 (bf16 activations, kind::f16)",
+            "gemm_tflops": flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
             "kernels_ms": {k: v[0] for k, v in tr.items()}}
 
 

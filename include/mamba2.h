@@ -165,8 +165,25 @@ int mamba2_layer_prefill_varlen(const m2_dims* dims, const m2_layer* layer, uint
                                 const int32_t* cu_seqlens, float* ssm_state, uint16_t* conv_state,
                                 int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Workspace bytes for mamba2_layer_prefill_varlen with at most max_seqs
- * sequences and max_total_tokens token rows.  Returns 0 for invalid dims. */
+/* The same prefill on the W8A8 arm: the inputs of the E4M3 projections are
+ * quantized to E4M3 too, per token row and 128-element k block
+ * (amax = max |v|, codes E4M3(v * (448 / amax)) rounded to nearest even and
+ * saturated, scale amax / 448, both in fp32; an all-zero block has scale 0),
+ * and the projections multiply E4M3 by E4M3 on the tensor cores:
+ *   out[m][n] = sum_b S[n/128][b] * s_a[m][b] * sum_{k in b} E4M3(q[m][k]) * E4M3(W[n][k]).
+ * The pages give FP8 x FP8 GEMMs and a bf16 -> FP8 activation conversion for
+ * prefill, not their scaling; this is the block scaling of the weights applied
+ * to the activations.  It changes the numbers (activation rounding of about
+ * 2^-4 relative) and is selected explicitly.  BF16-weight projections keep
+ * bf16 activations.  Needs more than 8 token rows (M2_ERR_UNSUPPORTED
+ * otherwise); arguments as mamba2_layer_prefill_varlen. */
+int mamba2_layer_prefill_varlen_w8a8(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t nseq,
+                                     const int32_t* cu_seqlens, float* ssm_state, uint16_t* conv_state,
+                                     int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes for mamba2_layer_prefill_varlen (and its W8A8 form) with at
+ * most max_seqs sequences and max_total_tokens token rows.  Returns 0 for
+ * invalid dims. */
 size_t m2_workspace_bytes_varlen(const m2_dims* dims, int32_t max_seqs, int32_t max_total_tokens);
 
 /* The w8a16 block-scaled GEMV/GEMM (page "Struct Qwen3SsmLayer",
@@ -176,6 +193,18 @@ size_t m2_workspace_bytes_varlen(const m2_dims* dims, int32_t max_seqs, int32_t 
  * [ceil(N/128)][ceil(K/128)], out [M][N] bf16.  fp32 accumulation. */
 int w8a16_gemv(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* out, int32_t M,
                int32_t N, int32_t K, cudaStream_t stream);
+
+/* The W8A8 arm's product as a unit (the FP8-activation counterpart of
+ * w8a16_gemv): each row of A [M][K] bf16 is quantized to E4M3 per 128-element
+ * k block as in mamba2_layer_prefill_varlen_w8a8, then
+ *   out[m][n] = bf16( sum_b S[n/128][b] * s_a[m][b] * sum_{k in b} E4M3(q[m][k]) * E4M3(W[n][k]) )
+ * on the tensor cores.  M > 8, K % 128 == 0.  ws: m2_w8a8_workspace_bytes(M,
+ * K) bytes, 256-byte aligned; on return it holds the codes [M][rup16(K)]
+ * (uint8) followed, at the next 256-byte boundary, by the scales
+ * [K/128][rup128(M)] (fp32). */
+size_t m2_w8a8_workspace_bytes(int32_t M, int32_t K);
+int w8a8_gemm(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* out, int32_t M, int32_t N, int32_t K,
+              void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* One-token causal depthwise conv update with bias and optional SiLU (source
  * listing, `conv1d_update_biased`) for B sequences of C channels:

@@ -33,6 +33,7 @@ M2_W_BF16 = 2
 # Every entry point include/mamba2.h declares (checked by the host tests).
 EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_decode", "mamba2_layer_prefill",
            "mamba2_layer_decode_noalloc", "mamba2_layer_prefill_varlen", "m2_workspace_bytes_varlen",
+           "mamba2_layer_prefill_varlen_w8a8", "w8a8_gemm", "m2_w8a8_workspace_bytes",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
            "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count")
 
@@ -89,8 +90,12 @@ def lib():
             l.mamba2_layer_prefill_varlen.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32,
                                                       C.POINTER(C.c_int32), P, P, P, P, SZ, P]
             l.mamba2_layer_prefill_varlen.restype = C.c_int
+            l.mamba2_layer_prefill_varlen_w8a8.argtypes = l.mamba2_layer_prefill_varlen.argtypes
+            l.mamba2_layer_prefill_varlen_w8a8.restype = C.c_int
             l.m2_workspace_bytes_varlen.argtypes = [C.POINTER(M2Dims), I32, I32]
             l.m2_workspace_bytes_varlen.restype = SZ
+            l.w8a8_gemm.argtypes = [P, P, P, P, I32, I32, I32, P, SZ, P]; l.w8a8_gemm.restype = C.c_int
+            l.m2_w8a8_workspace_bytes.argtypes = [I32, I32]; l.m2_w8a8_workspace_bytes.restype = SZ
             l.w8a16_gemv.argtypes = [P, P, P, P, I32, I32, I32, P]; l.w8a16_gemv.restype = C.c_int
             l.conv1d_update.argtypes = [P, P, P, I32, P, P, P, I32, I32, I32, I32, P]; l.conv1d_update.restype = C.c_int
             l.mamba2_ssm_step.argtypes = [P, P, P, P, P, I32, P, P, P, P, I32, I32, I32, I32, I32, P]
@@ -188,8 +193,27 @@ def mamba2_layer_prefill_varlen(dims, layer, hidden, cu_seqlens, ssm_state, conv
     return _check("mamba2_layer_prefill_varlen", st) if check else st
 
 
+def mamba2_layer_prefill_varlen_w8a8(dims, layer, hidden, cu_seqlens, ssm_state, conv_state, conv_pos, ws,
+                                     ws_bytes, stream=None, check=True) -> int:
+    """The W8A8 arm of the varlen prefill (FP8 activations into the E4M3 projections)."""
+    cu = (C.c_int32 * len(cu_seqlens))(*[int(v) for v in cu_seqlens])
+    st = lib().mamba2_layer_prefill_varlen_w8a8(C.byref(dims), C.byref(layer), _ptr(hidden), len(cu_seqlens) - 1,
+                                                cu, _ptr(ssm_state), _ptr(conv_state), _ptr(conv_pos), _ptr(ws),
+                                                ws_bytes, _stream(stream))
+    return _check("mamba2_layer_prefill_varlen_w8a8", st) if check else st
+
+
 def m2_workspace_bytes_varlen(dims: M2Dims, max_seqs: int, max_total_tokens: int) -> int:
     return lib().m2_workspace_bytes_varlen(C.byref(dims), max_seqs, max_total_tokens)
+
+
+def w8a8_gemm(A, W, S, out, M, N, K, ws, ws_bytes, stream=None, check=True) -> int:
+    st = lib().w8a8_gemm(_ptr(A), _ptr(W), _ptr(S), _ptr(out), M, N, K, _ptr(ws), ws_bytes, _stream(stream))
+    return _check("w8a8_gemm", st) if check else st
+
+
+def m2_w8a8_workspace_bytes(M: int, K: int) -> int:
+    return lib().m2_w8a8_workspace_bytes(M, K)
 
 
 def w8a16_gemv(A, W, S, out, M, N, K, stream=None, check=True) -> int:

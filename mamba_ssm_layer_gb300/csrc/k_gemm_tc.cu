@@ -52,14 +52,18 @@ constexpr int kTcTmemBufs = 4;   // k-block partials in TMEM
 constexpr int kTcBM = 128;       // weight rows per tile (UMMA M)
 constexpr int kTcBK = 128;       // k per block (= scale block)
 
-template <int NT>
+template <int NT, bool AQ8 = false>
 struct TcLayout {
-  static constexpr int kAStages = NT <= 64 ? 4 : 3;
   // offsets from a 1024-byte aligned base
-  static constexpr int kW = 0;         // fp8: 4 x 16 KB E4M3; bf16: 4 x 32 KB swizzled (through kWbf)
-  static constexpr int kWbf = 65536;   // fp8: 2 x 32 KB converted bf16, swizzled
-  static constexpr int kA = 131072;    // kAStages x NT*256 B bf16, swizzled
-  static constexpr int kBars = kA + kAStages * NT * kTcBK * 2;
+  // w8a16 / bf16: W ring at 0 (fp8: 4 x 16 KB E4M3; bf16: 4 x 32 KB swizzled,
+  // through kWbf), converted bf16 tiles at kWbf, bf16 activation tiles at kA.
+  // W8A8: 4 x 16 KB swizzled E4M3 weight tiles at 0, E4M3 activation tiles at kA.
+  static constexpr int kAStages = AQ8 ? 4 : (NT <= 64 ? 4 : 3);
+  static constexpr int kABytes = NT * kTcBK * (AQ8 ? 1 : 2);  // one activation stage
+  static constexpr int kW = 0;
+  static constexpr int kWbf = 65536;
+  static constexpr int kA = AQ8 ? 65536 : 131072;
+  static constexpr int kBars = kA + kAStages * kABytes;
 };
 
 struct TcBars {
@@ -70,9 +74,9 @@ struct TcBars {
   uint32_t tmem_base;
 };
 
-template <int NT>
+template <int NT, bool AQ8 = false>
 constexpr int tc_smem_bytes() {
-  return TcLayout<NT>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
+  return TcLayout<NT, AQ8>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
 }
 
 // ------------------------------------------------------------------ PTX helpers
@@ -117,6 +121,16 @@ __host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// kind::f8f6f4 instruction descriptor: D fp32, A and B E4M3 (format 0), both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc_f8(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
+}
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -153,6 +167,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 16 consecutive fp32 columns of TMEM into registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Two E4M3 -> two bf16, exactly (E4M3 -> f16 -> f32 -> bf16 are all exact).
@@ -234,10 +262,10 @@ __device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int rank, in
   kb1 = (int)((long long)ta.kblocks * (ks + 1) / ta.ksplit);
 }
 
-template <int NT>
+template <int NT, bool AQ8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, const TcArgs ta) {
-  using Lay = TcLayout<NT>;
+  using Lay = TcLayout<NT, AQ8>;
   constexpr int SA = Lay::kAStages;
   const GemvArgs& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
@@ -254,7 +282,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kTcWStages; ++s) {
       mbar_init(&bars->w_full[s], 1);
-      mbar_init(&bars->w_empty[s], ta.fp8 ? 4 : 1);  // the converter warps, or the MMA commit
+      mbar_init(&bars->w_empty[s], (ta.fp8 && !AQ8) ? 4 : 1);  // the converter warps, or the MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->wbf_full[b], 4);
@@ -299,7 +327,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int s = gk % kTcWStages;
           if (gk >= kTcWStages && !mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)) dead = true;
           if (dead) break;
-          if (ta.fp8) {
+          if (ta.fp8) {  // E4M3 tile (plain for the converters; 128-byte swizzled for the W8A8 MMA)
             mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK);
             tma_load_2d(smem + Lay::kW + s * kTcBM * kTcBK, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
           } else {
@@ -325,9 +353,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int s = gk % SA;
           if (gk >= SA && !mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)) dead = true;
           if (dead) break;
-          uint8_t* abuf = smem + Lay::kA + s * NT * kTcBK * 2;
-          mbar_arrive_expect_tx(&bars->a_full[s], NT * kTcBK * 2);  // from all cs slices
-          if (ta.cs == 1) {
+          uint8_t* abuf = smem + Lay::kA + s * Lay::kABytes;
+          mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);  // from all cs slices
+          if (AQ8) {  // E4M3 codes: one 128-byte-swizzled box of NT rows x 128 k
+            tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
+          } else if (ta.cs == 1) {
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
             tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
           } else {
@@ -349,6 +379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = tc_idesc(kTcBM, NT);
+      constexpr uint32_t idesc8 = tc_idesc_f8(kTcBM, NT);
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
@@ -356,7 +387,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1, sa = gk % SA, tb = gk % kTcTmemBufs;
-          if (ta.fp8) {
+          if (ta.fp8 && !AQ8) {
             if (!mbar_wait(&bars->wbf_full[b], (gk / 2) & 1)) dead = true;
           } else {
             if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
@@ -366,26 +397,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dead = true;
           if (dead) break;
           tc_fence_after();
-          const uint32_t wb = ta.fp8 ? smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2)
-                                     : smem_addr(smem + Lay::kW + s * kTcBM * kTcBK * 2);
-          const uint32_t ab = smem_addr(smem + Lay::kA + sa * NT * kTcBK * 2);
+          if (AQ8) {
+            // E4M3 x E4M3: one 128-byte swizzle row holds the whole 128-k block; K = 32 per MMA
+            const uint32_t wb = smem_addr(smem + Lay::kW + s * kTcBM * kTcBK);
+            const uint32_t ab = smem_addr(smem + Lay::kA + sa * Lay::kABytes);
 #pragma unroll
-          for (int kk = 0; kk < kTcBK / 16; ++kk) {
-            const int atom = kk >> 2, within = (kk & 3) * 32;  // 64-k atoms of 128 bytes per row
-            const uint64_t ad = sw128_desc(wb + atom * kTcBM * 128 + within);
-            const uint64_t bd = sw128_desc(ab + atom * NT * 128 + within);
-            tc_mma(tmem + tb * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
+            for (int kk = 0; kk < kTcBK / 32; ++kk)
+              tc_mma_f8(tmem + tb * NT, sw128_desc(wb + kk * 32), sw128_desc(ab + kk * 32), idesc8, kk > 0 ? 1 : 0);
+          } else {
+            const uint32_t wb = ta.fp8 ? smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2)
+                                       : smem_addr(smem + Lay::kW + s * kTcBM * kTcBK * 2);
+            const uint32_t ab = smem_addr(smem + Lay::kA + sa * Lay::kABytes);
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 16; ++kk) {
+              const int atom = kk >> 2, within = (kk & 3) * 32;  // 64-k atoms of 128 bytes per row
+              const uint64_t ad = sw128_desc(wb + atom * kTcBM * 128 + within);
+              const uint64_t bd = sw128_desc(ab + atom * NT * 128 + within);
+              tc_mma(tmem + tb * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
+            }
           }
           tc_commit(&bars->mma_done[tb]);
           if (ta.cs > 1) tc_commit_mc(&bars->a_empty[sa], cmask);
           else tc_commit(&bars->a_empty[sa]);
-          tc_commit(ta.fp8 ? &bars->wbf_empty[b] : &bars->w_empty[s]);
+          tc_commit((ta.fp8 && !AQ8) ? &bars->wbf_empty[b] : &bars->w_empty[s]);
         }
       }
     }
   } else if (warp < 6) {
     // -------------------------------------------------------- converters
-    if (ta.fp8) {
+    if (ta.fp8 && !AQ8) {
       const int ct = tid - 64;  // 0..127
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
@@ -453,12 +493,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1)) dead = true;
         if (dead) break;
         tc_fence_after();
+        if (AQ8) {
+          // token scales of this k block (rows padded to 128 tokens), 16 columns at a time
 #pragma unroll
-        for (int c = 0; c < HC / 32; ++c) {
-          float v[32];
-          tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 32, v);
+          for (int c = 0; c < HC / 16; ++c) {
+            float v[16];
+            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 16, v);
+            const float4* sq4 =
+                reinterpret_cast<const float4*>(a.sq + (size_t)kb * a.ldsq + mt * NT + hf * HC + c * 16);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, v[i], acc[c * 32 + i]);
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const float4 t4 = __ldg(sq4 + i4);
+              acc[c * 16 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c * 16 + 4 * i4 + 0]);
+              acc[c * 16 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c * 16 + 4 * i4 + 1]);
+              acc[c * 16 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c * 16 + 4 * i4 + 2]);
+              acc[c * 16 + 4 * i4 + 3] = fmaf(s * t4.w, v[4 * i4 + 3], acc[c * 16 + 4 * i4 + 3]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < HC / 32; ++c) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, v[i], acc[c * 32 + i]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -565,13 +624,13 @@ size_t gemm_tc_partial_bytes(int M, int N, int K) {
   return ks > 1 ? (size_t)ks * M * N * 4 : 0;
 }
 
-template <int NT>
+template <int NT, bool AQ8>
 static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   static int done_mask[64] = {0};
   CUtensorMap tmW, tmA;
   if (fp8) {
     if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.W, g.K, g.N, (uint64_t)g.K, kTcBK, kTcBM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+                   AQ8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
     if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.W, g.K, g.N, (uint64_t)g.K * 2, 64, kTcBM,
@@ -590,11 +649,17 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   // one CTA per cluster: sharing the activation tile across a cluster of CTAs
   // by multicast (ta.cs > 1, supported by the kernel) measured slower here
   ta.cs = 1;
-  if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64, NT / ta.cs,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  if (AQ8) {
+    ta.cs = 1;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.q8, g.K, g.M, (uint64_t)g.ldq, kTcBK, NT,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  } else if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64,
+                        NT / ta.cs, CU_TENSOR_MAP_SWIZZLE_128B)) {
     return cudaErrorInvalidValue;
-  const int smem = tc_smem_bytes<NT>();
-  auto kern = gemm_tc_kernel<NT>;
+  }
+  const int smem = tc_smem_bytes<NT, AQ8>();
+  auto kern = gemm_tc_kernel<NT, AQ8>;
   cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
   if (e != cudaSuccess) return e;
   const int nitems = ta.m_tiles * ((ta.n_tiles + ta.cs - 1) / ta.cs) * ta.ksplit;  // per cluster
@@ -615,8 +680,13 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
 }
 
 cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
-  if (tc_nt(g.M) == 64) return launch_tc<64>(g, fp8, s);
-  return launch_tc<128>(g, fp8, s);
+  if (g.q8) {  // W8A8: E4M3 activation codes with per-(token, k block) scales
+    if (!fp8 || g.K % 128 || g.ldq % 16 || g.ldsq % 128) return cudaErrorInvalidValue;
+    if (tc_nt(g.M) == 64) return launch_tc<64, true>(g, fp8, s);
+    return launch_tc<128, true>(g, fp8, s);
+  }
+  if (tc_nt(g.M) == 64) return launch_tc<64, false>(g, fp8, s);
+  return launch_tc<128, false>(g, fp8, s);
 }
 
 int status_gemm_tc(int clear) {

@@ -398,14 +398,14 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
   const int K = a.K;
   float v[kPrepMaxPer];
   uint4 wv[kPrepMaxPer / 8], zv[kPrepMaxPer / 8];  // issued with the inputs: independent loads
-  // element e of this thread: k = (tid + 512 * (e / 8)) * 8 + e % 8
+  // element e of this thread: k = (tid + kPrepThreads * (e / 8)) * 8 + e % 8
 #pragma unroll
   for (int c = 0; c < kPrepMaxPer / 8; ++c) {
     const int k0 = (tid + kPrepThreads * c) * 8;
     if (k0 < K) {
-      wv[c] = *reinterpret_cast<const uint4*>(a.w + k0);
+      if (a.mode != PREP_QUANT) wv[c] = *reinterpret_cast<const uint4*>(a.w + k0);  // no weight in QUANT mode
       if (a.mode == PREP_GATED) zv[c] = *reinterpret_cast<const uint4*>(a.z + (size_t)m * a.ldz + k0);
-      if (a.mode == PREP_RMSNORM) {
+      if (a.mode == PREP_RMSNORM || a.mode == PREP_QUANT) {
         const uint4 u = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.ldx + k0);
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -425,7 +425,9 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
     }
   }
-  if (a.mode == PREP_RMSNORM) {
+  if (a.mode == PREP_QUANT) {
+    // rows as they are
+  } else if (a.mode == PREP_RMSNORM) {
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
     for (int e = 0; e < kPrepMaxPer; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
@@ -531,6 +533,34 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       }
     }
   }
+  if (a.q8) {
+    // W8A8 activations: a 128-element block is the 8-element runs of 16
+    // consecutive threads (one half-warp)
+#pragma unroll
+    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+      const int k0 = (tid + kPrepThreads * c) * 8;
+      float bm = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) bm = fmaxf(bm, fabsf(v[c * 8 + e]));  // v = 0 past K
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+      if (k0 < K) {
+        const float inv = bm > 0.0f ? 448.0f / bm : 0.0f;
+        uint32_t q[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint16_t h;
+          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+              : "=h"(h)
+              : "f"(v[c * 8 + 2 * e + 1] * inv), "f"(v[c * 8 + 2 * e] * inv));
+          q[e] = h;
+        }
+        *reinterpret_cast<uint2*>(a.q8 + (size_t)m * a.ldq + k0) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+        if ((tid & 15) == 0) a.sq[(size_t)(k0 >> 7) * a.ldsq + m] = bm / 448.0f;
+      }
+    }
+  }
+  if (!a.out) return;
   float up = 1.0f;
   if (a.f16) {
     float mx = 0.0f;

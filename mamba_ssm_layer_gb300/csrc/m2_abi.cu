@@ -157,7 +157,16 @@ static size_t decode_ws(const m2_dims& d, int B) { return decode_ws_min(d, B) + 
 
 // Prefill workspace for T token rows in nseq sequences with nchunks SSD chunks
 // in total (ceil(T_i / 128) summed; at most T / 128 + nseq).
-static size_t prefill_ws(const m2_dims& d, int T, int nseq, int nchunks) {
+// W8A8 activation codes and block scales (the larger of the two projections' inputs).
+static size_t q8_ldq(const m2_dims& d) {
+  const Derived r = derive(d);
+  return rup((size_t)(d.hidden > r.d_inner ? d.hidden : r.d_inner), 16);
+}
+static size_t q8_bytes(const m2_dims& d, int T) {
+  return rup((size_t)T * q8_ldq(d), 256) + rup(q8_ldq(d) / 128 * rup((size_t)T, 128) * 4, 256);
+}
+
+static size_t prefill_ws(const m2_dims& d, int T, int nseq, int nchunks, bool w8a8 = true) {
   const Derived r = derive(d);
   size_t o = 0;
   o = rup(o + (size_t)T * d.hidden * 2, 256);   // xn
@@ -170,10 +179,11 @@ static size_t prefill_ws(const m2_dims& d, int T, int nseq, int nchunks) {
   if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups))
     o += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
   o += proj_part_bytes(d, T);  // tensor-core k-split partials
+  if (w8a8) o = rup(o, 256) + q8_bytes(d, T);  // W8A8 activation codes and scales
   return o;
 }
-static size_t prefill_ws_bound(const m2_dims& d, int T, int nseq) {
-  return prefill_ws(d, T, nseq, (T + 127) / 128 + nseq);
+static size_t prefill_ws_bound(const m2_dims& d, int T, int nseq, bool w8a8 = true) {
+  return prefill_ws(d, T, nseq, (T + 127) / 128 + nseq, w8a8);
 }
 
 // Whether a projection over M rows consumes f16 prescaled activations (the
@@ -258,7 +268,7 @@ int m2_validate(const m2_dims* dims, const m2_layer* L) {
 size_t m2_workspace_bytes(const m2_dims* dims, int32_t max_batch, int32_t max_tokens) {
   if (check_dims(dims) || max_batch < 0 || max_tokens < 0) return 0;
   const size_t a = max_batch > 0 ? decode_ws(*dims, max_batch) : 0;
-  const size_t b = max_tokens > 0 ? prefill_ws_bound(*dims, max_tokens, 1) : 0;
+  const size_t b = max_tokens > 0 ? prefill_ws_bound(*dims, max_tokens, 1, false) : 0;
   return a > b ? a : b;
 }
 
@@ -411,7 +421,7 @@ namespace m2 {
 // Prefill of a varlen batch (cu: host token offsets, nseq + 1 entries).
 static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t nseq, const int32_t* cu,
                         float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool w8a8) {
   int st = m2_validate(dims, L);
   if (st) return st;
   if (nseq <= 0 || !cu || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
@@ -424,7 +434,8 @@ static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   const m2_dims& d = *dims;
   std::vector<int32_t> tab(2 * (size_t)(nseq + 1));
   const int nchunks = ssd_chunk_table(cu, nseq, tab.data());
-  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < prefill_ws(d, T, nseq, nchunks))
+  if (w8a8 && T <= 8) return M2_ERR_UNSUPPORTED;  // the W8A8 arm runs on the tensor-core projections
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < prefill_ws(d, T, nseq, nchunks, w8a8))
     return M2_ERR_WORKSPACE;
   const Derived r = derive(d);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
@@ -452,6 +463,14 @@ static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   if (ssd) o += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);
   float* part = reinterpret_cast<float*>(w8 + o);
   const size_t part_bytes = proj_part_bytes(d, T);
+  o = rup(o + part_bytes, 256);
+  // W8A8: E4M3 codes [T][ldq] of the projection inputs, scales [K/128][rup(T, 128)]
+  uint8_t* q8 = w8 + o;
+  const int ldq = (int)q8_ldq(d);
+  float* sq = reinterpret_cast<float*>(w8 + o + rup((size_t)T * ldq, 256));
+  const int ldsq = (int)rup((size_t)T, 128);
+  const bool q_in = w8a8 && L->in_proj.fmt == M2_W_FP8_BLOCK128;
+  const bool q_out = w8a8 && L->out_proj.fmt == M2_W_FP8_BLOCK128;
 
   cudaError_t e;
   // the sequence tables, stream-ordered before the kernels that read them
@@ -471,8 +490,23 @@ static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   pa.ldo = d.hidden;
   pa.f16 = proj_f16(L->in_proj, T) ? 1 : 0;
   pa.unscale = us_in;
+  if (q_in) {
+    pa.out = nullptr;
+    pa.q8 = q8;
+    pa.ldq = ldq;
+    pa.sq = sq;
+    pa.ldsq = ldsq;
+  }
   if ((e = launch_prep(pa, stream))) return launch_status(e);
-  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream, nullptr, us_in, 0, part,
+  GemvArgs qa;
+  memset(&qa, 0, sizeof(qa));
+  if (q_in) {
+    qa.q8 = q8;
+    qa.ldq = ldq;
+    qa.sq = sq;
+    qa.ldsq = ldsq;
+  }
+  if ((e = proj(L->in_proj, xn, d.hidden, T, zx, r.ldz, EPI_STORE, nullptr, 0, stream, &qa, us_in, 0, part,
                 part_bytes)))
     return launch_status(e);
   if ((e = launch_conv_prefill(conv_state, conv_pos, zx + r.d_inner, r.ldz, L->conv_w, L->conv_b, u, r.d_xbc, T,
@@ -550,8 +584,22 @@ static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   pa.ldo = r.d_inner;
   pa.f16 = proj_f16(L->out_proj, T) ? 1 : 0;
   pa.unscale = us_out;
+  if (q_out) {
+    pa.out = nullptr;
+    pa.q8 = q8;
+    pa.ldq = ldq;
+    pa.sq = sq;
+    pa.ldsq = ldsq;
+  }
   if ((e = launch_prep(pa, stream))) return launch_status(e);
-  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, nullptr, us_out,
+  memset(&qa, 0, sizeof(qa));
+  if (q_out) {
+    qa.q8 = q8;
+    qa.ldq = ldq;
+    qa.sq = sq;
+    qa.ldsq = ldsq;
+  }
+  if ((e = proj(L->out_proj, g, r.d_inner, T, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, &qa, us_out,
                 0, part, part_bytes)))
     return launch_status(e);
   return M2_OK;
@@ -565,13 +613,21 @@ int mamba2_layer_prefill(const m2_dims* dims, const m2_layer* L, uint16_t* hidde
                          uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (T <= 0) return M2_ERR_ARG;
   const int32_t cu[2] = {0, T};
-  return prefill_impl(dims, L, hidden, 1, cu, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream);
+  return prefill_impl(dims, L, hidden, 1, cu, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream, false);
 }
 
 int mamba2_layer_prefill_varlen(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t nseq,
                                 const int32_t* cu_seqlens, float* ssm_state, uint16_t* conv_state, int32_t* conv_pos,
                                 void* ws, size_t ws_bytes, cudaStream_t stream) {
-  return prefill_impl(dims, L, hidden, nseq, cu_seqlens, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream);
+  return prefill_impl(dims, L, hidden, nseq, cu_seqlens, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream,
+                      false);
+}
+
+int mamba2_layer_prefill_varlen_w8a8(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t nseq,
+                                     const int32_t* cu_seqlens, float* ssm_state, uint16_t* conv_state,
+                                     int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return prefill_impl(dims, L, hidden, nseq, cu_seqlens, ssm_state, conv_state, conv_pos, ws, ws_bytes, stream,
+                      true);
 }
 
 size_t m2_workspace_bytes_varlen(const m2_dims* dims, int32_t max_seqs, int32_t max_total_tokens) {
@@ -591,6 +647,51 @@ int w8a16_gemv(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t*
   w.k = K;
   w.fmt = M2_W_FP8_BLOCK128;
   return launch_status(proj(w, A, K, M, out, N, EPI_STORE, nullptr, 0, stream));
+}
+
+size_t m2_w8a8_workspace_bytes(int32_t M, int32_t K) {
+  if (M <= 0 || K <= 0) return 0;
+  const size_t ldq = rup((size_t)K, 16);
+  return rup((size_t)M * ldq, 256) + rup((size_t)(K + 127) / 128 * rup((size_t)M, 128) * 4, 256);
+}
+
+int w8a8_gemm(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* out, int32_t M, int32_t N, int32_t K,
+              void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!A || !W || !S || !out || M <= 0 || N <= 0 || K <= 0) return M2_ERR_ARG;
+  if (K % 128 || K > 16384 || M <= 8) return M2_ERR_UNSUPPORTED;
+  if (!al16(A) || !al16(W)) return M2_ERR_ALIGN;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < m2_w8a8_workspace_bytes(M, K))
+    return M2_ERR_WORKSPACE;
+  uint8_t* q8 = static_cast<uint8_t*>(ws);
+  const int ldq = (int)rup((size_t)K, 16);
+  float* sq = reinterpret_cast<float*>(q8 + rup((size_t)M * ldq, 256));
+  const int ldsq = (int)rup((size_t)M, 128);
+  PrepArgs pa;
+  memset(&pa, 0, sizeof(pa));
+  pa.mode = PREP_QUANT;
+  pa.x = A;
+  pa.ldx = K;
+  pa.M = M;
+  pa.K = K;
+  pa.q8 = q8;
+  pa.ldq = ldq;
+  pa.sq = sq;
+  pa.ldsq = ldsq;
+  cudaError_t e = launch_prep(pa, stream);
+  if (e) return launch_status(e);
+  m2_weight w;
+  w.w = W;
+  w.scale = S;
+  w.n = N;
+  w.k = K;
+  w.fmt = M2_W_FP8_BLOCK128;
+  GemvArgs qa;
+  memset(&qa, 0, sizeof(qa));
+  qa.q8 = q8;
+  qa.ldq = ldq;
+  qa.sq = sq;
+  qa.ldsq = ldsq;
+  return launch_status(proj(w, A, K, M, out, N, EPI_STORE, nullptr, 0, stream, &qa));
 }
 
 int conv1d_update(uint16_t* conv_state, int32_t* conv_pos, const uint16_t* x, int32_t ld_x, const uint16_t* w,

@@ -97,6 +97,14 @@ struct GemvArgs {
   int32_t ldgy;
   const uint16_t* gz;
   int32_t ldgz;
+  // Tensor-core GEMM, W8A8 arm (E4M3 weights only): when q8 is set, the
+  // activations are E4M3 codes [M][ldq] (A unused) with fp32 scales
+  // [K/128][ldsq] (ldsq a multiple of 128), and the product is
+  // sum_b S[n/128][b] * sq[b][m] * sum_{k in b} q8[m][k] W[n][k].
+  const uint8_t* q8;
+  int32_t ldq;
+  const float* sq;
+  int32_t ldsq;
 };
 
 enum GemvNorm : int32_t {
@@ -117,7 +125,8 @@ enum GemvAct : int32_t {
 // (unscale[m] = 2^-j).
 enum PrepMode : int32_t {
   PREP_RMSNORM = 0,  // x * r * w, r = 1/sqrt(mean(x^2) + eps) (input RMSNorm)
-  PREP_GATED = 1     // y * r * w * silu(z), r over groups of `group` (gated RMSNorm)
+  PREP_GATED = 1,    // y * r * w * silu(z), r over groups of `group` (gated RMSNorm)
+  PREP_QUANT = 2     // x as is (bf16 rows), for the W8A8 quantization alone
 };
 struct PrepArgs {
   int32_t mode;
@@ -137,6 +146,13 @@ struct PrepArgs {
   float* unscale;     // [M] (f16 mode)
   int32_t pdl;
   double inv_k;       // 1/K (PREP_RMSNORM), so the kernel needs no double division
+  // W8A8 arm (out may be null): E4M3 codes [M][ldq] and fp32 block scales
+  // [ceil(K/128)][ldsq] of each row and 128-element block: amax = max |v|,
+  // codes E4M3(v * (448 / amax)), scale amax / 448 (fp32; zero block: 0, 0).
+  uint8_t* q8;
+  int32_t ldq;
+  float* sq;
+  int32_t ldsq;
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t s);
 

@@ -74,12 +74,14 @@ class DeviceLayer:
         n = abi.m2_workspace_bytes_varlen(self.dims, max_seqs, max_total_tokens)
         return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
-    def prefill_varlen(self, hidden: torch.Tensor, cu_seqlens, state, ws: torch.Tensor, stream=None) -> None:
+    def prefill_varlen(self, hidden: torch.Tensor, cu_seqlens, state, ws: torch.Tensor, stream=None,
+                       w8a8: bool = False) -> None:
         """hidden [T][hidden]: rows cu_seqlens[i] .. cu_seqlens[i+1]-1 belong to sequence i of `state`
-        (h [n][H][P][N], ring [n][d_conv-1][d_xbc], pos [n])."""
+        (h [n][H][P][N], ring [n][d_conv-1][d_xbc], pos [n]).  w8a8: the FP8-activation arm."""
         h, ring, pos = state
-        abi.mamba2_layer_prefill_varlen(self.dims, self.struct, hidden, list(cu_seqlens), h, ring, pos, ws, ws.numel(),
-                                        stream if stream is not None else torch.cuda.current_stream())
+        fn = abi.mamba2_layer_prefill_varlen_w8a8 if w8a8 else abi.mamba2_layer_prefill_varlen
+        fn(self.dims, self.struct, hidden, list(cu_seqlens), h, ring, pos, ws, ws.numel(),
+           stream if stream is not None else torch.cuda.current_stream())
 
     def prefill(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None) -> None:
         h, ring, pos = state

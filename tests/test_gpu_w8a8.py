@@ -1,0 +1,125 @@
+"""GPU parity of the W8A8 arm (FP8 activations into the E4M3 projections;
+tcgen05 kind::f8f6f4) against the oracle's W8A8 definition.
+
+Integer work is bit-exact: the activation codes and block scales (an integer
+decision taken in fp32 on both sides), and the whole product when every partial
+sum is an exactly representable integer.  Layer results follow the
+single-layer bar (2e-2 on bf16 outputs; the fp32 state within the flip-aware
+bound of tests/helpers.py)."""
+import numpy as np
+import pytest
+import torch
+
+from mamba_ssm_layer_gb300 import abi, synth
+from mamba_ssm_layer_gb300.layer import DeviceLayer, bits_u16, to_dev
+from oracle import oracle as orc
+from tests.helpers import TOL_BF16, FlipTracker, bf16_to_f64, floored_rel_err
+from tests.test_gpu_parity import _codes_prefill
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from __graft_entry__ import build
+    build()
+    abi.m2_device_status(clear=True)
+    yield
+    assert abi.m2_device_status() == abi.M2_OK
+
+
+def _rup(v, a):
+    return (v + a - 1) // a * a
+
+
+def _w8a8(A, W, S):
+    M, K = A.shape
+    N = W.shape[0]
+    ws = torch.empty(abi.m2_w8a8_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    out = torch.zeros((M, N), dtype=torch.int16, device="cuda")
+    abi.w8a8_gemm(to_dev(A), to_dev(W), to_dev(S), out, M, N, K, ws, ws.numel())
+    torch.cuda.synchronize()
+    ldq = _rup(K, 16)
+    off = _rup(M * ldq, 256)
+    q = ws[:M * ldq].view(M, ldq).cpu().numpy()[:, :K]
+    sq = ws[off:off + (K // 128) * _rup(M, 128) * 4].view(torch.float32).view(K // 128, _rup(M, 128)).cpu().numpy()
+    return bits_u16(out), q, sq[:, :M].T.copy()
+
+
+@pytest.mark.parametrize("M,N,K", [(9, 300, 256), (70, 552, 512), (130, 1000, 4096)])
+def test_w8a8_codes_scales_bit_exact_and_product(M, N, K):
+    rng = np.random.default_rng(M * 7 + K)
+    A = synth.to_bf16_bits((rng.standard_normal((M, K)) * np.exp(rng.uniform(-2, 2, (M, 1)))).astype(np.float32))
+    A[0, 128:256] = 0  # a zero block
+    W, S = synth.quantize_fp8_block128((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
+    got, q, sq = _w8a8(A, W, S)
+    ref = np.empty((M, N))
+    for m in range(M):
+        qo, so = orc.act_quant(A[m])
+        assert np.array_equal(q[m], qo), m          # codes: integer decisions, bit-exact
+        assert np.array_equal(sq[m], so), m         # fp32 scales, bit-exact
+        ref[m] = orc.w8a8_gemv(qo, so, W, S)
+    err = floored_rel_err(bf16_to_f64(got), bf16_to_f64(orc.f64_array_to_bf16(ref)), axis=-1)
+    assert err <= TOL_BF16, err
+
+
+def test_w8a8_product_exact_on_integer_operands():
+    # every block holds one 448 (so its scale is 1 and its codes are the values),
+    # the rest small integers; weights small integers; power-of-two weight scales:
+    # all partial sums are exact integers, so the bf16 result is the oracle's bit for bit
+    rng = np.random.default_rng(5)
+    M, N, K = 40, 384, 512
+    a = rng.integers(-8, 9, (M, K)).astype(np.float32)
+    a[:, ::128] = 448.0
+    A = synth.to_bf16_bits(a)
+    wv = rng.integers(-8, 9, (N, K)).astype(np.float32)
+    W = torch.from_numpy(wv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    S = synth.to_bf16_bits(np.exp2(rng.integers(-8, -2, (N // 128, K // 128))).astype(np.float32))
+    got, _, _ = _w8a8(A, W, S)
+    ref = np.stack([orc.w8a8_gemv(*orc.act_quant(A[m]), W, S) for m in range(M)])
+    assert np.array_equal(got, orc.f64_array_to_bf16(ref))
+
+
+def _w8a8_prefill_case(lay, T, key):
+    d = lay["dims"]
+    hd = d["hidden"]
+    dl = DeviceLayer(lay)
+    ol = orc.OracleLayer(lay, act_fp8=True)
+    st = dl.new_state(1)
+    ost = ol.new_state()
+    trk = FlipTracker(d, lay["A_log"], lay["dt_bias"], lay["conv_w"])
+    hid = synth.make_hidden(T, hd, *key)
+    x = to_dev(hid)
+    ws = dl.workspace_varlen(1, T)
+    dl.prefill_varlen(x, [0, T], st, ws, w8a8=True)
+    torch.cuda.synchronize()
+    r3, r4 = _codes_prefill(ws, T, lay)
+    ref = hid.copy()
+    _, e3, e4 = ol.run_traced(ref, *ost)
+    for t in range(T):
+        trk.token(r3[t], (e3[0][t], e3[1][t]), r4[t], (e4[0][t], e4[1][t]))
+    err = floored_rel_err(bf16_to_f64(bits_u16(x)), bf16_to_f64(ref), axis=-1)
+    rep = trk.check_state(st[0][0].cpu().numpy(), ost[0])
+    assert err <= TOL_BF16, err
+    assert int(st[2][0]) == T
+    print("w8a8 prefill parity", T, err, rep)
+
+
+@pytest.mark.parametrize("T", [9, 129, 300])
+def test_w8a8_prefill_tiny(T):
+    _w8a8_prefill_case(synth.make_layer(synth.TINY, synth.WL_TINY_DECODE), T, (synth.WL_TINY_DECODE, 90, T))
+
+
+def test_w8a8_prefill_8b_layer_1024_tokens():
+    _w8a8_prefill_case(synth.make_layer(synth.NEMOTRON_H_8B, synth.WL_8B_PREFILL_1K), 1024,
+                       (synth.WL_8B_PREFILL_1K, 91, 0))
+
+
+def test_w8a8_rejects_small_blocks():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    dl = DeviceLayer(lay)
+    st = dl.new_state(1)
+    x = to_dev(synth.make_hidden(8, 256, 1, 1, 1))
+    ws = dl.workspace_varlen(1, 8)
+    code = abi.mamba2_layer_prefill_varlen_w8a8(dl.dims, dl.struct, x, [0, 8], *st, ws, ws.numel(), check=False)
+    assert code == abi.M2_ERR_UNSUPPORTED
