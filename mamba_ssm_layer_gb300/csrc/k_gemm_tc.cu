@@ -63,7 +63,8 @@ struct TcLayout {
   static constexpr int kW = 0;
   static constexpr int kWbf = 65536;
   static constexpr int kA = AQ8 ? 65536 : 131072;
-  static constexpr int kBars = kA + kAStages * kABytes;
+  static constexpr int kSc = kA + kAStages * kABytes;                    // W8A8: token scales, one slot per TMEM buffer
+  static constexpr int kBars = kSc + (AQ8 ? kTcTmemBufs * NT * 4 : 0);
 };
 
 struct TcBars {
@@ -71,6 +72,7 @@ struct TcBars {
   uint64_t wbf_full[2], wbf_empty[2];
   uint64_t a_full[4], a_empty[4];
   uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
+  uint64_t sc_full[kTcTmemBufs];  // W8A8: the token scales of a k block have landed
   uint32_t tmem_base;
 };
 
@@ -295,6 +297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < kTcTmemBufs; ++b) {
       mbar_init(&bars->mma_done[b], 1);
       mbar_init(&bars->tmem_empty[b], kTcEpiWarps);
+      mbar_init(&bars->sc_full[b], 1);
     }
     fence_mbar_init();
   }
@@ -357,6 +360,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);  // from all cs slices
           if (AQ8) {  // E4M3 codes: one 128-byte-swizzled box of NT rows x 128 k
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
+            // the k block's token scales into the slot of its TMEM buffer, once the
+            // epilogue has finished with the k block that used the slot before
+            const int tb = gk % kTcTmemBufs;
+            if (gk >= kTcTmemBufs && !mbar_wait(&bars->tmem_empty[tb], ((gk / kTcTmemBufs) - 1) & 1)) dead = true;
+            if (dead) break;
+            mbar_arrive_expect_tx(&bars->sc_full[tb], NT * 4);
+            bulk_g2s(smem + Lay::kSc + tb * NT * 4, a.sq + (size_t)kb * a.ldsq + (size_t)mt * NT, NT * 4,
+                     &bars->sc_full[tb], pola);
           } else if (ta.cs == 1) {
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
             tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
@@ -494,16 +505,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (dead) break;
         tc_fence_after();
         if (AQ8) {
-          // token scales of this k block (rows padded to 128 tokens), 16 columns at a time
+          // token scales of this k block, staged in shared memory by the activation producer
+          if (!mbar_wait(&bars->sc_full[tb], (gk / kTcTmemBufs) & 1)) {
+            dead = true;
+            break;
+          }
 #pragma unroll
           for (int c = 0; c < HC / 16; ++c) {
             float v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 16, v);
-            const float4* sq4 =
-                reinterpret_cast<const float4*>(a.sq + (size_t)kb * a.ldsq + mt * NT + hf * HC + c * 16);
+            const float4* sq4 = reinterpret_cast<const float4*>(smem + Lay::kSc + tb * NT * 4) + (hf * HC + c * 16) / 4;
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
-              const float4 t4 = __ldg(sq4 + i4);
+              const float4 t4 = sq4[i4];
               acc[c * 16 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c * 16 + 4 * i4 + 0]);
               acc[c * 16 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c * 16 + 4 * i4 + 1]);
               acc[c * 16 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c * 16 + 4 * i4 + 2]);
