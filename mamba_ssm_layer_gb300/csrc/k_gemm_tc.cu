@@ -22,7 +22,7 @@
 //               (plain 2-D map) into a 4-stage ring; bf16 weights go straight
 //               into a 4-stage ring of 128-byte-swizzled tiles.  It does not
 //               wait for the previous kernel: weights are never its output.
-//   warp 14     activation producer (lane 0): after the dependency wait, TMA of
+//   warp 22     activation producer (lane 0): after the dependency wait, TMA of
 //               the bf16 activation tile [NT][128] (two 64-wide boxes, 128-byte
 //               swizzle = the UMMA K-major canonical layout), 3-4 stages;
 //   warps 2-5   converters: E4M3 tile -> bf16 tile in the swizzled layout the
@@ -30,8 +30,8 @@
 //   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each) per k block
 //               into one of 4 TMEM partial buffers and commits to the barriers
 //               that free the buffers it read and wake the epilogue;
-//   warps 6-13  epilogue, two warps per TMEM lane quarter (each half of the
-//               token columns): per k block, TMEM -> registers, acc += s * partial;
+//   warps 6-21  epilogue, four warps per TMEM lane quarter (each a quarter of
+//               the token columns): per k block, TMEM -> registers, acc += s * partial;
 //               per item, the store / residual / conv-update epilogue, or fp32
 //               partials that a second kernel sums in split order.
 // Every wait is bounded (see mbar_wait); TMEM is freed on every exit path.
@@ -45,8 +45,9 @@
 
 namespace m2 {
 
-constexpr int kTcEpiWarps = 8;   // two per TMEM lane quarter, each half of the token columns
-constexpr int kTcThreads = 480;  // 15 warps
+constexpr int kTcEpiWarps = 16;  // four per TMEM lane quarter, each a quarter of the token columns
+constexpr int kTcAWarp = 6 + kTcEpiWarps;       // activation producer
+constexpr int kTcThreads = (kTcAWarp + 1) * 32;  // 23 warps
 constexpr int kTcWStages = 4;    // weight tiles in flight
 constexpr int kTcTmemBufs = 4;   // k-block partials in TMEM
 constexpr int kTcBM = 128;       // weight rows per tile (UMMA M)
@@ -172,6 +173,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // 32 lanes x 16 consecutive fp32 columns of TMEM into registers.
+// Shared-memory float4 load that stays after the preceding TMEM wait (a plain
+// load may be hoisted above it, holding its registers across the wait).
+__device__ __forceinline__ float4 lds_f4_ordered(uint32_t addr) {
+  float4 r;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (warp == 14) {
+  } else if (warp == kTcAWarp) {
     // -------------------------------------------------------- activation producer
     pdl_wait();  // A is written by the previous kernel
     if (lane == 0) {
@@ -482,9 +491,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // -------------------------------------------------------- epilogue
-    // warps 6..13: TMEM lane quarter warp % 4 (a warp reaches only its own
-    // quarter), token columns [hf * NT/2, (hf + 1) * NT/2)
-    constexpr int HC = NT / 2;
+    // warps 6..21: TMEM lane quarter warp % 4 (a warp reaches only its own
+    // quarter), token columns [hf * HC, (hf + 1) * HC); each drains its part of
+    // a k block's partial with one TMEM load and one wait
+    constexpr int EPG = kTcEpiWarps / 4;  // warps per lane quarter
+    constexpr int HC = NT / EPG;
     const int q = warp & 3;
     const int hf = (warp - 6) >> 2;
     const int row = 32 * q + lane;  // weight row within the tile
@@ -502,35 +513,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int tb = gk % kTcTmemBufs;
         const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb)) : 1.0f;
         if (!mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1)) dead = true;
+        if (AQ8 && !dead && !mbar_wait(&bars->sc_full[tb], (gk / kTcTmemBufs) & 1)) dead = true;
         if (dead) break;
         tc_fence_after();
-        if (AQ8) {
-          // token scales of this k block, staged in shared memory by the activation producer
-          if (!mbar_wait(&bars->sc_full[tb], (gk / kTcTmemBufs) & 1)) {
-            dead = true;
-            break;
-          }
+        // 16 columns per TMEM load: two loads in flight before one wait at
+        // HC = 32 would hold 32 more registers than the 80 a thread has here
+        const uint32_t ta_ = tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC;
 #pragma unroll
-          for (int c = 0; c < HC / 16; ++c) {
-            float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 16, v);
-            const float4* sq4 = reinterpret_cast<const float4*>(smem + Lay::kSc + tb * NT * 4) + (hf * HC + c * 16) / 4;
+        for (int c0 = 0; c0 < HC; c0 += 16) {
+          float v[16];
+          tmem_ld16(ta_ + c0, v);
+          if (AQ8) {
+            // token scales of this k block, staged in shared memory by the activation producer
+            const uint32_t sq = smem_addr(smem + Lay::kSc + (tb * NT + hf * HC + c0) * 4);
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
-              const float4 t4 = sq4[i4];
-              acc[c * 16 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c * 16 + 4 * i4 + 0]);
-              acc[c * 16 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c * 16 + 4 * i4 + 1]);
-              acc[c * 16 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c * 16 + 4 * i4 + 2]);
-              acc[c * 16 + 4 * i4 + 3] = fmaf(s * t4.w, v[4 * i4 + 3], acc[c * 16 + 4 * i4 + 3]);
+              const float4 t4 = lds_f4_ordered(sq + 16 * i4);
+              acc[c0 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c0 + 4 * i4 + 0]);
+              acc[c0 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c0 + 4 * i4 + 1]);
+              acc[c0 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c0 + 4 * i4 + 2]);
+              acc[c0 + 4 * i4 + 3] = fmaf(s * t4.w, v[4 * i4 + 3], acc[c0 + 4 * i4 + 3]);
             }
-          }
-        } else {
+          } else {
 #pragma unroll
-          for (int c = 0; c < HC / 32; ++c) {
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC + c * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(s, v[i], acc[c * 32 + i]);
+            for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(s, v[i], acc[c0 + i]);
           }
         }
         tc_fence_before();
