@@ -341,16 +341,37 @@ def main():
     for i in range(K):
         step(W + K + i)
     tr = abi.trace_end()
-    in_ms, in_n = tr.get("gemv_fp8_inproj_conv", (0.0, 0))
-    tr_in = in_ms / in_n if in_n else None
+    # the dominant kernel: the single-launch step when it ran, else the in_proj GEMV
+    if "decode_step_fused" in tr:
+        rk, rk_desc, rk_bytes = "decode_step_fused", "decode_step_fused (whole layer step, one launch)", per_rep
+    else:
+        rk, rk_desc, rk_bytes = "gemv_fp8_inproj_conv", "gemv_fp8 (in_proj, conv1d fused)", inproj_bytes(d, B)
+    rk_ms, rk_n = tr.get(rk, (0.0, 0))
+    tr_rk = rk_ms / rk_n if rk_n else None
     hbm_peak, peak_src, peaks = measured_peaks()
-    in_bytes = inproj_bytes(d, B)
     roof = None
-    if tr_in:
-        achieved = in_bytes / (tr_in / 1e3) / 1e9
+    if tr_rk:
+        achieved = rk_bytes / (tr_rk / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": captured_traffic("gemv_fp8_inproj_conv", "decode_b1"), "kernel": "gemv_fp8 (in_proj, conv1d fused)", "bytes_per_launch": in_bytes,
-                "launch_us": tr_in * 1e3, "peak_source": f"{peak_src} hbm_gbs"}
+                "traffic": captured_traffic(rk, "decode_b1"), "kernel": rk_desc, "bytes_per_launch": rk_bytes,
+                "launch_us": tr_rk * 1e3, "peak_source": f"{peak_src} hbm_gbs"}
+
+    # the same steps in the other form of the batch-1 step (eager), for comparison
+    prev = abi.m2_set_fused_decode(not ("decode_step_fused" in tr))
+    Kc = min(K, 200)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(Kc):
+        step(W + i)
+    e1.record()
+    torch.cuda.synchronize()
+    abi.m2_set_fused_decode(prev)
+    msc = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    alt = {"value": job_rate(Kc * B, world, msc), "ms_per_step": msc / Kc, "steps": Kc,
+           "launch": ("eager, three kernels per step" if "decode_step_fused" in tr
+                      else "eager, one cooperative kernel per step (m2_set_fused_decode)")}
 
     out = {
         "metric": "decode tokens/s (Mamba-2 layer, batch 1)", "value": value, "unit": "tokens/s",
@@ -368,6 +389,7 @@ def main():
         "gpu_launches": int(round(launches_per_step * K_run)),
         "eager": eager,
         "graph": graph_info,
+        "other_form": alt,
         "kernels_ms_per_step": {k: v[0] / K for k, v in tr.items()},
         "clocks": (clk_g.summary() if use_graph and clk_g is not None else clk.summary()),
     }
@@ -426,8 +448,13 @@ def _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, steps):
     ms = e0.elapsed_time(e1) / steps
     per = layer_bytes_per_token(d, B)
     hbm, _, _ = measured_peaks()
+    abi.trace_begin(16 * steps)
+    for i in range(steps):
+        dl.decode(hs[i % 4], sts[i % 2], ws)
+    tr = abi.trace_end()
     return {"value": B / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "batch": B,
-            "hbm_gbs": per / (ms / 1e3) / 1e9, "hbm_frac": per / (ms / 1e3) / 1e9 / hbm}
+            "hbm_gbs": per / (ms / 1e3) / 1e9, "hbm_frac": per / (ms / 1e3) / 1e9 / hbm,
+            "kernels_ms_per_step": {k: v[0] / steps for k, v in tr.items()}}
 
 
 def _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, reps, w8a8=False):

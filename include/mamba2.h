@@ -123,10 +123,21 @@ size_t m2_workspace_bytes(const m2_dims* dims, int32_t max_batch, int32_t max_to
  *              slot t mod (d_conv-1); zero-initialise for a new sequence.
  *   conv_pos   [B] int32, tokens seen so far per sequence; advanced by 1.
  *   ws         workspace of at least m2_workspace_bytes(dims, B, 0) bytes,
- *              256-byte aligned; its contents are scratch. */
+ *              256-byte aligned; its contents are scratch.
+ * The step runs as a chain of three kernels (B <= 8) or five (tensor-core
+ * projections, B > 8).  After m2_set_fused_decode(1), a B = 1 step (both
+ * projections in one format, K <= 8192) runs as one cooperative launch with
+ * two grid-wide barriers instead; such calls on one device must not overlap
+ * in time (the barriers share one device-wide counter), so issue them on one
+ * stream.  Both forms give bit-identical results. */
 int mamba2_layer_decode(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t B,
                         float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
                         size_t ws_bytes, cudaStream_t stream);
+
+/* Select the single-launch batch-1 decode step (enable != 0) or the kernel
+ * chain (0, the default) for later mamba2_layer_decode calls in this process.
+ * Host setting only; returns the previous setting. */
+int m2_set_fused_decode(int enable);
 
 /* Prefill of T tokens of ONE sequence (page "Trait TransformerLayer",
  * `prefill`: projections as GEMMs over the T tokens; the result equals T

@@ -35,7 +35,7 @@ EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_dec
            "mamba2_layer_decode_noalloc", "mamba2_layer_prefill_varlen", "m2_workspace_bytes_varlen",
            "mamba2_layer_prefill_varlen_w8a8", "w8a8_gemm", "m2_w8a8_workspace_bytes",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
-           "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count")
+           "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count", "m2_set_fused_decode")
 
 
 class M2Dims(C.Structure):
@@ -107,6 +107,7 @@ def lib():
             l.m2_trace_end.restype = C.c_int
             l.m2_kernel_name.argtypes = [I32]; l.m2_kernel_name.restype = C.c_char_p
             l.m2_kernel_count.argtypes = []; l.m2_kernel_count.restype = I32
+            l.m2_set_fused_decode.argtypes = [C.c_int]; l.m2_set_fused_decode.restype = C.c_int
             _lib = l
     return _lib
 
@@ -241,6 +242,11 @@ def m2_device_status(clear: bool = False) -> int:
 
 def m2_launch_count() -> int:
     return lib().m2_launch_count()
+
+
+def m2_set_fused_decode(enable: bool) -> bool:
+    """Single-launch batch-1 decode step (True) or the kernel chain (False, the default); returns the previous setting."""
+    return bool(lib().m2_set_fused_decode(1 if enable else 0))
 
 
 def kernel_names() -> list[str]:

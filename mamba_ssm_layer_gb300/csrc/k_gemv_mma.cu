@@ -43,7 +43,8 @@ struct MmaTail {
   float unscale[8];
   int32_t pos[8];
   uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t epi_bar;  // epilogue inputs staged by bulk copies
+  uint64_t epi_bar;   // epilogue inputs staged by bulk copies
+  uint64_t epi_bar2;  // fused decode step: the residual rows of the out_proj epilogue
 };
 
 // Shared-memory layout.  kc: bytes of a row per stage (a multiple of 64
@@ -57,7 +58,7 @@ __host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int
   L.act_ld = K + 8;  // elements per activation row (the pad spreads rows over banks)
   L.tail = 0;
   L.act = (int)((sizeof(MmaTail) + 127) / 128 * 128);
-  L.tot = L.act + ((mb + 1) * L.act_ld * 2 + 127) / 128 * 128;  // + one zero row for lanes past the batch
+  L.tot = L.act + (mb * L.act_ld * 2 + 127) / 128 * 128;  // activation rows (lanes past the batch read row 0)
   L.epi = L.tot + (rows_max * kMmaWarps * mb * 4 + 127) / 128 * 128;  // per-warp partials
   int epi_bytes = 0;
   // conv: taps [rows_max][dconv], bias [rows_max], ring slots [mb][dconv-1][rows_max] (storage order)
@@ -146,8 +147,9 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
         }
       } else {
         zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
-        const float4 f0 = *reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0);
-        const float4 f1 = *reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0 + 4);
+        // L2 loads: y may come from other CTAs of the same launch (fused step)
+        const float4 f0 = __ldcg(reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0));
+        const float4 f1 = __ldcg(reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0 + 4));
         v[c * 8 + 0] = f0.x; v[c * 8 + 1] = f0.y; v[c * 8 + 2] = f0.z; v[c * 8 + 3] = f0.w;
         v[c * 8 + 4] = f1.x; v[c * 8 + 5] = f1.y; v[c * 8 + 6] = f1.z; v[c * 8 + 7] = f1.w;
       }
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   const int kb = (a.K + 127) / 128;
   const MmaLayout lay = mma_layout(a.K, ES, rows_max, MB, a.epi, a.dconv);
   MmaTail* tail = reinterpret_cast<MmaTail*>(smem + lay.tail);
-  uint16_t* act_s = reinterpret_cast<uint16_t*>(smem + lay.act);  // [MB + 1][act_ld]
+  uint16_t* act_s = reinterpret_cast<uint16_t*>(smem + lay.act);  // [MB][act_ld]
   float* tot = reinterpret_cast<float*>(smem + lay.tot);
   uint8_t* epi_s = smem + lay.epi;
   uint8_t* stg = smem + lay.stage;
@@ -423,19 +425,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     float* red = tot;  // scratch: tot is zeroed again below
     for (int m = 0; m < mvalid; ++m)
       fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, tail->unscale, tid, kC);
-    const int kv = a.K / 8;
-    for (int i = tid; i < kv; i += kC)  // zero row for lanes past the batch
-      *reinterpret_cast<uint4*>(act_s + (size_t)MB * lay.act_ld + i * 8) = make_uint4(0u, 0u, 0u, 0u);
     for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
     named_bar(1, kC);
   } else {
     // activations -> shared memory (coherent loads: written by the previous kernel)
     const int kv = a.K / 8;  // 16-byte vectors per row
-    for (int i = tid; i < (MB + 1) * kv; i += kC) {
+    for (int i = tid; i < mvalid * kv; i += kC) {
       const int m = i / kv, k8 = (i % kv) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (m < mvalid) v = *reinterpret_cast<const uint4*>(a.A + (size_t)m * a.lda + k8);
-      if (FP8 && a.act == ACT_PLAIN && m < mvalid) {
+      uint4 v = *reinterpret_cast<const uint4*>(a.A + (size_t)m * a.lda + k8);
+      if (FP8 && a.act == ACT_PLAIN) {
         const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
         float mx = 0.0f;
 #pragma unroll
@@ -472,7 +470,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
   }
 
   // ------------------------------------------------ consumers: main loop
-  const uint16_t* act_g = act_s + (size_t)(g < mvalid ? g : MB) * lay.act_ld;  // zero row past the batch
+  // MMA column g is batch row g; lanes past the batch read row 0 into columns
+  // that are never stored
+  const uint16_t* act_g = act_s + (size_t)(g < mvalid ? g : 0) * lay.act_ld;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < nst && !dead; ++j) {
     const int s = j % S;
@@ -621,12 +621,508 @@ cudaError_t launch_gemv_mma(const GemvArgs& a, bool fp8, cudaStream_t s) {
   }
 }
 
+// ------------------------------------------------------------------ fused decode step, batch 1
+//
+// The whole layer step of one sequence in one cooperative launch, one CTA per
+// SM, all CTAs resident:
+//   phase 1  in_proj GEMV, input RMSNorm in the prologue, conv1d update with
+//            bias and SiLU in the epilogue (this CTA's row groups)
+//   grid barrier
+//   phase 2  SSM step of this CTA's share of the H*P state rows
+//   grid barrier
+//   phase 3  out_proj GEMV, gated RMSNorm in the prologue, residual add in the
+//            epilogue (in place on the hidden row)
+// The producer warp streams both projections' weight rows through one ring
+// without a break, so the out_proj rows land in shared memory while the SSM
+// phase and the barriers run; the three-kernel chain pays a launch ramp and a
+// drain per kernel instead.  Row groups, the per-group MMA work and the
+// fixed-order reductions are those of gemv_mma_kernel, so the outputs are
+// bit-identical to the three-kernel chain.
+
+// One GEMV's share of this CTA: row groups [rg_begin, rg_end), streamed in
+// nst stages of kc bytes per row (whole 16-row groups when a row is <= 4 KB).
+struct MmaPlan {
+  int rg_begin, rg_end, row_begin, row_end, nrows, nrg, nch, nst, row_bytes, kc, pitch;
+  bool whole;
+};
+
+// kc / whole: the chunking the stand-alone GEMV launch would choose for this
+// projection (it decides which k each warp sums, hence the rounding).
+__device__ __forceinline__ MmaPlan mma_plan(const GemvArgs& a, int es, int kc, bool whole) {
+  MmaPlan p;
+  const int G = gridDim.x;
+  const int nrg_all = (a.N + kMmaRows - 1) / kMmaRows;
+  p.rg_begin = (int)(((long long)nrg_all * blockIdx.x) / G);
+  p.rg_end = (int)(((long long)nrg_all * (blockIdx.x + 1)) / G);
+  p.row_begin = p.rg_begin * kMmaRows;
+  p.row_end = min(a.N, p.rg_end * kMmaRows);
+  p.nrows = max(0, p.row_end - p.row_begin);
+  p.nrg = p.rg_end - p.rg_begin;
+  p.row_bytes = a.K * es;
+  p.whole = whole;
+  p.kc = kc;
+  p.pitch = p.whole ? p.row_bytes : p.kc + kRowPad;
+  p.nch = (p.row_bytes + p.kc - 1) / p.kc;
+  p.nst = p.nrg * p.nch;
+  return p;
+}
+
+constexpr int kFusedStride = kMmaRows * (4096 + kRowPad);  // bytes per ring stage
+
+struct FusedLayout {
+  int act, tot, epc, epr, stage, stages, total;
+};
+// k_in / k_out: the projections' K; rows_in / rows_out: row capacity per CTA.
+__host__ __device__ inline FusedLayout fused_layout(int k_in, int k_out, int rows_in, int rows_out, int dconv) {
+  FusedLayout L;
+  const int kmax = k_in > k_out ? k_in : k_out;
+  const int rmax = rows_in > rows_out ? rows_in : rows_out;
+  L.act = (int)((sizeof(MmaTail) + 127) / 128 * 128);
+  L.tot = L.act + ((kmax + 8) * 2 + 127) / 128 * 128;               // one activation row
+  L.epc = L.tot + (rmax * kMmaWarps * 4 + 127) / 128 * 128;          // per-warp row totals
+  L.epr = L.epc + (rows_in * (2 * dconv + 1) * 2 + 127) / 128 * 128;  // conv taps, bias, ring slots
+  L.stage = L.epr + (rows_out * 2 + 127) / 128 * 128;                // residual rows
+  L.stages = (227 * 1024 - L.stage) / kFusedStride;
+  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  L.total = L.stage + L.stages * kFusedStride;
+  return L;
+}
+
+// Issue the bulk copies of stage jl of plan p (whole warp; lane 0 arms the barrier).
+__device__ __forceinline__ void mma_produce(const GemvArgs& a, const MmaPlan& p, int jl, uint8_t* dst, uint64_t* full,
+                                            uint64_t pol, int lane) {
+  const uint8_t* W = static_cast<const uint8_t*>(a.W);
+  const int rg = p.rg_begin + jl / p.nch, ch = jl % p.nch;
+  const int cb = min(p.kc, p.row_bytes - ch * p.kc);
+  if (p.whole) {
+    if (lane == 0) {
+      const int nr = min(kMmaRows, a.N - rg * kMmaRows);
+      mbar_arrive_expect_tx(full, (uint32_t)(nr * p.row_bytes));
+      bulk_g2s(dst, W + (size_t)rg * kMmaRows * p.row_bytes, (uint32_t)(nr * p.row_bytes), full, pol);
+    }
+  } else {
+    if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)(kMmaRows * cb));
+    __syncwarp();
+    if (lane < kMmaRows) {
+      const int r = min(rg * kMmaRows + lane, a.N - 1);
+      bulk_g2s(dst + (size_t)lane * p.pitch, W + (size_t)r * p.row_bytes + (size_t)ch * p.kc, (uint32_t)cb, full, pol);
+    }
+  }
+}
+
+// Consume this CTA's stages of plan p (ring slots j0 + jl); one batch row
+// (act), totals per warp into tot [warp][rows_max].  False on a timeout.
+template <bool FP8>
+__device__ __forceinline__ bool mma_consume(const GemvArgs& a, const MmaPlan& p, int j0, int S, uint8_t* stg,
+                                            MmaTail* tail, const uint16_t* act, float* tot, int rows_max, int warp,
+                                            int lane) {
+  constexpr int ES = FP8 ? 1 : 2;
+  const int g = lane >> 2, t = lane & 3;
+  const int kb = (a.K + 127) / 128;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int jl = 0; jl < p.nst; ++jl) {
+    const int j = j0 + jl, s = j % S;
+    const int rg = p.rg_begin + jl / p.nch, ch = jl % p.nch;
+    const int cb = min(p.kc, p.row_bytes - ch * p.kc);
+    const int ng = cb / (64 * ES);
+    const int q0 = (ng * warp) / kMmaWarps, q1 = (ng * (warp + 1)) / kMmaWarps;
+    const int kel0 = ch * (p.kc / ES);
+    if (!mbar_wait(&tail->full[s], (j / S) & 1)) return false;
+    const uint8_t* st0 = stg + (size_t)s * kFusedStride + (size_t)g * p.pitch;
+    const uint8_t* st8 = st0 + (size_t)8 * p.pitch;
+    const int r0 = min(rg * kMmaRows + g, p.row_end - 1), r8 = min(rg * kMmaRows + g + 8, p.row_end - 1);
+    for (int q = q0; q < q1; ++q) {
+      const int k0 = kel0 + q * 64;
+      // every MMA column reads the one batch row; only column 0 is stored
+      const uint4 bl = *reinterpret_cast<const uint4*>(act + k0 + 16 * t);
+      const uint4 bh = *reinterpret_cast<const uint4*>(act + k0 + 16 * t + 8);
+      const uint32_t bw[8] = {bl.x, bl.y, bl.z, bl.w, bh.x, bh.y, bh.z, bh.w};
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (FP8) {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(st0 + q * 64 + 16 * t);
+        const uint4 v8 = *reinterpret_cast<const uint4*>(st8 + q * 64 + 16 * t);
+        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+        const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w};
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp)
+          mma16816<FP8>(d, cvt_e4m3x2(w0[sp]), cvt_e4m3x2(w8[sp]), cvt_e4m3x2(w0[sp] >> 16),
+                        cvt_e4m3x2(w8[sp] >> 16), bw[2 * sp], bw[2 * sp + 1]);
+        const int kbk = k0 >> 7;
+        const float s0 = bf16_to_f32(__ldg(a.S + (size_t)(r0 >> 7) * kb + kbk));
+        const float s8 = bf16_to_f32(__ldg(a.S + (size_t)(r8 >> 7) * kb + kbk));
+        acc[0] = fmaf(d[0], s0, acc[0]);
+        acc[2] = fmaf(d[2], s8, acc[2]);
+      } else {
+        const uint4 v0a = *reinterpret_cast<const uint4*>(st0 + q * 128 + 32 * t);
+        const uint4 v0b = *reinterpret_cast<const uint4*>(st0 + q * 128 + 32 * t + 16);
+        const uint4 v8a = *reinterpret_cast<const uint4*>(st8 + q * 128 + 32 * t);
+        const uint4 v8b = *reinterpret_cast<const uint4*>(st8 + q * 128 + 32 * t + 16);
+        const uint32_t w0[8] = {v0a.x, v0a.y, v0a.z, v0a.w, v0b.x, v0b.y, v0b.z, v0b.w};
+        const uint32_t w8[8] = {v8a.x, v8a.y, v8a.z, v8a.w, v8b.x, v8b.y, v8b.z, v8b.w};
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp)
+          mma16816<FP8>(d, w0[2 * sp], w8[2 * sp], w0[2 * sp + 1], w8[2 * sp + 1], bw[2 * sp], bw[2 * sp + 1]);
+        acc[0] += d[0];
+        acc[2] += d[2];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tail->empty[s]);
+    if (ch == p.nch - 1) {
+      const int lr = (rg - p.rg_begin) * kMmaRows;
+      if (t == 0) {  // column 0: the batch row
+        tot[(size_t)warp * rows_max + lr + g] = acc[0];
+        tot[(size_t)warp * rows_max + lr + g + 8] = acc[2];
+      }
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    }
+  }
+  return true;
+}
+
+// Grid-wide barrier of the fused step (all CTAs resident: cooperative launch).
+// Arrival count and generation persist across launches; the last arriver
+// resets the count before it advances the generation.  The wait is bounded: on
+// a timeout the status word is set and the CTA goes on.
+__device__ unsigned g_fused_bar[2];  // [0] arrivals, [1] generation
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __noinline__ void fused_grid_barrier(int tid, int nthreads) {
+  named_bar(1, nthreads);
+  if (tid == 0) {
+    const unsigned gen0 = ld_acquire_gpu(&g_fused_bar[1]);  // before arriving
+    __threadfence();
+    if (atomicAdd(&g_fused_bar[0], 1u) == gridDim.x - 1) {
+      atomicExch(&g_fused_bar[0], 0u);
+      __threadfence();
+      atomicAdd(&g_fused_bar[1], 1u);
+    } else {
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(&g_fused_bar[1]) == gen0) {
+        if (clock64() - t0 > kWaitCycles) {
+          record_timeout();
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  named_bar(1, nthreads);
+}
+
+// Chunking of the two projections (as the stand-alone GEMV launches choose it).
+struct FusedChunks {
+  int kc_in, whole_in, kc_out, whole_out;
+};
+
+template <bool FP8>
+__global__ void __launch_bounds__(kMmaThreads, 1)
+    decode_step_fused_kernel(const FusedStepArgs fa, int rows_in, int rows_out, const FusedChunks ck) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int ES = FP8 ? 1 : 2;
+  constexpr int kC = kMmaWarps * 32;  // consumer threads
+  const GemvArgs& a1 = fa.in;
+  const GemvArgs& a3 = fa.out;
+  const SsmArgs& sa = fa.ssm;
+  const FusedLayout lay = fused_layout(a1.K, a3.K, rows_in, rows_out, a1.dconv);
+  MmaTail* tail = reinterpret_cast<MmaTail*>(smem);
+  uint16_t* act_s = reinterpret_cast<uint16_t*>(smem + lay.act);
+  float* tot = reinterpret_cast<float*>(smem + lay.tot);
+  uint16_t* cwS = reinterpret_cast<uint16_t*>(smem + lay.epc);  // conv taps [rows_in][dconv]
+  uint16_t* bS = cwS + (size_t)rows_in * a1.dconv;                // conv bias [rows_in]
+  uint16_t* rgS = bS + rows_in;                                   // ring slots [L][rows_in], storage order
+  uint16_t* rsS = reinterpret_cast<uint16_t*>(smem + lay.epr);  // residual row [rows_out]
+  uint8_t* stg = smem + lay.stage;
+  const int S = lay.stages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const MmaPlan p1 = mma_plan(a1, ES, ck.kc_in, ck.whole_in != 0), p3 = mma_plan(a3, ES, ck.kc_out, ck.whole_out != 0);
+  const int L = a1.dconv - 1;
+  // this CTA's conv rows in phase 1: local rows [rx0, rx0 + nx) = channels [cx0, cx0 + nx)
+  const int xa = max(p1.row_begin, a1.xbc0), xb = min(p1.row_end, a1.xbc0 + a1.d_xbc);
+  const int nx = xb > xa ? xb - xa : 0;
+  const int rx0 = nx ? xa - p1.row_begin : 0, cx0 = nx ? xa - a1.xbc0 : 0;
+  auto al16p = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  const bool bulk1 = nx > 0 && nx % 8 == 0 && cx0 % 8 == 0 && rx0 % 8 == 0 && a1.d_xbc % 8 == 0 && a1.conv_b &&
+                     al16p(a1.conv_w) && al16p(a1.conv_b) && al16p(a1.ring);
+  const bool bulk3 = p3.nrows > 0 && p3.nrows % 8 == 0 && p3.row_begin % 8 == 0 && al16p(a3.resid);
+  // phase-2 rows of this CTA: [sr0, sr1) of the H*P state rows
+  const int nsr = sa.H * sa.P;
+  const int sr0 = (int)(((long long)nsr * blockIdx.x) / gridDim.x);
+  const int sr1 = (int)(((long long)nsr * (blockIdx.x + 1)) / gridDim.x);
+
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&tail->full[i], 1);
+      mbar_init(&tail->empty[i], kMmaWarps);
+    }
+    mbar_init(&tail->epi_bar, 1);
+    mbar_init(&tail->epi_bar2, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kMmaWarps) {
+    // ------------------------------------------------ producer warp
+    // Weights are never written by a kernel: the ring fills before the
+    // dependency wait.  Everything else (ring, residual) after it.
+    const uint64_t pol1 = a1.evict_first ? policy_evict_first() : policy_evict_normal();
+    const uint64_t pol3 = a3.evict_first ? policy_evict_first() : policy_evict_normal();
+    if (lane == 0 && sr1 > sr0) {
+      // this CTA's phase-2 state rows into L2 (one contiguous range)
+      const char* base = reinterpret_cast<const char*>(sa.h + (size_t)sr0 * sa.N);
+      const size_t bytes = (size_t)(sr1 - sr0) * sa.N * 4;
+      for (size_t o = 0; o < bytes; o += 65536) {
+        const uint32_t n = (uint32_t)(bytes - o < 65536 ? bytes - o : 65536);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + o), "r"(n) : "memory");
+      }
+    }
+    auto epi_copies = [&]() {
+      if (lane != 0) return;
+      const uint64_t pn = policy_evict_normal();
+      if (bulk1) {
+        mbar_arrive_expect_tx(&tail->epi_bar, (uint32_t)(nx * (a1.dconv + 1) * 2 + L * nx * 2));
+        bulk_g2s(cwS + (size_t)rx0 * a1.dconv, a1.conv_w + (size_t)cx0 * a1.dconv, (uint32_t)(nx * a1.dconv * 2),
+                 &tail->epi_bar, pn);
+        bulk_g2s(bS + rx0, a1.conv_b + cx0, (uint32_t)(nx * 2), &tail->epi_bar, pn);
+        for (int jj = 0; jj < L; ++jj)
+          bulk_g2s(rgS + (size_t)jj * rows_in + rx0, a1.ring + (size_t)jj * a1.d_xbc + cx0, (uint32_t)(nx * 2),
+                   &tail->epi_bar, pn);
+      }
+      if (bulk3) {
+        mbar_arrive_expect_tx(&tail->epi_bar2, (uint32_t)(p3.nrows * 2));
+        bulk_g2s(rsS, a3.resid + p3.row_begin, (uint32_t)(p3.nrows * 2), &tail->epi_bar2, pn);
+      }
+    };
+    bool dead = false, waited = false;
+    const int nst = p1.nst + p3.nst;
+    int j = 0;
+    for (; j < nst && !dead; ++j) {
+      const int s = j % S;
+      if (j == S) {
+        pdl_wait();
+        pdl_trigger();
+        waited = true;
+        epi_copies();
+      }
+      if (j >= S && !mbar_wait(&tail->empty[s], ((j / S) - 1) & 1)) dead = true;
+      if (dead) break;
+      uint8_t* dst = stg + (size_t)s * kFusedStride;
+      if (j < p1.nst) mma_produce(a1, p1, j, dst, &tail->full[s], pol1, lane);
+      else mma_produce(a3, p3, j - p1.nst, dst, &tail->full[s], pol3, lane);
+    }
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      epi_copies();
+    }
+    for (int k = max(0, j - S); k < j; ++k)
+      if (!mbar_wait(&tail->full[k % S], (k / S) & 1)) break;
+    __syncthreads();
+    return;
+  }
+
+  // ------------------------------------------------ consumers
+  pdl_wait();  // hidden, conv ring and position, SSM state: the previous launch's
+  pdl_trigger();
+  const int pos_r = __ldcg(a1.pos);
+  if (!bulk1) {
+    for (int r = rx0 + tid; r < rx0 + nx; r += kC) {
+      const int c = cx0 + (r - rx0);
+      for (int jj = 0; jj < a1.dconv; ++jj) cwS[r * a1.dconv + jj] = __ldg(a1.conv_w + (size_t)c * a1.dconv + jj);
+      bS[r] = a1.conv_b ? __ldg(a1.conv_b + c) : (uint16_t)0;
+      for (int jj = 0; jj < L; ++jj) rgS[(size_t)jj * rows_in + r] = __ldcg(a1.ring + (size_t)jj * a1.d_xbc + c);
+    }
+  }
+  if (!bulk3)
+    for (int r = tid; r < p3.nrows; r += kC) rsS[r] = __ldcg(a3.resid + p3.row_begin + r);
+  bool dead = false;
+
+  // ---- phase 1: in_proj
+  fused_norm_row<FP8>(a1, 0, act_s, tot, tail->unscale, tid, kC);
+  for (int i = tid; i < rows_in * kMmaWarps; i += kC) tot[i] = 0.0f;
+  named_bar(1, kC);
+  if (!mma_consume<FP8>(a1, p1, 0, S, stg, tail, act_s, tot, rows_in, warp, lane)) dead = true;
+  if (bulk1 && !dead && !mbar_wait(&tail->epi_bar, 0)) dead = true;
+  named_bar(1, kC);
+  {
+    const float us = tail->unscale[0];
+    for (int r = tid; r < p1.nrows; r += kC) {
+      const int n = p1.row_begin + r;
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) sum += tot[(size_t)w * rows_in + r];
+      const float accv = sum * us;
+      uint16_t* o = a1.out + n;
+      if (n >= a1.xbc0 && n < a1.xbc0 + a1.d_xbc) {
+        const uint16_t vb = f32_to_bf16(accv);  // rounding point of the in_proj output
+        const int c = n - a1.xbc0;
+        const uint16_t* w = cwS + r * a1.dconv;
+        float sc = bf16_to_f32(bS[r]);
+        for (int jj = 0; jj < L; ++jj) sc += bf16_to_f32(w[jj]) * bf16_to_f32(rgS[(size_t)((pos_r + jj) % L) * rows_in + r]);
+        sc += bf16_to_f32(w[L]) * bf16_to_f32(vb);
+        *o = f32_to_bf16(silu_f(sc));
+        a1.ring[(size_t)(pos_r % L) * a1.d_xbc + c] = vb;
+      } else {
+        *o = f32_to_bf16(accv);
+      }
+    }
+  }
+  fused_grid_barrier(tid, kC);
+
+  // ---- phase 2: SSM step, rows [sr0, sr1); a row is N/4 lanes x 4 states
+  {
+    const int lpr = sa.N / 4, rpw = 32 / lpr;
+    const int n4 = (lane % lpr) * 4;
+    const int hpg = sa.H / sa.G;
+    for (int rb = sr0 + warp * rpw; rb < sr1; rb += kMmaWarps * rpw) {
+      const int r = rb + lane / lpr;
+      const bool live = r < sr1;  // uniform across the lanes of one row
+      const int rr = live ? r : sr1 - 1;
+      const int h = rr / sa.P, p = rr % sa.P, gi = h / hpg;
+      float* hp = sa.h + (size_t)rr * sa.N + n4;
+      float4 hv = __ldcg(reinterpret_cast<const float4*>(hp));
+      float dt, dA;
+      ssm_dt_dA(bf16_to_f32(__ldcg(sa.dt + h)), __ldg(sa.dt_bias + h), __ldg(sa.A_log + h), dt, dA);
+      const float xv = bf16_to_f32(__ldcg(sa.x + (size_t)h * sa.P + p));
+      const uint2 bu = __ldcg(reinterpret_cast<const uint2*>(sa.Bm + (size_t)gi * sa.N + n4));
+      const uint2 cu = __ldcg(reinterpret_cast<const uint2*>(sa.Cm + (size_t)gi * sa.N + n4));
+      const float4 Bv = make_float4(bf16lo(bu.x), bf16hi(bu.x), bf16lo(bu.y), bf16hi(bu.y));
+      const float4 Cv = make_float4(bf16lo(cu.x), bf16hi(cu.x), bf16lo(cu.y), bf16hi(cu.y));
+      const float dtx = dt * xv;
+      hv.x = fmaf(dA, hv.x, dtx * Bv.x);
+      hv.y = fmaf(dA, hv.y, dtx * Bv.y);
+      hv.z = fmaf(dA, hv.z, dtx * Bv.z);
+      hv.w = fmaf(dA, hv.w, dtx * Bv.w);
+      if (live) *reinterpret_cast<float4*>(hp) = hv;
+      float yp = Cv.x * hv.x + Cv.y * hv.y + Cv.z * hv.z + Cv.w * hv.w;
+      for (int o = lpr / 2; o > 0; o >>= 1) yp += __shfl_xor_sync(0xffffffffu, yp, o);
+      if (live && (lane % lpr) == 0) sa.y[(size_t)h * sa.P + p] = yp + __ldg(sa.D + h) * xv;
+    }
+    if (blockIdx.x == 0 && tid == 0 && sa.pos_inc) sa.pos_inc[0] += 1;  // every CTA has read it
+  }
+  fused_grid_barrier(tid, kC);
+
+  // ---- phase 3: out_proj
+  fused_norm_row<FP8>(a3, 0, act_s, tot, tail->unscale, tid, kC);
+  for (int i = tid; i < rows_out * kMmaWarps; i += kC) tot[i] = 0.0f;
+  named_bar(1, kC);
+  if (!dead && !mma_consume<FP8>(a3, p3, p1.nst, S, stg, tail, act_s, tot, rows_out, warp, lane)) dead = true;
+  if (bulk3 && !dead && !mbar_wait(&tail->epi_bar2, 0)) dead = true;
+  __syncthreads();  // all consumers and the producer (after its drain)
+  {
+    const float us = tail->unscale[0];
+    for (int r = tid; r < p3.nrows; r += kC) {
+      float sum = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) sum += tot[(size_t)w * rows_out + r];
+      a3.out[p3.row_begin + r] = f32_to_bf16(bf16_to_f32(rsS[r]) + sum * us);
+    }
+  }
+}
+
+// The chunking gemv_mma_kernel's launch picks for projection a at batch 1.
+static void chain_chunking(const GemvArgs& a, int es, int& kc, int& whole) {
+  const int nrg = (a.N + kMmaRows - 1) / kMmaRows;
+  int grid = num_sms();
+  if (grid > nrg) grid = nrg;
+  const int rows_max = ((nrg + grid - 1) / grid) * kMmaRows;
+  const MmaLayout lay = mma_layout(a.K, es, rows_max, 1, a.epi, a.dconv);
+  kc = lay.kc;
+  whole = lay.whole ? 1 : 0;
+}
+
+bool decode_fused_supported(const FusedStepArgs& fa, bool fp8) {
+  const GemvArgs& a1 = fa.in;
+  const GemvArgs& a3 = fa.out;
+  const SsmArgs& s = fa.ssm;
+  if (a1.M != 1 || a3.M != 1 || !gemv_mma_supported(1, a1.K) || !gemv_mma_supported(1, a3.K)) return false;
+  if (a1.epi != EPI_INPROJ_CONV || a3.epi != EPI_RESID || a1.norm != NORM_RMS || a3.norm != NORM_GATED) return false;
+  if (a1.dconv < 2 || s.B != 1 || s.N % 4 != 0 || s.N < 4 || s.N > 128 || ((s.N / 4) & (s.N / 4 - 1)) != 0) return false;
+  if (s.G < 1 || s.H % s.G != 0) return false;
+  int coop = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+    return false;
+  if (!coop) return false;
+  const int G = num_sms();
+  const int rin = (((a1.N + kMmaRows - 1) / kMmaRows + G - 1) / G) * kMmaRows;
+  const int rout = (((a3.N + kMmaRows - 1) / kMmaRows + G - 1) / G) * kMmaRows;
+  const FusedLayout lay = fused_layout(a1.K, a3.K, rin, rout, a1.dconv);
+  int kc, whole;
+  for (const GemvArgs* g : {&a1, &a3}) {  // a stage of the stand-alone chunking fits the ring stride
+    chain_chunking(*g, fp8 ? 1 : 2, kc, whole);
+    const int sb = whole ? kMmaRows * g->K * (fp8 ? 1 : 2) : kMmaRows * (kc + kRowPad);
+    if (sb > kFusedStride) return false;
+  }
+  return lay.stages >= 2 && lay.total <= 227 * 1024;
+}
+
+template <bool FP8>
+static cudaError_t launch_fused_one(const FusedStepArgs& fa, cudaStream_t st) {
+  static int done_mask[64] = {0};
+  static int pdl_mode = -1;  // -1 untried, 1 cooperative + PDL accepted, 0 cooperative alone
+  const int G = num_sms();
+  const int rin = (((fa.in.N + kMmaRows - 1) / kMmaRows + G - 1) / G) * kMmaRows;
+  const int rout = (((fa.out.N + kMmaRows - 1) / kMmaRows + G - 1) / G) * kMmaRows;
+  const FusedLayout lay = fused_layout(fa.in.K, fa.out.K, rin, rout, fa.in.dconv);
+  if (lay.stages < 2 || lay.total > 227 * 1024) return cudaErrorInvalidConfiguration;
+  auto kern = decode_step_fused_kernel<FP8>;
+  cudaError_t e = set_smem_once((const void*)kern, lay.total, done_mask);
+  if (e != cudaSuccess) return e;
+  static int occ_smem = -1, occ_blocks = 0;  // all CTAs must be resident at once
+  if (occ_smem != lay.total) {
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, kMmaThreads, lay.total)) != cudaSuccess)
+      return e;
+    occ_smem = lay.total;
+  }
+  if (occ_blocks < 1) return cudaErrorCooperativeLaunchTooLarge;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = lay.total;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  trace_pre(K_DECODE_FUSED, st);
+  cfg.numAttrs = pdl_mode == 0 ? 1 : 2;
+  FusedChunks ck;
+  chain_chunking(fa.in, FP8 ? 1 : 2, ck.kc_in, ck.whole_in);
+  chain_chunking(fa.out, FP8 ? 1 : 2, ck.kc_out, ck.whole_out);
+  e = cudaLaunchKernelEx(&cfg, kern, fa, rin, rout, ck);
+  if (e != cudaSuccess && pdl_mode == -1) {
+    cudaGetLastError();  // the attribute pair was refused: cooperative alone from now on
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, fa, rin, rout, ck);
+    if (e == cudaSuccess) pdl_mode = 0;
+  } else if (e == cudaSuccess && pdl_mode == -1) {
+    pdl_mode = 1;
+  }
+  trace_post(K_DECODE_FUSED, st);
+  return e;
+}
+
+cudaError_t launch_decode_fused(const FusedStepArgs& fa, bool fp8, cudaStream_t s) {
+  return fp8 ? launch_fused_one<true>(fa, s) : launch_fused_one<false>(fa, s);
+}
+
 int status_gemv_mma(int clear) {
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
   if (clear) {
     const int z = 0;
     cudaMemcpyToSymbol(g_status, &z, sizeof(int));
+    // a timed-out grid barrier may have left arrivals behind
+    const unsigned zb[2] = {0u, 0u};
+    cudaMemcpyToSymbol(g_fused_bar, zb, sizeof(zb));
   }
   return v;
 }

@@ -191,10 +191,7 @@ __device__ __forceinline__ float4 ld4bf(const uint16_t* p) {
 
 __device__ __forceinline__ void head_scalars(const uint16_t* dt_row, const float* dt_bias, const float* A_log, int h,
                                              float& dt, float& dA) {
-  float d = softplus_f(bf16_to_f32(dt_row[h]) + dt_bias[h]);
-  d = fminf(fmaxf(d, 1e-9f), 1e9f);
-  dt = d;
-  dA = expf(d * -expf(A_log[h]));
+  ssm_dt_dA(bf16_to_f32(dt_row[h]), dt_bias[h], A_log[h], dt, dA);
 }
 
 template <int LPR, int ROWS>

@@ -77,7 +77,7 @@ static const char* kNames[K_COUNT] = {
     "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
     "conv_pos",      "ssm_step",        "conv_prefill",    "ssm_scan_seq",
     "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out",   "gemm_tc_reduce",
-    "conv_ring_store"};
+    "conv_ring_store", "decode_step_fused"};
 
 // ------------------------------------------------------------------ helpers
 
@@ -192,10 +192,10 @@ static bool proj_f16(const m2_weight& w, int M) {
   return w.fmt == M2_W_FP8_BLOCK128 && !gemm_tc_supported(M, w.n, w.k, true);
 }
 
-static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
-                        GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr,
-                        const float* unscale = nullptr, int pdl = 0, float* part = nullptr,
-                        size_t part_bytes = 0) {
+static GemvArgs proj_args(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
+                          GemvEpi epi, const uint16_t* resid, int ldr, GemvArgs* extra = nullptr,
+                          const float* unscale = nullptr, int pdl = 0, float* part = nullptr,
+                          size_t part_bytes = 0) {
   GemvArgs a;
   memset(&a, 0, sizeof(a));
   if (extra) a = *extra;
@@ -220,8 +220,22 @@ static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, u
   const int rowbytes = w.k * (w.fmt == M2_W_FP8_BLOCK128 ? 1 : 2);
   const int grp = rowbytes <= 4096 ? 4 : (rowbytes <= 8192 ? 2 : 1);
   a.evict_first = M <= grp ? 1 : 0;
+  return a;
+}
+
+static cudaError_t proj(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
+                        GemvEpi epi, const uint16_t* resid, int ldr, cudaStream_t s, GemvArgs* extra = nullptr,
+                        const float* unscale = nullptr, int pdl = 0, float* part = nullptr,
+                        size_t part_bytes = 0) {
+  const GemvArgs a = proj_args(w, A, lda, M, out, ldo, epi, resid, ldr, extra, unscale, pdl, part, part_bytes);
   return launch_gemv(a, w.fmt == M2_W_FP8_BLOCK128, s);
 }
+
+// Batch-1 decode as one cooperative launch (m2_set_fused_decode).  Off by
+// default: measured on the 8B-like layer it takes 43 us per step against 32 us
+// for the PDL-chained kernels, whose SSM and out_proj work hides under the
+// neighbouring kernels while the single launch runs its phases back to back.
+static int g_fused_decode = 0;
 
 static int launch_status(cudaError_t e) {
   if (e != cudaSuccess) {
@@ -302,8 +316,10 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   // Each kernel is launched as a programmatic dependent of the previous one,
   // so that a GEMV streams its weights while its predecessor drains.  With the
   // decode GEMV (B <= 8) the two norms run inside the GEMVs' prologues: three
-  // kernels per step.  Otherwise (tensor-core projections) a norm kernel
-  // precedes each projection: five.
+  // kernels per step (at B = 1 optionally one cooperative kernel for the whole
+  // step).
+  // Otherwise (tensor-core projections) a norm kernel precedes each
+  // projection: five.
   const bool fuse = !gemm_tc_supported(B, r.n_in, d.hidden, true) && gemv_mma_supported(B, d.hidden) &&
                     gemv_mma_supported(B, r.d_inner) && d.gnorm_group == r.d_inner;
   // 1. input RMSNorm -> GEMV activation
@@ -325,6 +341,8 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     if ((e = launch_prep(pa, stream))) return launch_status(e);
   }
   // 2+3. in_proj, conv1d update (bias, SiLU) in its epilogue
+  FusedStepArgs fa;
+  memset(&fa, 0, sizeof(fa));
   GemvArgs ex;
   memset(&ex, 0, sizeof(ex));
   ex.ring = conv_state;
@@ -340,9 +358,8 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     ex.norm_eps = d.eps_in;
     ex.norm_inv_k = 1.0 / (double)d.hidden;
   }
-  if ((e = proj(L->in_proj, fuse ? hidden : xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, stream, &ex,
-                fuse ? nullptr : us_in, 1, part, part_bytes)))
-    return launch_status(e);
+  fa.in = proj_args(L->in_proj, fuse ? hidden : xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, &ex,
+                    fuse ? nullptr : us_in, 1, part, part_bytes);
   // 4+5. split and SSM step (advances conv_pos)
   SsmArgs sa;
   memset(&sa, 0, sizeof(sa));
@@ -374,6 +391,31 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
       sa.l2_prefetch_bytes = wo_bytes;
     }
   }
+  // 7+8. out_proj with the residual add in its epilogue (in place on hidden)
+  GemvArgs eo;
+  memset(&eo, 0, sizeof(eo));
+  if (fuse) {
+    eo.norm = NORM_GATED;
+    eo.norm_w = L->gnorm_w;
+    eo.norm_eps = d.eps_gated;
+    eo.norm_inv_k = 1.0 / (double)r.d_inner;
+    eo.gy = y;
+    eo.ldgy = r.d_inner;
+    eo.gz = zxu;
+    eo.ldgz = r.ldz;
+  }
+  fa.out = proj_args(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, &eo,
+                     fuse ? nullptr : us_out, 1, part, part_bytes);
+  fa.ssm = sa;
+  const bool fp8 = L->in_proj.fmt == M2_W_FP8_BLOCK128;
+  if (fuse && B == 1 && g_fused_decode && L->in_proj.fmt == L->out_proj.fmt) {
+    // the whole step in one launch: SSM state and the out_proj weights are
+    // handled inside (no L2 prefetch hand-off needed)
+    fa.ssm.l2_prefetch = nullptr;
+    fa.ssm.l2_prefetch_bytes = 0;
+    if (decode_fused_supported(fa, fp8)) return launch_status(launch_decode_fused(fa, fp8, stream));
+  }
+  if ((e = launch_gemv(fa.in, fp8, stream))) return launch_status(e);
   if ((e = launch_ssm_step(sa, stream))) return launch_status(e);
   // 6. gated RMSNorm -> GEMV activation
   if (!fuse) {
@@ -395,22 +437,7 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     pa.pdl = 1;
     if ((e = launch_prep(pa, stream))) return launch_status(e);
   }
-  // 7+8. out_proj with the residual add in its epilogue (in place on hidden)
-  GemvArgs eo;
-  memset(&eo, 0, sizeof(eo));
-  if (fuse) {
-    eo.norm = NORM_GATED;
-    eo.norm_w = L->gnorm_w;
-    eo.norm_eps = d.eps_gated;
-    eo.norm_inv_k = 1.0 / (double)r.d_inner;
-    eo.gy = y;
-    eo.ldgy = r.d_inner;
-    eo.gz = zxu;
-    eo.ldgz = r.ldz;
-  }
-  if ((e = proj(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, stream, &eo,
-                fuse ? nullptr : us_out, 1, part, part_bytes)))
-    return launch_status(e);
+  if ((e = launch_gemv(fa.out, L->out_proj.fmt == M2_W_FP8_BLOCK128, stream))) return launch_status(e);
   return M2_OK;
 }
 
@@ -821,6 +848,12 @@ int m2_trace_end(double* ms, int32_t* launches, int32_t n_ids) {
   const int used = g_trace_used;
   g_trace_used = 0;
   return used;
+}
+
+int m2_set_fused_decode(int enable) {
+  const int prev = g_fused_decode;
+  g_fused_decode = enable ? 1 : 0;
+  return prev;
 }
 
 const char* m2_kernel_name(int32_t id) { return (id >= 0 && id < K_COUNT) ? kNames[id] : nullptr; }

@@ -119,6 +119,15 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t v, float& lo, float& hi) 
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 __device__ __forceinline__ float softplus_f(float v) { return v > 20.0f ? v : log1pf(expf(v)); }
 
+// Per-head scalars of the SSM step from the raw dt projection output:
+// dt = clamp(softplus(dt_raw + dt_bias), 1e-9, 1e9), dA = exp(dt * A), A = -exp(A_log).
+__device__ __forceinline__ void ssm_dt_dA(float dt_raw, float dt_bias, float A_log, float& dt, float& dA) {
+  float d = softplus_f(dt_raw + dt_bias);
+  d = fminf(fmaxf(d, 1e-9f), 1e9f);
+  dt = d;
+  dA = expf(d * -expf(A_log));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

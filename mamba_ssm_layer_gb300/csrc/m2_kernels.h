@@ -30,6 +30,7 @@ enum KernelId : int32_t {
   K_SSD_CHUNK_OUT,
   K_GEMM_TC_REDUCE,
   K_CONV_RING,
+  K_DECODE_FUSED,
   K_COUNT
 };
 
@@ -224,6 +225,20 @@ struct SsmArgs {
   size_t l2_prefetch_bytes;
 };
 cudaError_t launch_ssm_step(const SsmArgs& a, cudaStream_t s);
+
+// The whole decode step of one sequence in one cooperative launch
+// (k_gemv_mma.cu): in = the in_proj GEMV (M = 1, NORM_RMS, EPI_INPROJ_CONV),
+// ssm = the SSM step (B = 1, y written for the gated norm, pos_inc advanced),
+// out = the out_proj GEMV (M = 1, NORM_GATED on ssm.y and z, EPI_RESID in
+// place).  Both projections in the same format (fp8).  Calls on one device
+// must not overlap: the grid barriers share one device-wide counter.
+struct FusedStepArgs {
+  GemvArgs in;
+  SsmArgs ssm;
+  GemvArgs out;
+};
+bool decode_fused_supported(const FusedStepArgs& fa, bool fp8);
+cudaError_t launch_decode_fused(const FusedStepArgs& fa, bool fp8, cudaStream_t s);
 
 // Largest batch row count one GEMV pass covers for a K-wide row.
 int gemv_rows_per_pass(int K, bool fp8);

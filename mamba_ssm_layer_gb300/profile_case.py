@@ -3,6 +3,7 @@
   python -m mamba_ssm_layer_gb300.profile_case decode_b1  [--steps 4]
   python -m mamba_ssm_layer_gb300.profile_case decode_b64 [--steps 3]
   python -m mamba_ssm_layer_gb300.profile_case prefill_1k [--steps 2]
+  python -m mamba_ssm_layer_gb300.profile_case prefill_1k_w8a8 [--steps 2]
 
 Small on purpose: at most a few hundred MB on the device, with the weights
 rotated over two copies so that a decode step's inputs are not left in L2 by
@@ -34,19 +35,20 @@ def _copy_layer(dl: DeviceLayer) -> DeviceLayer:
 
 def main() -> None:
     p = argparse.ArgumentParser()
-    p.add_argument("workload", choices=["decode_b1", "decode_b64", "prefill_1k"])
+    p.add_argument("workload", choices=["decode_b1", "decode_b64", "prefill_1k", "prefill_1k_w8a8"])
     p.add_argument("--steps", type=int, default=4)
     a = p.parse_args()
     abi.lib()
     d = synth.NEMOTRON_H_8B
-    if a.workload == "prefill_1k":
+    if a.workload.startswith("prefill_1k"):
         T = 1024
         dl = DeviceLayer(synth.make_layer(d, synth.WL_8B_PREFILL_1K))
-        ws = dl.workspace(1, T)
+        ws = dl.workspace_varlen(1, T)
         st = dl.new_state(1)
         x = to_dev(synth.make_hidden(T, d["hidden"], synth.WL_8B_PREFILL_1K, 0, 0))
         for _ in range(a.steps):
-            dl.prefill(x, (st[0][0], st[1][0], st[2][:1]), ws)
+            dl.prefill_varlen(x, [0, T], (st[0][:1], st[1][:1], st[2][:1]), ws,
+                              w8a8=a.workload.endswith("w8a8"))
     else:
         B = 1 if a.workload == "decode_b1" else 64
         wl = synth.WL_8B_DECODE_B1 if B == 1 else synth.WL_8B_DECODE_B64
