@@ -395,7 +395,8 @@ def main():
     }
 
     if not args.no_extras:
-        out["decode_b64"] = _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, 8 if args.quick else 32)
+        out["decode_tiny"] = _bench_tiny(torch, synth, DeviceLayer, to_dev, 100 if args.quick else 400)
+        out["decode_b64"] = _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, 8 if args.quick else 64)
         out["prefill_1k"] = _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, 2 if args.quick else 5)
         out["prefill_1k_w8a8"] = _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, 2 if args.quick else 5,
                                                 w8a8=True)
@@ -436,7 +437,7 @@ def _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, steps):
     sts = [dl.new_state(B) for _ in range(2)]  # 2 x 268 MB of state > L2
     ws = dl.workspace(B, 0)
     hs = [to_dev(synth.make_hidden(B, d["hidden"], synth.WL_8B_DECODE_B64, 0, i)) for i in range(4)]
-    for i in range(3):
+    for i in range(64):  # 32 warm-up steps of random inputs for each of the two state sets
         dl.decode(hs[i % 4], sts[i % 2], ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -455,6 +456,28 @@ def _bench_b64(torch, synth, DeviceLayer, to_dev, abi, lay, steps):
     return {"value": B / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "batch": B,
             "hbm_gbs": per / (ms / 1e3) / 1e9, "hbm_frac": per / (ms / 1e3) / 1e9 / hbm,
             "kernels_ms_per_step": {k: v[0] / steps for k, v in tr.items()}}
+
+
+def _bench_tiny(torch, synth, DeviceLayer, to_dev, steps):
+    """Tiny layer (hidden 256), batch-1 decode: launch-latency bound, L2-resident."""
+    d = synth.TINY
+    lay = synth.make_layer(d, synth.WL_TINY_DECODE)
+    dl = DeviceLayer(lay)
+    st = dl.new_state(1)
+    ws = dl.workspace(1, 0)
+    hs = [to_dev(synth.make_hidden(1, d["hidden"], synth.WL_TINY_DECODE, 3, i)) for i in range(16)]
+    for i in range(10):
+        dl.decode(hs[i % 16], st, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        dl.decode(hs[i % 16], st, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": 1.0 / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "batch": 1,
+            "launch": "eager", "bound": "launch latency (weights and state L2-resident)"}
 
 
 def _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, reps, w8a8=False):

@@ -26,9 +26,10 @@ def _built():
     assert abi.m2_device_status() == abi.M2_OK
 
 
-def _varlen_case(lay, lens, warm, key):
+def _varlen_case(lay, lens, warm, key, w8a8=False):
     """`warm` batched decode steps of all sequences, then one varlen prefill of
-    lens[i] tokens per sequence; every sequence checked against the oracle."""
+    lens[i] tokens per sequence (w8a8: on the FP8-activation arm, against the
+    oracle's W8A8 layer); every sequence checked against the oracle."""
     d = lay["dims"]
     hd = d["hidden"]
     n = len(lens)
@@ -36,6 +37,7 @@ def _varlen_case(lay, lens, warm, key):
     T = int(cu[-1])
     dl = DeviceLayer(lay)
     ol = orc.OracleLayer(lay)
+    olp = orc.OracleLayer(lay, act_fp8=True) if w8a8 else ol  # the prefill's definition
     st = dl.new_state(n)
     ost = [ol.new_state() for _ in range(n)]
     trk = [FlipTracker(d, lay["A_log"], lay["dt_bias"], lay["conv_w"]) for _ in range(n)]
@@ -53,7 +55,7 @@ def _varlen_case(lay, lens, warm, key):
     hid = synth.make_hidden(T, hd, *key, 0)
     x = to_dev(hid)
     ws = dl.workspace_varlen(n, T)
-    dl.prefill_varlen(x, cu, st, ws)
+    dl.prefill_varlen(x, cu, st, ws, w8a8=w8a8)
     torch.cuda.synchronize()
     assert abi.m2_device_status() == abi.M2_OK
     r3, r4 = _codes_prefill(ws, T, lay)
@@ -66,7 +68,7 @@ def _varlen_case(lay, lens, warm, key):
         a, b = int(cu[i]), int(cu[i + 1])
         ref = hid[a:b].copy()
         if b > a:
-            _, e3, e4 = ol.run_traced(ref, *ost[i])
+            _, e3, e4 = olp.run_traced(ref, *ost[i])
             for t in range(b - a):
                 trk[i].token(r3[a + t], (e3[0][t], e3[1][t]), r4[a + t], (e4[0][t], e4[1][t]))
             worst = max(worst, floored_rel_err(bf16_to_f64(got[a:b]), bf16_to_f64(ref), axis=-1))
@@ -81,6 +83,13 @@ def _varlen_case(lay, lens, warm, key):
 def test_varlen_tiny_mixed_lengths_with_empty_sequence():
     lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
     _varlen_case(lay, [5, 0, 130, 1, 127, 128, 3], 2, (synth.WL_TINY_DECODE, 70))
+
+
+def test_varlen_w8a8_tiny_mixed_lengths():
+    # the W8A8 arm over a varlen batch: per-token activation blocks ignore
+    # sequence boundaries; an empty and a one-token sequence included
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    _varlen_case(lay, [9, 1, 130, 0, 40], 2, (synth.WL_TINY_DECODE, 74), w8a8=True)
 
 
 def test_varlen_tiny_bf16_weights():
