@@ -475,9 +475,31 @@ def _bench_tiny(torch, synth, DeviceLayer, to_dev, steps):
         dl.decode(hs[i % 16], st, ws)
     e1.record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    return {"value": 1.0 / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "batch": 1,
-            "launch": "eager", "bound": "launch latency (weights and state L2-resident)"}
+    ms_eager = e0.elapsed_time(e1) / steps
+    ms, launch = ms_eager, "eager"
+    try:  # the same steps replayed from a CUDA graph of 16 steps
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(16):
+                dl.decode(hs[i], st, ws)
+        torch.cuda.current_stream().wait_stream(cap)
+        reps = max(1, steps // 16)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_g = e0.elapsed_time(e1) / (reps * 16)
+        if ms_g < ms:
+            ms, launch = ms_g, "cuda_graph replay"
+    except Exception:  # capture unsupported: the eager number stands
+        pass
+    return {"value": 1.0 / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms, "batch": 1, "launch": launch,
+            "ms_per_step_eager": ms_eager, "bound": "launch latency (weights and state L2-resident)"}
 
 
 def _bench_prefill(torch, synth, DeviceLayer, to_dev, abi, reps, w8a8=False):
@@ -558,26 +580,85 @@ def _bench_stack8(torch, synth, to_dev):
 def _bench_e2e(torch, synth, reps, ws, d, B, K):
     """Same decode metric through the C ABI with host buffers: per step the
     hidden row is copied from pinned host memory to the device and the layer
-    output back, inside the timed region."""
+    output back, inside the timed region.  Three forms are timed and the
+    fastest is reported: (a) cudaMemcpyAsync and kernels on one stream; (b)
+    copies on a second stream, double-buffered, so that step i+1's input lands
+    while step i runs and step i's output drains while step i+1 runs (events
+    order them); (c) the library's m2_copy kernels on the one stream, which keep
+    the launch chain unbroken."""
     R = len(reps)
     host_in = [torch.from_numpy(synth.make_hidden(B, d["hidden"], 9, 9, i).view(np.int16)).pin_memory()
                for i in range(8)]
-    host_out = torch.empty((B, d["hidden"]), dtype=torch.int16).pin_memory()
-    dev = torch.empty((B, d["hidden"]), dtype=torch.int16, device="cuda")
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(K):
-        dev.copy_(host_in[i % 8], non_blocking=True)
-        dl, st = reps[i % R]
-        dl.decode(dev, st, ws)
-        host_out.copy_(dev, non_blocking=True)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / K
+    host_out = [torch.empty((B, d["hidden"]), dtype=torch.int16).pin_memory() for _ in range(2)]
+    devs = [torch.empty((B, d["hidden"]), dtype=torch.int16, device="cuda") for _ in range(2)]
     nbytes = B * d["hidden"] * 2
+    comp = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def one_stream():
+        e0.record()
+        for i in range(K):
+            devs[0].copy_(host_in[i % 8], non_blocking=True)
+            dl, st = reps[i % R]
+            dl.decode(devs[0], st, ws)
+            host_out[0].copy_(devs[0], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    def two_streams():
+        copy = torch.cuda.Stream()
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_dec = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        e0.record(comp)
+        copy.wait_stream(comp)
+        with torch.cuda.stream(copy):
+            devs[0].copy_(host_in[0], non_blocking=True)
+            ev_in[0].record(copy)
+        for i in range(K):
+            b, nb = i % 2, (i + 1) % 2
+            if i + 1 < K:
+                with torch.cuda.stream(copy):
+                    if i >= 1:
+                        copy.wait_event(ev_out[nb])  # step i-1's output has left devs[nb]
+                    devs[nb].copy_(host_in[(i + 1) % 8], non_blocking=True)
+                    ev_in[nb].record(copy)
+            comp.wait_event(ev_in[b])
+            dl, st = reps[i % R]
+            dl.decode(devs[b], st, ws)
+            ev_dec[b].record(comp)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev_dec[b])
+                host_out[b].copy_(devs[b], non_blocking=True)
+                ev_out[b].record(copy)
+        comp.wait_event(ev_out[(K - 1) % 2])
+        e1.record(comp)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    def copy_kernels():
+        # the library's staging copy (a kernel in the same launch chain)
+        from mamba_ssm_layer_gb300 import abi
+        e0.record()
+        for i in range(K):
+            abi.m2_copy(devs[0], host_in[i % 8], nbytes, comp)
+            dl, st = reps[i % R]
+            dl.decode(devs[0], st, ws)
+            abi.m2_copy(host_out[0], devs[0], nbytes, comp)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    forms = {"one stream, cudaMemcpyAsync": one_stream, "copy stream, double-buffered": two_streams,
+             "one stream, m2_copy kernels": copy_kernels}
+    for f in forms.values():  # warm every form
+        f()
+    times = {k: f() for k, f in forms.items()}
+    best = min(times, key=times.get)
+    ms = times[best]
     return {"value": B / (ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes,
-            "ms_per_step": ms}
+            "ms_per_step": ms, "form": best, "ms_per_step_by_form": times}
 
 
 if __name__ == "__main__":

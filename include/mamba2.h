@@ -266,6 +266,18 @@ int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint1
 int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t B,
                                 float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, cudaStream_t stream);
 
+/* Stream-ordered copy of `bytes` between device memory and/or page-locked host
+ * memory (cudaHostAlloc / cudaHostRegister), done by a kernel launched as a
+ * programmatic dependent of the previous kernel on `stream`.  A decode loop
+ * that stages its hidden rows through host buffers then stays one chain of
+ * kernels: a cudaMemcpyAsync between two launches keeps the next layer kernel
+ * from starting its weight stream before the copy and the kernel before it
+ * have finished.  dst and src 16-byte aligned, bytes a multiple of 16
+ * (M2_ERR_ALIGN otherwise); pageable host memory or an unknown pointer:
+ * M2_ERR_ARG, nothing launched.  Host pointers are checked on the host
+ * (cudaPointerGetAttributes) before the launch. */
+int m2_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------ diagnostics */
 
 /* Device status word: M2_OK, or the first M2_ERR_TIMEOUT a kernel recorded on

@@ -35,7 +35,7 @@ EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_dec
            "mamba2_layer_decode_noalloc", "mamba2_layer_prefill_varlen", "m2_workspace_bytes_varlen",
            "mamba2_layer_prefill_varlen_w8a8", "w8a8_gemm", "m2_w8a8_workspace_bytes",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
-           "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count", "m2_set_fused_decode")
+           "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count", "m2_set_fused_decode", "m2_copy")
 
 
 class M2Dims(C.Structure):
@@ -108,6 +108,7 @@ def lib():
             l.m2_kernel_name.argtypes = [I32]; l.m2_kernel_name.restype = C.c_char_p
             l.m2_kernel_count.argtypes = []; l.m2_kernel_count.restype = I32
             l.m2_set_fused_decode.argtypes = [C.c_int]; l.m2_set_fused_decode.restype = C.c_int
+            l.m2_copy.argtypes = [P, P, C.c_size_t, P]; l.m2_copy.restype = C.c_int
             _lib = l
     return _lib
 
@@ -234,6 +235,12 @@ def mamba2_ssm_step(h, x, Bm, Cm, dt_raw, ld_in, A_log, D, dt_bias, y, B, H, P, 
     st = lib().mamba2_ssm_step(_ptr(h), _ptr(x), _ptr(Bm), _ptr(Cm), _ptr(dt_raw), ld_in, _ptr(A_log), _ptr(D),
                                _ptr(dt_bias), _ptr(y), B, H, P, N, G, _stream(stream))
     return _check("mamba2_ssm_step", st) if check else st
+
+
+def m2_copy(dst, src, nbytes: int, stream=None, check=True) -> int:
+    """Kernel copy between device tensors and/or pinned host tensors (stays in the PDL launch chain)."""
+    st = lib().m2_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream))
+    return _check("m2_copy", st) if check else st
 
 
 def m2_device_status(clear: bool = False) -> int:

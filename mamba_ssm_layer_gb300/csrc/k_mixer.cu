@@ -62,6 +62,30 @@ cudaError_t launch_conv_pos(int32_t* pos, int32_t B, int32_t add, cudaStream_t s
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ staging copy
+
+// Stream-ordered copy by a kernel (device memory and/or pinned host memory
+// reached through its unified address).  Launched as a programmatic dependent:
+// it waits for the previous kernel (which may still read dst or write src)
+// before touching either, and lets the next kernel start its own prologue.
+__global__ void __launch_bounds__(256) copy16_kernel(const uint4* src, uint4* dst, size_t n16) {
+  pdl_wait();
+  pdl_trigger();
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
+cudaError_t launch_copy16(const void* src, void* dst, size_t n16, cudaStream_t s) {
+  size_t blocks = (n16 + 255) / 256;
+  if (blocks > (size_t)num_sms()) blocks = (size_t)num_sms();
+  if (blocks < 1) blocks = 1;
+  trace_pre(K_COPY, s);
+  const cudaError_t e = launch_k(copy16_kernel, dim3((unsigned)blocks), dim3(256), 0, s, true,
+                                 static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
+  trace_post(K_COPY, s);
+  return e;
+}
+
 // Sequence of token row t in a varlen batch: the i with cu[i] <= t < cu[i+1]
 // (sequences of length 0 are skipped by taking the last such i).
 __device__ __forceinline__ int seq_of(const int32_t* cu, int n, int t) {

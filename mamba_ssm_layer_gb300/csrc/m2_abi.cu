@@ -77,7 +77,7 @@ static const char* kNames[K_COUNT] = {
     "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
     "conv_pos",      "ssm_step",        "conv_prefill",    "ssm_scan_seq",
     "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out",   "gemm_tc_reduce",
-    "conv_ring_store", "decode_step_fused"};
+    "conv_ring_store", "decode_step_fused", "copy"};
 
 // ------------------------------------------------------------------ helpers
 
@@ -719,6 +719,34 @@ int w8a8_gemm(const uint16_t* A, const uint8_t* W, const uint16_t* S, uint16_t* 
   qa.sq = sq;
   qa.ldsq = ldsq;
   return launch_status(proj(w, A, K, M, out, N, EPI_STORE, nullptr, 0, stream, &qa));
+}
+
+// Device-accessible address of p: device memory as is; page-locked host memory
+// through its unified address; nullptr for anything else (pageable host memory).
+static const void* device_view(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+  if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+    // the same offset into the page-locked allocation
+    const char* hb = static_cast<const char*>(at.hostPointer);
+    const char* db = static_cast<const char*>(at.devicePointer);
+    return db + (static_cast<const char*>(p) - hb);
+  }
+  return nullptr;
+}
+
+int m2_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+  if (!dst || !src) return M2_ERR_ARG;
+  if (bytes == 0) return M2_OK;
+  if (!al16(dst) || !al16(src) || bytes % 16) return M2_ERR_ALIGN;
+  const void* s = device_view(src);
+  void* d = const_cast<void*>(device_view(dst));
+  if (!s || !d) return M2_ERR_ARG;
+  return launch_status(launch_copy16(s, d, bytes / 16, stream));
 }
 
 int conv1d_update(uint16_t* conv_state, int32_t* conv_pos, const uint16_t* x, int32_t ld_x, const uint16_t* w,

@@ -31,6 +31,7 @@ enum KernelId : int32_t {
   K_GEMM_TC_REDUCE,
   K_CONV_RING,
   K_DECODE_FUSED,
+  K_COPY,
   K_COUNT
 };
 
@@ -203,6 +204,9 @@ cudaError_t launch_conv_update(uint16_t* ring, const int32_t* pos, const uint16_
                                const uint16_t* w, const uint16_t* b, uint16_t* out, int32_t ldo, int32_t B,
                                int32_t C, int32_t dconv, int32_t silu, cudaStream_t s);
 cudaError_t launch_conv_pos(int32_t* pos, int32_t B, int32_t add, cudaStream_t s);
+// n16 16-byte units from src to dst (both 16-byte aligned, device-accessible
+// addresses), as a programmatic dependent of the previous kernel.
+cudaError_t launch_copy16(const void* src, void* dst, size_t n16, cudaStream_t s);
 
 struct SsmArgs {
   float* h;            // [B][H][P][N]

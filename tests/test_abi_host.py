@@ -119,4 +119,8 @@ def test_entry_points_reject_before_launch(lib):
                                check=False) == abi.M2_ERR_UNSUPPORTED
     assert abi.mamba2_ssm_step(FAKE, FAKE, FAKE, FAKE, FAKE, 64, FAKE, FAKE, FAKE, FAKE, 1, 8, 8, 16, 3,
                                check=False) == abi.M2_ERR_ARG
+    assert abi.m2_copy(None, FAKE, 16, check=False) == abi.M2_ERR_ARG
+    assert abi.m2_copy(FAKE, FAKE + 8, 16, check=False) == abi.M2_ERR_ALIGN
+    assert abi.m2_copy(FAKE, FAKE, 24, check=False) == abi.M2_ERR_ALIGN
+    assert abi.m2_copy(FAKE, FAKE, 0, check=False) == abi.M2_OK  # nothing to copy
     assert abi.m2_launch_count() == launches0  # nothing was launched by any of the above
