@@ -171,7 +171,7 @@ void or_bf16_gemv(const uint16_t* A, int M, const uint16_t* W, int N, int K, dou
 
 /* Sum of |terms| of the same products (the scale of the summation error of
  * any floating-point evaluation of the dot product); used only by tests that
- * judge rounding decisions. */
+ * check rounding decisions. */
 static void proj_abs(int fmt, const void* w, const uint16_t* s, const uint16_t* a, int N, int K, double* out) {
   int kb = (K + 127) / 128;
 #pragma omp parallel for schedule(static)
