@@ -77,6 +77,15 @@ struct TcBars {
   uint32_t tmem_base;
 };
 
+// Wait for the completion of k block j's MMAs: one tcgen05.commit per k block
+// arrives on mma_done[j % kTcTmemBufs].  Every caller asks for a k block whose
+// barrier cannot have completed a later phase yet (parity would alias): that
+// phase belongs to k block j + kTcTmemBufs, whose operands (or TMEM buffer)
+// the caller itself has still to provide.
+__device__ __forceinline__ bool kblock_done(TcBars* bars, int j) {
+  return mbar_wait(&bars->mma_done[j % kTcTmemBufs], (uint32_t)(j / kTcTmemBufs) & 1u);
+}
+
 template <int NT, bool AQ8 = false>
 constexpr int tc_smem_bytes() {
   return TcLayout<NT, AQ8>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
@@ -337,7 +346,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages;
-          if (gk >= kTcWStages && !mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)) dead = true;
+          if (gk >= kTcWStages) {
+            // the slot's previous tile: freed by the converters (w8a16), or by
+            // the completion of its k block's MMAs
+            const bool ok = (ta.fp8 && !AQ8) ? mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)
+                                             : kblock_done(bars, gk - kTcWStages);
+            if (!ok) dead = true;
+          }
           if (dead) break;
           if (ta.fp8) {  // E4M3 tile (plain for the converters; 128-byte swizzled for the W8A8 MMA)
             mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK);
@@ -363,7 +378,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % SA;
-          if (gk >= SA && !mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)) dead = true;
+          if (gk >= SA && !(ta.cs > 1 ? mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)
+                                      : kblock_done(bars, gk - SA)))
+            dead = true;
           if (dead) break;
           uint8_t* abuf = smem + Lay::kA + s * Lay::kABytes;
           mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);  // from all cs slices
@@ -436,10 +453,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc_mma(tmem + tb * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
             }
           }
+          // one commit per k block: its completion frees the TMEM partial for the
+          // epilogue and the operand slots it read (their producers wait on it)
           tc_commit(&bars->mma_done[tb]);
           if (ta.cs > 1) tc_commit_mc(&bars->a_empty[sa], cmask);
-          else tc_commit(&bars->a_empty[sa]);
-          tc_commit((ta.fp8 && !AQ8) ? &bars->wbf_empty[b] : &bars->w_empty[s]);
         }
       }
     }
@@ -455,7 +472,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1;
           if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
-          if (!dead && gk >= 2 && !mbar_wait(&bars->wbf_empty[b], ((gk / 2) - 1) & 1)) dead = true;
+          if (!dead && gk >= 2 && !kblock_done(bars, gk - 2)) dead = true;  // k block gk-2 read buffer b
           if (dead) break;
           const uint8_t* raw = smem + Lay::kW + s * kTcBM * kTcBK;
           uint8_t* dst = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
