@@ -16,8 +16,8 @@
 // Persistent CTAs walk work items (a tile, or a k range of a tile when the
 // tiles alone would leave most SMs idle) weight-tile major, so the token tiles
 // of one weight tile are adjacent and its bytes are re-read from L2.  Roles
-// (each ring has its own full/empty mbarriers, so no role waits on another
-// role's unrelated progress):
+// (each ring has its own fill barriers; a slot the MMA read is free again once
+// that k block's MMAs have completed, which one commit per k block signals):
 //   warp 0      weight producer (lane 0): TMA of the E4M3 tile [128][128]
 //               (plain 2-D map) into a 4-stage ring; bf16 weights go straight
 //               into a 4-stage ring of 128-byte-swizzled tiles.  It does not
@@ -27,9 +27,9 @@
 //               swizzle = the UMMA K-major canonical layout), 3-4 stages;
 //   warps 2-5   converters: E4M3 tile -> bf16 tile in the swizzled layout the
 //               MMA descriptor expects (double-buffered);
-//   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each) per k block
-//               into one of 4 TMEM partial buffers and commits to the barriers
-//               that free the buffers it read and wake the epilogue;
+//   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each; W8A8: 4 of
+//               K = 32) per k block into one of 4 TMEM partial buffers and one
+//               commit, which wakes the epilogue and frees the operand slots;
 //   warps 6-21  epilogue, four warps per TMEM lane quarter (each a quarter of
 //               the token columns): per k block, TMEM -> registers, acc += s * partial;
 //               per item, the store / residual / conv-update epilogue, or fp32
@@ -70,7 +70,7 @@ struct TcLayout {
 
 struct TcBars {
   uint64_t w_full[kTcWStages], w_empty[kTcWStages];
-  uint64_t wbf_full[2], wbf_empty[2];
+  uint64_t wbf_full[2];
   uint64_t a_full[4], a_empty[4];
   uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
   uint64_t sc_full[kTcTmemBufs];  // W8A8: the token scales of a k block have landed
@@ -302,15 +302,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kTcWStages; ++s) {
       mbar_init(&bars->w_full[s], 1);
-      mbar_init(&bars->w_empty[s], (ta.fp8 && !AQ8) ? 4 : 1);  // the converter warps, or the MMA commit
+      mbar_init(&bars->w_empty[s], 4);  // w8a16: the converter warps (otherwise the k block's completion frees it)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->wbf_full[b], 4);
-      mbar_init(&bars->wbf_empty[b], 1);
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(&bars->a_full[s], 1);
-      mbar_init(&bars->a_empty[s], ta.cs);  // the MMA commits of every CTA of the cluster
+      mbar_init(&bars->a_empty[s], ta.cs);  // cs > 1: the MMA commits of every CTA of the cluster
     }
     for (int b = 0; b < kTcTmemBufs; ++b) {
       mbar_init(&bars->mma_done[b], 1);
