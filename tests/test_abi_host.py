@@ -124,3 +124,40 @@ def test_entry_points_reject_before_launch(lib):
     assert abi.m2_copy(FAKE, FAKE, 24, check=False) == abi.M2_ERR_ALIGN
     assert abi.m2_copy(FAKE, FAKE, 0, check=False) == abi.M2_OK  # nothing to copy
     assert abi.m2_launch_count() == launches0  # nothing was launched by any of the above
+
+
+def _rup(v, a):
+    return (v + a - 1) // a * a
+
+
+def test_w8a8_workspace_follows_documented_layout(lib):
+    # codes [M][rup16(K)] bytes, then at the next 256-byte boundary the fp32
+    # scales [K/128][rup128(M)], the whole rounded up to 256 bytes
+    for M, K in [(9, 256), (70, 512), (1024, 4096), (130, 8192)]:
+        want = _rup(M * _rup(K, 16), 256) + _rup((K // 128) * _rup(M, 128) * 4, 256)
+        assert abi.m2_w8a8_workspace_bytes(M, K) == want, (M, K)
+    assert abi.m2_w8a8_workspace_bytes(0, 128) == 0
+
+
+def test_varlen_workspace_and_rejections_before_launch(lib):
+    d, L = _dims(), _layer()
+    w1 = abi.m2_workspace_bytes_varlen(d, 1, 1024)
+    assert 0 < w1 <= abi.m2_workspace_bytes_varlen(d, 16, 1024) < abi.m2_workspace_bytes_varlen(d, 16, 2048)
+    assert w1 >= abi.m2_workspace_bytes(d, 0, 1024)  # plus the W8A8 arm's codes and scales
+    assert abi.m2_workspace_bytes_varlen(_dims(d_state=96), 1, 64) == 0
+    launches0 = abi.m2_launch_count()
+    for cu in ([1, 5], [0, 5, 3], [0, 0]):
+        st = abi.mamba2_layer_prefill_varlen(d, L, FAKE, cu, FAKE, FAKE, FAKE, FAKE, 1 << 34, check=False)
+        assert st == abi.M2_ERR_ARG, cu
+    # the W8A8 arm needs more than 8 token rows (tensor-core projections)
+    st = abi.mamba2_layer_prefill_varlen_w8a8(d, L, FAKE, [0, 3, 8], FAKE, FAKE, FAKE, FAKE, 1 << 34, check=False)
+    assert st == abi.M2_ERR_UNSUPPORTED
+    need = abi.m2_workspace_bytes_varlen(d, 2, 300)
+    st = abi.mamba2_layer_prefill_varlen(d, L, FAKE, [0, 100, 300], FAKE, FAKE, FAKE, FAKE, need // 2, check=False)
+    assert st == abi.M2_ERR_WORKSPACE
+    # the W8A8 product as a unit
+    assert abi.w8a8_gemm(FAKE, FAKE, FAKE, FAKE, 8, 256, 256, FAKE, 1 << 30, check=False) == abi.M2_ERR_UNSUPPORTED
+    assert abi.w8a8_gemm(FAKE, FAKE, FAKE, FAKE, 64, 256, 200, FAKE, 1 << 30, check=False) == abi.M2_ERR_UNSUPPORTED
+    small = abi.m2_w8a8_workspace_bytes(64, 256) - 1
+    assert abi.w8a8_gemm(FAKE, FAKE, FAKE, FAKE, 64, 256, 256, FAKE, small, check=False) == abi.M2_ERR_WORKSPACE
+    assert abi.m2_launch_count() == launches0
