@@ -171,10 +171,11 @@ def _run_conv(xs, w, b, pos0=0, silu=False, ring=None):
     return np.array(outs), ring
 
 
-def test_conv_matches_zero_padded_direct_convolution():
+@pytest.mark.parametrize("dconv", [2, 3, 4, 6])
+def test_conv_matches_zero_padded_direct_convolution(dconv):
     # small integers keep every value exact, so the comparison is exact
-    rng = np.random.default_rng(5)
-    T, Cc, dconv = 11, 7, 4
+    rng = np.random.default_rng(5 + dconv)
+    T, Cc = 11, 7
     x = rng.integers(-8, 9, (T, Cc)).astype(np.float32)
     w = rng.integers(-3, 4, (Cc, dconv)).astype(np.float32)
     b = rng.integers(-4, 5, Cc).astype(np.float32)
@@ -199,10 +200,10 @@ def test_conv_impulse_returns_taps_in_time_reversed_order():
     assert np.all(got[4:] == 0)
 
 
-@pytest.mark.parametrize("pos0", [0, 1, 2, 5, 1000])
-def test_conv_ring_slots_and_positions_counter(pos0):
+@pytest.mark.parametrize("pos0,dconv", [(0, 4), (1, 4), (2, 4), (5, 4), (1000, 4), (3, 2), (7, 3), (11, 6)])
+def test_conv_ring_slots_and_positions_counter(pos0, dconv):
     # x_t = t+1 (exact); a one-hot tap j returns the token d_conv-1-j steps back
-    Cc, dconv, T = 2, 4, 9
+    Cc, T = 2, 9
     x = np.tile(np.arange(1, T + 1, dtype=np.float32)[:, None], (1, Cc))
     for j in range(dconv):
         w = np.zeros((Cc, dconv), np.float32)
@@ -211,9 +212,10 @@ def test_conv_ring_slots_and_positions_counter(pos0):
         lag = dconv - 1 - j
         expect = np.array([t + 1 - lag if t - lag >= 0 else 0 for t in range(T)], np.float64)
         assert np.array_equal(bf(outs)[:, 0], expect)
-        # after T tokens, the ring holds the last 3 tokens at slots (pos0+t) mod 3
-        for t in range(T - 3, T):
-            assert bf(ring)[(pos0 + t) % 3, 0] == t + 1
+        # after T tokens, the ring holds the last d_conv-1 tokens at slots (pos0+t) mod (d_conv-1)
+        L = dconv - 1
+        for t in range(T - L, T):
+            assert bf(ring)[(pos0 + t) % L, 0] == t + 1
 
 
 def test_conv_silu_and_bias():
