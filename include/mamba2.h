@@ -18,9 +18,10 @@
  * (`set_fp8_weights`).
  *
  * Conventions for every entry point below:
- *  - Every data pointer is a DEVICE pointer owned by the caller.  The library
- *    allocates and frees no device memory; scratch comes from the caller's
- *    workspace (`ws`, `ws_bytes`).
+ *  - Every data pointer is a DEVICE pointer owned by the caller (m2_copy also
+ *    takes page-locked host pointers).  The library allocates and frees no
+ *    device memory; scratch comes from the caller's workspace (`ws`,
+ *    `ws_bytes`), or from the built-in scratch of mamba2_layer_decode_noalloc.
  *  - bf16 values are passed as uint16_t bit patterns; E4M3 as uint8_t.
  *    Matrices are row-major with the last index contiguous.
  *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream)
@@ -33,7 +34,10 @@
  *    gives up, the kernel records M2_ERR_TIMEOUT in a device status word that
  *    m2_device_status() returns.
  *  - Calls that share state or workspace must be ordered (same stream, or
- *    synchronised); concurrent calls on distinct buffers are independent.
+ *    synchronised); concurrent calls on distinct buffers are independent,
+ *    except mamba2_layer_decode_noalloc (one built-in scratch per device) and
+ *    the single-launch batch-1 decode selected by m2_set_fused_decode(1) (one
+ *    grid-barrier counter per device).
  */
 #ifndef MAMBA2_GB300_H
 #define MAMBA2_GB300_H
