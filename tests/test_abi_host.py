@@ -161,3 +161,10 @@ def test_varlen_workspace_and_rejections_before_launch(lib):
     small = abi.m2_w8a8_workspace_bytes(64, 256) - 1
     assert abi.w8a8_gemm(FAKE, FAKE, FAKE, FAKE, 64, 256, 256, FAKE, small, check=False) == abi.M2_ERR_WORKSPACE
     assert abi.m2_launch_count() == launches0
+
+
+def test_fused_decode_toggle_is_host_only(lib):
+    # the batch-1 single-launch step is off by default; the setter returns the previous value
+    assert abi.m2_set_fused_decode(True) is False
+    assert abi.m2_set_fused_decode(False) is True
+    assert abi.m2_set_fused_decode(False) is False
