@@ -71,7 +71,7 @@ struct TcLayout {
 struct TcBars {
   uint64_t w_full[kTcWStages], w_empty[kTcWStages];
   uint64_t wbf_full[2];
-  uint64_t a_full[4], a_empty[4];
+  uint64_t a_full[4];
   uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
   uint64_t sc_full[kTcTmemBufs];  // W8A8: the token scales of a k block have landed
   uint32_t tmem_base;
@@ -100,25 +100,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
-}
-
-// The same 2-D load delivered to the same shared-memory offset (and mbarrier)
-// of every CTA in the cluster named by mask.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint "
-      "[%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // K-major operand descriptor, 128-byte swizzle: rows of 128 bytes, 8-row atoms
@@ -152,13 +133,6 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 // Arrives on the mbarrier once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-// The same, arriving on the mbarrier at this offset in every CTA of the mask.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_addr(bar)),
-               "h"(mask)
                : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -261,23 +235,15 @@ struct TcArgs {
   int32_t fp8;
   int32_t ksplit;  // > 1: k blocks split over work items, fp32 partials to `part`
   float* part;     // [ksplit][M][N]
-  int32_t cs;      // cluster size: the cs CTAs of a cluster take cs adjacent weight tiles of the same
-                   // token tile and k range, each loading 1/cs of the activation tile for all of them
 };
 
-// Work item i of a cluster (the same for its cs CTAs): token tile, k range and
-// a group of cs adjacent weight tiles, weight-tile-group major so that the
-// token tiles of one weight tile are adjacent and its bytes are re-read from
-// L2; this CTA takes the tile of its rank (past the last tile: a dummy that
-// repeats the last tile's loads and stores nothing).
-__device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int rank, int& nt, int& mt, int& kb0, int& kb1,
-                                        bool& real) {
+// Work item i: weight tile, token tile and k range, weight-tile major so that
+// the token tiles of one weight tile are adjacent and its bytes are re-read
+// from L2.
+__device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int& nt, int& mt, int& kb0, int& kb1) {
   const int tile = item / ta.ksplit, ks = item % ta.ksplit;
-  const int ntg = tile / ta.m_tiles;
+  nt = tile / ta.m_tiles;
   mt = tile % ta.m_tiles;
-  nt = ntg * ta.cs + rank;
-  real = nt < ta.n_tiles;
-  if (!real) nt = ta.n_tiles - 1;
   kb0 = (int)((long long)ta.kblocks * ks / ta.ksplit);
   kb1 = (int)((long long)ta.kblocks * (ks + 1) / ta.ksplit);
 }
@@ -292,11 +258,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + Lay::kBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ngroups = (ta.n_tiles + ta.cs - 1) / ta.cs;
-  const int nitems = ta.m_tiles * ngroups * ta.ksplit;  // per cluster
-  const int rank = ta.cs > 1 ? (int)cluster_rank() : 0;
-  const int cid = blockIdx.x / ta.cs, ncl = gridDim.x / ta.cs;
-  const uint16_t cmask = (uint16_t)((1u << ta.cs) - 1u);
+  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
+  const int cid = blockIdx.x, ncl = gridDim.x;
   const int L = a.dconv - 1;
 
   if (tid == 0) {
@@ -309,7 +272,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(&bars->a_full[s], 1);
-      mbar_init(&bars->a_empty[s], ta.cs);  // cs > 1: the MMA commits of every CTA of the cluster
     }
     for (int b = 0; b < kTcTmemBufs; ++b) {
       mbar_init(&bars->mma_done[b], 1);
@@ -328,7 +290,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (ta.cs > 1) cluster_sync_all();  // every CTA's barriers exist before any multicast lands
   const uint32_t tmem = bars->tmem_base;
   bool dead = false;
 
@@ -341,8 +302,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        bool real;
-        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
+        tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages;
           if (gk >= kTcWStages) {
@@ -373,16 +333,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        bool real;
-        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
+        tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % SA;
-          if (gk >= SA && !(ta.cs > 1 ? mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)
-                                      : kblock_done(bars, gk - SA)))
-            dead = true;
+          if (gk >= SA && !kblock_done(bars, gk - SA)) dead = true;
           if (dead) break;
           uint8_t* abuf = smem + Lay::kA + s * Lay::kABytes;
-          mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);  // from all cs slices
+          mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);
           if (AQ8) {  // E4M3 codes: one 128-byte-swizzled box of NT rows x 128 k
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
             // the k block's token scales into the slot of its TMEM buffer, once the
@@ -393,23 +350,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive_expect_tx(&bars->sc_full[tb], NT * 4);
             bulk_g2s(smem + Lay::kSc + tb * NT * 4, a.sq + (size_t)kb * a.ldsq + (size_t)mt * NT, NT * 4,
                      &bars->sc_full[tb], pola);
-          } else if (ta.cs == 1) {
+          } else {
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
             tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
-          } else {
-            // rows [rank*NT/cs, (rank+1)*NT/cs) of the tile, to every CTA of the cluster
-            const int rs = NT / ta.cs, r0 = rank * rs;
-            tma_load_2d_mc(abuf + r0 * 128, &tmA, kb * kTcBK, mt * NT + r0, &bars->a_full[s], cmask, pola);
-            tma_load_2d_mc(abuf + NT * 128 + r0 * 128, &tmA, kb * kTcBK + 64, mt * NT + r0, &bars->a_full[s], cmask,
-                           pola);
           }
         }
       }
-      // drain: every CTA of the cluster has finished reading the last stages
-      // (their commits arrive here) before this CTA may exit
-      if (ta.cs > 1)
-        for (int k = max(0, gk - SA); k < gk && !dead; ++k)
-          if (!mbar_wait(&bars->a_empty[k % SA], (k / SA) & 1)) dead = true;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
@@ -419,8 +365,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        bool real;
-        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
+        tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1, sa = gk % SA, tb = gk % kTcTmemBufs;
           if (ta.fp8 && !AQ8) {
@@ -455,7 +400,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // one commit per k block: its completion frees the TMEM partial for the
           // epilogue and the operand slots it read (their producers wait on it)
           tc_commit(&bars->mma_done[tb]);
-          if (ta.cs > 1) tc_commit_mc(&bars->a_empty[sa], cmask);
         }
       }
     }
@@ -466,8 +410,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
-        bool real;
-        tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
+        tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1;
           if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
@@ -520,8 +463,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int gk = 0;
     for (int item = cid; item < nitems && !dead; item += ncl) {
       int nt, mt, kb0, kb1;
-      bool real;
-      tc_item(ta, item, rank, nt, mt, kb0, kb1, real);
+      tc_item(ta, item, nt, mt, kb0, kb1);
       const int ks = item % ta.ksplit;
 #pragma unroll
       for (int j = 0; j < HC; ++j) acc[j] = 0.0f;
@@ -561,7 +503,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (dead) break;
       const int n = nt * kTcBM + row;
-      if (real && n < a.N) {
+      if (n < a.N) {
         if (ta.ksplit > 1) {
           float* pp = ta.part + ((size_t)ks * a.M) * a.N + n;
 #pragma unroll
@@ -682,27 +624,23 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   ta.ksplit = gemm_tc_ksplit(g.M, g.N, g.K);
   ta.part = g.part;
   if (ta.ksplit > 1 && (!g.part || g.part_bytes < gemm_tc_partial_bytes(g.M, g.N, g.K))) ta.ksplit = 1;
-  // one CTA per cluster: sharing the activation tile across a cluster of CTAs
-  // by multicast (ta.cs > 1, supported by the kernel) measured slower here
-  ta.cs = 1;
   if (AQ8) {
-    ta.cs = 1;
     if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.q8, g.K, g.M, (uint64_t)g.ldq, kTcBK, NT,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64,
-                        NT / ta.cs, CU_TENSOR_MAP_SWIZZLE_128B)) {
+                        NT, CU_TENSOR_MAP_SWIZZLE_128B)) {
     return cudaErrorInvalidValue;
   }
   const int smem = tc_smem_bytes<NT, AQ8>();
   auto kern = gemm_tc_kernel<NT, AQ8>;
   cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
   if (e != cudaSuccess) return e;
-  const int nitems = ta.m_tiles * ((ta.n_tiles + ta.cs - 1) / ta.cs) * ta.ksplit;  // per cluster
-  int clusters = num_sms() / ta.cs;
-  if (clusters > nitems) clusters = nitems;
+  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
+  int grid = num_sms();
+  if (grid > nitems) grid = nitems;
   trace_pre(K_GEMM_TC, s);
-  e = launch_kc(kern, dim3(clusters * ta.cs), dim3(kTcThreads), smem, s, g.pdl != 0, ta.cs, tmW, tmA, ta);
+  e = launch_k(kern, dim3(grid), dim3(kTcThreads), smem, s, g.pdl != 0, tmW, tmA, ta);
   trace_post(K_GEMM_TC, s);
   if (e != cudaSuccess || ta.ksplit == 1) return e;
   const size_t total = (size_t)g.M * g.N;

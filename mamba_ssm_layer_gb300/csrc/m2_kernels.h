@@ -166,35 +166,23 @@ cudaError_t launch_gemv(const GemvArgs& a, bool fp8, cudaStream_t s);
 // kernel may start while the previous kernel in the stream is still running;
 // it must execute griddepcontrol.wait before touching that kernel's outputs).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kc(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                      int cluster, Args&&... args) {
+cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   int na = 0;
   if (pdl) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (cluster > 1) {  // thread-block clusters of `cluster` CTAs along x
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = (unsigned)cluster;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
   cfg.attrs = attr;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
-}
-template <typename... KArgs, typename... Args>
-cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                     Args&&... args) {
-  return launch_kc(k, grid, block, smem, s, pdl, 1, std::forward<Args>(args)...);
 }
 
 // ------------------------------------------------------------------ mixer ops
