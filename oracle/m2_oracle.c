@@ -169,10 +169,11 @@ void or_bf16_gemv(const uint16_t* A, int M, const uint16_t* W, int N, int K, dou
   }
 }
 
-/* Sum of |terms| of the same products (the scale of the summation error of
- * any floating-point evaluation of the dot product); used only by tests that
- * check rounding decisions. */
-static void proj_abs(int fmt, const void* w, const uint16_t* s, const uint16_t* a, int N, int K, double* out) {
+/* Sum of |terms| of the same products, sum_k |A[k] * W~[n][k]| (fmt 1: E4M3
+ * with block scales, 2: bf16): the scale of the summation error of any
+ * floating-point evaluation of the dot product.  Used only where tests judge
+ * rounding decisions. */
+void or_proj_abs(int fmt, const void* w, const uint16_t* s, const uint16_t* a, int N, int K, double* out) {
   int kb = (K + 127) / 128;
 #pragma omp parallel for schedule(static)
   for (int n = 0; n < N; ++n) {
@@ -193,7 +194,7 @@ static void proj_abs(int fmt, const void* w, const uint16_t* s, const uint16_t* 
  * *pos is the number of tokens seen so far (not advanced here).  The current
  * token x (bf16, R3) is used as tap d_conv-1 and then stored into slot
  * pos mod (d_conv-1).  Output rounded to bf16 (R4). */
-static void conv1d_update_exact(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
+void or_conv1d_update_exact(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
                                 const uint16_t* b, int C, int dconv, int silu, uint16_t* out, double* exact,
                                 double* exact_abs) {
   int L = dconv - 1;
@@ -219,7 +220,7 @@ static void conv1d_update_exact(uint16_t* ring, const int32_t* pos, const uint16
 
 void or_conv1d_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, const uint16_t* w,
                       const uint16_t* b, int C, int dconv, int silu, uint16_t* out) {
-  conv1d_update_exact(ring, pos, x, w, b, C, dconv, silu, out, NULL, NULL);
+  or_conv1d_update_exact(ring, pos, x, w, b, C, dconv, silu, out, NULL, NULL);
 }
 
 /* ---------------------------------------------------------------- step 5 */
@@ -230,9 +231,21 @@ void or_conv1d_update(uint16_t* ring, const int32_t* pos, const uint16_t* x, con
  *   h[h][p][n] = dA * h[h][p][n] + dt * x[h*P+p] * B[g*N+n]
  *   y[h*P+p]   = sum_n C[g*N+n] * h[h][p][n] + D[h] * x[h*P+p]
  * with g = h / (H/G).  h and y in double; *clamp_hits counts clamp events. */
+static void ssm_step_impl(double* hs, const uint16_t* x, const uint16_t* Bm, const uint16_t* Cm,
+                          const uint16_t* dt_raw, const float* A_log, const float* D, const float* dt_bias,
+                          int H, int P, int N, int G, double* y, double* y_abs, long* clamp_hits);
+
 void or_ssm_step(double* hs, const uint16_t* x, const uint16_t* Bm, const uint16_t* Cm,
                  const uint16_t* dt_raw, const float* A_log, const float* D, const float* dt_bias,
                  int H, int P, int N, int G, double* y, long* clamp_hits) {
+  ssm_step_impl(hs, x, Bm, Cm, dt_raw, A_log, D, dt_bias, H, P, N, G, y, NULL, clamp_hits);
+}
+
+/* The same step; y_abs (if not NULL) receives sum_n |C h| + |D x| per output,
+ * the scale of the evaluation error of y. */
+static void ssm_step_impl(double* hs, const uint16_t* x, const uint16_t* Bm, const uint16_t* Cm,
+                          const uint16_t* dt_raw, const float* A_log, const float* D, const float* dt_bias,
+                          int H, int P, int N, int G, double* y, double* y_abs, long* clamp_hits) {
   int hpg = H / G;
   for (int h = 0; h < H; ++h) {
     int g = h / hpg;
@@ -244,12 +257,14 @@ void or_ssm_step(double* hs, const uint16_t* x, const uint16_t* Bm, const uint16
     for (int p = 0; p < P; ++p) {
       double xv = bf(x[h * P + p]);
       double* hrow = hs + ((size_t)h * P + p) * N;
-      double acc = 0.0;
+      double acc = 0.0, aacc = 0.0;
       for (int n = 0; n < N; ++n) {
         hrow[n] = dA * hrow[n] + dt * xv * bf(Bm[g * N + n]);
         acc += bf(Cm[g * N + n]) * hrow[n];
+        aacc += fabs(bf(Cm[g * N + n]) * hrow[n]);
       }
       y[h * P + p] = acc + (double)D[h] * xv;
+      if (y_abs) y_abs[h * P + p] = aacc + fabs((double)D[h] * xv);
     }
   }
 }
@@ -267,6 +282,22 @@ void or_gated_rmsnorm(const double* y, const uint16_t* z, const uint16_t* w, int
     double r = 1.0 / sqrt(ss / (double)group + eps);
     for (int i = g0; i < g0 + group; ++i)
       out[i] = or_f64_to_bf16(y[i] * r * bf(w[i]) * or_silu(bf(z[i])));
+  }
+}
+
+/* The gated RMSNorm's unrounded outputs (exact[d]) and, from y's own scale
+ * y_abs[d], the scale of their evaluation error: |r * w * silu(z)| * y_abs + |exact|. */
+static void gated_rmsnorm_exact(const double* y, const double* y_abs, const uint16_t* z, const uint16_t* w, int d,
+                                int group, double eps, double* exact, double* scale) {
+  for (int g0 = 0; g0 < d; g0 += group) {
+    double ss = 0.0;
+    for (int i = g0; i < g0 + group; ++i) ss += y[i] * y[i];
+    double r = 1.0 / sqrt(ss / (double)group + eps);
+    for (int i = g0; i < g0 + group; ++i) {
+      double f = r * bf(w[i]) * or_silu(bf(z[i]));
+      exact[i] = y[i] * f;
+      scale[i] = fabs(f) * y_abs[i] + fabs(exact[i]);
+    }
   }
 }
 
@@ -343,6 +374,22 @@ void or_w8a8_gemv(const uint8_t* q, const float* sa, const uint8_t* W, const uin
   }
 }
 
+/* Sum of |terms| of the W8A8 product: sum_b |sa[b] * S[n/128][b]| * sum_{k in b} |E4M3(q[k]) * E4M3(W[n][k])|. */
+void or_w8a8_abs(const uint8_t* q, const float* sa, const uint8_t* W, const uint16_t* S, int N, int K, double* out) {
+  int kb = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; ++n) {
+    double acc = 0.0;
+    for (int b = 0; b < kb; ++b) {
+      int k0 = b * 128, k1 = k0 + 128 < K ? k0 + 128 : K;
+      double part = 0.0;
+      for (int k = k0; k < k1; ++k) part += fabs(e4m3(q[k]) * e4m3(W[(size_t)n * K + k]));
+      acc += fabs((double)sa[b] * bf(S[(size_t)(n / 128) * kb + b])) * part;
+    }
+    out[n] = acc;
+  }
+}
+
 /* ---------------------------------------------------------------- layer */
 
 typedef struct {
@@ -407,12 +454,12 @@ long or_layer_token_traced(const or_layer* L, uint16_t* hidden, double* hs, uint
   proj(L->in_fmt, L->act_fp8, L->in_w, L->in_s, xn, n_in, L->hidden, zx);
   for (int i = 0; i < n_in; ++i) zxb[i] = or_f64_to_bf16(zx[i]);
   if (tr_zx) memcpy(tr_zx, zx, sizeof(double) * n_in);
-  if (tr_zx_abs) proj_abs(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, tr_zx_abs);
+  if (tr_zx_abs) or_proj_abs(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, tr_zx_abs);
   const uint16_t* z = zxb;
   const uint16_t* xbc = zxb + d_inner;
   const uint16_t* dt = zxb + d_inner + d_xbc;
   /* 3. conv1d update on xBC with bias and SiLU (R4) */
-  conv1d_update_exact(ring, pos, xbc, L->conv_w, L->conv_b, d_xbc, L->dconv, 1, u, tr_u, tr_u_abs);
+  or_conv1d_update_exact(ring, pos, xbc, L->conv_w, L->conv_b, d_xbc, L->dconv, 1, u, tr_u, tr_u_abs);
   *pos += 1;
   /* 4. split into x, B, C */
   const uint16_t* xs = u;
@@ -462,4 +509,159 @@ long or_layer_prefill_traced(const or_layer* L, uint16_t* hidden, int T, double*
 /* Vector form of or_f64_to_bf16. */
 void or_f64_to_bf16_array(const double* v, uint16_t* out, long n) {
   for (long i = 0; i < n; ++i) out[i] = or_f64_to_bf16(v[i]);
+}
+
+/* ------------------------------------------------------- rounding decisions */
+
+/* Where a value lies within floating-point evaluation error of a bfloat16
+ * rounding boundary, an fp32 evaluation and this double one may round to the
+ * two neighbouring codes, and both are correct roundings of a correct value.
+ * The functions below let the oracle follow another evaluation's decision at
+ * the rounding points R3..R6 -- but only after checking it: the candidate code
+ * is taken only if the exact value lies within tol * scale of the interval of
+ * reals that round to that code, scale being the point's sum of |terms| (the
+ * size of any evaluation's error).  Every other difference is refused (the
+ * oracle keeps its own code) and counted.  The oracle still computes every
+ * value itself. */
+
+/* The interval [lo, hi] of reals that round (to nearest) to the finite bf16
+ * code c; returns 0 for NaN and infinity codes. */
+int or_bf16_round_interval(uint16_t c, double* lo, double* hi) {
+  uint16_t mag = c & 0x7FFF;
+  if (mag >= 0x7F80) return 0;
+  double v = bf(mag);
+  double below = mag == 0 ? -bf(1) : bf((uint16_t)(mag - 1));
+  double above = mag == 0x7F7F ? ldexp(1.0, 128) : bf((uint16_t)(mag + 1));
+  double a = 0.5 * (below + v), b = 0.5 * (v + above);
+  if (c & 0x8000) {
+    *lo = -b;
+    *hi = -a;
+  } else {
+    *lo = a;
+    *hi = b;
+  }
+  return 1;
+}
+
+/* Distance of `exact` from the rounding interval of code c, over `scale`
+ * (0 inside the interval; infinite for a NaN or infinity code or a zero
+ * scale with a nonzero distance). */
+double or_decision_excess(uint16_t c, double exact, double scale) {
+  double lo, hi;
+  if (!or_bf16_round_interval(c, &lo, &hi)) return INFINITY;
+  double dist = exact < lo ? lo - exact : (exact > hi ? exact - hi : 0.0);
+  if (dist == 0.0) return 0.0;
+  return scale > 0.0 ? dist / scale : INFINITY;
+}
+
+typedef struct {
+  const uint16_t* cand[4]; /* candidate codes at R3 [n_in], R4 [d_xbc], R5 [d_inner], R6 [hidden]; NULL: none */
+  long ld[4];              /* row stride of each candidate array (prefill: next token) */
+  double tol[4];           /* relative tolerance of each point */
+  long taken[4];           /* candidates that differed from the oracle's code and were legitimate */
+  long refused[4];         /* candidates that differed and were not */
+  double worst_taken[4];   /* largest excess among taken candidates */
+  double worst_refused[4]; /* largest excess among refused ones */
+  long first_refused[4];   /* token * row + index of the first refused candidate, -1 if none */
+} or_decisions;
+
+/* One rounding point: codes[i] = the candidate where it is legitimate, else
+ * the oracle's own rounding of exact[i]. */
+static void decide(or_decisions* dec, int pt, long token, const double* exact, const double* scale, int n,
+                   uint16_t* codes) {
+  const uint16_t* cand = dec && dec->cand[pt] ? dec->cand[pt] + token * dec->ld[pt] : NULL;
+  for (int i = 0; i < n; ++i) {
+    uint16_t own = or_f64_to_bf16(exact[i]);
+    codes[i] = own;
+    if (!cand || cand[i] == own) continue;
+    double ex = or_decision_excess(cand[i], exact[i], scale[i] > fabs(exact[i]) ? scale[i] : fabs(exact[i]));
+    if (ex <= dec->tol[pt]) {
+      codes[i] = cand[i];
+      dec->taken[pt]++;
+      if (ex > dec->worst_taken[pt]) dec->worst_taken[pt] = ex;
+    } else {
+      dec->refused[pt]++;
+      if (ex > dec->worst_refused[pt]) dec->worst_refused[pt] = ex;
+      if (dec->first_refused[pt] < 0) dec->first_refused[pt] = token * (long)n + i;
+    }
+  }
+}
+
+/* The layer's token (steps 1..8 as or_layer_token_traced) with the decisions
+ * at R3..R6 judged against `dec`; token is the row index into the candidates. */
+static long layer_token_decided(const or_layer* L, uint16_t* hidden, double* hs, uint16_t* ring, int32_t* pos,
+                                or_decisions* dec, long token) {
+  int d_inner = L->H * L->P;
+  int d_xbc = d_inner + 2 * L->G * L->N;
+  int n_in = d_inner + d_xbc + L->H;
+  int kmax = L->hidden > d_inner ? L->hidden : d_inner;
+  long hits = 0;
+  uint16_t* xn = (uint16_t*)malloc(sizeof(uint16_t) * L->hidden);
+  double* zx = (double*)malloc(sizeof(double) * n_in);
+  double* zxa = (double*)malloc(sizeof(double) * n_in);
+  uint16_t* zxb = (uint16_t*)malloc(sizeof(uint16_t) * n_in);
+  uint16_t* u = (uint16_t*)malloc(sizeof(uint16_t) * d_xbc);
+  double* ue = (double*)malloc(sizeof(double) * d_xbc);
+  double* ua = (double*)malloc(sizeof(double) * d_xbc);
+  double* y = (double*)malloc(sizeof(double) * d_inner);
+  double* ya = (double*)malloc(sizeof(double) * d_inner);
+  double* ge = (double*)malloc(sizeof(double) * d_inner);
+  double* ga = (double*)malloc(sizeof(double) * d_inner);
+  uint16_t* gout = (uint16_t*)malloc(sizeof(uint16_t) * d_inner);
+  double* o = (double*)malloc(sizeof(double) * L->hidden);
+  double* oa = (double*)malloc(sizeof(double) * L->hidden);
+  uint8_t* q = (uint8_t*)malloc((size_t)kmax);
+  float* sa = (float*)malloc(sizeof(float) * (size_t)((kmax + 127) / 128));
+
+  /* 1. RMSNorm (R2) */
+  or_rmsnorm(hidden, L->norm_w, L->hidden, L->eps_in, xn);
+  /* 2. in_proj -> [z, xBC, dt] (R3) */
+  if (L->in_fmt == 1 && L->act_fp8) {
+    or_act_quant(xn, L->hidden, q, sa);
+    or_w8a8_gemv(q, sa, (const uint8_t*)L->in_w, L->in_s, n_in, L->hidden, zx);
+    or_w8a8_abs(q, sa, (const uint8_t*)L->in_w, L->in_s, n_in, L->hidden, zxa);
+  } else {
+    proj(L->in_fmt, 0, L->in_w, L->in_s, xn, n_in, L->hidden, zx);
+    or_proj_abs(L->in_fmt, L->in_w, L->in_s, xn, n_in, L->hidden, zxa);
+  }
+  decide(dec, 0, token, zx, zxa, n_in, zxb);
+  /* 3. conv1d update with bias and SiLU (R4) */
+  or_conv1d_update_exact(ring, pos, zxb + d_inner, L->conv_w, L->conv_b, d_xbc, L->dconv, 1, u, ue, ua);
+  for (int c = 0; c < d_xbc; ++c) ua[c] *= 1.1; /* |silu'| <= 1.1: the pre-activation's error, carried through */
+  decide(dec, 1, token, ue, ua, d_xbc, u);
+  *pos += 1;
+  /* 4, 5. split, SSM step */
+  ssm_step_impl(hs, u, u + d_inner, u + d_inner + L->G * L->N, zxb + d_inner + d_xbc, L->A_log, L->D, L->dt_bias,
+                L->H, L->P, L->N, L->G, y, ya, &hits);
+  /* 6. gated RMSNorm (R5) */
+  gated_rmsnorm_exact(y, ya, zxb, L->gnorm_w, d_inner, L->gnorm_group, L->eps_gated, ge, ga);
+  decide(dec, 2, token, ge, ga, d_inner, gout);
+  /* 7, 8. out_proj and residual (R6) */
+  if (L->out_fmt == 1 && L->act_fp8) {
+    or_act_quant(gout, d_inner, q, sa);
+    or_w8a8_gemv(q, sa, (const uint8_t*)L->out_w, L->out_s, L->hidden, d_inner, o);
+    or_w8a8_abs(q, sa, (const uint8_t*)L->out_w, L->out_s, L->hidden, d_inner, oa);
+  } else {
+    proj(L->out_fmt, 0, L->out_w, L->out_s, gout, L->hidden, d_inner, o);
+    or_proj_abs(L->out_fmt, L->out_w, L->out_s, gout, L->hidden, d_inner, oa);
+  }
+  for (int i = 0; i < L->hidden; ++i) {
+    o[i] += bf(hidden[i]);
+    oa[i] += fabs(bf(hidden[i]));
+  }
+  decide(dec, 3, token, o, oa, L->hidden, hidden);
+
+  free(xn); free(zx); free(zxa); free(zxb); free(u); free(ue); free(ua); free(y); free(ya); free(ge); free(ga);
+  free(gout); free(o); free(oa); free(q); free(sa);
+  return hits;
+}
+
+/* T tokens of one sequence (hidden [T][hidden], in place), each decision
+ * judged against the candidates of its token row. */
+long or_layer_prefill_decided(const or_layer* L, uint16_t* hidden, int T, double* hs, uint16_t* ring, int32_t* pos,
+                              or_decisions* dec) {
+  long hits = 0;
+  for (int t = 0; t < T; ++t)
+    hits += layer_token_decided(L, hidden + (size_t)t * L->hidden, hs, ring, pos, dec, t);
+  return hits;
 }

@@ -67,6 +67,14 @@ def lib():
             l.or_f32_to_e4m3_sat.argtypes = [C.c_float]; l.or_f32_to_e4m3_sat.restype = u8
             l.or_act_quant.argtypes = [P, C.c_int, P, P]
             l.or_w8a8_gemv.argtypes = [P, P, P, P, C.c_int, C.c_int, P]
+            l.or_w8a8_abs.argtypes = [P, P, P, P, C.c_int, C.c_int, P]
+            l.or_proj_abs.argtypes = [C.c_int, P, P, P, C.c_int, C.c_int, P]
+            l.or_conv1d_update_exact.argtypes = [P, P, P, P, P, C.c_int, C.c_int, C.c_int, P, P, P]
+            l.or_bf16_round_interval.argtypes = [u16, C.POINTER(d), C.POINTER(d)]
+            l.or_bf16_round_interval.restype = C.c_int
+            l.or_decision_excess.argtypes = [u16, d, d]; l.or_decision_excess.restype = d
+            l.or_layer_prefill_decided.argtypes = [P, P, C.c_int, P, P, P, C.POINTER(_OrDecisions)]
+            l.or_layer_prefill_decided.restype = C.c_long
             l.or_init()
             _lib = l
     return _lib
@@ -197,6 +205,56 @@ def act_quant(a_bits: np.ndarray):
     return q, s
 
 
+def proj_abs(a: np.ndarray, W: np.ndarray, S=None) -> np.ndarray:
+    """sum_k |a[k] * W~[n][k]| of one bf16 row a against E4M3 W with bf16 block
+    scales S (or bf16 W when S is None)."""
+    a = _c(a, np.uint16)
+    N, K = W.shape
+    out = np.empty(N, np.float64)
+    if S is None:
+        lib().or_proj_abs(2, _p(_c(W, np.uint16)), None, _p(a), N, K, _p(out))
+    else:
+        lib().or_proj_abs(1, _p(_c(W, np.uint8)), _p(_c(S, np.uint16)), _p(a), N, K, _p(out))
+    return out
+
+
+def w8a8_abs(q: np.ndarray, sa: np.ndarray, W: np.ndarray, S: np.ndarray) -> np.ndarray:
+    """The W8A8 product's sum of |terms| for one quantized row."""
+    q = _c(q, np.uint8); sa = _c(sa, np.float32); W = _c(W, np.uint8); S = _c(S, np.uint16)
+    N, K = W.shape
+    out = np.empty(N, np.float64)
+    lib().or_w8a8_abs(_p(q), _p(sa), _p(W), _p(S), N, K, _p(out))
+    return out
+
+
+def conv1d_update_exact(ring: np.ndarray, pos: int, x: np.ndarray, w: np.ndarray, b, silu_on: bool = True):
+    """As conv1d_update, also returning the unrounded outputs and their sums of |terms|."""
+    ring = np.array(ring, np.uint16, copy=True, order="C")
+    L1, Cc = ring.shape
+    dconv = L1 + 1
+    out = np.empty(Cc, np.uint16)
+    ex = np.empty(Cc, np.float64)
+    ab = np.empty(Cc, np.float64)
+    p = np.array([pos], np.int32)
+    bb = None if b is None else _p(_c(b, np.uint16))
+    lib().or_conv1d_update_exact(_p(ring), _p(p), _p(_c(x, np.uint16)), _p(_c(w, np.uint16)), bb, Cc, dconv,
+                                 1 if silu_on else 0, _p(out), _p(ex), _p(ab))
+    return out, ring, ex, ab
+
+
+def bf16_round_interval(code: int):
+    """[lo, hi]: the reals that round to the bf16 code (None for NaN / infinity)."""
+    lo, hi = C.c_double(), C.c_double()
+    if not lib().or_bf16_round_interval(int(code), C.byref(lo), C.byref(hi)):
+        return None
+    return lo.value, hi.value
+
+
+def decision_excess(code: int, exact: float, scale: float) -> float:
+    """Distance of `exact` from the rounding interval of `code`, over `scale`."""
+    return float(lib().or_decision_excess(int(code), float(exact), float(scale)))
+
+
 def w8a8_gemv(q: np.ndarray, sa: np.ndarray, W: np.ndarray, S: np.ndarray) -> np.ndarray:
     """W8A8 product of one quantized row with E4M3 W [N][K] and bf16 block scales S (double)."""
     q = _c(q, np.uint8); sa = _c(sa, np.float32); W = _c(W, np.uint8); S = _c(S, np.uint16)
@@ -207,6 +265,23 @@ def w8a8_gemv(q: np.ndarray, sa: np.ndarray, W: np.ndarray, S: np.ndarray) -> np
 
 
 # ------------------------------------------------------------------ layer
+
+class _OrDecisions(C.Structure):
+    _fields_ = [("cand", C.c_void_p * 4), ("ld", C.c_long * 4), ("tol", C.c_double * 4),
+                ("taken", C.c_long * 4), ("refused", C.c_long * 4), ("worst_taken", C.c_double * 4),
+                ("worst_refused", C.c_double * 4), ("first_refused", C.c_long * 4)]
+
+
+# Rounding points whose decisions the oracle can follow, and the relative
+# tolerance of each (times the point's sum of |terms|):
+#   R3 in_proj output, R4 conv output, R6 layer output: fp32 summation of at
+#   most 16384 terms errs by far less than 2^-20 of their sum of |terms|; a
+#   dropped or wrong term moves a value by about 2^-12 of it or more.
+#   R5 gated-norm output: y comes from the fp32 state, whose own bar is 1e-3;
+#   2^-12 of y's sum of |terms| is four times tighter than that bar.
+POINTS = ("R3", "R4", "R5", "R6")
+DECISION_TOL = {"R3": 2.0 ** -20, "R4": 2.0 ** -20, "R5": 2.0 ** -12, "R6": 2.0 ** -20}
+
 
 class _OrLayer(C.Structure):
     _fields_ = [("hidden", C.c_int), ("H", C.c_int), ("P", C.c_int), ("N", C.c_int), ("G", C.c_int),
@@ -260,6 +335,36 @@ class OracleLayer:
         assert h.dtype == np.float64 and ring.dtype == np.uint16 and pos.dtype == np.int32
         T = hidden.shape[0]
         return lib().or_layer_prefill(C.byref(self._s), _p(hidden), T, _p(h), _p(ring), _p(pos))
+
+    def run_decided(self, hidden, h, ring, pos, cand: dict, tol: dict | None = None) -> dict:
+        """Run T = hidden.shape[0] tokens (in place) following, at each rounding
+        point named in `cand` ("R3": [T][n_in], "R4": [T][d_xbc], "R5":
+        [T][d_inner], "R6": [T][hidden] bf16 codes), every candidate code that
+        is a correct rounding of a value within tol * (sum of |terms|) of the
+        oracle's exact value; any other difference is refused and counted, and
+        the oracle keeps its own code there.  Returns per point the taken and
+        refused counts, the worst excess of each, and the first refused index."""
+        assert hidden.dtype == np.uint16 and hidden.flags["C_CONTIGUOUS"]
+        tol = dict(DECISION_TOL, **(tol or {}))
+        T = hidden.shape[0]
+        dec = _OrDecisions()
+        keep = []
+        for i, pt in enumerate(POINTS):
+            c = cand.get(pt)
+            dec.tol[i] = tol[pt]
+            dec.first_refused[i] = -1
+            if c is None:
+                continue
+            c = np.ascontiguousarray(c, np.uint16).reshape(T, -1)
+            keep.append(c)
+            dec.cand[i] = c.ctypes.data
+            dec.ld[i] = c.shape[1]
+        hits = lib().or_layer_prefill_decided(C.byref(self._s), _p(hidden), T, _p(h), _p(ring), _p(pos),
+                                              C.byref(dec))
+        return {"hits": hits,
+                **{pt: {"taken": dec.taken[i], "refused": dec.refused[i], "worst_taken": dec.worst_taken[i],
+                        "worst_refused": dec.worst_refused[i], "first_refused": dec.first_refused[i]}
+                   for i, pt in enumerate(POINTS) if cand.get(pt) is not None}}
 
     def run_traced(self, hidden, h, ring, pos):
         """As run(), also returning the unrounded in_proj outputs [T][n_in] and conv

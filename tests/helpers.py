@@ -32,127 +32,130 @@ def state_rel_err(got_h, ref_h) -> float:
 
 
 # ---------------------------------------------------------------------------
-# Rounding-decision analysis for multi-step layer runs.
+# Rounding decisions.
 #
-# The layer rounds the in_proj outputs (R3) and the conv outputs (R4) to bf16.
-# The GPU accumulates in fp32, the oracle in double; when an exact value lies
-# within fp32 accumulation error of a bf16 rounding tie, the two sides may pick
-# the two neighbouring bf16 codes -- both are correct roundings.  A flipped dt
-# code moves dt by up to one bf16 ulp of dt_raw (<= 2^-4 relative for
-# |dt_raw| < 16), and the SSM state of that head by up to ~6 %, decaying with
-# prod(dA) afterwards.  The checks below therefore:
-#   1. require every GPU/oracle code difference at R3 to be legitimate: the GPU
-#      code is a correct rounding of a value within 2^-20 * sum|terms| of the
-#      oracle's exact value (fp32 summation of K = 4096 terms errs by far less:
-#      ~1e-9 * sum|terms| observed; a missing or wrong term would move the value
-#      by ~sum|terms|/K = 2^-12 * sum|terms|); every R4 difference must be
-#      legitimate in the same sense or within the propagated effect
-#      sum_j |w_j| |dx_j| of R3 differences inside its conv window;
-#   2. require the 1e-3 state bound for every head whose inputs saw no flip
-#      that is still visible (residual decay weight >= 1e-3), and the derived
-#      7e-2 bound for the (reported) heads that did.
-
-FLIP_REL = 2.0 ** -20
-FLIP_STATE_CAP = 7e-2
+# The layer rounds to bf16 at R3 (in_proj output), R4 (conv output), R5
+# (gated-norm output) and R6 (layer output).  The GPU evaluates in fp32, the
+# oracle in double; where an exact value lies within fp32 evaluation error of a
+# bf16 rounding boundary the two may pick the neighbouring codes -- both are
+# correct roundings.  Left alone, one flipped dt code moves dt by up to 2^-4
+# relative and its head's state by several percent.  So the oracle follows the
+# GPU's decisions (OracleLayer.run_decided): at each point it takes the GPU's
+# code only where that code is a correct rounding of a value within the
+# point's tolerance (times its sum of |terms|) of the oracle's own exact value,
+# refuses every other difference, and still computes every value itself.  A
+# test then requires zero refusals, the fp32 state within 1e-3 on every head,
+# and bit-equal rings and positions.
+#
+# The GPU's codes are read back from the call's workspace: R3 and R4 always;
+# R5 where the gated norm writes bf16 rows (tensor-core projections: decode of
+# more than 8 rows, prefill of more than 8 tokens on the w8a16 arm); R6 (the
+# output rows) together with R5 only, since R6's exact value depends on every
+# R5 code.
 
 
-def _bf16_ord(c):
-    c = np.asarray(c).astype(np.int64)
-    return np.where(c & 0x8000, -(c & 0x7FFF), c)
+def _rup(v, a):
+    return (v + a - 1) // a * a
 
 
-def legit_flips(gpu_codes, exact, oracle_codes, abssum=None):
-    """Indices where the codes differ, and whether each is legitimate: the GPU
-    code must be the correct rounding of some value within FLIP_REL * sum|terms|
-    of the exact value (its rounding interval meets that error interval).
-    Under cancellation (|exact| << sum|terms|) that can be several ulps."""
-    idx = np.nonzero(np.asarray(gpu_codes) != np.asarray(oracle_codes))[0]
-    if idx.size == 0:
-        return idx, np.ones(0, bool)
-    g, e = np.asarray(gpu_codes)[idx], np.asarray(exact)[idx]
-    scale = np.abs(e) if abssum is None else np.maximum(np.asarray(abssum)[idx], np.abs(e))
-    gv = bf16_to_f64(g)
-    half_ulp = 0.5 * np.spacing(np.abs(gv).astype(np.float32)).astype(np.float64) * 65536.0
-    ok = np.abs(gv - e) <= half_ulp + FLIP_REL * scale
-    return idx, ok
+def _dd(d):
+    di = d["nheads"] * d["head_dim"]
+    dx = di + 2 * d["n_groups"] * d["d_state"]
+    return di, dx, di + dx + d["nheads"]
 
 
-class FlipTracker:
-    """Follows one sequence through decode / prefill tokens (see above)."""
+def _u16(ws, off, rows, cols, sel=None):
+    import torch
+    t = ws[off: off + rows * cols * 2].view(torch.int16).view(rows, cols)
+    if sel is not None:
+        t = t[sel]
+    return t.cpu().numpy().view(np.uint16)
 
-    def __init__(self, dims, A_log, dt_bias, conv_w):
-        self.H, self.P, self.N, self.G = dims["nheads"], dims["head_dim"], dims["d_state"], dims["n_groups"]
-        self.L = dims["d_conv"] - 1
-        self.d_inner = self.H * self.P
-        self.d_xbc = self.d_inner + 2 * self.G * self.N
-        self.A = np.exp(np.asarray(A_log, np.float64))
-        self.dt_bias = np.asarray(dt_bias, np.float64)
-        self.absw = np.abs(bf16_to_f64(conv_w)).reshape(self.d_xbc, self.L + 1)
-        self.dx_hist = [np.zeros(self.d_xbc) for _ in range(self.L)]  # |R3 xBC differences| of past tokens
-        self.taint_weight = np.zeros(self.H)  # residual weight of past taints per head
-        self.n_r3 = 0
-        self.n_r4 = 0
-        self.bad = []
 
-    def token(self, g3, e3, g4, e4):
-        """g3: GPU R3 codes [n_in] (z | raw xBC | dt); e3: oracle (exact values,
-        sums of |terms|); g4: GPU R4 codes [d_xbc]; e4: oracle (exact conv
-        outputs, sums of |terms|)."""
-        from oracle import oracle as orc
-        di, dx, H, P, N, G = self.d_inner, self.d_xbc, self.H, self.P, self.N, self.G
-        e3, a3 = e3
-        e4, a4 = e4
-        o3 = orc.f64_array_to_bf16(e3)
-        idx3, ok3 = legit_flips(g3, e3, o3, a3)
-        self.n_r3 += idx3.size
-        self.bad += [("R3", int(i), int(g3[i]), int(o3[i]), float(e3[i]), float(a3[i])) for i in idx3[~ok3]]
-        # the conv consumes the xBC codes of this and the previous L tokens;
-        # a difference there propagates as sum_j |w_j| * |dx_j| (SiLU' <= 1.1)
-        dxc = np.abs(bf16_to_f64(g3[di:di + dx]) - bf16_to_f64(o3[di:di + dx]))
-        window = np.stack(self.dx_hist + [dxc], axis=1)           # [d_xbc][L+1], oldest first
-        prop = 1.1 * np.sum(self.absw * window, axis=1)
-        self.dx_hist = (self.dx_hist + [dxc])[-self.L:]
-        o4 = orc.f64_array_to_bf16(e4)
-        idx4, ok4 = legit_flips(g4, e4, o4, a4)
-        self.n_r4 += idx4.size
-        for i, ok in zip(idx4, ok4):
-            if ok:
+def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None):
+    """Per batch row (or for the rows in `only`, others None), the GPU's codes
+    of the last decode step: R3 (z, raw xBC from the ring slot just written,
+    dt) and R4; R5 and R6 for B > 8."""
+    di, dx, n_in = _dd(d)
+    ldz = _rup(n_in, 8)
+    L = d["d_conv"] - 1
+    sel = list(range(B)) if only is None else list(only)
+    o_zxu = _rup(B * d["hidden"] * 2, 256)
+    zxu_s = _u16(ws, o_zxu, B, ldz, sel)
+    o_y = o_zxu + _rup(B * ldz * 2, 256)
+    o_g = o_y + _rup(B * di * 4, 256)
+    g_s = _u16(ws, o_g, B, di, sel) if B > 8 else None
+    zxu = {b: zxu_s[i] for i, b in enumerate(sel)}
+    g = None if g_s is None else {b: g_s[i] for i, b in enumerate(sel)}
+    out = []
+    for b in range(B):
+        if b not in zxu:
+            out.append(None)
+            continue
+        r3 = np.empty(n_in, np.uint16)
+        r3[:di] = zxu[b][:di]
+        r3[di:di + dx] = ring_after[b][pos_before[b] % L]
+        r3[di + dx:] = zxu[b][di + dx:n_in]
+        c = {"R3": r3[None], "R4": zxu[b][None, di:di + dx].copy()}
+        if g is not None:
+            c["R5"] = g[b][None].copy()
+            c["R6"] = np.asarray(hidden_out[b:b + 1], np.uint16).copy()
+        out.append(c)
+    return out
+
+
+def prefill_candidates(ws, T, d, hidden_out, r5_available, a=0, b=None):
+    """The GPU's codes of token rows a..b-1 of a (varlen) prefill of T rows:
+    R3, R4, and R5 and R6 when the gated norm wrote bf16 rows (hidden_out:
+    those rows' outputs)."""
+    di, dx, n_in = _dd(d)
+    b = T if b is None else b
+    ldz = _rup(n_in, 8)
+    o_zx = _rup(T * d["hidden"] * 2, 256)
+    zx = _u16(ws, o_zx, T, ldz, slice(a, b))
+    o_u = o_zx + _rup(T * ldz * 2, 256)
+    u = _u16(ws, o_u, T, dx, slice(a, b))
+    c = {"R3": zx[:, :n_in].copy(), "R4": u.copy()}
+    if r5_available:
+        o_y = o_u + _rup(T * dx * 2, 256)
+        o_g = o_y + _rup(T * di * 4, 256)
+        c["R5"] = _u16(ws, o_g, T, di, slice(a, b)).copy()
+        c["R6"] = np.asarray(hidden_out, np.uint16).copy()
+    return c
+
+
+def rows(cand: dict, a: int, b: int) -> dict:
+    """Rows a..b-1 of every candidate array."""
+    return {k: v[a:b] for k, v in cand.items()}
+
+
+class DecisionLog:
+    """Sums the oracle's decision reports over tokens and sequences."""
+
+    def __init__(self):
+        self.taken = {}
+        self.refused = {}
+        self.worst = {}
+        self.first = {}
+
+    def add(self, rep: dict, where=None):
+        for pt, r in rep.items():
+            if pt == "hits":
+                assert r == 0, f"dt clamp hit in the oracle at {where}"
                 continue
-            gv = bf16_to_f64(g4[i:i + 1])[0]
-            half_ulp = 0.5 * float(np.spacing(np.float32(abs(gv)))) * 65536.0
-            if abs(gv - e4[i]) > half_ulp + FLIP_REL * max(a4[i], abs(e4[i])) + prop[i]:
-                self.bad.append(("R4", int(i), int(g4[i]), int(o4[i]), float(e4[i]), float(prop[i])))
-        # heads whose state inputs differ this token
-        u_diff = set(int(i) for i in idx4)
-        r3_diff = set(int(i) for i in idx3)
-        tainted = np.zeros(H, bool)
-        for hh in range(H):
-            g = hh // (H // G)
-            if (di + dx + hh) in r3_diff:
-                tainted[hh] = True
-                continue
-            lo = hh * P
-            if any(lo <= i < lo + P for i in u_diff):
-                tainted[hh] = True
-                continue
-            b0, c0 = di + g * N, di + G * N + g * N
-            if any(b0 <= i < b0 + N or c0 <= i < c0 + N for i in u_diff):
-                tainted[hh] = True
-        # decay this token (oracle dt), then add new taints at full weight
-        dt_raw = bf16_to_f64(o3[di + dx: di + dx + H])
-        dt = np.logaddexp(0.0, dt_raw + self.dt_bias)
-        self.taint_weight = self.taint_weight * np.exp(-dt * self.A)
-        self.taint_weight[tainted] = 1.0
+            self.taken[pt] = self.taken.get(pt, 0) + r["taken"]
+            self.refused[pt] = self.refused.get(pt, 0) + r["refused"]
+            self.worst[pt] = max(self.worst.get(pt, 0.0), r["worst_taken"])
+            if r["refused"] and pt not in self.first:
+                self.first[pt] = (where, r["first_refused"], r["worst_refused"])
 
-    def check_state(self, gpu_h, oracle_h, tol=TOL_STATE):
-        """Per-head floored relative error with the rules above; returns a report dict."""
-        assert not self.bad, f"illegitimate rounding differences: {self.bad[:10]}"
-        g = np.asarray(gpu_h, np.float64).reshape(self.H, self.P, self.N)
-        o = np.asarray(oracle_h, np.float64).reshape(self.H, self.P, self.N)
-        errs = np.array([floored_rel_err(g[h], o[h]) for h in range(self.H)])
-        visible = self.taint_weight >= 1e-3
-        strict = errs[~visible]
-        assert strict.size == 0 or strict.max() <= tol, f"state err {strict.max()} > {tol} on an untainted head"
-        assert errs.max() <= FLIP_STATE_CAP, f"state err {errs.max()} above the flip bound"
-        return {"r3_flips": self.n_r3, "r4_diffs": self.n_r4, "heads_exempt": int(visible.sum()),
-                "max_err_strict": float(strict.max()) if strict.size else 0.0, "max_err": float(errs.max())}
+    def check(self):
+        assert not any(self.refused.values()), f"GPU codes that are not correct roundings: {self.refused} {self.first}"
+        return {"taken": dict(self.taken), "worst_excess": {k: float(v) for k, v in self.worst.items()}}
+
+
+def check_state_all_heads(gpu_h, oracle_h, tol=TOL_STATE):
+    """Floored relative error of every (sequence, head) slice of the state; all held to tol."""
+    e = state_rel_err(gpu_h, oracle_h)
+    assert e <= tol, f"state error {e} > {tol}"
+    return e
