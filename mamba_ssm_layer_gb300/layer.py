@@ -12,6 +12,30 @@ import torch
 from . import abi
 
 
+# Optional device allocator: a callable (nbytes, device) -> uint8 tensor of at
+# least nbytes, 256-byte aligned.  None: torch's allocator.  Tests install one
+# that surrounds every buffer with guard bands.
+_ALLOC = None
+
+
+def set_allocator(fn):
+    """Route this module's device buffers through fn (None restores torch's); returns the previous one."""
+    global _ALLOC
+    prev, _ALLOC = _ALLOC, fn
+    return prev
+
+
+def _empty(shape, dtype, device) -> torch.Tensor:
+    if _ALLOC is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+    return _ALLOC(max(n, 1), device)[:n].view(dtype).view(shape)
+
+
+def _zeros(shape, dtype, device) -> torch.Tensor:
+    return _empty(shape, dtype, device).zero_()
+
+
 def to_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
     """Upload a numpy array (uint16 bf16 bits stay int16-typed bit patterns)."""
     a = np.ascontiguousarray(a)
@@ -21,7 +45,11 @@ def to_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
         t = torch.from_numpy(a)
     else:
         t = torch.from_numpy(a)
-    return t.to(device)
+    if _ALLOC is None:
+        return t.to(device)
+    out = _empty(tuple(t.shape), t.dtype, device)
+    out.copy_(t)
+    return out
 
 
 def bits_u16(t: torch.Tensor) -> np.ndarray:
@@ -55,14 +83,14 @@ class DeviceLayer:
 
     def new_state(self, B: int, device="cuda"):
         d = self.dims_dict
-        h = torch.zeros((B, d["nheads"], d["head_dim"], d["d_state"]), dtype=torch.float32, device=device)
-        ring = torch.zeros((B, d["d_conv"] - 1, self.d_xbc), dtype=torch.int16, device=device)
-        pos = torch.zeros(B, dtype=torch.int32, device=device)
+        h = _zeros((B, d["nheads"], d["head_dim"], d["d_state"]), torch.float32, device)
+        ring = _zeros((B, d["d_conv"] - 1, self.d_xbc), torch.int16, device)
+        pos = _zeros((B,), torch.int32, device)
         return h, ring, pos
 
     def workspace(self, max_batch: int, max_tokens: int, device="cuda") -> torch.Tensor:
         n = abi.m2_workspace_bytes(self.dims, max_batch, max_tokens)
-        return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        return _empty((max(n, 256),), torch.uint8, device)
 
     def decode(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None) -> None:
         h, ring, pos = state
@@ -72,7 +100,7 @@ class DeviceLayer:
 
     def workspace_varlen(self, max_seqs: int, max_total_tokens: int, device="cuda") -> torch.Tensor:
         n = abi.m2_workspace_bytes_varlen(self.dims, max_seqs, max_total_tokens)
-        return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        return _empty((max(n, 256),), torch.uint8, device)
 
     def prefill_varlen(self, hidden: torch.Tensor, cu_seqlens, state, ws: torch.Tensor, stream=None,
                        w8a8: bool = False) -> None:

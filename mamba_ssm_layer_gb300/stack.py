@@ -10,7 +10,7 @@ from __future__ import annotations
 import torch
 
 from . import abi
-from .layer import DeviceLayer
+from .layer import DeviceLayer, _empty
 
 
 class DeviceStack:
@@ -27,7 +27,7 @@ class DeviceStack:
         max_tokens, and varlen prefill of max_seqs sequences with max_tokens rows."""
         n = max(max(abi.m2_workspace_bytes(dl.dims, max_batch, max_tokens),
                     abi.m2_workspace_bytes_varlen(dl.dims, max_seqs, max_tokens)) for dl in self.layers)
-        return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        return _empty((max(n, 256),), torch.uint8, self.device)
 
     def prefill(self, hidden: torch.Tensor, states, seq: int, ws: torch.Tensor, stream=None) -> None:
         """hidden [T, hidden] bf16 bits of sequence `seq`, transformed in place by every layer."""

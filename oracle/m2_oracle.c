@@ -563,6 +563,15 @@ typedef struct {
   double worst_taken[4];   /* largest excess among taken candidates */
   double worst_refused[4]; /* largest excess among refused ones */
   long first_refused[4];   /* token * row + index of the first refused candidate, -1 if none */
+  /* W8A8 arm: the out_proj's E4M3 input codes [d_inner] and block scales
+   * [d_inner/128] ("Q5"), rows q5_ld / q5_lds apart; judged per 128-block */
+  const uint8_t* q5_codes;
+  const float* q5_scales;
+  long q5_ld, q5_lds;
+  long q5_taken, q5_refused, q5_first_refused;
+  uint16_t* r5_trace; /* if not NULL: the decided R5 codes of each token [T][d_inner] */
+  double* q5_diag;    /* if not NULL: the first refused Q5 block, [4][128] + 2: exact R5 values,
+                         their scales, own codes, candidate codes, candidate scale, own scale */
 } or_decisions;
 
 /* One rounding point: codes[i] = the candidate where it is legitimate, else
@@ -585,6 +594,67 @@ static void decide(or_decisions* dec, int pt, long token, const double* exact, c
       if (dec->first_refused[pt] < 0) dec->first_refused[pt] = token * (long)n + i;
     }
   }
+}
+
+/* bf16 codes as ordered integers (value order) and back; finite codes only. */
+static int code_ord(uint16_t c) { return (c & 0x8000) ? -(int)(c & 0x7FFF) : (int)(c & 0x7FFF); }
+static uint16_t ord_code(int o) { return o < 0 ? (uint16_t)(0x8000 | (-o)) : (uint16_t)o; }
+/* E4M3 codes as ordered integers. */
+static int e4m3_ord(uint8_t q) { return (q & 0x80) ? -(int)(q & 0x7F) : (int)(q & 0x7F); }
+
+/* The range [*lo, *hi] (ordered bf16 codes) of the codes decide() would take
+ * for an exact value with this scale: the own code c and every code next to
+ * the range whose excess is <= tol. */
+static void legit_code_range(uint16_t c, double exact, double scale, double tol, int* lo, int* hi) {
+  double sc = scale > fabs(exact) ? scale : fabs(exact);
+  int o = code_ord(c), l = o, h = o;
+  for (int it = 0; it < 65536 && l - 1 >= -0x7F7F && or_decision_excess(ord_code(l - 1), exact, sc) <= tol; ++it) --l;
+  for (int it = 0; it < 65536 && h + 1 <= 0x7F7F && or_decision_excess(ord_code(h + 1), exact, sc) <= tol; ++it) ++h;
+  *lo = l;
+  *hi = h;
+}
+
+/* Whether an E4M3 block (codes gq[n], scale gs) is what the W8A8 activation
+ * quantization makes of some choice of bf16 inputs, each element a code that
+ * decide() would take at R5 (the oracle's own code c[i], or any code whose
+ * excess is <= tol: a contiguous range of codes).  The quantization is the
+ * oracle's own (or_act_quant): amax over the block, scale amax / 448 and codes
+ * E4M3(v * (448 / amax)) in fp32, which is monotonic in v; so for a given amax
+ * each element reaches a contiguous range of E4M3 codes. */
+static int q5_block_legit(const double* exact, const double* scale, const uint16_t* c, int n, const uint8_t* gq,
+                          float gs, double tol) {
+  int lo[128], hi[128];
+  for (int i = 0; i < n; ++i) legit_code_range(c[i], exact[i], scale[i], tol, &lo[i], &hi[i]);
+  if (gs == 0.0f) {  /* an all-zero block: every element must be able to be zero */
+    for (int i = 0; i < n; ++i)
+      if (lo[i] > 0 || hi[i] < 0 || gq[i] != 0) return 0;
+    return 1;
+  }
+  /* amax candidates: the bf16 magnitudes m with m / 448 == gs in fp32 */
+  uint16_t m0 = or_f64_to_bf16((double)gs * 448.0);
+  for (int dm = -3; dm <= 3; ++dm) {
+    int om = code_ord(m0) + dm;
+    if (om <= 0 || om > 0x7F7F) continue;
+    float m = (float)bf(ord_code(om));
+    if (m / 448.0f != gs) continue;
+    volatile float inv = 448.0f / m;
+    int ok = 1, attained = 0;
+    for (int i = 0; i < n && ok; ++i) {
+      /* the element's values within [-m, m] */
+      int l = lo[i] > -om ? lo[i] : -om, h = hi[i] < om ? hi[i] : om;
+      if (l > h) {
+        ok = 0;
+        break;
+      }
+      volatile float vl = (float)bf(ord_code(l)) * inv, vh = (float)bf(ord_code(h)) * inv;
+      int ql = e4m3_ord(or_f32_to_e4m3_sat(vl)), qh = e4m3_ord(or_f32_to_e4m3_sat(vh)), g = e4m3_ord(gq[i]);
+      if (g < ql || g > qh) ok = 0;
+      /* an element that can be +-m and whose code is the one +-m gives */
+      if ((h == om && g == qh) || (l == -om && g == ql)) attained = 1;
+    }
+    if (ok && attained) return 1;
+  }
+  return 0;
 }
 
 /* The layer's token (steps 1..8 as or_layer_token_traced) with the decisions
@@ -636,9 +706,40 @@ static long layer_token_decided(const or_layer* L, uint16_t* hidden, double* hs,
   /* 6. gated RMSNorm (R5) */
   gated_rmsnorm_exact(y, ya, zxb, L->gnorm_w, d_inner, L->gnorm_group, L->eps_gated, ge, ga);
   decide(dec, 2, token, ge, ga, d_inner, gout);
+  if (dec && dec->r5_trace) memcpy(dec->r5_trace + token * (long)d_inner, gout, sizeof(uint16_t) * d_inner);
   /* 7, 8. out_proj and residual (R6) */
   if (L->out_fmt == 1 && L->act_fp8) {
     or_act_quant(gout, d_inner, q, sa);
+    if (dec && dec->q5_codes) {
+      /* the quantized input, block by block, as the candidate has it where
+       * that is what legitimate R5 decisions would give */
+      const uint8_t* gq = dec->q5_codes + token * dec->q5_ld;
+      const float* gs = dec->q5_scales + token * dec->q5_lds;
+      for (int b = 0; b * 128 < d_inner; ++b) {
+        int k0 = b * 128, n = d_inner - k0 < 128 ? d_inner - k0 : 128;
+        if (!memcmp(gq + k0, q + k0, (size_t)n) && gs[b] == sa[b]) continue;
+        if (q5_block_legit(ge + k0, ga + k0, gout + k0, n, gq + k0, gs[b], dec->tol[2])) {
+          memcpy(q + k0, gq + k0, (size_t)n);
+          sa[b] = gs[b];
+          dec->q5_taken++;
+        } else {
+          dec->q5_refused++;
+          if (dec->q5_first_refused < 0) {
+            dec->q5_first_refused = token * (long)d_inner + k0;
+            if (dec->q5_diag) {
+              for (int i = 0; i < n; ++i) {
+                dec->q5_diag[i] = ge[k0 + i];
+                dec->q5_diag[128 + i] = ga[k0 + i];
+                dec->q5_diag[256 + i] = gout[k0 + i];
+                dec->q5_diag[384 + i] = gq[k0 + i];
+              }
+              dec->q5_diag[512] = gs[b];
+              dec->q5_diag[513] = sa[b];
+            }
+          }
+        }
+      }
+    }
     or_w8a8_gemv(q, sa, (const uint8_t*)L->out_w, L->out_s, L->hidden, d_inner, o);
     or_w8a8_abs(q, sa, (const uint8_t*)L->out_w, L->out_s, L->hidden, d_inner, oa);
   } else {

@@ -269,7 +269,10 @@ def w8a8_gemv(q: np.ndarray, sa: np.ndarray, W: np.ndarray, S: np.ndarray) -> np
 class _OrDecisions(C.Structure):
     _fields_ = [("cand", C.c_void_p * 4), ("ld", C.c_long * 4), ("tol", C.c_double * 4),
                 ("taken", C.c_long * 4), ("refused", C.c_long * 4), ("worst_taken", C.c_double * 4),
-                ("worst_refused", C.c_double * 4), ("first_refused", C.c_long * 4)]
+                ("worst_refused", C.c_double * 4), ("first_refused", C.c_long * 4),
+                ("q5_codes", C.c_void_p), ("q5_scales", C.c_void_p), ("q5_ld", C.c_long), ("q5_lds", C.c_long),
+                ("q5_taken", C.c_long), ("q5_refused", C.c_long), ("q5_first_refused", C.c_long),
+                ("r5_trace", C.c_void_p), ("q5_diag", C.c_void_p)]
 
 
 # Rounding points whose decisions the oracle can follow, and the relative
@@ -336,14 +339,18 @@ class OracleLayer:
         T = hidden.shape[0]
         return lib().or_layer_prefill(C.byref(self._s), _p(hidden), T, _p(h), _p(ring), _p(pos))
 
-    def run_decided(self, hidden, h, ring, pos, cand: dict, tol: dict | None = None) -> dict:
+    def run_decided(self, hidden, h, ring, pos, cand: dict, tol: dict | None = None, r5_trace=None) -> dict:
         """Run T = hidden.shape[0] tokens (in place) following, at each rounding
         point named in `cand` ("R3": [T][n_in], "R4": [T][d_xbc], "R5":
         [T][d_inner], "R6": [T][hidden] bf16 codes), every candidate code that
         is a correct rounding of a value within tol * (sum of |terms|) of the
         oracle's exact value; any other difference is refused and counted, and
-        the oracle keeps its own code there.  Returns per point the taken and
-        refused counts, the worst excess of each, and the first refused index."""
+        the oracle keeps its own code there.  "Q5" (W8A8 arm): a pair (E4M3
+        codes [T][d_inner], fp32 block scales [T][d_inner/128]) of the
+        out_proj's quantized input, taken per 128-block where it is what the
+        quantization makes of legitimate R5 decisions.  Returns per point the
+        taken and refused counts, the worst excess of each, and the first
+        refused index."""
         assert hidden.dtype == np.uint16 and hidden.flags["C_CONTIGUOUS"]
         tol = dict(DECISION_TOL, **(tol or {}))
         T = hidden.shape[0]
@@ -359,9 +366,24 @@ class OracleLayer:
             keep.append(c)
             dec.cand[i] = c.ctypes.data
             dec.ld[i] = c.shape[1]
+        dec.q5_first_refused = -1
+        diag = np.zeros(514, np.float64)
+        dec.q5_diag = diag.ctypes.data
+        if r5_trace is not None:
+            assert r5_trace.dtype == np.uint16 and r5_trace.flags["C_CONTIGUOUS"] and r5_trace.shape[0] == T
+            dec.r5_trace = r5_trace.ctypes.data
+        if cand.get("Q5") is not None:
+            qc = np.ascontiguousarray(cand["Q5"][0], np.uint8).reshape(T, -1)
+            qs = np.ascontiguousarray(cand["Q5"][1], np.float32).reshape(T, -1)
+            keep += [qc, qs]
+            dec.q5_codes, dec.q5_scales = qc.ctypes.data, qs.ctypes.data
+            dec.q5_ld, dec.q5_lds = qc.shape[1], qs.shape[1]
         hits = lib().or_layer_prefill_decided(C.byref(self._s), _p(hidden), T, _p(h), _p(ring), _p(pos),
                                               C.byref(dec))
-        return {"hits": hits,
+        q5 = {"Q5": {"taken": dec.q5_taken, "refused": dec.q5_refused, "worst_taken": 0.0, "worst_refused": 0.0,
+                     "first_refused": dec.q5_first_refused,
+                     "diag": diag if dec.q5_refused else None}} if cand.get("Q5") is not None else {}
+        return {"hits": hits, **q5,
                 **{pt: {"taken": dec.taken[i], "refused": dec.refused[i], "worst_taken": dec.worst_taken[i],
                         "worst_refused": dec.worst_refused[i], "first_refused": dec.first_refused[i]}
                    for i, pt in enumerate(POINTS) if cand.get(pt) is not None}}

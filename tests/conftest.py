@@ -26,3 +26,28 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _guard_bands(request):
+    """GPU tests: guard bands around the layer helpers' device buffers, checked after the test."""
+    if "gpu" not in request.keywords:
+        yield
+        return
+    try:
+        import torch
+        if not torch.cuda.is_available():
+            yield
+            return
+    except Exception:  # pragma: no cover
+        yield
+        return
+    from mamba_ssm_layer_gb300 import layer
+    from tests.helpers import GuardBands
+    g = GuardBands()
+    prev = layer.set_allocator(g.alloc)
+    try:
+        yield
+    finally:
+        layer.set_allocator(prev)
+    g.check()

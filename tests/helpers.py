@@ -72,19 +72,25 @@ def _u16(ws, off, rows, cols, sel=None):
     return t.cpu().numpy().view(np.uint16)
 
 
+def _u8(ws, off, rows, cols, sel=None):
+    t = ws[off: off + rows * cols].view(rows, cols)
+    if sel is not None:
+        t = t[sel]
+    return t.cpu().numpy()
+
+
 def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None):
     """Per batch row (or for the rows in `only`, others None), the GPU's codes
     of the last decode step: R3 (z, raw xBC from the ring slot just written,
     dt) and R4; R5 and R6 for B > 8."""
+    from mamba_ssm_layer_gb300 import abi
     di, dx, n_in = _dd(d)
     ldz = _rup(n_in, 8)
     L = d["d_conv"] - 1
     sel = list(range(B)) if only is None else list(only)
-    o_zxu = _rup(B * d["hidden"] * 2, 256)
-    zxu_s = _u16(ws, o_zxu, B, ldz, sel)
-    o_y = o_zxu + _rup(B * ldz * 2, 256)
-    o_g = o_y + _rup(B * di * 4, 256)
-    g_s = _u16(ws, o_g, B, di, sel) if B > 8 else None
+    wm = abi.m2_workspace_map(abi.dims_struct(d), abi.M2_WS_KIND_DECODE, B)
+    zxu_s = _u16(ws, wm["zx"], B, ldz, sel)
+    g_s = _u16(ws, wm["g"], B, di, sel) if B > 8 else None
     zxu = {b: zxu_s[i] for i, b in enumerate(sel)}
     g = None if g_s is None else {b: g_s[i] for i, b in enumerate(sel)}
     out = []
@@ -104,29 +110,39 @@ def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None):
     return out
 
 
-def prefill_candidates(ws, T, d, hidden_out, r5_available, a=0, b=None):
-    """The GPU's codes of token rows a..b-1 of a (varlen) prefill of T rows:
-    R3, R4, and R5 and R6 when the gated norm wrote bf16 rows (hidden_out:
-    those rows' outputs)."""
+def prefill_candidates(ws, cu, d, hidden_out, r5_available, a=0, b=None, w8a8=False):
+    """The GPU's codes of token rows a..b-1 of a (varlen) prefill over the
+    sequences of cu: R3, R4, and R5 and R6 when the gated norm wrote bf16 rows
+    (hidden_out: those rows' outputs).  W8A8 arm: the out_proj's E4M3 input
+    codes and block scales ("Q5") and R6."""
+    from mamba_ssm_layer_gb300 import abi
     di, dx, n_in = _dd(d)
+    cu = [int(v) for v in cu]
+    T = cu[-1]
     b = T if b is None else b
+    kind = abi.M2_WS_KIND_PREFILL_W8A8 if w8a8 else abi.M2_WS_KIND_PREFILL
+    wm = abi.m2_workspace_map(abi.dims_struct(d), kind, len(cu) - 1, cu)
     ldz = _rup(n_in, 8)
-    o_zx = _rup(T * d["hidden"] * 2, 256)
-    zx = _u16(ws, o_zx, T, ldz, slice(a, b))
-    o_u = o_zx + _rup(T * ldz * 2, 256)
-    u = _u16(ws, o_u, T, dx, slice(a, b))
+    zx = _u16(ws, wm["zx"], T, ldz, slice(a, b))
+    u = _u16(ws, wm["u"], T, dx, slice(a, b))
     c = {"R3": zx[:, :n_in].copy(), "R4": u.copy()}
     if r5_available:
-        o_y = o_u + _rup(T * dx * 2, 256)
-        o_g = o_y + _rup(T * di * 4, 256)
-        c["R5"] = _u16(ws, o_g, T, di, slice(a, b)).copy()
+        c["R5"] = _u16(ws, wm["g"], T, di, slice(a, b)).copy()
+        c["R6"] = np.asarray(hidden_out, np.uint16).copy()
+    elif w8a8:
+        import torch
+        ldq = _rup(max(d["hidden"], di), 16)
+        ldsq = _rup(T, 128)
+        q = _u8(ws, wm["q8"], T, ldq, slice(a, b))[:, :di]
+        sq = ws[wm["sq"]: wm["sq"] + (di // 128) * ldsq * 4].view(torch.float32).view(di // 128, ldsq)
+        c["Q5"] = (q.copy(), sq[:, a:b].cpu().numpy().T.copy())
         c["R6"] = np.asarray(hidden_out, np.uint16).copy()
     return c
 
 
 def rows(cand: dict, a: int, b: int) -> dict:
-    """Rows a..b-1 of every candidate array."""
-    return {k: v[a:b] for k, v in cand.items()}
+    """Rows a..b-1 of every candidate array (of each array of a tuple)."""
+    return {k: (tuple(x[a:b] for x in v) if isinstance(v, tuple) else v[a:b]) for k, v in cand.items()}
 
 
 class DecisionLog:
@@ -148,8 +164,17 @@ class DecisionLog:
             self.worst[pt] = max(self.worst.get(pt, 0.0), r["worst_taken"])
             if r["refused"] and pt not in self.first:
                 self.first[pt] = (where, r["first_refused"], r["worst_refused"])
+                if r.get("diag") is not None:
+                    self.diag = r["diag"]
 
     def check(self):
+        if getattr(self, "diag", None) is not None:
+            dg = self.diag
+            own, cand = dg[256:384].astype(np.int64), dg[384:512].astype(np.int64)
+            print("first refused Q5 block: candidate scale", dg[512], "own scale", dg[513])
+            for i in range(128):
+                print(f"  {i:3d} exact {dg[i]: .9e} scale {dg[128 + i]:.3e} own bf16 {own[i]:#06x} "
+                      f"gpu e4m3 {cand[i]:#04x}")
         assert not any(self.refused.values()), f"GPU codes that are not correct roundings: {self.refused} {self.first}"
         return {"taken": dict(self.taken), "worst_excess": {k: float(v) for k, v in self.worst.items()}}
 
@@ -159,3 +184,40 @@ def check_state_all_heads(gpu_h, oracle_h, tol=TOL_STATE):
     e = state_rel_err(gpu_h, oracle_h)
     assert e <= tol, f"state error {e} > {tol}"
     return e
+
+
+# ---------------------------------------------------------------------------
+# Guard bands: every device buffer the layer helpers allocate (states,
+# workspaces, uploaded inputs and weights) sits between two 4 KB bands of a
+# known byte pattern; after each GPU test the bands must be intact, so a
+# kernel that writes past any of those buffers fails the test even where no
+# compared output is hit.
+
+GUARD = 4096
+GUARD_BYTE = 0xA5
+
+
+class GuardBands:
+    def __init__(self):
+        self.bufs = []
+
+    def alloc(self, nbytes: int, device):
+        import torch
+        n = (nbytes + 255) // 256 * 256
+        raw = torch.empty(n + 2 * GUARD, dtype=torch.uint8, device=device)
+        raw[:GUARD].fill_(GUARD_BYTE)
+        raw[GUARD + nbytes:].fill_(GUARD_BYTE)
+        self.bufs.append((raw, nbytes))
+        return raw[GUARD:GUARD + n]
+
+    def check(self):
+        import torch
+        torch.cuda.synchronize()
+        bad = []
+        for raw, nbytes in self.bufs:
+            lo = raw[:GUARD]
+            hi = raw[GUARD + nbytes:]
+            if bool((lo != GUARD_BYTE).any()) or bool((hi != GUARD_BYTE).any()):
+                bad.append((raw.numel() - 2 * GUARD, nbytes))
+        self.bufs.clear()
+        assert not bad, f"writes past the end or before the start of {len(bad)} buffers: {bad[:5]}"

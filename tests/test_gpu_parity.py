@@ -255,7 +255,7 @@ def _prefill_case(lay, T, warm_decode, key):
     dl.prefill(x, (st[0][0], st[1][0], st[2][:1]), ws)
     _sync()
     got = bits_u16(x)
-    cand = prefill_candidates(ws, T, d, got, r5_available=T > 8)
+    cand = prefill_candidates(ws, [0, T], d, got, r5_available=T > 8)
     ref = hid.copy()
     log.add(ol.run_decided(ref, *ost, cand), "prefill")
     rep = log.check()

@@ -64,7 +64,7 @@ def test_stack8_prefill_and_256_decode_steps_sampled_sequence():
         dl.prefill_varlen(xall, cu, st[l], ws)
         torch.cuda.synchronize()
         got = bits_u16(xall[a:b])
-        cand = prefill_candidates(ws, int(cu[-1]), d, got, r5_available=True, a=a, b=b)
+        cand = prefill_candidates(ws, cu, d, got, r5_available=True, a=a, b=b)
         logs[l].add(ols[l].run_decided(x_or, *ost[l], cand), ("prefill", l))
         assert floored_rel_err(bf16_to_f64(got), bf16_to_f64(x_or), axis=-1) <= TOL_BF16, l
     # ---- 256 decode steps of all 16 sequences

@@ -62,7 +62,7 @@ def _varlen_case(lay, lens, warm, key, w8a8=False):
     # the gated norm writes bf16 rows on the tensor-core path, except on the
     # W8A8 arm with an E4M3 out_proj (codes and scales instead)
     r5 = T > 8 and not (w8a8 and lay["out_fmt"] == "fp8")
-    cand = prefill_candidates(ws, T, d, got, r5_available=r5)
+    cand = prefill_candidates(ws, cu, d, got, r5_available=r5, w8a8=w8a8)
     worst = 0.0
     errs = []
     h = st[0].cpu().numpy()

@@ -92,8 +92,9 @@ def _w8a8_prefill_case(lay, T, key):
     dl.prefill_varlen(x, [0, T], st, ws, w8a8=True)
     torch.cuda.synchronize()
     got = bits_u16(x)
-    # the E4M3 out_proj takes codes and scales: no bf16 gated-norm rows to read
-    cand = prefill_candidates(ws, T, d, got, r5_available=False)
+    # the E4M3 out_proj takes codes and scales (no bf16 gated-norm rows): the
+    # oracle judges those per 128-block, then the outputs (R6)
+    cand = prefill_candidates(ws, [0, T], d, got, r5_available=False, w8a8=True)
     ref = hid.copy()
     log = DecisionLog()
     log.add(ol.run_decided(ref, *ost, cand), "prefill")

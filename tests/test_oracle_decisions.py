@@ -191,3 +191,73 @@ def test_codes_of_an_evaluation_that_drops_a_term_are_refused():
     assert n_diff > 10
     dec = _run(ol, hid, {"R3": wrong})
     assert dec[2]["R3"]["refused"] == n_diff and dec[2]["R3"]["taken"] == 0
+
+
+def test_w8a8_quantized_inputs_no_decision_gives_are_refused():
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    ol = orc.OracleLayer(lay, act_fp8=True)
+    d = lay["dims"]
+    di = d["nheads"] * d["head_dim"]
+    hid = synth.make_hidden(3, 256, 44, 0, 0)
+    st = ol.new_state()
+    plain = hid.copy()
+    ol.run(plain, *st)
+    # candidates that no legitimate R5 decision gives, in every block: all
+    # refused, and the result equals the plain run
+    bad_q = np.full((3, di), 0x38, np.uint8)            # every code 1.0
+    bad_s = np.full((3, di // 128), 1.0, np.float32)    # scale 1: amax 448, not these rows'
+    st2 = ol.new_state()
+    h2 = hid.copy()
+    rep = ol.run_decided(h2, *st2, {"Q5": (bad_q, bad_s)})
+    assert rep["Q5"]["refused"] == 3 * (di // 128) and rep["Q5"]["taken"] == 0
+    assert rep["Q5"]["first_refused"] == 0
+    assert np.array_equal(h2, plain) and np.array_equal(st2[0], st[0])
+
+
+def test_w8a8_quantized_inputs_of_legitimate_r5_decisions_are_taken():
+    # the own quantization as candidates changes nothing; the quantization of
+    # gated-norm rows with one legitimate near-tie flip is taken (its block
+    # only), and gives the same result as taking that flip at R5 itself
+    lay = synth.make_layer(synth.TINY, synth.WL_TINY_DECODE)
+    ol = orc.OracleLayer(lay, act_fp8=True)
+    d = lay["dims"]
+    di = d["nheads"] * d["head_dim"]
+    T = 6
+    hid = synth.make_hidden(T, 256, 45, 0, 0)
+
+    def run(cand, trace=False):
+        st = ol.new_state()
+        h = hid.copy()
+        tr = np.zeros((T, di), np.uint16) if trace else None
+        rep = ol.run_decided(h, *st, cand, r5_trace=tr)
+        return h, st, rep, tr
+
+    def quant(rows):
+        q = np.zeros((T, di), np.uint8)
+        s = np.zeros((T, di // 128), np.float32)
+        for t in range(T):
+            q[t], s[t] = orc.act_quant(rows[t])
+        return q, s
+
+    h0, st0, _, r5 = run({}, trace=True)
+    h1, st1, rep1, _ = run({"Q5": quant(r5)})
+    assert rep1["Q5"]["taken"] == 0 and rep1["Q5"]["refused"] == 0
+    assert np.array_equal(h0, h1) and np.array_equal(st0[0], st1[0])
+    # flip one R5 code of token 2 to its neighbour: try elements until the R5
+    # decision takes it and the flip changes that block's quantization
+    for i in range(di):
+        r5f = r5.copy()
+        mag, sgn = int(r5[2, i]) & 0x7FFF, int(r5[2, i]) & 0x8000
+        if mag in (0, 0x7F7F):
+            continue
+        for step in (1, -1):
+            r5f[2, i] = sgn | (mag + step)
+            ha, sta, repa, _ = run({"R5": r5f})
+            qf = quant(r5f)
+            if repa["R5"]["taken"] != 1 or np.array_equal(qf[0][2], quant(r5)[0][2]):
+                continue
+            hb, stb, repb, _ = run({"Q5": qf})
+            assert repb["Q5"]["taken"] == 1 and repb["Q5"]["refused"] == 0
+            assert np.array_equal(ha, hb)  # the same decision, taken at R5 or at its quantization
+            return
+    pytest.fail("no legitimate R5 neighbour changes a quantized block")
