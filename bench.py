@@ -376,7 +376,8 @@ def main():
     out = {
         "metric": "decode tokens/s (Mamba-2 layer, batch 1)", "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": K_run, "warmup": W, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 weights x bf16 activations, fp32 accumulate", "data": "synthetic",
         "config": {"workload": "nemotron_h_8b_like_decode_b1", "batch": B, "hidden": 4096, "nheads": 128,
                    "head_dim": 64, "d_state": 128, "n_groups": 8, "d_conv": 4,
                    "weights": "e4m3 128x128 block-scaled, bf16 scales", "activations": "bf16",

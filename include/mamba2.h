@@ -277,16 +277,65 @@ int mamba2_layer_decode_noalloc(const m2_dims* dims, const m2_layer* layer, uint
  * kernels: a cudaMemcpyAsync between two launches keeps the next layer kernel
  * from starting its weight stream before the copy and the kernel before it
  * have finished.  dst and src 16-byte aligned, bytes a multiple of 16
- * (M2_ERR_ALIGN otherwise); pageable host memory or an unknown pointer:
- * M2_ERR_ARG, nothing launched.  Host pointers are checked on the host
- * (cudaPointerGetAttributes) before the launch. */
+ * (M2_ERR_ALIGN otherwise); pageable host memory, an unknown pointer, or a
+ * range [p, p + bytes) that does not lie inside one allocation of dst or of
+ * src: M2_ERR_ARG, nothing launched.  Both pointers are checked on the host
+ * (cudaPointerGetAttributes, and the allocation's address range) before the
+ * launch. */
 int m2_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------ diagnostics */
 
+/* Where a call keeps its intermediate values in the workspace, for reading
+ * them back (tests, debugging).  kind: M2_WS_KIND_DECODE (n = batch rows,
+ * cu_seqlens unused), M2_WS_KIND_PREFILL or M2_WS_KIND_PREFILL_W8A8 (n =
+ * sequences, cu_seqlens their host offsets as for the varlen prefill; the
+ * one-sequence prefill is n = 1, {0, T}).  offsets[n_offsets >= M2_WS_COUNT]
+ * receives byte offsets from ws, SIZE_MAX for a region the call does not use:
+ *   M2_WS_XN  input RMSNorm output [rows][hidden] (tensor-core paths)
+ *   M2_WS_ZX  in_proj output [rows][rup8(n_in)] bf16: z | xBC | dt (decode:
+ *             the xBC part holds the conv output; the raw xBC is in the ring)
+ *   M2_WS_U   prefill conv output [T][d_xbc] bf16
+ *   M2_WS_Y   SSM output y [rows][d_inner] fp32
+ *   M2_WS_G   gated-norm output [rows][d_inner] (bf16 when the out_proj runs
+ *             on the tensor cores with bf16 activations)
+ *   M2_WS_Q8  W8A8: E4M3 codes [T][rup16(max(hidden, d_inner))] of the last
+ *             projection's input; M2_WS_SQ: its fp32 block scales
+ *             [d_inner/128][rup128(T)].
+ * Contents are valid after the call completes and until the next call on the
+ * same workspace.  Host only; returns M2_OK or M2_ERR_ARG. */
+enum { M2_WS_KIND_DECODE = 0, M2_WS_KIND_PREFILL = 1, M2_WS_KIND_PREFILL_W8A8 = 2 };
+enum { M2_WS_XN = 0, M2_WS_ZX, M2_WS_U, M2_WS_Y, M2_WS_G, M2_WS_Q8, M2_WS_SQ, M2_WS_COUNT };
+int m2_workspace_map(const m2_dims* dims, int32_t kind, int32_t n, const int32_t* cu_seqlens, size_t* offsets,
+                     int32_t n_offsets);
+
 /* Device status word: M2_OK, or the first M2_ERR_TIMEOUT a kernel recorded on
  * the current device.  Synchronises the device.  clear != 0 resets it. */
 int m2_device_status(int clear);
+
+/* Limit of the library's in-kernel pipeline waits on the current device, in
+ * SM clock cycles (cycles <= 0 restores the default, 4e9: about 2 s at the
+ * maximum clock).  A pipeline wait that reaches the limit gives up: the kernel
+ * records M2_ERR_TIMEOUT (see m2_device_status), stops its own loop, waits for
+ * the copies and tensor-core work it already issued (that wait always uses the
+ * default limit), frees its tensor memory and returns; the outputs of that
+ * call are undefined.  A limit shorter than a correct call needs therefore
+ * turns every call into a timeout: it is meant for detecting a stalled
+ * pipeline sooner and for testing the timeout path, not for tuning.  Affects
+ * launches made after the call; returns M2_OK or M2_ERR_DEVICE. */
+int m2_set_wait_limit(int64_t cycles);
+
+/* Check of the timeout path on the current device: enqueues one small kernel
+ * that holds tensor memory and has a bulk copy of the 16 bytes at `probe` into
+ * shared memory in flight while it waits, with the pipeline wait limit, on a
+ * barrier that nothing signals.  The wait gives up (the status word then holds
+ * M2_ERR_TIMEOUT), the kernel waits for its own copy, writes the 16 bytes to
+ * `out`, frees its tensor memory and returns, leaving the device usable.  probe
+ * and out are 16-byte aligned device pointers (M2_ERR_ALIGN / M2_ERR_ARG
+ * otherwise, nothing launched).  Lower the limit first (m2_set_wait_limit):
+ * with the default the kernel runs for about two seconds.  Returns the launch
+ * status, not the timeout (read that with m2_device_status). */
+int m2_wait_check(const void* probe, void* out, cudaStream_t stream);
 
 /* Number of kernels this library has launched in this process (all devices). */
 int64_t m2_launch_count(void);

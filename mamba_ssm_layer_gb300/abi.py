@@ -35,7 +35,8 @@ EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_dec
            "mamba2_layer_decode_noalloc", "mamba2_layer_prefill_varlen", "m2_workspace_bytes_varlen",
            "mamba2_layer_prefill_varlen_w8a8", "w8a8_gemm", "m2_w8a8_workspace_bytes",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
-           "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count", "m2_set_fused_decode", "m2_copy")
+           "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count", "m2_set_fused_decode", "m2_copy",
+           "m2_set_wait_limit", "m2_wait_check", "m2_workspace_map")
 
 
 class M2Dims(C.Structure):
@@ -109,6 +110,10 @@ def lib():
             l.m2_kernel_count.argtypes = []; l.m2_kernel_count.restype = I32
             l.m2_set_fused_decode.argtypes = [C.c_int]; l.m2_set_fused_decode.restype = C.c_int
             l.m2_copy.argtypes = [P, P, C.c_size_t, P]; l.m2_copy.restype = C.c_int
+            l.m2_set_wait_limit.argtypes = [C.c_int64]; l.m2_set_wait_limit.restype = C.c_int
+            l.m2_wait_check.argtypes = [P, P, P]; l.m2_wait_check.restype = C.c_int
+            l.m2_workspace_map.argtypes = [C.POINTER(M2Dims), I32, I32, C.POINTER(C.c_int32), C.POINTER(SZ), I32]
+            l.m2_workspace_map.restype = C.c_int
             _lib = l
     return _lib
 
@@ -254,6 +259,35 @@ def m2_launch_count() -> int:
 def m2_set_fused_decode(enable: bool) -> bool:
     """Single-launch batch-1 decode step (True) or the kernel chain (False, the default); returns the previous setting."""
     return bool(lib().m2_set_fused_decode(1 if enable else 0))
+
+
+def m2_set_wait_limit(cycles: int, check=True) -> int:
+    """Limit of the in-kernel pipeline waits on the current device (SM clock cycles; <= 0: the default)."""
+    st = lib().m2_set_wait_limit(int(cycles))
+    return _check("m2_set_wait_limit", st) if check else st
+
+
+def m2_wait_check(probe, out, stream=None, check=True) -> int:
+    """Timeout-path check: a kernel waits on a barrier nothing signals (see include/mamba2.h)."""
+    st = lib().m2_wait_check(_ptr(probe), _ptr(out), _stream(stream))
+    return _check("m2_wait_check", st) if check else st
+
+
+M2_WS_KIND_DECODE, M2_WS_KIND_PREFILL, M2_WS_KIND_PREFILL_W8A8 = 0, 1, 2
+WS_REGIONS = ("xn", "zx", "u", "y", "g", "q8", "sq")
+
+
+def m2_workspace_map(dims, kind: int, n: int, cu_seqlens=None) -> dict:
+    """Byte offsets of a call's workspace regions ({name: offset}; regions the call does not use are left out)."""
+    k = len(WS_REGIONS)
+    out = (C.c_size_t * k)()
+    cu = None
+    if cu_seqlens is not None:
+        arr = (C.c_int32 * len(cu_seqlens))(*[int(v) for v in cu_seqlens])
+        cu = C.cast(arr, C.POINTER(C.c_int32))
+    _check("m2_workspace_map", lib().m2_workspace_map(C.byref(dims), kind, n, cu, out, k))
+    none = (1 << (8 * C.sizeof(C.c_size_t))) - 1
+    return {name: out[i] for i, name in enumerate(WS_REGIONS) if out[i] != none}
 
 
 def kernel_names() -> list[str]:

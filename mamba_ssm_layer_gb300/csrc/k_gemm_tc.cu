@@ -42,6 +42,7 @@
 
 #include "m2_common.cuh"
 #include "m2_kernels.h"
+#include "m2_tc.cuh"
 
 namespace m2 {
 
@@ -100,81 +101,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
-}
-
-// K-major operand descriptor, 128-byte swizzle: rows of 128 bytes, 8-row atoms
-// 1024 bytes apart (stride byte offset), leading byte offset unused.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major.
-__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-
-// kind::f8f6f4 instruction descriptor: D fp32, A and B E4M3 (format 0), both K-major.
-__host__ __device__ constexpr uint32_t tc_idesc_f8(int m, int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
-}
-__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
-}
-// Arrives on the mbarrier once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// 32 lanes x 32 consecutive fp32 columns of TMEM into registers.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 lanes x 16 consecutive fp32 columns of TMEM into registers.
-// Shared-memory float4 load that stays after the preceding TMEM wait (a plain
-// load may be hoisted above it, holding its registers across the wait).
-__device__ __forceinline__ float4 lds_f4_ordered(uint32_t addr) {
-  float4 r;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w) : "r"(addr));
-  return r;
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // Two E4M3 -> two bf16, exactly (E4M3 -> f16 -> f32 -> bf16 are all exact).
@@ -324,13 +250,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+      // drain: the tiles issued (k blocks [0, gk)) have landed before the CTA
+      // may exit, also after a timeout stopped their consumers
+      for (int k = max(0, gk - kTcWStages); k < gk; ++k)
+        if (!mbar_drain(&bars->w_full[k % kTcWStages], (k / kTcWStages) & 1)) break;
     }
   } else if (warp == kTcAWarp) {
     // -------------------------------------------------------- activation producer
     pdl_wait();  // A is written by the previous kernel
     if (lane == 0) {
       const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
-      int gk = 0;
+      int gk = 0, a_iss = 0, sc_iss = 0;  // k blocks whose activation tile / token scales are issued
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
@@ -342,6 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);
           if (AQ8) {  // E4M3 codes: one 128-byte-swizzled box of NT rows x 128 k
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
+            a_iss = gk + 1;
             // the k block's token scales into the slot of its TMEM buffer, once the
             // epilogue has finished with the k block that used the slot before
             const int tb = gk % kTcTmemBufs;
@@ -350,12 +281,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_arrive_expect_tx(&bars->sc_full[tb], NT * 4);
             bulk_g2s(smem + Lay::kSc + tb * NT * 4, a.sq + (size_t)kb * a.ldsq + (size_t)mt * NT, NT * 4,
                      &bars->sc_full[tb], pola);
+            sc_iss = gk + 1;
           } else {
             tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
             tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
+            a_iss = gk + 1;
           }
         }
       }
+      // drain: everything issued has landed before the CTA may exit
+      for (int k = max(0, a_iss - SA); k < a_iss; ++k)
+        if (!mbar_drain(&bars->a_full[k % SA], (k / SA) & 1)) break;
+      for (int k = max(0, sc_iss - kTcTmemBufs); k < sc_iss; ++k)
+        if (!mbar_drain(&bars->sc_full[k % kTcTmemBufs], (k / kTcTmemBufs) & 1)) break;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
@@ -402,6 +340,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_commit(&bars->mma_done[tb]);
         }
       }
+      // drain: no MMA of this thread is still writing TMEM when it is freed
+      // (the last commit tracks all earlier MMAs)
+      if (gk > 0) mbar_drain(&bars->mma_done[(gk - 1) % kTcTmemBufs], ((gk - 1) / kTcTmemBufs) & 1);
     }
   } else if (warp < 6) {
     // -------------------------------------------------------- converters
@@ -413,8 +354,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1;
-          if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
-          if (!dead && gk >= 2 && !kblock_done(bars, gk - 2)) dead = true;  // k block gk-2 read buffer b
+          // each warp decides together (its lanes meet at __syncwarp below)
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1))) dead = true;
+          if (!dead && gk >= 2 && !__all_sync(0xffffffffu, kblock_done(bars, gk - 2)))
+            dead = true;  // k block gk-2 read buffer b
           if (dead) break;
           const uint8_t* raw = smem + Lay::kW + s * kTcBM * kTcBK;
           uint8_t* dst = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
@@ -470,8 +413,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
         const int tb = gk % kTcTmemBufs;
         const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb)) : 1.0f;
-        if (!mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1)) dead = true;
-        if (AQ8 && !dead && !mbar_wait(&bars->sc_full[tb], (gk / kTcTmemBufs) & 1)) dead = true;
+        // the TMEM loads below are warp-collective: the warp decides together
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1))) dead = true;
+        if (AQ8 && !dead && !__all_sync(0xffffffffu, mbar_wait(&bars->sc_full[tb], (gk / kTcTmemBufs) & 1)))
+          dead = true;
         if (dead) break;
         tc_fence_after();
         // 16 columns per TMEM load: two loads in flight before one wait at
@@ -553,31 +498,6 @@ __global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const GemvArgs a, c
 
 // ------------------------------------------------------------------ host
 
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
-static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                      uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t es[2] = {1, 1};
-  return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool gemm_tc_supported(int M, int N, int K, bool fp8) {
   (void)N;
   (void)fp8;
@@ -653,6 +573,53 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   return e;
 }
 
+// ------------------------------------------------------------------ wait-path check
+//
+// One CTA that holds tensor memory and has a bulk copy in flight waits, with
+// the pipeline limit, on a barrier that nothing signals.  It must give up
+// (M2_ERR_TIMEOUT in the status word), wait for its copy with the drain limit,
+// pass the copied bytes to `out`, free its tensor memory and return.
+__global__ void __launch_bounds__(128, 1) wait_check_kernel(const uint4* probe, uint4* out) {
+  __shared__ __align__(128) uint4 buf;
+  __shared__ __align__(8) uint64_t bar_copy, bar_never;
+  __shared__ uint32_t tmem_base;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_copy, 1);
+    mbar_init(&bar_never, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
+                 "r"(32));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0 && lane == 0) {
+    mbar_arrive_expect_tx(&bar_copy, 16);
+    bulk_g2s(&buf, probe, 16, &bar_copy, policy_evict_normal());
+    if (!mbar_wait(&bar_never, 0)) {  // nothing arrives: this times out
+      if (mbar_drain(&bar_copy, 0)) *out = buf;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(32));
+  }
+}
+
+cudaError_t launch_wait_check(const void* probe, void* out, cudaStream_t s) {
+  trace_pre(K_WAIT_CHECK, s);
+  const cudaError_t e = launch_k(wait_check_kernel, dim3(1), dim3(128), 0, s, false,
+                                 static_cast<const uint4*>(probe), static_cast<uint4*>(out));
+  trace_post(K_WAIT_CHECK, s);
+  return e;
+}
+
 cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   if (g.q8) {  // W8A8: E4M3 activation codes with per-(token, k block) scales
     if (!fp8 || g.K % 128 || g.ldq % 16 || g.ldsq % 128) return cudaErrorInvalidValue;
@@ -663,14 +630,8 @@ cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   return launch_tc<128, false>(g, fp8, s);
 }
 
-int status_gemm_tc(int clear) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
-  if (clear) {
-    const int z = 0;
-    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
-  }
-  return v;
-}
+int status_gemm_tc(int clear) { return tu_status(clear); }
+
+cudaError_t wait_limit_gemm_tc(long long cycles) { return tu_set_wait_limit(cycles); }
 
 }  // namespace m2

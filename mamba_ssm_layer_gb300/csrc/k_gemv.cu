@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   if (warp == kGemvProducerWarp) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      for (int it = stages; it < niter; ++it) {
+      int it = stages;
+      for (; it < niter; ++it) {
         const int s = it % stages;
         if (!mbar_wait(&tail->empty[s], ((it / stages) - 1) & 1)) break;  // status recorded
         const int rows = min(R, nrows - it * R);
@@ -326,12 +327,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         mbar_arrive_expect_tx(&tail->full[s], bytes);
         bulk_g2s(smem + (size_t)s * stage_bytes, wbase + (size_t)it * R * rowbytes, bytes, &tail->full[s], pol);
       }
+      // drain: the copies issued (stages [0, it)) have landed before the CTA
+      // may exit, also when the consumers stopped after a timeout
+      const int issued = min(it, niter);
+      for (int k = max(0, issued - stages); k < issued; ++k)
+        if (!mbar_drain(&tail->full[k % stages], (k / stages) & 1)) break;
     }
   } else if (warp == kGemvHelperWarp) {
     // ---------------------------------------------------------- helper
     for (int it = 0; it < niter; ++it) {
       const int slot = it % kGemvSlots;
-      if (!dead && !mbar_wait(&tail->red_full[slot], (it / kGemvSlots) & 1)) dead = true;
+      // the lanes meet at __syncwarp below: the warp decides together
+      if (!dead && !__all_sync(0xffffffffu, mbar_wait(&tail->red_full[slot], (it / kGemvSlots) & 1))) dead = true;
       if (!dead && lane < V) {
         float t = 0.0f;
 #pragma unroll
@@ -347,7 +354,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       const int s = it % stages;
       const int row0 = row_begin + it * R;
       const int rows = min(R, nrows - it * R);
-      if (!dead && !mbar_wait(&tail->full[s], (it / stages) & 1)) dead = true;
+      // shuffles and __syncwarp follow: the warp decides together
+      if (!dead && !__all_sync(0xffffffffu, mbar_wait(&tail->full[s], (it / stages) & 1))) dead = true;
       const uint8_t* st = smem + (size_t)s * stage_bytes;
 
       float v[V];
@@ -395,7 +403,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
       if (lane == 0) mbar_arrive(&tail->empty[s]);
       Butterfly<V, 16>::run(v, lane);
       const int slot = it % kGemvSlots;
-      if (it >= kGemvSlots && !dead && !mbar_wait(&tail->red_empty[slot], ((it / kGemvSlots) - 1) & 1)) dead = true;
+      if (it >= kGemvSlots && !dead &&
+          !__all_sync(0xffffffffu, mbar_wait(&tail->red_empty[slot], ((it / kGemvSlots) - 1) & 1)))
+        dead = true;
       if ((lane & ((1 << (5 - LOGV)) - 1)) == 0) tail->red[slot][gwarp][lane >> (5 - LOGV)] = v[0];
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->red_full[slot]);
@@ -512,14 +522,8 @@ int gemv_rows_per_pass(int K, bool fp8) {
   return cpt == 1 ? 4 : (cpt == 2 ? 2 : 1);
 }
 
-int status_gemv(int clear) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
-  if (clear) {
-    const int z = 0;
-    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
-  }
-  return v;
-}
+int status_gemv(int clear) { return tu_status(clear); }
+
+cudaError_t wait_limit_gemv(long long cycles) { return tu_set_wait_limit(cycles); }
 
 }  // namespace m2

@@ -26,9 +26,13 @@
 // warps' tiles in a fixed order (deterministic) and run the epilogue.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "m2_common.cuh"
 #include "m2_kernels.h"
+#include "m2_tc.cuh"
 
 namespace m2 {
 
@@ -52,8 +56,13 @@ struct MmaTail {
 struct MmaLayout {
   int act_ld, tail, act, tot, epi, stage, stage_bytes, kc, pitch, stages, total;
   bool whole;  // a stage is one contiguous block of 16 whole rows (one copy, no row padding)
+  bool tma;    // a stage of row pieces arrives as one 3-D tensor copy, rows unpadded
 };
-__host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int mb, int epi, int dconv) {
+// tma: stages of row pieces (rows longer than 4 KB) come as one 3-D tensor
+// copy into unpadded rows; kc, and with it which k each warp sums, is the
+// same either way.
+__host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int mb, int epi, int dconv,
+                                                bool tma = false) {
   MmaLayout L;
   L.act_ld = K + 8;  // elements per activation row (the pad spreads rows over banks)
   L.tail = 0;
@@ -76,7 +85,8 @@ __host__ __device__ inline MmaLayout mma_layout(int K, int es, int rows_max, int
   if (!L.whole)
     while (kc > 64 * es && budget / (kMmaRows * (kc + kRowPad)) < 3) kc = (kc / 2 + 64 * es - 1) / (64 * es) * (64 * es);
   L.kc = kc;
-  L.pitch = L.whole ? row_bytes : kc + kRowPad;
+  L.tma = tma && !L.whole;
+  L.pitch = L.whole ? row_bytes : (L.tma ? kc : kc + kRowPad);
   L.stage_bytes = kMmaRows * L.pitch;
   L.stages = budget / L.stage_bytes;
   if (L.stages > kMaxStages) L.stages = kMaxStages;
@@ -119,13 +129,19 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // E4M3 weights, unscale[m] = 2^-j).  Same arithmetic as the separate norm
 // kernel (k_mixer.cu): the RMSNorm sum of squares as error-free fp32 pairs
 // and near-tie decisions in double, so its rounding decisions do not depend on
-// the order; the
-// gated sum in a fixed order (every CTA computes the same row identically).
-// red[] (64 floats): warp partials; red[62..63] the combined pair.
+// the order; the gated sum in a fixed order (every CTA computes the same row
+// identically).  One exchange through shared memory: each warp leaves its
+// partial sums and the largest |product| it will scale; every thread then
+// combines the warps' values in the same fixed order itself (no second round
+// and no single-thread combine).  The f16 prescale comes from that largest
+// product times the norm factor, enlarged by 2^-20 so that it never falls
+// below the largest rounded output: the rows' maximum lands in [2^13, 2^15)
+// and every bf16 value within 2^30 of it stays exact in f16.
 template <bool F16>
 __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* red, float* unscale, int tid,
                                int nC) {
   const int K = a.K, warp = tid >> 5, lane = tid & 31;
+  const int nw = nC / 32;
   constexpr int kPer = 2;  // 16-byte chunks of 8 elements per thread (K <= 8192 with 512 threads)
   float v[kPer * 8];
   uint4 wv[kPer], zv[kPer];
@@ -155,7 +171,28 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
       }
     }
   }
+  // the weights, silu(z) (gated), and the largest |v * w (* silu(z))|
+  float wf[kPer * 8], sz[kPer * 8];
+  float pm = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kPer; ++c) {
+    const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w}, z4[4] = {zv[c].x, zv[c].y, zv[c].z, zv[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      wf[c * 8 + 2 * e] = bf16lo(w4[e]);
+      wf[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
+      sz[c * 8 + 2 * e] = a.norm == NORM_RMS ? 1.0f : silu_f(bf16lo(z4[e]));
+      sz[c * 8 + 2 * e + 1] = a.norm == NORM_RMS ? 1.0f : silu_f(bf16hi(z4[e]));
+    }
+  }
+  if (F16) {
+#pragma unroll
+    for (int e = 0; e < kPer * 8; ++e) pm = fmaxf(pm, fabsf(v[e] * wf[e] * sz[e]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
+  }
   uint16_t o[kPer * 8];
+  float r;  // the norm factor as the rounding uses it
   if (a.norm == NORM_RMS) {
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
@@ -163,25 +200,24 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
     two_sum_warp(hi, lo);
     if (lane == 0) {
       red[warp] = hi;
-      red[32 + warp] = lo;
+      red[16 + warp] = lo;
+      red[32 + warp] = pm;
     }
     named_bar(1, nC);
-    if (tid == 0) {
-      float h = 0.0f, l = 0.0f;
-      for (int w = 0; w < nC / 32; ++w) {
-        two_sum_acc(h, l, red[w]);
-        l += red[32 + w];
-      }
-      red[62] = h;
-      red[63] = l;
+    float h = 0.0f, l = 0.0f;
+    pm = 0.0f;
+    for (int w = 0; w < nw; ++w) {  // the same fixed order in every thread
+      two_sum_acc(h, l, red[w]);
+      l += red[16 + w];
+      pm = fmaxf(pm, red[32 + w]);
     }
-    named_bar(1, nC);
     NormR nr;
-    nr.h = red[62];
-    nr.l = red[63];
+    nr.h = h;
+    nr.l = l;
     nr.inv_k = a.norm_inv_k;
     nr.eps = a.norm_eps;
     const float rf = norm_rf(nr);
+    r = rf;
 #pragma unroll
     for (int c = 0; c < kPer; ++c) {
       const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
@@ -200,38 +236,22 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
 #pragma unroll
       for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
       ss = warp_sum(ss);
-      if (lane == 0) red[c * (nC / 32) + warp] = ss;  // chunk (warp + 16c) of 256 elements
+      if (lane == 0) red[c * nw + warp] = ss;  // chunk (warp + 16c) of 256 elements
     }
+    if (lane == 0) red[kPer * nw + warp] = pm;
     named_bar(1, nC);
-    if (tid == 0) {
-      float gs = 0.0f;
-      for (int j = 0; j < K / 256; ++j) gs += red[j];
-      red[63] = 1.0f / sqrtf(gs / (float)K + a.norm_eps);
-    }
-    named_bar(1, nC);
-    const float r = red[63];
+    float gs = 0.0f;
+    for (int j = 0; j < K / 256; ++j) gs += red[j];
+    pm = 0.0f;
+    for (int w = 0; w < nw; ++w) pm = fmaxf(pm, red[kPer * nw + w]);
+    r = 1.0f / sqrtf(gs / (float)K + a.norm_eps);
 #pragma unroll
-    for (int c = 0; c < kPer; ++c) {
-      const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w}, z4[4] = {zv[c].x, zv[c].y, zv[c].z, zv[c].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[c * 8 + 2 * e] = f32_to_bf16(v[c * 8 + 2 * e] * r * bf16lo(w4[e]) * silu_f(bf16lo(z4[e])));
-        o[c * 8 + 2 * e + 1] = f32_to_bf16(v[c * 8 + 2 * e + 1] * r * bf16hi(w4[e]) * silu_f(bf16hi(z4[e])));
-      }
-    }
+    for (int e = 0; e < kPer * 8; ++e) o[e] = f32_to_bf16(v[e] * r * wf[e] * sz[e]);
   }
   float up = 1.0f;
   if (F16) {
-    float mx = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kPer * 8; ++e) mx = fmaxf(mx, fabsf(bf16_to_f32(o[e])));
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
-    named_bar(1, nC);  // every reader of red[] above is done
-    if (lane == 0) red[warp] = mx;
-    named_bar(1, nC);
-    mx = 0.0f;
-    for (int w = 0; w < nC / 32; ++w) mx = fmaxf(mx, red[w]);
+    // exponent of an upper bound of the largest rounded output
+    const float mx = pm * r * (1.0f + 0x1p-20f);
     const unsigned bits = __float_as_uint(mx);
     const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
     const int jx = max(-120, min(120, 14 - ex));
@@ -256,16 +276,16 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
       *reinterpret_cast<uint4*>(act + k0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
     }
   }
-  named_bar(1, nC);  // red[] is reused by the next row
+  named_bar(1, nC);  // act is complete, and red[] may be reused by the next row
 }
 
 template <bool FP8, int MB>
 __global__ void __launch_bounds__(kMmaThreads, 1)
-    gemv_mma_kernel(const GemvArgs a, int rows_max) {
+    gemv_mma_kernel(const GemvArgs a, int rows_max, const __grid_constant__ CUtensorMap tmW, int tma) {
   constexpr int ES = FP8 ? 1 : 2;  // bytes per weight
   extern __shared__ __align__(128) uint8_t smem[];
   const int kb = (a.K + 127) / 128;
-  const MmaLayout lay = mma_layout(a.K, ES, rows_max, MB, a.epi, a.dconv);
+  const MmaLayout lay = mma_layout(a.K, ES, rows_max, MB, a.epi, a.dconv, tma != 0);
   MmaTail* tail = reinterpret_cast<MmaTail*>(smem + lay.tail);
   uint16_t* act_s = reinterpret_cast<uint16_t*>(smem + lay.act);  // [MB][act_ld]
   float* tot = reinterpret_cast<float*>(smem + lay.tot);
@@ -348,6 +368,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
     int j = 0;
     bool waited = false;
+    // a tensor copy needs a 128-byte aligned destination (the layout keeps
+    // every stage at a multiple of 128 from the base): if the base is not,
+    // stop here -- the consumers' waits then time out and report it
+    if (lay.tma && (smem_addr(stg) & 127u)) {
+      if (lane == 0) record_timeout();
+      dead = true;
+    }
     for (; j < nst && !dead; ++j) {
       const int s = j % S;
       if (j == S) {
@@ -356,7 +383,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         pdl_trigger();
         waited = true;
       }
-      if (j >= S && !mbar_wait(&tail->empty[s], ((j / S) - 1) & 1)) dead = true;
+      // every lane waits; the warp goes on only if all saw the slot freed
+      if (j >= S && !__all_sync(0xffffffffu, mbar_wait(&tail->empty[s], ((j / S) - 1) & 1))) dead = true;
       if (dead) break;
       const int rg = rg_begin + j / nch, ch = j % nch;
       const int cb = min(lay.kc, row_bytes - ch * lay.kc);  // bytes of each row in this chunk
@@ -367,6 +395,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
           mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(nr * row_bytes));
           bulk_g2s(stg + (size_t)s * lay.stage_bytes, W + (size_t)rg * kMmaRows * row_bytes, (uint32_t)(nr * row_bytes),
                    &tail->full[s], pol);
+        }
+      } else if (lay.tma) {
+        // 16 rows x kc bytes in one copy (pieces past a row's end and rows past
+        // N arrive as zeros; the whole box counts)
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(kMmaRows * lay.kc));
+          tma_load_3d(stg + (size_t)s * lay.stage_bytes, &tmW, 0, ch * (lay.kc / 256), rg * kMmaRows, &tail->full[s],
+                      pol);
         }
       } else {
         if (lane == 0) mbar_arrive_expect_tx(&tail->full[s], (uint32_t)(kMmaRows * cb));
@@ -383,8 +419,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       pdl_trigger();
     }
     // drain: every copy this warp issued has landed before the CTA may exit
+    // (also after a timeout, when the consumers may have stopped reading)
     for (int k = max(0, j - S); k < j; ++k)
-      if (!mbar_wait(&tail->full[k % S], (k / S) & 1)) break;
+      if (!mbar_drain(&tail->full[k % S], (k / S) & 1)) break;
+    if (epi_bulk && lane == 0) mbar_drain(&tail->epi_bar, 0);
     __syncthreads();  // pairs with the consumers' barrier before the epilogue
     return;
   }
@@ -481,7 +519,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     const int ng = cb / (64 * ES);                      // 64-element groups in this chunk
     const int q0 = (ng * warp) / kMmaWarps, q1 = (ng * (warp + 1)) / kMmaWarps;
     const int kel0 = ch * (lay.kc / ES);                // first k of the chunk
-    if (!mbar_wait(&tail->full[s], (j / S) & 1)) {
+    // the MMAs below are warp-collective: the warp decides together
+    if (!__all_sync(0xffffffffu, mbar_wait(&tail->full[s], (j / S) & 1))) {
       dead = true;
       break;
     }
@@ -588,14 +627,24 @@ static cudaError_t launch_mma_one(const GemvArgs& a, cudaStream_t s) {
   int grid = num_sms();
   if (grid > nrg) grid = nrg;
   const int rows_max = ((nrg + grid - 1) / grid) * kMmaRows;
-  const MmaLayout lay = mma_layout(a.K, FP8 ? 1 : 2, rows_max, MB, a.epi, a.dconv);
+  // rows longer than 4 KB: each stage (16 row pieces) as one 3-D tensor copy
+  // instead of 16 row copies, when the rows split into 256-byte pieces
+  CUtensorMap tmW;
+  memset(&tmW, 0, sizeof(tmW));
+  const int row_bytes = a.K * (FP8 ? 1 : 2);
+  const MmaLayout plain = mma_layout(a.K, FP8 ? 1 : 2, rows_max, MB, a.epi, a.dconv);
+  const int tma = (!plain.whole && row_bytes % 256 == 0 && plain.kc % 256 == 0 &&
+                   encode_rows_3d(&tmW, a.W, (uint64_t)row_bytes, (uint64_t)a.N, 256, plain.kc / 256, kMmaRows))
+                      ? 1
+                      : 0;
+  const MmaLayout lay = mma_layout(a.K, FP8 ? 1 : 2, rows_max, MB, a.epi, a.dconv, tma != 0);
   if (lay.stages < 2 || lay.total > 227 * 1024) return cudaErrorInvalidConfiguration;
   auto kern = gemv_mma_kernel<FP8, MB>;
   cudaError_t e = set_smem_once((const void*)kern, lay.total, done_mask);
   if (e != cudaSuccess) return e;
   const int id = (FP8 ? K_GEMV_FP8 : K_GEMV_BF16) + (a.epi == EPI_INPROJ_CONV ? 1 : (a.epi == EPI_RESID ? 2 : 0));
   trace_pre(id, s);
-  e = launch_k(kern, dim3(grid), dim3(kMmaThreads), lay.total, s, a.pdl != 0, a, rows_max);
+  e = launch_k(kern, dim3(grid), dim3(kMmaThreads), lay.total, s, a.pdl != 0, a, rows_max, tmW, tma);
   trace_post(id, s);
   return e;
 }
@@ -727,7 +776,7 @@ __device__ __forceinline__ bool mma_consume(const GemvArgs& a, const MmaPlan& p,
     const int ng = cb / (64 * ES);
     const int q0 = (ng * warp) / kMmaWarps, q1 = (ng * (warp + 1)) / kMmaWarps;
     const int kel0 = ch * (p.kc / ES);
-    if (!mbar_wait(&tail->full[s], (j / S) & 1)) return false;
+    if (!__all_sync(0xffffffffu, mbar_wait(&tail->full[s], (j / S) & 1))) return false;  // warp-collective MMAs follow
     const uint8_t* st0 = stg + (size_t)s * kFusedStride + (size_t)g * p.pitch;
     const uint8_t* st8 = st0 + (size_t)8 * p.pitch;
     const int r0 = min(rg * kMmaRows + g, p.row_end - 1), r8 = min(rg * kMmaRows + g + 8, p.row_end - 1);
@@ -781,33 +830,34 @@ __device__ __forceinline__ bool mma_consume(const GemvArgs& a, const MmaPlan& p,
 }
 
 // Grid-wide barrier of the fused step (all CTAs resident: cooperative launch).
-// Arrival count and generation persist across launches; the last arriver
-// resets the count before it advances the generation.  The wait is bounded: on
-// a timeout the status word is set and the CTA goes on.
-__device__ unsigned g_fused_bar[2];  // [0] arrivals, [1] generation
+// One 64-bit arrival counter that only grows: an arrival that finds the count
+// at c waits until it reaches the next multiple of the grid size above c.
+// Every CTA arrives exactly once at each barrier, timed out or not (a timeout
+// only ends the wait: the status word is set and the CTA goes on), so the
+// count is a multiple of the grid size again when a launch ends, and the next
+// launch's barriers line up however the previous one ended; nothing has to be
+// reset between launches.
+__device__ unsigned long long g_fused_arrivals;
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
 __device__ __noinline__ void fused_grid_barrier(int tid, int nthreads) {
   named_bar(1, nthreads);
   if (tid == 0) {
-    const unsigned gen0 = ld_acquire_gpu(&g_fused_bar[1]);  // before arriving
-    __threadfence();
-    if (atomicAdd(&g_fused_bar[0], 1u) == gridDim.x - 1) {
-      atomicExch(&g_fused_bar[0], 0u);
-      __threadfence();
-      atomicAdd(&g_fused_bar[1], 1u);
-    } else {
-      const long long t0 = clock64();
-      while (ld_acquire_gpu(&g_fused_bar[1]) == gen0) {
-        if (clock64() - t0 > kWaitCycles) {
-          record_timeout();
-          break;
-        }
+    const unsigned long long G = gridDim.x;
+    __threadfence();  // this CTA's writes before its arrival
+    const unsigned long long c = atomicAdd(&g_fused_arrivals, 1ull);
+    const unsigned long long target = (c / G + 1) * G;
+    const long long limit = *reinterpret_cast<volatile long long*>(&g_wait_limit);
+    const long long t0 = clock64();
+    while (ld_acquire_gpu_u64(&g_fused_arrivals) < target) {
+      if (clock64() - t0 > limit) {
+        record_timeout();
+        break;
       }
     }
     __threadfence();
@@ -910,7 +960,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
         waited = true;
         epi_copies();
       }
-      if (j >= S && !mbar_wait(&tail->empty[s], ((j / S) - 1) & 1)) dead = true;
+      if (j >= S && !__all_sync(0xffffffffu, mbar_wait(&tail->empty[s], ((j / S) - 1) & 1))) dead = true;
       if (dead) break;
       uint8_t* dst = stg + (size_t)s * kFusedStride;
       if (j < p1.nst) mma_produce(a1, p1, j, dst, &tail->full[s], pol1, lane);
@@ -921,8 +971,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       pdl_trigger();
       epi_copies();
     }
+    // drain: the weight stages and epilogue copies this warp issued have
+    // landed before the CTA may exit (also after a timeout)
     for (int k = max(0, j - S); k < j; ++k)
-      if (!mbar_wait(&tail->full[k % S], (k / S) & 1)) break;
+      if (!mbar_drain(&tail->full[k % S], (k / S) & 1)) break;
+    if (lane == 0 && bulk1) mbar_drain(&tail->epi_bar, 0);
+    if (lane == 0 && bulk3) mbar_drain(&tail->epi_bar2, 0);
     __syncthreads();
     return;
   }
@@ -1062,10 +1116,23 @@ bool decode_fused_supported(const FusedStepArgs& fa, bool fp8) {
   return lay.stages >= 2 && lay.total <= 227 * 1024;
 }
 
+// Per device: whether the cooperative launch accepts the PDL attribute (-1
+// untried, 1 yes, 0 cooperative alone) and the occupancy probed for a layout.
+struct FusedLaunchInfo {
+  int pdl_mode = -1;
+  int occ_smem = -1;
+  int occ_blocks = 0;
+};
+static std::mutex g_fused_mu;
+
 template <bool FP8>
 static cudaError_t launch_fused_one(const FusedStepArgs& fa, cudaStream_t st) {
   static int done_mask[64] = {0};
-  static int pdl_mode = -1;  // -1 untried, 1 cooperative + PDL accepted, 0 cooperative alone
+  static FusedLaunchInfo info[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_fused_mu);
+  FusedLaunchInfo& fi = info[dev];
   const int G = num_sms();
   const int rin = (((fa.in.N + kMmaRows - 1) / kMmaRows + G - 1) / G) * kMmaRows;
   const int rout = (((fa.out.N + kMmaRows - 1) / kMmaRows + G - 1) / G) * kMmaRows;
@@ -1074,13 +1141,13 @@ static cudaError_t launch_fused_one(const FusedStepArgs& fa, cudaStream_t st) {
   auto kern = decode_step_fused_kernel<FP8>;
   cudaError_t e = set_smem_once((const void*)kern, lay.total, done_mask);
   if (e != cudaSuccess) return e;
-  static int occ_smem = -1, occ_blocks = 0;  // all CTAs must be resident at once
-  if (occ_smem != lay.total) {
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, kMmaThreads, lay.total)) != cudaSuccess)
+  if (fi.occ_smem != lay.total) {  // all CTAs must be resident at once
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fi.occ_blocks, kern, kMmaThreads, lay.total)) !=
+        cudaSuccess)
       return e;
-    occ_smem = lay.total;
+    fi.occ_smem = lay.total;
   }
-  if (occ_blocks < 1) return cudaErrorCooperativeLaunchTooLarge;
+  if (fi.occ_blocks < 1) return cudaErrorCooperativeLaunchTooLarge;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(kMmaThreads);
@@ -1093,18 +1160,18 @@ static cudaError_t launch_fused_one(const FusedStepArgs& fa, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   trace_pre(K_DECODE_FUSED, st);
-  cfg.numAttrs = pdl_mode == 0 ? 1 : 2;
+  cfg.numAttrs = fi.pdl_mode == 0 ? 1 : 2;
   FusedChunks ck;
   chain_chunking(fa.in, FP8 ? 1 : 2, ck.kc_in, ck.whole_in);
   chain_chunking(fa.out, FP8 ? 1 : 2, ck.kc_out, ck.whole_out);
   e = cudaLaunchKernelEx(&cfg, kern, fa, rin, rout, ck);
-  if (e != cudaSuccess && pdl_mode == -1) {
+  if (e != cudaSuccess && fi.pdl_mode == -1) {
     cudaGetLastError();  // the attribute pair was refused: cooperative alone from now on
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, fa, rin, rout, ck);
-    if (e == cudaSuccess) pdl_mode = 0;
-  } else if (e == cudaSuccess && pdl_mode == -1) {
-    pdl_mode = 1;
+    if (e == cudaSuccess) fi.pdl_mode = 0;
+  } else if (e == cudaSuccess && fi.pdl_mode == -1) {
+    fi.pdl_mode = 1;
   }
   trace_post(K_DECODE_FUSED, st);
   return e;
@@ -1114,17 +1181,8 @@ cudaError_t launch_decode_fused(const FusedStepArgs& fa, bool fp8, cudaStream_t 
   return fp8 ? launch_fused_one<true>(fa, s) : launch_fused_one<false>(fa, s);
 }
 
-int status_gemv_mma(int clear) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
-  if (clear) {
-    const int z = 0;
-    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
-    // a timed-out grid barrier may have left arrivals behind
-    const unsigned zb[2] = {0u, 0u};
-    cudaMemcpyToSymbol(g_fused_bar, zb, sizeof(zb));
-  }
-  return v;
-}
+int status_gemv_mma(int clear) { return tu_status(clear); }
+
+cudaError_t wait_limit_gemv_mma(long long cycles) { return tu_set_wait_limit(cycles); }
 
 }  // namespace m2

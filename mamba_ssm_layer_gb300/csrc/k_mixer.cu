@@ -634,14 +634,8 @@ cudaError_t launch_prep(const PrepArgs& a0, cudaStream_t s) {
   return e;
 }
 
-int status_mixer(int clear) {
-  int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
-  if (clear) {
-    const int z = 0;
-    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
-  }
-  return v;
-}
+int status_mixer(int clear) { return tu_status(clear); }
+
+cudaError_t wait_limit_mixer(long long cycles) { return tu_set_wait_limit(cycles); }
 
 }  // namespace m2

@@ -23,6 +23,7 @@
 
 #include "m2_common.cuh"
 #include "m2_kernels.h"
+#include "m2_tc.cuh"
 
 namespace m2 {
 
@@ -528,6 +529,331 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_mma_kernel(const SsdArgs 
   }
 }
 
+// ------------------------------------------------------------------ tcgen05 chunk kernels
+//
+// The chunk products of the 128-state shape on the 5th-generation tensor
+// cores: operands in shared memory in the K-major, 128-byte-swizzled layout
+// (sw128_desc), one thread issuing tcgen05.mma (kind::f16, bf16 operands,
+// fp32 accumulation in tensor memory), four warps draining tensor memory
+// (warp w reads lanes 32w..32w+31).  Operand rounding as in the warp-MMA
+// kernels: x, B, C enter exactly; the fp32 operands (the decay-weighted L,
+// w_s x_s, h_in) as hi + lo bf16 pairs, two MMAs each.
+//   state: dH^T [n][p] = B^T [n][s] (w x)^T [p][s]^T   (M = 128 n, N = P, K = 128 s)
+//   out:   S = C [t][n] B [s][n]^T                      (M = 128 t, N = 128 s, K = 128 n)
+//          Yi = C [t][n] h_in [p][n]^T                  (N = P, K = 128 n)
+//          Y  = L [t][s] x^T [p][s]^T                   (N = P, K = 128 s), L = mask(S) * exp(s_t - s_s) * dt_s
+// Every wait is bounded; the issuing thread drains its MMAs before tensor
+// memory is freed.
+constexpr int kSsdTcThreads = 128;
+
+// Stores the 8 bf16 values v[0..7] of K positions k0..k0+7 of row r of a
+// K-major swizzled tile of R rows (k0 % 8 == 0).
+__device__ __forceinline__ void sw_store8(uint8_t* tile, int R, int r, int k0, const uint4& v) {
+  *reinterpret_cast<uint4*>(tile + sw128_chunk(R, r, k0 >> 3)) = v;
+}
+// Stores one bf16 value at (row r, position k).
+__device__ __forceinline__ void sw_store1(uint8_t* tile, int R, int r, int k, uint16_t v) {
+  *reinterpret_cast<uint16_t*>(tile + sw128_chunk(R, r, k >> 3) + (k & 7) * 2) = v;
+}
+
+// 8 fp32 values -> hi and lo bf16 parts, v = hi + lo (packed in pairs).
+__device__ __forceinline__ void split8(const float (&v)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split2(v[2 * i], v[2 * i + 1], h[i], l[i]);
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// MMAs of an M = 128 tile: K = 128 (8 steps of 16) from K-major swizzled A
+// (128 rows) and B (NB rows) into tensor memory at d; accumulate onto d when
+// acc0 (else the first step overwrites).
+__device__ __forceinline__ void tc_mma_k128(uint32_t d, const uint8_t* A, const uint8_t* B, int NB, uint32_t idesc,
+                                            int acc0) {
+  const uint32_t a0 = smem_addr(A), b0 = smem_addr(B);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int atom = kk >> 2, within = (kk & 3) * 32;
+    tc_mma(d, sw128_desc(a0 + atom * 128 * 128 + within), sw128_desc(b0 + atom * NB * 128 + within), idesc,
+           (acc0 || kk > 0) ? 1 : 0);
+  }
+}
+
+template <int P>
+__global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_state_tc_kernel(const SsdArgs a) {
+  constexpr int N = 128;
+  const int h = blockIdx.x, c = blockIdx.y;
+  int seq, t0, qc;
+  chunk_info(a, c, seq, t0, qc);
+  const int g = h / (a.H / a.G);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ float dt_s[kQ], cs_s[kQ];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ uint32_t tmem_slot;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Bt = sm;                   // B^T [128 n][128 s]
+  uint8_t* Wh = Bt + N * kQ * 2;      // (w x)^T hi [P][128 s]
+  uint8_t* Wl = Wh + P * kQ * 2;      // lo
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_slot, P < 32 ? 32 : P);
+  chunk_decay(a, h, t0, qc, dt_s, cs_s);  // ends with __syncthreads
+  const float last = cs_s[max(qc - 1, 0)];
+  // B^T and (w x)^T, zero past the chunk's tokens
+  for (int i = tid; i < kQ * (N / 8); i += kSsdTcThreads) {
+    const int s_ = i / (N / 8), n0 = (i % (N / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (s_ < qc) v = *reinterpret_cast<const uint4*>(a.Bm + (size_t)(t0 + s_) * a.ld_in + (size_t)g * N + n0);
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sw_store1(Bt, N, n0 + 2 * e, s_, (uint16_t)(w4[e] & 0xFFFFu));
+      sw_store1(Bt, N, n0 + 2 * e + 1, s_, (uint16_t)(w4[e] >> 16));
+    }
+  }
+  for (int i = tid; i < kQ * (P / 8); i += kSsdTcThreads) {
+    const int s_ = i / (P / 8), p0 = (i % (P / 8)) * 8;
+    float v[8];
+    if (s_ < qc) {
+      const uint4 xv = *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s_) * a.ld_in + (size_t)h * P + p0);
+      const float w = expf(last - cs_s[s_]) * dt_s[s_];
+      const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = w * bf16lo(x4[e]);
+        v[2 * e + 1] = w * bf16hi(x4[e]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint16_t hi = f32_to_bf16(v[e]);
+      sw_store1(Wh, P, p0 + e, s_, hi);
+      sw_store1(Wl, P, p0 + e, s_, f32_to_bf16(v[e] - bf16_to_f32(hi)));
+    }
+  }
+  fence_proxy_async();  // generic-proxy stores -> visible to the tensor cores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (tid == 0) {
+    constexpr uint32_t idesc = tc_idesc(128, P);
+    tc_mma_k128(tmem, Bt, Wh, P, idesc, 0);
+    tc_mma_k128(tmem, Bt, Wl, P, idesc, 1);
+    tc_commit(&bar);
+  }
+  // tcgen05.ld is warp-collective (.sync.aligned): every lane of a warp takes
+  // the same branch around it
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar, 0));
+  tc_fence_after();
+  if (ok) {
+    // thread (warp w, lane l) holds row n = 32 w + l: P columns
+    const int n = tid;
+    float* out = a.dH + ((size_t)h * a.nchunks + c) * P * N;
+#pragma unroll
+    for (int c0 = 0; c0 < P; c0 += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) out[(size_t)(c0 + j) * N + n] = v[j];
+    }
+  }
+  if (tid == 0) {
+    a.decay[(size_t)h * a.nchunks + c] = expf(last);
+    mbar_drain(&bar, 0);  // no MMA still writes tensor memory when it is freed
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_free(tmem, P < 32 ? 32 : P);
+  }
+}
+
+template <int P>
+__global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_out_tc_kernel(const SsdArgs a) {
+  constexpr int N = 128;
+  constexpr uint32_t kCols = 256;  // S: 128, Yi: P, Y: P
+  const int h = blockIdx.x, c = blockIdx.y;
+  int seq, t0, qc;
+  chunk_info(a, c, seq, t0, qc);
+  const int g = h / (a.H / a.G);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  __shared__ float dt_s[kQ], cs_s[kQ];
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ uint32_t tmem_slot;
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  // 96 KB at P = 64 (two CTAs per SM): the space of C and B takes L once S
+  // and Yi are done, that of h_in takes x^T
+  uint8_t* Cs = sm;                   // C [128 t][128 n], then L hi [128 t][128 s]
+  uint8_t* Bs = Cs + kQ * N * 2;      // B [128 s][128 n], then L lo
+  uint8_t* Hh = Bs + kQ * N * 2;      // h_in hi [P][128 n], then x^T [P][128 s]
+  uint8_t* Hl = Hh + P * N * 2;       // h_in lo
+  uint8_t* Xt = Hh;
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_slot, kCols);
+  chunk_decay(a, h, t0, qc, dt_s, cs_s);
+  // C, B rows (zero past the chunk), x^T, h_in split
+  for (int i = tid; i < kQ * (N / 8); i += kSsdTcThreads) {
+    const int r = i / (N / 8), n0 = (i % (N / 8)) * 8;
+    uint4 cv = make_uint4(0u, 0u, 0u, 0u), bv = cv;
+    if (r < qc) {
+      const size_t row = (size_t)(t0 + r) * a.ld_in + (size_t)g * N + n0;
+      cv = *reinterpret_cast<const uint4*>(a.Cm + row);
+      bv = *reinterpret_cast<const uint4*>(a.Bm + row);
+    }
+    sw_store8(Cs, kQ, r, n0, cv);
+    sw_store8(Bs, kQ, r, n0, bv);
+  }
+  const float* hin = a.dH + ((size_t)h * a.nchunks + c) * P * N;
+  for (int i = tid; i < P * (N / 8); i += kSsdTcThreads) {
+    const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
+    const float4 f0 = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0);
+    const float4 f1 = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0 + 4);
+    const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    uint4 hi, lo;
+    split8(v, hi, lo);
+    sw_store8(Hh, P, pp, n0, hi);
+    sw_store8(Hl, P, pp, n0, lo);
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t tS = tmem, tYi = tmem + 128, tY = tmem + 128 + P;
+  if (tid == 0) {
+    tc_mma_k128(tS, Cs, Bs, kQ, tc_idesc(128, 128), 0);  // S = C B^T
+    tc_mma_k128(tYi, Cs, Hh, P, tc_idesc(128, P), 0);    // Yi = C h_in^T
+    tc_mma_k128(tYi, Cs, Hl, P, tc_idesc(128, P), 1);
+    tc_commit(&bar[0]);
+  }
+  // tcgen05.ld is warp-collective (.sync.aligned): every lane of a warp loads,
+  // whatever its own row; only stores depend on the row
+  bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[0], 0));
+  tc_fence_after();
+  // x^T into the space of h_in (no longer read)
+  for (int i = tid; i < kQ * (P / 8); i += kSsdTcThreads) {
+    const int s_ = i / (P / 8), p0 = (i % (P / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (s_ < qc) v = *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s_) * a.ld_in + (size_t)h * P + p0);
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sw_store1(Xt, P, p0 + 2 * e, s_, (uint16_t)(w4[e] & 0xFFFFu));
+      sw_store1(Xt, P, p0 + 2 * e + 1, s_, (uint16_t)(w4[e] >> 16));
+    }
+  }
+  // L row t = 32 w + l (C and B are no longer read: their space takes L)
+  const int t = tid;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  {
+    const float cst = cs_s[t];
+#pragma unroll 1
+    for (int s0 = 0; s0 < kQ; s0 += 16) {
+      float v[16];
+      if (ok) {
+        tmem_ld16(tS + lane_base + s0, v);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float l8[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int s_ = s0 + 8 * half + j;
+          l8[j] = (s_ <= t) ? v[8 * half + j] * expf(cst - cs_s[s_]) * dt_s[s_] : 0.0f;
+        }
+        uint4 hi, lo;
+        split8(l8, hi, lo);
+        sw_store8(Cs, kQ, t, s0 + 8 * half, hi);
+        sw_store8(Bs, kQ, t, s0 + 8 * half, lo);
+      }
+    }
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (tid == 0) {
+    tc_mma_k128(tY, Cs, Xt, P, tc_idesc(128, P), 0);  // Y = L x
+    tc_mma_k128(tY, Bs, Xt, P, tc_idesc(128, P), 1);
+    tc_commit(&bar[1]);
+  }
+  ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], 0)) && ok;
+  tc_fence_after();
+  if (ok) {
+    const bool live = t < qc;
+    const float Dh = a.D[h];
+    const float ex = expf(cs_s[t]);
+    const uint16_t* xr = a.x + (size_t)(t0 + (live ? t : 0)) * a.ld_in + (size_t)h * P;
+    float* yo = a.y + (size_t)(t0 + t) * a.ldy + (size_t)h * P;
+#pragma unroll
+    for (int c0 = 0; c0 < P; c0 += 16) {
+      float y1[16], yi[16];
+      tmem_ld16(tY + lane_base + c0, y1);
+      tmem_ld16(tYi + lane_base + c0, yi);
+      if (!live) continue;
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        const uint2 xx = *reinterpret_cast<const uint2*>(xr + c0 + j);
+        float4 r;
+        r.x = y1[j] + ex * yi[j] + Dh * bf16lo(xx.x);
+        r.y = y1[j + 1] + ex * yi[j + 1] + Dh * bf16hi(xx.x);
+        r.z = y1[j + 2] + ex * yi[j + 2] + Dh * bf16lo(xx.y);
+        r.w = y1[j + 3] + ex * yi[j + 3] + Dh * bf16hi(xx.y);
+        *reinterpret_cast<float4*>(yo + c0 + j) = r;
+      }
+    }
+  }
+  if (tid == 0) mbar_drain(&bar[1], 0);  // no MMA still writes tensor memory when it is freed
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_free(tmem, kCols);
+  }
+}
+
+template <int P>
+constexpr int ssd_state_tc_smem() { return (128 * kQ + 2 * P * kQ) * 2 + 1024; }
+template <int P>
+constexpr int ssd_out_tc_smem() { return (2 * kQ * 128 + 2 * P * 128) * 2 + 1024; }
+
+template <int P>
+static cudaError_t launch_ssd_tc_t(const SsdArgs& a, const dim3& grid, int which, cudaStream_t s) {
+  static int done_s[64], done_o[64];
+  if (which == 0) {
+    constexpr int smem = ssd_state_tc_smem<P>();
+    cudaError_t e = set_smem_once((const void*)ssd_state_tc_kernel<P>, smem, done_s);
+    if (e != cudaSuccess) return e;
+    ssd_state_tc_kernel<P><<<grid, kSsdTcThreads, smem, s>>>(a);
+  } else {
+    constexpr int smem = ssd_out_tc_smem<P>();
+    cudaError_t e = set_smem_once((const void*)ssd_out_tc_kernel<P>, smem, done_o);
+    if (e != cudaSuccess) return e;
+    ssd_out_tc_kernel<P><<<grid, kSsdTcThreads, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+// Shapes on the tcgen05 chunk kernels: 128 states (M = 128 for the state
+// product), head dims 32 and 64.
+static bool ssd_tc_shape(int P, int N) { return N == 128 && (P == 64 || P == 32); }
+
 template <int P, int N>
 constexpr int ssd_state_mma_smem() { return (kQ * (N + 8) + 2 * kQ * (P + 8)) * 2; }
 template <int P, int N>
@@ -594,9 +920,12 @@ cudaError_t launch_ssd(const SsdArgs& a0, cudaStream_t s) {
   e = set_smem_once((const void*)ssd_chunk_out_kernel, smem_out, done_out);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.H, a.nchunks);
+  const bool tc = ssd_tc_shape(a.P, a.N);
   const bool mma = ssd_mma_shape(a.P, a.N);
   trace_pre(K_SSD_CHUNK_STATE, s);
-  if (mma) {
+  if (tc) {
+    e = a.P == 64 ? launch_ssd_tc_t<64>(a, grid, 0, s) : launch_ssd_tc_t<32>(a, grid, 0, s);
+  } else if (mma) {
     e = launch_ssd_mma(a, grid, 0, s);
   } else {
     ssd_chunk_state_kernel<<<grid, kSsdThreads, smem_state, s>>>(a);
@@ -610,7 +939,9 @@ cudaError_t launch_ssd(const SsdArgs& a0, cudaStream_t s) {
   trace_post(K_SSD_STATE_PASS, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   trace_pre(K_SSD_CHUNK_OUT, s);
-  if (mma) {
+  if (tc) {
+    e = a.P == 64 ? launch_ssd_tc_t<64>(a, grid, 1, s) : launch_ssd_tc_t<32>(a, grid, 1, s);
+  } else if (mma) {
     e = launch_ssd_mma(a, grid, 1, s);
   } else {
     ssd_chunk_out_kernel<<<grid, kSsdThreads, smem_out, s>>>(a);

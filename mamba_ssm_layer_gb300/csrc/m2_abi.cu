@@ -1,6 +1,7 @@
 // m2_abi.cu -- the exported C ABI (include/mamba2.h): host-side validation,
 // workspace carving, the launch sequence of the decode and prefill paths,
 // launch counting, per-kernel event tracing and the device status word.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -77,7 +78,7 @@ static const char* kNames[K_COUNT] = {
     "gemv_bf16",     "gemv_bf16_inproj_conv", "gemv_bf16_outproj_resid", "conv_update",
     "conv_pos",      "ssm_step",        "conv_prefill",    "ssm_scan_seq",
     "gemm_tc",       "ssd_chunk_state", "ssd_state_pass",  "ssd_chunk_out",   "gemm_tc_reduce",
-    "conv_ring_store", "decode_step_fused", "copy"};
+    "conv_ring_store", "decode_step_fused", "copy", "wait_check"};
 
 // ------------------------------------------------------------------ helpers
 
@@ -141,18 +142,28 @@ static size_t proj_part_bytes(const m2_dims& d, int M) {
   return rup(a > b ? a : b, 256);
 }
 
+// Byte offsets of the decode workspace regions for B rows (each 256-aligned):
+// xn [B][hidden] (2 B), zxu [B][ldz] bf16 (z | conv output u | dt), y
+// [B][d_inner] fp32, g [B][d_inner] (2 B), unscale [2][B] fp32, then the
+// optional k-split partials of the tensor-core projections at `end`.
+struct DecodeMap {
+  size_t xn, zxu, y, g, unscale, end;
+};
+static DecodeMap decode_map(const m2_dims& d, int B) {
+  const Derived r = derive(d);
+  DecodeMap m;
+  m.xn = 0;
+  m.zxu = rup(m.xn + (size_t)B * d.hidden * 2, 256);
+  m.y = rup(m.zxu + (size_t)B * r.ldz * 2, 256);
+  m.g = rup(m.y + (size_t)B * r.d_inner * 4, 256);
+  m.unscale = rup(m.g + (size_t)B * r.d_inner * 2, 256);
+  m.end = rup(m.unscale + (size_t)2 * B * 4, 256);
+  return m;
+}
+
 // Decode workspace without (min) and with the tensor-core k-split partials;
 // a workspace between the two runs the projections without the split.
-static size_t decode_ws_min(const m2_dims& d, int B) {
-  const Derived r = derive(d);
-  size_t o = 0;
-  o = rup(o + (size_t)B * d.hidden * 2, 256);
-  o = rup(o + (size_t)B * r.ldz * 2, 256);
-  o = rup(o + (size_t)B * r.d_inner * 4, 256);
-  o = rup(o + (size_t)B * r.d_inner * 2, 256);
-  o = rup(o + (size_t)2 * B * 4, 256);
-  return o;
-}
+static size_t decode_ws_min(const m2_dims& d, int B) { return decode_map(d, B).end; }
 static size_t decode_ws(const m2_dims& d, int B) { return decode_ws_min(d, B) + proj_part_bytes(d, B); }
 
 // Prefill workspace for T token rows in nseq sequences with nchunks SSD chunks
@@ -166,21 +177,39 @@ static size_t q8_bytes(const m2_dims& d, int T) {
   return rup((size_t)T * q8_ldq(d), 256) + rup(q8_ldq(d) / 128 * rup((size_t)T, 128) * 4, 256);
 }
 
-static size_t prefill_ws(const m2_dims& d, int T, int nseq, int nchunks, bool w8a8 = true) {
+// Byte offsets of the prefill workspace regions for T token rows in nseq
+// sequences with nchunks SSD chunks (each region 256-aligned): xn [T][hidden],
+// zx [T][ldz] (raw in_proj output), u [T][d_xbc] (conv output), y [T][d_inner]
+// fp32, g [T][d_inner], unscale [2][T] fp32, the sequence tables (token and
+// chunk offsets), the SSD chunk states and decays, the tensor-core k-split
+// partials, and (W8A8 arm) the E4M3 codes [T][ldq] and scales [K/128][rup(T, 128)].
+struct PrefillMap {
+  size_t xn, zx, u, y, g, unscale, tab, ssd, part, q8, sq, end, end_w8a8;
+};
+static PrefillMap prefill_map(const m2_dims& d, int T, int nseq, int nchunks) {
   const Derived r = derive(d);
-  size_t o = 0;
-  o = rup(o + (size_t)T * d.hidden * 2, 256);   // xn
-  o = rup(o + (size_t)T * r.ldz * 2, 256);      // zx (raw in_proj output)
-  o = rup(o + (size_t)T * r.d_xbc * 2, 256);    // u (conv output)
-  o = rup(o + (size_t)T * r.d_inner * 4, 256);  // y
-  o = rup(o + (size_t)T * r.d_inner * 2, 256);  // g
-  o = rup(o + (size_t)2 * T * 4, 256);          // unscale
-  o = rup(o + (size_t)2 * (nseq + 1) * 4, 256); // token and chunk offsets of the sequences
+  PrefillMap m;
+  m.xn = 0;
+  m.zx = rup(m.xn + (size_t)T * d.hidden * 2, 256);
+  m.u = rup(m.zx + (size_t)T * r.ldz * 2, 256);
+  m.y = rup(m.u + (size_t)T * r.d_xbc * 2, 256);
+  m.g = rup(m.y + (size_t)T * r.d_inner * 4, 256);
+  m.unscale = rup(m.g + (size_t)T * r.d_inner * 2, 256);
+  m.tab = rup(m.unscale + (size_t)2 * T * 4, 256);
+  m.ssd = rup(m.tab + (size_t)2 * (nseq + 1) * 4, 256);
+  m.part = m.ssd;
   if (ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups))
-    o += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
-  o += proj_part_bytes(d, T);  // tensor-core k-split partials
-  if (w8a8) o = rup(o, 256) + q8_bytes(d, T);  // W8A8 activation codes and scales
-  return o;
+    m.part += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);  // chunk states + decays
+  m.end = m.part + proj_part_bytes(d, T);
+  m.q8 = rup(m.end, 256);
+  m.sq = m.q8 + rup((size_t)T * q8_ldq(d), 256);
+  m.end_w8a8 = m.q8 + q8_bytes(d, T);
+  return m;
+}
+
+static size_t prefill_ws(const m2_dims& d, int T, int nseq, int nchunks, bool w8a8 = true) {
+  const PrefillMap m = prefill_map(d, T, nseq, nchunks);
+  return w8a8 ? m.end_w8a8 : m.end;
 }
 static size_t prefill_ws_bound(const m2_dims& d, int T, int nseq, bool w8a8 = true) {
   return prefill_ws(d, T, nseq, (T + 127) / 128 + nseq, w8a8);
@@ -296,20 +325,14 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   const m2_dims& d = *dims;
   const Derived r = derive(d);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  size_t o = 0;
-  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + o);
-  o = rup(o + (size_t)B * d.hidden * 2, 256);
-  uint16_t* zxu = reinterpret_cast<uint16_t*>(w8 + o);
-  o = rup(o + (size_t)B * r.ldz * 2, 256);
-  float* y = reinterpret_cast<float*>(w8 + o);
-  o = rup(o + (size_t)B * r.d_inner * 4, 256);
-  uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
-
-  o = rup(o + (size_t)B * r.d_inner * 2, 256);
-  float* us_in = reinterpret_cast<float*>(w8 + o);
+  const DecodeMap wm = decode_map(d, B);
+  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + wm.xn);
+  uint16_t* zxu = reinterpret_cast<uint16_t*>(w8 + wm.zxu);
+  float* y = reinterpret_cast<float*>(w8 + wm.y);
+  uint16_t* g = reinterpret_cast<uint16_t*>(w8 + wm.g);
+  float* us_in = reinterpret_cast<float*>(w8 + wm.unscale);
   float* us_out = us_in + B;
-  o = rup(o + (size_t)2 * B * 4, 256);
-  float* part = reinterpret_cast<float*>(w8 + o);
+  float* part = reinterpret_cast<float*>(w8 + wm.end);
   const size_t part_bytes = ws_bytes >= decode_ws(d, B) ? proj_part_bytes(d, B) : 0;  // 0: no k split
 
   cudaError_t e;
@@ -384,6 +407,8 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
   {
     // the SSM kernel starts while the in_proj drains and moves little data
     // itself: it pulls the out_proj weights into L2 for the GEMV two launches on
+    // (pulling them, and the state, in from the in_proj's producer instead
+    // measured slower: 32.7 against 31.8 us per step)
     const m2_weight& wo = L->out_proj;
     const size_t wo_bytes = (size_t)wo.n * wo.k * (wo.fmt == M2_W_BF16 ? 2 : 1);
     if (wo_bytes <= (64ull << 20)) {
@@ -466,35 +491,25 @@ static int prefill_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     return M2_ERR_WORKSPACE;
   const Derived r = derive(d);
   uint8_t* w8 = static_cast<uint8_t*>(ws);
-  size_t o = 0;
-  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + o);
-  o = rup(o + (size_t)T * d.hidden * 2, 256);
-  uint16_t* zx = reinterpret_cast<uint16_t*>(w8 + o);
-  o = rup(o + (size_t)T * r.ldz * 2, 256);
-  uint16_t* u = reinterpret_cast<uint16_t*>(w8 + o);
-  o = rup(o + (size_t)T * r.d_xbc * 2, 256);
-  float* y = reinterpret_cast<float*>(w8 + o);
-  o = rup(o + (size_t)T * r.d_inner * 4, 256);
-  uint16_t* g = reinterpret_cast<uint16_t*>(w8 + o);
-
-  o = rup(o + (size_t)T * r.d_inner * 2, 256);
-  float* us_in = reinterpret_cast<float*>(w8 + o);
+  const PrefillMap wm = prefill_map(d, T, nseq, nchunks);
+  uint16_t* xn = reinterpret_cast<uint16_t*>(w8 + wm.xn);
+  uint16_t* zx = reinterpret_cast<uint16_t*>(w8 + wm.zx);
+  uint16_t* u = reinterpret_cast<uint16_t*>(w8 + wm.u);
+  float* y = reinterpret_cast<float*>(w8 + wm.y);
+  uint16_t* g = reinterpret_cast<uint16_t*>(w8 + wm.g);
+  float* us_in = reinterpret_cast<float*>(w8 + wm.unscale);
   float* us_out = us_in + T;
-  o = rup(o + (size_t)2 * T * 4, 256);
-  int32_t* dtab = reinterpret_cast<int32_t*>(w8 + o);  // cu, then chunk offsets
-  o = rup(o + (size_t)2 * (nseq + 1) * 4, 256);
+  int32_t* dtab = reinterpret_cast<int32_t*>(w8 + wm.tab);  // cu, then chunk offsets
   const bool ssd = ssd_supported(d.nheads, d.head_dim, d.d_state, d.n_groups);
-  float* ssd_dh = reinterpret_cast<float*>(w8 + o);
+  float* ssd_dh = reinterpret_cast<float*>(w8 + wm.ssd);
   float* ssd_decay =
-      reinterpret_cast<float*>(w8 + rup(o + (size_t)nchunks * d.nheads * d.head_dim * d.d_state * 4, 256));
-  if (ssd) o += ssd_workspace_bytes(nchunks, d.nheads, d.head_dim, d.d_state);
-  float* part = reinterpret_cast<float*>(w8 + o);
+      reinterpret_cast<float*>(w8 + rup(wm.ssd + (size_t)nchunks * d.nheads * d.head_dim * d.d_state * 4, 256));
+  float* part = reinterpret_cast<float*>(w8 + wm.part);
   const size_t part_bytes = proj_part_bytes(d, T);
-  o = rup(o + part_bytes, 256);
   // W8A8: E4M3 codes [T][ldq] of the projection inputs, scales [K/128][rup(T, 128)]
-  uint8_t* q8 = w8 + o;
+  uint8_t* q8 = w8 + wm.q8;
   const int ldq = (int)q8_ldq(d);
-  float* sq = reinterpret_cast<float*>(w8 + o + rup((size_t)T * ldq, 256));
+  float* sq = reinterpret_cast<float*>(w8 + wm.sq);
   const int ldsq = (int)rup((size_t)T, 128);
   const bool q_in = w8a8 && L->in_proj.fmt == M2_W_FP8_BLOCK128;
   const bool q_out = w8a8 && L->out_proj.fmt == M2_W_FP8_BLOCK128;
@@ -739,6 +754,34 @@ static const void* device_view(const void* p) {
   return nullptr;
 }
 
+// Whether [p, p + bytes) lies inside one allocation the driver knows: the
+// allocation's address range when the driver reports it, else both ends must
+// be device-accessible at the same offset of one mapping.
+typedef CUresult (*PFN_pointer_get_attribute)(void*, CUpointer_attribute, CUdeviceptr);
+static bool within_one_allocation(const void* p, size_t bytes) {
+  static PFN_pointer_get_attribute fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_pointer_get_attribute>(f);
+  });
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  if (bytes > UINTPTR_MAX - a) return false;
+  if (fn) {
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (fn(&base, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, (CUdeviceptr)a) == CUDA_SUCCESS &&
+        fn(&size, CU_POINTER_ATTRIBUTE_RANGE_SIZE, (CUdeviceptr)a) == CUDA_SUCCESS && size > 0)
+      return a >= (uintptr_t)base && a - (uintptr_t)base <= size && bytes <= size - (a - (uintptr_t)base);
+  }
+  const char* first = static_cast<const char*>(device_view(p));
+  const char* last = static_cast<const char*>(device_view(static_cast<const char*>(p) + bytes - 16));
+  return first && last && last == first + (bytes - 16);
+}
+
 int m2_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
   if (!dst || !src) return M2_ERR_ARG;
   if (bytes == 0) return M2_OK;
@@ -746,6 +789,7 @@ int m2_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
   const void* s = device_view(src);
   void* d = const_cast<void*>(device_view(dst));
   if (!s || !d) return M2_ERR_ARG;
+  if (!within_one_allocation(src, bytes) || !within_one_allocation(dst, bytes)) return M2_ERR_ARG;
   return launch_status(launch_copy16(s, d, bytes / 16, stream));
 }
 
@@ -829,6 +873,55 @@ int m2_device_status(int clear) {
   for (int v : parts)
     if (v != 0) return v;
   return M2_OK;
+}
+
+int m2_workspace_map(const m2_dims* dims, int32_t kind, int32_t n, const int32_t* cu_seqlens, size_t* offsets,
+                     int32_t n_offsets) {
+  if (check_dims(dims) || !offsets || n_offsets < M2_WS_COUNT || n <= 0) return M2_ERR_ARG;
+  for (int i = 0; i < n_offsets; ++i) offsets[i] = SIZE_MAX;
+  if (kind == M2_WS_KIND_DECODE) {
+    const DecodeMap m = decode_map(*dims, n);
+    offsets[M2_WS_XN] = m.xn;
+    offsets[M2_WS_ZX] = m.zxu;
+    offsets[M2_WS_Y] = m.y;
+    offsets[M2_WS_G] = m.g;
+    return M2_OK;
+  }
+  if (kind != M2_WS_KIND_PREFILL && kind != M2_WS_KIND_PREFILL_W8A8) return M2_ERR_ARG;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return M2_ERR_ARG;
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i]) return M2_ERR_ARG;
+  const int T = cu_seqlens[n];
+  if (T <= 0) return M2_ERR_ARG;
+  std::vector<int32_t> tab(2 * (size_t)(n + 1));
+  const int nchunks = ssd_chunk_table(cu_seqlens, n, tab.data());
+  const PrefillMap m = prefill_map(*dims, T, n, nchunks);
+  offsets[M2_WS_XN] = m.xn;
+  offsets[M2_WS_ZX] = m.zx;
+  offsets[M2_WS_U] = m.u;
+  offsets[M2_WS_Y] = m.y;
+  offsets[M2_WS_G] = m.g;
+  if (kind == M2_WS_KIND_PREFILL_W8A8) {
+    offsets[M2_WS_Q8] = m.q8;
+    offsets[M2_WS_SQ] = m.sq;
+  }
+  return M2_OK;
+}
+
+int m2_set_wait_limit(int64_t cycles) {
+  const long long v = cycles > 0 ? (long long)cycles : 4000000000LL;
+  if (wait_limit_gemv(v) != cudaSuccess || wait_limit_gemv_mma(v) != cudaSuccess ||
+      wait_limit_gemm_tc(v) != cudaSuccess || wait_limit_mixer(v) != cudaSuccess) {
+    cudaGetLastError();
+    return M2_ERR_DEVICE;
+  }
+  return M2_OK;
+}
+
+int m2_wait_check(const void* probe, void* out, cudaStream_t stream) {
+  if (!probe || !out) return M2_ERR_ARG;
+  if (!al16(probe) || !al16(out)) return M2_ERR_ALIGN;
+  return launch_status(launch_wait_check(probe, out, stream));
 }
 
 int64_t m2_launch_count(void) { return g_launches.load(); }

@@ -11,14 +11,35 @@ namespace m2 {
 
 // ------------------------------------------------------------------ status
 
-// First in-kernel failure (M2_ERR_TIMEOUT) recorded on this device.  Each
-// translation unit has its own word (no relocatable device code is needed);
-// each defines a host reader (status_<unit>) that m2_device_status() polls.
+// Default limit of a bounded wait, in SM clock cycles (about 2 s): a correct
+// pipeline completes its waits in microseconds.
+constexpr long long kWaitCycles = 4000000000LL;
+
+// First in-kernel failure (M2_ERR_TIMEOUT) recorded on this device, and the
+// limit of the pipeline waits (m2_set_wait_limit).  Each translation unit has
+// its own copies (no relocatable device code is needed); each defines host
+// accessors (status_<unit>, wait_limit_<unit>) built on tu_status and
+// tu_set_wait_limit below.
 namespace {
 __device__ int g_status = 0;
+__device__ long long g_wait_limit = kWaitCycles;
 }
 
 __device__ __forceinline__ void record_timeout() { atomicCAS(&g_status, 0, -8); }
+
+// Host side: this unit's status word (clear != 0 resets it) and wait limit.
+static inline int tu_status(int clear) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof(int)) != cudaSuccess) return -4;
+  if (clear) {
+    const int z = 0;
+    cudaMemcpyToSymbol(g_status, &z, sizeof(int));
+  }
+  return v;
+}
+static inline cudaError_t tu_set_wait_limit(long long cycles) {
+  return cudaMemcpyToSymbol(g_wait_limit, &cycles, sizeof(cycles));
+}
 
 // ------------------------------------------------------------------ bf16
 
@@ -154,32 +175,61 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity to complete.  Returns
-// false (and records M2_ERR_TIMEOUT) if it did not complete within about
-// kWaitCycles SM clocks (~2 s): a correct pipeline completes in microseconds.
-constexpr long long kWaitCycles = 4000000000LL;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Potentially blocking test: the thread may be suspended until the phase
+// completes, for at most about `hint_ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Polls until the phase with the given parity completes or `limit` SM clocks
+// pass; on a timeout records M2_ERR_TIMEOUT and returns false.  Polls suspend
+// the thread (try_wait, at most about 1 us each; the hardware may hold it
+// longer while the phase is pending), except under a limit below 1e6 clocks,
+// where they only test, so that the clock is read often enough to end the wait
+// in time.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, long long limit) {
   const long long t0 = clock64();
+  const bool suspend = limit >= 1000000;
   for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitCycles) break;
+    if (suspend ? mbar_try_wait(bar, parity, 1000u) : mbar_test_wait(bar, parity)) return true;
+    if (clock64() - t0 > limit) break;
   }
   record_timeout();
   return false;
+}
+// Bounded wait of the pipeline (a stage filled, a slot freed, a k block
+// done): gives up after this device's wait limit (default kWaitCycles).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, *reinterpret_cast<volatile long long*>(&g_wait_limit));
+}
+// Wait for this thread's own asynchronous work (copies or MMAs it issued)
+// before the CTA exits or frees what that work writes.  Such work always
+// completes, so the limit is the fixed default, never the (possibly lowered)
+// pipeline limit: a CTA that gave up on its pipeline still leaves nothing in
+// flight behind it.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, kWaitCycles);
 }
 
 // ------------------------------------------------------------------ bulk copy

@@ -32,6 +32,7 @@ enum KernelId : int32_t {
   K_CONV_RING,
   K_DECODE_FUSED,
   K_COPY,
+  K_WAIT_CHECK,
   K_COUNT
 };
 
@@ -45,6 +46,11 @@ int status_gemv(int clear);
 int status_gemv_mma(int clear);
 int status_gemm_tc(int clear);
 int status_mixer(int clear);
+// Setters of each translation unit's pipeline wait limit (SM clock cycles).
+cudaError_t wait_limit_gemv(long long cycles);
+cudaError_t wait_limit_gemv_mma(long long cycles);
+cudaError_t wait_limit_gemm_tc(long long cycles);
+cudaError_t wait_limit_mixer(long long cycles);
 
 // Number of SMs of the current device (cached).
 int num_sms();
@@ -242,6 +248,9 @@ bool gemm_tc_supported(int M, int N, int K, bool fp8);
 int gemm_tc_ksplit(int M, int N, int K);
 size_t gemm_tc_partial_bytes(int M, int N, int K);
 cudaError_t launch_gemm_tc(const GemvArgs& a, bool fp8, cudaStream_t s);
+// The timeout-path check of m2_wait_check (k_gemm_tc.cu): probe and out are
+// 16-byte aligned device addresses of 16 bytes.
+cudaError_t launch_wait_check(const void* probe, void* out, cudaStream_t s);
 
 // Warp-MMA decode GEMV (k_gemv_mma.cu): M <= 8, K % 64 == 0, K <= 8192.
 bool gemv_mma_supported(int M, int K);

@@ -70,3 +70,21 @@ def test_host_staged_decode_loop_matches_runtime_copies():
         outs[form] = (np.stack([o.numpy() for o in host_out]), st[0].cpu().numpy())
     assert np.array_equal(outs["runtime"][0], outs["kernel"][0])
     assert np.array_equal(outs["runtime"][1].view(np.uint8), outs["kernel"][1].view(np.uint8))
+
+
+def test_copy_refuses_a_range_past_the_allocation():
+    # a size no allocation holds: refused on the host before any launch, in
+    # either direction and for device and page-locked host memory alike
+    dev = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    pinned = torch.zeros(4096, dtype=torch.uint8).pin_memory()
+    huge = 1 << 44
+    n0 = abi.m2_launch_count()
+    assert abi.m2_copy(dev, pinned, huge, check=False) == abi.M2_ERR_ARG
+    assert abi.m2_copy(pinned, dev, huge, check=False) == abi.M2_ERR_ARG
+    assert abi.m2_copy(dev, dev, huge, check=False) == abi.M2_ERR_ARG
+    assert abi.m2_launch_count() == n0
+    # in range: still copies
+    pinned[:] = torch.arange(4096, dtype=torch.int32).to(torch.uint8)
+    abi.m2_copy(dev, pinned, 4096)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), pinned)

@@ -27,7 +27,11 @@ def _built():
 
 
 @pytest.mark.parametrize("dims,wl,B", [(synth.TINY, synth.WL_TINY_DECODE, 3),
-                                       (synth.NEMOTRON_H_8B, synth.WL_8B_DECODE_B1, 1)])
+                                       (synth.NEMOTRON_H_8B, synth.WL_8B_DECODE_B1, 1),
+                                       # tensor-core projections, k-split partials in the built-in array
+                                       (synth.NEMOTRON_H_8B, synth.WL_8B_DECODE_B64, 16),
+                                       # the largest batch the built-in array holds for this layer
+                                       (synth.NEMOTRON_H_8B, synth.WL_8B_DECODE_B64, 88)])
 def test_noalloc_decode_matches_workspace_decode(dims, wl, B):
     lay = synth.make_layer(dims, wl)
     dl = DeviceLayer(lay)
