@@ -478,6 +478,243 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ W8A8 kernel
+//
+// The W8A8 product with stages of two k blocks: the weight tiles, the
+// activation codes and the token scales of two k blocks each arrive as ONE
+// tensor copy (3-D boxes for the tiles, a 2-D box for the scales).  A CTA's
+// copy engine takes a roughly fixed time per copy whatever its size, so one
+// copy per operand per k block paced this kernel at about one k block per
+// microsecond; stages of two halve the copies.  Stage slots are freed by their
+// own barriers (a tcgen05.commit after the stage's last k block for the
+// tiles, the epilogue warps for the scales), independent of the per-k-block
+// TMEM barriers, so stages can be deeper than the four TMEM buffers.
+constexpr int kW8Kbs = 2;      // k blocks per stage
+constexpr int kW8Stages = 3;   // weight and activation stages
+constexpr int kW8ScSlots = 4;  // token-scale slots
+
+template <int NT>
+struct W8Layout {
+  static constexpr int kWStage = kW8Kbs * kTcBM * kTcBK;  // E4M3 weight tiles of one stage
+  static constexpr int kAStage = kW8Kbs * NT * kTcBK;     // E4M3 activation tiles
+  static constexpr int kScSlot = kW8Kbs * NT * 4;         // fp32 token scales
+  static constexpr int kW = 0;
+  static constexpr int kA = kW + kW8Stages * kWStage;
+  static constexpr int kSc = kA + kW8Stages * kAStage;
+  static constexpr int kBars = kSc + kW8ScSlots * kScSlot;
+};
+
+struct W8Bars {
+  uint64_t w_full[kW8Stages], w_empty[kW8Stages];
+  uint64_t a_full[kW8Stages], a_empty[kW8Stages];
+  uint64_t sc_full[kW8ScSlots], sc_empty[kW8ScSlots];
+  uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
+  uint32_t tmem_base;
+};
+
+template <int NT>
+constexpr int w8_smem_bytes() {
+  return W8Layout<NT>::kBars + (int)sizeof(W8Bars) + 1024;  // + alignment slack
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmS, const TcArgs ta) {
+  using Lay = W8Layout<NT>;
+  const GemvArgs& a = ta.g;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  W8Bars* bars = reinterpret_cast<W8Bars*>(smem + Lay::kBars);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
+  const int cid = blockIdx.x, ncl = gridDim.x;
+  const int L = a.dconv - 1;
+
+  if (tid == 0) {
+    for (int s = 0; s < kW8Stages; ++s) {
+      mbar_init(&bars->w_full[s], 1);
+      mbar_init(&bars->w_empty[s], 1);
+      mbar_init(&bars->a_full[s], 1);
+      mbar_init(&bars->a_empty[s], 1);
+    }
+    for (int s = 0; s < kW8ScSlots; ++s) {
+      mbar_init(&bars->sc_full[s], 1);
+      mbar_init(&bars->sc_empty[s], kTcEpiWarps);
+    }
+    for (int b = 0; b < kTcTmemBufs; ++b) {
+      mbar_init(&bars->mma_done[b], 1);
+      mbar_init(&bars->tmem_empty[b], kTcEpiWarps);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&bars->tmem_base, kTcTmemBufs * NT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  bool dead = false;
+
+  if (warp == 0) {
+    // -------------------------------------------------------- weight producer
+    if (lane == 0) {
+      const uint64_t polw = policy_evict_normal();  // weight tiles are re-read by the token tiles
+      int gs = 0;
+      for (int item = cid; item < nitems && !dead; item += ncl) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
+          const int s = gs % kW8Stages;
+          if (gs >= kW8Stages && !mbar_wait(&bars->w_empty[s], ((gs / kW8Stages) - 1) & 1)) dead = true;
+          if (dead) break;
+          // two k blocks per copy (past the tensor's k extent: zeros; past the
+          // item's range: loaded, unused); the whole box counts
+          mbar_arrive_expect_tx(&bars->w_full[s], Lay::kWStage);
+          tma_load_3d(smem + Lay::kW + s * Lay::kWStage, &tmW, 0, nt * kTcBM, kb, &bars->w_full[s], polw);
+        }
+      }
+      for (int k = max(0, gs - kW8Stages); k < gs; ++k)
+        if (!mbar_drain(&bars->w_full[k % kW8Stages], (k / kW8Stages) & 1)) break;
+    }
+  } else if (warp == kTcAWarp) {
+    // -------------------------------------------------------- activation producer
+    pdl_wait();  // the codes and scales are written by the previous kernel
+    if (lane == 0) {
+      const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
+      int gs = 0, a_iss = 0, sc_iss = 0;
+      for (int item = cid; item < nitems && !dead; item += ncl) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
+          const int sa = gs % kW8Stages, ss = gs % kW8ScSlots;
+          if (gs >= kW8Stages && !mbar_wait(&bars->a_empty[sa], ((gs / kW8Stages) - 1) & 1)) dead = true;
+          if (dead) break;
+          mbar_arrive_expect_tx(&bars->a_full[sa], Lay::kAStage);
+          tma_load_3d(smem + Lay::kA + sa * Lay::kAStage, &tmA, 0, mt * NT, kb, &bars->a_full[sa], pola);
+          a_iss = gs + 1;
+          if (gs >= kW8ScSlots && !mbar_wait(&bars->sc_empty[ss], ((gs / kW8ScSlots) - 1) & 1)) dead = true;
+          if (dead) break;
+          mbar_arrive_expect_tx(&bars->sc_full[ss], Lay::kScSlot);
+          tma_load_2d(smem + Lay::kSc + ss * Lay::kScSlot, &tmS, mt * NT, kb, &bars->sc_full[ss], pola);
+          sc_iss = gs + 1;
+        }
+      }
+      for (int k = max(0, a_iss - kW8Stages); k < a_iss; ++k)
+        if (!mbar_drain(&bars->a_full[k % kW8Stages], (k / kW8Stages) & 1)) break;
+      for (int k = max(0, sc_iss - kW8ScSlots); k < sc_iss; ++k)
+        if (!mbar_drain(&bars->sc_full[k % kW8ScSlots], (k / kW8ScSlots) & 1)) break;
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc8 = tc_idesc_f8(kTcBM, NT);
+      int gs = 0, gk = 0;
+      for (int item = cid; item < nitems && !dead; item += ncl) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
+          const int s = gs % kW8Stages, nk = min(kW8Kbs, kb1 - kb);
+          if (!mbar_wait(&bars->w_full[s], (gs / kW8Stages) & 1)) dead = true;
+          if (!dead && !mbar_wait(&bars->a_full[s], (gs / kW8Stages) & 1)) dead = true;
+          for (int i = 0; i < nk && !dead; ++i, ++gk) {
+            const int tb = gk % kTcTmemBufs;
+            if (gk >= kTcTmemBufs && !mbar_wait(&bars->tmem_empty[tb], ((gk / kTcTmemBufs) - 1) & 1)) dead = true;
+            if (dead) break;
+            tc_fence_after();
+            const uint32_t wb = smem_addr(smem + Lay::kW + s * Lay::kWStage + i * kTcBM * kTcBK);
+            const uint32_t ab = smem_addr(smem + Lay::kA + s * Lay::kAStage + i * NT * kTcBK);
+#pragma unroll
+            for (int kk = 0; kk < kTcBK / 32; ++kk)
+              tc_mma_f8(tmem + tb * NT, sw128_desc(wb + kk * 32), sw128_desc(ab + kk * 32), idesc8, kk > 0 ? 1 : 0);
+            tc_commit(&bars->mma_done[tb]);  // frees the TMEM partial for the epilogue
+          }
+          if (dead) break;
+          tc_commit(&bars->w_empty[s]);  // the stage's tiles are read once its last MMAs complete
+          tc_commit(&bars->a_empty[s]);
+        }
+      }
+      if (gk > 0) mbar_drain(&bars->mma_done[(gk - 1) % kTcTmemBufs], ((gk - 1) / kTcTmemBufs) & 1);
+    }
+  } else if (warp >= 6 && warp < 6 + kTcEpiWarps) {
+    // -------------------------------------------------------- epilogue
+    constexpr int EPG = kTcEpiWarps / 4;
+    constexpr int HC = NT / EPG;
+    const int q = warp & 3;
+    const int hf = (warp - 6) >> 2;
+    const int row = 32 * q + lane;
+    pdl_wait();
+    float acc[HC];
+    int gs = 0, gk = 0;
+    for (int item = cid; item < nitems && !dead; item += ncl) {
+      int nt, mt, kb0, kb1;
+      tc_item(ta, item, nt, mt, kb0, kb1);
+      const int ks = item % ta.ksplit;
+#pragma unroll
+      for (int j = 0; j < HC; ++j) acc[j] = 0.0f;
+      for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
+        const int ss = gs % kW8ScSlots, nk = min(kW8Kbs, kb1 - kb);
+        // the TMEM loads below are warp-collective: the warp decides together
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->sc_full[ss], (gs / kW8ScSlots) & 1))) dead = true;
+        for (int i = 0; i < nk && !dead; ++i, ++gk) {
+          const int tb = gk % kTcTmemBufs;
+          const float s = bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb + i));
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1))) dead = true;
+          if (dead) break;
+          tc_fence_after();
+          const uint32_t ta_ = tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC;
+#pragma unroll
+          for (int c0 = 0; c0 < HC; c0 += 16) {
+            float v[16];
+            tmem_ld16(ta_ + c0, v);
+            const uint32_t sq = smem_addr(smem + Lay::kSc + ss * Lay::kScSlot + (i * NT + hf * HC + c0) * 4);
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const float4 t4 = lds_f4_ordered(sq + 16 * i4);
+              acc[c0 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c0 + 4 * i4 + 0]);
+              acc[c0 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c0 + 4 * i4 + 1]);
+              acc[c0 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c0 + 4 * i4 + 2]);
+              acc[c0 + 4 * i4 + 3] = fmaf(s * t4.w, v[4 * i4 + 3], acc[c0 + 4 * i4 + 3]);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sc_empty[ss]);  // this warp is done with the stage's scales
+      }
+      if (dead) break;
+      const int n = nt * kTcBM + row;
+      if (n < a.N) {
+        if (ta.ksplit > 1) {
+          float* pp = ta.part + ((size_t)ks * a.M) * a.N + n;
+#pragma unroll
+          for (int j = 0; j < HC; ++j) {
+            const int m = mt * NT + hf * HC + j;
+            if (m < a.M) pp[(size_t)m * a.N] = acc[j];
+          }
+        } else {
+          const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
+          ConvTaps taps;
+          if (conv) load_taps(a, n - a.xbc0, L, taps);
+#pragma unroll
+          for (int j = 0; j < HC; ++j) {
+            const int m = mt * NT + hf * HC + j;
+            if (m < a.M) tc_epi_elem(a, m, n, acc[j], conv, taps, L);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  pdl_trigger();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_free(tmem, kTcTmemBufs * NT);
+  }
+}
+
 // Split-k reduction: sums the k-split partials of each output in split order
 // (deterministic) and runs the epilogue.
 __global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const GemvArgs a, const float* part, int ksplit) {
@@ -520,6 +757,63 @@ int gemm_tc_ksplit(int M, int N, int K) {
 size_t gemm_tc_partial_bytes(int M, int N, int K) {
   const int ks = gemm_tc_ksplit(M, N, K);
   return ks > 1 ? (size_t)ks * M * N * 4 : 0;
+}
+
+// Host: a 3-D map over a byte matrix of `rows` rows (pitch `ld` bytes) whose
+// first kblocks * 128 bytes are used, taken as {128-byte k block piece, rows,
+// k blocks}: a box {128, box_rows, kbs} lands as kbs consecutive
+// [box_rows][128] tiles, each 128-byte swizzled (the UMMA K-major layout of
+// one k block).  Rows or k blocks past the extents read as zero.
+static bool encode_kblocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t ld, uint64_t kblocks,
+                           uint32_t box_rows, uint32_t kbs) {
+  auto enc = tensor_map_encoder();
+  if (!enc || ld % 16 || ld < kblocks * 128) return false;
+  const cuuint64_t dims[3] = {128, rows, kblocks};
+  const cuuint64_t strides[2] = {ld, 128};
+  const cuuint32_t box[3] = {128, box_rows, kbs};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT>
+static cudaError_t launch_w8a8(const GemvArgs& g, cudaStream_t s) {
+  static int done_mask[64] = {0};
+  CUtensorMap tmW, tmA, tmS;
+  TcArgs ta;
+  ta.g = g;
+  ta.m_tiles = (g.M + NT - 1) / NT;
+  ta.n_tiles = (g.N + kTcBM - 1) / kTcBM;
+  ta.kblocks = (g.K + kTcBK - 1) / kTcBK;
+  ta.fp8 = 1;
+  ta.ksplit = gemm_tc_ksplit(g.M, g.N, g.K);
+  ta.part = g.part;
+  if (ta.ksplit > 1 && (!g.part || g.part_bytes < gemm_tc_partial_bytes(g.M, g.N, g.K))) ta.ksplit = 1;
+  if (!encode_kblocks(&tmW, g.W, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)ta.kblocks, kTcBM, kW8Kbs) ||
+      !encode_kblocks(&tmA, g.q8, (uint64_t)g.M, (uint64_t)g.ldq, (uint64_t)ta.kblocks, NT, kW8Kbs) ||
+      !encode_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.sq, (uint64_t)g.ldsq, (uint64_t)ta.kblocks,
+                 (uint64_t)g.ldsq * 4, NT, kW8Kbs, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const int smem = w8_smem_bytes<NT>();
+  auto kern = gemm_w8a8_kernel<NT>;
+  cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
+  if (e != cudaSuccess) return e;
+  const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
+  int grid = num_sms();
+  if (grid > nitems) grid = nitems;
+  trace_pre(K_GEMM_TC, s);
+  e = launch_k(kern, dim3(grid), dim3(kTcThreads), smem, s, g.pdl != 0, tmW, tmA, tmS, ta);
+  trace_post(K_GEMM_TC, s);
+  if (e != cudaSuccess || ta.ksplit == 1) return e;
+  const size_t total = (size_t)g.M * g.N;
+  int rgrid = (int)((total + 255) / 256);
+  if (rgrid > 8 * num_sms()) rgrid = 8 * num_sms();
+  trace_pre(K_GEMM_TC_REDUCE, s);
+  e = launch_k(gemm_tc_reduce_kernel, dim3(rgrid), dim3(256), 0, s, g.pdl != 0, g, (const float*)ta.part,
+               ta.ksplit);
+  trace_post(K_GEMM_TC_REDUCE, s);
+  return e;
 }
 
 template <int NT, bool AQ8>
@@ -623,8 +917,8 @@ cudaError_t launch_wait_check(const void* probe, void* out, cudaStream_t s) {
 cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   if (g.q8) {  // W8A8: E4M3 activation codes with per-(token, k block) scales
     if (!fp8 || g.K % 128 || g.ldq % 16 || g.ldsq % 128) return cudaErrorInvalidValue;
-    if (tc_nt(g.M) == 64) return launch_tc<64, true>(g, fp8, s);
-    return launch_tc<128, true>(g, fp8, s);
+    if (tc_nt(g.M) == 64) return launch_w8a8<64>(g, s);
+    return launch_w8a8<128>(g, s);
   }
   if (tc_nt(g.M) == 64) return launch_tc<64, false>(g, fp8, s);
   return launch_tc<128, false>(g, fp8, s);

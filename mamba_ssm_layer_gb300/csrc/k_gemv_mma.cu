@@ -137,12 +137,35 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // product times the norm factor, enlarged by 2^-20 so that it never falls
 // below the largest rounded output: the rows' maximum lands in [2^13, 2^15)
 // and every bf16 value within 2^30 of it stays exact in f16.
+// The norm's inputs that never come from the immediately preceding kernel:
+// the weight, and (gated norm) z, which the in_proj two launches back wrote.
+// Loaded before the dependency wait, so that their latency -- long while the
+// weight stream fills the memory system -- overlaps the wait.
+constexpr int kNormPer = 2;  // 16-byte chunks of 8 elements per thread (K <= 8192 with 512 threads)
+struct NormPre {
+  uint4 wv[kNormPer], zv[kNormPer];
+  bool w, z;  // which of them are loaded
+};
+__device__ __forceinline__ void norm_preload(const GemvArgs& a, int m, int tid, int nC, bool z, NormPre& pre) {
+#pragma unroll
+  for (int c = 0; c < kNormPer; ++c) {
+    const int k0 = (tid + nC * c) * 8;
+    pre.wv[c] = pre.zv[c] = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 < a.K) {
+      pre.wv[c] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + k0));
+      if (z && a.norm == NORM_GATED) pre.zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
+    }
+  }
+  pre.w = true;
+  pre.z = z && a.norm == NORM_GATED;
+}
+
 template <bool F16>
 __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* red, float* unscale, int tid,
-                               int nC) {
+                               int nC, const NormPre* pre = nullptr) {
   const int K = a.K, warp = tid >> 5, lane = tid & 31;
   const int nw = nC / 32;
-  constexpr int kPer = 2;  // 16-byte chunks of 8 elements per thread (K <= 8192 with 512 threads)
+  constexpr int kPer = kNormPer;
   float v[kPer * 8];
   uint4 wv[kPer], zv[kPer];
 #pragma unroll
@@ -152,7 +175,7 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
     if (k0 < K) {
-      wv[c] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + k0));
+      wv[c] = (pre && pre->w) ? pre->wv[c] : __ldg(reinterpret_cast<const uint4*>(a.norm_w + k0));
       if (a.norm == NORM_RMS) {
         const uint4 u = *reinterpret_cast<const uint4*>(a.A + (size_t)m * a.lda + k0);  // coherent: previous kernel
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
@@ -162,7 +185,7 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
           v[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
         }
       } else {
-        zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
+        zv[c] = (pre && pre->z && m == 0) ? pre->zv[c] : __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
         // L2 loads: y may come from other CTAs of the same launch (fused step)
         const float4 f0 = __ldcg(reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0));
         const float4 f1 = __ldcg(reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0 + 4));
@@ -453,6 +476,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       rsS[m * rows_max + r] = __ldcg(a.resid + (size_t)m * a.ldr + row_begin + r);
     }
   }
+  NormPre pre;
+  if (a.norm != NORM_NONE) norm_preload(a, 0, tid, kC, mvalid == 1, pre);  // before the wait
   pdl_wait();
   pdl_trigger();
   for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
@@ -462,7 +487,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     // the activation rows are this kernel's own norm of its inputs
     float* red = tot;  // scratch: tot is zeroed again below
     for (int m = 0; m < mvalid; ++m)
-      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, tail->unscale, tid, kC);
+      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, tail->unscale, tid, kC, &pre);
     for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
     named_bar(1, kC);
   } else {

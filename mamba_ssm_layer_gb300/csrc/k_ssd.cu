@@ -544,16 +544,36 @@ __global__ void __launch_bounds__(kSsdThreads) ssd_out_mma_kernel(const SsdArgs 
 //          Y  = L [t][s] x^T [p][s]^T                   (N = P, K = 128 s), L = mask(S) * exp(s_t - s_s) * dt_s
 // Every wait is bounded; the issuing thread drains its MMAs before tensor
 // memory is freed.
-constexpr int kSsdTcThreads = 128;
+constexpr int kSsdTcThreads = 128;     // state kernel: 4 warps, one per TMEM lane quarter
+constexpr int kSsdTcOutThreads = 256;  // output kernel: 8 warps, two per lane quarter (column halves)
 
 // Stores the 8 bf16 values v[0..7] of K positions k0..k0+7 of row r of a
 // K-major swizzled tile of R rows (k0 % 8 == 0).
 __device__ __forceinline__ void sw_store8(uint8_t* tile, int R, int r, int k0, const uint4& v) {
   *reinterpret_cast<uint4*>(tile + sw128_chunk(R, r, k0 >> 3)) = v;
 }
-// Stores one bf16 value at (row r, position k).
-__device__ __forceinline__ void sw_store1(uint8_t* tile, int R, int r, int k, uint16_t v) {
-  *reinterpret_cast<uint16_t*>(tile + sw128_chunk(R, r, k >> 3) + (k & 7) * 2) = v;
+// 8 x 8 block of 16-bit values: in[r] holds row r (8 values, packed in
+// pairs), out[c] receives column c (the 8 rows' values).
+__device__ __forceinline__ void transpose8x8(const uint4 (&in)[8], uint4 (&out)[8]) {
+  uint32_t w[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    w[r][0] = in[r].x;
+    w[r][1] = in[r].y;
+    w[r][2] = in[r].z;
+    w[r][3] = in[r].w;
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // rows 2j and 2j+1 of column c: low or high half of word c/2
+      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+      o[j] = __byte_perm(w[2 * j][c >> 1], w[2 * j + 1][c >> 1], sel);
+    }
+    out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // 8 fp32 values -> hi and lo bf16 parts, v = hi + lo (packed in pairs).
@@ -602,39 +622,49 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_state_tc_kernel(const Ss
   if (warp == 0) tmem_alloc(&tmem_slot, P < 32 ? 32 : P);
   chunk_decay(a, h, t0, qc, dt_s, cs_s);  // ends with __syncthreads
   const float last = cs_s[max(qc - 1, 0)];
-  // B^T and (w x)^T, zero past the chunk's tokens
-  for (int i = tid; i < kQ * (N / 8); i += kSsdTcThreads) {
-    const int s_ = i / (N / 8), n0 = (i % (N / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (s_ < qc) v = *reinterpret_cast<const uint4*>(a.Bm + (size_t)(t0 + s_) * a.ld_in + (size_t)g * N + n0);
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  // B^T and (w x)^T, zero past the chunk's tokens, in 8 x 8 blocks (16-byte
+  // loads, a register transpose, 16-byte stores; block (sb, nb) of a thread:
+  // the eight lanes of a store phase hold eight different sb, so their
+  // swizzled chunks differ)
+  for (int i = tid; i < (kQ / 8) * (N / 8); i += kSsdTcThreads) {
+    const int s0 = (i % (kQ / 8)) * 8, n0 = (i / (kQ / 8)) * 8;
+    uint4 rows[8], cols[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sw_store1(Bt, N, n0 + 2 * e, s_, (uint16_t)(w4[e] & 0xFFFFu));
-      sw_store1(Bt, N, n0 + 2 * e + 1, s_, (uint16_t)(w4[e] >> 16));
-    }
+    for (int r = 0; r < 8; ++r)
+      rows[r] = s0 + r < qc ? *reinterpret_cast<const uint4*>(a.Bm + (size_t)(t0 + s0 + r) * a.ld_in + (size_t)g * N + n0)
+                            : make_uint4(0u, 0u, 0u, 0u);
+    transpose8x8(rows, cols);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) sw_store8(Bt, N, n0 + c, s0, cols[c]);
   }
-  for (int i = tid; i < kQ * (P / 8); i += kSsdTcThreads) {
-    const int s_ = i / (P / 8), p0 = (i % (P / 8)) * 8;
-    float v[8];
-    if (s_ < qc) {
-      const uint4 xv = *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s_) * a.ld_in + (size_t)h * P + p0);
-      const float w = expf(last - cs_s[s_]) * dt_s[s_];
-      const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
+  for (int i = tid; i < (kQ / 8) * (P / 8); i += kSsdTcThreads) {
+    const int s0 = (i % (kQ / 8)) * 8, p0 = (i / (kQ / 8)) * 8;
+    uint4 rh[8], rl[8], ch[8], cl[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[2 * e] = w * bf16lo(x4[e]);
-        v[2 * e + 1] = w * bf16hi(x4[e]);
+    for (int r = 0; r < 8; ++r) {
+      const int s_ = s0 + r;
+      float v[8];
+      if (s_ < qc) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s_) * a.ld_in + (size_t)h * P + p0);
+        const float w = expf(last - cs_s[s_]) * dt_s[s_];
+        const uint32_t x4[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] = w * bf16lo(x4[e]);
+          v[2 * e + 1] = w * bf16hi(x4[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.0f;
       }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+      split8(v, rh[r], rl[r]);
     }
+    transpose8x8(rh, ch);
+    transpose8x8(rl, cl);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint16_t hi = f32_to_bf16(v[e]);
-      sw_store1(Wh, P, p0 + e, s_, hi);
-      sw_store1(Wl, P, p0 + e, s_, f32_to_bf16(v[e] - bf16_to_f32(hi)));
+    for (int c = 0; c < 8; ++c) {
+      sw_store8(Wh, P, p0 + c, s0, ch[c]);
+      sw_store8(Wl, P, p0 + c, s0, cl[c]);
     }
   }
   fence_proxy_async();  // generic-proxy stores -> visible to the tensor cores
@@ -677,7 +707,7 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_state_tc_kernel(const Ss
 }
 
 template <int P>
-__global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_out_tc_kernel(const SsdArgs a) {
+__global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const SsdArgs a) {
   constexpr int N = 128;
   constexpr uint32_t kCols = 256;  // S: 128, Yi: P, Y: P
   const int h = blockIdx.x, c = blockIdx.y;
@@ -705,7 +735,7 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_out_tc_kernel(const SsdA
   if (warp == 0) tmem_alloc(&tmem_slot, kCols);
   chunk_decay(a, h, t0, qc, dt_s, cs_s);
   // C, B rows (zero past the chunk), x^T, h_in split
-  for (int i = tid; i < kQ * (N / 8); i += kSsdTcThreads) {
+  for (int i = tid; i < kQ * (N / 8); i += kSsdTcOutThreads) {
     const int r = i / (N / 8), n0 = (i % (N / 8)) * 8;
     uint4 cv = make_uint4(0u, 0u, 0u, 0u), bv = cv;
     if (r < qc) {
@@ -717,7 +747,7 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_out_tc_kernel(const SsdA
     sw_store8(Bs, kQ, r, n0, bv);
   }
   const float* hin = a.dH + ((size_t)h * a.nchunks + c) * P * N;
-  for (int i = tid; i < P * (N / 8); i += kSsdTcThreads) {
+  for (int i = tid; i < P * (N / 8); i += kSsdTcOutThreads) {
     const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
     const float4 f0 = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0);
     const float4 f1 = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0 + 4);
@@ -743,25 +773,27 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_out_tc_kernel(const SsdA
   // whatever its own row; only stores depend on the row
   bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[0], 0));
   tc_fence_after();
-  // x^T into the space of h_in (no longer read)
-  for (int i = tid; i < kQ * (P / 8); i += kSsdTcThreads) {
-    const int s_ = i / (P / 8), p0 = (i % (P / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (s_ < qc) v = *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s_) * a.ld_in + (size_t)h * P + p0);
-    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+  // x^T into the space of h_in (no longer read), in 8 x 8 blocks
+  for (int i = tid; i < (kQ / 8) * (P / 8); i += kSsdTcOutThreads) {
+    const int s0 = (i % (kQ / 8)) * 8, p0 = (i / (kQ / 8)) * 8;
+    uint4 rows[8], cols[8];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sw_store1(Xt, P, p0 + 2 * e, s_, (uint16_t)(w4[e] & 0xFFFFu));
-      sw_store1(Xt, P, p0 + 2 * e + 1, s_, (uint16_t)(w4[e] >> 16));
-    }
+    for (int r = 0; r < 8; ++r)
+      rows[r] = s0 + r < qc ? *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s0 + r) * a.ld_in + (size_t)h * P + p0)
+                            : make_uint4(0u, 0u, 0u, 0u);
+    transpose8x8(rows, cols);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) sw_store8(Xt, P, p0 + c, s0, cols[c]);
   }
-  // L row t = 32 w + l (C and B are no longer read: their space takes L)
-  const int t = tid;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  // L row t = 32 (w mod 4) + l, columns [64 (w / 4), +64) (C and B are no
+  // longer read: their space takes L)
+  const int q = warp & 3, half = warp >> 2;
+  const int t = 32 * q + (tid & 31);
+  const uint32_t lane_base = (uint32_t)(32 * q) << 16;
   {
     const float cst = cs_s[t];
 #pragma unroll 1
-    for (int s0 = 0; s0 < kQ; s0 += 16) {
+    for (int s0 = 64 * half; s0 < 64 * half + 64; s0 += 16) {
       float v[16];
       if (ok) {
         tmem_ld16(tS + lane_base + s0, v);
@@ -802,7 +834,7 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_out_tc_kernel(const SsdA
     const uint16_t* xr = a.x + (size_t)(t0 + (live ? t : 0)) * a.ld_in + (size_t)h * P;
     float* yo = a.y + (size_t)(t0 + t) * a.ldy + (size_t)h * P;
 #pragma unroll
-    for (int c0 = 0; c0 < P; c0 += 16) {
+    for (int c0 = half * (P / 2); c0 < (half + 1) * (P / 2); c0 += 16) {
       float y1[16], yi[16];
       tmem_ld16(tY + lane_base + c0, y1);
       tmem_ld16(tYi + lane_base + c0, yi);
@@ -845,7 +877,7 @@ static cudaError_t launch_ssd_tc_t(const SsdArgs& a, const dim3& grid, int which
     constexpr int smem = ssd_out_tc_smem<P>();
     cudaError_t e = set_smem_once((const void*)ssd_out_tc_kernel<P>, smem, done_o);
     if (e != cudaSuccess) return e;
-    ssd_out_tc_kernel<P><<<grid, kSsdTcThreads, smem, s>>>(a);
+    ssd_out_tc_kernel<P><<<grid, kSsdTcOutThreads, smem, s>>>(a);
   }
   return cudaGetLastError();
 }
