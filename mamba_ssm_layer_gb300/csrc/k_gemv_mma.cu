@@ -234,20 +234,15 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
       l += red[16 + w];
       pm = fmaxf(pm, red[32 + w]);
     }
-    NormR nr;
-    nr.h = h;
-    nr.l = l;
-    nr.inv_k = a.norm_inv_k;
-    nr.eps = a.norm_eps;
-    const float rf = norm_rf(nr);
-    r = rf;
+    const NormR nr = norm_r(h, l, K, a.norm_eps);
+    r = nr.hi;
 #pragma unroll
     for (int c = 0; c < kPer; ++c) {
       const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        o[c * 8 + 2 * e] = norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, nr);
-        o[c * 8 + 2 * e + 1] = norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, nr);
+        o[c * 8 + 2 * e] = norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), nr);
+        o[c * 8 + 2 * e + 1] = norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), nr);
       }
     }
   } else {

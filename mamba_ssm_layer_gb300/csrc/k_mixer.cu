@@ -288,14 +288,16 @@ __global__ void __launch_bounds__(256) ssm_step_kernel(const SsmArgs a, int pspl
 
 template <int LPR>
 static cudaError_t launch_ssm_lpr(const SsmArgs& a, cudaStream_t s, bool pdl) {
-  // rows per thread: 1 when the batch is small (most CTAs, most loads in
-  // flight), up to 8 when B*H alone fills the GPU
+  // rows per thread: doubled from 1 (up to 8, or one CTA per head) while the
+  // grid has more CTAs than the GPU has SMs
   constexpr int RPW = 32 / LPR;
   const long long heads = (long long)a.B * a.H;
   const int max_rows = (a.P + 8 * RPW - 1) / (8 * RPW);  // rows per thread with one CTA per head
+  // A batch-1 step then leaves each SM room for the next kernel's CTA, which
+  // launches early (programmatic dependent launch) and starts streaming its
+  // weights while this one runs.
   int rows = 1;
-  while (rows < 8 && rows < max_rows && heads * ((a.P + 8 * RPW * rows * 2 - 1) / (8 * RPW * rows * 2)) >= 8LL * num_sms())
-    rows *= 2;
+  while (rows < 8 && rows < max_rows && heads * ((a.P + 8 * RPW * rows - 1) / (8 * RPW * rows)) > num_sms()) rows *= 2;
   const int cta_rows = 8 * RPW * rows;
   const int psplit = (a.P + cta_rows - 1) / cta_rows;
   dim3 grid(a.H * psplit, a.B);
@@ -401,8 +403,8 @@ cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s) {
 // rounded to bf16 (the layer's rounding point), then stored as bf16 or, for an
 // E4M3-weight GEMV, as f16 after the exact row prescale 2^j (max |v| * 2^j in
 // [2^14, 2^15); unscale = 2^-j).  The RMSNorm sum of squares is an error-free
-// fp32 pair and r is evaluated once in double, so its rounding decisions do
-// not depend on the summation order (norm_round_bf16).
+// fp32 pair and r an fp32 pair, so its outputs are the correct roundings of
+// the exact products whatever the summation order (norm_round_bf16).
 constexpr int kPrepMaxPer = 32;  // elements per thread: K <= 32 * threads
 
 // One CTA of kPrepThreads threads per row (128 for K <= 4096, 256 for K <= 8192,
@@ -469,12 +471,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
       s_lo[0] = l;
     }
     __syncthreads();
-    NormR nr;
-    nr.h = s_hi[0];
-    nr.l = s_lo[0];
-    nr.inv_k = a.inv_k;
-    nr.eps = a.eps;
-    const float rf = norm_rf(nr);
+    const NormR nr = norm_r(s_hi[0], s_lo[0], K, a.eps);
 #pragma unroll
     for (int c = 0; c < kPrepMaxPer / 8; ++c) {
       const int k0 = (tid + kPrepThreads * c) * 8;
@@ -483,8 +480,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
         const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), rf, nr));
-          v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), rf, nr));
+          v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), nr));
+          v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), nr));
         }
       }
     }
@@ -623,8 +620,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
 }
 
 cudaError_t launch_prep(const PrepArgs& a0, cudaStream_t s) {
-  PrepArgs a = a0;
-  a.inv_k = 1.0 / (double)a.K;
+  const PrepArgs& a = a0;
   trace_pre(K_PREP, s);
   cudaError_t e;
   if (a.K <= 128 * kPrepMaxPer) e = launch_k(prep_kernel<128>, dim3(a.M), dim3(128), 0, s, a.pdl != 0, a);

@@ -379,7 +379,6 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     ex.norm = NORM_RMS;
     ex.norm_w = L->norm_w;
     ex.norm_eps = d.eps_in;
-    ex.norm_inv_k = 1.0 / (double)d.hidden;
   }
   fa.in = proj_args(L->in_proj, fuse ? hidden : xn, d.hidden, B, zxu, r.ldz, EPI_INPROJ_CONV, nullptr, 0, &ex,
                     fuse ? nullptr : us_in, 1, part, part_bytes);
@@ -423,7 +422,6 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     eo.norm = NORM_GATED;
     eo.norm_w = L->gnorm_w;
     eo.norm_eps = d.eps_gated;
-    eo.norm_inv_k = 1.0 / (double)r.d_inner;
     eo.gy = y;
     eo.ldgy = r.d_inner;
     eo.gz = zxu;

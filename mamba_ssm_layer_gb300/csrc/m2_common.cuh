@@ -81,46 +81,49 @@ __device__ __forceinline__ void two_sum_warp(float& hi, float& lo) {
   }
 }
 
-// Correct rounding of a double to bf16: round to odd at fp32 precision, then
-// to nearest even at bf16 precision (24 >= 8 + 2 bits, so the result equals a
-// single round-to-nearest-even of v).
-static __device__ __noinline__ uint16_t f64_to_bf16_rn(double v) {
-  float f = __double2float_rz(v);
-  if ((double)f != v) f = __uint_as_float(__float_as_uint(f) | 1u);
-  return f32_to_bf16(f);
-}
-
-// r = 1/sqrt(mean + eps) of an RMSNorm row, from its sum of squares held as
-// an fp32 pair (h + l): rf is the fp32 estimate (all threads of a row compute
-// the same one); the double value, ~2^-44 accurate, is evaluated only where a
-// rounding decision needs it.
+// r = 1/sqrt(S/K + eps) of an RMSNorm row as an unevaluated pair hi + lo
+// (relative error about 2^-43), from its sum of squares S = h + l, in fp32
+// arithmetic only: 1/K and S/K carry their fma-exact errors, and one Newton
+// step with an fma-exact residual refines rsqrtf.  Every thread of a row
+// computes the same pair.
 struct NormR {
-  float h, l;     // sum of squares, error-free pair
-  double inv_k;   // 1 / K
-  float eps;
+  float hi, lo;
 };
-__device__ __forceinline__ float norm_rf(const NormR& n) {
-  return rsqrtf((n.h + n.l) * (float)n.inv_k + n.eps);
+__device__ __forceinline__ NormR norm_r(float h, float l, int K, float eps) {
+  const float kf = (float)K;
+  const float ik = __fdiv_rn(1.0f, kf);
+  const float ik_lo = __fdiv_rn(fmaf(-ik, kf, 1.0f), kf);  // 1/K - ik
+  const float m = h * ik;                                   // S/K = m + me
+  const float me = fmaf(h, ik_lo, fmaf(l, ik, fmaf(h, ik, -m)));
+  const float v = m + eps;                                  // S/K + eps = v + ve
+  const float z = v - m;
+  const float ve = ((m - (v - z)) + (eps - z)) + me;
+  const float r0 = rsqrtf(v);
+  const float q = r0 * r0;                                  // r0^2 = q + qe
+  const float qe = fmaf(r0, r0, -q);
+  float d = fmaf(-v, q, 1.0f);                              // 1 - (v + ve) * r0^2
+  d = fmaf(-v, qe, d);
+  d = fmaf(-ve, q, d);
+  NormR r;
+  r.hi = r0;
+  r.lo = 0.5f * r0 * d;
+  return r;
 }
-__device__ __forceinline__ double norm_rd(const NormR& n) {
-  const double v = ((double)n.h + (double)n.l) * n.inv_k + (double)n.eps;
-  const double r0 = (double)rsqrtf((float)v);
-  return r0 * (1.5 - 0.5 * v * r0 * r0);  // one Newton step
-}
-
-// bf16(x * r * w) rounded as the exact product would round: the fp32 product
-// (rf within ~3 fp32 ulps of r, so the product within ~4 ulps of exact) decides
-// unless it lies within 32 fp32 ulps of a bf16 rounding tie; then the product
-// in double (r in double) decides.  This makes the RMSNorm's rounding point
-// independent of summation order.
-static __device__ __noinline__ uint16_t norm_round_bf16_slow(float x, float w, NormR n) {
-  return f64_to_bf16_rn((double)x * norm_rd(n) * (double)w);
-}
-__device__ __forceinline__ uint16_t norm_round_bf16(float x, float w, float rf, const NormR& n) {
-  const float v = x * rf * w;
-  const int low = (int)(__float_as_uint(v) & 0xFFFFu);
-  if (abs(low - 0x8000) <= 32) return norm_round_bf16_slow(x, w, n);  // rare; kept out of line
-  return f32_to_bf16(v);
+// bf16(x * w * r), correctly rounded: x * w is exact in fp32 (both are bf16
+// values), its product with the pair r is carried as s + t, and t decides the
+// rounding where s lies exactly halfway between two bf16 values.  The result
+// equals the rounding of the exact product unless that lies within about
+// 2^-43 (relative) of a rounding boundary, and it does not depend on the
+// order in which the sum of squares was accumulated.
+__device__ __forceinline__ uint16_t norm_round_bf16(float x, float w, const NormR& r) {
+  const float xw = x * w;
+  const float p = xw * r.hi;
+  const float e = fmaf(xw, r.lo, fmaf(xw, r.hi, -p));
+  const float s = p + e;  // |e| << |p|: s + t = p + e exactly
+  const float t = e - (s - p);
+  const uint32_t b = __float_as_uint(s);
+  if ((b & 0xFFFFu) != 0x8000u || t == 0.0f) return f32_to_bf16(s);
+  return (uint16_t)((b >> 16) + ((t > 0.0f) == (s > 0.0f) ? 1u : 0u));  // away from zero iff |s + t| > |s|
 }
 
 // ------------------------------------------------------------------ E4M3

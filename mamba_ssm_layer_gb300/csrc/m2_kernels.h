@@ -100,7 +100,6 @@ struct GemvArgs {
   int32_t norm;             // GemvNorm
   const uint16_t* norm_w;   // [K] bf16 norm weight
   float norm_eps;
-  double norm_inv_k;        // 1/K
   const float* gy;          // NORM_GATED: y [M][ldgy] fp32, z [M][ldgz] bf16 (whole-row span)
   int32_t ldgy;
   const uint16_t* gz;
@@ -153,7 +152,6 @@ struct PrepArgs {
   int32_t f16;        // 1: prescaled f16 + unscale; 0: bf16
   float* unscale;     // [M] (f16 mode)
   int32_t pdl;
-  double inv_k;       // 1/K (PREP_RMSNORM), so the kernel needs no double division
   // W8A8 arm (out may be null): E4M3 codes [M][ldq] and fp32 block scales
   // [ceil(K/128)][ldsq] of each row and 128-element block: amax = max |v|,
   // codes E4M3(v * (448 / amax)), scale amax / 448 (fp32; zero block: 0, 0).
