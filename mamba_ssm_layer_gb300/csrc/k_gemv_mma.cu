@@ -46,6 +46,7 @@ struct MmaTail {
   unsigned amax[8];
   float unscale[8];
   int32_t pos[8];
+  float red[48];  // the norm's cross-warp partials
   uint64_t full[kMaxStages], empty[kMaxStages];
   uint64_t epi_bar;   // epilogue inputs staged by bulk copies
   uint64_t epi_bar2;  // fused decode step: the residual rows of the out_proj epilogue
@@ -143,31 +144,54 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 // weight stream fills the memory system -- overlaps the wait.
 constexpr int kNormPer = 2;  // 16-byte chunks of 8 elements per thread (K <= 8192 with 512 threads)
 struct NormPre {
-  uint4 wv[kNormPer], zv[kNormPer];
-  bool w, z;  // which of them are loaded
+  uint4 wv[kNormPer];
+  float sz[kNormPer * 8];  // gated: silu(z)
+  bool w, z;               // which of them are loaded
 };
 __device__ __forceinline__ void norm_preload(const GemvArgs& a, int m, int tid, int nC, bool z, NormPre& pre) {
+  pre.z = z && a.norm == NORM_GATED;
+  uint4 zv[kNormPer];
 #pragma unroll
   for (int c = 0; c < kNormPer; ++c) {
     const int k0 = (tid + nC * c) * 8;
-    pre.wv[c] = pre.zv[c] = make_uint4(0u, 0u, 0u, 0u);
+    pre.wv[c] = zv[c] = make_uint4(0u, 0u, 0u, 0u);
     if (k0 < a.K) {
       pre.wv[c] = __ldg(reinterpret_cast<const uint4*>(a.norm_w + k0));
-      if (z && a.norm == NORM_GATED) pre.zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
+      if (pre.z) zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
+    }
+  }
+  if (pre.z) {
+#pragma unroll
+    for (int c = 0; c < kNormPer; ++c) {
+      const uint32_t z4[4] = {zv[c].x, zv[c].y, zv[c].z, zv[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        pre.sz[c * 8 + 2 * e] = silu_f(bf16lo(z4[e]));
+        pre.sz[c * 8 + 2 * e + 1] = silu_f(bf16hi(z4[e]));
+      }
     }
   }
   pre.w = true;
-  pre.z = z && a.norm == NORM_GATED;
 }
 
+// 2^j for |j| <= 126, exactly
+__device__ __forceinline__ float exp2i(int j) { return __uint_as_float((uint32_t)(127 + j) << 23); }
+
+// One activation row's norm into shared memory.  red: 48 floats of scratch
+// (not aliasing act or zero); zero[0, nzero): a region this call clears while
+// the row's loads are in flight (the caller's accumulators).
 template <bool F16>
 __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* red, float* unscale, int tid,
-                               int nC, const NormPre* pre = nullptr) {
+                               int nC, const NormPre* pre = nullptr, float* zero = nullptr, int nzero = 0) {
   const int K = a.K, warp = tid >> 5, lane = tid & 31;
   const int nw = nC / 32;
   constexpr int kPer = kNormPer;
   float v[kPer * 8];
   uint4 wv[kPer], zv[kPer];
+  // chunk c of this thread holds elements k0 = (tid + nC * c) * 8 ..; chunks
+  // past K (uniform across a warp when K is a multiple of 256) are skipped
+  auto live = [&](int c) { return (tid + nC * c) * 8 < K; };
+  const bool zpre = pre && pre->z && m == 0;
 #pragma unroll
   for (int c = 0; c < kPer; ++c) {
     const int k0 = (tid + nC * c) * 8;
@@ -185,7 +209,7 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
           v[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
         }
       } else {
-        zv[c] = (pre && pre->z && m == 0) ? pre->zv[c] : __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
+        if (!zpre) zv[c] = __ldcg(reinterpret_cast<const uint4*>(a.gz + (size_t)m * a.ldgz + k0));
         // L2 loads: y may come from other CTAs of the same launch (fused step)
         const float4 f0 = __ldcg(reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0));
         const float4 f1 = __ldcg(reinterpret_cast<const float4*>(a.gy + (size_t)m * a.ldgy + k0 + 4));
@@ -194,23 +218,29 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
       }
     }
   }
-  // the weights, silu(z) (gated), and the largest |v * w (* silu(z))|
-  float wf[kPer * 8], sz[kPer * 8];
+  for (int i = tid; i < nzero; i += nC) zero[i] = 0.0f;
+  // silu(z) (gated), and the largest |v * w (* silu(z))|
+  float sz[kPer * 8];
   float pm = 0.0f;
 #pragma unroll
   for (int c = 0; c < kPer; ++c) {
     const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w}, z4[4] = {zv[c].x, zv[c].y, zv[c].z, zv[c].w};
 #pragma unroll
+    for (int e = 0; e < 8; ++e) sz[c * 8 + e] = 1.0f;
+    if (!live(c)) continue;
+#pragma unroll
     for (int e = 0; e < 4; ++e) {
-      wf[c * 8 + 2 * e] = bf16lo(w4[e]);
-      wf[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
-      sz[c * 8 + 2 * e] = a.norm == NORM_RMS ? 1.0f : silu_f(bf16lo(z4[e]));
-      sz[c * 8 + 2 * e + 1] = a.norm == NORM_RMS ? 1.0f : silu_f(bf16hi(z4[e]));
+      if (a.norm != NORM_RMS) {
+        sz[c * 8 + 2 * e] = zpre ? pre->sz[c * 8 + 2 * e] : silu_f(bf16lo(z4[e]));
+        sz[c * 8 + 2 * e + 1] = zpre ? pre->sz[c * 8 + 2 * e + 1] : silu_f(bf16hi(z4[e]));
+      }
+      if (F16) {
+        pm = fmaxf(pm, fabsf(v[c * 8 + 2 * e] * bf16lo(w4[e]) * sz[c * 8 + 2 * e]));
+        pm = fmaxf(pm, fabsf(v[c * 8 + 2 * e + 1] * bf16hi(w4[e]) * sz[c * 8 + 2 * e + 1]));
+      }
     }
   }
   if (F16) {
-#pragma unroll
-    for (int e = 0; e < kPer * 8; ++e) pm = fmaxf(pm, fabsf(v[e] * wf[e] * sz[e]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o));
   }
@@ -219,7 +249,11 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
   if (a.norm == NORM_RMS) {
     float hi = 0.0f, lo = 0.0f;
 #pragma unroll
-    for (int e = 0; e < kPer * 8; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
+    for (int c = 0; c < kPer; ++c) {
+      if (!live(c)) continue;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) two_sum_acc(hi, lo, v[c * 8 + e] * v[c * 8 + e]);
+    }
     two_sum_warp(hi, lo);
     if (lane == 0) {
       red[warp] = hi;
@@ -227,17 +261,26 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
       red[32 + warp] = pm;
     }
     named_bar(1, nC);
-    float h = 0.0f, l = 0.0f;
-    pm = 0.0f;
-    for (int w = 0; w < nw; ++w) {  // the same fixed order in every thread
-      two_sum_acc(h, l, red[w]);
-      l += red[16 + w];
-      pm = fmaxf(pm, red[32 + w]);
+    // the warps' partials combined by a fixed butterfly (lanes 16..31 mirror
+    // 0..15); every thread then takes lane 0's result
+    const int src = lane & 15;
+    float h = src < nw ? red[src] : 0.0f, l = src < nw ? red[16 + src] : 0.0f;
+    pm = src < nw ? red[32 + src] : 0.0f;
+#pragma unroll
+    for (int sh = 8; sh > 0; sh >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, h, sh), ol = __shfl_xor_sync(0xffffffffu, l, sh);
+      two_sum_acc(h, l, oh);
+      l += ol;
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, sh));
     }
+    h = __shfl_sync(0xffffffffu, h, 0);
+    l = __shfl_sync(0xffffffffu, l, 0);
+    pm = __shfl_sync(0xffffffffu, pm, 0);
     const NormR nr = norm_r(h, l, K, a.norm_eps);
     r = nr.hi;
 #pragma unroll
     for (int c = 0; c < kPer; ++c) {
+      if (!live(c)) continue;
       const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -258,13 +301,28 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
     }
     if (lane == 0) red[kPer * nw + warp] = pm;
     named_bar(1, nC);
-    float gs = 0.0f;
-    for (int j = 0; j < K / 256; ++j) gs += red[j];
-    pm = 0.0f;
-    for (int w = 0; w < nw; ++w) pm = fmaxf(pm, red[kPer * nw + w]);
+    // the 256-element chunks' sums and the warps' maxima, combined by fixed
+    // butterflies; every thread then takes lane 0's result
+    float gs = lane < kPer * nw ? red[lane] : 0.0f;
+    pm = lane < nw ? red[kPer * nw + lane] : 0.0f;
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+      gs += __shfl_xor_sync(0xffffffffu, gs, sh);
+      pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, sh));
+    }
+    gs = __shfl_sync(0xffffffffu, gs, 0);
+    pm = __shfl_sync(0xffffffffu, pm, 0);
     r = 1.0f / sqrtf(gs / (float)K + a.norm_eps);
 #pragma unroll
-    for (int e = 0; e < kPer * 8; ++e) o[e] = f32_to_bf16(v[e] * r * wf[e] * sz[e]);
+    for (int c = 0; c < kPer; ++c) {
+      if (!live(c)) continue;
+      const uint32_t w4[4] = {wv[c].x, wv[c].y, wv[c].z, wv[c].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        o[c * 8 + 2 * e] = f32_to_bf16(v[c * 8 + 2 * e] * r * bf16lo(w4[e]) * sz[c * 8 + 2 * e]);
+        o[c * 8 + 2 * e + 1] = f32_to_bf16(v[c * 8 + 2 * e + 1] * r * bf16hi(w4[e]) * sz[c * 8 + 2 * e + 1]);
+      }
+    }
   }
   float up = 1.0f;
   if (F16) {
@@ -273,8 +331,8 @@ __device__ void fused_norm_row(const GemvArgs& a, int m, uint16_t* act, float* r
     const unsigned bits = __float_as_uint(mx);
     const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
     const int jx = max(-120, min(120, 14 - ex));
-    up = ldexpf(1.0f, jx);
-    if (tid == 0) unscale[m] = ldexpf(1.0f, -jx);
+    up = exp2i(jx);
+    if (tid == 0) unscale[m] = exp2i(-jx);
   } else if (tid == 0) {
     unscale[m] = 1.0f;
   }
@@ -472,20 +530,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
     }
   }
   NormPre pre;
-  if (a.norm != NORM_NONE) norm_preload(a, 0, tid, kC, mvalid == 1, pre);  // before the wait
+  // before the wait; silu(z) only for a single row (registers)
+  if (a.norm != NORM_NONE) norm_preload(a, 0, tid, kC, MB == 1 && mvalid == 1, pre);
   pdl_wait();
   pdl_trigger();
-  for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
-  if (tid < 8) tail->amax[tid] = 0u;
-  named_bar(1, kC);
+  const int ntot = rows_max * kMmaWarps * MB;
   if (a.norm != NORM_NONE) {
-    // the activation rows are this kernel's own norm of its inputs
-    float* red = tot;  // scratch: tot is zeroed again below
+    // the activation rows are this kernel's own norm of its inputs; the
+    // accumulators are cleared while the first row's loads are in flight
+    // (the norm's barriers order that before the main loop)
     for (int m = 0; m < mvalid; ++m)
-      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, red, tail->unscale, tid, kC, &pre);
-    for (int i = tid; i < rows_max * kMmaWarps * MB; i += kC) tot[i] = 0.0f;
-    named_bar(1, kC);
+      fused_norm_row<FP8>(a, m, act_s + (size_t)m * lay.act_ld, tail->red, tail->unscale, tid, kC, &pre,
+                          m == 0 ? tot : nullptr, m == 0 ? ntot : 0);
   } else {
+    for (int i = tid; i < ntot; i += kC) tot[i] = 0.0f;
+    if (tid < 8) tail->amax[tid] = 0u;
+    named_bar(1, kC);
     // activations -> shared memory (coherent loads: written by the previous kernel)
     const int kv = a.K / 8;  // 16-byte vectors per row
     for (int i = tid; i < mvalid * kv; i += kC) {
@@ -644,9 +704,12 @@ template <bool FP8, int MB>
 static cudaError_t launch_mma_one(const GemvArgs& a, cudaStream_t s) {
   static int done_mask[64] = {0};
   const int nrg = (a.N + kMmaRows - 1) / kMmaRows;
-  int grid = num_sms();
-  if (grid > nrg) grid = nrg;
-  const int rows_max = ((nrg + grid - 1) / grid) * kMmaRows;
+  // the fewest CTAs whose largest share of row groups is that of one CTA per
+  // SM: the step takes as long, every CTA finishes at about the same time,
+  // and the SMs left over take the next kernel's CTAs early
+  const int per = (nrg + num_sms() - 1) / num_sms();
+  const int grid = (nrg + per - 1) / per;
+  const int rows_max = per * kMmaRows;
   // rows longer than 4 KB: each stage (16 row pieces) as one 3-D tensor copy
   // instead of 16 row copies, when the rows split into 256-byte pieces
   CUtensorMap tmW;

@@ -83,7 +83,7 @@ __device__ __forceinline__ void two_sum_warp(float& hi, float& lo) {
 
 // r = 1/sqrt(S/K + eps) of an RMSNorm row as an unevaluated pair hi + lo
 // (relative error about 2^-43), from its sum of squares S = h + l, in fp32
-// arithmetic only: 1/K and S/K carry their fma-exact errors, and one Newton
+// arithmetic only: 1/K and S/K carry their (fma-computed) errors, and one Newton
 // step with an fma-exact residual refines rsqrtf.  Every thread of a row
 // computes the same pair.
 struct NormR {
@@ -91,8 +91,8 @@ struct NormR {
 };
 __device__ __forceinline__ NormR norm_r(float h, float l, int K, float eps) {
   const float kf = (float)K;
-  const float ik = __fdiv_rn(1.0f, kf);
-  const float ik_lo = __fdiv_rn(fmaf(-ik, kf, 1.0f), kf);  // 1/K - ik
+  const float ik = __frcp_rn(kf);
+  const float ik_lo = fmaf(-ik, kf, 1.0f) * ik;  // 1/K - ik, to ~2^-24 of itself
   const float m = h * ik;                                   // S/K = m + me
   const float me = fmaf(h, ik_lo, fmaf(l, ik, fmaf(h, ik, -m)));
   const float v = m + eps;                                  // S/K + eps = v + ve
@@ -122,8 +122,9 @@ __device__ __forceinline__ uint16_t norm_round_bf16(float x, float w, const Norm
   const float s = p + e;  // |e| << |p|: s + t = p + e exactly
   const float t = e - (s - p);
   const uint32_t b = __float_as_uint(s);
-  if ((b & 0xFFFFu) != 0x8000u || t == 0.0f) return f32_to_bf16(s);
-  return (uint16_t)((b >> 16) + ((t > 0.0f) == (s > 0.0f) ? 1u : 0u));  // away from zero iff |s + t| > |s|
+  const uint16_t rn = f32_to_bf16(s);
+  const uint16_t dir = (uint16_t)((b >> 16) + ((t > 0.0f) == (s > 0.0f) ? 1u : 0u));  // away from zero iff |s + t| > |s|
+  return ((b & 0xFFFFu) == 0x8000u && t != 0.0f) ? dir : rn;
 }
 
 // ------------------------------------------------------------------ E4M3
