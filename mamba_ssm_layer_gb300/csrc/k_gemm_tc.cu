@@ -480,208 +480,205 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ------------------------------------------------------------------ W8A8 kernel
 //
-// The W8A8 product with stages of two k blocks: the weight tiles, the
-// activation codes and the token scales of two k blocks each arrive as ONE
-// tensor copy (3-D boxes for the tiles, a 2-D box for the scales).  A CTA's
-// copy engine takes a roughly fixed time per copy whatever its size, so one
-// copy per operand per k block paced this kernel at about one k block per
-// microsecond; stages of two halve the copies.  Stage slots are freed by their
-// own barriers (a tcgen05.commit after the stage's last k block for the
-// tiles, the epilogue warps for the scales), independent of the per-k-block
-// TMEM barriers, so stages can be deeper than the four TMEM buffers.
-constexpr int kW8Kbs = 2;      // k blocks per stage
-constexpr int kW8Stages = 3;   // weight and activation stages
-constexpr int kW8ScSlots = 4;  // token-scale slots
+// E4M3 weights x E4M3 activation codes (kind::f8f6f4) in tiles of 128 weight
+// rows x NT tokens (UMMA N = NT, up to 256), one k block per stage.  What
+// bounds this product is the operands' path from L2 into the SM, so the tile
+// is as wide as TMEM allows: at NT = 256 a k block moves 48 KB for 8.4 MFLOP
+// (32 KB for 4.2 at NT = 128).  A bulk copy also costs the thread that issues
+// it a fixed time, so each operand has its own issuing thread.  Roles:
+//   warp 0, lane 0   weight tiles [128][128] (128-byte swizzle) into a ring of S stages
+//   warp 0, lane 1   activation tiles [NT][128] (128-byte swizzle), same ring positions
+//   warp 0, lane 2   the token scales of each k block (fp32 [NT]) into S slots
+//   warp 1           TMEM; lane 0 issues 4 MMAs (K = 32) per k block into one of the
+//                    partial buffers, then commits twice: the stage is free, the
+//                    partial is done
+//   warps 2-17       epilogue, four warps per TMEM lane quarter, NT/4 token columns
+//                    each: per k block, c = s_w * s_a for its columns (into its own
+//                    scratch, which frees the scale slot), then acc += c * partial,
+//                    two columns per fma; per item, the store epilogue or split-k
+//                    partials
+// Every wait is bounded; every issuing thread waits for its own copies and
+// MMAs before the CTA frees TMEM and exits.
+constexpr int kW8Warps = 18;
+constexpr int kW8Threads = kW8Warps * 32;
+constexpr int kW8EpiWarp0 = 2;
+constexpr int kW8EpiWarps = 16;
+constexpr int kW8Ring = 196608;  // operand ring bytes
 
 template <int NT>
-struct W8Layout {
-  static constexpr int kWStage = kW8Kbs * kTcBM * kTcBK;  // E4M3 weight tiles of one stage
-  static constexpr int kAStage = kW8Kbs * NT * kTcBK;     // E4M3 activation tiles
-  static constexpr int kScSlot = kW8Kbs * NT * 4;         // fp32 token scales
+struct W8Cfg {
+  static constexpr int kWBytes = kTcBM * kTcBK;                  // 16 KB of E4M3 weights
+  static constexpr int kABytes = NT * kTcBK;                     // NT x 128 E4M3 codes
+  static constexpr int kStages = kW8Ring / (kWBytes + kABytes);  // 256: 4, 128: 6, 64: 8
+  static constexpr int kBufs = NT >= 256 ? 2 : 4;                // TMEM partials of NT columns
+  static constexpr int kTmemCols = NT >= 128 ? 512 : 256;
   static constexpr int kW = 0;
-  static constexpr int kA = kW + kW8Stages * kWStage;
-  static constexpr int kSc = kA + kW8Stages * kAStage;
-  static constexpr int kBars = kSc + kW8ScSlots * kScSlot;
+  static constexpr int kA = kW + kStages * kWBytes;
+  static constexpr int kSc = kA + kStages * kABytes;             // [kStages][NT] fp32
+  static constexpr int kC = kSc + kStages * NT * 4;              // [16 warps][NT / 4] fp32
+  static constexpr int kBars = kC + kW8EpiWarps * (NT / 4) * 4;
 };
 
 struct W8Bars {
-  uint64_t w_full[kW8Stages], w_empty[kW8Stages];
-  uint64_t a_full[kW8Stages], a_empty[kW8Stages];
-  uint64_t sc_full[kW8ScSlots], sc_empty[kW8ScSlots];
-  uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
+  uint64_t w_full[8], a_full[8], stage_empty[8];
+  uint64_t sc_full[8], sc_empty[8];
+  uint64_t mma_done[4], tmem_empty[4];
   uint32_t tmem_base;
 };
 
 template <int NT>
 constexpr int w8_smem_bytes() {
-  return W8Layout<NT>::kBars + (int)sizeof(W8Bars) + 1024;  // + alignment slack
+  return W8Cfg<NT>::kBars + (int)sizeof(W8Bars) + 1024;  // + alignment slack
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kW8Threads, 1)
     gemm_w8a8_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmS, const TcArgs ta) {
-  using Lay = W8Layout<NT>;
+  using Cfg = W8Cfg<NT>;
+  constexpr int S = Cfg::kStages, NB = Cfg::kBufs;
+  static_assert(S <= 8 && NB <= 4, "barrier arrays");
   const GemvArgs& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  W8Bars* bars = reinterpret_cast<W8Bars*>(smem + Lay::kBars);
+  W8Bars* bars = reinterpret_cast<W8Bars*>(smem + Cfg::kBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
   const int cid = blockIdx.x, ncl = gridDim.x;
   const int L = a.dconv - 1;
 
   if (tid == 0) {
-    for (int s = 0; s < kW8Stages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars->w_full[s], 1);
-      mbar_init(&bars->w_empty[s], 1);
       mbar_init(&bars->a_full[s], 1);
-      mbar_init(&bars->a_empty[s], 1);
-    }
-    for (int s = 0; s < kW8ScSlots; ++s) {
+      mbar_init(&bars->stage_empty[s], 1);
       mbar_init(&bars->sc_full[s], 1);
-      mbar_init(&bars->sc_empty[s], kTcEpiWarps);
+      mbar_init(&bars->sc_empty[s], kW8EpiWarps);
     }
-    for (int b = 0; b < kTcTmemBufs; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(&bars->mma_done[b], 1);
-      mbar_init(&bars->tmem_empty[b], kTcEpiWarps);
+      mbar_init(&bars->tmem_empty[b], kW8EpiWarps);
     }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&bars->tmem_base, kTcTmemBufs * NT);
+  if (warp == 1) tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   bool dead = false;
 
-  if (warp == 0) {
-    // -------------------------------------------------------- weight producer
-    if (lane == 0) {
-      const uint64_t polw = policy_evict_normal();  // weight tiles are re-read by the token tiles
-      int gs = 0;
-      for (int item = cid; item < nitems && !dead; item += ncl) {
-        int nt, mt, kb0, kb1;
-        tc_item(ta, item, nt, mt, kb0, kb1);
-        for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
-          const int s = gs % kW8Stages;
-          if (gs >= kW8Stages && !mbar_wait(&bars->w_empty[s], ((gs / kW8Stages) - 1) & 1)) dead = true;
-          if (dead) break;
-          // two k blocks per copy (past the tensor's k extent: zeros; past the
-          // item's range: loaded, unused); the whole box counts
-          mbar_arrive_expect_tx(&bars->w_full[s], Lay::kWStage);
-          tma_load_3d(smem + Lay::kW + s * Lay::kWStage, &tmW, 0, nt * kTcBM, kb, &bars->w_full[s], polw);
+  if (warp == 0 && lane < 3) {
+    // -------------------------------------------------------- operand issuers
+    // lane 0: weights (never the previous kernel's output: no dependency wait);
+    // lanes 1, 2: activation codes and token scales (written by the previous kernel)
+    if (lane > 0) pdl_wait();
+    const uint64_t pol = lane == 0 ? policy_evict_normal() : policy_evict_last();
+    uint64_t* full = lane == 0 ? bars->w_full : (lane == 1 ? bars->a_full : bars->sc_full);
+    uint64_t* empty = lane == 2 ? bars->sc_empty : bars->stage_empty;
+    const uint32_t bytes = lane == 0 ? Cfg::kWBytes : (lane == 1 ? Cfg::kABytes : NT * 4);
+    int gk = 0;
+    for (int item = cid; item < nitems && !dead; item += ncl) {
+      int nt, mt, kb0, kb1;
+      tc_item(ta, item, nt, mt, kb0, kb1);
+      for (int kb = kb0; kb < kb1; ++kb, ++gk) {
+        const int s = gk % S;
+        if (gk >= S && !mbar_wait(&empty[s], ((gk / S) - 1) & 1)) {
+          dead = true;
+          break;
         }
+        mbar_arrive_expect_tx(&full[s], bytes);
+        if (lane == 0)
+          tma_load_2d(smem + Cfg::kW + s * Cfg::kWBytes, &tmW, kb * kTcBK, nt * kTcBM, &full[s], pol);
+        else if (lane == 1)
+          tma_load_2d(smem + Cfg::kA + s * Cfg::kABytes, &tmA, kb * kTcBK, mt * NT, &full[s], pol);
+        else
+          tma_load_2d(smem + Cfg::kSc + s * NT * 4, &tmS, mt * NT, kb, &full[s], pol);
       }
-      for (int k = max(0, gs - kW8Stages); k < gs; ++k)
-        if (!mbar_drain(&bars->w_full[k % kW8Stages], (k / kW8Stages) & 1)) break;
     }
-  } else if (warp == kTcAWarp) {
-    // -------------------------------------------------------- activation producer
-    pdl_wait();  // the codes and scales are written by the previous kernel
-    if (lane == 0) {
-      const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
-      int gs = 0, a_iss = 0, sc_iss = 0;
-      for (int item = cid; item < nitems && !dead; item += ncl) {
-        int nt, mt, kb0, kb1;
-        tc_item(ta, item, nt, mt, kb0, kb1);
-        for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
-          const int sa = gs % kW8Stages, ss = gs % kW8ScSlots;
-          if (gs >= kW8Stages && !mbar_wait(&bars->a_empty[sa], ((gs / kW8Stages) - 1) & 1)) dead = true;
-          if (dead) break;
-          mbar_arrive_expect_tx(&bars->a_full[sa], Lay::kAStage);
-          tma_load_3d(smem + Lay::kA + sa * Lay::kAStage, &tmA, 0, mt * NT, kb, &bars->a_full[sa], pola);
-          a_iss = gs + 1;
-          if (gs >= kW8ScSlots && !mbar_wait(&bars->sc_empty[ss], ((gs / kW8ScSlots) - 1) & 1)) dead = true;
-          if (dead) break;
-          mbar_arrive_expect_tx(&bars->sc_full[ss], Lay::kScSlot);
-          tma_load_2d(smem + Lay::kSc + ss * Lay::kScSlot, &tmS, mt * NT, kb, &bars->sc_full[ss], pola);
-          sc_iss = gs + 1;
-        }
-      }
-      for (int k = max(0, a_iss - kW8Stages); k < a_iss; ++k)
-        if (!mbar_drain(&bars->a_full[k % kW8Stages], (k / kW8Stages) & 1)) break;
-      for (int k = max(0, sc_iss - kW8ScSlots); k < sc_iss; ++k)
-        if (!mbar_drain(&bars->sc_full[k % kW8ScSlots], (k / kW8ScSlots) & 1)) break;
-    }
+    // drain: every copy this thread issued has landed
+    for (int k = max(0, gk - S); k < gk; ++k)
+      if (!mbar_drain(&full[k % S], (k / S) & 1)) break;
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc8 = tc_idesc_f8(kTcBM, NT);
-      int gs = 0, gk = 0;
+      int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
-        for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
-          const int s = gs % kW8Stages, nk = min(kW8Kbs, kb1 - kb);
-          if (!mbar_wait(&bars->w_full[s], (gs / kW8Stages) & 1)) dead = true;
-          if (!dead && !mbar_wait(&bars->a_full[s], (gs / kW8Stages) & 1)) dead = true;
-          for (int i = 0; i < nk && !dead; ++i, ++gk) {
-            const int tb = gk % kTcTmemBufs;
-            if (gk >= kTcTmemBufs && !mbar_wait(&bars->tmem_empty[tb], ((gk / kTcTmemBufs) - 1) & 1)) dead = true;
-            if (dead) break;
-            tc_fence_after();
-            const uint32_t wb = smem_addr(smem + Lay::kW + s * Lay::kWStage + i * kTcBM * kTcBK);
-            const uint32_t ab = smem_addr(smem + Lay::kA + s * Lay::kAStage + i * NT * kTcBK);
-#pragma unroll
-            for (int kk = 0; kk < kTcBK / 32; ++kk)
-              tc_mma_f8(tmem + tb * NT, sw128_desc(wb + kk * 32), sw128_desc(ab + kk * 32), idesc8, kk > 0 ? 1 : 0);
-            tc_commit(&bars->mma_done[tb]);  // frees the TMEM partial for the epilogue
+        for (int kb = kb0; kb < kb1; ++kb, ++gk) {
+          const int s = gk % S, tb = gk % NB;
+          if (!mbar_wait(&bars->w_full[s], (gk / S) & 1) || !mbar_wait(&bars->a_full[s], (gk / S) & 1) ||
+              (gk >= NB && !mbar_wait(&bars->tmem_empty[tb], ((gk / NB) - 1) & 1))) {
+            dead = true;
+            break;
           }
-          if (dead) break;
-          tc_commit(&bars->w_empty[s]);  // the stage's tiles are read once its last MMAs complete
-          tc_commit(&bars->a_empty[s]);
+          tc_fence_after();
+          const uint32_t wb = smem_addr(smem + Cfg::kW + s * Cfg::kWBytes);
+          const uint32_t ab = smem_addr(smem + Cfg::kA + s * Cfg::kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 32; ++kk)
+            tc_mma_f8(tmem + tb * NT, sw128_desc(wb + kk * 32), sw128_desc(ab + kk * 32), idesc8, kk > 0 ? 1 : 0);
+          tc_commit(&bars->stage_empty[s]);  // the stage's tiles have been read
+          tc_commit(&bars->mma_done[tb]);    // the partial is complete
         }
       }
-      if (gk > 0) mbar_drain(&bars->mma_done[(gk - 1) % kTcTmemBufs], ((gk - 1) / kTcTmemBufs) & 1);
+      if (gk > 0) mbar_drain(&bars->mma_done[(gk - 1) % NB], ((gk - 1) / NB) & 1);
     }
-  } else if (warp >= 6 && warp < 6 + kTcEpiWarps) {
+  } else if (warp >= kW8EpiWarp0 && warp < kW8EpiWarp0 + kW8EpiWarps) {
     // -------------------------------------------------------- epilogue
-    constexpr int EPG = kTcEpiWarps / 4;
-    constexpr int HC = NT / EPG;
-    const int q = warp & 3;
-    const int hf = (warp - 6) >> 2;
+    constexpr int HC = NT / 4;  // token columns of this warp
+    const int q = warp & 3;     // TMEM lane quarter this warp may access
+    const int hf = (warp - kW8EpiWarp0) >> 2;
     const int row = 32 * q + lane;
     pdl_wait();
-    float acc[HC];
-    int gs = 0, gk = 0;
+    float2 acc[HC / 2];
+    float* cw = reinterpret_cast<float*>(smem + Cfg::kC) + (warp - kW8EpiWarp0) * HC;  // this warp's c
+    const uint32_t cws = smem_addr(cw);
+    int gk = 0;
     for (int item = cid; item < nitems && !dead; item += ncl) {
       int nt, mt, kb0, kb1;
       tc_item(ta, item, nt, mt, kb0, kb1);
       const int ks = item % ta.ksplit;
 #pragma unroll
-      for (int j = 0; j < HC; ++j) acc[j] = 0.0f;
-      for (int kb = kb0; kb < kb1 && !dead; kb += kW8Kbs, ++gs) {
-        const int ss = gs % kW8ScSlots, nk = min(kW8Kbs, kb1 - kb);
-        // the TMEM loads below are warp-collective: the warp decides together
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->sc_full[ss], (gs / kW8ScSlots) & 1))) dead = true;
-        for (int i = 0; i < nk && !dead; ++i, ++gk) {
-          const int tb = gk % kTcTmemBufs;
-          const float s = bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb + i));
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1))) dead = true;
-          if (dead) break;
-          tc_fence_after();
-          const uint32_t ta_ = tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC;
-#pragma unroll
-          for (int c0 = 0; c0 < HC; c0 += 16) {
-            float v[16];
-            tmem_ld16(ta_ + c0, v);
-            const uint32_t sq = smem_addr(smem + Lay::kSc + ss * Lay::kScSlot + (i * NT + hf * HC + c0) * 4);
-#pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-              const float4 t4 = lds_f4_ordered(sq + 16 * i4);
-              acc[c0 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c0 + 4 * i4 + 0]);
-              acc[c0 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c0 + 4 * i4 + 1]);
-              acc[c0 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c0 + 4 * i4 + 2]);
-              acc[c0 + 4 * i4 + 3] = fmaf(s * t4.w, v[4 * i4 + 3], acc[c0 + 4 * i4 + 3]);
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
+      for (int j = 0; j < HC / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      for (int kb = kb0; kb < kb1; ++kb, ++gk) {
+        const int s = gk % S, tb = gk % NB;
+        const float sw = bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb));
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->sc_full[s], (gk / S) & 1))) {
+          dead = true;
+          break;
         }
+        const float* sa = reinterpret_cast<const float*>(smem + Cfg::kSc + s * NT * 4) + hf * HC;
+#pragma unroll
+        for (int j = lane; j < HC; j += 32) cw[j] = sw * sa[j];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->sc_empty[ss]);  // this warp is done with the stage's scales
+        if (lane == 0) mbar_arrive(&bars->sc_empty[s]);  // the slot is read
+        // the TMEM loads below are warp-collective: the warp decides together
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / NB) & 1))) {
+          dead = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tadr = tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC;
+        // 8 columns per TMEM load: the NT = 256 accumulators leave few registers
+#pragma unroll
+        for (int c0 = 0; c0 < HC; c0 += 8) {
+          float v[8];
+          tmem_ld8(tadr + c0, v);
+#pragma unroll
+          for (int i4 = 0; i4 < 2; ++i4) {
+            const float4 c4 = lds_f4_ordered(cws + (c0 + 4 * i4) * 4);
+            float2& a0 = acc[(c0 + 4 * i4) / 2];
+            float2& a1 = acc[(c0 + 4 * i4) / 2 + 1];
+            a0 = ffma2(make_float2(c4.x, c4.y), make_float2(v[4 * i4], v[4 * i4 + 1]), a0);
+            a1 = ffma2(make_float2(c4.z, c4.w), make_float2(v[4 * i4 + 2], v[4 * i4 + 3]), a1);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();  // also: every lane has read cw before the next k block rewrites it
+        if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
       }
       if (dead) break;
       const int n = nt * kTcBM + row;
@@ -691,7 +688,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < HC; ++j) {
             const int m = mt * NT + hf * HC + j;
-            if (m < a.M) pp[(size_t)m * a.N] = acc[j];
+            if (m < a.M) pp[(size_t)m * a.N] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
           }
         } else {
           const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
@@ -700,7 +697,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int j = 0; j < HC; ++j) {
             const int m = mt * NT + hf * HC + j;
-            if (m < a.M) tc_epi_elem(a, m, n, acc[j], conv, taps, L);
+            if (m < a.M) tc_epi_elem(a, m, n, (j & 1) ? acc[j / 2].y : acc[j / 2].x, conv, taps, L);
           }
         }
       }
@@ -711,7 +708,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
-    tmem_free(tmem, kTcTmemBufs * NT);
+    tmem_free(tmem, Cfg::kTmemCols);
   }
 }
 
@@ -759,22 +756,20 @@ size_t gemm_tc_partial_bytes(int M, int N, int K) {
   return ks > 1 ? (size_t)ks * M * N * 4 : 0;
 }
 
-// Host: a 3-D map over a byte matrix of `rows` rows (pitch `ld` bytes) whose
-// first kblocks * 128 bytes are used, taken as {128-byte k block piece, rows,
-// k blocks}: a box {128, box_rows, kbs} lands as kbs consecutive
-// [box_rows][128] tiles, each 128-byte swizzled (the UMMA K-major layout of
-// one k block).  Rows or k blocks past the extents read as zero.
-static bool encode_kblocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t ld, uint64_t kblocks,
-                           uint32_t box_rows, uint32_t kbs) {
-  auto enc = tensor_map_encoder();
-  if (!enc || ld % 16 || ld < kblocks * 128) return false;
-  const cuuint64_t dims[3] = {128, rows, kblocks};
-  const cuuint64_t strides[2] = {ld, 128};
-  const cuuint32_t box[3] = {128, box_rows, kbs};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+// Token tile of the W8A8 product: as wide as the token count needs, up to 256.
+static int w8_nt(int M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
+
+// k split of the W8A8 product: as gemm_tc_ksplit, for its own tiles, and no
+// more splits than `part_bytes` holds partials for.
+static int w8_ksplit(int M, int N, int K, size_t part_bytes) {
+  const int nt = w8_nt(M);
+  const int tiles = ((M + nt - 1) / nt) * ((N + kTcBM - 1) / kTcBM);
+  const int kb = (K + kTcBK - 1) / kTcBK;
+  int ks = num_sms() / tiles;
+  if (ks > kb / 4) ks = kb / 4;
+  const size_t per = (size_t)M * N * 4;
+  if (ks > 1 && (size_t)ks * per > part_bytes) ks = (int)(part_bytes / per);
+  return ks > 1 ? ks : 1;
 }
 
 template <int NT>
@@ -787,13 +782,14 @@ static cudaError_t launch_w8a8(const GemvArgs& g, cudaStream_t s) {
   ta.n_tiles = (g.N + kTcBM - 1) / kTcBM;
   ta.kblocks = (g.K + kTcBK - 1) / kTcBK;
   ta.fp8 = 1;
-  ta.ksplit = gemm_tc_ksplit(g.M, g.N, g.K);
   ta.part = g.part;
-  if (ta.ksplit > 1 && (!g.part || g.part_bytes < gemm_tc_partial_bytes(g.M, g.N, g.K))) ta.ksplit = 1;
-  if (!encode_kblocks(&tmW, g.W, (uint64_t)g.N, (uint64_t)g.K, (uint64_t)ta.kblocks, kTcBM, kW8Kbs) ||
-      !encode_kblocks(&tmA, g.q8, (uint64_t)g.M, (uint64_t)g.ldq, (uint64_t)ta.kblocks, NT, kW8Kbs) ||
+  ta.ksplit = g.part ? w8_ksplit(g.M, g.N, g.K, g.part_bytes) : 1;
+  if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.W, g.K, g.N, (uint64_t)g.K, kTcBK, kTcBM,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.q8, g.K, g.M, (uint64_t)g.ldq, kTcBK, NT,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tmS, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.sq, (uint64_t)g.ldsq, (uint64_t)ta.kblocks,
-                 (uint64_t)g.ldsq * 4, NT, kW8Kbs, CU_TENSOR_MAP_SWIZZLE_NONE))
+                 (uint64_t)g.ldsq * 4, NT, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const int smem = w8_smem_bytes<NT>();
   auto kern = gemm_w8a8_kernel<NT>;
@@ -803,7 +799,7 @@ static cudaError_t launch_w8a8(const GemvArgs& g, cudaStream_t s) {
   int grid = num_sms();
   if (grid > nitems) grid = nitems;
   trace_pre(K_GEMM_TC, s);
-  e = launch_k(kern, dim3(grid), dim3(kTcThreads), smem, s, g.pdl != 0, tmW, tmA, tmS, ta);
+  e = launch_k(kern, dim3(grid), dim3(kW8Threads), smem, s, g.pdl != 0, tmW, tmA, tmS, ta);
   trace_post(K_GEMM_TC, s);
   if (e != cudaSuccess || ta.ksplit == 1) return e;
   const size_t total = (size_t)g.M * g.N;
@@ -917,8 +913,10 @@ cudaError_t launch_wait_check(const void* probe, void* out, cudaStream_t s) {
 cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   if (g.q8) {  // W8A8: E4M3 activation codes with per-(token, k block) scales
     if (!fp8 || g.K % 128 || g.ldq % 16 || g.ldsq % 128) return cudaErrorInvalidValue;
-    if (tc_nt(g.M) == 64) return launch_w8a8<64>(g, s);
-    return launch_w8a8<128>(g, s);
+    const int nt = w8_nt(g.M);
+    if (nt == 64) return launch_w8a8<64>(g, s);
+    if (nt == 128) return launch_w8a8<128>(g, s);
+    return launch_w8a8<256>(g, s);
   }
   if (tc_nt(g.M) == 64) return launch_tc<64, false>(g, fp8, s);
   return launch_tc<128, false>(g, fp8, s);
