@@ -153,6 +153,44 @@ __device__ __forceinline__ void tc_epi_elem(const GemvArgs& a, int m, int n, flo
   }
 }
 
+// The end-of-item epilogue of one thread: weight row n, token columns m0 ..
+// m0 + HC - 1 of acc.  The mode is decided once, outside the per-column loops,
+// so that each unrolled loop stays a few hundred instructions (every epilogue
+// warp runs it once per item; one loop holding all modes' code, 64 times over,
+// ran from instruction-cache misses).  The conv update, the one long body,
+// loops over a local copy of acc.
+template <int HC>
+__device__ __forceinline__ void tc_item_store(const GemvArgs& a, int ksplit, float* part, int ks, int n, int m0,
+                                              const float (&acc)[HC], int L) {
+  if (n >= a.N) return;
+  const int mc = min(HC, a.M - m0);
+  if (ksplit > 1) {
+    float* pp = part + ((size_t)ks * a.M + m0) * a.N + n;
+#pragma unroll
+    for (int j = 0; j < HC; ++j)
+      if (j < mc) pp[(size_t)j * a.N] = acc[j];
+  } else if (a.epi == EPI_RESID) {
+    uint16_t* o = a.out + (size_t)m0 * a.ldo + n;
+    const uint16_t* r = a.resid + (size_t)m0 * a.ldr + n;
+#pragma unroll
+    for (int j = 0; j < HC; ++j)
+      if (j < mc) o[(size_t)j * a.ldo] = f32_to_bf16(bf16_to_f32(r[(size_t)j * a.ldr]) + acc[j]);
+  } else if (a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc) {
+    ConvTaps taps;
+    load_taps(a, n - a.xbc0, L, taps);
+    float v[HC];
+#pragma unroll
+    for (int j = 0; j < HC; ++j) v[j] = acc[j];
+#pragma unroll 1
+    for (int j = 0; j < mc; ++j) tc_epi_elem(a, m0 + j, n, v[j], true, taps, L);
+  } else {
+    uint16_t* o = a.out + (size_t)m0 * a.ldo + n;
+#pragma unroll
+    for (int j = 0; j < HC; ++j)
+      if (j < mc) o[(size_t)j * a.ldo] = f32_to_bf16(acc[j]);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 struct TcArgs {
@@ -447,26 +485,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
       }
       if (dead) break;
-      const int n = nt * kTcBM + row;
-      if (n < a.N) {
-        if (ta.ksplit > 1) {
-          float* pp = ta.part + ((size_t)ks * a.M) * a.N + n;
-#pragma unroll
-          for (int j = 0; j < HC; ++j) {
-            const int m = mt * NT + hf * HC + j;
-            if (m < a.M) pp[(size_t)m * a.N] = acc[j];
-          }
-        } else {
-          const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
-          ConvTaps taps;
-          if (conv) load_taps(a, n - a.xbc0, L, taps);
-#pragma unroll
-          for (int j = 0; j < HC; ++j) {
-            const int m = mt * NT + hf * HC + j;
-            if (m < a.M) tc_epi_elem(a, m, n, acc[j], conv, taps, L);
-          }
-        }
-      }
+      tc_item_store<HC>(a, ta.ksplit, ta.part, ks, nt * kTcBM + row, mt * NT + hf * HC, acc, L);
     }
   }
   tc_fence_before();
@@ -633,7 +652,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
     const int hf = (warp - kW8EpiWarp0) >> 2;
     const int row = 32 * q + lane;
     pdl_wait();
-    float2 acc[HC / 2];
+    float acc[HC];
     float* cw = reinterpret_cast<float*>(smem + Cfg::kC) + (warp - kW8EpiWarp0) * HC;  // this warp's c
     const uint32_t cws = smem_addr(cw);
     int gk = 0;
@@ -642,7 +661,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
       tc_item(ta, item, nt, mt, kb0, kb1);
       const int ks = item % ta.ksplit;
 #pragma unroll
-      for (int j = 0; j < HC / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
+      for (int j = 0; j < HC; ++j) acc[j] = 0.0f;
       for (int kb = kb0; kb < kb1; ++kb, ++gk) {
         const int s = gk % S, tb = gk % NB;
         const float sw = bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb));
@@ -670,10 +689,15 @@ __global__ void __launch_bounds__(kW8Threads, 1)
 #pragma unroll
           for (int i4 = 0; i4 < 2; ++i4) {
             const float4 c4 = lds_f4_ordered(cws + (c0 + 4 * i4) * 4);
-            float2& a0 = acc[(c0 + 4 * i4) / 2];
-            float2& a1 = acc[(c0 + 4 * i4) / 2 + 1];
-            a0 = ffma2(make_float2(c4.x, c4.y), make_float2(v[4 * i4], v[4 * i4 + 1]), a0);
-            a1 = ffma2(make_float2(c4.z, c4.w), make_float2(v[4 * i4 + 2], v[4 * i4 + 3]), a1);
+            const int j = c0 + 4 * i4;
+            const float2 a0 = ffma2(make_float2(c4.x, c4.y), make_float2(v[4 * i4], v[4 * i4 + 1]),
+                                    make_float2(acc[j], acc[j + 1]));
+            const float2 a1 = ffma2(make_float2(c4.z, c4.w), make_float2(v[4 * i4 + 2], v[4 * i4 + 3]),
+                                    make_float2(acc[j + 2], acc[j + 3]));
+            acc[j] = a0.x;
+            acc[j + 1] = a0.y;
+            acc[j + 2] = a1.x;
+            acc[j + 3] = a1.y;
           }
         }
         tc_fence_before();
@@ -681,26 +705,7 @@ __global__ void __launch_bounds__(kW8Threads, 1)
         if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
       }
       if (dead) break;
-      const int n = nt * kTcBM + row;
-      if (n < a.N) {
-        if (ta.ksplit > 1) {
-          float* pp = ta.part + ((size_t)ks * a.M) * a.N + n;
-#pragma unroll
-          for (int j = 0; j < HC; ++j) {
-            const int m = mt * NT + hf * HC + j;
-            if (m < a.M) pp[(size_t)m * a.N] = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-          }
-        } else {
-          const bool conv = a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc;
-          ConvTaps taps;
-          if (conv) load_taps(a, n - a.xbc0, L, taps);
-#pragma unroll
-          for (int j = 0; j < HC; ++j) {
-            const int m = mt * NT + hf * HC + j;
-            if (m < a.M) tc_epi_elem(a, m, n, (j & 1) ? acc[j / 2].y : acc[j / 2].x, conv, taps, L);
-          }
-        }
-      }
+      tc_item_store<HC>(a, ta.ksplit, ta.part, ks, nt * kTcBM + row, mt * NT + hf * HC, acc, L);
     }
   }
   tc_fence_before();
