@@ -297,15 +297,19 @@ int m2_copy(void* dst, const void* src, size_t bytes, cudaStream_t stream);
  *             the xBC part holds the conv output; the raw xBC is in the ring)
  *   M2_WS_U   prefill conv output [T][d_xbc] bf16
  *   M2_WS_Y   SSM output y [rows][d_inner] fp32
- *   M2_WS_G   gated-norm output [rows][d_inner] (bf16 when the out_proj runs
- *             on the tensor cores with bf16 activations)
+ *   M2_WS_G   gated-norm output [rows][d_inner], when a separate kernel
+ *             writes it (tensor-core projections): bf16 for an out_proj with
+ *             bf16 weights; for E4M3 weights f16, row r prescaled by an exact
+ *             power of two 2^j whose inverse is M2_WS_UNSCALE's entry rows + r
+ *   M2_WS_UNSCALE  fp32 [2][rows]: the inverse prescale of each row of the
+ *             in_proj input (first half) and of the out_proj input (second)
  *   M2_WS_Q8  W8A8: E4M3 codes [T][rup16(max(hidden, d_inner))] of the last
  *             projection's input; M2_WS_SQ: its fp32 block scales
  *             [d_inner/128][rup128(T)].
  * Contents are valid after the call completes and until the next call on the
  * same workspace.  Host only; returns M2_OK or M2_ERR_ARG. */
 enum { M2_WS_KIND_DECODE = 0, M2_WS_KIND_PREFILL = 1, M2_WS_KIND_PREFILL_W8A8 = 2 };
-enum { M2_WS_XN = 0, M2_WS_ZX, M2_WS_U, M2_WS_Y, M2_WS_G, M2_WS_Q8, M2_WS_SQ, M2_WS_COUNT };
+enum { M2_WS_XN = 0, M2_WS_ZX, M2_WS_U, M2_WS_Y, M2_WS_G, M2_WS_Q8, M2_WS_SQ, M2_WS_UNSCALE, M2_WS_COUNT };
 int m2_workspace_map(const m2_dims* dims, int32_t kind, int32_t n, const int32_t* cu_seqlens, size_t* offsets,
                      int32_t n_offsets);
 

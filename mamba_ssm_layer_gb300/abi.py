@@ -274,7 +274,7 @@ def m2_wait_check(probe, out, stream=None, check=True) -> int:
 
 
 M2_WS_KIND_DECODE, M2_WS_KIND_PREFILL, M2_WS_KIND_PREFILL_W8A8 = 0, 1, 2
-WS_REGIONS = ("xn", "zx", "u", "y", "g", "q8", "sq")
+WS_REGIONS = ("xn", "zx", "u", "y", "g", "q8", "sq", "unscale")
 
 
 def m2_workspace_map(dims, kind: int, n: int, cu_seqlens=None) -> dict:

@@ -22,9 +22,10 @@
 //               (plain 2-D map) into a 4-stage ring; bf16 weights go straight
 //               into a 4-stage ring of 128-byte-swizzled tiles.  It does not
 //               wait for the previous kernel: weights are never its output.
-//   warp 22     activation producer (lane 0): after the dependency wait, TMA of
-//               the bf16 activation tile [NT][128] (two 64-wide boxes, 128-byte
-//               swizzle = the UMMA K-major canonical layout), 3-4 stages;
+//   warp 22     activation producer (lane 0): after the dependency wait, one
+//               3-D tensor copy per k block of the bf16 activation tile [NT][128]
+//               (two 64-wide halves, 128-byte swizzle = the UMMA K-major
+//               canonical layout), 3-4 stages;
 //   warps 2-5   converters: E4M3 tile -> bf16 tile in the swizzled layout the
 //               MMA descriptor expects (double-buffered);
 //   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each; W8A8: 4 of
@@ -54,19 +55,17 @@ constexpr int kTcTmemBufs = 4;   // k-block partials in TMEM
 constexpr int kTcBM = 128;       // weight rows per tile (UMMA M)
 constexpr int kTcBK = 128;       // k per block (= scale block)
 
-template <int NT, bool AQ8 = false>
+template <int NT>
 struct TcLayout {
-  // offsets from a 1024-byte aligned base
-  // w8a16 / bf16: W ring at 0 (fp8: 4 x 16 KB E4M3; bf16: 4 x 32 KB swizzled,
-  // through kWbf), converted bf16 tiles at kWbf, bf16 activation tiles at kA.
-  // W8A8: 4 x 16 KB swizzled E4M3 weight tiles at 0, E4M3 activation tiles at kA.
-  static constexpr int kAStages = AQ8 ? 4 : (NT <= 64 ? 4 : 3);
-  static constexpr int kABytes = NT * kTcBK * (AQ8 ? 1 : 2);  // one activation stage
+  // offsets from a 1024-byte aligned base: W ring at 0 (fp8: 4 x 16 KB E4M3;
+  // bf16: 4 x 32 KB swizzled, through kWbf), converted 16-bit weight tiles at
+  // kWbf, 16-bit activation tiles at kA
+  static constexpr int kAStages = NT <= 64 ? 4 : 3;
+  static constexpr int kABytes = NT * kTcBK * 2;  // one activation stage
   static constexpr int kW = 0;
   static constexpr int kWbf = 65536;
-  static constexpr int kA = AQ8 ? 65536 : 131072;
-  static constexpr int kSc = kA + kAStages * kABytes;                    // W8A8: token scales, one slot per TMEM buffer
-  static constexpr int kBars = kSc + (AQ8 ? kTcTmemBufs * NT * 4 : 0);
+  static constexpr int kA = 131072;
+  static constexpr int kBars = kA + kAStages * kABytes;
 };
 
 struct TcBars {
@@ -74,7 +73,6 @@ struct TcBars {
   uint64_t wbf_full[2];
   uint64_t a_full[4];
   uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
-  uint64_t sc_full[kTcTmemBufs];  // W8A8: the token scales of a k block have landed
   uint32_t tmem_base;
 };
 
@@ -87,9 +85,9 @@ __device__ __forceinline__ bool kblock_done(TcBars* bars, int j) {
   return mbar_wait(&bars->mma_done[j % kTcTmemBufs], (uint32_t)(j / kTcTmemBufs) & 1u);
 }
 
-template <int NT, bool AQ8 = false>
+template <int NT>
 constexpr int tc_smem_bytes() {
-  return TcLayout<NT, AQ8>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
+  return TcLayout<NT>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
 }
 
 // ------------------------------------------------------------------ PTX helpers
@@ -112,6 +110,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two_bytes) {
       : "=f"(lo), "=f"(hi)
       : "r"(h2));
   return pack_bf16x2(lo, hi);
+}
+
+// Two E4M3 -> two f16, exactly (every E4M3 value is an f16 normal).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two_bytes));
+  return h2;
 }
 
 // Conv taps of one channel: history taps 0..L-1 (oldest first) and the tap
@@ -197,6 +202,7 @@ struct TcArgs {
   GemvArgs g;      // operand pointers, sizes, epilogue
   int32_t m_tiles, n_tiles, kblocks;
   int32_t fp8;
+  int32_t f16;     // fp8 weights with prescaled f16 activations: f16 x f16 MMAs, columns unscaled
   int32_t ksplit;  // > 1: k blocks split over work items, fp32 partials to `part`
   float* part;     // [ksplit][M][N]
 };
@@ -212,10 +218,10 @@ __device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int& nt, int
   kb1 = (int)((long long)ta.kblocks * (ks + 1) / ta.ksplit);
 }
 
-template <int NT, bool AQ8>
+template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, const TcArgs ta) {
-  using Lay = TcLayout<NT, AQ8>;
+  using Lay = TcLayout<NT>;
   constexpr int SA = Lay::kAStages;
   const GemvArgs& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
@@ -240,7 +246,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int b = 0; b < kTcTmemBufs; ++b) {
       mbar_init(&bars->mma_done[b], 1);
       mbar_init(&bars->tmem_empty[b], kTcEpiWarps);
-      mbar_init(&bars->sc_full[b], 1);
     }
     fence_mbar_init();
   }
@@ -272,12 +277,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (gk >= kTcWStages) {
             // the slot's previous tile: freed by the converters (w8a16), or by
             // the completion of its k block's MMAs
-            const bool ok = (ta.fp8 && !AQ8) ? mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)
-                                             : kblock_done(bars, gk - kTcWStages);
+            const bool ok = ta.fp8 ? mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)
+                                   : kblock_done(bars, gk - kTcWStages);
             if (!ok) dead = true;
           }
           if (dead) break;
-          if (ta.fp8) {  // E4M3 tile (plain for the converters; 128-byte swizzled for the W8A8 MMA)
+          if (ta.fp8) {  // E4M3 tile, plain, for the converters
             mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK);
             tma_load_2d(smem + Lay::kW + s * kTcBM * kTcBK, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
           } else {
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_wait();  // A is written by the previous kernel
     if (lane == 0) {
       const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
-      int gk = 0, a_iss = 0, sc_iss = 0;  // k blocks whose activation tile / token scales are issued
+      int gk = 0, a_iss = 0;  // k blocks whose activation tile is issued
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
@@ -308,43 +313,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (dead) break;
           uint8_t* abuf = smem + Lay::kA + s * Lay::kABytes;
           mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);
-          if (AQ8) {  // E4M3 codes: one 128-byte-swizzled box of NT rows x 128 k
-            tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
-            a_iss = gk + 1;
-            // the k block's token scales into the slot of its TMEM buffer, once the
-            // epilogue has finished with the k block that used the slot before
-            const int tb = gk % kTcTmemBufs;
-            if (gk >= kTcTmemBufs && !mbar_wait(&bars->tmem_empty[tb], ((gk / kTcTmemBufs) - 1) & 1)) dead = true;
-            if (dead) break;
-            mbar_arrive_expect_tx(&bars->sc_full[tb], NT * 4);
-            bulk_g2s(smem + Lay::kSc + tb * NT * 4, a.sq + (size_t)kb * a.ldsq + (size_t)mt * NT, NT * 4,
-                     &bars->sc_full[tb], pola);
-            sc_iss = gk + 1;
-          } else {
-            tma_load_2d(abuf, &tmA, kb * kTcBK, mt * NT, &bars->a_full[s], pola);
-            tma_load_2d(abuf + NT * 128, &tmA, kb * kTcBK + 64, mt * NT, &bars->a_full[s], pola);
-            a_iss = gk + 1;
-          }
+          tma_load_3d(abuf, &tmA, 0, mt * NT, kb * 2, &bars->a_full[s], pola);  // both halves
+          a_iss = gk + 1;
         }
       }
       // drain: everything issued has landed before the CTA may exit
       for (int k = max(0, a_iss - SA); k < a_iss; ++k)
         if (!mbar_drain(&bars->a_full[k % SA], (k / SA) & 1)) break;
-      for (int k = max(0, sc_iss - kTcTmemBufs); k < sc_iss; ++k)
-        if (!mbar_drain(&bars->sc_full[k % kTcTmemBufs], (k / kTcTmemBufs) & 1)) break;
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = tc_idesc(kTcBM, NT);
-      constexpr uint32_t idesc8 = tc_idesc_f8(kTcBM, NT);
+      const uint32_t idesc = ta.f16 ? tc_idesc_f16(kTcBM, NT) : tc_idesc(kTcBM, NT);
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % kTcWStages, b = gk & 1, sa = gk % SA, tb = gk % kTcTmemBufs;
-          if (ta.fp8 && !AQ8) {
+          if (ta.fp8) {
             if (!mbar_wait(&bars->wbf_full[b], (gk / 2) & 1)) dead = true;
           } else {
             if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
@@ -354,14 +341,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dead = true;
           if (dead) break;
           tc_fence_after();
-          if (AQ8) {
-            // E4M3 x E4M3: one 128-byte swizzle row holds the whole 128-k block; K = 32 per MMA
-            const uint32_t wb = smem_addr(smem + Lay::kW + s * kTcBM * kTcBK);
-            const uint32_t ab = smem_addr(smem + Lay::kA + sa * Lay::kABytes);
-#pragma unroll
-            for (int kk = 0; kk < kTcBK / 32; ++kk)
-              tc_mma_f8(tmem + tb * NT, sw128_desc(wb + kk * 32), sw128_desc(ab + kk * 32), idesc8, kk > 0 ? 1 : 0);
-          } else {
+          {
             const uint32_t wb = ta.fp8 ? smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2)
                                        : smem_addr(smem + Lay::kW + s * kTcBM * kTcBK * 2);
             const uint32_t ab = smem_addr(smem + Lay::kA + sa * Lay::kABytes);
@@ -384,7 +364,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp < 6) {
     // -------------------------------------------------------- converters
-    if (ta.fp8 && !AQ8) {
+    if (ta.fp8) {
       const int ct = tid - 64;  // 0..127
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
@@ -406,15 +386,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kTcBK + 16 * j);
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
             uint4 o0, o1;
-            o0.x = e4m3x2_to_bf16x2(w4[0]);
-            o0.y = e4m3x2_to_bf16x2(w4[0] >> 16);
-            o0.z = e4m3x2_to_bf16x2(w4[1]);
-            o0.w = e4m3x2_to_bf16x2(w4[1] >> 16);
-            o1.x = e4m3x2_to_bf16x2(w4[2]);
-            o1.y = e4m3x2_to_bf16x2(w4[2] >> 16);
-            o1.z = e4m3x2_to_bf16x2(w4[3]);
-            o1.w = e4m3x2_to_bf16x2(w4[3] >> 16);
-            // bf16 chunks c, c+1 (8 elements each) of atom j/4, 128-byte swizzle
+            if (ta.f16) {  // one exact conversion per pair
+              o0.x = e4m3x2_to_f16x2(w4[0]);
+              o0.y = e4m3x2_to_f16x2(w4[0] >> 16);
+              o0.z = e4m3x2_to_f16x2(w4[1]);
+              o0.w = e4m3x2_to_f16x2(w4[1] >> 16);
+              o1.x = e4m3x2_to_f16x2(w4[2]);
+              o1.y = e4m3x2_to_f16x2(w4[2] >> 16);
+              o1.z = e4m3x2_to_f16x2(w4[3]);
+              o1.w = e4m3x2_to_f16x2(w4[3] >> 16);
+            } else {
+              o0.x = e4m3x2_to_bf16x2(w4[0]);
+              o0.y = e4m3x2_to_bf16x2(w4[0] >> 16);
+              o0.z = e4m3x2_to_bf16x2(w4[1]);
+              o0.w = e4m3x2_to_bf16x2(w4[1] >> 16);
+              o1.x = e4m3x2_to_bf16x2(w4[2]);
+              o1.y = e4m3x2_to_bf16x2(w4[2] >> 16);
+              o1.z = e4m3x2_to_bf16x2(w4[3]);
+              o1.w = e4m3x2_to_bf16x2(w4[3] >> 16);
+            }
+            // 16-bit chunks c, c+1 (8 elements each) of atom j/4, 128-byte swizzle
             const int atom = j >> 2, c = (j & 3) * 2, r8 = row & 7;
             uint8_t* base = dst + atom * kTcBM * 128 + row * 128;
             *reinterpret_cast<uint4*>(base + ((c ^ r8) << 4)) = o0;
@@ -453,8 +444,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb)) : 1.0f;
         // the TMEM loads below are warp-collective: the warp decides together
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1))) dead = true;
-        if (AQ8 && !dead && !__all_sync(0xffffffffu, mbar_wait(&bars->sc_full[tb], (gk / kTcTmemBufs) & 1)))
-          dead = true;
         if (dead) break;
         tc_fence_after();
         // 16 columns per TMEM load: two loads in flight before one wait at
@@ -464,28 +453,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int c0 = 0; c0 < HC; c0 += 16) {
           float v[16];
           tmem_ld16(ta_ + c0, v);
-          if (AQ8) {
-            // token scales of this k block, staged in shared memory by the activation producer
-            const uint32_t sq = smem_addr(smem + Lay::kSc + (tb * NT + hf * HC + c0) * 4);
 #pragma unroll
-            for (int i4 = 0; i4 < 4; ++i4) {
-              const float4 t4 = lds_f4_ordered(sq + 16 * i4);
-              acc[c0 + 4 * i4 + 0] = fmaf(s * t4.x, v[4 * i4 + 0], acc[c0 + 4 * i4 + 0]);
-              acc[c0 + 4 * i4 + 1] = fmaf(s * t4.y, v[4 * i4 + 1], acc[c0 + 4 * i4 + 1]);
-              acc[c0 + 4 * i4 + 2] = fmaf(s * t4.z, v[4 * i4 + 2], acc[c0 + 4 * i4 + 2]);
-              acc[c0 + 4 * i4 + 3] = fmaf(s * t4.w, v[4 * i4 + 3], acc[c0 + 4 * i4 + 3]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(s, v[i], acc[c0 + i]);
-          }
+          for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(s, v[i], acc[c0 + i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->tmem_empty[tb]);
       }
       if (dead) break;
-      tc_item_store<HC>(a, ta.ksplit, ta.part, ks, nt * kTcBM + row, mt * NT + hf * HC, acc, L);
+      const int m0 = mt * NT + hf * HC;
+      if (ta.f16) {  // the activation rows' prescale 2^j, undone exactly
+#pragma unroll
+        for (int j = 0; j < HC; ++j)
+          if (m0 + j < a.M) acc[j] *= __ldg(a.unscale + m0 + j);
+      }
+      tc_item_store<HC>(a, ta.ksplit, ta.part, ks, nt * kTcBM + row, m0, acc, L);
     }
   }
   tc_fence_before();
@@ -817,13 +799,13 @@ static cudaError_t launch_w8a8(const GemvArgs& g, cudaStream_t s) {
   return e;
 }
 
-template <int NT, bool AQ8>
+template <int NT>
 static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   static int done_mask[64] = {0};
   CUtensorMap tmW, tmA;
   if (fp8) {
     if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.W, g.K, g.N, (uint64_t)g.K, kTcBK, kTcBM,
-                   AQ8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   } else {
     if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.W, g.K, g.N, (uint64_t)g.K * 2, 64, kTcBM,
@@ -836,19 +818,27 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
   ta.n_tiles = (g.N + kTcBM - 1) / kTcBM;
   ta.kblocks = (g.K + kTcBK - 1) / kTcBK;
   ta.fp8 = fp8 ? 1 : 0;
+  ta.f16 = (fp8 && g.act == ACT_PREPARED && g.unscale) ? 1 : 0;
   ta.ksplit = gemm_tc_ksplit(g.M, g.N, g.K);
   ta.part = g.part;
   if (ta.ksplit > 1 && (!g.part || g.part_bytes < gemm_tc_partial_bytes(g.M, g.N, g.K))) ta.ksplit = 1;
-  if (AQ8) {
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.q8, g.K, g.M, (uint64_t)g.ldq, kTcBK, NT,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+  {
+    // bf16 activations as {64-element half of a k block, rows, halves}: one
+    // copy of box {64, NT, 2} lands the two 128-byte-swizzled [NT][64] halves
+    // of a k block back to back
+    auto enc = tensor_map_encoder();
+    const cuuint64_t dims[3] = {64, (cuuint64_t)g.M, (cuuint64_t)(g.K / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)g.lda * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)NT, 2};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (!enc || g.K % 64 ||
+        enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(g.A), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
-  } else if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.A, g.K, g.M, (uint64_t)g.lda * 2, 64,
-                        NT, CU_TENSOR_MAP_SWIZZLE_128B)) {
-    return cudaErrorInvalidValue;
   }
-  const int smem = tc_smem_bytes<NT, AQ8>();
-  auto kern = gemm_tc_kernel<NT, AQ8>;
+  const int smem = tc_smem_bytes<NT>();
+  auto kern = gemm_tc_kernel<NT>;
   cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
   if (e != cudaSuccess) return e;
   const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
@@ -923,8 +913,8 @@ cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
     if (nt == 128) return launch_w8a8<128>(g, s);
     return launch_w8a8<256>(g, s);
   }
-  if (tc_nt(g.M) == 64) return launch_tc<64, false>(g, fp8, s);
-  return launch_tc<128, false>(g, fp8, s);
+  if (tc_nt(g.M) == 64) return launch_tc<64>(g, fp8, s);
+  return launch_tc<128>(g, fp8, s);
 }
 
 int status_gemm_tc(int clear) { return tu_status(clear); }

@@ -215,10 +215,13 @@ static size_t prefill_ws_bound(const m2_dims& d, int T, int nseq, bool w8a8 = tr
   return prefill_ws(d, T, nseq, (T + 127) / 128 + nseq, w8a8);
 }
 
-// Whether a projection over M rows consumes f16 prescaled activations (the
-// E4M3 GEMV paths, M <= 8) or bf16 ones (bf16 weights, or the tensor-core GEMM).
+// Whether a projection consumes f16 activation rows, each prescaled by an
+// exact power of two (E4M3 weights: their f16 conversion is one instruction a
+// pair, in the GEMV and in the tensor-core GEMM's f16 x f16 MMAs), or bf16 rows
+// (bf16 weights: both MMA operands must have one type).
 static bool proj_f16(const m2_weight& w, int M) {
-  return w.fmt == M2_W_FP8_BLOCK128 && !gemm_tc_supported(M, w.n, w.k, true);
+  (void)M;
+  return w.fmt == M2_W_FP8_BLOCK128;
 }
 
 static GemvArgs proj_args(const m2_weight& w, const uint16_t* A, int lda, int M, uint16_t* out, int ldo,
@@ -883,6 +886,7 @@ int m2_workspace_map(const m2_dims* dims, int32_t kind, int32_t n, const int32_t
     offsets[M2_WS_ZX] = m.zxu;
     offsets[M2_WS_Y] = m.y;
     offsets[M2_WS_G] = m.g;
+    offsets[M2_WS_UNSCALE] = m.unscale;
     return M2_OK;
   }
   if (kind != M2_WS_KIND_PREFILL && kind != M2_WS_KIND_PREFILL_W8A8) return M2_ERR_ARG;
@@ -899,6 +903,7 @@ int m2_workspace_map(const m2_dims* dims, int32_t kind, int32_t n, const int32_t
   offsets[M2_WS_U] = m.u;
   offsets[M2_WS_Y] = m.y;
   offsets[M2_WS_G] = m.g;
+  offsets[M2_WS_UNSCALE] = m.unscale;
   if (kind == M2_WS_KIND_PREFILL_W8A8) {
     offsets[M2_WS_Q8] = m.q8;
     offsets[M2_WS_SQ] = m.sq;

@@ -23,6 +23,10 @@ __host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// kind::f16 instruction descriptor with f16 A and B (format 0), D fp32, both K-major.
+__host__ __device__ constexpr uint32_t tc_idesc_f16(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
 // kind::f8f6f4 instruction descriptor: D fp32, A and B E4M3 (format 0), both K-major.
 __host__ __device__ constexpr uint32_t tc_idesc_f8(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);

@@ -48,10 +48,12 @@ def state_rel_err(got_h, ref_h) -> float:
 # and bit-equal rings and positions.
 #
 # The GPU's codes are read back from the call's workspace: R3 and R4 always;
-# R5 where the gated norm writes bf16 rows (tensor-core projections: decode of
-# more than 8 rows, prefill of more than 8 tokens on the w8a16 arm); R6 (the
-# output rows) together with R5 only, since R6's exact value depends on every
-# R5 code.
+# R5 where a separate kernel writes the gated norm's rows (tensor-core
+# projections: decode of more than 8 rows, prefill of more than 8 tokens on the
+# w8a16 arm) -- bf16 rows as they are, and the f16 rows of an E4M3 out_proj
+# (each prescaled by an exact power of two) unscaled and taken as the bf16
+# codes they hold; R6 (the output rows) together with R5 only, since R6's
+# exact value depends on every R5 code.
 
 
 def _rup(v, a):
@@ -72,6 +74,22 @@ def _u16(ws, off, rows, cols, sel=None):
     return t.cpu().numpy().view(np.uint16)
 
 
+def _g_codes(ws, wm, rows, di, sel, g_f16):
+    """The gated norm's rows as bf16 codes: read as they are (bf16), or as f16
+    rows times their unscale (E4M3 out_proj; the second half of the unscale
+    region), rounded to bf16 (exact for every value the f16 row holds in its
+    normal range)."""
+    import torch
+    raw = _u16(ws, wm["g"], rows, di, sel)
+    if not g_f16:
+        return raw.copy()
+    from oracle import oracle as orc
+    us = ws[wm["unscale"]: wm["unscale"] + 2 * rows * 4].view(torch.float32)[rows:].cpu().numpy().astype(np.float64)
+    us = us[sel] if sel is not None else us
+    vals = raw.view(np.float16).astype(np.float64) * np.asarray(us).reshape(-1, 1)
+    return orc.f64_array_to_bf16(vals)
+
+
 def _u8(ws, off, rows, cols, sel=None):
     t = ws[off: off + rows * cols].view(rows, cols)
     if sel is not None:
@@ -79,10 +97,10 @@ def _u8(ws, off, rows, cols, sel=None):
     return t.cpu().numpy()
 
 
-def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None):
+def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None, g_f16=False):
     """Per batch row (or for the rows in `only`, others None), the GPU's codes
     of the last decode step: R3 (z, raw xBC from the ring slot just written,
-    dt) and R4; R5 and R6 for B > 8."""
+    dt) and R4; R5 and R6 for B > 8.  g_f16: the out_proj has E4M3 weights."""
     from mamba_ssm_layer_gb300 import abi
     di, dx, n_in = _dd(d)
     ldz = _rup(n_in, 8)
@@ -90,7 +108,7 @@ def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None):
     sel = list(range(B)) if only is None else list(only)
     wm = abi.m2_workspace_map(abi.dims_struct(d), abi.M2_WS_KIND_DECODE, B)
     zxu_s = _u16(ws, wm["zx"], B, ldz, sel)
-    g_s = _u16(ws, wm["g"], B, di, sel) if B > 8 else None
+    g_s = _g_codes(ws, wm, B, di, sel, g_f16) if B > 8 else None
     zxu = {b: zxu_s[i] for i, b in enumerate(sel)}
     g = None if g_s is None else {b: g_s[i] for i, b in enumerate(sel)}
     out = []
@@ -110,11 +128,12 @@ def decode_candidates(ws, B, d, ring_after, pos_before, hidden_out, only=None):
     return out
 
 
-def prefill_candidates(ws, cu, d, hidden_out, r5_available, a=0, b=None, w8a8=False):
+def prefill_candidates(ws, cu, d, hidden_out, r5_available, a=0, b=None, w8a8=False, g_f16=False):
     """The GPU's codes of token rows a..b-1 of a (varlen) prefill over the
-    sequences of cu: R3, R4, and R5 and R6 when the gated norm wrote bf16 rows
-    (hidden_out: those rows' outputs).  W8A8 arm: the out_proj's E4M3 input
-    codes and block scales ("Q5") and R6."""
+    sequences of cu: R3, R4, and R5 and R6 when a separate kernel wrote the
+    gated norm's rows (hidden_out: those rows' outputs; g_f16: the out_proj has
+    E4M3 weights).  W8A8 arm: the out_proj's E4M3 input codes and block scales
+    ("Q5") and R6."""
     from mamba_ssm_layer_gb300 import abi
     di, dx, n_in = _dd(d)
     cu = [int(v) for v in cu]
@@ -127,7 +146,7 @@ def prefill_candidates(ws, cu, d, hidden_out, r5_available, a=0, b=None, w8a8=Fa
     u = _u16(ws, wm["u"], T, dx, slice(a, b))
     c = {"R3": zx[:, :n_in].copy(), "R4": u.copy()}
     if r5_available:
-        c["R5"] = _u16(ws, wm["g"], T, di, slice(a, b)).copy()
+        c["R5"] = _g_codes(ws, wm, T, di, slice(a, b), g_f16)
         c["R6"] = np.asarray(hidden_out, np.uint16).copy()
     elif w8a8:
         import torch

@@ -178,7 +178,7 @@ def _run_decode(lay, B, steps, seqs_checked, hidden_key, warm=0):
         dl.decode(x, st, ws)
         _sync()
         got = bits_u16(x)
-        cand = decode_candidates(ws, B, d, bits_u16(st[1]), pos_before, got)
+        cand = decode_candidates(ws, B, d, bits_u16(st[1]), pos_before, got, g_f16=lay["out_fmt"] == "fp8")
         for b in seqs_checked:
             ref = np.ascontiguousarray(hid[b:b + 1])
             log.add(ol.run_decided(ref, *ost[b], cand[b]), (t, b))
@@ -255,7 +255,7 @@ def _prefill_case(lay, T, warm_decode, key):
     dl.prefill(x, (st[0][0], st[1][0], st[2][:1]), ws)
     _sync()
     got = bits_u16(x)
-    cand = prefill_candidates(ws, [0, T], d, got, r5_available=T > 8)
+    cand = prefill_candidates(ws, [0, T], d, got, r5_available=T > 8, g_f16=lay["out_fmt"] == "fp8")
     ref = hid.copy()
     log.add(ol.run_decided(ref, *ost, cand), "prefill")
     rep = log.check()

@@ -64,7 +64,8 @@ def test_stack8_prefill_and_256_decode_steps_sampled_sequence():
         dl.prefill_varlen(xall, cu, st[l], ws)
         torch.cuda.synchronize()
         got = bits_u16(xall[a:b])
-        cand = prefill_candidates(ws, cu, d, got, r5_available=True, a=a, b=b)
+        cand = prefill_candidates(ws, cu, d, got, r5_available=True, a=a, b=b,
+                                  g_f16=layers[l]["out_fmt"] == "fp8")
         logs[l].add(ols[l].run_decided(x_or, *ost[l], cand), ("prefill", l))
         assert floored_rel_err(bf16_to_f64(got), bf16_to_f64(x_or), axis=-1) <= TOL_BF16, l
     # ---- 256 decode steps of all 16 sequences
@@ -78,7 +79,8 @@ def test_stack8_prefill_and_256_decode_steps_sampled_sequence():
             torch.cuda.synchronize()
             got = bits_u16(x[samp:samp + 1])
             ring = {samp: bits_u16(st[l][1][samp:samp + 1])[0]}
-            cand = decode_candidates(ws, S, d, ring, pos_before, np.repeat(got, S, axis=0), only=[samp])[samp]
+            cand = decode_candidates(ws, S, d, ring, pos_before, np.repeat(got, S, axis=0), only=[samp],
+                                     g_f16=layers[l]["out_fmt"] == "fp8")[samp]
             logs[l].add(ols[l].run_decided(row, *ost[l], cand), ("decode", k, l))
             worst = max(worst, floored_rel_err(bf16_to_f64(got), bf16_to_f64(row), axis=-1))
     assert abi.m2_device_status() == abi.M2_OK

@@ -49,7 +49,7 @@ def _varlen_case(lay, lens, warm, key, w8a8=False):
         pos_before = st[2].cpu().numpy().copy()
         dl.decode(x, st, wsd)
         torch.cuda.synchronize()
-        cand = decode_candidates(wsd, n, d, bits_u16(st[1]), pos_before, bits_u16(x))
+        cand = decode_candidates(wsd, n, d, bits_u16(st[1]), pos_before, bits_u16(x), g_f16=lay["out_fmt"] == "fp8")
         for i in range(n):
             log.add(ol.run_decided(np.ascontiguousarray(hid[i:i + 1]), *ost[i], cand[i]), ("decode", t, i))
     hid = synth.make_hidden(T, hd, *key, 0)
@@ -62,7 +62,7 @@ def _varlen_case(lay, lens, warm, key, w8a8=False):
     # the gated norm writes bf16 rows on the tensor-core path, except on the
     # W8A8 arm with an E4M3 out_proj (codes and scales instead)
     r5 = T > 8 and not (w8a8 and lay["out_fmt"] == "fp8")
-    cand = prefill_candidates(ws, cu, d, got, r5_available=r5, w8a8=w8a8)
+    cand = prefill_candidates(ws, cu, d, got, r5_available=r5, w8a8=w8a8, g_f16=lay["out_fmt"] == "fp8")
     worst = 0.0
     errs = []
     h = st[0].cpu().numpy()
