@@ -274,9 +274,14 @@ def main():
     K, W = args.steps, args.warmup
     hiddens = [to_dev(synth.make_hidden(B, d["hidden"], synth.WL_8B_DECODE_B1, rank, i)) for i in range(64)]
 
+    # Each step hints the layer that follows it (the next replica, as the next
+    # layer of a model): the first DeviceLayer.AHEAD_BYTES of that layer's
+    # in_proj weights are pulled toward L2 during the step's out_proj.
+    hint = {"on": True}
+
     def step(i):
         dl, st = reps[i % R]
-        dl.decode(hiddens[i % 64], st, ws)
+        dl.decode(hiddens[i % 64], st, ws, ahead=reps[(i + 1) % R][0] if hint["on"] else None)
 
     for i in range(W):
         step(i)
@@ -328,6 +333,24 @@ def main():
                       "steps": reps_g * R, "steps_per_graph": R}
         if graph_info["value"] > eager["value"]:
             ms, K_run = ms_g, reps_g * R
+        # the same graph without the L2 hint, for comparison
+        hint["on"] = False
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=cap):
+            for i in range(R):
+                step(W + i)
+        torch.cuda.current_stream().wait_stream(cap)
+        hint["on"] = True
+        g2.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps_g):
+            g2.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms_g2 = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        graph_info["without_l2_hint"] = {"value": job_rate(reps_g * R * B, world, ms_g2),
+                                         "ms_per_step": ms_g2 / (reps_g * R)}
     except Exception as ex:  # capture unsupported here: the eager number stands
         graph_info = {"error": f"{type(ex).__name__}: {ex}"[:200]}
     ms_step = ms / K_run
@@ -383,7 +406,9 @@ def main():
                    "weights": "e4m3 128x128 block-scaled, bf16 scales", "activations": "bf16",
                    "l2": f"rotating {R} layer replicas ({R * per_rep / 1e9:.2f} GB) > L2 {l2 / 2**20:.0f} MiB",
                    "parallelism": f"replicas x{world}",
-                   "launch": "cuda_graph replay of the library's launches" if use_graph else "eager calls"},
+                   "launch": ("cuda_graph replay of the library's launches" if use_graph else "eager calls")
+                   + "; each step hints the next layer (its first in_proj weights pulled toward L2 during the"
+                   " step's out_proj: mamba2_layer_decode_prefetch)"},
         "step_hbm": {"bytes_per_token": per_rep, "gbs": per_rep / (ms_step / 1e3) / 1e9,
                      "frac": per_rep / (ms_step / 1e3) / 1e9 / hbm_peak},
         "roofline": roof,
@@ -601,7 +626,7 @@ def _bench_e2e(torch, synth, reps, ws, d, B, K):
         for i in range(K):
             devs[0].copy_(host_in[i % 8], non_blocking=True)
             dl, st = reps[i % R]
-            dl.decode(devs[0], st, ws)
+            dl.decode(devs[0], st, ws, ahead=reps[(i + 1) % R][0])
             host_out[0].copy_(devs[0], non_blocking=True)
         e1.record()
         torch.cuda.synchronize()
@@ -627,7 +652,7 @@ def _bench_e2e(torch, synth, reps, ws, d, B, K):
                     ev_in[nb].record(copy)
             comp.wait_event(ev_in[b])
             dl, st = reps[i % R]
-            dl.decode(devs[b], st, ws)
+            dl.decode(devs[b], st, ws, ahead=reps[(i + 1) % R][0])
             ev_dec[b].record(comp)
             with torch.cuda.stream(copy):
                 copy.wait_event(ev_dec[b])
@@ -645,7 +670,7 @@ def _bench_e2e(torch, synth, reps, ws, d, B, K):
         for i in range(K):
             abi.m2_copy(devs[0], host_in[i % 8], nbytes, comp)
             dl, st = reps[i % R]
-            dl.decode(devs[0], st, ws)
+            dl.decode(devs[0], st, ws, ahead=reps[(i + 1) % R][0])
             abi.m2_copy(host_out[0], devs[0], nbytes, comp)
         e1.record()
         torch.cuda.synchronize()

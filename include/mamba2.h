@@ -138,6 +138,23 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* layer, uint16_t* hi
                         float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
                         size_t ws_bytes, cudaStream_t stream);
 
+/* mamba2_layer_decode with a prefetch hint: the device byte range
+ * [prefetch, prefetch + prefetch_bytes) -- typically the first weights the
+ * NEXT call on this stream reads, e.g. the following layer's in_proj -- is
+ * pulled toward L2 while this step's out_proj runs, when the memory system
+ * has spare bandwidth (the out_proj reads its own weights from L2, where the
+ * SSM kernel put them).  A hint only: results are bit-identical to
+ * mamba2_layer_decode, and it applies to the batch <= 8 kernel chain (other
+ * forms ignore it).  prefetch_bytes 0 (or a null prefetch) means no hint.
+ * Errors, returned before anything is launched: M2_ERR_ALIGN if prefetch is
+ * not 16-byte aligned; M2_ERR_ARG if the range is not inside one device
+ * allocation or exceeds M2_PREFETCH_MAX_BYTES.  Other arguments and errors as
+ * mamba2_layer_decode. */
+#define M2_PREFETCH_MAX_BYTES (96ull << 20)
+int mamba2_layer_decode_prefetch(const m2_dims* dims, const m2_layer* layer, uint16_t* hidden, int32_t B,
+                                 float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
+                                 size_t ws_bytes, const void* prefetch, size_t prefetch_bytes, cudaStream_t stream);
+
 /* Select the single-launch batch-1 decode step (enable != 0) or the kernel
  * chain (0, the default) for later mamba2_layer_decode calls in this process.
  * Host setting only; returns the previous setting. */

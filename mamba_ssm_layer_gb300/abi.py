@@ -32,7 +32,8 @@ M2_W_BF16 = 2
 
 # Every entry point include/mamba2.h declares (checked by the host tests).
 EXPORTS = ("m2_strerror", "m2_validate", "m2_workspace_bytes", "mamba2_layer_decode", "mamba2_layer_prefill",
-           "mamba2_layer_decode_noalloc", "mamba2_layer_prefill_varlen", "m2_workspace_bytes_varlen",
+           "mamba2_layer_decode_noalloc", "mamba2_layer_decode_prefetch", "mamba2_layer_prefill_varlen",
+           "m2_workspace_bytes_varlen",
            "mamba2_layer_prefill_varlen_w8a8", "w8a8_gemm", "m2_w8a8_workspace_bytes",
            "w8a16_gemv", "conv1d_update", "mamba2_ssm_step", "m2_device_status", "m2_launch_count",
            "m2_trace_begin", "m2_trace_end", "m2_kernel_name", "m2_kernel_count", "m2_set_fused_decode", "m2_copy",
@@ -86,6 +87,9 @@ def lib():
             l.mamba2_layer_decode.restype = C.c_int
             l.mamba2_layer_decode_noalloc.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P]
             l.mamba2_layer_decode_noalloc.restype = C.c_int
+            l.mamba2_layer_decode_prefetch.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P, SZ,
+                                                       P, SZ, P]
+            l.mamba2_layer_decode_prefetch.restype = C.c_int
             l.mamba2_layer_prefill.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32, P, P, P, P, SZ, P]
             l.mamba2_layer_prefill.restype = C.c_int
             l.mamba2_layer_prefill_varlen.argtypes = [C.POINTER(M2Dims), C.POINTER(M2Layer), P, I32,
@@ -172,6 +176,18 @@ def mamba2_layer_decode(dims, layer, hidden, B, ssm_state, conv_state, conv_pos,
     st = lib().mamba2_layer_decode(C.byref(dims), C.byref(layer), _ptr(hidden), B, _ptr(ssm_state),
                                    _ptr(conv_state), _ptr(conv_pos), _ptr(ws), ws_bytes, _stream(stream))
     return _check("mamba2_layer_decode", st) if check else st
+
+
+M2_PREFETCH_MAX_BYTES = 96 << 20
+
+
+def mamba2_layer_decode_prefetch(dims, layer, hidden, B, ssm_state, conv_state, conv_pos, ws, ws_bytes, prefetch,
+                                 prefetch_bytes, stream=None, check=True) -> int:
+    """Decode step with a hint: [prefetch, prefetch + prefetch_bytes) is pulled toward L2 during the out_proj."""
+    st = lib().mamba2_layer_decode_prefetch(C.byref(dims), C.byref(layer), _ptr(hidden), B, _ptr(ssm_state),
+                                            _ptr(conv_state), _ptr(conv_pos), _ptr(ws), ws_bytes, _ptr(prefetch),
+                                            prefetch_bytes, _stream(stream))
+    return _check("mamba2_layer_decode_prefetch", st) if check else st
 
 
 def mamba2_layer_decode_noalloc(dims, layer, hidden, B, ssm_state, conv_state, conv_pos, stream=None,

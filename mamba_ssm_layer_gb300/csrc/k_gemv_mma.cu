@@ -442,6 +442,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
                    &tail->epi_bar, pn);
       }
     }
+    // a later launch's bytes (a hint): this CTA's share is pulled toward L2
+    // once its own ring is issued
+    auto pull_ahead = [&]() {
+      if (lane != 0 || !a.l2_ahead_bytes) return;
+      const size_t units = a.l2_ahead_bytes / 16;
+      const size_t u0 = units * blockIdx.x / G, u1 = units * (blockIdx.x + 1) / G;
+      for (size_t u = u0; u < u1; u += 4096) {  // at most 64 KB per request
+        const uint32_t n = (uint32_t)((u1 - u < 4096 ? u1 - u : 4096) * 16);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.l2_ahead + u * 16), "r"(n) : "memory");
+      }
+    };
     int j = 0;
     bool waited = false;
     // a tensor copy needs a 128-byte aligned destination (the layout keeps
@@ -455,6 +466,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int s = j % S;
       if (j == S) {
         // the ring is full: now take part in the dependency protocol
+        pull_ahead();
         pdl_wait();
         pdl_trigger();
         waited = true;
@@ -491,6 +503,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       }
     }
     if (!waited) {
+      if (!dead) pull_ahead();
       pdl_wait();
       pdl_trigger();
     }

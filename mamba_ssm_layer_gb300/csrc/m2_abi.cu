@@ -318,8 +318,9 @@ size_t m2_workspace_bytes(const m2_dims* dims, int32_t max_batch, int32_t max_to
   return a > b ? a : b;
 }
 
-int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t B, float* ssm_state,
-                        uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+static int decode_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t B, float* ssm_state,
+                       uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, const char* ahead,
+                       size_t ahead_bytes, cudaStream_t stream) {
   int st = m2_validate(dims, L);
   if (st) return st;
   if (B <= 0 || !hidden || !ssm_state || !conv_state || !conv_pos) return M2_ERR_ARG;
@@ -430,6 +431,8 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden
     eo.gz = zxu;
     eo.ldgz = r.ldz;
   }
+  eo.l2_ahead = ahead;
+  eo.l2_ahead_bytes = ahead_bytes;
   fa.out = proj_args(L->out_proj, g, r.d_inner, B, hidden, d.hidden, EPI_RESID, hidden, d.hidden, &eo,
                      fuse ? nullptr : us_out, 1, part, part_bytes);
   fa.ssm = sa;
@@ -832,6 +835,23 @@ int mamba2_ssm_step(float* h, const uint16_t* x, const uint16_t* Bm, const uint1
   sa.G = G;
   sa.pos_inc = nullptr;
   return launch_status(launch_ssm_step(sa, stream));
+}
+
+int mamba2_layer_decode(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t B, float* ssm_state,
+                        uint16_t* conv_state, int32_t* conv_pos, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return decode_impl(dims, L, hidden, B, ssm_state, conv_state, conv_pos, ws, ws_bytes, nullptr, 0, stream);
+}
+
+int mamba2_layer_decode_prefetch(const m2_dims* dims, const m2_layer* L, uint16_t* hidden, int32_t B,
+                                 float* ssm_state, uint16_t* conv_state, int32_t* conv_pos, void* ws,
+                                 size_t ws_bytes, const void* prefetch, size_t prefetch_bytes, cudaStream_t stream) {
+  size_t n = prefetch ? prefetch_bytes / 16 * 16 : 0;
+  if (n) {
+    if (!al16(prefetch)) return M2_ERR_ALIGN;
+    if (n > (size_t)M2_PREFETCH_MAX_BYTES || !within_one_allocation(prefetch, n)) return M2_ERR_ARG;
+  }
+  return decode_impl(dims, L, hidden, B, ssm_state, conv_state, conv_pos, ws, ws_bytes,
+                     static_cast<const char*>(prefetch), n, stream);
 }
 
 // Scratch of mamba2_layer_decode_noalloc: a fixed device array, so that

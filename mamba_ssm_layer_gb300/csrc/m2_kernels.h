@@ -100,6 +100,8 @@ struct GemvArgs {
   int32_t norm;             // GemvNorm
   const uint16_t* norm_w;   // [K] bf16 norm weight
   float norm_eps;
+  const char* l2_ahead;     // optional: bytes for a later launch, pulled toward L2 once this
+  size_t l2_ahead_bytes;    // launch's own weight ring is issued (16-byte aligned, multiple of 16)
   const float* gy;          // NORM_GATED: y [M][ldgy] fp32, z [M][ldgz] bf16 (whole-row span)
   int32_t ldgy;
   const uint16_t* gz;

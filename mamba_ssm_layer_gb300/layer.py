@@ -92,11 +92,26 @@ class DeviceLayer:
         n = abi.m2_workspace_bytes(self.dims, max_batch, max_tokens)
         return _empty((max(n, 256),), torch.uint8, device)
 
-    def decode(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None) -> None:
+    # Bytes of the next layer's in_proj pulled toward L2 during a step's
+    # out_proj (decode(..., ahead=...)).  Measured on the 8B-like layer at batch
+    # 1: 20-24 MB of the 76 MB matrix gave the shortest step (30.3 against
+    # 31.4 us); the whole matrix was slower (32.6 us), its traffic competing
+    # with the step's own out_proj reads from L2.
+    AHEAD_BYTES = 24 << 20
+
+    def decode(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None, ahead=None) -> None:
+        """One decode step.  ahead: the DeviceLayer decoded next on this stream;
+        the first AHEAD_BYTES of its in_proj weights are pulled toward L2 during
+        this step's out_proj (a hint: the results do not change)."""
         h, ring, pos = state
         B = hidden.shape[0]
-        abi.mamba2_layer_decode(self.dims, self.struct, hidden, B, h, ring, pos, ws, ws.numel(),
-                                stream if stream is not None else torch.cuda.current_stream())
+        s = stream if stream is not None else torch.cuda.current_stream()
+        if ahead is None:
+            abi.mamba2_layer_decode(self.dims, self.struct, hidden, B, h, ring, pos, ws, ws.numel(), s)
+        else:
+            w = ahead.t["in_w"]
+            n = min(w.numel() * w.element_size(), self.AHEAD_BYTES)
+            abi.mamba2_layer_decode_prefetch(self.dims, self.struct, hidden, B, h, ring, pos, ws, ws.numel(), w, n, s)
 
     def workspace_varlen(self, max_seqs: int, max_total_tokens: int, device="cuda") -> torch.Tensor:
         n = abi.m2_workspace_bytes_varlen(self.dims, max_seqs, max_total_tokens)

@@ -41,6 +41,10 @@ class DeviceStack:
             dl.prefill_varlen(hidden, cu_seqlens, st, ws, stream)
 
     def decode(self, hidden: torch.Tensor, states, ws: torch.Tensor, stream=None) -> None:
-        """hidden [B, hidden]: one token of each of the B sequences, in place through every layer."""
-        for dl, st in zip(self.layers, states):
-            dl.decode(hidden, st, ws, stream)
+        """hidden [B, hidden]: one token of each of the B sequences, in place
+        through every layer; each layer's out_proj pulls part of the next
+        layer's in_proj weights toward L2 (the last layer's: the first one's,
+        for the next token)."""
+        n = len(self.layers)
+        for i, (dl, st) in enumerate(zip(self.layers, states)):
+            dl.decode(hidden, st, ws, stream, ahead=self.layers[(i + 1) % n])

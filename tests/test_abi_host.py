@@ -105,6 +105,14 @@ def test_entry_points_reject_before_launch(lib):
     assert st == abi.M2_ERR_ALIGN
     st = abi.mamba2_layer_decode(d, L, FAKE, 2, FAKE, FAKE, FAKE, FAKE + 16, ws_need, check=False)
     assert st == abi.M2_ERR_WORKSPACE  # workspace must be 256-byte aligned
+    # the L2 hint of the prefetching decode: checked first, then the decode's own checks
+    st = abi.mamba2_layer_decode_prefetch(d, L, FAKE, 2, FAKE, FAKE, FAKE, FAKE, ws_need, FAKE + 8, 4096, check=False)
+    assert st == abi.M2_ERR_ALIGN
+    st = abi.mamba2_layer_decode_prefetch(d, L, FAKE, 2, FAKE, FAKE, FAKE, FAKE, ws_need, FAKE,
+                                          abi.M2_PREFETCH_MAX_BYTES + 16, check=False)
+    assert st == abi.M2_ERR_ARG
+    st = abi.mamba2_layer_decode_prefetch(d, L, FAKE, 2, FAKE, FAKE, FAKE, FAKE, ws_need - 1, FAKE, 0, check=False)
+    assert st == abi.M2_ERR_WORKSPACE  # no hint: exactly mamba2_layer_decode
     st = abi.mamba2_layer_prefill(d, L, FAKE, 5, FAKE, FAKE, None, FAKE, 1 << 30, check=False)
     assert st == abi.M2_ERR_ARG
     bad = _layer(in_fmt=3)
