@@ -146,6 +146,10 @@ int mamba2_layer_decode(const m2_dims* dims, const m2_layer* layer, uint16_t* hi
  * SSM kernel put them).  A hint only: results are bit-identical to
  * mamba2_layer_decode, and it applies to the batch <= 8 kernel chain (other
  * forms ignore it).  prefetch_bytes 0 (or a null prefetch) means no hint.
+ * More is not better: the pulled bytes share the memory system with the
+ * step's own traffic (measured on the 8B-like layer at batch 1: the first
+ * 8 MB of the next layer's 76 MB in_proj gave the shortest step, the whole
+ * matrix a longer one than no hint).
  * Errors, returned before anything is launched: M2_ERR_ALIGN if prefetch is
  * not 16-byte aligned; M2_ERR_ARG if the range is not inside one device
  * allocation or exceeds M2_PREFETCH_MAX_BYTES.  Other arguments and errors as

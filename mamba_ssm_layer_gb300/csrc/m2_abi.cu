@@ -409,15 +409,18 @@ static int decode_impl(const m2_dims* dims, const m2_layer* L, uint16_t* hidden,
   sa.pdl = 1;
   {
     // the SSM kernel starts while the in_proj drains and moves little data
-    // itself: it pulls the out_proj weights into L2 for the GEMV two launches on
-    // (pulling them, and the state, in from the in_proj's producer instead
-    // measured slower: 32.7 against 31.8 us per step)
+    // itself: it pulls the first rows of the out_proj weights into L2 for the
+    // GEMV two launches on.  Only the first kSsmPrefetch bytes: the out_proj's
+    // CTAs launch during the SSM step and fill their own rings, and more
+    // prefetch traffic delays the SSM's state reads.  Measured on the 8B-like
+    // layer at batch 1 (with the 8 MB next-layer hint of the prefetching
+    // decode): 10 MB 30.06 us per step, 4 MB 30.65, the whole 33.5 MB 30.5;
+    // without the hint: 10 MB 30.26, none 31.18, all 31.44.
+    constexpr size_t kSsmPrefetch = 10ull << 20;
     const m2_weight& wo = L->out_proj;
     const size_t wo_bytes = (size_t)wo.n * wo.k * (wo.fmt == M2_W_BF16 ? 2 : 1);
-    if (wo_bytes <= (64ull << 20)) {
-      sa.l2_prefetch = wo.w;
-      sa.l2_prefetch_bytes = wo_bytes;
-    }
+    sa.l2_prefetch = wo.w;
+    sa.l2_prefetch_bytes = wo_bytes < kSsmPrefetch ? wo_bytes : kSsmPrefetch;
   }
   // 7+8. out_proj with the residual add in its epilogue (in place on hidden)
   GemvArgs eo;

@@ -94,10 +94,10 @@ class DeviceLayer:
 
     # Bytes of the next layer's in_proj pulled toward L2 during a step's
     # out_proj (decode(..., ahead=...)).  Measured on the 8B-like layer at batch
-    # 1: 20-24 MB of the 76 MB matrix gave the shortest step (30.3 against
-    # 31.4 us); the whole matrix was slower (32.6 us), its traffic competing
-    # with the step's own out_proj reads from L2.
-    AHEAD_BYTES = 24 << 20
+    # 1, with the SSM step's 10 MB out_proj prefetch: 8 MB of the 76 MB matrix
+    # gave the shortest step (30.06 against 30.26 us without a hint; 12 MB
+    # 30.19, 16 MB 30.36); more competes with the step's own traffic.
+    AHEAD_BYTES = 8 << 20
 
     def decode(self, hidden: torch.Tensor, state, ws: torch.Tensor, stream=None, ahead=None) -> None:
         """One decode step.  ahead: the DeviceLayer decoded next on this stream;

@@ -57,8 +57,8 @@ def main() -> None:
         sts = [r.new_state(B) for r in reps]
         ws = base.workspace(B, 0)
         x = to_dev(synth.make_hidden(B, d["hidden"], wl, 0, 0))
-        for i in range(a.steps):
-            reps[i % 2].decode(x, sts[i % 2], ws)
+        for i in range(a.steps):  # each step hints the other replica, as the decode benchmark does
+            reps[i % 2].decode(x, sts[i % 2], ws, ahead=reps[(i + 1) % 2] if B == 1 else None)
     torch.cuda.synchronize()
     st = abi.m2_device_status()
     if st != abi.M2_OK:
