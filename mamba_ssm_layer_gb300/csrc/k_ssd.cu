@@ -734,28 +734,57 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const S
   }
   if (warp == 0) tmem_alloc(&tmem_slot, kCols);
   chunk_decay(a, h, t0, qc, dt_s, cs_s);
-  // C, B rows (zero past the chunk), x^T, h_in split
-  for (int i = tid; i < kQ * (N / 8); i += kSsdTcOutThreads) {
-    const int r = i / (N / 8), n0 = (i % (N / 8)) * 8;
-    uint4 cv = make_uint4(0u, 0u, 0u, 0u), bv = cv;
-    if (r < qc) {
-      const size_t row = (size_t)(t0 + r) * a.ld_in + (size_t)g * N + n0;
-      cv = *reinterpret_cast<const uint4*>(a.Cm + row);
-      bv = *reinterpret_cast<const uint4*>(a.Bm + row);
+  // C, B rows (zero past the chunk), x^T, h_in split.  Each thread issues a
+  // batch of its loads before any of the stores that use them (the stores go
+  // through generic pointers, so the compiler keeps a later iteration's loads
+  // behind an earlier iteration's stores: one L2 round trip per iteration).
+  constexpr int kCb = kQ * (N / 8) / kSsdTcOutThreads;  // 8 row pieces of C and of B per thread
+  static_assert(kQ * (N / 8) % kSsdTcOutThreads == 0 && kCb % 2 == 0, "C/B pieces per thread");
+#pragma unroll
+  for (int bt = 0; bt < 2; ++bt) {
+    uint4 cv[kCb / 2], bv[kCb / 2];
+#pragma unroll
+    for (int j = 0; j < kCb / 2; ++j) {
+      const int i = tid + kSsdTcOutThreads * (bt * (kCb / 2) + j);
+      const int r = i / (N / 8), n0 = (i % (N / 8)) * 8;
+      cv[j] = bv[j] = make_uint4(0u, 0u, 0u, 0u);
+      if (r < qc) {
+        const size_t row = (size_t)(t0 + r) * a.ld_in + (size_t)g * N + n0;
+        cv[j] = *reinterpret_cast<const uint4*>(a.Cm + row);
+        bv[j] = *reinterpret_cast<const uint4*>(a.Bm + row);
+      }
     }
-    sw_store8(Cs, kQ, r, n0, cv);
-    sw_store8(Bs, kQ, r, n0, bv);
+#pragma unroll
+    for (int j = 0; j < kCb / 2; ++j) {
+      const int i = tid + kSsdTcOutThreads * (bt * (kCb / 2) + j);
+      const int r = i / (N / 8), n0 = (i % (N / 8)) * 8;
+      sw_store8(Cs, kQ, r, n0, cv[j]);
+      sw_store8(Bs, kQ, r, n0, bv[j]);
+    }
   }
   const float* hin = a.dH + ((size_t)h * a.nchunks + c) * P * N;
-  for (int i = tid; i < P * (N / 8); i += kSsdTcOutThreads) {
-    const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
-    const float4 f0 = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0);
-    const float4 f1 = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0 + 4);
-    const float v[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-    uint4 hi, lo;
-    split8(v, hi, lo);
-    sw_store8(Hh, P, pp, n0, hi);
-    sw_store8(Hl, P, pp, n0, lo);
+  {
+    constexpr int kHp = P * (N / 8) / kSsdTcOutThreads;  // row pieces of h_in per thread
+    static_assert(P * (N / 8) % kSsdTcOutThreads == 0, "h_in pieces per thread");
+    float4 f[2 * kHp];
+#pragma unroll
+    for (int j = 0; j < kHp; ++j) {
+      const int i = tid + kSsdTcOutThreads * j;
+      const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
+      f[2 * j] = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0);
+      f[2 * j + 1] = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0 + 4);
+    }
+#pragma unroll
+    for (int j = 0; j < kHp; ++j) {
+      const int i = tid + kSsdTcOutThreads * j;
+      const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
+      const float v[8] = {f[2 * j].x, f[2 * j].y, f[2 * j].z, f[2 * j].w,
+                          f[2 * j + 1].x, f[2 * j + 1].y, f[2 * j + 1].z, f[2 * j + 1].w};
+      uint4 hi, lo;
+      split8(v, hi, lo);
+      sw_store8(Hh, P, pp, n0, hi);
+      sw_store8(Hl, P, pp, n0, lo);
+    }
   }
   fence_proxy_async();
   tc_fence_before();
