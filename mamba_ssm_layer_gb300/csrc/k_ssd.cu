@@ -707,7 +707,8 @@ __global__ void __launch_bounds__(kSsdTcThreads, 1) ssd_state_tc_kernel(const Ss
 }
 
 template <int P>
-__global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const SsdArgs a) {
+// two CTAs per SM: 97 KB of shared memory and 256 TMEM columns each
+__global__ void __launch_bounds__(kSsdTcOutThreads, 2) ssd_out_tc_kernel(const SsdArgs a) {
   constexpr int N = 128;
   constexpr uint32_t kCols = 256;  // S: 128, Yi: P, Y: P
   const int h = blockIdx.x, c = blockIdx.y;
@@ -733,16 +734,20 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const S
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(&tmem_slot, kCols);
-  chunk_decay(a, h, t0, qc, dt_s, cs_s);
   // C, B rows (zero past the chunk), x^T, h_in split.  Each thread issues a
   // batch of its loads before any of the stores that use them (the stores go
   // through generic pointers, so the compiler keeps a later iteration's loads
-  // behind an earlier iteration's stores: one L2 round trip per iteration).
+  // behind an earlier iteration's stores: one L2 round trip per iteration),
+  // and the first batch before the chunk's decays, whose dt loads and prefix
+  // sum then overlap it.
   constexpr int kCb = kQ * (N / 8) / kSsdTcOutThreads;  // 8 row pieces of C and of B per thread
+  constexpr int kHp = P * (N / 8) / kSsdTcOutThreads;   // row pieces of h_in per thread
   static_assert(kQ * (N / 8) % kSsdTcOutThreads == 0 && kCb % 2 == 0, "C/B pieces per thread");
-#pragma unroll
-  for (int bt = 0; bt < 2; ++bt) {
-    uint4 cv[kCb / 2], bv[kCb / 2];
+  static_assert(P * (N / 8) % kSsdTcOutThreads == 0, "h_in pieces per thread");
+  const float* hin = a.dH + ((size_t)h * a.nchunks + c) * P * N;
+  uint4 cv[kCb / 2], bv[kCb / 2];
+  float4 f[2 * kHp];
+  auto load_cb = [&](int bt) {
 #pragma unroll
     for (int j = 0; j < kCb / 2; ++j) {
       const int i = tid + kSsdTcOutThreads * (bt * (kCb / 2) + j);
@@ -754,6 +759,8 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const S
         bv[j] = *reinterpret_cast<const uint4*>(a.Bm + row);
       }
     }
+  };
+  auto store_cb = [&](int bt) {
 #pragma unroll
     for (int j = 0; j < kCb / 2; ++j) {
       const int i = tid + kSsdTcOutThreads * (bt * (kCb / 2) + j);
@@ -761,30 +768,29 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const S
       sw_store8(Cs, kQ, r, n0, cv[j]);
       sw_store8(Bs, kQ, r, n0, bv[j]);
     }
+  };
+  load_cb(0);
+#pragma unroll
+  for (int j = 0; j < kHp; ++j) {
+    const int i = tid + kSsdTcOutThreads * j;
+    const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
+    f[2 * j] = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0);
+    f[2 * j + 1] = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0 + 4);
   }
-  const float* hin = a.dH + ((size_t)h * a.nchunks + c) * P * N;
-  {
-    constexpr int kHp = P * (N / 8) / kSsdTcOutThreads;  // row pieces of h_in per thread
-    static_assert(P * (N / 8) % kSsdTcOutThreads == 0, "h_in pieces per thread");
-    float4 f[2 * kHp];
+  chunk_decay(a, h, t0, qc, dt_s, cs_s);
+  store_cb(0);
+  load_cb(1);
+  store_cb(1);
 #pragma unroll
-    for (int j = 0; j < kHp; ++j) {
-      const int i = tid + kSsdTcOutThreads * j;
-      const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
-      f[2 * j] = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0);
-      f[2 * j + 1] = *reinterpret_cast<const float4*>(hin + (size_t)pp * N + n0 + 4);
-    }
-#pragma unroll
-    for (int j = 0; j < kHp; ++j) {
-      const int i = tid + kSsdTcOutThreads * j;
-      const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
-      const float v[8] = {f[2 * j].x, f[2 * j].y, f[2 * j].z, f[2 * j].w,
-                          f[2 * j + 1].x, f[2 * j + 1].y, f[2 * j + 1].z, f[2 * j + 1].w};
-      uint4 hi, lo;
-      split8(v, hi, lo);
-      sw_store8(Hh, P, pp, n0, hi);
-      sw_store8(Hl, P, pp, n0, lo);
-    }
+  for (int j = 0; j < kHp; ++j) {
+    const int i = tid + kSsdTcOutThreads * j;
+    const int pp = i / (N / 8), n0 = (i % (N / 8)) * 8;
+    const float v[8] = {f[2 * j].x, f[2 * j].y, f[2 * j].z, f[2 * j].w,
+                        f[2 * j + 1].x, f[2 * j + 1].y, f[2 * j + 1].z, f[2 * j + 1].w};
+    uint4 hi, lo;
+    split8(v, hi, lo);
+    sw_store8(Hh, P, pp, n0, hi);
+    sw_store8(Hl, P, pp, n0, lo);
   }
   fence_proxy_async();
   tc_fence_before();
@@ -798,21 +804,26 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 1) ssd_out_tc_kernel(const S
     tc_mma_k128(tYi, Cs, Hl, P, tc_idesc(128, P), 1);
     tc_commit(&bar[0]);
   }
+  // x^T goes into the space of h_in once the MMAs above have read it, in
+  // 8 x 8 blocks (one per thread at most); its rows are loaded while they run
+  static_assert((kQ / 8) * (P / 8) <= kSsdTcOutThreads, "one x^T block per thread");
+  const bool xb = tid < (kQ / 8) * (P / 8);
+  const int xs0 = (tid % (kQ / 8)) * 8, xp0 = (tid / (kQ / 8)) * 8;
+  uint4 xrows[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    xrows[r] = (xb && xs0 + r < qc)
+                   ? *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + xs0 + r) * a.ld_in + (size_t)h * P + xp0)
+                   : make_uint4(0u, 0u, 0u, 0u);
   // tcgen05.ld is warp-collective (.sync.aligned): every lane of a warp loads,
   // whatever its own row; only stores depend on the row
   bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[0], 0));
   tc_fence_after();
-  // x^T into the space of h_in (no longer read), in 8 x 8 blocks
-  for (int i = tid; i < (kQ / 8) * (P / 8); i += kSsdTcOutThreads) {
-    const int s0 = (i % (kQ / 8)) * 8, p0 = (i / (kQ / 8)) * 8;
-    uint4 rows[8], cols[8];
+  if (xb) {
+    uint4 cols[8];
+    transpose8x8(xrows, cols);
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      rows[r] = s0 + r < qc ? *reinterpret_cast<const uint4*>(a.x + (size_t)(t0 + s0 + r) * a.ld_in + (size_t)h * P + p0)
-                            : make_uint4(0u, 0u, 0u, 0u);
-    transpose8x8(rows, cols);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) sw_store8(Xt, P, p0 + c, s0, cols[c]);
+    for (int c8 = 0; c8 < 8; ++c8) sw_store8(Xt, P, xp0 + c8, xs0, cols[c8]);
   }
   // L row t = 32 (w mod 4) + l, columns [64 (w / 4), +64) (C and B are no
   // longer read: their space takes L)
