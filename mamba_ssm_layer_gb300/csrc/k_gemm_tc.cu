@@ -3,34 +3,37 @@
 //
 // W~ = E4M3(W) * S[n/128][k/128] (page "Struct Qwen3SsmLayer",
 // `set_fp8_decode_weights`; scale index of "Struct NemotronMamba2Layer",
-// `set_fp8_weights`), or bf16 W.  tcgen05 has no bf16 x E4M3 MMA and E4M3
-// activations would change the numbers, so the weight tile is converted
-// E4M3 -> bf16 exactly (every E4M3 value is a bf16 value) in shared memory and
-// multiplied by the bf16 activations with kind::f16 (fp32 accumulation in
-// TMEM).  The 128x128 block scale is not a power of two and varies with the k
-// block, so it cannot ride on the MMA: each 128-wide k block is accumulated
-// alone into a TMEM buffer and the epilogue promotes it, acc += s * partial.
+// `set_fp8_weights`), or bf16 W.  tcgen05 has no 16-bit x E4M3 MMA and E4M3
+// activations would change the numbers, so each E4M3 weight tile is converted
+// exactly (every E4M3 value is an f16 and a bf16 value) and multiplied by the
+// 16-bit activations with kind::f16 (fp32 accumulation in TMEM).  The
+// converted tile goes to tensor memory, the MMA's A operand there: the
+// converters read 16 KB of shared memory per k block and the MMA reads only
+// the activation tile from shared memory.  The 128x128 block scale is not a
+// power of two and varies with the k block, so it cannot ride on the MMA:
+// each 128-wide k block is accumulated alone into a TMEM buffer and the
+// epilogue promotes it, acc += s * partial.
 //
 // The MMA computes D^T: UMMA M = 128 weight rows (one scale row block), UMMA N
 // = NT token rows, so one tile is [128 weight rows] x [NT tokens].
 // Persistent CTAs walk work items (a tile, or a k range of a tile when the
 // tiles alone would leave most SMs idle) weight-tile major, so the token tiles
 // of one weight tile are adjacent and its bytes are re-read from L2.  Roles
-// (each ring has its own fill barriers; a slot the MMA read is free again once
-// that k block's MMAs have completed, which one commit per k block signals):
+// (each ring has its own fill and free barriers; the MMA issuer frees the
+// slots it read with one commit each per k block):
 //   warp 0      weight producer (lane 0): TMA of the E4M3 tile [128][128]
-//               (plain 2-D map) into a 4-stage ring; bf16 weights go straight
-//               into a 4-stage ring of 128-byte-swizzled tiles.  It does not
-//               wait for the previous kernel: weights are never its output.
+//               (128-byte swizzle) into a ring; bf16 weights go straight into a
+//               ring of 128-byte-swizzled tiles, the MMA's A operand.  It does
+//               not wait for the previous kernel: weights are never its output.
 //   warp 22     activation producer (lane 0): after the dependency wait, one
-//               3-D tensor copy per k block of the bf16 activation tile [NT][128]
-//               (two 64-wide halves, 128-byte swizzle = the UMMA K-major
-//               canonical layout), 3-4 stages;
-//   warps 2-5   converters: E4M3 tile -> bf16 tile in the swizzled layout the
-//               MMA descriptor expects (double-buffered);
-//   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each; W8A8: 4 of
-//               K = 32) per k block into one of 4 TMEM partial buffers and one
-//               commit, which wakes the epilogue and frees the operand slots;
+//               3-D tensor copy per k block of the 16-bit activation tile
+//               [NT][128] (two 64-wide halves, 128-byte swizzle = the UMMA
+//               K-major canonical layout) into a ring;
+//   warps 2-5   converters (E4M3 weights): one weight row per thread (its TMEM
+//               lane), E4M3 -> f16 (prescaled f16 activations) or bf16, stored
+//               with tcgen05.st into one of the A stages in TMEM;
+//   warp 1      TMEM allocation; lane 0 issues 8 MMAs (K = 16 each) per k block
+//               into one of the TMEM partial buffers, then commits per ring;
 //   warps 6-21  epilogue, four warps per TMEM lane quarter (each a quarter of
 //               the token columns): per k block, TMEM -> registers, acc += s * partial;
 //               per item, the store / residual / conv-update epilogue, or fp32
@@ -50,44 +53,45 @@ namespace m2 {
 constexpr int kTcEpiWarps = 16;  // four per TMEM lane quarter, each a quarter of the token columns
 constexpr int kTcAWarp = 6 + kTcEpiWarps;       // activation producer
 constexpr int kTcThreads = (kTcAWarp + 1) * 32;  // 23 warps
-constexpr int kTcWStages = 4;    // weight tiles in flight
-constexpr int kTcTmemBufs = 4;   // k-block partials in TMEM
 constexpr int kTcBM = 128;       // weight rows per tile (UMMA M)
 constexpr int kTcBK = 128;       // k per block (= scale block)
 
-template <int NT>
-struct TcLayout {
-  // offsets from a 1024-byte aligned base: W ring at 0 (fp8: 4 x 16 KB E4M3;
-  // bf16: 4 x 32 KB swizzled, through kWbf), converted 16-bit weight tiles at
-  // kWbf, 16-bit activation tiles at kA
-  static constexpr int kAStages = NT <= 64 ? 4 : 3;
-  static constexpr int kABytes = NT * kTcBK * 2;  // one activation stage
-  static constexpr int kW = 0;
-  static constexpr int kWbf = 65536;
-  static constexpr int kA = 131072;
-  static constexpr int kBars = kA + kAStages * kABytes;
-};
-
 struct TcBars {
-  uint64_t w_full[kTcWStages], w_empty[kTcWStages];
-  uint64_t wbf_full[2];
-  uint64_t a_full[4];
-  uint64_t mma_done[kTcTmemBufs], tmem_empty[kTcTmemBufs];
+  static constexpr int kMaxRing = 8, kMaxTmem = 4;
+  uint64_t w_full[kMaxRing], w_empty[kMaxRing];
+  uint64_t a_full[kMaxRing], a_empty[kMaxRing];
+  uint64_t ta_full[kMaxTmem], ta_empty[kMaxTmem];
+  uint64_t mma_done[kMaxTmem], tmem_empty[kMaxTmem];
   uint32_t tmem_base;
 };
 
-// Wait for the completion of k block j's MMAs: one tcgen05.commit per k block
-// arrives on mma_done[j % kTcTmemBufs].  Every caller asks for a k block whose
-// barrier cannot have completed a later phase yet (parity would alias): that
-// phase belongs to k block j + kTcTmemBufs, whose operands (or TMEM buffer)
-// the caller itself has still to provide.
-__device__ __forceinline__ bool kblock_done(TcBars* bars, int j) {
-  return mbar_wait(&bars->mma_done[j % kTcTmemBufs], (uint32_t)(j / kTcTmemBufs) & 1u);
-}
+// Shared memory (offsets from a 1024-byte aligned base) and tensor memory of
+// one CTA.  E4M3 weights (FP8): raw 16 KB tiles in the weight ring, converted
+// tiles in TMEM (64 columns each, after the partial buffers), so both rings
+// fill shared memory.  bf16 weights: 32 KB swizzled tiles.
+template <int NT, bool FP8>
+struct TcLayout {
+  static constexpr int kWStages = FP8 ? (NT <= 64 ? 6 : 4) : 4;
+  static constexpr int kWBytes = FP8 ? kTcBM * kTcBK : kTcBM * kTcBK * 2;
+  static constexpr int kAStages = FP8 ? (NT <= 64 ? 6 : 5) : (NT <= 64 ? 4 : 3);
+  static constexpr int kABytes = NT * kTcBK * 2;  // one activation stage
+  static constexpr int kTBufs = (FP8 && NT > 64) ? 3 : 4;  // k-block partials in TMEM
+  static constexpr int kTAStages = FP8 ? (NT <= 64 ? 4 : 2) : 0;  // converted weight tiles in TMEM
+  static constexpr int kTACol = kTBufs * NT;  // first column of the A stages
+  static constexpr int kTmemCols = FP8 ? 512 : kTBufs * NT;
+  static constexpr int kW = 0;
+  static constexpr int kA = kWStages * kWBytes;
+  static constexpr int kBars = kA + kAStages * kABytes;
+  static_assert(kTACol + kTAStages * (kTcBK / 2) <= kTmemCols && kTmemCols <= 512, "TMEM budget");
+  static_assert(kWStages <= TcBars::kMaxRing && kAStages <= TcBars::kMaxRing, "ring barriers");
+  static_assert(kTAStages <= TcBars::kMaxTmem && kTBufs <= TcBars::kMaxTmem, "TMEM barriers");
+  static_assert(kBars + (int)sizeof(TcBars) + 1024 <= 232448, "shared memory");
+};
 
-template <int NT>
+
+template <int NT, bool FP8>
 constexpr int tc_smem_bytes() {
-  return TcLayout<NT>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
+  return TcLayout<NT, FP8>::kBars + (int)sizeof(TcBars) + 1024;  // + alignment slack
 }
 
 // ------------------------------------------------------------------ PTX helpers
@@ -162,8 +166,12 @@ __device__ __forceinline__ void tc_epi_elem(const GemvArgs& a, int m, int n, flo
 // m0 + HC - 1 of acc.  The mode is decided once, outside the per-column loops,
 // so that each unrolled loop stays a few hundred instructions (every epilogue
 // warp runs it once per item; one loop holding all modes' code, 64 times over,
-// ran from instruction-cache misses).  The conv update, the one long body,
-// loops over a local copy of acc.
+// ran from instruction-cache misses).  Loads come before the stores of the
+// same columns: `out` may alias `resid` (and the conv ring is written here), so
+// a load placed after a store could not be moved ahead of it, and each column
+// would wait one memory round trip behind the previous column's store.  Each
+// element is read and written by this thread alone, so reading all first is
+// exact.
 template <int HC>
 __device__ __forceinline__ void tc_item_store(const GemvArgs& a, int ksplit, float* part, int ks, int n, int m0,
                                               const float (&acc)[HC], int L) {
@@ -177,17 +185,53 @@ __device__ __forceinline__ void tc_item_store(const GemvArgs& a, int ksplit, flo
   } else if (a.epi == EPI_RESID) {
     uint16_t* o = a.out + (size_t)m0 * a.ldo + n;
     const uint16_t* r = a.resid + (size_t)m0 * a.ldr + n;
+    constexpr int G = HC < 8 ? HC : (HC >= 64 ? 4 : 8);  // columns whose loads are in flight together
 #pragma unroll
-    for (int j = 0; j < HC; ++j)
-      if (j < mc) o[(size_t)j * a.ldo] = f32_to_bf16(bf16_to_f32(r[(size_t)j * a.ldr]) + acc[j]);
+    for (int j0 = 0; j0 < HC; j0 += G) {
+      uint16_t rv[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) rv[g] = j0 + g < mc ? r[(size_t)(j0 + g) * a.ldr] : (uint16_t)0;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        if (j0 + g < mc) o[(size_t)(j0 + g) * a.ldo] = f32_to_bf16(bf16_to_f32(rv[g]) + acc[j0 + g]);
+    }
   } else if (a.epi == EPI_INPROJ_CONV && n >= a.xbc0 && n < a.xbc0 + a.d_xbc) {
-    ConvTaps taps;
-    load_taps(a, n - a.xbc0, L, taps);
+    // conv update of channel c for each token column (a sequence in batched
+    // decode), G columns at a time: their positions and ring taps are loaded,
+    // then their outputs and new ring slots stored
+    constexpr int G = 4;
+    const int c = n - a.xbc0;
+    ConvTaps t;
+    load_taps(a, c, L, t);
     float v[HC];
 #pragma unroll
     for (int j = 0; j < HC; ++j) v[j] = acc[j];
 #pragma unroll 1
-    for (int j = 0; j < mc; ++j) tc_epi_elem(a, m0 + j, n, v[j], true, taps, L);
+    for (int j0 = 0; j0 < mc; j0 += G) {
+      int p[G];
+      float hv[G][7];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        p[g] = j0 + g < mc ? a.pos[m0 + j0 + g] : 0;
+        const uint16_t* rg = a.ring + (size_t)(m0 + j0 + g) * L * a.d_xbc + c;
+#pragma unroll
+        for (int i = 0; i < 7; ++i)
+          hv[g][i] = (i < L && j0 + g < mc) ? bf16_to_f32(rg[(size_t)((p[g] + i) % L) * a.d_xbc]) : 0.0f;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (j0 + g >= mc) break;
+        const int m = m0 + j0 + g;
+        const uint16_t vb = f32_to_bf16(v[j0 + g]);  // rounding point of the in_proj output
+        float sv = t.bias;
+#pragma unroll
+        for (int i = 0; i < 7; ++i)
+          if (i < L) sv += t.hist[i] * hv[g][i];
+        sv += t.cur * bf16_to_f32(vb);
+        a.out[(size_t)m * a.ldo + n] = f32_to_bf16(silu_f(sv));
+        a.ring[(size_t)m * L * a.d_xbc + (size_t)(p[g] % L) * a.d_xbc + c] = vb;
+      }
+    }
   } else {
     uint16_t* o = a.out + (size_t)m0 * a.ldo + n;
 #pragma unroll
@@ -218,11 +262,11 @@ __device__ __forceinline__ void tc_item(const TcArgs& ta, int item, int& nt, int
   kb1 = (int)((long long)ta.kblocks * (ks + 1) / ta.ksplit);
 }
 
-template <int NT>
+template <int NT, bool FP8>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA, const TcArgs ta) {
-  using Lay = TcLayout<NT>;
-  constexpr int SA = Lay::kAStages;
+  using Lay = TcLayout<NT, FP8>;
+  constexpr int SW = Lay::kWStages, SA = Lay::kAStages, TB = Lay::kTBufs, NA = Lay::kTAStages;
   const GemvArgs& a = ta.g;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -233,29 +277,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int L = a.dconv - 1;
 
   if (tid == 0) {
-    for (int s = 0; s < kTcWStages; ++s) {
+    for (int s = 0; s < SW; ++s) {
       mbar_init(&bars->w_full[s], 1);
-      mbar_init(&bars->w_empty[s], 4);  // w8a16: the converter warps (otherwise the k block's completion frees it)
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->wbf_full[b], 4);
+      mbar_init(&bars->w_empty[s], FP8 ? 4 : 1);  // the converter warps, or the MMA issuer's commit
     }
     for (int s = 0; s < SA; ++s) {
       mbar_init(&bars->a_full[s], 1);
+      mbar_init(&bars->a_empty[s], 1);
     }
-    for (int b = 0; b < kTcTmemBufs; ++b) {
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&bars->ta_full[s], 4);
+      mbar_init(&bars->ta_empty[s], 1);
+    }
+    for (int b = 0; b < TB; ++b) {
       mbar_init(&bars->mma_done[b], 1);
       mbar_init(&bars->tmem_empty[b], kTcEpiWarps);
     }
     fence_mbar_init();
   }
-  if (warp == 1) {
-    // kTcTmemBufs x NT fp32 columns of TMEM (a power of two >= 32)
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(&bars->tmem_base)),
-                 "r"(kTcTmemBufs * NT));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-  }
+  if (warp == 1) tmem_alloc(&bars->tmem_base, Lay::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -273,21 +313,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
-          const int s = gk % kTcWStages;
-          if (gk >= kTcWStages) {
-            // the slot's previous tile: freed by the converters (w8a16), or by
-            // the completion of its k block's MMAs
-            const bool ok = ta.fp8 ? mbar_wait(&bars->w_empty[s], ((gk / kTcWStages) - 1) & 1)
-                                   : kblock_done(bars, gk - kTcWStages);
-            if (!ok) dead = true;
-          }
+          const int s = gk % SW;
+          if (gk >= SW && !mbar_wait(&bars->w_empty[s], ((gk / SW) - 1) & 1)) dead = true;
           if (dead) break;
-          if (ta.fp8) {  // E4M3 tile, plain, for the converters
-            mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK);
-            tma_load_2d(smem + Lay::kW + s * kTcBM * kTcBK, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
+          uint8_t* wbuf = smem + Lay::kW + s * Lay::kWBytes;
+          mbar_arrive_expect_tx(&bars->w_full[s], Lay::kWBytes);
+          if constexpr (FP8) {  // E4M3 tile, 128-byte swizzle, for the converters
+            tma_load_2d(wbuf, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
           } else {
-            uint8_t* wbuf = smem + Lay::kW + s * kTcBM * kTcBK * 2;
-            mbar_arrive_expect_tx(&bars->w_full[s], kTcBM * kTcBK * 2);
             tma_load_2d(wbuf, &tmW, kb * kTcBK, nt * kTcBM, &bars->w_full[s], polw);
             tma_load_2d(wbuf + kTcBM * 128, &tmW, kb * kTcBK + 64, nt * kTcBM, &bars->w_full[s], polw);
           }
@@ -295,30 +328,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // drain: the tiles issued (k blocks [0, gk)) have landed before the CTA
       // may exit, also after a timeout stopped their consumers
-      for (int k = max(0, gk - kTcWStages); k < gk; ++k)
-        if (!mbar_drain(&bars->w_full[k % kTcWStages], (k / kTcWStages) & 1)) break;
+      for (int k = max(0, gk - SW); k < gk; ++k)
+        if (!mbar_drain(&bars->w_full[k % SW], (k / SW) & 1)) break;
     }
   } else if (warp == kTcAWarp) {
     // -------------------------------------------------------- activation producer
     pdl_wait();  // A is written by the previous kernel
     if (lane == 0) {
       const uint64_t pola = policy_evict_last();  // activations are re-read by every weight tile
-      int gk = 0, a_iss = 0;  // k blocks whose activation tile is issued
+      int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
           const int s = gk % SA;
-          if (gk >= SA && !kblock_done(bars, gk - SA)) dead = true;
+          if (gk >= SA && !mbar_wait(&bars->a_empty[s], ((gk / SA) - 1) & 1)) dead = true;
           if (dead) break;
           uint8_t* abuf = smem + Lay::kA + s * Lay::kABytes;
           mbar_arrive_expect_tx(&bars->a_full[s], Lay::kABytes);
           tma_load_3d(abuf, &tmA, 0, mt * NT, kb * 2, &bars->a_full[s], pola);  // both halves
-          a_iss = gk + 1;
         }
       }
       // drain: everything issued has landed before the CTA may exit
-      for (int k = max(0, a_iss - SA); k < a_iss; ++k)
+      for (int k = max(0, gk - SA); k < gk; ++k)
         if (!mbar_drain(&bars->a_full[k % SA], (k / SA) & 1)) break;
     }
   } else if (warp == 1) {
@@ -330,93 +362,89 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
-          const int s = gk % kTcWStages, b = gk & 1, sa = gk % SA, tb = gk % kTcTmemBufs;
-          if (ta.fp8) {
-            if (!mbar_wait(&bars->wbf_full[b], (gk / 2) & 1)) dead = true;
+          const int s = gk % SW, sa = gk % SA, tb = gk % TB;
+          const int na = FP8 ? gk % NA : 0;
+          if constexpr (FP8) {
+            if (!mbar_wait(&bars->ta_full[na], (gk / NA) & 1)) dead = true;
           } else {
-            if (!mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1)) dead = true;
+            if (!mbar_wait(&bars->w_full[s], (gk / SW) & 1)) dead = true;
           }
           if (!dead && !mbar_wait(&bars->a_full[sa], (gk / SA) & 1)) dead = true;
-          if (!dead && gk >= kTcTmemBufs && !mbar_wait(&bars->tmem_empty[tb], ((gk / kTcTmemBufs) - 1) & 1))
-            dead = true;
+          if (!dead && gk >= TB && !mbar_wait(&bars->tmem_empty[tb], ((gk / TB) - 1) & 1)) dead = true;
           if (dead) break;
           tc_fence_after();
-          {
-            const uint32_t wb = ta.fp8 ? smem_addr(smem + Lay::kWbf + b * kTcBM * kTcBK * 2)
-                                       : smem_addr(smem + Lay::kW + s * kTcBM * kTcBK * 2);
-            const uint32_t ab = smem_addr(smem + Lay::kA + sa * Lay::kABytes);
+          const uint32_t ab = smem_addr(smem + Lay::kA + sa * Lay::kABytes);
 #pragma unroll
-            for (int kk = 0; kk < kTcBK / 16; ++kk) {
-              const int atom = kk >> 2, within = (kk & 3) * 32;  // 64-k atoms of 128 bytes per row
-              const uint64_t ad = sw128_desc(wb + atom * kTcBM * 128 + within);
-              const uint64_t bd = sw128_desc(ab + atom * NT * 128 + within);
-              tc_mma(tmem + tb * NT, ad, bd, idesc, kk > 0 ? 1 : 0);
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const int atom = kk >> 2, within = (kk & 3) * 32;  // 64-k atoms of 128 bytes per row
+            const uint64_t bd = sw128_desc(ab + atom * NT * 128 + within);
+            if constexpr (FP8) {
+              // converted tile: k = 16 kk .. 16 kk + 15 in columns 8 kk .. 8 kk + 7
+              tc_mma_ts(tmem + tb * NT, tmem + Lay::kTACol + na * (kTcBK / 2) + kk * 8, bd, idesc, kk > 0 ? 1 : 0);
+            } else {
+              const uint32_t wb = smem_addr(smem + Lay::kW + s * Lay::kWBytes);
+              tc_mma(tmem + tb * NT, sw128_desc(wb + atom * kTcBM * 128 + within), bd, idesc, kk > 0 ? 1 : 0);
             }
           }
-          // one commit per k block: its completion frees the TMEM partial for the
-          // epilogue and the operand slots it read (their producers wait on it)
+          // commits: the partial is done (epilogue), and the operand slots this
+          // k block read are free (their producers wait on them)
           tc_commit(&bars->mma_done[tb]);
+          tc_commit(&bars->a_empty[sa]);
+          tc_commit(FP8 ? &bars->ta_empty[na] : &bars->w_empty[s]);
         }
       }
-      // drain: no MMA of this thread is still writing TMEM when it is freed
+      // drain: no MMA of this thread is still running when TMEM is freed
       // (the last commit tracks all earlier MMAs)
-      if (gk > 0) mbar_drain(&bars->mma_done[(gk - 1) % kTcTmemBufs], ((gk - 1) / kTcTmemBufs) & 1);
+      if (gk > 0) mbar_drain(&bars->mma_done[(gk - 1) % TB], ((gk - 1) / TB) & 1);
     }
   } else if (warp < 6) {
     // -------------------------------------------------------- converters
-    if (ta.fp8) {
-      const int ct = tid - 64;  // 0..127
+    if constexpr (FP8) {
+      // warp w reaches TMEM lanes 32 (w % 4) .. + 31: one weight row per thread
+      const int q = warp & 3, row = 32 * q + lane, r8 = row & 7;
+      const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16) + Lay::kTACol;
       int gk = 0;
       for (int item = cid; item < nitems && !dead; item += ncl) {
         int nt, mt, kb0, kb1;
         tc_item(ta, item, nt, mt, kb0, kb1);
         for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
-          const int s = gk % kTcWStages, b = gk & 1;
-          // each warp decides together (its lanes meet at __syncwarp below)
-          if (!__all_sync(0xffffffffu, mbar_wait(&bars->w_full[s], (gk / kTcWStages) & 1))) dead = true;
-          if (!dead && gk >= 2 && !__all_sync(0xffffffffu, kblock_done(bars, gk - 2)))
-            dead = true;  // k block gk-2 read buffer b
+          const int s = gk % SW, na = gk % NA;
+          // each warp decides together (the TMEM stores are warp-collective)
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->w_full[s], (gk / SW) & 1))) dead = true;
+          if (!dead && gk >= NA && !__all_sync(0xffffffffu, mbar_wait(&bars->ta_empty[na], ((gk / NA) - 1) & 1)))
+            dead = true;  // k block gk - NA read this A stage
           if (dead) break;
-          const uint8_t* raw = smem + Lay::kW + s * kTcBM * kTcBK;
-          uint8_t* dst = smem + Lay::kWbf + b * kTcBM * kTcBK * 2;
-#pragma unroll 2
-          for (int i = 0; i < 8; ++i) {
-            const int id = ct + 128 * i;
-            const int row = id >> 3, j = id & 7;  // 16-byte chunk j of the row: k = 16j .. 16j+15
-            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kTcBK + 16 * j);
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint4 o0, o1;
-            if (ta.f16) {  // one exact conversion per pair
-              o0.x = e4m3x2_to_f16x2(w4[0]);
-              o0.y = e4m3x2_to_f16x2(w4[0] >> 16);
-              o0.z = e4m3x2_to_f16x2(w4[1]);
-              o0.w = e4m3x2_to_f16x2(w4[1] >> 16);
-              o1.x = e4m3x2_to_f16x2(w4[2]);
-              o1.y = e4m3x2_to_f16x2(w4[2] >> 16);
-              o1.z = e4m3x2_to_f16x2(w4[3]);
-              o1.w = e4m3x2_to_f16x2(w4[3] >> 16);
-            } else {
-              o0.x = e4m3x2_to_bf16x2(w4[0]);
-              o0.y = e4m3x2_to_bf16x2(w4[0] >> 16);
-              o0.z = e4m3x2_to_bf16x2(w4[1]);
-              o0.w = e4m3x2_to_bf16x2(w4[1] >> 16);
-              o1.x = e4m3x2_to_bf16x2(w4[2]);
-              o1.y = e4m3x2_to_bf16x2(w4[2] >> 16);
-              o1.z = e4m3x2_to_bf16x2(w4[3]);
-              o1.w = e4m3x2_to_bf16x2(w4[3] >> 16);
+          tc_fence_after();
+          // row `row` of the raw tile: 16-byte chunk j (k = 16j .. 16j+15) at
+          // chunk position j ^ (row mod 8) (128-byte swizzle; a warp's 32 rows
+          // spread over all banks)
+          const uint8_t* rr = smem + Lay::kW + s * Lay::kWBytes + row * kTcBK;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {  // 32 k -> 16 columns
+            const uint4 v0 = *reinterpret_cast<const uint4*>(rr + (((2 * h) ^ r8) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(rr + (((2 * h + 1) ^ r8) << 4));
+            const uint32_t w8[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            uint32_t o[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              if (ta.f16) {  // one exact conversion per pair
+                o[2 * i] = e4m3x2_to_f16x2(w8[i]);
+                o[2 * i + 1] = e4m3x2_to_f16x2(w8[i] >> 16);
+              } else {
+                o[2 * i] = e4m3x2_to_bf16x2(w8[i]);
+                o[2 * i + 1] = e4m3x2_to_bf16x2(w8[i] >> 16);
+              }
             }
-            // 16-bit chunks c, c+1 (8 elements each) of atom j/4, 128-byte swizzle
-            const int atom = j >> 2, c = (j & 3) * 2, r8 = row & 7;
-            uint8_t* base = dst + atom * kTcBM * 128 + row * 128;
-            *reinterpret_cast<uint4*>(base + ((c ^ r8) << 4)) = o0;
-            *reinterpret_cast<uint4*>(base + (((c + 1) ^ r8) << 4)) = o1;
+            tmem_st16(trow + na * (kTcBK / 2) + 16 * h, o);
           }
-          fence_proxy_async();  // generic-proxy stores -> visible to the MMA (async proxy)
+          // the raw tile is in registers: its slot is free
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars->wbf_full[b]);
-            mbar_arrive(&bars->w_empty[s]);
-          }
+          if (lane == 0) mbar_arrive(&bars->w_empty[s]);
+          // the A stage is written before the MMA issuer may read it
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->ta_full[na]);
         }
       }
     }
@@ -431,19 +459,48 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int hf = (warp - 6) >> 2;
     const int row = 32 * q + lane;  // weight row within the tile
     pdl_wait();
+    // Per item, lane l holds the weight-tile scales of k blocks kb0 + l and
+    // kb0 + 32 + l, and the unscale of this warp's token column l; they are
+    // loaded one item ahead, so that no load latency falls between items.
+    struct ItemConsts {
+      float s0, s1, u;
+    };
+    auto load_consts = [&](int item) {
+      ItemConsts c{1.0f, 1.0f, 1.0f};
+      if (item < nitems) {
+        int nt, mt, kb0, kb1;
+        tc_item(ta, item, nt, mt, kb0, kb1);
+        if (FP8) {
+          const uint16_t* srow = a.S + (size_t)nt * ta.kblocks;
+          if (kb0 + lane < kb1) c.s0 = bf16_to_f32(__ldg(srow + kb0 + lane));
+          if (kb0 + 32 + lane < kb1) c.s1 = bf16_to_f32(__ldg(srow + kb0 + 32 + lane));
+        }
+        const int mc0 = mt * NT + hf * HC;
+        if (ta.f16 && lane < HC && mc0 + lane < a.M) c.u = __ldg(a.unscale + mc0 + lane);
+      }
+      return c;
+    };
+    ItemConsts cur = load_consts(cid);
     float acc[HC];
     int gk = 0;
     for (int item = cid; item < nitems && !dead; item += ncl) {
       int nt, mt, kb0, kb1;
       tc_item(ta, item, nt, mt, kb0, kb1);
       const int ks = item % ta.ksplit;
+      const ItemConsts nxt = load_consts(item + ncl);
 #pragma unroll
       for (int j = 0; j < HC; ++j) acc[j] = 0.0f;
       for (int kb = kb0; kb < kb1 && !dead; ++kb, ++gk) {
-        const int tb = gk % kTcTmemBufs;
-        const float s = ta.fp8 ? bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb)) : 1.0f;
-        // the TMEM loads below are warp-collective: the warp decides together
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / kTcTmemBufs) & 1))) dead = true;
+        const int tb = gk % TB;
+        const int i = kb - kb0;
+        float s = 1.0f;
+        if (FP8)
+          s = i < 64 ? __shfl_sync(0xffffffffu, i < 32 ? cur.s0 : cur.s1, i & 31)
+                     : bf16_to_f32(__ldg(a.S + (size_t)nt * ta.kblocks + kb));
+        // the TMEM loads below are warp-collective: the warp decides together.
+        // The phase awaited cannot alias a later one: k block gk + TB needs the
+        // TMEM buffer this warp frees below.
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / TB) & 1))) dead = true;
         if (dead) break;
         tc_fence_after();
         // 16 columns per TMEM load: two loads in flight before one wait at
@@ -464,9 +521,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int m0 = mt * NT + hf * HC;
       if (ta.f16) {  // the activation rows' prescale 2^j, undone exactly
 #pragma unroll
-        for (int j = 0; j < HC; ++j)
-          if (m0 + j < a.M) acc[j] *= __ldg(a.unscale + m0 + j);
+        for (int j = 0; j < HC; ++j) acc[j] *= __shfl_sync(0xffffffffu, cur.u, j);
       }
+      cur = nxt;
       tc_item_store<HC>(a, ta.ksplit, ta.part, ks, nt * kTcBM + row, m0, acc, L);
     }
   }
@@ -475,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_trigger();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemBufs * NT));
+    tmem_free(tmem, Lay::kTmemCols);
   }
 }
 
@@ -521,14 +578,17 @@ struct W8Cfg {
 };
 
 struct W8Bars {
-  uint64_t w_full[8], a_full[8], stage_empty[8];
-  uint64_t sc_full[8], sc_empty[8];
-  uint64_t mma_done[4], tmem_empty[4];
+  static constexpr int kMaxRing = 8, kMaxTmem = 4;
+  uint64_t w_full[kMaxRing], a_full[kMaxRing], stage_empty[kMaxRing];
+  uint64_t sc_full[kMaxRing], sc_empty[kMaxRing];
+  uint64_t mma_done[kMaxTmem], tmem_empty[kMaxTmem];
   uint32_t tmem_base;
 };
 
 template <int NT>
 constexpr int w8_smem_bytes() {
+  static_assert(W8Cfg<NT>::kStages <= W8Bars::kMaxRing && W8Cfg<NT>::kBufs <= W8Bars::kMaxTmem, "barriers");
+  static_assert(W8Cfg<NT>::kBars + (int)sizeof(W8Bars) + 1024 <= 232448, "shared memory");
   return W8Cfg<NT>::kBars + (int)sizeof(W8Bars) + 1024;  // + alignment slack
 }
 
@@ -799,13 +859,14 @@ static cudaError_t launch_w8a8(const GemvArgs& g, cudaStream_t s) {
   return e;
 }
 
-template <int NT>
-static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
+template <int NT, bool FP8>
+static cudaError_t launch_tc(const GemvArgs& g, cudaStream_t s) {
   static int done_mask[64] = {0};
+  constexpr bool fp8 = FP8;
   CUtensorMap tmW, tmA;
   if (fp8) {
     if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, g.W, g.K, g.N, (uint64_t)g.K, kTcBK, kTcBM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+                   CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   } else {
     if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g.W, g.K, g.N, (uint64_t)g.K * 2, 64, kTcBM,
@@ -837,8 +898,8 @@ static cudaError_t launch_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int smem = tc_smem_bytes<NT>();
-  auto kern = gemm_tc_kernel<NT>;
+  const int smem = tc_smem_bytes<NT, FP8>();
+  auto kern = gemm_tc_kernel<NT, FP8>;
   cudaError_t e = set_smem_once((const void*)kern, smem, done_mask);
   if (e != cudaSuccess) return e;
   const int nitems = ta.m_tiles * ta.n_tiles * ta.ksplit;
@@ -913,8 +974,8 @@ cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
     if (nt == 128) return launch_w8a8<128>(g, s);
     return launch_w8a8<256>(g, s);
   }
-  if (tc_nt(g.M) == 64) return launch_tc<64>(g, fp8, s);
-  return launch_tc<128>(g, fp8, s);
+  if (tc_nt(g.M) == 64) return fp8 ? launch_tc<64, true>(g, s) : launch_tc<64, false>(g, s);
+  return fp8 ? launch_tc<128, true>(g, s) : launch_tc<128, false>(g, s);
 }
 
 int status_gemm_tc(int clear) { return tu_status(clear); }
