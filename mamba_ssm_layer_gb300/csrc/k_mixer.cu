@@ -395,7 +395,7 @@ cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------------------ activation prep
 
-// The norm that produces a GEMV's activation, one CTA (512 threads) per row:
+// The norm that produces a GEMV's or GEMM's activation rows:
 //   PREP_RMSNORM  x * r * w,            r = 1/sqrt(mean(x^2) + eps)   (source
 //                 listing "nemotron_mamba2.rs", module header step 1: weight*x)
 //   PREP_GATED    y * r * w * silu(z),  r over groups of `group`      (step 6:
@@ -407,225 +407,308 @@ cudaError_t launch_ssm_scan_seq(const ScanArgs& a, cudaStream_t s) {
 // the exact products whatever the summation order (norm_round_bf16).
 constexpr int kPrepMaxPer = 32;  // elements per thread: K <= 32 * threads
 
-// One CTA of kPrepThreads threads per row (128 for K <= 4096, 256 for K <= 8192,
-// 512 above): small CTAs keep several rows resident per SM.
+// Bytes of one row's staged inputs: per chunk of 8 elements and thread, the
+// fp32 y (32 B) and bf16 z (16 B) of the gated norm, or the bf16 x (16 B).
+__host__ __device__ constexpr int prep_stage_bytes(int threads, bool gated) {
+  return threads * (kPrepMaxPer / 8) * (gated ? 48 : 16);
+}
+
+// silu of the gated norm.  Its bf16 output is a rounding point whose
+// decisions are held to 2^-12 of the exact value, so the hardware exp2 and
+// divide approximations (relative errors of a few 2^-23) serve; for z below
+// about -87 the gate is 0 (the exact value is below 1e-36).
+__device__ __forceinline__ float silu_gate(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Persistent CTAs of kPrepThreads threads (128 for K <= 4096, 256 for K <=
+// 8192, 512 above) walk rows m = blockIdx.x, + gridDim.x, ...  While a row is
+// computed, the next row's inputs are copied into the other of two shared
+// stages (cp.async); each thread copies exactly the 16-byte pieces it later
+// reads, so the hand-over needs no barrier.  The norm weight is read once per
+// CTA.
 template <int kPrepThreads>
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
-  constexpr int kW = kPrepThreads / 32;  // warps
-  pdl_wait();
-  pdl_trigger();
-  const int m = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ float s_hi[kW], s_lo[kW], s_max[kW];
-  __shared__ float part[kPrepThreads * kPrepMaxPer / 8];  // gated mode: per-run sums of squares
-  const int K = a.K;
-  float v[kPrepMaxPer];
-  uint4 wv[kPrepMaxPer / 8], zv[kPrepMaxPer / 8];  // issued with the inputs: independent loads
-  // element e of this thread: k = (tid + kPrepThreads * (e / 8)) * 8 + e % 8
+__device__ __forceinline__ void prep_fetch_row(const PrepArgs& a, int m, uint8_t* st, int tid) {
+  const bool gated = a.mode == PREP_GATED;
 #pragma unroll
   for (int c = 0; c < kPrepMaxPer / 8; ++c) {
     const int k0 = (tid + kPrepThreads * c) * 8;
-    if (k0 < K) {
-      if (a.mode != PREP_QUANT) wv[c] = *reinterpret_cast<const uint4*>(a.w + k0);  // no weight in QUANT mode
-      if (a.mode == PREP_GATED) zv[c] = *reinterpret_cast<const uint4*>(a.z + (size_t)m * a.ldz + k0);
-      if (a.mode == PREP_RMSNORM || a.mode == PREP_QUANT) {
-        const uint4 u = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.ldx + k0);
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[c * 8 + 2 * e] = bf16lo(w4[e]);
-          v[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
-        }
+    const int u = c * kPrepThreads + tid;  // this thread's piece of chunk c
+    if (k0 < a.K) {
+      if (gated) {
+        cp_async16(st + u * 32, a.y + (size_t)m * a.ldy + k0);
+        cp_async16(st + u * 32 + 16, a.y + (size_t)m * a.ldy + k0 + 4);
+        cp_async16(st + kPrepThreads * (kPrepMaxPer / 8) * 32 + u * 16, a.z + (size_t)m * a.ldz + k0);
       } else {
-        const float4 f0 = *reinterpret_cast<const float4*>(a.y + (size_t)m * a.ldy + k0);
-        const float4 f1 = *reinterpret_cast<const float4*>(a.y + (size_t)m * a.ldy + k0 + 4);
-        v[c * 8 + 0] = f0.x; v[c * 8 + 1] = f0.y; v[c * 8 + 2] = f0.z; v[c * 8 + 3] = f0.w;
-        v[c * 8 + 4] = f1.x; v[c * 8 + 5] = f1.y; v[c * 8 + 6] = f1.z; v[c * 8 + 7] = f1.w;
+        cp_async16(st + u * 16, a.x + (size_t)m * a.ldx + k0);
       }
-    } else {
-      wv[c] = zv[c] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
-    }
-  }
-  if (a.mode == PREP_QUANT) {
-    // rows as they are
-  } else if (a.mode == PREP_RMSNORM) {
-    float hi = 0.0f, lo = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kPrepMaxPer; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
-    two_sum_warp(hi, lo);
-    if (lane == 0) {
-      s_hi[warp] = hi;
-      s_lo[warp] = lo;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      // combine the warps' pairs in a fixed order
-      float h = 0.0f, l = 0.0f;
-      for (int w = 0; w < kW; ++w) {
-        two_sum_acc(h, l, s_hi[w]);
-        l += s_lo[w];
-      }
-      s_hi[0] = h;
-      s_lo[0] = l;
-    }
-    __syncthreads();
-    const NormR nr = norm_r(s_hi[0], s_lo[0], K, a.eps);
-#pragma unroll
-    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-      const int k0 = (tid + kPrepThreads * c) * 8;
-      if (k0 < K) {
-        const uint4 u = wv[c];
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), nr));
-          v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), nr));
-        }
-      }
-    }
-  } else {
-    // sum of squares per group in a fixed order (results do not depend on
-    // scheduling, so equal rows give equal outputs): each run of 8 elements
-    // in sequence, then either warp butterflies and the warps' chunks of 256
-    // in index order (group % 256 == 0), or a pairwise tree over the runs of
-    // each group
-    const int nrun = K / 8;  // runs of 8 in the row; a run never straddles a group (group % 16 == 0)
-    float ssr[kPrepMaxPer / 8];
-#pragma unroll
-    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-      float ss = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
-      ssr[c] = ss;  // zero past K
-    }
-    int gstride;  // part[] index of group j's sum = j * gstride
-    if (a.group % 256 == 0) {
-#pragma unroll
-      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-        const float ws = warp_sum(ssr[c]);
-        if (lane == 0) part[c * kW + warp] = ws;  // chunk of 256 elements starting at (warp + kW c) * 256
-      }
-      __syncthreads();
-      const int cpg = a.group / 256, ngroups = K / a.group;
-      float gs = 0.0f;
-      if (tid < ngroups)
-        for (int j = 0; j < cpg; ++j) gs += part[tid * cpg + j];
-      __syncthreads();
-      if (tid < ngroups) part[tid] = gs;
-      gstride = 1;
-    } else {
-      const int R = a.group / 8;
-#pragma unroll
-      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-        const int run = tid + kPrepThreads * c;
-        if (run < nrun) part[run] = ssr[c];
-      }
-      __syncthreads();
-      for (int st = 1; st < R; st <<= 1) {
-        for (int run = tid; run < nrun; run += kPrepThreads) {
-          const int li = run % R;
-          if ((li & (2 * st - 1)) == 0 && li + st < R) part[run] += part[run + st];
-        }
-        __syncthreads();
-      }
-      gstride = R;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-      const int k0 = (tid + kPrepThreads * c) * 8;
-      if (k0 < K) {
-        const float r = 1.0f / sqrtf(part[(k0 / a.group) * gstride] / (float)a.group + a.eps);
-        const uint4 u = wv[c];
-        const uint4 zz = zv[c];
-        const uint32_t w4[4] = {u.x, u.y, u.z, u.w}, z4[4] = {zz.x, zz.y, zz.z, zz.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float g0 = v[c * 8 + 2 * e] * r * bf16lo(w4[e]) * silu_f(bf16lo(z4[e]));
-          const float g1 = v[c * 8 + 2 * e + 1] * r * bf16hi(w4[e]) * silu_f(bf16hi(z4[e]));
-          v[c * 8 + 2 * e] = bf16_to_f32(f32_to_bf16(g0));
-          v[c * 8 + 2 * e + 1] = bf16_to_f32(f32_to_bf16(g1));
-        }
-      }
-    }
-  }
-  if (a.q8) {
-    // W8A8 activations: a 128-element block is the 8-element runs of 16
-    // consecutive threads (one half-warp)
-#pragma unroll
-    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-      const int k0 = (tid + kPrepThreads * c) * 8;
-      float bm = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) bm = fmaxf(bm, fabsf(v[c * 8 + e]));  // v = 0 past K
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-      if (k0 < K) {
-        const float inv = bm > 0.0f ? 448.0f / bm : 0.0f;
-        uint32_t q[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint16_t h;
-          asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-              : "=h"(h)
-              : "f"(v[c * 8 + 2 * e + 1] * inv), "f"(v[c * 8 + 2 * e] * inv));
-          q[e] = h;
-        }
-        *reinterpret_cast<uint2*>(a.q8 + (size_t)m * a.ldq + k0) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
-        if ((tid & 15) == 0) a.sq[(size_t)(k0 >> 7) * a.ldsq + m] = bm / 448.0f;
-      }
-    }
-  }
-  if (!a.out) return;
-  float up = 1.0f;
-  if (a.f16) {
-    float mx = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kPrepMaxPer; ++e) mx = fmaxf(mx, fabsf(v[e]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) s_max[warp] = mx;
-    __syncthreads();
-    mx = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) mx = fmaxf(mx, s_max[w]);
-    const unsigned bits = __float_as_uint(mx);
-    const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
-    const int jx = max(-120, min(120, 14 - ex));
-    up = ldexpf(1.0f, jx);
-    if (tid == 0) a.unscale[m] = ldexpf(1.0f, -jx);
-  } else if (a.unscale && tid == 0) {
-    a.unscale[m] = 1.0f;
-  }
-#pragma unroll
-  for (int c = 0; c < kPrepMaxPer / 8; ++c) {
-    const int k0 = (tid + kPrepThreads * c) * 8;
-    if (k0 < K) {
-      uint32_t o4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (a.f16) {
-          uint32_t h;
-          asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(v[c * 8 + 2 * e + 1] * up), "f"(v[c * 8 + 2 * e] * up));
-          o4[e] = h;
-        } else {
-          o4[e] = pack_bf16x2(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
-        }
-      }
-      *reinterpret_cast<uint4*>(a.out + (size_t)m * a.ldo + k0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
     }
   }
 }
 
+template <int kPrepThreads>
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
+  constexpr int kW = kPrepThreads / 32;  // warps
+  extern __shared__ __align__(16) uint8_t prep_stage[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float s_hi[kW], s_lo[kW], s_max[kW];
+  __shared__ float part[kPrepThreads * kPrepMaxPer / 8];  // gated mode: per-run sums of squares
+  const int K = a.K;
+  const bool gated = a.mode == PREP_GATED;
+  const int sbytes = prep_stage_bytes(kPrepThreads, gated);
+  uint4 wv[kPrepMaxPer / 8];  // the norm weight: not an output of the previous kernel
+#pragma unroll
+  for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+    const int k0 = (tid + kPrepThreads * c) * 8;
+    wv[c] = (k0 < K && a.mode != PREP_QUANT) ? *reinterpret_cast<const uint4*>(a.w + k0) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  pdl_wait();
+  pdl_trigger();
+  if ((int)blockIdx.x < a.M) prep_fetch_row<kPrepThreads>(a, blockIdx.x, prep_stage, tid);
+  cp_async_commit();
+  int it = 0;
+  for (int m = blockIdx.x; m < a.M; m += gridDim.x, ++it) {
+    uint8_t* cur = prep_stage + (it & 1) * sbytes;
+    if (m + (int)gridDim.x < a.M) prep_fetch_row<kPrepThreads>(a, m + gridDim.x, prep_stage + ((it + 1) & 1) * sbytes, tid);
+    cp_async_commit();
+    cp_async_wait1();  // this thread's pieces of row m have landed
+    float v[kPrepMaxPer];
+    uint4 zv[kPrepMaxPer / 8];
+    // element e of this thread: k = (tid + kPrepThreads * (e / 8)) * 8 + e % 8
+#pragma unroll
+    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+      const int k0 = (tid + kPrepThreads * c) * 8;
+      const int u = c * kPrepThreads + tid;
+      zv[c] = make_uint4(0u, 0u, 0u, 0u);
+      if (k0 < K) {
+        if (!gated) {
+          const uint4 x4 = *reinterpret_cast<const uint4*>(cur + u * 16);
+          const uint32_t w4[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[c * 8 + 2 * e] = bf16lo(w4[e]);
+            v[c * 8 + 2 * e + 1] = bf16hi(w4[e]);
+          }
+        } else {
+          const float4 f0 = *reinterpret_cast<const float4*>(cur + u * 32);
+          const float4 f1 = *reinterpret_cast<const float4*>(cur + u * 32 + 16);
+          zv[c] = *reinterpret_cast<const uint4*>(cur + kPrepThreads * (kPrepMaxPer / 8) * 32 + u * 16);
+          v[c * 8 + 0] = f0.x; v[c * 8 + 1] = f0.y; v[c * 8 + 2] = f0.z; v[c * 8 + 3] = f0.w;
+          v[c * 8 + 4] = f1.x; v[c * 8 + 5] = f1.y; v[c * 8 + 6] = f1.z; v[c * 8 + 7] = f1.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[c * 8 + e] = 0.0f;
+      }
+    }
+    if (a.mode == PREP_QUANT) {
+      // rows as they are
+    } else if (a.mode == PREP_RMSNORM) {
+      float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+      for (int e = 0; e < kPrepMaxPer; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
+      two_sum_warp(hi, lo);
+      if (lane == 0) {
+        s_hi[warp] = hi;
+        s_lo[warp] = lo;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        // combine the warps' pairs in a fixed order
+        float h = 0.0f, l = 0.0f;
+        for (int w = 0; w < kW; ++w) {
+          two_sum_acc(h, l, s_hi[w]);
+          l += s_lo[w];
+        }
+        s_hi[0] = h;
+        s_lo[0] = l;
+      }
+      __syncthreads();
+      const NormR nr = norm_r(s_hi[0], s_lo[0], K, a.eps);
+#pragma unroll
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        const int k0 = (tid + kPrepThreads * c) * 8;
+        if (k0 < K) {
+          const uint4 u = wv[c];
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[c * 8 + 2 * e] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e], bf16lo(w4[e]), nr));
+            v[c * 8 + 2 * e + 1] = bf16_to_f32(norm_round_bf16(v[c * 8 + 2 * e + 1], bf16hi(w4[e]), nr));
+          }
+        }
+      }
+    } else {
+      // sum of squares per group in a fixed order (results do not depend on
+      // scheduling, so equal rows give equal outputs): each run of 8 elements
+      // in sequence, then either warp butterflies and the warps' chunks of 256
+      // in index order (group % 256 == 0), or a pairwise tree over the runs of
+      // each group
+      const int nrun = K / 8;  // runs of 8 in the row; a run never straddles a group (group % 16 == 0)
+      float ssr[kPrepMaxPer / 8];
+#pragma unroll
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        float ss = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[c * 8 + e], v[c * 8 + e], ss);
+        ssr[c] = ss;  // zero past K
+      }
+      int gstride;  // part[] index of group j's sum = j * gstride
+      if (a.group % 256 == 0) {
+#pragma unroll
+        for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+          const float ws = warp_sum(ssr[c]);
+          if (lane == 0) part[c * kW + warp] = ws;  // chunk of 256 elements starting at (warp + kW c) * 256
+        }
+        __syncthreads();
+        const int cpg = a.group / 256, ngroups = K / a.group;
+        float gs = 0.0f;
+        if (tid < ngroups)
+          for (int j = 0; j < cpg; ++j) gs += part[tid * cpg + j];
+        __syncthreads();
+        if (tid < ngroups) part[tid] = gs;
+        gstride = 1;
+      } else {
+        const int R = a.group / 8;
+#pragma unroll
+        for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+          const int run = tid + kPrepThreads * c;
+          if (run < nrun) part[run] = ssr[c];
+        }
+        __syncthreads();
+        for (int st = 1; st < R; st <<= 1) {
+          for (int run = tid; run < nrun; run += kPrepThreads) {
+            const int li = run % R;
+            if ((li & (2 * st - 1)) == 0 && li + st < R) part[run] += part[run + st];
+          }
+          __syncthreads();
+        }
+        gstride = R;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        const int k0 = (tid + kPrepThreads * c) * 8;
+        if (k0 < K) {
+          const float r = rsqrtf(part[(k0 / a.group) * gstride] / (float)a.group + a.eps);
+          const uint4 u = wv[c];
+          const uint4 zz = zv[c];
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w}, z4[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float g0 = v[c * 8 + 2 * e] * r * bf16lo(w4[e]) * silu_gate(bf16lo(z4[e]));
+            const float g1 = v[c * 8 + 2 * e + 1] * r * bf16hi(w4[e]) * silu_gate(bf16hi(z4[e]));
+            v[c * 8 + 2 * e] = bf16_to_f32(f32_to_bf16(g0));
+            v[c * 8 + 2 * e + 1] = bf16_to_f32(f32_to_bf16(g1));
+          }
+        }
+      }
+    }
+    if (a.q8) {
+      // W8A8 activations: a 128-element block is the 8-element runs of 16
+      // consecutive threads (one half-warp)
+#pragma unroll
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        const int k0 = (tid + kPrepThreads * c) * 8;
+        float bm = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) bm = fmaxf(bm, fabsf(v[c * 8 + e]));  // v = 0 past K
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+        if (k0 < K) {
+          const float inv = bm > 0.0f ? 448.0f / bm : 0.0f;
+          uint32_t q[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint16_t h;
+            asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                : "=h"(h)
+                : "f"(v[c * 8 + 2 * e + 1] * inv), "f"(v[c * 8 + 2 * e] * inv));
+            q[e] = h;
+          }
+          *reinterpret_cast<uint2*>(a.q8 + (size_t)m * a.ldq + k0) = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+          if ((tid & 15) == 0) a.sq[(size_t)(k0 >> 7) * a.ldsq + m] = bm / 448.0f;
+        }
+      }
+    }
+    if (a.out) {
+    float up = 1.0f;
+    if (a.f16) {
+      float mx = 0.0f;
+#pragma unroll
+      for (int e = 0; e < kPrepMaxPer; ++e) mx = fmaxf(mx, fabsf(v[e]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) s_max[warp] = mx;
+      __syncthreads();
+      mx = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kW; ++w) mx = fmaxf(mx, s_max[w]);
+      const unsigned bits = __float_as_uint(mx);
+      const int ex = bits ? (int)((bits >> 23) & 0xFF) - 127 : 14;
+      const int jx = max(-120, min(120, 14 - ex));
+      up = ldexpf(1.0f, jx);
+      if (tid == 0) a.unscale[m] = ldexpf(1.0f, -jx);
+    } else if (a.unscale && tid == 0) {
+      a.unscale[m] = 1.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+      const int k0 = (tid + kPrepThreads * c) * 8;
+      if (k0 < K) {
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (a.f16) {
+            uint32_t h;
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(v[c * 8 + 2 * e + 1] * up), "f"(v[c * 8 + 2 * e] * up));
+            o4[e] = h;
+          } else {
+            o4[e] = pack_bf16x2(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+          }
+        }
+        *reinterpret_cast<uint4*>(a.out + (size_t)m * a.ldo + k0) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+    }
+    }
+    __syncthreads();  // the shared reduction scratch is reused by the next row
+  }
+}
+
+// Grid of the persistent prep kernel: as many CTAs as fit on the SMs (from the
+// occupancy query, cached per variant and stage size), at most one per row.
+template <int T>
+static cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
+  static int done_mask[64] = {0};
+  static int cached_smem[2] = {-1, -1}, cached_nb[2] = {0, 0};
+  const bool gated = a.mode == PREP_GATED;
+  const int smem = 2 * prep_stage_bytes(T, gated);
+  cudaError_t e = set_smem_once((const void*)prep_kernel<T>, smem, done_mask);
+  if (e != cudaSuccess) return e;
+  int& nb = cached_nb[gated ? 1 : 0];
+  if (cached_smem[gated ? 1 : 0] != smem) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, prep_kernel<T>, T, smem);
+    if (e != cudaSuccess) return e;
+    if (nb < 1) nb = 1;
+    cached_smem[gated ? 1 : 0] = smem;
+  }
+  int grid = nb * num_sms();
+  if (grid > a.M) grid = a.M;
+  return launch_k(prep_kernel<T>, dim3(grid), dim3(T), smem, s, a.pdl != 0, a);
+}
+
 cudaError_t launch_prep(const PrepArgs& a0, cudaStream_t s) {
   const PrepArgs& a = a0;
+  if (a.M <= 0) return cudaSuccess;
   trace_pre(K_PREP, s);
   cudaError_t e;
-  if (a.K <= 128 * kPrepMaxPer) e = launch_k(prep_kernel<128>, dim3(a.M), dim3(128), 0, s, a.pdl != 0, a);
-  else if (a.K <= 256 * kPrepMaxPer) e = launch_k(prep_kernel<256>, dim3(a.M), dim3(256), 0, s, a.pdl != 0, a);
-  else e = launch_k(prep_kernel<512>, dim3(a.M), dim3(512), 0, s, a.pdl != 0, a);
+  if (a.K <= 128 * kPrepMaxPer) e = launch_prep_t<128>(a, s);
+  else if (a.K <= 256 * kPrepMaxPer) e = launch_prep_t<256>(a, s);
+  else e = launch_prep_t<512>(a, s);
   trace_post(K_PREP, s);
   return e;
 }
