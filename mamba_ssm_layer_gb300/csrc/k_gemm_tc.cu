@@ -760,11 +760,42 @@ __global__ void __launch_bounds__(kW8Threads, 1)
 }
 
 // Split-k reduction: sums the k-split partials of each output in split order
-// (deterministic) and runs the epilogue.
-__global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const GemvArgs a, const float* part, int ksplit) {
+// (deterministic) and runs the epilogue.  vec4: four adjacent outputs per
+// thread (store and residual epilogues with 4-aligned rows), the splits'
+// loads issued together.
+__global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const GemvArgs a, const float* part, int ksplit,
+                                                              int vec4) {
   pdl_wait();
   pdl_trigger();
   const int L = a.dconv - 1;
+  if (vec4) {
+    const int nq = a.N / 4;
+    const size_t quads = (size_t)a.M * nq, sstride = (size_t)a.M * a.N;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < quads; i += (size_t)gridDim.x * blockDim.x) {
+      const int m = (int)(i / nq), n = (int)(i % nq) * 4;
+      uint2 r = make_uint2(0u, 0u);
+      if (a.epi == EPI_RESID) r = *reinterpret_cast<const uint2*>(a.resid + (size_t)m * a.ldr + n);
+      const float* pp = part + (size_t)m * a.N + n;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+      for (int ks = 0; ks < ksplit; ++ks) {
+        const float4 v = *reinterpret_cast<const float4*>(pp + ks * sstride);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      if (a.epi == EPI_RESID) {
+        acc.x += bf16lo(r.x);
+        acc.y += bf16hi(r.x);
+        acc.z += bf16lo(r.y);
+        acc.w += bf16hi(r.y);
+      }
+      *reinterpret_cast<uint2*>(a.out + (size_t)m * a.ldo + n) =
+          make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+    }
+    return;
+  }
   const size_t total = (size_t)a.M * a.N;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
     const int m = (int)(i / a.N), n = (int)(i % a.N);
@@ -778,6 +809,13 @@ __global__ void __launch_bounds__(256) gemm_tc_reduce_kernel(const GemvArgs a, c
 }
 
 // ------------------------------------------------------------------ host
+
+// Whether the split-k reduction may take four adjacent outputs per thread.
+static bool reduce_vec4(const GemvArgs& g) {
+  if (g.epi == EPI_INPROJ_CONV || g.N % 4 || g.ldo % 4 || (reinterpret_cast<uintptr_t>(g.out) & 7)) return false;
+  if (g.epi == EPI_RESID && (g.ldr % 4 || (reinterpret_cast<uintptr_t>(g.resid) & 7))) return false;
+  return true;
+}
 
 bool gemm_tc_supported(int M, int N, int K, bool fp8) {
   (void)N;
@@ -850,11 +888,11 @@ static cudaError_t launch_w8a8(const GemvArgs& g, cudaStream_t s) {
   trace_post(K_GEMM_TC, s);
   if (e != cudaSuccess || ta.ksplit == 1) return e;
   const size_t total = (size_t)g.M * g.N;
-  int rgrid = (int)((total + 255) / 256);
+  int rgrid = (int)(((reduce_vec4(g) ? total / 4 : total) + 255) / 256);
   if (rgrid > 8 * num_sms()) rgrid = 8 * num_sms();
   trace_pre(K_GEMM_TC_REDUCE, s);
   e = launch_k(gemm_tc_reduce_kernel, dim3(rgrid), dim3(256), 0, s, g.pdl != 0, g, (const float*)ta.part,
-               ta.ksplit);
+               ta.ksplit, reduce_vec4(g) ? 1 : 0);
   trace_post(K_GEMM_TC_REDUCE, s);
   return e;
 }
@@ -910,11 +948,11 @@ static cudaError_t launch_tc(const GemvArgs& g, cudaStream_t s) {
   trace_post(K_GEMM_TC, s);
   if (e != cudaSuccess || ta.ksplit == 1) return e;
   const size_t total = (size_t)g.M * g.N;
-  int rgrid = (int)((total + 255) / 256);
+  int rgrid = (int)(((reduce_vec4(g) ? total / 4 : total) + 255) / 256);
   if (rgrid > 8 * num_sms()) rgrid = 8 * num_sms();
   trace_pre(K_GEMM_TC_REDUCE, s);
   e = launch_k(gemm_tc_reduce_kernel, dim3(rgrid), dim3(256), 0, s, g.pdl != 0, g, (const float*)ta.part,
-               ta.ksplit);
+               ta.ksplit, reduce_vec4(g) ? 1 : 0);
   trace_post(K_GEMM_TC_REDUCE, s);
   return e;
 }
