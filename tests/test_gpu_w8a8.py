@@ -62,18 +62,21 @@ def test_w8a8_codes_scales_bit_exact_and_product(M, N, K):
     assert err <= TOL_BF16, err
 
 
-def test_w8a8_product_exact_on_integer_operands():
+# (40, 384, 512): 64-token tiles.  (300, 4900, 512): 256-token tiles, the second
+# one ragged, over 39 weight tiles, without a k split (the call has no
+# partials buffer).
+@pytest.mark.parametrize("M,N,K", [(40, 384, 512), (300, 4900, 512)])
+def test_w8a8_product_exact_on_integer_operands(M, N, K):
     # every block holds one 448 (so its scale is 1 and its codes are the values),
     # the rest small integers; weights small integers; power-of-two weight scales:
     # all partial sums are exact integers, so the bf16 result is the oracle's bit for bit
     rng = np.random.default_rng(5)
-    M, N, K = 40, 384, 512
     a = rng.integers(-8, 9, (M, K)).astype(np.float32)
     a[:, ::128] = 448.0
     A = synth.to_bf16_bits(a)
     wv = rng.integers(-8, 9, (N, K)).astype(np.float32)
     W = torch.from_numpy(wv).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-    S = synth.to_bf16_bits(np.exp2(rng.integers(-8, -2, (N // 128, K // 128))).astype(np.float32))
+    S = synth.to_bf16_bits(np.exp2(rng.integers(-8, -2, (-(-N // 128), K // 128))).astype(np.float32))
     got, _, _ = _w8a8(A, W, S)
     ref = np.stack([orc.w8a8_gemv(*orc.act_quant(A[m]), W, S) for m in range(M)])
     assert np.array_equal(got, orc.f64_array_to_bf16(ref))
