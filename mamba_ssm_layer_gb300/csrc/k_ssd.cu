@@ -847,7 +847,9 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 2) ssd_out_tc_kernel(const S
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int s_ = s0 + 8 * half + j;
-          l8[j] = (s_ <= t) ? v[8 * half + j] * expf(cst - cs_s[s_]) * dt_s[s_] : 0.0f;
+          // the hardware exp2 approximation (relative error a few 2^-23): L
+          // enters the MMA as a bf16 hi + lo pair, about 16 significant bits
+          l8[j] = (s_ <= t) ? v[8 * half + j] * __expf(cst - cs_s[s_]) * dt_s[s_] : 0.0f;
         }
         uint4 hi, lo;
         split8(l8, hi, lo);
@@ -867,28 +869,34 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 2) ssd_out_tc_kernel(const S
   }
   ok = __all_sync(0xffffffffu, mbar_wait(&bar[1], 0)) && ok;
   tc_fence_after();
+  // y = Y + exp(s_t) Yi + D x through shared memory (the space of L, whose
+  // MMAs are done; x from the x^T tile): each thread its row's half, then
+  // each warp stores whole rows
+  constexpr int kYp = P + 1;  // row pitch in floats: a warp's 32 rows fall in 32 banks
+  float* Ys = reinterpret_cast<float*>(Cs);
+  static_assert(kQ * (P + 1) * 4 <= 2 * kQ * N * 2, "y tile in the space of L");
   if (ok) {
-    const bool live = t < qc;
     const float Dh = a.D[h];
     const float ex = expf(cs_s[t]);
-    const uint16_t* xr = a.x + (size_t)(t0 + (live ? t : 0)) * a.ld_in + (size_t)h * P;
-    float* yo = a.y + (size_t)(t0 + t) * a.ldy + (size_t)h * P;
 #pragma unroll
     for (int c0 = half * (P / 2); c0 < (half + 1) * (P / 2); c0 += 16) {
       float y1[16], yi[16];
       tmem_ld16(tY + lane_base + c0, y1);
       tmem_ld16(tYi + lane_base + c0, yi);
-      if (!live) continue;
 #pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        const uint2 xx = *reinterpret_cast<const uint2*>(xr + c0 + j);
-        float4 r;
-        r.x = y1[j] + ex * yi[j] + Dh * bf16lo(xx.x);
-        r.y = y1[j + 1] + ex * yi[j + 1] + Dh * bf16hi(xx.x);
-        r.z = y1[j + 2] + ex * yi[j + 2] + Dh * bf16lo(xx.y);
-        r.w = y1[j + 3] + ex * yi[j + 3] + Dh * bf16hi(xx.y);
-        *reinterpret_cast<float4*>(yo + c0 + j) = r;
+      for (int j = 0; j < 16; ++j) {
+        const int pp = c0 + j;
+        const uint16_t xv = *reinterpret_cast<const uint16_t*>(Xt + sw128_chunk(P, pp, t >> 3) + (t & 7) * 2);
+        Ys[t * kYp + pp] = y1[j] + ex * yi[j] + Dh * bf16_to_f32(xv);
       }
+    }
+  }
+  __syncthreads();
+  if (ok) {
+    for (int r = warp; r < qc; r += kSsdTcOutThreads / 32) {
+      float* yo = a.y + (size_t)(t0 + r) * a.ldy + (size_t)h * P;
+#pragma unroll
+      for (int pp = (tid & 31); pp < P; pp += 32) yo[pp] = Ys[r * kYp + pp];
     }
   }
   if (tid == 0) mbar_drain(&bar[1], 0);  // no MMA still writes tensor memory when it is freed
