@@ -834,6 +834,16 @@ __global__ void __launch_bounds__(kSsdTcOutThreads, 2) ssd_out_tc_kernel(const S
     const float cst = cs_s[t];
 #pragma unroll 1
     for (int s0 = 64 * half; s0 < 64 * half + 64; s0 += 16) {
+      // columns s0 .. s0 + 15 lie above the diagonal for all of this warp's
+      // rows t < 32 (q + 1) when s0 >= 32 (q + 1): zeros, nothing to compute
+      if (s0 >= 32 * (q + 1)) {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        sw_store8(Cs, kQ, t, s0, z);
+        sw_store8(Bs, kQ, t, s0, z);
+        sw_store8(Cs, kQ, t, s0 + 8, z);
+        sw_store8(Bs, kQ, t, s0 + 8, z);
+        continue;
+      }
       float v[16];
       if (ok) {
         tmem_ld16(tS + lane_base + s0, v);
