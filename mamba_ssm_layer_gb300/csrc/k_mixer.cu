@@ -508,9 +508,22 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepArgs a) {
     if (a.mode == PREP_QUANT) {
       // rows as they are
     } else if (a.mode == PREP_RMSNORM) {
-      float hi = 0.0f, lo = 0.0f;
+      // one error-free pair per 8-element chunk (independent chains), then
+      // the chunks' pairs in order: the pair holds the sum to about 2^-48
+      // whatever the order
+      float hs[kPrepMaxPer / 8], ls[kPrepMaxPer / 8];
 #pragma unroll
-      for (int e = 0; e < kPrepMaxPer; ++e) two_sum_acc(hi, lo, v[e] * v[e]);
+      for (int c = 0; c < kPrepMaxPer / 8; ++c) {
+        hs[c] = ls[c] = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) two_sum_acc(hs[c], ls[c], v[c * 8 + e] * v[c * 8 + e]);
+      }
+      float hi = hs[0], lo = ls[0];
+#pragma unroll
+      for (int c = 1; c < kPrepMaxPer / 8; ++c) {
+        two_sum_acc(hi, lo, hs[c]);
+        lo += ls[c];
+      }
       two_sum_warp(hi, lo);
       if (lane == 0) {
         s_hi[warp] = hi;
