@@ -426,7 +426,8 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Persistent CTAs of kPrepThreads threads (128 for K <= 4096, 256 for K <=
-// 8192, 512 above) walk rows m = blockIdx.x, + gridDim.x, ...  While a row is
+// 8192, 512 above, and 512 whenever the rows are no more than the SMs) walk
+// rows m = blockIdx.x, + gridDim.x, ...  While a row is
 // computed, the next row's inputs are copied into the other of two shared
 // stages (cp.async); each thread copies exactly the 16-byte pieces it later
 // reads, so the hand-over needs no barrier.  The norm weight is read once per
@@ -719,9 +720,12 @@ cudaError_t launch_prep(const PrepArgs& a0, cudaStream_t s) {
   if (a.M <= 0) return cudaSuccess;
   trace_pre(K_PREP, s);
   cudaError_t e;
-  if (a.K <= 128 * kPrepMaxPer) e = launch_prep_t<128>(a, s);
-  else if (a.K <= 256 * kPrepMaxPer) e = launch_prep_t<256>(a, s);
-  else e = launch_prep_t<512>(a, s);
+  // rows no more than the SMs (batched decode): one 512-thread CTA per row,
+  // each thread with a short share of the row (the results do not depend on
+  // the thread count); else the smallest CTA that covers K, several rows per SM
+  if (a.M <= num_sms() || a.K > 256 * kPrepMaxPer) e = launch_prep_t<512>(a, s);
+  else if (a.K <= 128 * kPrepMaxPer) e = launch_prep_t<128>(a, s);
+  else e = launch_prep_t<256>(a, s);
   trace_post(K_PREP, s);
   return e;
 }
