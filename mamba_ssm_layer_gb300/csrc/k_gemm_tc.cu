@@ -71,9 +71,9 @@ struct TcBars {
 // fill shared memory.  bf16 weights: 32 KB swizzled tiles.
 template <int NT, bool FP8>
 struct TcLayout {
-  static constexpr int kWStages = FP8 ? (NT <= 64 ? 6 : 4) : 4;
+  static constexpr int kWStages = FP8 ? (NT <= 32 ? 8 : (NT <= 64 ? 6 : 4)) : 4;
   static constexpr int kWBytes = FP8 ? kTcBM * kTcBK : kTcBM * kTcBK * 2;
-  static constexpr int kAStages = FP8 ? (NT <= 64 ? 6 : 5) : (NT <= 64 ? 4 : 3);
+  static constexpr int kAStages = FP8 ? (NT <= 32 ? 8 : (NT <= 64 ? 6 : 5)) : (NT <= 64 ? 4 : 3);
   static constexpr int kABytes = NT * kTcBK * 2;  // one activation stage
   static constexpr int kTBufs = (FP8 && NT > 64) ? 3 : 4;  // k-block partials in TMEM
   static constexpr int kTAStages = FP8 ? (NT <= 64 ? 4 : 2) : 0;  // converted weight tiles in TMEM
@@ -503,15 +503,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!__all_sync(0xffffffffu, mbar_wait(&bars->mma_done[tb], (gk / TB) & 1))) dead = true;
         if (dead) break;
         tc_fence_after();
-        // 16 columns per TMEM load: two loads in flight before one wait at
-        // HC = 32 would hold 32 more registers than the 80 a thread has here
+        // at most 16 columns per TMEM load: two loads in flight before one
+        // wait at HC = 32 would hold 32 more registers than the 80 a thread
+        // has here
         const uint32_t ta_ = tmem + ((uint32_t)(32 * q) << 16) + tb * NT + hf * HC;
+        constexpr int CH = HC < 16 ? HC : 16;
 #pragma unroll
-        for (int c0 = 0; c0 < HC; c0 += 16) {
-          float v[16];
-          tmem_ld16(ta_ + c0, v);
+        for (int c0 = 0; c0 < HC; c0 += CH) {
+          float v[CH];
+          if constexpr (CH == 16) tmem_ld16(ta_ + c0, v);
+          else if constexpr (CH == 8) tmem_ld8(ta_ + c0, v);
+          else tmem_ld4(ta_ + c0, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[c0 + i] = fmaf(s, v[i], acc[c0 + i]);
+          for (int i = 0; i < CH; ++i) acc[c0 + i] = fmaf(s, v[i], acc[c0 + i]);
         }
         tc_fence_before();
         __syncwarp();
@@ -823,7 +827,9 @@ bool gemm_tc_supported(int M, int N, int K, bool fp8) {
   return M > 8 && K % 16 == 0;
 }
 
-static int tc_nt(int M) { return M <= 64 ? 64 : 128; }
+// Token tile: as narrow as the rows need (the activation tile is copied and
+// multiplied whole), up to 128.
+static int tc_nt(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
 
 // k split for grids that would leave most SMs idle (few weight tiles at small
 // M): enough items to cover the SMs, at least 4 k blocks per item.
@@ -1012,8 +1018,12 @@ cudaError_t launch_gemm_tc(const GemvArgs& g, bool fp8, cudaStream_t s) {
     if (nt == 128) return launch_w8a8<128>(g, s);
     return launch_w8a8<256>(g, s);
   }
-  if (tc_nt(g.M) == 64) return fp8 ? launch_tc<64, true>(g, s) : launch_tc<64, false>(g, s);
-  return fp8 ? launch_tc<128, true>(g, s) : launch_tc<128, false>(g, s);
+  switch (tc_nt(g.M)) {
+    case 16: return fp8 ? launch_tc<16, true>(g, s) : launch_tc<16, false>(g, s);
+    case 32: return fp8 ? launch_tc<32, true>(g, s) : launch_tc<32, false>(g, s);
+    case 64: return fp8 ? launch_tc<64, true>(g, s) : launch_tc<64, false>(g, s);
+    default: return fp8 ? launch_tc<128, true>(g, s) : launch_tc<128, false>(g, s);
+  }
 }
 
 int status_gemm_tc(int clear) { return tu_status(clear); }

@@ -41,7 +41,7 @@ def _rand_fp8(N, K, seed):
     return synth.quantize_fp8_block128((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32))
 
 
-@pytest.mark.parametrize("M", [1, 3, 16, 70])
+@pytest.mark.parametrize("M", [1, 3, 16, 30, 70])
 def test_gemv_one_hot_is_bit_exact(M):
     # one-hot activations with power-of-two scales: out = E4M3(W[n,k]) * S exactly
     N, K = 300, 448
@@ -66,8 +66,10 @@ def test_gemv_one_hot_is_bit_exact(M):
 
 @pytest.mark.parametrize("M,N,K", [(1, 552, 256), (3, 300, 448), (1, 18560, 4096), (2, 4096, 8192),
                                    (5, 1000, 4096), (4, 129, 16384),
-                                   # tensor-core GEMM (M > 8): ragged M / N / K tiles
-                                   (9, 300, 448), (64, 552, 256), (130, 1000, 4096), (200, 256, 8192)])
+                                   # tensor-core GEMM (M > 8): ragged M / N / K tiles, token
+                                   # tiles of 16, 32, 64 and 128
+                                   (9, 300, 448), (24, 1000, 4096), (64, 552, 256), (130, 1000, 4096),
+                                   (200, 256, 8192)])
 def test_gemv_matches_oracle(M, N, K):
     W, S = _rand_fp8(N, K, N + K)
     A = synth.to_bf16_bits(np.random.default_rng(M).standard_normal((M, K)))
