@@ -15,7 +15,9 @@
 // epilogue promotes it, acc += s * partial.
 //
 // The MMA computes D^T: UMMA M = 128 weight rows (one scale row block), UMMA N
-// = NT token rows, so one tile is [128 weight rows] x [NT tokens].
+// = NT token rows, so one tile is [128 weight rows] x [NT tokens]; NT is 16,
+// 32, 64 or 128, the narrowest that holds the rows (the activation tile is
+// copied and multiplied whole).
 // Persistent CTAs walk work items (a tile, or a k range of a tile when the
 // tiles alone would leave most SMs idle) weight-tile major, so the token tiles
 // of one weight tile are adjacent and its bytes are re-read from L2.  Roles
